@@ -1,0 +1,64 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each.
+
+Each mutant is compiled from a patched copy of ``oracle/a2av_oracle.c`` into a
+temporary directory and checked by ``python -m tests._pins <lib>`` in a
+subprocess, so that a mutant that corrupts memory or crashes cannot take the
+test session with it: a crash counts as caught.  The mistakes planted are the
+kinds the definition leaves room for -- a transposed operand, an inclusive
+instead of exclusive scan, a dropped term, a reversed order, an off-by-one in
+a bound, a swapped output row.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "in_offset_transposed": ("off += S[(int64_t)r * W + q];", "off += S[(int64_t)q * W + r];"),
+    "out_offset_inclusive": ("for (int q = 0; q < r; ++q) off += S[(int64_t)q * W + p];",
+                             "for (int q = 0; q <= r; ++q) off += S[(int64_t)q * W + p];"),
+    "sources_reversed": ("for (int q = 0; q < r; ++q) off += S[(int64_t)q * W + p];",
+                         "for (int q = r + 1; q < W; ++q) off += S[(int64_t)q * W + p];"),
+    "count_transposed": ("const int64_t n = in_splits[(int64_t)r * W + p];",
+                         "const int64_t n = in_splits[(int64_t)p * W + r];"),
+    "offset_row_is_source_offset": ("out_so_p[W + r] = dst_row;", "out_so_p[W + r] = src_row;"),
+    "so_rows_swapped": ("out_so_p[r] = n;\n      out_so_p[W + r] = dst_row;",
+                        "out_so_p[W + r] = n;\n      out_so_p[r] = dst_row;"),
+    "row_index_dropped": ("in[r] + (src_row + i) * row_bytes", "in[r] + (src_row) * row_bytes"),
+    "self_chunk_dropped": ("if (out_p == NULL) continue;", "if (out_p == NULL || r == p) continue;"),
+    "in_capacity_off_by_one": ("rows > in_capacity_rows) return", "rows > in_capacity_rows + 1) return"),
+    "out_capacity_off_by_one": ("rows > out_capacity_rows) return", "rows > out_capacity_rows + 1) return"),
+    "negative_accepted": ("in_splits[e] < 0 ||", "in_splits[e] < -1 ||"),
+    "limit_drops_W": ("kMaxBytes / ((int64_t)W * row_bytes)", "kMaxBytes / (row_bytes)"),
+    "null_input_unchecked": ("if (in != NULL && in[r] == NULL && rows > 0)",
+                             "if (in != NULL && in[r] == NULL && rows > kMaxBytes)"),
+    "row_source_wrong_chunk": ("*i = in_offset(W, in_splits, q, p) + (k - start);",
+                               "*i = in_offset(W, in_splits, p, q) + (k - start);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    path = tmp_path / "a2av_oracle.c"
+    path.write_text(src.replace(old, new))
+    lib = oracle.build(str(path), str(tmp_path / "liba2av_oracle_mutant.so"))
+    res = subprocess.run([sys.executable, "-m", "tests._pins", lib], cwd=ROOT,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout}{res.stderr}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    path = tmp_path / "a2av_oracle.c"
+    path.write_text(open(oracle.SOURCE).read())
+    lib = oracle.build(str(path), str(tmp_path / "liba2av_oracle_copy.so"))
+    res = subprocess.run([sys.executable, "-m", "tests._pins", lib], cwd=ROOT,
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stdout + res.stderr
