@@ -1,0 +1,502 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 variable-size all-to-all (a2av).
+
+Workload (one "step" = one a2av over the whole batch): W=4 ranks, 4 GiB of
+rows of 7168 bf16 (14336 B) per rank, uniform random bits, splits ~
+Multinomial(rows, 1/4 each), seed 0 -- the top point of the 1 MiB .. 4 GiB
+payload sweep of "[a2av] Improve tuning for 4 GPUs" (pytorch PR 154580,
+"Before"/"After" tables).  The whole sweep is also timed and reported.
+
+Metric: moved GB/s = bytes moved per step / step time (GB = 1e9), and the
+fraction of the HBM roofline = 2 x moved bytes / time / HBM peak.  The page's
+BusBw (per-rank bytes / time) is reported beside it for context.
+
+Timing: CUDA events on the launching stream around every launch, after
+warm-up, bracketed by barrier + synchronize; inputs (16 GiB) exceed the L2, and
+the sweep flushes L2 between launches.  The CPU oracle is timed on a bounded
+sample (whole peers' outputs) on one host core, and its result is compared
+with the GPU's, outside every timed region.
+
+Multi-GPU: the exchange emulates its ranks inside one GPU, so N GPUs run N
+independent replicas ("replicas only"), each on its own copy of the workload;
+value = all replicas' bytes / the slowest replica's time.
+
+``--impl reference`` times the CPU oracle alone as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "a2av moved GB/s and fraction of GB300 HBM roofline vs payload size"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+ROW_BYTES = 7168 * 2
+W = 4
+
+
+# ------------------------------------------------------------ arithmetic --
+def moved_bytes(splits, row_bytes) -> int:
+    """Bytes one exchange moves: every row once (read once, written once)."""
+    return int(np.asarray(splits, dtype=np.int64).sum()) * int(row_bytes)
+
+
+def algorithmic_bytes(splits, row_bytes) -> int:
+    """DRAM bytes an ideal exchange touches: read + write of every row, the
+    split matrix read (8 W^2) and out_splits_offsets written (16 W^2)."""
+    Wn = np.asarray(splits).shape[0]
+    return 2 * moved_bytes(splits, row_bytes) + 24 * Wn * Wn
+
+
+def busbw_gbps(per_rank_bytes: float, seconds: float) -> float:
+    """The page's BusBw: per-rank payload bytes / time, GB = 1e9."""
+    return per_rank_bytes / seconds / 1e9
+
+
+def workload_name(per_rank_bytes: int) -> str:
+    return (f"a2av W={W}, {per_rank_bytes / 2**20:g} MiB/rank of 7168-bf16 rows "
+            f"(14336 B), uniform random bits, in_splits ~ Multinomial(rows, 1/4), seed 0")
+
+
+# -------------------------------------------------------------- process --
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, _, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Maximum of x over ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Aggregate throughput: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during a timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu, self.period = gpu_index, period_ms
+        self.proc, self.path = None, None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k] == "Active"})
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_median": statistics.median([num(r[3]) for r in rows
+                                                     if num(r[3]) is not None] or [0])}
+
+
+# ------------------------------------------------------------ roofline --
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        for key in ("hbm_gbs", "hbm_GBps", "hbm_copy_gbs"):
+            if key in d and d[key]:
+                return float(d[key]), "of measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_source_sha() -> str:
+    src = os.path.join(ROOT, "variable_size_all_gb300", "csrc", "a2av.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, algo_bytes: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this
+    launch's algorithmic bytes; None when absent or taken on other source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return int(round(e["dram_bytes"] / e["algorithmic_bytes"] * algo_bytes))
+
+
+# -------------------------------------------------------------- oracle ----
+def time_oracle(inputs, splits, row_bytes, budget_s: float, peers=None, check=None):
+    """Run the CPU oracle peer by peer (one host thread) until the budget is
+    spent; returns (seconds, bytes moved, peers done).  ``check(p, out, so)``,
+    if given, sees each peer's output outside the timed part."""
+    import oracle
+    o = oracle.default()
+    Wn = len(inputs)
+    peers = list(range(Wn)) if peers is None else peers
+    spent, moved, done = 0.0, 0, []
+    for p in peers:
+        buf = np.empty(int(splits[:, p].sum()) * row_bytes, dtype=np.uint8)
+        so = np.empty((2, Wn), dtype=np.int64)
+        t0 = time.perf_counter()
+        rc = o.dest(inputs, splits, p, buf, so, row_bytes)
+        spent += time.perf_counter() - t0
+        assert rc == 0
+        moved += buf.size
+        done.append(p)
+        if check is not None:
+            check(p, buf, so)
+        del buf
+        if spent >= budget_s:
+            break
+    return spent, moved, done
+
+
+# ----------------------------------------------------------------- ours ----
+def run_ours(args):
+    import torch
+    import variable_size_all_gb300 as a2av
+    import workloads as wl
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    a2av.build()
+    path_id = {"auto": a2av.PATH_AUTO, "vector": a2av.PATH_VECTOR, "bulk": a2av.PATH_BULK}[args.path]
+
+    P = args.per_rank_bytes
+    rows = P // ROW_BYTES
+    nbytes = rows * ROW_BYTES
+    # Inputs drawn on the host into pinned memory (they are also the e2e sources).
+    h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
+    t0 = time.time()
+    w = wl.cfg2(P, seed=0, buffers=[t.numpy() for t in h_in])
+    gen_s = time.time() - t0
+    S = w.splits
+    recv = [int(S[:, p].sum()) * ROW_BYTES for p in range(W)]
+    T = moved_bytes(S, ROW_BYTES)
+    d_in = [t.to(dev) for t in h_in]
+    d_out = [torch.empty(n, dtype=torch.uint8, device=dev) for n in recv]
+    d_S = torch.from_numpy(S).to(dev)
+    d_so = torch.empty((W, 2, W), dtype=torch.int64, device=dev)
+    eng = a2av.A2av(W, path=path_id, ctas_per_sm=args.ctas_per_sm)
+    stream = torch.cuda.current_stream()
+
+    def step(ins=d_in, outs=d_out, splits=d_S):
+        eng.run(ins, splits, outs, d_so, ROW_BYTES, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during warm-up")
+    launch = eng.last_launch()
+
+    # ---- timed region: exactly K steps, one kernel launch each ----------
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t_begin.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during the timed region")
+    max_s = reduce_max(total_ms / 1e3, dev)
+    value = whole_job_value(T * K / 1e9, world, max_s)
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    med_launch_s = statistics.median(launch_ms) / 1e3
+
+    # ---- roofline of the (only) kernel -----------------------------------
+    algo = algorithmic_bytes(S, ROW_BYTES)
+    peak, peak_kind = hbm_peak()
+    kname = "a2av_bulk_kernel" if launch["path"] == a2av.PATH_BULK else "a2av_vector_kernel"
+    achieved = algo / avg_launch_s / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": measured_traffic(kname, algo),
+                "algorithmic_bytes_per_launch": algo}
+
+    # ---- device-to-device memcpy ceiling for the same bytes ---------------
+    src = torch.cat([t for t in d_in])
+    dst = torch.empty_like(src)
+    for _ in range(3):
+        dst.copy_(src)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        dst.copy_(src)
+    b.record(stream)
+    torch.cuda.synchronize()
+    d2d_gbps = src.numel() * 5 / (a.elapsed_time(b) / 1e3) / 1e9
+    del src, dst
+
+    # ---- payload sweep (cold L2 between launches) --------------------------
+    sweep = []
+    if not args.no_sweep:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        for Pk in wl.CFG2_SWEEP_BYTES:
+            if Pk > P:
+                break
+            Sk = wl.cfg2_splits(Pk, 0)
+            nk = (Pk // ROW_BYTES) * ROW_BYTES
+            ins = [t[:nk] for t in d_in]  # prefix of the same draw = cfg2(Pk)'s inputs
+            outs = [t[: int(Sk[:, p].sum()) * ROW_BYTES] for p, t in enumerate(d_out)]
+            dSk = torch.from_numpy(Sk).to(dev)
+            for _ in range(3):
+                step(ins, outs, dSk)
+            times = []
+            for _ in range(args.sweep_reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step(ins, outs, dSk)
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b) / 1e3)
+            t_med = statistics.median(times)
+            Tk = moved_bytes(Sk, ROW_BYTES)
+            sweep.append({"per_rank_MiB": Pk / 2**20, "moved_bytes": Tk,
+                          "us_median": round(t_med * 1e6, 2),
+                          "us_min": round(min(times) * 1e6, 2),
+                          "moved_GBps": round(Tk / t_med / 1e9, 1),
+                          "busbw_GBps": round(busbw_gbps(nk, t_med), 1),
+                          "hbm_frac": round(algorithmic_bytes(Sk, ROW_BYTES) / t_med / 1e9 / peak, 4)})
+        del flush
+        if eng.status() != a2av.OK:
+            raise SystemExit("device reported an error during the sweep")
+
+    # ---- end to end through the public API, host buffers ------------------
+    e2e = None
+    if not args.no_e2e:
+        h_out = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for n in recv]
+        h_S = torch.from_numpy(S).pin_memory()
+        h_so = torch.empty((W, 2, W), dtype=torch.int64, pin_memory=True)
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            d_S.copy_(h_S, non_blocking=True)
+            step()
+            for h, d in zip(h_out, d_out):
+                h.copy_(d, non_blocking=True)
+            h_so.copy_(d_so, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        Ke = args.e2e_steps
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_s = reduce_max(a.elapsed_time(b) / 1e3, dev)
+        e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, e_s), 2), "unit": UNIT,
+               "h2d_bytes_per_step": sum(t.numel() for t in h_in) + S.size * 8,
+               "d2h_bytes_per_step": sum(recv) + 2 * W * W * 8, "steps": Ke}
+        if eng.status() != a2av.OK:
+            raise SystemExit("device reported an error during the e2e run")
+
+    # ---- CPU oracle: baseline timing and a parity check of this run -------
+    cpu = None
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inputs = [t.numpy() for t in h_in]
+        mismatched = []
+
+        def compare(p, buf, so):
+            if not (np.array_equal(d_out[p].cpu().numpy(), buf)
+                    and np.array_equal(d_so[p].cpu().numpy(), so)):
+                mismatched.append(p)
+
+        spent, moved, peers = time_oracle(inputs, S, ROW_BYTES, args.cpu_budget, check=compare)
+        cpu = {"value": round(moved / spent / 1e9, 3), "unit": UNIT, "cores": 1,
+               "kind": "oracle",
+               "sample": f"peers {peers} of the same {P >> 20} MiB/rank exchange "
+                         f"({moved / 2**30:.2f} GiB of the {T / 2**30:.2f} GiB moved per step)",
+               "seconds": round(spent, 2)}
+        parity = {"bit_exact": not mismatched, "peers_checked": peers}
+        if mismatched:
+            raise SystemExit(f"GPU output differs from the oracle on peers {mismatched}")
+
+    eng.close()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws; no dataset)",
+        "config": {"workload": workload_name(P), "ranks": W, "row_bytes": ROW_BYTES,
+                   "per_rank_bytes": nbytes, "moved_bytes_per_step": T,
+                   "l2": "inputs larger than L2 (4 x 4 GiB per step); sweep flushes L2",
+                   "engine": kname, "grid": launch["grid"], "block": launch["block"],
+                   "parallelism": f"replicas x{world} (ranks emulated inside each GPU)"},
+        "hbm_fraction": round(2 * T / (max_s / K) / 1e9 / peak, 4),
+        "busbw_GBps": round(busbw_gbps(nbytes, max_s / K), 1),
+        "launch_us_median": round(med_launch_s * 1e6, 2),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K,
+        "clocks": clocks.summary(),
+        "d2d_memcpy_GBps": round(d2d_gbps, 1),
+        "sweep": sweep,
+        "parity": parity,
+        "input_generation_s": round(gen_s, 2),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference ----
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step runs it on one peer's
+    whole output of the same workload (a bounded sample), one host core."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import workloads as wl
+    P = args.per_rank_bytes
+    w = wl.cfg2(P, seed=0)
+    S, inputs = w.splits, w.inputs
+    K, Wm = args.steps, args.warmup
+    for k in range(Wm):
+        time_oracle(inputs, S, ROW_BYTES, 0.0, peers=[k % W])
+    total_s, total_b = 0.0, 0
+    for k in range(K):
+        s, b, _ = time_oracle(inputs, S, ROW_BYTES, 0.0, peers=[k % W])
+        total_s += s
+        total_b += b
+    value = total_b / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(total_s * 1e3 / K, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws; no dataset)",
+        "config": {"workload": workload_name(P), "ranks": W, "row_bytes": ROW_BYTES,
+                   "per_rank_bytes": (P // ROW_BYTES) * ROW_BYTES,
+                   "parallelism": "one host core"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one peer's whole output per step (peer = step mod 4)"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--per-rank-bytes", type=int, default=1 << 32)
+    ap.add_argument("--path", choices=["auto", "vector", "bulk"], default="auto")
+    ap.add_argument("--ctas-per-sm", type=int, default=0)
+    ap.add_argument("--sweep-reps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

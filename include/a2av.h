@@ -1,0 +1,175 @@
+/*
+ * a2av.h -- C ABI of a GB300 (sm_103a) variable-size all-to-all with
+ * device-resident splits (all_to_all_vdev).
+ *
+ * The operation ("[a2av] Improve tuning for 4 GPUs", pytorch PR 154580,
+ * section "Problem": nvshmem_all_to_all_vdev, each rank sending a
+ * variable-size chunk to every peer, with the split sizes held on the device):
+ *
+ *   W ranks, r, p in [0, W).  S[r][p] = in_splits[r*W + p] rows go from rank
+ *   r to peer p.  Rank r's input holds its chunks back to back in peer order,
+ *   starting at row 0; peer p's output receives them back to back in
+ *   source-rank order, starting at row 0:
+ *
+ *     out[p] rows [out_off[p][r], out_off[p][r] + S[r][p])
+ *        = in[r] rows [in_off[r][p], in_off[r][p] + S[r][p])
+ *     in_off[r][p]  = sum_{q<p} S[r][q]      out_off[p][r] = sum_{q<r} S[q][p]
+ *
+ *   and out_splits_offsets[p][0][r] = S[r][p], out_splits_offsets[p][1][r] =
+ *   out_off[p][r].  A row is row_bytes bytes, copied bit for bit.
+ *
+ * Here the W ranks are W pairs of buffers in the HBM of ONE GPU; the exchange
+ * is one kernel launch that reads the split matrix on the device (no host
+ * round trip), scans it, writes out_splits_offsets and moves every chunk.
+ * The pages' NVSHMEM design split its CTAs between the peers and, when the
+ * peers are few, the data-parallel dimension within each chunk (same page,
+ * section "Change"); this library balances bytes, not chunks, across CTAs.
+ *
+ * Conventions for every entry point:
+ *  - Return value: A2AV_OK or a negative a2av_status_t.  Host-detectable
+ *    errors are returned synchronously and launch nothing.
+ *  - Device pointers are CUDA device (or managed) addresses on the device
+ *    that was current when the handle was created; that device must be
+ *    current on every call.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  The caller owns every buffer and the stream; the library never
+ *    allocates, frees or retains them.
+ *  - Not thread-safe per handle: one host thread at a time per handle.
+ */
+#ifndef A2AV_H_
+#define A2AV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest number of ranks one exchange supports. */
+#define A2AV_MAX_RANKS 32
+
+typedef enum {
+  A2AV_OK = 0,
+  A2AV_ERR_INVALID_ARG = -1, /* a host-checked argument is wrong */
+  A2AV_ERR_UNSUPPORTED = -2, /* a valid request this build does not serve (W > 32) */
+  A2AV_ERR_CUDA = -3,        /* a CUDA runtime call failed (no device, launch failure...) */
+  A2AV_ERR_BAD_SPLITS = -4,  /* device-detected: the split matrix is invalid */
+  A2AV_ERR_TIMEOUT = -5      /* device-detected: a bounded wait inside a kernel gave up */
+} a2av_status_t;
+
+/* Copy engine selection (a2av_set_path). */
+typedef enum {
+  A2AV_PATH_AUTO = 0,   /* bulk when every row and buffer is 16-byte aligned, else vector */
+  A2AV_PATH_VECTOR = 1, /* 16-byte vector loads/stores with in-register realignment */
+  A2AV_PATH_BULK = 2    /* cp.async.bulk global->shared->global staging (aligned only) */
+} a2av_path_t;
+
+typedef struct a2av_handle a2av_handle;
+
+/*
+ * a2av_create -- make a handle for exchanges among `world_size` ranks on the
+ * current CUDA device.
+ *
+ *  world_size          W, 1 <= W <= A2AV_MAX_RANKS (W > 32: A2AV_ERR_UNSUPPORTED).
+ *  in_capacity_rows    rows every input buffer can hold; sum_p S[r][p] above it is
+ *                      rejected on the device.  0 = unchecked.
+ *  out_capacity_rows   rows every output buffer can hold; sum_r S[r][p] above it is
+ *                      rejected on the device.  0 = unchecked.
+ *  out                 receives the handle (host pointer, must not be NULL).
+ *
+ * Allocates a small device status word (cudaMalloc) on the current device.
+ * Errors: A2AV_ERR_INVALID_ARG (W < 1, negative capacity, out == NULL),
+ * A2AV_ERR_UNSUPPORTED, A2AV_ERR_CUDA (no usable device).
+ */
+int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_rows,
+                a2av_handle **out);
+
+/*
+ * a2av_run -- one all_to_all_vdev over the handle's W ranks, enqueued on
+ * `stream` as a single kernel launch; returns without waiting for it.
+ *
+ *  in_ptrs            HOST array of W device pointers: rank r's input, its chunks
+ *                     back to back in peer order from row 0.  Read only.  A NULL
+ *                     entry is a rank with no input (it must send 0 rows).
+ *  in_splits_dev      DEVICE int64 [W][W], row-major by source rank: S[r][p] at
+ *                     in_splits_dev[r*W + p].  Read only; 8-byte aligned.
+ *  out_ptrs           HOST array of W device pointers: peer p's output.  Written
+ *                     only in its first sum_r S[r][p] rows.  A NULL entry is a
+ *                     peer that receives nothing (it must receive 0 rows).
+ *  out_splits_offsets_dev  DEVICE int64 [W][2][W]: written with
+ *                     [p][0][r] = S[r][p] and [p][1][r] = out_off[p][r] (rows).
+ *  row_bytes          bytes per row, >= 1, any value (no alignment needed).
+ *  stream             cudaStream_t as void*.
+ *
+ * Memory rules: no output may overlap an input, the split matrix or another
+ * output; inputs may share memory.  Bytes of an input past its last chunk are
+ * never used and bytes of an output past its last received row are never
+ * written.  (Whole 16-byte-aligned granules that hold a needed input byte may
+ * be loaded and their other bytes discarded; such loads never leave the
+ * granule and so never fault.)
+ *
+ * Split validity, checked on the device before anything is written:
+ * S[r][p] >= 0; S[r][p] <= 2^62 / (W * row_bytes); sum_p S[r][p] <=
+ * in_capacity_rows and sum_r S[r][p] <= out_capacity_rows when those are
+ * nonzero; 0 rows for a NULL buffer.  Invalid splits write NOTHING (no output
+ * byte, no out_splits_offsets entry) and record A2AV_ERR_BAD_SPLITS in the
+ * handle's status word, read by a2av_status.
+ *
+ * Host errors (nothing launched): A2AV_ERR_INVALID_ARG for a NULL handle or
+ * array, a NULL split or out_splits_offsets pointer, a misaligned split
+ * pointer, row_bytes < 1, or a current device other than the handle's;
+ * A2AV_ERR_CUDA when the launch fails.
+ */
+int a2av_run(a2av_handle *h, const void *const *in_ptrs, const int64_t *in_splits_dev,
+             void *const *out_ptrs, int64_t *out_splits_offsets_dev, int64_t row_bytes,
+             void *stream);
+
+/*
+ * a2av_status -- read and clear the handle's device status word: the first
+ * device-detected error (A2AV_ERR_BAD_SPLITS or A2AV_ERR_TIMEOUT) of the runs
+ * since the last call, or A2AV_OK.  Enqueues a 4-byte device-to-host copy and
+ * a reset on `stream` and synchronizes that stream: the only host round trip
+ * of the library.  `device_status` is a host pointer.
+ * Errors: A2AV_ERR_INVALID_ARG, A2AV_ERR_CUDA.
+ */
+int a2av_status(a2av_handle *h, void *stream, int *device_status);
+
+/*
+ * a2av_destroy -- free the handle and its status word.  Work already
+ * enqueued must have finished (synchronize its stream first).  NULL is a
+ * no-op returning A2AV_OK.
+ */
+int a2av_destroy(a2av_handle *h);
+
+/*
+ * a2av_set_path -- choose the copy engine for later runs (a2av_path_t).
+ * A2AV_PATH_BULK on a run whose row_bytes or buffer addresses are not all
+ * 16-byte aligned falls back to the vector engine for that run.
+ * Errors: A2AV_ERR_INVALID_ARG.
+ */
+int a2av_set_path(a2av_handle *h, int path);
+
+/*
+ * a2av_set_grid -- CTAs launched per SM for later runs (1..32; 0 restores
+ * the engine's default).  Errors: A2AV_ERR_INVALID_ARG.
+ */
+int a2av_set_grid(a2av_handle *h, int ctas_per_sm);
+
+/*
+ * a2av_last_launch -- describe the most recent successful a2av_run of this
+ * handle: the engine used (a2av_path_t, never AUTO), the grid size and the
+ * threads per CTA.  Any output pointer may be NULL.
+ */
+int a2av_last_launch(const a2av_handle *h, int *path, int *grid, int *block);
+
+/* a2av_error_string -- a static English description of a status code. */
+const char *a2av_error_string(int code);
+
+/* a2av_version -- 10000*major + 100*minor + patch of this library. */
+int a2av_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* A2AV_H_ */

@@ -1,0 +1,82 @@
+"""Helpers for the GPU parity tests: guarded device buffers and a checked run.
+
+Every device buffer sits inside a larger allocation whose surrounding bytes
+(4 KiB before and after) hold a canary; outputs also get a few rows of
+sentinel-filled slack past the rows they receive.  ``run_and_check`` runs the
+exchange through the C ABI (the Python binding), then checks, against the CPU
+oracle: every output byte, out_splits_offsets, that canaries and slack are
+untouched, and that the inputs were not modified.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import variable_size_all_gb300 as a2av
+
+GUARD = 4096
+CANARY = 0xA5
+SENTINEL = 0xEE
+SLACK_ROWS = 3
+
+
+class Guarded:
+    """A device view of ``nbytes`` bytes at ``mis`` bytes past a 4 KiB boundary."""
+
+    def __init__(self, nbytes: int, mis: int = 0, fill: int = CANARY, host=None):
+        self.nbytes, self.mis = int(nbytes), int(mis)
+        self.full = torch.full((GUARD + self.mis + self.nbytes + GUARD,), CANARY,
+                               dtype=torch.uint8, device="cuda")
+        self.view = self.full[GUARD + self.mis: GUARD + self.mis + self.nbytes]
+        if host is not None:
+            self.view.copy_(torch.from_numpy(np.ascontiguousarray(host)))
+        elif fill != CANARY:
+            self.view.fill_(fill)
+
+    def guards_intact(self) -> bool:
+        f = self.full.cpu().numpy()
+        lo, hi = GUARD + self.mis, GUARD + self.mis + self.nbytes
+        return bool(np.all(f[:lo] == CANARY) and np.all(f[hi:] == CANARY))
+
+
+def exchange_checked(inputs, S, rb, path=a2av.PATH_AUTO, in_mis=None, out_mis=None,
+                     ctas_per_sm=0, stream=None, engine=None, expect_path=None):
+    """Run one exchange on the GPU and compare everything with the oracle."""
+    W = len(inputs)
+    S = np.ascontiguousarray(S, dtype=np.int64)
+    in_mis = in_mis or [0] * W
+    out_mis = out_mis or [0] * W
+    recv = [int(S[:, p].sum()) for p in range(W)]
+    ins = [Guarded(inputs[r].size, in_mis[r], host=inputs[r]) for r in range(W)]
+    outs = [Guarded((recv[p] + SLACK_ROWS) * rb, out_mis[p], fill=SENTINEL) for p in range(W)]
+    splits = torch.from_numpy(S).cuda()
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    own = engine is None
+    eng = engine or a2av.A2av(W, path=path, ctas_per_sm=ctas_per_sm)
+    try:
+        eng.run([g.view for g in ins], splits, [g.view for g in outs], so, rb, stream=stream)
+        st = eng.status(stream)
+        launch = eng.last_launch()
+    finally:
+        if own:
+            eng.close()
+    torch.cuda.synchronize()
+    assert st == a2av.OK, f"device status {st}"
+    if expect_path is not None:
+        assert launch["path"] == expect_path, launch
+    ref, ref_so = oracle.default().exchange(inputs, S, rb)
+    assert np.array_equal(so.cpu().numpy(), ref_so), "out_splits_offsets differ from the oracle"
+    for p in range(W):
+        got = outs[p].view.cpu().numpy()
+        n = recv[p] * rb
+        if not np.array_equal(got[:n], ref[p]):
+            bad = np.nonzero(got[:n] != ref[p])[0]
+            raise AssertionError(f"peer {p}: {bad.size} bytes differ, first at {bad[0]} "
+                                 f"(row {bad[0] // rb}) W={W} rb={rb}")
+        assert np.all(got[n:] == SENTINEL), f"peer {p}: bytes past the received rows written"
+        assert outs[p].guards_intact(), f"peer {p}: canary before/after the output overwritten"
+    for r in range(W):
+        assert np.array_equal(ins[r].view.cpu().numpy(), inputs[r]), f"input {r} modified"
+        assert ins[r].guards_intact(), f"input {r}: canary modified"
+    return launch

@@ -1,0 +1,81 @@
+"""bench.py's host logic without a GPU: the metric formulas against the page's
+printed table, the reference arm end to end, and the multi-rank aggregation
+over a world-size-2 gloo process group."""
+import json
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _golden():
+    rows = []
+    for line in open(os.path.join(ROOT, "tests", "golden", "busbw_pr154580.txt")):
+        if line.strip() and not line.startswith("#"):
+            table, mib, us, gbps = line.split()
+            rows.append((table, float(mib), float(us), float(gbps)))
+    return rows
+
+
+def test_busbw_reproduces_the_pages_table():
+    rows = _golden()
+    assert len(rows) == 28
+    for table, mib, us, gbps in rows:
+        got = bench.busbw_gbps(mib * 2**20, us * 1e-6)
+        # the page rounds time to 0.01 us and BusBw to 0.01 GB/s
+        assert abs(got - gbps) <= 0.01 + gbps * 0.01 / us + 1e-9, (table, mib, got, gbps)
+
+
+def test_moved_and_algorithmic_bytes():
+    S = np.array([[1, 2], [3, 4]])
+    assert bench.moved_bytes(S, 8) == 80
+    assert bench.algorithmic_bytes(S, 8) == 160 + 24 * 4
+    assert bench.whole_job_value(10.0, 4, 2.0) == 20.0
+
+
+def test_reference_arm_runs_on_cpu():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--per-rank-bytes", str(1 << 22), "--steps", "3", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["steps"] == 3 and line["warmup"] == 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _gloo_worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench as b
+    b.dist_init("gloo")
+    b.barrier()
+    m = b.reduce_max(1.0 + rank)
+    v = b.whole_job_value(5.0, world, m)
+    q.put((rank, m, v))
+    dist.destroy_process_group()
+
+
+def test_replicas_aggregate_over_gloo():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29000 + os.getpid() % 1000
+    procs = [ctx.Process(target=_gloo_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    assert [m for _, m, _ in res] == [2.0, 2.0]  # max over ranks
+    assert [v for _, _, v in res] == [5.0, 5.0]  # 2 ranks x 5 units / 2 s

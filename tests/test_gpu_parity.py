@@ -1,0 +1,162 @@
+"""GPU parity: the CUDA exchange against the CPU oracle, byte for byte.
+
+Covers the five workloads (config 4 over its 16 seeds), both copy engines,
+random split matrices with empty, skewed, diagonal and single-chunk patterns,
+row sizes from 1 B to 14336 B, misaligned buffer addresses, small and large
+grids (few or many tiles per CTA), W from 1 to 32, streams and reuse.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests._gpu import exchange_checked
+
+pytestmark = pytest.mark.gpu
+
+a2av = pytest.importorskip("variable_size_all_gb300")
+VEC, BULK, AUTO = a2av.PATH_VECTOR, a2av.PATH_BULK, a2av.PATH_AUTO
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    a2av.build()
+    a2av.load()
+
+
+@pytest.mark.parametrize("path", [AUTO, VEC])
+def test_cfg1(path):
+    w = wl.cfg1(0)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, path=path,
+                     expect_path=BULK if path == AUTO else VEC)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_cfg4_seeds(seed):
+    w = wl.cfg4(seed)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, expect_path=VEC)
+
+
+def test_cfg5():
+    w = wl.cfg5(0)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, expect_path=VEC)
+
+
+@pytest.mark.parametrize("path", [AUTO, VEC])
+def test_cfg3_full(path):
+    w = wl.cfg3(0)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, path=path)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_cfg3_seeds_small_grid(seed):
+    w = wl.cfg3(seed, tokens=2048)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=1)
+
+
+@pytest.mark.parametrize("mib", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("path", [AUTO, VEC])
+def test_cfg2_sweep_points(mib, path):
+    w = wl.cfg2(mib << 20)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, path=path)
+
+
+ROW_BYTES = [1, 2, 3, 4, 7, 8, 13, 16, 17, 31, 48, 256, 14336]
+
+
+@pytest.mark.parametrize("rb", ROW_BYTES)
+def test_random_splits(rb):
+    rng = np.random.default_rng(rb)
+    modes = ["uniform", "skew", "sparse", "empty", "diag", "one"]
+    for k, W in enumerate([1, 2, 3, 5, 8, 13, 32]):
+        for mode in modes:
+            max_rows = 3000 if rb <= 16 else (300 if rb <= 256 else 6)
+            w = wl.random_case(1000 * rb + 10 * k + modes.index(mode), W, rb, max_rows, mode)
+            in_mis = [int(rng.integers(0, 16)) for _ in range(W)]
+            out_mis = [int(rng.integers(0, 16)) for _ in range(W)]
+            exchange_checked(w.inputs, w.splits, rb, in_mis=in_mis, out_mis=out_mis,
+                             ctas_per_sm=int(rng.choice([0, 1, 4])))
+
+
+@pytest.mark.parametrize("path", [VEC, BULK])
+def test_aligned_engines_agree(path):
+    for W, rb in ((4, 16), (8, 32), (3, 4096), (32, 16)):
+        w = wl.random_case(7 + W, W, rb, 500, "uniform")
+        exchange_checked(w.inputs, w.splits, rb, path=path, expect_path=path)
+
+
+def test_bulk_request_on_misaligned_falls_back_to_vector():
+    w = wl.random_case(3, 4, 16, 100, "uniform")
+    exchange_checked(w.inputs, w.splits, 16, path=BULK, in_mis=[0, 4, 0, 0], expect_path=VEC)
+    w = wl.random_case(4, 4, 24, 100, "uniform")
+    exchange_checked(w.inputs, w.splits, 24, path=BULK, expect_path=VEC)
+
+
+@pytest.mark.parametrize("grid", [1, 2, 8, 32])
+def test_grid_sizes(grid):
+    w = wl.cfg4(5, rows=1 << 16)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=grid)
+    w = wl.cfg2(4 << 20)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=grid)
+
+
+def test_single_huge_chunk_and_tile_edges():
+    # one chunk that is an exact multiple of the tile, one with a ragged tail
+    for rows in (4096, 4097, 65536 + 3):
+        S = np.zeros((4, 4), np.int64)
+        S[2, 1] = rows
+        inputs = [np.zeros(0, np.uint8)] * 4
+        inputs[2] = np.random.default_rng(rows).integers(0, 256, rows * 16, dtype=np.uint8)
+        exchange_checked(inputs, S, 16)
+        exchange_checked(inputs, S, 16, path=VEC)
+
+
+def test_side_stream_and_reuse():
+    s = torch.cuda.Stream()
+    eng = a2av.A2av(4)
+    try:
+        for seed in range(3):
+            w = wl.cfg4(seed, rows=1 << 14, W=4)
+            with torch.cuda.stream(s):
+                exchange_checked(w.inputs, w.splits, w.row_bytes, stream=s, engine=eng)
+    finally:
+        eng.close()
+
+
+def test_round_trip_restores_inputs():
+    w = wl.cfg4(9, rows=1 << 15)
+    W, rb = w.W, w.row_bytes
+    eng = a2av.A2av(W)
+    ins = [torch.from_numpy(b).cuda() for b in w.inputs]
+    S = torch.from_numpy(w.splits).cuda()
+    mid = [torch.empty(int(w.splits[:, p].sum()) * rb, dtype=torch.uint8, device="cuda")
+           for p in range(W)]
+    back = [torch.empty_like(t) for t in ins]
+    so1 = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    so2 = torch.empty_like(so1)
+    eng.run(ins, S, mid, so1, rb)
+    eng.run(mid, S.t().contiguous(), back, so2, rb)
+    assert eng.status() == a2av.OK
+    eng.close()
+    for r in range(W):
+        assert torch.equal(back[r], ins[r])
+    assert torch.equal(so2[:, 0, :], S)
+
+
+def test_back_to_back_without_sync_keeps_stream_order():
+    eng = a2av.A2av(2)
+    a = torch.arange(64, dtype=torch.uint8, device="cuda")
+    b = torch.arange(64, 128, dtype=torch.uint8, device="cuda")
+    o = [torch.zeros(64, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    so = torch.empty((2, 2, 2), dtype=torch.int64, device="cuda")
+    S1 = torch.tensor([[64, 0], [0, 64]], dtype=torch.int64, device="cuda")
+    S2 = torch.tensor([[0, 64], [64, 0]], dtype=torch.int64, device="cuda")
+    for _ in range(50):
+        eng.run([a, b], S1, o, so, 1)
+        eng.run([a, b], S2, o, so, 1)
+    assert eng.status() == a2av.OK
+    eng.close()
+    assert torch.equal(o[0], b) and torch.equal(o[1], a)
+    assert so[:, 0, :].tolist() == [[0, 64], [64, 0]]

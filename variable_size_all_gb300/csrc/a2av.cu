@@ -1,0 +1,656 @@
+// a2av.cu -- GB300 (sm_103a) variable-size all-to-all with device-resident
+// splits: the kernels and the C ABI declared in include/a2av.h.
+//
+// What is computed ("[a2av] Improve tuning for 4 GPUs", pytorch PR 154580,
+// section "Problem"): W ranks; rank r sends S[r][p] rows to peer p; peer p
+// receives the chunks back to back in source-rank order; out_splits_offsets
+// holds the transposed splits and their exclusive scan.
+//
+// How (one launch, no host round trip):
+//   1. Every CTA loads the W x W split matrix (<= 8 KiB, L2-resident after the
+//      first CTA), validates it and builds, in shared memory, the row-offset
+//      tables with warp-shuffle exclusive scans: out_off[p][r] (column scans)
+//      and in_off[r][p] (row scans).  All CTAs reach the same verdict, so an
+//      invalid matrix stops every CTA before any byte is written, without any
+//      inter-CTA synchronisation.
+//   2. The received streams of all peers, each contiguous in its output
+//      buffer, are cut into equal tiles of at most `max_tile` bytes; the tile
+//      size shrinks with the payload so that small exchanges still occupy the
+//      whole GPU.  CTAs take tiles round-robin.  A tile maps to one peer p and
+//      a contiguous byte range of out[p]; the source chunks it overlaps are
+//      found from out_off[p][*].  This is the pages' "shift CTAs onto the
+//      data-parallel dimension" (same page, section "Change") taken to its
+//      limit: CTAs follow bytes, so one huge chunk gets most CTAs, empty
+//      chunks get none and many tiny chunks share a CTA.
+//   3. Copy engines:
+//      - vector: 16-byte loads/stores aligned on the destination; when the
+//        source is misaligned relative to the destination (row sizes that are
+//        not multiples of 16, e.g. 13 B or 8 B rows) each lane loads its
+//        aligned source granule, takes its neighbour's by a warp shuffle and
+//        funnel-shifts the pair into place; head and tail bytes go one by one.
+//      - bulk: when every row and buffer is 16-byte aligned, one thread per
+//        CTA streams tiles global -> shared -> global with cp.async.bulk,
+//        completion tracked by mbarriers, through a ring of shared-memory
+//        stages.  No cluster multicast.
+//   CTA 0 writes out_splits_offsets.
+#include "a2av.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+namespace {
+
+constexpr int kMaxW = A2AV_MAX_RANKS;
+constexpr long long kMaxBytes = 1LL << 62;  // byte offsets stay below 2^62
+constexpr unsigned kFull = 0xffffffffu;
+constexpr long long kTileGranule = 4096;     // tile sizes are multiples of this
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+
+// Engine shapes.  Each can be overridden at compile time (-DA2AV_...) for
+// tuning sweeps; the defaults are the measured choices.
+#ifndef A2AV_VEC_THREADS
+#define A2AV_VEC_THREADS 512
+#endif
+#ifndef A2AV_VEC_UNROLL
+#define A2AV_VEC_UNROLL 4
+#endif
+#ifndef A2AV_VEC_SHIFT_UNROLL
+#define A2AV_VEC_SHIFT_UNROLL 2
+#endif
+#ifndef A2AV_VEC_MAX_TILE
+#define A2AV_VEC_MAX_TILE (64 * 1024)
+#endif
+#ifndef A2AV_VEC_CTAS_PER_SM
+#define A2AV_VEC_CTAS_PER_SM 2
+#endif
+#ifndef A2AV_BULK_STAGES
+#define A2AV_BULK_STAGES 4
+#endif
+#ifndef A2AV_BULK_LEAD
+#define A2AV_BULK_LEAD 2
+#endif
+#ifndef A2AV_BULK_STAGE_BYTES
+#define A2AV_BULK_STAGE_BYTES (32 * 1024)
+#endif
+#ifndef A2AV_BULK_CTAS_PER_SM
+#define A2AV_BULK_CTAS_PER_SM 1
+#endif
+
+// Vector engine: 512 threads (64 registers each, two CTAs per SM), 4
+// independent 16-byte loads in flight per thread on the aligned path (32 KiB
+// per CTA pass) and 2 on the realigning path, tiles of at most 64 KiB.
+constexpr int kVecThreads = A2AV_VEC_THREADS;
+constexpr int kVecUnroll = A2AV_VEC_UNROLL;
+constexpr int kVecShiftUnroll = A2AV_VEC_SHIFT_UNROLL;
+constexpr long long kVecMaxTile = A2AV_VEC_MAX_TILE;
+constexpr int kVecCtasPerSm = A2AV_VEC_CTAS_PER_SM;
+
+// Bulk engine: stages of 32 KiB in a ring of 4; loads run 2 tiles ahead of
+// the stores that drain them.
+constexpr int kBulkThreads = 128;
+constexpr int kBulkStages = A2AV_BULK_STAGES;
+constexpr int kBulkLead = A2AV_BULK_LEAD;
+constexpr int kBulkStageBytes = A2AV_BULK_STAGE_BYTES;
+constexpr int kBulkCtasPerSm = A2AV_BULK_CTAS_PER_SM;
+
+struct Params {
+  const unsigned char* in[kMaxW];
+  unsigned char* out[kMaxW];
+  const long long* splits;  // [W][W], S[r][p] at r*W + p
+  long long* out_so;        // [W][2][W]
+  int* status;
+  long long rb;             // row bytes
+  long long in_cap;         // rows, 0 = unchecked
+  long long out_cap;        // rows, 0 = unchecked
+  int W;
+};
+
+// Per-CTA plan in shared memory.  Offsets are in rows.
+struct Plan {
+  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = sum_{q<r} S[q][p]; [p][W] = rows p receives
+  long long in_off[kMaxW][kMaxW];       // [r][p] = sum_{q<p} S[r][q]
+  long long tile_first[kMaxW + 1];      // first tile of peer p; [W] = number of tiles
+  long long tile;                       // tile size in bytes
+};
+
+__device__ __forceinline__ long long warp_inclusive_scan(long long x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  return x;
+}
+
+__device__ __forceinline__ void record_error(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+// Step 1 of the header comment.  Returns false (in every thread of the CTA)
+// when the splits are invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
+__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  const int W = P.W;
+  const long long limit = kMaxBytes / ((long long)W * P.rb);
+
+  int bad = 0;
+  for (int e = tid; e < W * W; e += nt) {
+    const long long s = P.splits[e];
+    if (s < 0 || s > limit) bad = 1;
+    pl.in_off[e / W][e % W] = s;  // raw S[r][p] until the row scans below
+  }
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+    return false;
+  }
+
+  // Column scans: lane r holds S[r][p]; out_off[p][r] is its exclusive prefix.
+  for (int p = warp; p < W; p += nwarps) {
+    const long long x = lane < W ? pl.in_off[lane][p] : 0;
+    const long long inc = warp_inclusive_scan(x, lane);
+    if (lane < W) pl.out_off[p][lane] = inc - x;
+    if (lane == 31) {
+      pl.out_off[p][W] = inc;
+      if ((P.out_cap > 0 && inc > P.out_cap) || (P.out[p] == nullptr && inc > 0)) bad = 1;
+    }
+  }
+  __syncthreads();
+  // Row scans, in place: lane p holds S[r][p]; in_off[r][p] is its exclusive prefix.
+  for (int r = warp; r < W; r += nwarps) {
+    const long long x = lane < W ? pl.in_off[r][lane] : 0;
+    const long long inc = warp_inclusive_scan(x, lane);
+    if (lane < W) pl.in_off[r][lane] = inc - x;
+    if (lane == 31) {
+      if ((P.in_cap > 0 && inc > P.in_cap) || (P.in[r] == nullptr && inc > 0)) bad = 1;
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+    return false;
+  }
+
+  // Tiles: peer p's received stream (out_off[p][W] * rb bytes) is cut into
+  // ceil(bytes / tile) tiles; tile_first is their exclusive prefix.
+  if (warp == 0) {
+    const long long bytes = lane < W ? pl.out_off[lane][W] * P.rb : 0;
+    const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
+    const long long per_cta = (total + gridDim.x - 1) / gridDim.x;
+    long long tile = (per_cta + kTileGranule - 1) / kTileGranule * kTileGranule;
+    tile = tile < kTileGranule ? kTileGranule : (tile > max_tile ? max_tile : tile);
+    const long long n = (bytes + tile - 1) / tile;
+    const long long inc = warp_inclusive_scan(n, lane);
+    if (lane < W) pl.tile_first[lane] = inc - n;
+    if (lane == 31) {
+      pl.tile_first[W] = inc;
+      pl.tile = tile;
+    }
+  }
+  __syncthreads();
+
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < W * W; e += nt) {
+      const int p = e / W, r = e % W;
+      long long* so = P.out_so + (long long)p * 2 * W;
+      so[r] = pl.out_off[p][r + 1] - pl.out_off[p][r];
+      so[W + r] = pl.out_off[p][r];
+    }
+  }
+  return true;
+}
+
+// Tile t -> peer p and the byte range [lo, hi) of out[p] it covers.
+__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long rb,
+                                         long long* lo, long long* hi) {
+  int p = 0;
+  while (p + 1 < W && pl.tile_first[p + 1] <= t) ++p;
+  const long long bytes = pl.out_off[p][W] * rb;
+  *lo = (t - pl.tile_first[p]) * pl.tile;
+  const long long end = *lo + pl.tile;
+  *hi = end < bytes ? end : bytes;
+  return p;
+}
+
+// ---------------------------------------------------------------- vector --
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Bytes [s, s + 16) of the 32-byte little-endian concatenation a:b, where
+// s = 4*Q + r8/8.
+template <int Q>
+__device__ __forceinline__ uint4 extract16(const uint4& a, const uint4& b, unsigned r8) {
+  const unsigned w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint4 o;
+  o.x = __funnelshift_r(w[Q + 0], w[Q + 1], r8);
+  o.y = __funnelshift_r(w[Q + 1], w[Q + 2], r8);
+  o.z = __funnelshift_r(w[Q + 2], w[Q + 3], r8);
+  o.w = __funnelshift_r(w[Q + 3], w[Q + 4], r8);
+  return o;
+}
+
+// nv 16-byte vectors, source and destination both 16-byte aligned.
+template <int NT, int U>
+__device__ __forceinline__ void copy_aligned(uint4* dst, const uint4* src, long long nv, int tid) {
+  for (long long base = 0; base < nv; base += (long long)NT * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = base + (long long)u * NT + tid;
+      if (i < nv) v[u] = ld_stream(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = base + (long long)u * NT + tid;
+      if (i < nv) st_stream(dst + i, v[u]);
+    }
+  }
+}
+
+// nv destination-aligned vectors whose source starts 4*Q + r8/8 bytes
+// (1..15) past the aligned granule `src`: vector i is built from source
+// granules i and i + 1.  A warp owns 32*U consecutive vectors per pass, lane
+// l of step u holding vector 32*u + l, so granule i + 1 is the next lane's
+// granule i, or for lane 31 lane 0's granule of step u + 1: one rotated
+// shuffle per step delivers both.  Only lane 31 of the last step and the
+// last vector of the span load their second granule themselves.
+template <int NT, int U, int Q>
+__device__ __forceinline__ void copy_shifted(uint4* dst, const uint4* src, long long nv,
+                                             unsigned r8, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  for (long long base = 0; base < nv; base += (long long)NT * U) {
+    const long long wbase = base + (long long)warp * 32 * U + lane;
+    uint4 a[U];
+    uint4 extra = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = wbase + 32 * u;
+      a[u] = make_uint4(0, 0, 0, 0);
+      if (i < nv) {
+        a[u] = ld_stream(src + i);
+        if (i == nv - 1 || (lane == 31 && u == U - 1)) extra = ld_stream(src + i + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = wbase + 32 * u;
+      const uint4 give = (u + 1 < U && lane == 0) ? a[u + 1 < U ? u + 1 : u] : a[u];
+      uint4 n;
+      n.x = __shfl_sync(kFull, give.x, lane + 1);
+      n.y = __shfl_sync(kFull, give.y, lane + 1);
+      n.z = __shfl_sync(kFull, give.z, lane + 1);
+      n.w = __shfl_sync(kFull, give.w, lane + 1);
+      if (i < nv) {
+        const bool own = i == nv - 1 || (lane == 31 && u == U - 1);
+        st_stream(dst + i, extract16<Q>(a[u], own ? extra : n, r8));
+      }
+    }
+  }
+}
+
+// n bytes from s to d, any alignment, by all NT threads of the CTA.
+template <int NT, int U, int US>
+__device__ __forceinline__ void copy_span(unsigned char* d, const unsigned char* s, long long n,
+                                          int tid) {
+  long long head = (16 - (long long)((uintptr_t)d & 15)) & 15;
+  if (head > n) head = n;
+  if (tid < head) d[tid] = __ldg(s + tid);
+  d += head;
+  s += head;
+  n -= head;
+  const long long nv = n >> 4;
+  const int tail = (int)(n & 15);
+  if (tid < tail) d[nv * 16 + tid] = __ldg(s + nv * 16 + tid);
+  if (nv == 0) return;
+  uint4* dv = reinterpret_cast<uint4*>(d);
+  const unsigned shift = (unsigned)((uintptr_t)s & 15);
+  if (shift == 0) {
+    copy_aligned<NT, U>(dv, reinterpret_cast<const uint4*>(s), nv, tid);
+    return;
+  }
+  const uint4* sa = reinterpret_cast<const uint4*>(s - shift);
+  const unsigned r8 = (shift & 3) * 8;
+  switch (shift >> 2) {
+    case 0: copy_shifted<NT, US, 0>(dv, sa, nv, r8, tid); break;
+    case 1: copy_shifted<NT, US, 1>(dv, sa, nv, r8, tid); break;
+    case 2: copy_shifted<NT, US, 2>(dv, sa, nv, r8, tid); break;
+    default: copy_shifted<NT, US, 3>(dv, sa, nv, r8, tid); break;
+  }
+}
+
+template <int NT, int U, int US>
+__global__ void __launch_bounds__(NT, kVecCtasPerSm) a2av_vector_kernel(const __grid_constant__ Params P,
+                                                         long long max_tile) {
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, max_tile)) return;
+  const int W = P.W, tid = threadIdx.x;
+  const long long rb = P.rb, ntiles = pl.tile_first[W];
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    long long lo, hi;
+    const int p = tile_peer(pl, W, t, rb, &lo, &hi);
+    unsigned char* out = P.out[p];
+    for (int r = 0; r < W; ++r) {
+      const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
+      const long long a = lo > c_lo ? lo : c_lo, b = hi < c_hi ? hi : c_hi;
+      if (a >= b) continue;
+      const unsigned char* src = P.in[r] + pl.in_off[r][p] * rb + (a - c_lo);
+      copy_span<NT, U, US>(out + a, src, b - a, tid);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ bulk --
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Bounded wait for phase `parity` of the mbarrier; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
+  const long long start = clock64();
+  for (;;) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - start > kWaitCycles) return false;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, unsigned bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(src_smem), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Issue the loads of tile t into the stage at `stage`; returns its byte count.
+__device__ __forceinline__ unsigned bulk_issue_tile(const Params& P, const Plan& pl, long long t,
+                                                    uint32_t stage, uint32_t bar) {
+  const int W = P.W;
+  const long long rb = P.rb;
+  long long lo, hi;
+  const int p = tile_peer(pl, W, t, rb, &lo, &hi);
+  mbar_expect_tx(bar, (unsigned)(hi - lo));
+  for (int r = 0; r < W; ++r) {
+    const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
+    const long long a = lo > c_lo ? lo : c_lo, b = hi < c_hi ? hi : c_hi;
+    if (a >= b) continue;
+    bulk_load(stage + (uint32_t)(a - lo), P.in[r] + pl.in_off[r][p] * rb + (a - c_lo),
+              (unsigned)(b - a), bar);
+  }
+  return (unsigned)(hi - lo);
+}
+
+template <int NS, int LEAD>
+__global__ void __launch_bounds__(kBulkThreads) a2av_bulk_kernel(const __grid_constant__ Params P,
+                                                                 int stage_bytes) {
+  static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 tiles ahead of stores");
+  __shared__ Plan pl;
+  __shared__ alignas(8) unsigned long long bars[NS];
+  extern __shared__ __align__(128) unsigned char stages[];
+  if (!build_plan(P, pl, stage_bytes)) return;
+  if (threadIdx.x != 0) return;
+
+  const int W = P.W;
+  const long long rb = P.rb, ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
+  const long long nk = ntiles > b0 ? (ntiles - b0 + G - 1) / G : 0;
+  if (nk == 0) return;
+  const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
+  for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+
+  long long issued = 0;  // tiles whose loads are issued
+  long long stored = 0;  // tiles whose stores are issued
+  bool ok = true;
+  for (long long k = 0; k < nk + LEAD && ok; ++k) {
+    if (k < nk) {
+      const int s = (int)(k % NS);
+      // The store that last read stage s was issued NS - LEAD - 1 stores ago.
+      if (k >= NS) bulk_wait_read<NS - LEAD - 1>();
+      bulk_issue_tile(P, pl, b0 + k * G, stage0 + (uint32_t)s * stage_bytes, bar0 + 8 * s);
+      issued = k + 1;
+    }
+    const long long j = k - LEAD;
+    if (j >= 0 && j < nk) {
+      const int s = (int)(j % NS);
+      if (!mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1))) {
+        ok = false;
+        break;
+      }
+      long long lo, hi;
+      const int p = tile_peer(pl, W, b0 + j * G, rb, &lo, &hi);
+      bulk_store(P.out[p] + lo, stage0 + (uint32_t)s * stage_bytes, (unsigned)(hi - lo));
+      stored = j + 1;
+    }
+  }
+  if (!ok) {
+    // A load never completed: report it, give the loads still in flight a
+    // bounded chance to land, then leave.
+    record_error(P.status, A2AV_ERR_TIMEOUT);
+    for (long long j = stored; j < issued; ++j)
+      mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
+  }
+  bulk_wait_all();
+}
+
+}  // namespace
+
+// ================================================================ host ABI ==
+struct a2av_handle {
+  int W;
+  long long in_cap, out_cap;
+  int device;
+  int sms;
+  int* d_status;
+  int path;         // a2av_path_t
+  int ctas_per_sm;  // 0 = engine default
+  int last_path, last_grid, last_block;
+};
+
+namespace {
+
+using BulkKernel = void (*)(Params, int);
+const BulkKernel kBulk = a2av_bulk_kernel<kBulkStages, kBulkLead>;
+using VecKernel = void (*)(Params, long long);
+const VecKernel kVec = a2av_vector_kernel<kVecThreads, kVecUnroll, kVecShiftUnroll>;
+
+int env_int(const char* name, int fallback) {
+  const char* v = std::getenv(name);
+  if (v == nullptr || *v == '\0') return fallback;
+  return std::atoi(v);
+}
+
+}  // namespace
+
+extern "C" {
+
+int a2av_version(void) { return 10000; }
+
+const char* a2av_error_string(int code) {
+  switch (code) {
+    case A2AV_OK: return "ok";
+    case A2AV_ERR_INVALID_ARG: return "invalid argument";
+    case A2AV_ERR_UNSUPPORTED: return "unsupported (world size above A2AV_MAX_RANKS)";
+    case A2AV_ERR_CUDA: return "CUDA runtime error";
+    case A2AV_ERR_BAD_SPLITS: return "invalid split matrix (detected on the device)";
+    case A2AV_ERR_TIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_rows,
+                a2av_handle** out) {
+  if (out == nullptr) return A2AV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (world_size < 1 || in_capacity_rows < 0 || out_capacity_rows < 0) return A2AV_ERR_INVALID_ARG;
+  if (world_size > kMaxW) return A2AV_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  const int smem = kBulkStages * kBulkStageBytes;
+  if (cudaFuncSetAttribute(kBulk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return A2AV_ERR_CUDA;
+  int* status = nullptr;
+  if (cudaMalloc(&status, 256) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (cudaMemset(status, 0, 256) != cudaSuccess) {
+    cudaFree(status);
+    return A2AV_ERR_CUDA;
+  }
+  a2av_handle* h = new (std::nothrow) a2av_handle();
+  if (h == nullptr) {
+    cudaFree(status);
+    return A2AV_ERR_CUDA;
+  }
+  h->W = world_size;
+  h->in_cap = in_capacity_rows;
+  h->out_cap = out_capacity_rows;
+  h->device = dev;
+  h->sms = sms;
+  h->d_status = status;
+  h->path = env_int("A2AV_PATH", A2AV_PATH_AUTO);
+  if (h->path < A2AV_PATH_AUTO || h->path > A2AV_PATH_BULK) h->path = A2AV_PATH_AUTO;
+  h->ctas_per_sm = env_int("A2AV_CTAS_PER_SM", 0);
+  if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
+  h->last_path = h->last_grid = h->last_block = 0;
+  *out = h;
+  return A2AV_OK;
+}
+
+int a2av_set_path(a2av_handle* h, int path) {
+  if (h == nullptr || path < A2AV_PATH_AUTO || path > A2AV_PATH_BULK) return A2AV_ERR_INVALID_ARG;
+  h->path = path;
+  return A2AV_OK;
+}
+
+int a2av_set_grid(a2av_handle* h, int ctas_per_sm) {
+  if (h == nullptr || ctas_per_sm < 0 || ctas_per_sm > 32) return A2AV_ERR_INVALID_ARG;
+  h->ctas_per_sm = ctas_per_sm;
+  return A2AV_OK;
+}
+
+int a2av_last_launch(const a2av_handle* h, int* path, int* grid, int* block) {
+  if (h == nullptr) return A2AV_ERR_INVALID_ARG;
+  if (path) *path = h->last_path;
+  if (grid) *grid = h->last_grid;
+  if (block) *block = h->last_block;
+  return A2AV_OK;
+}
+
+int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_splits_dev,
+             void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
+             void* stream) {
+  if (h == nullptr || in_ptrs == nullptr || out_ptrs == nullptr || in_splits_dev == nullptr ||
+      out_splits_offsets_dev == nullptr || row_bytes < 1)
+    return A2AV_ERR_INVALID_ARG;
+  if (((uintptr_t)in_splits_dev & 7) != 0 || ((uintptr_t)out_splits_offsets_dev & 7) != 0)
+    return A2AV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (dev != h->device) return A2AV_ERR_INVALID_ARG;
+
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  bool aligned = (row_bytes % 16) == 0;
+  for (int r = 0; r < h->W; ++r) {
+    P.in[r] = static_cast<const unsigned char*>(in_ptrs[r]);
+    P.out[r] = static_cast<unsigned char*>(out_ptrs[r]);
+    aligned = aligned && ((uintptr_t)P.in[r] & 15) == 0 && ((uintptr_t)P.out[r] & 15) == 0;
+  }
+  P.splits = reinterpret_cast<const long long*>(in_splits_dev);
+  P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
+  P.status = h->d_status;
+  P.rb = row_bytes;
+  P.in_cap = h->in_cap;
+  P.out_cap = h->out_cap;
+  P.W = h->W;
+
+  const int path = (h->path == A2AV_PATH_VECTOR || !aligned) ? A2AV_PATH_VECTOR : A2AV_PATH_BULK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  int grid, block;
+  if (path == A2AV_PATH_BULK) {
+    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kBulkCtasPerSm);
+    block = kBulkThreads;
+    kBulk<<<grid, block, kBulkStages * kBulkStageBytes, s>>>(P, kBulkStageBytes);
+  } else {
+    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kVecCtasPerSm);
+    block = kVecThreads;
+    kVec<<<grid, block, 0, s>>>(P, kVecMaxTile);
+  }
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return A2AV_ERR_CUDA;
+  h->last_path = path;
+  h->last_grid = grid;
+  h->last_block = block;
+  return A2AV_OK;
+}
+
+int a2av_status(a2av_handle* h, void* stream, int* device_status) {
+  if (h == nullptr || device_status == nullptr) return A2AV_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int value = 0;
+  if (cudaMemcpyAsync(&value, h->d_status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  if (cudaMemsetAsync(h->d_status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return A2AV_ERR_CUDA;
+  *device_status = value;
+  return A2AV_OK;
+}
+
+int a2av_destroy(a2av_handle* h) {
+  if (h == nullptr) return A2AV_OK;
+  const cudaError_t err = cudaFree(h->d_status);
+  delete h;
+  return err == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
+}
+
+}  // extern "C"

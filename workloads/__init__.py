@@ -42,6 +42,7 @@ __all__ = [
     "Workload",
     "cfg1",
     "cfg2",
+    "cfg2_splits",
     "cfg3",
     "cfg4",
     "cfg5",
@@ -162,6 +163,14 @@ def cfg1(seed: int = 0, rows: int = 4096, hidden: int = 128, W: int = 4) -> Work
     return Workload("cfg1", W, rb, splits, inputs, {"rows_per_rank": rows, "dtype": "bf16"})
 
 
+def cfg2_splits(per_rank_bytes: int, seed: int = 0, W: int = 4,
+                row_bytes: int = CFG2_ROW_BYTES) -> np.ndarray:
+    """The split matrix of ``cfg2`` alone: Multinomial(floor(P / row_bytes), 1/W each) per rank."""
+    rows = per_rank_bytes // row_bytes
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 2, per_rank_bytes]))
+    return np.stack([rng.multinomial(rows, [1.0 / W] * W) for _ in range(W)]).astype(np.int64)
+
+
 def cfg2(per_rank_bytes: int, seed: int = 0, W: int = 4, row_bytes: int = CFG2_ROW_BYTES,
          buffers=None) -> Workload:
     """W=4 payload-sweep point: floor(P / row_bytes) rows per rank, uniform random bits.
@@ -170,8 +179,7 @@ def cfg2(per_rank_bytes: int, seed: int = 0, W: int = 4, row_bytes: int = CFG2_R
     views of pinned host memory) to fill instead of allocating.
     """
     rows = per_rank_bytes // row_bytes
-    rng = np.random.default_rng(np.random.SeedSequence([seed, 2, per_rank_bytes]))
-    splits = np.stack([rng.multinomial(rows, [1.0 / W] * W) for _ in range(W)]).astype(np.int64)
+    splits = cfg2_splits(per_rank_bytes, seed, W, row_bytes)
     inputs = []
     for r in range(W):
         buf = _alloc(rows * row_bytes, None if buffers is None else buffers[r])
