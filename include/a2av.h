@@ -168,6 +168,52 @@ const char *a2av_error_string(int code);
 /* a2av_version -- 10000*major + 100*minor + patch of this library. */
 int a2av_version(void);
 
+/* Bytes of device memory the library reserves for a2av_run_noalloc. */
+#define A2AV_NOALLOC_SCRATCH_BYTES 256
+
+/*
+ * a2av_run_noalloc -- the same exchange as a2av_run, for callers that cannot
+ * allocate device memory.  (The pages have no counterpart; this is an
+ * interface addition of this library.)
+ *
+ * Who needs it: a2av_create calls cudaMalloc for the handle's status word.
+ * Some callers may not do that: engines that plan every byte of device memory
+ * up front and forbid allocation once they run, hosts that own the only
+ * allocator and hand plug-ins nothing but buffers, and code on a latency path
+ * where cudaMalloc's implicit device synchronisation is not acceptable.  This
+ * entry point takes no handle and allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  The caller still passes every
+ * input and output.
+ *
+ * Scratch: the status word lives in a fixed A2AV_NOALLOC_SCRATCH_BYTES-byte
+ * array inside the library's own device code.  Every GPU that loads the
+ * library holds that array until the process exits.  Each call clears the
+ * status word on `stream` before its kernel runs.  All calls in the process
+ * share the one array: calls whose work overlaps on the GPU (different
+ * streams, or different host threads) race on it, so their statuses are not
+ * reliable; serialise such calls.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and configures the kernels, with that device
+ * current.  Make that first call before any stream capture begins.
+ *
+ * Arguments: world_size, in_capacity_rows and out_capacity_rows as in
+ * a2av_create; in_ptrs .. stream as in a2av_run (the copy engine is chosen as
+ * A2AV_PATH_AUTO does).  device_status: NULL makes the call asynchronous like
+ * a2av_run, with no status reported; a host int* makes the call wait for the
+ * exchange (it synchronises `stream`) and store the device-detected status
+ * there (A2AV_OK, A2AV_ERR_BAD_SPLITS or A2AV_ERR_TIMEOUT).
+ *
+ * Limit: the scratch does not grow with the exchange, so the only size the
+ * call can exceed is the rank count.  world_size > A2AV_MAX_RANKS returns
+ * A2AV_ERR_UNSUPPORTED; a device ordinal of 64 or more also returns
+ * A2AV_ERR_UNSUPPORTED.  Other host errors are those of a2av_run.
+ */
+int a2av_run_noalloc(int world_size, int64_t in_capacity_rows, int64_t out_capacity_rows,
+                     const void *const *in_ptrs, const int64_t *in_splits_dev,
+                     void *const *out_ptrs, int64_t *out_splits_offsets_dev, int64_t row_bytes,
+                     void *stream, int *device_status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -17,7 +17,7 @@ from ._build import LIBRARY, build
 __all__ = [
     "A2av", "A2avError", "load", "build",
     "a2av_create", "a2av_run", "a2av_status", "a2av_destroy", "a2av_set_path",
-    "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version",
+    "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "MAX_RANKS",
 ]
@@ -55,11 +55,12 @@ def load():
     lib.a2av_set_grid.argtypes = [vp, ci]
     lib.a2av_last_launch.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci),
                                      ctypes.POINTER(ci)]
+    lib.a2av_run_noalloc.argtypes = [ci, i64, i64, pp, vp, pp, vp, i64, vp, ctypes.POINTER(ci)]
     lib.a2av_error_string.argtypes = [ci]
     lib.a2av_error_string.restype = ctypes.c_char_p
     lib.a2av_version.argtypes = []
     for f in ("a2av_create", "a2av_run", "a2av_status", "a2av_destroy", "a2av_set_path",
-              "a2av_set_grid", "a2av_last_launch", "a2av_version"):
+              "a2av_set_grid", "a2av_last_launch", "a2av_version", "a2av_run_noalloc"):
         getattr(lib, f).restype = ci
     _lib = lib
     return lib
@@ -122,6 +123,23 @@ def a2av_last_launch(handle):
     p, g, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = load().a2av_last_launch(handle, ctypes.byref(p), ctypes.byref(g), ctypes.byref(b))
     return rc, p.value, g.value, b.value
+
+
+def a2av_run_noalloc(world_size: int, in_capacity_rows: int, out_capacity_rows: int, in_ptrs,
+                     in_splits_dev: int, out_ptrs, out_splits_offsets_dev: int, row_bytes: int,
+                     stream: int = 0, wait: bool = True):
+    """The allocation-free entry point (no handle; see include/a2av.h).
+
+    Returns (status, device_status); with ``wait`` False the call is
+    asynchronous and device_status is None."""
+    v = ctypes.c_int(0)
+    rc = load().a2av_run_noalloc(int(world_size), int(in_capacity_rows), int(out_capacity_rows),
+                                 _ptr_array(in_ptrs), ctypes.c_void_p(int(in_splits_dev) or None),
+                                 _ptr_array(out_ptrs),
+                                 ctypes.c_void_p(int(out_splits_offsets_dev) or None),
+                                 int(row_bytes), ctypes.c_void_p(int(stream) or None),
+                                 ctypes.byref(v) if wait else None)
+    return rc, (v.value if wait else None)
 
 
 # --------------------------------------------------------- torch-facing --

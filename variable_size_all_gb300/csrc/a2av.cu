@@ -40,6 +40,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 namespace {
@@ -654,3 +655,94 @@ int a2av_destroy(a2av_handle* h) {
 }
 
 }  // extern "C"
+
+// ===================================================== allocation-free call ==
+// The status word of a2av_run_noalloc.  Host code never touches this name:
+// on the host it is only a stand-in, so its device address is looked up once
+// per device (with that device current) and passed to the kernels.
+static __device__ __align__(256) int g_noalloc_scratch[A2AV_NOALLOC_SCRATCH_BYTES / sizeof(int)];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+int* g_noalloc_status[kNoAllocMaxDevices];  // device address of g_noalloc_scratch
+int g_noalloc_sms[kNoAllocMaxDevices];
+
+int noalloc_setup(int dev, int** status, int* sms) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_status[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess) return A2AV_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return A2AV_ERR_CUDA;
+    if (cudaFuncSetAttribute(kBulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kBulkStages * kBulkStageBytes) != cudaSuccess)
+      return A2AV_ERR_CUDA;
+    g_noalloc_sms[dev] = n;
+    g_noalloc_status[dev] = static_cast<int*>(addr);
+  }
+  *status = g_noalloc_status[dev];
+  *sms = g_noalloc_sms[dev];
+  return A2AV_OK;
+}
+
+}  // namespace
+
+extern "C" int a2av_run_noalloc(int world_size, int64_t in_capacity_rows,
+                                int64_t out_capacity_rows, const void* const* in_ptrs,
+                                const int64_t* in_splits_dev, void* const* out_ptrs,
+                                int64_t* out_splits_offsets_dev, int64_t row_bytes, void* stream,
+                                int* device_status) {
+  static_assert(sizeof(int) <= A2AV_NOALLOC_SCRATCH_BYTES, "the status word fits the scratch");
+  if (world_size < 1 || in_capacity_rows < 0 || out_capacity_rows < 0 || in_ptrs == nullptr ||
+      out_ptrs == nullptr || in_splits_dev == nullptr || out_splits_offsets_dev == nullptr ||
+      row_bytes < 1)
+    return A2AV_ERR_INVALID_ARG;
+  if (world_size > kMaxW) return A2AV_ERR_UNSUPPORTED;
+  if (((uintptr_t)in_splits_dev & 7) != 0 || ((uintptr_t)out_splits_offsets_dev & 7) != 0)
+    return A2AV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return A2AV_ERR_UNSUPPORTED;
+  int* status = nullptr;
+  int sms = 0;
+  const int rc = noalloc_setup(dev, &status, &sms);
+  if (rc != A2AV_OK) return rc;
+
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  bool aligned = (row_bytes % 16) == 0;
+  for (int r = 0; r < world_size; ++r) {
+    P.in[r] = static_cast<const unsigned char*>(in_ptrs[r]);
+    P.out[r] = static_cast<unsigned char*>(out_ptrs[r]);
+    aligned = aligned && ((uintptr_t)P.in[r] & 15) == 0 && ((uintptr_t)P.out[r] & 15) == 0;
+  }
+  P.splits = reinterpret_cast<const long long*>(in_splits_dev);
+  P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
+  P.status = status;
+  P.rb = row_bytes;
+  P.in_cap = in_capacity_rows;
+  P.out_cap = out_capacity_rows;
+  P.W = world_size;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The kernels only ever set the status word, so it must start at zero.
+  if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (aligned) {
+    kBulk<<<sms * kBulkCtasPerSm, kBulkThreads, kBulkStages * kBulkStageBytes, s>>>(
+        P, kBulkStageBytes);
+  } else {
+    kVec<<<sms * kVecCtasPerSm, kVecThreads, 0, s>>>(P, kVecMaxTile);
+  }
+  if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  if (device_status != nullptr) {
+    int value = 0;
+    if (cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return A2AV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return A2AV_ERR_CUDA;
+    *device_status = value;
+  }
+  return A2AV_OK;
+}
