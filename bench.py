@@ -230,6 +230,40 @@ def time_oracle(inputs, splits, row_bytes, budget_s: float, peers=None, check=No
 
 
 # ----------------------------------------------------------------- ours ----
+L2_BYTES = 129 * 10**6
+WORKLOADS = ("cfg2", "cfg1", "cfg3", "cfg4", "cfg5")
+
+
+def describe(name: str, per_rank_bytes: int, seed: int) -> str:
+    if name == "cfg2":
+        return workload_name(per_rank_bytes)
+    return {
+        "cfg1": "a2av W=4, 4096 rows/rank of 128 bf16 (256 B), N(0,1) bf16, "
+                "in_splits ~ Multinomial(4096, 1/4)",
+        "cfg3": "a2av W=8 MoE dispatch: 8192 tokens/rank, hidden 7168 bf16 (14336 B rows), "
+                "top-2 of 64 experts (8 per rank), Zipf(1.2) popularity shuffled per seed",
+        "cfg4": "a2av W=8, 2^20 rows/rank of 13 int8 bytes (unaligned), "
+                "in_splits ~ Multinomial(2^20, Dirichlet(0.1))",
+        "cfg5": "a2av W=2 embedding keys: 26 features x 8192 bags per rank, "
+                "min(Poisson(3), 20) int64 keys per bag, U[0, 1e7), feature mod 2 ownership",
+    }[name] + f", seed {seed}"
+
+
+def load_workload(args, torch):
+    """The workload's inputs in pinned host memory (also the e2e sources)."""
+    import workloads as wl
+    if args.workload == "cfg2":
+        P = args.per_rank_bytes
+        nbytes = (P // ROW_BYTES) * ROW_BYTES
+        h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
+        w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
+    else:
+        w = {"cfg1": wl.cfg1, "cfg3": wl.cfg3, "cfg4": wl.cfg4, "cfg5": wl.cfg5}[args.workload](
+            args.seed)
+        h_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
+    return w, h_in
+
+
 def run_ours(args):
     import torch
     import variable_size_all_gb300 as a2av
@@ -242,26 +276,28 @@ def run_ours(args):
     a2av.build()
     path_id = {"auto": a2av.PATH_AUTO, "vector": a2av.PATH_VECTOR, "bulk": a2av.PATH_BULK}[args.path]
 
-    P = args.per_rank_bytes
-    rows = P // ROW_BYTES
-    nbytes = rows * ROW_BYTES
-    # Inputs drawn on the host into pinned memory (they are also the e2e sources).
-    h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
     t0 = time.time()
-    w = wl.cfg2(P, seed=0, buffers=[t.numpy() for t in h_in])
+    w, h_in = load_workload(args, torch)
     gen_s = time.time() - t0
-    S = w.splits
-    recv = [int(S[:, p].sum()) * ROW_BYTES for p in range(W)]
-    T = moved_bytes(S, ROW_BYTES)
+    Wn, rb, S = w.W, w.row_bytes, w.splits
+    P = args.per_rank_bytes
+    in_bytes = [t.numel() for t in h_in]
+    recv = [int(S[:, p].sum()) * rb for p in range(Wn)]
+    T = moved_bytes(S, rb)
     d_in = [t.to(dev) for t in h_in]
     d_out = [torch.empty(n, dtype=torch.uint8, device=dev) for n in recv]
     d_S = torch.from_numpy(S).to(dev)
-    d_so = torch.empty((W, 2, W), dtype=torch.int64, device=dev)
-    eng = a2av.A2av(W, path=path_id, ctas_per_sm=args.ctas_per_sm)
+    d_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, device=dev)
+    eng = a2av.A2av(Wn, path=path_id, ctas_per_sm=args.ctas_per_sm)
     stream = torch.cuda.current_stream()
+    # Inputs larger than twice the L2 stream from HBM anyway; smaller ones get
+    # the L2 flushed before every timed launch by reading 512 MiB (a read leaves
+    # clean lines, so no earlier write-back lands inside the timed launch).
+    cold = sum(in_bytes) < 2 * L2_BYTES
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
 
     def step(ins=d_in, outs=d_out, splits=d_S):
-        eng.run(ins, splits, outs, d_so, ROW_BYTES, stream=stream)
+        eng.run(ins, splits, outs, d_so, rb, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -280,23 +316,26 @@ def run_ours(args):
         torch.cuda.synchronize()
         t_begin.record(stream)
         for a, b in ev:
+            if cold:
+                flush.sum()
             a.record(stream)
             step()
             b.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier()
-    total_ms = t_begin.elapsed_time(t_end)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
+    # with flushes in between, a step's time is its launch's own duration
+    timed_s = (sum(launch_ms) if cold else t_begin.elapsed_time(t_end)) / 1e3
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during the timed region")
-    max_s = reduce_max(total_ms / 1e3, dev)
+    max_s = reduce_max(timed_s, dev)
     value = whole_job_value(T * K / 1e9, world, max_s)
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     med_launch_s = statistics.median(launch_ms) / 1e3
 
     # ---- roofline of the (only) kernel -----------------------------------
-    algo = algorithmic_bytes(S, ROW_BYTES)
+    algo = algorithmic_bytes(S, rb)
     peak, peak_kind = hbm_peak()
     kname = "a2av_bulk_kernel" if launch["path"] == a2av.PATH_BULK else "a2av_vector_kernel"
     achieved = algo / avg_launch_s / 1e9
@@ -310,23 +349,26 @@ def run_ours(args):
     dst = torch.empty_like(src)
     for _ in range(3):
         dst.copy_(src)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    d2d = []
     for _ in range(5):
+        if cold:
+            flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
         dst.copy_(src)
-    b.record(stream)
-    torch.cuda.synchronize()
-    d2d_gbps = src.numel() * 5 / (a.elapsed_time(b) / 1e3) / 1e9
+        b.record(stream)
+        b.synchronize()
+        d2d.append(a.elapsed_time(b) / 1e3)
+    d2d_gbps = src.numel() / statistics.median(d2d) / 1e9
     del src, dst
 
     # ---- payload sweep (cold L2 between launches) --------------------------
     sweep = []
-    if not args.no_sweep:
-        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    if args.workload == "cfg2" and not args.no_sweep:
         for Pk in wl.CFG2_SWEEP_BYTES:
             if Pk > P:
                 break
-            Sk = wl.cfg2_splits(Pk, 0)
+            Sk = wl.cfg2_splits(Pk, args.seed)
             nk = (Pk // ROW_BYTES) * ROW_BYTES
             ins = [t[:nk] for t in d_in]  # prefix of the same draw = cfg2(Pk)'s inputs
             outs = [t[: int(Sk[:, p].sum()) * ROW_BYTES] for p, t in enumerate(d_out)]
@@ -335,7 +377,7 @@ def run_ours(args):
                 step(ins, outs, dSk)
             times = []
             for _ in range(args.sweep_reps):
-                flush.zero_()
+                flush.sum()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 step(ins, outs, dSk)
@@ -350,16 +392,16 @@ def run_ours(args):
                           "moved_GBps": round(Tk / t_med / 1e9, 1),
                           "busbw_GBps": round(busbw_gbps(nk, t_med), 1),
                           "hbm_frac": round(algorithmic_bytes(Sk, ROW_BYTES) / t_med / 1e9 / peak, 4)})
-        del flush
         if eng.status() != a2av.OK:
             raise SystemExit("device reported an error during the sweep")
+    del flush
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
     if not args.no_e2e:
         h_out = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for n in recv]
         h_S = torch.from_numpy(S).pin_memory()
-        h_so = torch.empty((W, 2, W), dtype=torch.int64, pin_memory=True)
+        h_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, pin_memory=True)
 
         def e2e_step():
             for h, d in zip(h_in, d_in):
@@ -384,8 +426,8 @@ def run_ours(args):
         barrier()
         e_s = reduce_max(a.elapsed_time(b) / 1e3, dev)
         e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, e_s), 2), "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() for t in h_in) + S.size * 8,
-               "d2h_bytes_per_step": sum(recv) + 2 * W * W * 8, "steps": Ke}
+               "h2d_bytes_per_step": sum(in_bytes) + S.size * 8,
+               "d2h_bytes_per_step": sum(recv) + 2 * Wn * Wn * 8, "steps": Ke}
         if eng.status() != a2av.OK:
             raise SystemExit("device reported an error during the e2e run")
 
@@ -401,29 +443,33 @@ def run_ours(args):
                     and np.array_equal(d_so[p].cpu().numpy(), so)):
                 mismatched.append(p)
 
-        spent, moved, peers = time_oracle(inputs, S, ROW_BYTES, args.cpu_budget, check=compare)
+        spent, moved, peers = time_oracle(inputs, S, rb, args.cpu_budget, check=compare)
         cpu = {"value": round(moved / spent / 1e9, 3), "unit": UNIT, "cores": 1,
                "kind": "oracle",
-               "sample": f"peers {peers} of the same {P >> 20} MiB/rank exchange "
-                         f"({moved / 2**30:.2f} GiB of the {T / 2**30:.2f} GiB moved per step)",
-               "seconds": round(spent, 2)}
+               "sample": f"peers {peers} of the same exchange "
+                         f"({moved / 2**30:.3f} GiB of the {T / 2**30:.3f} GiB moved per step)",
+               "seconds": round(spent, 3)}
         parity = {"bit_exact": not mismatched, "peers_checked": peers}
         if mismatched:
             raise SystemExit(f"GPU output differs from the oracle on peers {mismatched}")
 
     eng.close()
+    per_rank = statistics.mean(in_bytes)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": workload_name(P), "ranks": W, "row_bytes": ROW_BYTES,
-                   "per_rank_bytes": nbytes, "moved_bytes_per_step": T,
-                   "l2": "inputs larger than L2 (4 x 4 GiB per step); sweep flushes L2",
+        "config": {"workload": describe(args.workload, P, args.seed), "name": args.workload,
+                   "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
+                   "moved_bytes_per_step": T,
+                   "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
+                          "the launch's CUDA-event duration") if cold else
+                         "inputs larger than L2; step time = bracketed CUDA-event time",
                    "engine": kname, "grid": launch["grid"], "block": launch["block"],
                    "parallelism": f"replicas x{world} (ranks emulated inside each GPU)"},
         "hbm_fraction": round(2 * T / (max_s / K) / 1e9 / peak, 4),
-        "busbw_GBps": round(busbw_gbps(nbytes, max_s / K), 1),
+        "busbw_GBps": round(busbw_gbps(per_rank, max_s / K), 1),
         "launch_us_median": round(med_launch_s * 1e6, 2),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -448,14 +494,18 @@ def run_reference(args):
         return
     import workloads as wl
     P = args.per_rank_bytes
-    w = wl.cfg2(P, seed=0)
-    S, inputs = w.splits, w.inputs
+    if args.workload == "cfg2":
+        w = wl.cfg2(P, seed=args.seed)
+    else:
+        w = {"cfg1": wl.cfg1, "cfg3": wl.cfg3, "cfg4": wl.cfg4, "cfg5": wl.cfg5}[args.workload](
+            args.seed)
+    S, inputs, rb, Wn = w.splits, w.inputs, w.row_bytes, w.W
     K, Wm = args.steps, args.warmup
     for k in range(Wm):
-        time_oracle(inputs, S, ROW_BYTES, 0.0, peers=[k % W])
+        time_oracle(inputs, S, rb, 0.0, peers=[k % Wn])
     total_s, total_b = 0.0, 0
     for k in range(K):
-        s, b, _ = time_oracle(inputs, S, ROW_BYTES, 0.0, peers=[k % W])
+        s, b, _ = time_oracle(inputs, S, rb, 0.0, peers=[k % Wn])
         total_s += s
         total_b += b
     value = total_b / total_s / 1e9
@@ -464,11 +514,12 @@ def run_reference(args):
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(total_s * 1e3 / K, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": workload_name(P), "ranks": W, "row_bytes": ROW_BYTES,
-                   "per_rank_bytes": (P // ROW_BYTES) * ROW_BYTES,
+        "config": {"workload": describe(args.workload, P, args.seed), "name": args.workload,
+                   "ranks": Wn, "row_bytes": rb,
+                   "per_rank_bytes": int(statistics.mean(b.size for b in inputs)),
                    "parallelism": "one host core"},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "one peer's whole output per step (peer = step mod 4)"},
+                         "sample": f"one peer's whole output per step (peer = step mod {Wn})"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -481,7 +532,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--per-rank-bytes", type=int, default=1 << 32)
+    ap.add_argument("--workload", choices=WORKLOADS, default="cfg2")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--per-rank-bytes", type=int, default=1 << 32, help="cfg2 payload per rank")
     ap.add_argument("--path", choices=["auto", "vector", "bulk"], default="auto")
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--sweep-reps", type=int, default=20)

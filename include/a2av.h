@@ -59,9 +59,10 @@ typedef enum {
 
 /* Copy engine selection (a2av_set_path). */
 typedef enum {
-  A2AV_PATH_AUTO = 0,   /* bulk when every row and buffer is 16-byte aligned, else vector */
-  A2AV_PATH_VECTOR = 1, /* 16-byte vector loads/stores with in-register realignment */
-  A2AV_PATH_BULK = 2    /* cp.async.bulk global->shared->global staging (aligned only) */
+  A2AV_PATH_AUTO = 0,   /* bulk when every row and buffer is 16-byte aligned, else staged */
+  A2AV_PATH_VECTOR = 1, /* 16-byte register loads/stores, realigned by warp shuffles */
+  A2AV_PATH_BULK = 2,   /* cp.async.bulk global->shared->global (aligned exchanges only) */
+  A2AV_PATH_STAGED = 3  /* cp.async.bulk granules -> shared -> realigned 16-byte stores */
 } a2av_path_t;
 
 typedef struct a2av_handle a2av_handle;
@@ -144,7 +145,7 @@ int a2av_destroy(a2av_handle *h);
 /*
  * a2av_set_path -- choose the copy engine for later runs (a2av_path_t).
  * A2AV_PATH_BULK on a run whose row_bytes or buffer addresses are not all
- * 16-byte aligned falls back to the vector engine for that run.
+ * 16-byte aligned falls back to the staged engine for that run.
  * Errors: A2AV_ERR_INVALID_ARG.
  */
 int a2av_set_path(a2av_handle *h, int path);

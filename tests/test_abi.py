@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_host_checks_without_gpu(lib):
-    assert a2av.a2av_version() == 10000
+    assert a2av.a2av_version() >= 10000
     assert a2av.a2av_error_string(a2av.ERR_BAD_SPLITS).startswith("invalid split")
     assert a2av.a2av_error_string(12345) == "unknown status"
     assert a2av.a2av_create(0)[0] == a2av.ERR_INVALID_ARG

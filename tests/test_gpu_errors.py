@@ -38,7 +38,7 @@ def _untouched(outs, so):
 S0 = np.array([[1, 2, 0], [0, 1, 1], [2, 0, 3]], dtype=np.int64)
 
 
-@pytest.mark.parametrize("path", [a2av.PATH_AUTO, a2av.PATH_VECTOR])
+@pytest.mark.parametrize("path", [a2av.PATH_AUTO, a2av.PATH_VECTOR, a2av.PATH_STAGED])
 @pytest.mark.parametrize("case", ["negative", "in_cap", "out_cap", "limit", "null_in", "null_out"])
 def test_bad_splits_write_nothing(case, path):
     rb = 16
@@ -101,6 +101,7 @@ def test_host_rejections_launch_nothing():
     assert a2av.a2av_run(h, ip, S.data_ptr() + 4, op, so.data_ptr(), 4) == a2av.ERR_INVALID_ARG
     assert a2av.a2av_run(None, ip, S.data_ptr(), op, so.data_ptr(), 4) == a2av.ERR_INVALID_ARG
     assert a2av.a2av_set_path(h, 7) == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_set_path(h, 4) == a2av.ERR_INVALID_ARG
     assert a2av.a2av_set_grid(h, 33) == a2av.ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert _untouched(outs, so)

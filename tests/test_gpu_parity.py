@@ -1,6 +1,6 @@
 """GPU parity: the CUDA exchange against the CPU oracle, byte for byte.
 
-Covers the five workloads (config 4 over its 16 seeds), both copy engines,
+Covers the five workloads (config 4 over its 16 seeds), all three copy engines,
 random split matrices with empty, skewed, diagonal and single-chunk patterns,
 row sizes from 1 B to 14336 B, misaligned buffer addresses, small and large
 grids (few or many tiles per CTA), W from 1 to 32, streams and reuse.
@@ -15,7 +15,7 @@ from tests._gpu import exchange_checked
 pytestmark = pytest.mark.gpu
 
 a2av = pytest.importorskip("variable_size_all_gb300")
-VEC, BULK, AUTO = a2av.PATH_VECTOR, a2av.PATH_BULK, a2av.PATH_AUTO
+VEC, BULK, AUTO, STAGED = a2av.PATH_VECTOR, a2av.PATH_BULK, a2av.PATH_AUTO, a2av.PATH_STAGED
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,25 +26,29 @@ def _cuda():
     a2av.load()
 
 
-@pytest.mark.parametrize("path", [AUTO, VEC])
+@pytest.mark.parametrize("path", [AUTO, VEC, STAGED])
 def test_cfg1(path):
     w = wl.cfg1(0)
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path,
-                     expect_path=BULK if path == AUTO else VEC)
+                     expect_path=BULK if path == AUTO else path)
 
 
 @pytest.mark.parametrize("seed", range(16))
 def test_cfg4_seeds(seed):
     w = wl.cfg4(seed)
-    exchange_checked(w.inputs, w.splits, w.row_bytes, expect_path=VEC)
-
-
-def test_cfg5():
-    w = wl.cfg5(0)
-    exchange_checked(w.inputs, w.splits, w.row_bytes, expect_path=VEC)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, expect_path=STAGED)
+    if seed < 4:
+        exchange_checked(w.inputs, w.splits, w.row_bytes, path=VEC, expect_path=VEC)
 
 
 @pytest.mark.parametrize("path", [AUTO, VEC])
+def test_cfg5(path):
+    w = wl.cfg5(0)
+    exchange_checked(w.inputs, w.splits, w.row_bytes, path=path,
+                     expect_path=STAGED if path == AUTO else VEC)
+
+
+@pytest.mark.parametrize("path", [AUTO, VEC, STAGED])
 def test_cfg3_full(path):
     w = wl.cfg3(0)
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path)
@@ -57,7 +61,7 @@ def test_cfg3_seeds_small_grid(seed):
 
 
 @pytest.mark.parametrize("mib", [1, 2, 4, 8, 16, 32, 64])
-@pytest.mark.parametrize("path", [AUTO, VEC])
+@pytest.mark.parametrize("path", [AUTO, VEC, STAGED])
 def test_cfg2_sweep_points(mib, path):
     w = wl.cfg2(mib << 20)
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path)
@@ -76,30 +80,34 @@ def test_random_splits(rb):
             w = wl.random_case(1000 * rb + 10 * k + modes.index(mode), W, rb, max_rows, mode)
             in_mis = [int(rng.integers(0, 16)) for _ in range(W)]
             out_mis = [int(rng.integers(0, 16)) for _ in range(W)]
-            exchange_checked(w.inputs, w.splits, rb, in_mis=in_mis, out_mis=out_mis,
-                             ctas_per_sm=int(rng.choice([0, 1, 4])))
+            path = [AUTO, VEC, STAGED][(k + modes.index(mode)) % 3]
+            exchange_checked(w.inputs, w.splits, rb, path=path, in_mis=in_mis, out_mis=out_mis,
+                             ctas_per_sm=int(rng.choice([0, 1, 2])))
 
 
-@pytest.mark.parametrize("path", [VEC, BULK])
+@pytest.mark.parametrize("path", [VEC, BULK, STAGED])
 def test_aligned_engines_agree(path):
     for W, rb in ((4, 16), (8, 32), (3, 4096), (32, 16)):
         w = wl.random_case(7 + W, W, rb, 500, "uniform")
         exchange_checked(w.inputs, w.splits, rb, path=path, expect_path=path)
 
 
-def test_bulk_request_on_misaligned_falls_back_to_vector():
+def test_bulk_request_on_misaligned_falls_back_to_staged():
     w = wl.random_case(3, 4, 16, 100, "uniform")
-    exchange_checked(w.inputs, w.splits, 16, path=BULK, in_mis=[0, 4, 0, 0], expect_path=VEC)
+    exchange_checked(w.inputs, w.splits, 16, path=BULK, in_mis=[0, 4, 0, 0], expect_path=STAGED)
     w = wl.random_case(4, 4, 24, 100, "uniform")
-    exchange_checked(w.inputs, w.splits, 24, path=BULK, expect_path=VEC)
+    exchange_checked(w.inputs, w.splits, 24, path=BULK, expect_path=STAGED)
 
 
 @pytest.mark.parametrize("grid", [1, 2, 8, 32])
 def test_grid_sizes(grid):
+    # more CTAs than fit on the GPU at once, for every engine
     w = wl.cfg4(5, rows=1 << 16)
-    exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=grid)
+    for path in (AUTO, VEC):
+        exchange_checked(w.inputs, w.splits, w.row_bytes, path=path, ctas_per_sm=grid)
     w = wl.cfg2(4 << 20)
-    exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=grid)
+    for path in (AUTO, VEC, STAGED):
+        exchange_checked(w.inputs, w.splits, w.row_bytes, path=path, ctas_per_sm=grid)
 
 
 def test_single_huge_chunk_and_tile_edges():
@@ -109,8 +117,8 @@ def test_single_huge_chunk_and_tile_edges():
         S[2, 1] = rows
         inputs = [np.zeros(0, np.uint8)] * 4
         inputs[2] = np.random.default_rng(rows).integers(0, 256, rows * 16, dtype=np.uint8)
-        exchange_checked(inputs, S, 16)
-        exchange_checked(inputs, S, 16, path=VEC)
+        for path in (AUTO, VEC, STAGED):
+            exchange_checked(inputs, S, 16, path=path)
 
 
 def test_side_stream_and_reuse():
@@ -160,3 +168,15 @@ def test_back_to_back_without_sync_keeps_stream_order():
     eng.close()
     assert torch.equal(o[0], b) and torch.equal(o[1], a)
     assert so[:, 0, :].tolist() == [[0, 64], [64, 0]]
+
+
+def test_many_tiny_segments_per_tile():
+    # W = 32 ranks, a few 1-byte or 13-byte rows per chunk: every tile holds
+    # dozens of segments, each with its own granule overhang in the stage
+    for rb in (1, 13):
+        S = np.random.default_rng(rb).integers(0, 4, size=(32, 32)).astype(np.int64)
+        inputs = [np.random.default_rng(100 + r).integers(0, 256, int(S[r].sum()) * rb,
+                                                          dtype=np.uint8) for r in range(32)]
+        mis = list(range(16)) * 2
+        for path in (AUTO, VEC, STAGED):
+            exchange_checked(inputs, S, rb, path=path, in_mis=mis, out_mis=mis[::-1])

@@ -19,11 +19,11 @@ __all__ = [
     "a2av_create", "a2av_run", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
-    "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "MAX_RANKS",
+    "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BAD_SPLITS, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
-PATH_AUTO, PATH_VECTOR, PATH_BULK = 0, 1, 2
+PATH_AUTO, PATH_VECTOR, PATH_BULK, PATH_STAGED = 0, 1, 2, 3
 MAX_RANKS = 32
 
 _lib = None

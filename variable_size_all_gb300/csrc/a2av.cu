@@ -8,7 +8,7 @@
 //
 // How (one launch, no host round trip):
 //   1. Every CTA loads the W x W split matrix (<= 8 KiB, L2-resident after the
-//      first CTA), validates it and builds, in shared memory, the row-offset
+//      first CTA), validates it and builds, in shared memory, the offset
 //      tables with warp-shuffle exclusive scans: out_off[p][r] (column scans)
 //      and in_off[r][p] (row scans).  All CTAs reach the same verdict, so an
 //      invalid matrix stops every CTA before any byte is written, without any
@@ -23,15 +23,21 @@
 //      limit: CTAs follow bytes, so one huge chunk gets most CTAs, empty
 //      chunks get none and many tiny chunks share a CTA.
 //   3. Copy engines:
-//      - vector: 16-byte loads/stores aligned on the destination; when the
-//        source is misaligned relative to the destination (row sizes that are
-//        not multiples of 16, e.g. 13 B or 8 B rows) each lane loads its
-//        aligned source granule, takes its neighbour's by a warp shuffle and
-//        funnel-shifts the pair into place; head and tail bytes go one by one.
-//      - bulk: when every row and buffer is 16-byte aligned, one thread per
-//        CTA streams tiles global -> shared -> global with cp.async.bulk,
-//        completion tracked by mbarriers, through a ring of shared-memory
-//        stages.  No cluster multicast.
+//      - bulk (every row and buffer 16-byte aligned): one warp per CTA streams
+//        tiles global -> shared -> global with cp.async.bulk; lane r loads
+//        source r's part of a tile, lane 0 stores the tile; mbarriers track
+//        the loads through a ring of shared-memory stages.
+//      - staged (any alignment): a producer warp loads, with cp.async.bulk,
+//        the 16-byte granules that hold each source segment of a tile into a
+//        shared-memory stage; consumer warps rebuild destination-aligned
+//        16-byte vectors from shared memory (funnel shifts when source and
+//        destination differ mod 16) and store them with st.global.v4; head
+//        and tail bytes go one by one.  Full/empty mbarriers pair the warps.
+//      - vector (any alignment, no shared-memory staging): 16-byte loads and
+//        stores from registers; a misaligned source is realigned with a warp
+//        shuffle of neighbouring granules and a funnel shift.
+//      No cluster multicast anywhere.  Every mbarrier wait is bounded (~1 s),
+//      after which the kernel records A2AV_ERR_TIMEOUT and leaves.
 //   CTA 0 writes out_splits_offsets.
 #include "a2av.h"
 
@@ -48,8 +54,10 @@ namespace {
 constexpr int kMaxW = A2AV_MAX_RANKS;
 constexpr long long kMaxBytes = 1LL << 62;  // byte offsets stay below 2^62
 constexpr unsigned kFull = 0xffffffffu;
-constexpr long long kTileGranule = 4096;     // tile sizes are multiples of this
+constexpr long long kTileGranule = 4096;         // tile sizes are multiples of this
 constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+
+}  // namespace
 
 // Engine shapes.  Each can be overridden at compile time (-DA2AV_...) for
 // tuning sweeps; the defaults are the measured choices.
@@ -80,6 +88,32 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 #ifndef A2AV_BULK_CTAS_PER_SM
 #define A2AV_BULK_CTAS_PER_SM 1
 #endif
+#ifndef A2AV_STAGED_STAGES
+#define A2AV_STAGED_STAGES 4
+#endif
+#ifndef A2AV_STAGED_STAGE_BYTES
+#define A2AV_STAGED_STAGE_BYTES (32 * 1024)
+#endif
+#ifndef A2AV_STAGED_CONSUMER_WARPS
+#define A2AV_STAGED_CONSUMER_WARPS 4
+#endif
+#ifndef A2AV_STAGED_CTAS_PER_SM
+#define A2AV_STAGED_CTAS_PER_SM 1
+#endif
+#ifndef A2AV_TILES_PER_CTA
+#define A2AV_TILES_PER_CTA 1
+#endif
+// L2 eviction hints of the bulk engine: bit 0 marks loaded lines
+// evict-first, bit 1 stored lines (each byte is used exactly once).
+#ifndef A2AV_L2_HINT
+#define A2AV_L2_HINT 0
+#endif
+
+namespace {
+
+// Tiles each CTA gets at least, when the payload allows (smaller tiles for
+// small payloads keep more of them in flight per CTA).
+constexpr long long kTilesPerCta = A2AV_TILES_PER_CTA;
 
 // Vector engine: 512 threads (64 registers each, two CTAs per SM), 4
 // independent 16-byte loads in flight per thread on the aligned path (32 KiB
@@ -90,13 +124,25 @@ constexpr int kVecShiftUnroll = A2AV_VEC_SHIFT_UNROLL;
 constexpr long long kVecMaxTile = A2AV_VEC_MAX_TILE;
 constexpr int kVecCtasPerSm = A2AV_VEC_CTAS_PER_SM;
 
-// Bulk engine: stages of 32 KiB in a ring of 4; loads run 2 tiles ahead of
-// the stores that drain them.
+// Bulk engine: a ring of stages (tile = stage size); loads run LEAD tiles
+// ahead of the stores that drain them.
 constexpr int kBulkThreads = 128;
 constexpr int kBulkStages = A2AV_BULK_STAGES;
 constexpr int kBulkLead = A2AV_BULK_LEAD;
 constexpr int kBulkStageBytes = A2AV_BULK_STAGE_BYTES;
 constexpr int kBulkCtasPerSm = A2AV_BULK_CTAS_PER_SM;
+
+// Staged engine: one producer warp, consumer warps, a ring of stages.  A stage
+// holds a tile plus the granule overhang of up to W segments (at most 15 bytes
+// before and after each, rounded) so that every segment lands whole.
+constexpr int kStagedStages = A2AV_STAGED_STAGES;
+constexpr int kStagedStageBytes = A2AV_STAGED_STAGE_BYTES;
+constexpr int kStagedConsumerWarps = A2AV_STAGED_CONSUMER_WARPS;
+constexpr int kStagedThreads = 32 * (1 + kStagedConsumerWarps);
+constexpr int kStagedCtasPerSm = A2AV_STAGED_CTAS_PER_SM;
+constexpr int kStagedPad = 32 * kMaxW + 128;
+constexpr int kStagedAlloc = kStagedStageBytes + kStagedPad;
+static_assert(kStagedPad % 128 == 0 && kStagedStageBytes % 128 == 0, "128-byte aligned stages");
 
 struct Params {
   const unsigned char* in[kMaxW];
@@ -110,10 +156,10 @@ struct Params {
   int W;
 };
 
-// Per-CTA plan in shared memory.  Offsets are in rows.
+// Per-CTA plan in shared memory.  Once build_plan returns, offsets are BYTES.
 struct Plan {
-  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = sum_{q<r} S[q][p]; [p][W] = rows p receives
-  long long in_off[kMaxW][kMaxW];       // [r][p] = sum_{q<p} S[r][q]
+  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = rb * sum_{q<r} S[q][p]; [p][W] = bytes p receives
+  long long in_off[kMaxW][kMaxW];       // [r][p] = rb * sum_{q<p} S[r][q]
   long long tile_first[kMaxW + 1];      // first tile of peer p; [W] = number of tiles
   long long tile;                       // tile size in bytes
 };
@@ -137,7 +183,8 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
-  const long long limit = kMaxBytes / ((long long)W * P.rb);
+  const long long rb = P.rb;
+  const long long limit = kMaxBytes / ((long long)W * rb);
 
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {
@@ -178,9 +225,10 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   // Tiles: peer p's received stream (out_off[p][W] * rb bytes) is cut into
   // ceil(bytes / tile) tiles; tile_first is their exclusive prefix.
   if (warp == 0) {
-    const long long bytes = lane < W ? pl.out_off[lane][W] * P.rb : 0;
+    const long long bytes = lane < W ? pl.out_off[lane][W] * rb : 0;
     const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
-    const long long per_cta = (total + gridDim.x - 1) / gridDim.x;
+    const long long per_cta =
+        (total + kTilesPerCta * gridDim.x - 1) / (kTilesPerCta * gridDim.x);
     long long tile = (per_cta + kTileGranule - 1) / kTileGranule * kTileGranule;
     tile = tile < kTileGranule ? kTileGranule : (tile > max_tile ? max_tile : tile);
     const long long n = (bytes + tile - 1) / tile;
@@ -201,22 +249,56 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
       so[W + r] = pl.out_off[p][r];
     }
   }
+  __syncthreads();
+  // From here on the tables hold bytes.
+  for (int e = tid; e < W * (W + 1); e += nt) pl.out_off[e / (W + 1)][e % (W + 1)] *= rb;
+  for (int e = tid; e < W * W; e += nt) pl.in_off[e / W][e % W] *= rb;
+  __syncthreads();
   return true;
 }
 
-// Tile t -> peer p and the byte range [lo, hi) of out[p] it covers.
-__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long rb,
-                                         long long* lo, long long* hi) {
+// Tile t -> peer p and the byte range [lo, hi) of out[p] it covers (all
+// threads of the caller compute the same).
+__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long* lo,
+                                         long long* hi) {
   int p = 0;
   while (p + 1 < W && pl.tile_first[p + 1] <= t) ++p;
-  const long long bytes = pl.out_off[p][W] * rb;
   *lo = (t - pl.tile_first[p]) * pl.tile;
   const long long end = *lo + pl.tile;
-  *hi = end < bytes ? end : bytes;
+  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
   return p;
 }
 
-// ---------------------------------------------------------------- vector --
+// The same for a whole warp at once: the largest p with tile_first[p] <= t
+// (peers without tiles share their successor's tile_first, so the largest
+// such p is the one that owns tile t).
+__device__ __forceinline__ int tile_peer_warp(const Plan& pl, int W, long long t, int lane,
+                                              long long* lo, long long* hi) {
+  const unsigned m = __ballot_sync(kFull, lane < W && pl.tile_first[lane] <= t);
+  const int p = 31 - __clz(m);
+  *lo = (t - pl.tile_first[p]) * pl.tile;
+  const long long end = *lo + pl.tile;
+  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
+  return p;
+}
+
+// Lane r's part of the tile [lo, hi) of peer p: the destination offset a, the
+// byte count n (0 when source r contributes nothing) and the source address.
+__device__ __forceinline__ long long lane_segment(const Params& P, const Plan& pl, int W, int p,
+                                                  int r, long long lo, long long hi, long long* a,
+                                                  const unsigned char** src) {
+  *a = 0;
+  *src = nullptr;
+  if (r >= W) return 0;
+  const long long c_lo = pl.out_off[p][r], c_hi = pl.out_off[p][r + 1];
+  const long long x = lo > c_lo ? lo : c_lo, y = hi < c_hi ? hi : c_hi;
+  if (x >= y) return 0;
+  *a = x;
+  *src = P.in[r] + pl.in_off[r][p] + (x - c_lo);
+  return y - x;
+}
+
+// ------------------------------------------------------- memory helpers --
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -229,6 +311,24 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ unsigned char lds8(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+  return (unsigned char)v;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
 // Bytes [s, s + 16) of the 32-byte little-endian concatenation a:b, where
@@ -244,6 +344,96 @@ __device__ __forceinline__ uint4 extract16(const uint4& a, const uint4& b, unsig
   return o;
 }
 
+// ------------------------------------------------------------ mbarriers --
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Bounded wait for phase `parity` of the mbarrier; false after ~1 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
+  const long long start = clock64();
+  for (;;) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - start > kWaitCycles) return false;
+  }
+}
+
+// Every lane of the warp waits (so each one observes the phase, and the data
+// it guards); the warp agrees on the outcome, so a timeout is warp-uniform.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, unsigned parity) {
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(kFull, ok) != 0;
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, unsigned bytes,
+                                          uint32_t bar) {
+  if (A2AV_L2_HINT & 1) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar), "l"(evict_first_policy())
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst_smem),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, unsigned bytes) {
+  if (A2AV_L2_HINT & 2) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                     "l"(dst),
+                 "r"(src_smem), "r"(bytes), "l"(evict_first_policy())
+                 : "memory");
+  } else {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(src_smem), "r"(bytes)
+                 : "memory");
+  }
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- vector --
 // nv 16-byte vectors, source and destination both 16-byte aligned.
 template <int NT, int U>
 __device__ __forceinline__ void copy_aligned(uint4* dst, const uint4* src, long long nv, int tid) {
@@ -334,151 +524,234 @@ __device__ __forceinline__ void copy_span(unsigned char* d, const unsigned char*
 }
 
 template <int NT, int U, int US>
-__global__ void __launch_bounds__(NT, kVecCtasPerSm) a2av_vector_kernel(const __grid_constant__ Params P,
-                                                         long long max_tile) {
+__global__ void __launch_bounds__(NT, kVecCtasPerSm)
+    a2av_vector_kernel(const __grid_constant__ Params P, long long max_tile) {
   __shared__ Plan pl;
   if (!build_plan(P, pl, max_tile)) return;
   const int W = P.W, tid = threadIdx.x;
-  const long long rb = P.rb, ntiles = pl.tile_first[W];
+  const long long ntiles = pl.tile_first[W];
   for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
     long long lo, hi;
-    const int p = tile_peer(pl, W, t, rb, &lo, &hi);
+    const int p = tile_peer(pl, W, t, &lo, &hi);
     unsigned char* out = P.out[p];
     for (int r = 0; r < W; ++r) {
-      const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
+      const long long c_lo = pl.out_off[p][r], c_hi = pl.out_off[p][r + 1];
       const long long a = lo > c_lo ? lo : c_lo, b = hi < c_hi ? hi : c_hi;
       if (a >= b) continue;
-      const unsigned char* src = P.in[r] + pl.in_off[r][p] * rb + (a - c_lo);
+      const unsigned char* src = P.in[r] + pl.in_off[r][p] + (a - c_lo);
       copy_span<NT, U, US>(out + a, src, b - a, tid);
     }
   }
 }
 
 // ------------------------------------------------------------------ bulk --
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-// Bounded wait for phase `parity` of the mbarrier; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
-  const long long start = clock64();
-  for (;;) {
-    unsigned done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (clock64() - start > kWaitCycles) return false;
-  }
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, unsigned bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst_smem),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, unsigned bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(src_smem), "r"(bytes)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Issue the loads of tile t into the stage at `stage`; returns its byte count.
-__device__ __forceinline__ unsigned bulk_issue_tile(const Params& P, const Plan& pl, long long t,
-                                                    uint32_t stage, uint32_t bar) {
-  const int W = P.W;
-  const long long rb = P.rb;
-  long long lo, hi;
-  const int p = tile_peer(pl, W, t, rb, &lo, &hi);
-  mbar_expect_tx(bar, (unsigned)(hi - lo));
-  for (int r = 0; r < W; ++r) {
-    const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
-    const long long a = lo > c_lo ? lo : c_lo, b = hi < c_hi ? hi : c_hi;
-    if (a >= b) continue;
-    bulk_load(stage + (uint32_t)(a - lo), P.in[r] + pl.in_off[r][p] * rb + (a - c_lo),
-              (unsigned)(b - a), bar);
-  }
-  return (unsigned)(hi - lo);
-}
-
+// Every tile's source segments, destination and size are 16-byte aligned.
+// Warp 0 does all the work: each tile is loaded by the lanes of the sources
+// it overlaps (lane r, source r) into one stage, and stored by lane 0 in one
+// piece, which tracks its own bulk stores.
 template <int NS, int LEAD>
-__global__ void __launch_bounds__(kBulkThreads) a2av_bulk_kernel(const __grid_constant__ Params P,
-                                                                 int stage_bytes) {
+__global__ void __launch_bounds__(kBulkThreads)
+    a2av_bulk_kernel(const __grid_constant__ Params P, int stage_bytes) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 tiles ahead of stores");
   __shared__ Plan pl;
   __shared__ alignas(8) unsigned long long bars[NS];
+  __shared__ unsigned char* stage_dst[NS];
+  __shared__ unsigned stage_len[NS];
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, stage_bytes)) return;
-  if (threadIdx.x != 0) return;
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
 
   const int W = P.W;
-  const long long rb = P.rb, ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
+  const long long ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
   const long long nk = ntiles > b0 ? (ntiles - b0 + G - 1) / G : 0;
   if (nk == 0) return;
   const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
-  for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
 
   long long issued = 0;  // tiles whose loads are issued
   long long stored = 0;  // tiles whose stores are issued
   bool ok = true;
-  for (long long k = 0; k < nk + LEAD && ok; ++k) {
+  for (long long k = 0; k < nk + LEAD; ++k) {
     if (k < nk) {
       const int s = (int)(k % NS);
       // The store that last read stage s was issued NS - LEAD - 1 stores ago.
-      if (k >= NS) bulk_wait_read<NS - LEAD - 1>();
-      bulk_issue_tile(P, pl, b0 + k * G, stage0 + (uint32_t)s * stage_bytes, bar0 + 8 * s);
+      if (k >= NS && lane == 0) bulk_wait_read<NS - LEAD - 1>();
+      __syncwarp();
+      long long lo, hi, a;
+      const unsigned char* src;
+      const int p = tile_peer_warp(pl, W, b0 + k * G, lane, &lo, &hi);
+      const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
+      const uint32_t bar = bar0 + 8 * s, stage = stage0 + (uint32_t)s * stage_bytes;
+      if (lane == 0) {
+        stage_dst[s] = P.out[p] + lo;
+        stage_len[s] = (unsigned)(hi - lo);
+        mbar_expect_tx(bar, (unsigned)(hi - lo));
+      }
+      __syncwarp();
+      if (n > 0) bulk_load(stage + (uint32_t)(a - lo), src, (unsigned)n, bar);
       issued = k + 1;
     }
     const long long j = k - LEAD;
     if (j >= 0 && j < nk) {
       const int s = (int)(j % NS);
-      if (!mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1))) {
-        ok = false;
-        break;
+      const uint32_t stage = stage0 + (uint32_t)s * stage_bytes;
+      if (lane == 0) {
+        ok = mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1));
+        if (ok) bulk_store(stage_dst[s], stage, stage_len[s]);
       }
-      long long lo, hi;
-      const int p = tile_peer(pl, W, b0 + j * G, rb, &lo, &hi);
-      bulk_store(P.out[p] + lo, stage0 + (uint32_t)s * stage_bytes, (unsigned)(hi - lo));
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
       stored = j + 1;
     }
   }
-  if (!ok) {
-    // A load never completed: report it, give the loads still in flight a
-    // bounded chance to land, then leave.
-    record_error(P.status, A2AV_ERR_TIMEOUT);
-    for (long long j = stored; j < issued; ++j)
-      mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
+  if (lane == 0) {
+    if (!ok) {
+      // A load never completed: report it, give the loads still in flight a
+      // bounded chance to land, then leave.
+      record_error(P.status, A2AV_ERR_TIMEOUT);
+      for (long long j = stored; j < issued; ++j)
+        mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
+    }
+    bulk_wait_all();
   }
-  bulk_wait_all();
+}
+
+// ---------------------------------------------------------------- staged --
+// Where each source segment of a staged tile sits: written by the producer
+// warp before it arms the stage's full barrier, read by the consumers after
+// they see that barrier complete.
+struct StageDesc {
+  unsigned char* dst;   // out[p] + lo
+  int count;            // segments in the tile
+  int seg_dst[kMaxW];   // first byte of the segment, relative to lo
+  int seg_len[kMaxW];   // bytes
+  int seg_src[kMaxW];   // stage offset of the segment's first byte
+};
+
+// n bytes from stage address m to global d, any alignment of either, by the
+// NTC consumer threads.
+template <int NTC>
+__device__ __forceinline__ void copy_span_smem(unsigned char* d, uint32_t m, int n, int ct) {
+  int head = (16 - (int)((uintptr_t)d & 15)) & 15;
+  if (head > n) head = n;
+  if (ct < head) d[ct] = lds8(m + ct);
+  d += head;
+  m += head;
+  n -= head;
+  const int nv = n >> 4, tail = n & 15;
+  if (ct < tail) d[nv * 16 + ct] = lds8(m + nv * 16 + ct);
+  if (nv == 0) return;
+  uint4* dv = reinterpret_cast<uint4*>(d);
+  const unsigned shift = m & 15;
+  if (shift == 0) {
+#pragma unroll 4
+    for (int i = ct; i < nv; i += NTC) st_stream(dv + i, lds128(m + 16 * i));
+    return;
+  }
+  const uint32_t mb = m - shift;
+  const unsigned r8 = (shift & 3) * 8;
+#define A2AV_SHIFTED_FROM_SMEM(Q)                                                     \
+  _Pragma("unroll 4") for (int i = ct; i < nv; i += NTC)                              \
+      st_stream(dv + i, extract16<Q>(lds128(mb + 16 * i), lds128(mb + 16 * i + 16), r8))
+  switch (shift >> 2) {
+    case 0: A2AV_SHIFTED_FROM_SMEM(0); break;
+    case 1: A2AV_SHIFTED_FROM_SMEM(1); break;
+    case 2: A2AV_SHIFTED_FROM_SMEM(2); break;
+    default: A2AV_SHIFTED_FROM_SMEM(3); break;
+  }
+#undef A2AV_SHIFTED_FROM_SMEM
+}
+
+template <int NS, int NC>
+__global__ void __launch_bounds__(32 * (NC + 1))
+    a2av_staged_kernel(const __grid_constant__ Params P, int stage_bytes) {
+  __shared__ Plan pl;
+  __shared__ StageDesc desc[NS];
+  __shared__ alignas(8) unsigned long long full[NS];
+  __shared__ alignas(8) unsigned long long empty[NS];
+  extern __shared__ __align__(128) unsigned char stages[];
+  if (!build_plan(P, pl, stage_bytes)) return;
+
+  const int W = P.W, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
+  const long long nk = ntiles > b0 ? (ntiles - b0 + G - 1) / G : 0;
+  if (nk == 0) return;
+  const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), stage0 = smem_u32(stages);
+  const uint32_t alloc = (uint32_t)stage_bytes + kStagedPad;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, NC);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // Producer: one tile per iteration, lane r loading source r's granules.
+    for (long long k = 0; k < nk; ++k) {
+      const int s = (int)(k % NS);
+      if (k >= NS && !mbar_wait_warp(empty0 + 8 * s, (unsigned)((k / NS - 1) & 1))) {
+        if (lane == 0) record_error(P.status, A2AV_ERR_TIMEOUT);
+        break;
+      }
+      long long lo, hi, a;
+      const unsigned char* src;
+      const int p = tile_peer_warp(pl, W, b0 + k * G, lane, &lo, &hi);
+      const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
+      const uintptr_t g_lo = (uintptr_t)src & ~(uintptr_t)15;
+      const unsigned gb =
+          n > 0 ? (unsigned)((((uintptr_t)src + (uintptr_t)n + 15) & ~(uintptr_t)15) - g_lo) : 0;
+      unsigned inc = gb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += y;
+      }
+      const unsigned off = inc - gb, total = __shfl_sync(kFull, inc, 31);
+      const unsigned has = __ballot_sync(kFull, n > 0);
+      StageDesc& d = desc[s];
+      if (n > 0) {
+        const int idx = __popc(has & ((1u << lane) - 1u));
+        d.seg_dst[idx] = (int)(a - lo);
+        d.seg_len[idx] = (int)n;
+        d.seg_src[idx] = (int)(off + (unsigned)((uintptr_t)src - g_lo));
+      }
+      if (lane == 0) {
+        d.count = __popc(has);
+        d.dst = P.out[p] + lo;
+      }
+      __syncwarp();
+      const uint32_t bar = full0 + 8 * s;
+      if (lane == 0) mbar_expect_tx(bar, total);
+      __syncwarp();
+      if (n > 0) bulk_load(stage0 + (uint32_t)s * alloc + off, (const void*)g_lo, gb, bar);
+    }
+    return;
+  }
+
+  // Consumers: rebuild each tile from its stage with destination-aligned stores.
+  const int ct = threadIdx.x - 32;
+  for (long long k = 0; k < nk; ++k) {
+    const int s = (int)(k % NS);
+    if (!mbar_wait_warp(full0 + 8 * s, (unsigned)((k / NS) & 1))) {
+      if (lane == 0) record_error(P.status, A2AV_ERR_TIMEOUT);
+      break;
+    }
+    const StageDesc& d = desc[s];
+    const int count = d.count;
+    unsigned char* dst = d.dst;
+    const uint32_t stage = stage0 + (uint32_t)s * alloc;
+    for (int i = 0; i < count; ++i)
+      copy_span_smem<32 * NC>(dst + d.seg_dst[i], stage + (uint32_t)d.seg_src[i], d.seg_len[i], ct);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+  }
 }
 
 }  // namespace
@@ -499,6 +772,7 @@ namespace {
 
 using BulkKernel = void (*)(Params, int);
 const BulkKernel kBulk = a2av_bulk_kernel<kBulkStages, kBulkLead>;
+const BulkKernel kStaged = a2av_staged_kernel<kStagedStages, kStagedConsumerWarps>;
 using VecKernel = void (*)(Params, long long);
 const VecKernel kVec = a2av_vector_kernel<kVecThreads, kVecUnroll, kVecShiftUnroll>;
 
@@ -508,11 +782,69 @@ int env_int(const char* name, int fallback) {
   return std::atoi(v);
 }
 
+// Shared-memory opt-in of the staging engines (once per device).
+int configure_kernels() {
+  if (cudaFuncSetAttribute(kBulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kBulkStages * kBulkStageBytes) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  if (cudaFuncSetAttribute(kStaged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStagedStages * kStagedAlloc) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  return A2AV_OK;
+}
+
+// Fill the kernel parameters; returns whether every row and buffer is
+// 16-byte aligned (the bulk engine's precondition).
+bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in_splits_dev,
+                 void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
+                 long long in_cap, long long out_cap, int* status) {
+  std::memset(P, 0, sizeof(*P));
+  bool aligned = (row_bytes % 16) == 0;
+  for (int r = 0; r < W; ++r) {
+    P->in[r] = static_cast<const unsigned char*>(in_ptrs[r]);
+    P->out[r] = static_cast<unsigned char*>(out_ptrs[r]);
+    aligned = aligned && ((uintptr_t)P->in[r] & 15) == 0 && ((uintptr_t)P->out[r] & 15) == 0;
+  }
+  P->splits = reinterpret_cast<const long long*>(in_splits_dev);
+  P->out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
+  P->status = status;
+  P->rb = row_bytes;
+  P->in_cap = in_cap;
+  P->out_cap = out_cap;
+  P->W = W;
+  return aligned;
+}
+
+// Engine actually used for a request: BULK needs full alignment (else STAGED);
+// AUTO is BULK when aligned, STAGED otherwise.
+int resolve_path(int requested, bool aligned) {
+  if (requested == A2AV_PATH_VECTOR || requested == A2AV_PATH_STAGED) return requested;
+  return aligned ? A2AV_PATH_BULK : A2AV_PATH_STAGED;
+}
+
+int launch(const Params& P, int path, int ctas_per_sm, int sms, cudaStream_t s, int* grid,
+           int* block) {
+  if (path == A2AV_PATH_BULK) {
+    *grid = sms * (ctas_per_sm ? ctas_per_sm : kBulkCtasPerSm);
+    *block = kBulkThreads;
+    kBulk<<<*grid, *block, kBulkStages * kBulkStageBytes, s>>>(P, kBulkStageBytes);
+  } else if (path == A2AV_PATH_STAGED) {
+    *grid = sms * (ctas_per_sm ? ctas_per_sm : kStagedCtasPerSm);
+    *block = kStagedThreads;
+    kStaged<<<*grid, *block, kStagedStages * kStagedAlloc, s>>>(P, kStagedStageBytes);
+  } else {
+    *grid = sms * (ctas_per_sm ? ctas_per_sm : kVecCtasPerSm);
+    *block = kVecThreads;
+    kVec<<<*grid, *block, 0, s>>>(P, kVecMaxTile);
+  }
+  return cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
-int a2av_version(void) { return 10000; }
+int a2av_version(void) { return 10100; }
 
 const char* a2av_error_string(int code) {
   switch (code) {
@@ -536,10 +868,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return A2AV_ERR_CUDA;
-  const int smem = kBulkStages * kBulkStageBytes;
-  if (cudaFuncSetAttribute(kBulk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-      cudaSuccess)
-    return A2AV_ERR_CUDA;
+  if (configure_kernels() != A2AV_OK) return A2AV_ERR_CUDA;
   int* status = nullptr;
   if (cudaMalloc(&status, 256) != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaMemset(status, 0, 256) != cudaSuccess) {
@@ -558,7 +887,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   h->sms = sms;
   h->d_status = status;
   h->path = env_int("A2AV_PATH", A2AV_PATH_AUTO);
-  if (h->path < A2AV_PATH_AUTO || h->path > A2AV_PATH_BULK) h->path = A2AV_PATH_AUTO;
+  if (h->path < A2AV_PATH_AUTO || h->path > A2AV_PATH_STAGED) h->path = A2AV_PATH_AUTO;
   h->ctas_per_sm = env_int("A2AV_CTAS_PER_SM", 0);
   if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
   h->last_path = h->last_grid = h->last_block = 0;
@@ -567,7 +896,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
 }
 
 int a2av_set_path(a2av_handle* h, int path) {
-  if (h == nullptr || path < A2AV_PATH_AUTO || path > A2AV_PATH_BULK) return A2AV_ERR_INVALID_ARG;
+  if (h == nullptr || path < A2AV_PATH_AUTO || path > A2AV_PATH_STAGED) return A2AV_ERR_INVALID_ARG;
   h->path = path;
   return A2AV_OK;
 }
@@ -599,36 +928,14 @@ int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_split
   if (dev != h->device) return A2AV_ERR_INVALID_ARG;
 
   Params P;
-  std::memset(&P, 0, sizeof(P));
-  bool aligned = (row_bytes % 16) == 0;
-  for (int r = 0; r < h->W; ++r) {
-    P.in[r] = static_cast<const unsigned char*>(in_ptrs[r]);
-    P.out[r] = static_cast<unsigned char*>(out_ptrs[r]);
-    aligned = aligned && ((uintptr_t)P.in[r] & 15) == 0 && ((uintptr_t)P.out[r] & 15) == 0;
-  }
-  P.splits = reinterpret_cast<const long long*>(in_splits_dev);
-  P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
-  P.status = h->d_status;
-  P.rb = row_bytes;
-  P.in_cap = h->in_cap;
-  P.out_cap = h->out_cap;
-  P.W = h->W;
-
-  const int path = (h->path == A2AV_PATH_VECTOR || !aligned) ? A2AV_PATH_VECTOR : A2AV_PATH_BULK;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err;
-  int grid, block;
-  if (path == A2AV_PATH_BULK) {
-    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kBulkCtasPerSm);
-    block = kBulkThreads;
-    kBulk<<<grid, block, kBulkStages * kBulkStageBytes, s>>>(P, kBulkStageBytes);
-  } else {
-    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kVecCtasPerSm);
-    block = kVecThreads;
-    kVec<<<grid, block, 0, s>>>(P, kVecMaxTile);
-  }
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return A2AV_ERR_CUDA;
+  const bool aligned = fill_params(&P, h->W, in_ptrs, in_splits_dev, out_ptrs,
+                                   out_splits_offsets_dev, row_bytes, h->in_cap, h->out_cap,
+                                   h->d_status);
+  const int path = resolve_path(h->path, aligned);
+  int grid = 0, block = 0;
+  const int rc = launch(P, path, h->ctas_per_sm, h->sms, static_cast<cudaStream_t>(stream),
+                        &grid, &block);
+  if (rc != A2AV_OK) return rc;
   h->last_path = path;
   h->last_grid = grid;
   h->last_block = block;
@@ -677,9 +984,7 @@ int noalloc_setup(int dev, int** status, int* sms) {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return A2AV_ERR_CUDA;
-    if (cudaFuncSetAttribute(kBulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kBulkStages * kBulkStageBytes) != cudaSuccess)
-      return A2AV_ERR_CUDA;
+    if (configure_kernels() != A2AV_OK) return A2AV_ERR_CUDA;
     g_noalloc_sms[dev] = n;
     g_noalloc_status[dev] = static_cast<int*>(addr);
   }
@@ -708,35 +1013,19 @@ extern "C" int a2av_run_noalloc(int world_size, int64_t in_capacity_rows,
   if (dev < 0 || dev >= kNoAllocMaxDevices) return A2AV_ERR_UNSUPPORTED;
   int* status = nullptr;
   int sms = 0;
-  const int rc = noalloc_setup(dev, &status, &sms);
+  int rc = noalloc_setup(dev, &status, &sms);
   if (rc != A2AV_OK) return rc;
 
   Params P;
-  std::memset(&P, 0, sizeof(P));
-  bool aligned = (row_bytes % 16) == 0;
-  for (int r = 0; r < world_size; ++r) {
-    P.in[r] = static_cast<const unsigned char*>(in_ptrs[r]);
-    P.out[r] = static_cast<unsigned char*>(out_ptrs[r]);
-    aligned = aligned && ((uintptr_t)P.in[r] & 15) == 0 && ((uintptr_t)P.out[r] & 15) == 0;
-  }
-  P.splits = reinterpret_cast<const long long*>(in_splits_dev);
-  P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
-  P.status = status;
-  P.rb = row_bytes;
-  P.in_cap = in_capacity_rows;
-  P.out_cap = out_capacity_rows;
-  P.W = world_size;
-
+  const bool aligned = fill_params(&P, world_size, in_ptrs, in_splits_dev, out_ptrs,
+                                   out_splits_offsets_dev, row_bytes, in_capacity_rows,
+                                   out_capacity_rows, status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The kernels only ever set the status word, so it must start at zero.
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
-  if (aligned) {
-    kBulk<<<sms * kBulkCtasPerSm, kBulkThreads, kBulkStages * kBulkStageBytes, s>>>(
-        P, kBulkStageBytes);
-  } else {
-    kVec<<<sms * kVecCtasPerSm, kVecThreads, 0, s>>>(P, kVecMaxTile);
-  }
-  if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  int grid = 0, block = 0;
+  rc = launch(P, resolve_path(A2AV_PATH_AUTO, aligned), 0, sms, s, &grid, &block);
+  if (rc != A2AV_OK) return rc;
   if (device_status != nullptr) {
     int value = 0;
     if (cudaMemcpyAsync(&value, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
