@@ -274,7 +274,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     dist_init("nccl")
     a2av.build()
-    path_id = {"auto": a2av.PATH_AUTO, "vector": a2av.PATH_VECTOR, "bulk": a2av.PATH_BULK}[args.path]
+    path_id = {"auto": a2av.PATH_AUTO, "vector": a2av.PATH_VECTOR, "bulk": a2av.PATH_BULK,
+               "staged": a2av.PATH_STAGED}[args.path]
 
     t0 = time.time()
     w, h_in = load_workload(args, torch)
@@ -298,6 +299,20 @@ def run_ours(args):
 
     def step(ins=d_in, outs=d_out, splits=d_S):
         eng.run(ins, splits, outs, d_so, rb, stream=stream)
+
+    if args.op == "combine":
+        # The reverse exchange: its inputs are the forward exchange's outputs,
+        # made once on the device (untimed); a step sends every row home.
+        step()
+        torch.cuda.synchronize()
+        if eng.status() != a2av.OK:
+            raise SystemExit("device reported an error in the forward exchange")
+        c_in, c_dso = d_out, d_so.clone()
+        c_out = [torch.empty_like(t) for t in d_in]
+        c_so = torch.empty_like(d_so)
+
+        def step(ins=c_in, outs=c_out, splits=c_dso):  # noqa: F811
+            eng.combine(ins, splits, outs, c_so, rb, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -337,7 +352,8 @@ def run_ours(args):
     # ---- roofline of the (only) kernel -----------------------------------
     algo = algorithmic_bytes(S, rb)
     peak, peak_kind = hbm_peak()
-    kname = "a2av_bulk_kernel" if launch["path"] == a2av.PATH_BULK else "a2av_vector_kernel"
+    kname = {a2av.PATH_BULK: "a2av_bulk_kernel", a2av.PATH_STAGED: "a2av_staged_kernel",
+             a2av.PATH_VECTOR: "a2av_vector_kernel"}[launch["path"]]
     achieved = algo / avg_launch_s / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
@@ -364,7 +380,7 @@ def run_ours(args):
 
     # ---- payload sweep (cold L2 between launches) --------------------------
     sweep = []
-    if args.workload == "cfg2" and not args.no_sweep:
+    if args.workload == "cfg2" and args.op == "dispatch" and not args.no_sweep:
         for Pk in wl.CFG2_SWEEP_BYTES:
             if Pk > P:
                 break
@@ -399,18 +415,25 @@ def run_ours(args):
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
     if not args.no_e2e:
-        h_out = [torch.empty(n, dtype=torch.uint8, pin_memory=True) for n in recv]
-        h_S = torch.from_numpy(S).pin_memory()
+        if args.op == "combine":
+            # host copies of the combine's own inputs (the forward outputs)
+            e_src = [t.cpu().pin_memory() for t in c_in]
+            e_dev, e_sp, e_spd = c_in, c_dso.cpu().pin_memory(), c_dso
+            e_outs, e_so = c_out, c_so
+        else:
+            e_src, e_dev, e_sp, e_spd = h_in, d_in, torch.from_numpy(S).pin_memory(), d_S
+            e_outs, e_so = d_out, d_so
+        h_out = [torch.empty(t.numel(), dtype=torch.uint8, pin_memory=True) for t in e_outs]
         h_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, pin_memory=True)
 
         def e2e_step():
-            for h, d in zip(h_in, d_in):
+            for h, d in zip(e_src, e_dev):
                 d.copy_(h, non_blocking=True)
-            d_S.copy_(h_S, non_blocking=True)
+            e_spd.copy_(e_sp, non_blocking=True)
             step()
-            for h, d in zip(h_out, d_out):
+            for h, d in zip(h_out, e_outs):
                 h.copy_(d, non_blocking=True)
-            h_so.copy_(d_so, non_blocking=True)
+            h_so.copy_(e_so, non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize()
@@ -426,15 +449,35 @@ def run_ours(args):
         barrier()
         e_s = reduce_max(a.elapsed_time(b) / 1e3, dev)
         e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, e_s), 2), "unit": UNIT,
-               "h2d_bytes_per_step": sum(in_bytes) + S.size * 8,
-               "d2h_bytes_per_step": sum(recv) + 2 * Wn * Wn * 8, "steps": Ke}
+               "h2d_bytes_per_step": sum(t.numel() for t in e_src) + e_sp.numel() * 8,
+               "d2h_bytes_per_step": sum(t.numel() for t in h_out) + 2 * Wn * Wn * 8,
+               "steps": Ke}
         if eng.status() != a2av.OK:
             raise SystemExit("device reported an error during the e2e run")
 
     # ---- CPU oracle: baseline timing and a parity check of this run -------
     cpu = None
     parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "combine":
+        import oracle
+        inputs = [t.numpy() for t in h_in]
+        mid, dso = oracle.default().exchange(inputs, S, rb)
+        back = [np.empty_like(b) for b in inputs]
+        cso = np.empty((Wn, 2, Wn), dtype=np.int64)
+        t0 = time.perf_counter()
+        assert oracle.default().combine(mid, dso, back, cso, rb) == 0
+        spent = time.perf_counter() - t0
+        cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "the whole reverse exchange of the same workload", "seconds": round(spent, 3)}
+        # parity: the round trip is the identity, on the device and on the oracle
+        ok = all(torch.equal(c_out[r], d_in[r]) for r in range(Wn))
+        ok = ok and np.array_equal(c_so.cpu().numpy(), cso)
+        ok = ok and all(np.array_equal(back[r], inputs[r]) for r in range(Wn))
+        parity = {"bit_exact": bool(ok), "check": "combine(dispatch(x)) == x on GPU and oracle; "
+                                                  "offsets equal the oracle's"}
+        if not ok:
+            raise SystemExit("the GPU's reverse exchange does not return the inputs")
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
         inputs = [t.numpy() for t in h_in]
         mismatched = []
 
@@ -461,7 +504,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
         "config": {"workload": describe(args.workload, P, args.seed), "name": args.workload,
-                   "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
+                   "op": args.op, "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
                    "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
                           "the launch's CUDA-event duration") if cold else
@@ -533,9 +576,11 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="cfg2")
+    ap.add_argument("--op", choices=["dispatch", "combine"], default="dispatch",
+                    help="dispatch = a2av_run; combine = a2av_combine on its outputs")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--per-rank-bytes", type=int, default=1 << 32, help="cfg2 payload per rank")
-    ap.add_argument("--path", choices=["auto", "vector", "bulk"], default="auto")
+    ap.add_argument("--path", choices=["auto", "vector", "bulk", "staged"], default="auto")
     ap.add_argument("--ctas-per-sm", type=int, default=0)
     ap.add_argument("--sweep-reps", type=int, default=20)
     ap.add_argument("--e2e-steps", type=int, default=5)

@@ -126,6 +126,33 @@ int a2av_run(a2av_handle *h, const void *const *in_ptrs, const int64_t *in_split
              void *stream);
 
 /*
+ * a2av_combine -- the reverse exchange: every peer sends each chunk it
+ * received back to the rank it came from (the return path of an MoE token
+ * dispatch).  The pages define only the forward exchange; this is that same
+ * exchange applied to the transposed split matrix S', S'[p][r] = S[r][p],
+ * which a dispatch's out_splits_offsets already holds (its row 0 for peer p).
+ * One kernel launch on `stream`, like a2av_run.
+ *
+ *  in_ptrs            HOST array of W device pointers: peer p's buffer laid out
+ *                     like the dispatch's output (chunks in source-rank order).
+ *  dispatch_splits_offsets_dev  DEVICE int64 [W][2][W]: the out_splits_offsets
+ *                     a2av_run wrote for the dispatch (only rows [p][0][*] are read).
+ *  out_ptrs           HOST array of W device pointers: rank r's buffer receives,
+ *                     in peer order, the rows it sent -- the dispatch input's
+ *                     layout, so combine(dispatch(x)) == x byte for byte.
+ *  out_splits_offsets_dev  DEVICE int64 [W][2][W]: written with
+ *                     [r][0][p] = S[r][p] and [r][1][p] = sum_{q<p} S[r][q].
+ *  row_bytes, stream  as in a2av_run.
+ *
+ * Capacities, validity checks, errors and memory rules are a2av_run's, with
+ * the combine's own inputs and outputs; dispatch_splits_offsets_dev counts as
+ * an input and must not overlap any output.
+ */
+int a2av_combine(a2av_handle *h, const void *const *in_ptrs,
+                 const int64_t *dispatch_splits_offsets_dev, void *const *out_ptrs,
+                 int64_t *out_splits_offsets_dev, int64_t row_bytes, void *stream);
+
+/*
  * a2av_status -- read and clear the handle's device status word: the first
  * device-detected error (A2AV_ERR_BAD_SPLITS or A2AV_ERR_TIMEOUT) of the runs
  * since the last call, or A2AV_OK.  Enqueues a 4-byte device-to-host copy and

@@ -53,8 +53,10 @@ def _bind(lib):
                                       ctypes.c_int64, vpp, vpp]
     lib.a2av_oracle_row_source.argtypes = [ctypes.c_int, _i64p, ctypes.c_int, ctypes.c_int64,
                                            ctypes.POINTER(ctypes.c_int), _i64p]
+    lib.a2av_oracle_combine.argtypes = [ctypes.c_int, vpp, _i64p, vpp, _i64p, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64]
     for f in (lib.a2av_oracle, lib.a2av_oracle_dest, lib.a2av_oracle_check,
-              lib.a2av_oracle_row_source):
+              lib.a2av_oracle_row_source, lib.a2av_oracle_combine):
         f.restype = ctypes.c_int
     return lib
 
@@ -135,6 +137,18 @@ class Oracle:
                                              ctypes.byref(r), ctypes.byref(i))
         return None if rc != OK else (r.value, i.value)
 
+    def combine(self, inputs, dispatch_so, outputs, out_splits_offsets, row_bytes,
+                in_capacity_rows=0, out_capacity_rows=0) -> int:
+        """The reverse exchange, splits read from a dispatch's [W][2][W] out_splits_offsets."""
+        W = len(inputs)
+        dso = np.ascontiguousarray(dispatch_so, dtype=np.int64)
+        assert dso.size == 2 * W * W and out_splits_offsets.size == 2 * W * W
+        assert out_splits_offsets.dtype == np.int64 and out_splits_offsets.flags.c_contiguous
+        return self.lib.a2av_oracle_combine(W, _ptrs(inputs), dso.ctypes.data_as(_i64p),
+                                            _ptrs(outputs), out_splits_offsets.ctypes.data_as(_i64p),
+                                            int(row_bytes), int(in_capacity_rows),
+                                            int(out_capacity_rows))
+
     # ---- convenience: allocate outputs of exactly the received size -------
     def exchange(self, inputs, splits, row_bytes):
         """Return (outputs, out_splits_offsets[W][2][W]) for valid splits."""
@@ -143,6 +157,17 @@ class Oracle:
         outs = [np.empty(int(S[:, p].sum()) * row_bytes, dtype=np.uint8) for p in range(W)]
         so = np.empty((W, 2, W), dtype=np.int64)
         rc = self.run(inputs, S, outs, so, row_bytes)
+        if rc != OK:
+            raise ValueError(f"oracle rejected the splits (status {rc})")
+        return outs, so
+
+    def exchange_back(self, inputs, dispatch_so, row_bytes):
+        """Return (outputs, out_splits_offsets) of the reverse exchange."""
+        W = len(inputs)
+        dso = np.ascontiguousarray(dispatch_so, dtype=np.int64).reshape(W, 2, W)
+        outs = [np.empty(int(dso[:, 0, r].sum()) * row_bytes, dtype=np.uint8) for r in range(W)]
+        so = np.empty((W, 2, W), dtype=np.int64)
+        rc = self.combine(inputs, dso, outs, so, row_bytes)
         if rc != OK:
             raise ValueError(f"oracle rejected the splits (status {rc})")
         return outs, so

@@ -31,6 +31,7 @@
  */
 #include <stdint.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define ORACLE_OK 0
@@ -146,4 +147,22 @@ int a2av_oracle_row_source(int W, const int64_t *in_splits, int p, int64_t k, in
     }
   }
   return ORACLE_INVALID_ARG;
+}
+
+/* The reverse exchange (the return path of a dispatch): peer p sends back to
+ * rank r the S[r][p] rows it received from it.  That is the exchange above
+ * with the transposed split matrix, S'[p][r] = S[r][p], read from the
+ * dispatch's out_splits_offsets (row 0 of peer p's [2][W] block). */
+int a2av_oracle_combine(int W, const uint8_t *const *in, const int64_t *dispatch_so,
+                        uint8_t *const *out, int64_t *out_splits_offsets, int64_t row_bytes,
+                        int64_t in_capacity_rows, int64_t out_capacity_rows) {
+  if (W < 1 || dispatch_so == NULL) return ORACLE_INVALID_ARG;
+  int64_t *St = (int64_t *)malloc(sizeof(int64_t) * (size_t)W * (size_t)W);
+  if (St == NULL) return ORACLE_INVALID_ARG;
+  for (int p = 0; p < W; ++p)
+    for (int r = 0; r < W; ++r) St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + r];
+  const int rc = a2av_oracle(W, in, St, out, out_splits_offsets, row_bytes, in_capacity_rows,
+                             out_capacity_rows);
+  free(St);
+  return rc;
 }

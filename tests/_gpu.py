@@ -80,3 +80,36 @@ def exchange_checked(inputs, S, rb, path=a2av.PATH_AUTO, in_mis=None, out_mis=No
         assert np.array_equal(ins[r].view.cpu().numpy(), inputs[r]), f"input {r} modified"
         assert ins[r].guards_intact(), f"input {r}: canary modified"
     return launch
+
+
+def combine_checked(inputs, dispatch_so, rb, path=a2av.PATH_AUTO, in_mis=None, out_mis=None,
+                    ctas_per_sm=0, expect_path=None):
+    """Run the reverse exchange on the GPU and compare with the oracle's."""
+    W = len(inputs)
+    dso = np.ascontiguousarray(dispatch_so, dtype=np.int64).reshape(W, 2, W)
+    in_mis = in_mis or [0] * W
+    out_mis = out_mis or [0] * W
+    back = [int(dso[:, 0, r].sum()) for r in range(W)]
+    ins = [Guarded(inputs[p].size, in_mis[p], host=inputs[p]) for p in range(W)]
+    outs = [Guarded((back[r] + SLACK_ROWS) * rb, out_mis[r], fill=SENTINEL) for r in range(W)]
+    d_dso = torch.from_numpy(dso).cuda()
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    with a2av.A2av(W, path=path, ctas_per_sm=ctas_per_sm) as eng:
+        eng.combine([g.view for g in ins], d_dso, [g.view for g in outs], so, rb)
+        st = eng.status()
+        launch = eng.last_launch()
+    torch.cuda.synchronize()
+    assert st == a2av.OK, f"device status {st}"
+    if expect_path is not None:
+        assert launch["path"] == expect_path, launch
+    ref, ref_so = oracle.default().exchange_back(inputs, dso, rb)
+    assert np.array_equal(so.cpu().numpy(), ref_so), "combine out_splits_offsets differ"
+    for r in range(W):
+        got = outs[r].view.cpu().numpy()
+        n = back[r] * rb
+        assert np.array_equal(got[:n], ref[r]), f"combine: rank {r} differs from the oracle"
+        assert np.all(got[n:] == SENTINEL), f"combine: rank {r} written past its rows"
+        assert outs[r].guards_intact(), f"combine: rank {r} canary overwritten"
+    for p in range(W):
+        assert np.array_equal(ins[p].view.cpu().numpy(), inputs[p]), f"combine input {p} modified"
+    return [outs[r].view.cpu().numpy()[: back[r] * rb] for r in range(W)]

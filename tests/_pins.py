@@ -284,8 +284,39 @@ def pin_dest_and_row_source(o):
             assert o.row_source(S, p, int(S[:, p].sum())) is None
 
 
+def pin_combine_round_trip(o):
+    """The reverse exchange undoes the exchange: rows come home in their
+    original places, and its offsets are the original splits and their
+    row-wise exclusive scan (numpy cumsum)."""
+    rng = np.random.default_rng(16)
+    for W, rb in ((1, 3), (2, 8), (3, 13), (5, 1), (8, 16)):
+        S = rng.integers(0, 6, size=(W, W)).astype(np.int64)
+        S[rng.random((W, W)) < 0.3] = 0
+        inp = tagged_inputs(S, rb)
+        rc, mid, dso = run_fresh(o, inp, S, rb)
+        assert rc == 0
+        outs = [np.full(b.size, SENTINEL, np.uint8) for b in inp]
+        so = np.full((W, 2, W), -7, np.int64)
+        assert o.combine(mid, dso, outs, so, rb) == 0
+        for r in range(W):
+            _eq(outs[r], inp[r], "combine must return every row to its original place")
+        _eq(so[:, 0, :], S, "combine's splits must be the original splits")
+        excl = np.concatenate([np.zeros((W, 1), np.int64), np.cumsum(S, axis=1)[:, :-1]], axis=1)
+        _eq(so[:, 1, :], excl, "combine's offsets must be the row-wise exclusive scan")
+        # uniform splits: the reverse exchange is the inverse transpose
+        x = rng.integers(0, 256, size=(W, W, 2, rb), dtype=np.uint8)  # [p][r][row][byte]
+        back = [np.full(W * 2 * rb, SENTINEL, np.uint8) for _ in range(W)]
+        uso = np.zeros((W, 2, W), np.int64)
+        uso[:, 0, :] = 2
+        assert o.combine([x[p].reshape(-1).copy() for p in range(W)], uso, back,
+                         np.zeros((W, 2, W), np.int64), rb) == 0
+        for r in range(W):
+            _eq(back[r], x.transpose(1, 0, 2, 3)[r].reshape(-1), "uniform combine = transpose")
+
+
 PINS = [pin_identity_w1, pin_errors, pin_diagonal_and_permutation, pin_uniform_transpose,
-        pin_round_trip, pin_dest_and_row_source, pin_invariants_random, pin_bruteforce_tiny]
+        pin_round_trip, pin_combine_round_trip, pin_dest_and_row_source, pin_invariants_random,
+        pin_bruteforce_tiny]
 
 
 def main(argv):

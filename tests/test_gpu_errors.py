@@ -128,3 +128,16 @@ def test_binding_rejects_bad_tensors():
     with pytest.raises(a2av.A2avError):
         eng.run(x, S, x, so, 0)
     eng.close()
+
+
+def test_combine_with_bad_splits_writes_nothing():
+    rb = 8
+    dso = np.zeros((3, 2, 3), dtype=np.int64)
+    dso[:, 0, :] = S0.T
+    dso[1, 0, 2] = -3
+    ins, outs, so = _setup(S0.T.copy(), rb)
+    eng = a2av.A2av(3)
+    eng.combine(ins, torch.from_numpy(dso).cuda(), outs, so, rb)
+    assert eng.status() == a2av.ERR_BAD_SPLITS
+    eng.close()
+    assert _untouched(outs, so)

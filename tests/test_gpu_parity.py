@@ -180,3 +180,37 @@ def test_many_tiny_segments_per_tile():
         mis = list(range(16)) * 2
         for path in (AUTO, VEC, STAGED):
             exchange_checked(inputs, S, rb, path=path, in_mis=mis, out_mis=mis[::-1])
+
+
+@pytest.mark.parametrize("path", [AUTO, VEC, STAGED])
+def test_combine_returns_every_row_home(path):
+    from tests._gpu import combine_checked
+    import oracle
+    cases = [wl.cfg3(4, tokens=1024), wl.cfg4(3, rows=1 << 16), wl.cfg5(1, batch=1024),
+             wl.random_case(21, 13, 7, 200, "skew"), wl.random_case(22, 32, 1, 50, "sparse")]
+    for w in cases:
+        mid, dso = oracle.default().exchange(w.inputs, w.splits, w.row_bytes)
+        mis = [r % 16 for r in range(w.W)]
+        back = combine_checked(mid, dso, w.row_bytes, path=path, in_mis=mis, out_mis=mis[::-1])
+        for r in range(w.W):
+            assert np.array_equal(back[r], w.inputs[r]), "combine(dispatch(x)) != x"
+
+
+def test_dispatch_then_combine_on_device():
+    # the GPU's own out_splits_offsets drives the GPU's reverse exchange
+    w = wl.cfg3(5, tokens=2048)
+    W, rb = w.W, w.row_bytes
+    ins = [torch.from_numpy(b).cuda() for b in w.inputs]
+    S = torch.from_numpy(w.splits).cuda()
+    mid = [torch.empty(int(w.splits[:, p].sum()) * rb, dtype=torch.uint8, device="cuda")
+           for p in range(W)]
+    back = [torch.full_like(t, 0xEE) for t in ins]
+    dso = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    cso = torch.empty_like(dso)
+    with a2av.A2av(W) as eng:
+        eng.run(ins, S, mid, dso, rb)
+        eng.combine(mid, dso, back, cso, rb)
+        assert eng.status() == a2av.OK
+    for r in range(W):
+        assert torch.equal(back[r], ins[r])
+    assert torch.equal(cso[:, 0, :], S)

@@ -37,6 +37,10 @@ MUTANTS = {
     "limit_drops_W": ("kMaxBytes / ((int64_t)W * row_bytes)", "kMaxBytes / (row_bytes)"),
     "null_input_unchecked": ("if (in != NULL && in[r] == NULL && rows > 0)",
                              "if (in != NULL && in[r] == NULL && rows > kMaxBytes)"),
+    "combine_reads_offsets_row": ("St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + r];",
+                                  "St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + W + r];"),
+    "combine_not_transposed": ("St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + r];",
+                               "St[(int64_t)r * W + p] = dispatch_so[(int64_t)p * 2 * W + r];"),
     "row_source_wrong_chunk": ("*i = in_offset(W, in_splits, q, p) + (k - start);",
                                "*i = in_offset(W, in_splits, p, q) + (k - start);"),
 }

@@ -16,7 +16,7 @@ from ._build import LIBRARY, build
 
 __all__ = [
     "A2av", "A2avError", "load", "build",
-    "a2av_create", "a2av_run", "a2av_status", "a2av_destroy", "a2av_set_path",
+    "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
@@ -49,6 +49,7 @@ def load():
     pp = ctypes.POINTER(ctypes.c_void_p)
     lib.a2av_create.argtypes = [ci, i64, i64, pp]
     lib.a2av_run.argtypes = [vp, pp, vp, pp, vp, i64, vp]
+    lib.a2av_combine.argtypes = [vp, pp, vp, pp, vp, i64, vp]
     lib.a2av_status.argtypes = [vp, vp, ctypes.POINTER(ci)]
     lib.a2av_destroy.argtypes = [vp]
     lib.a2av_set_path.argtypes = [vp, ci]
@@ -59,7 +60,7 @@ def load():
     lib.a2av_error_string.argtypes = [ci]
     lib.a2av_error_string.restype = ctypes.c_char_p
     lib.a2av_version.argtypes = []
-    for f in ("a2av_create", "a2av_run", "a2av_status", "a2av_destroy", "a2av_set_path",
+    for f in ("a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
               "a2av_set_grid", "a2av_last_launch", "a2av_version", "a2av_run_noalloc"):
         getattr(lib, f).restype = ci
     _lib = lib
@@ -97,6 +98,16 @@ def a2av_run(handle, in_ptrs, in_splits_dev: int, out_ptrs, out_splits_offsets_d
                            _ptr_array(out_ptrs),
                            ctypes.c_void_p(int(out_splits_offsets_dev) or None), int(row_bytes),
                            ctypes.c_void_p(int(stream) or None))
+
+
+def a2av_combine(handle, in_ptrs, dispatch_splits_offsets_dev: int, out_ptrs,
+                 out_splits_offsets_dev: int, row_bytes: int, stream: int = 0) -> int:
+    """Raw reverse exchange: integer device addresses, integer cudaStream_t."""
+    return load().a2av_combine(handle, _ptr_array(in_ptrs),
+                               ctypes.c_void_p(int(dispatch_splits_offsets_dev) or None),
+                               _ptr_array(out_ptrs),
+                               ctypes.c_void_p(int(out_splits_offsets_dev) or None),
+                               int(row_bytes), ctypes.c_void_p(int(stream) or None))
 
 
 def a2av_status(handle, stream: int = 0):
@@ -203,6 +214,24 @@ class A2av:
                       self._buffers(outputs, "outputs"), out_splits_offsets.data_ptr(),
                       row_bytes, self._stream(stream))
         self._check(rc, "a2av_run")
+
+    def combine(self, inputs, dispatch_splits_offsets, outputs, out_splits_offsets,
+                row_bytes: int, stream=None):
+        """The reverse exchange: send every received chunk back to its source
+        rank; ``dispatch_splits_offsets`` is the [W, 2, W] tensor a previous
+        ``run`` wrote."""
+        import torch
+        W = self.world_size
+        for t, name in ((dispatch_splits_offsets, "dispatch_splits_offsets"),
+                        (out_splits_offsets, "out_splits_offsets")):
+            if (not isinstance(t, torch.Tensor) or t.dtype != torch.int64 or not t.is_cuda
+                    or tuple(t.shape) != (W, 2, W) or not t.is_contiguous()):
+                raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of shape "
+                                 f"{(W, 2, W)}")
+        rc = a2av_combine(self.handle, self._buffers(inputs, "inputs"),
+                          dispatch_splits_offsets.data_ptr(), self._buffers(outputs, "outputs"),
+                          out_splits_offsets.data_ptr(), row_bytes, self._stream(stream))
+        self._check(rc, "a2av_combine")
 
     def status(self, stream=None) -> int:
         rc, v = a2av_status(self.handle, self._stream(stream))

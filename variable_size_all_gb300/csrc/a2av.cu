@@ -104,9 +104,10 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 #define A2AV_TILES_PER_CTA 1
 #endif
 // L2 eviction hints of the bulk engine: bit 0 marks loaded lines
-// evict-first, bit 1 stored lines (each byte is used exactly once).
+// evict-first, bit 1 stored lines (each byte is used exactly once; marking
+// the stored lines measured best).
 #ifndef A2AV_L2_HINT
-#define A2AV_L2_HINT 0
+#define A2AV_L2_HINT 2
 #endif
 
 namespace {
@@ -147,7 +148,9 @@ static_assert(kStagedPad % 128 == 0 && kStagedStageBytes % 128 == 0, "128-byte a
 struct Params {
   const unsigned char* in[kMaxW];
   unsigned char* out[kMaxW];
-  const long long* splits;  // [W][W], S[r][p] at r*W + p
+  const long long* splits;  // S[r][p] at splits[r * split_stride + p]
+  long long split_stride;   // W for a2av_run; 2W when the splits are a previous
+                            // exchange's out_splits_offsets (a2av_combine)
   long long* out_so;        // [W][2][W]
   int* status;
   long long rb;             // row bytes
@@ -188,7 +191,7 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
 
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {
-    const long long s = P.splits[e];
+    const long long s = P.splits[(long long)(e / W) * P.split_stride + e % W];
     if (s < 0 || s > limit) bad = 1;
     pl.in_off[e / W][e % W] = s;  // raw S[r][p] until the row scans below
   }
@@ -797,7 +800,7 @@ int configure_kernels() {
 // 16-byte aligned (the bulk engine's precondition).
 bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in_splits_dev,
                  void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
-                 long long in_cap, long long out_cap, int* status) {
+                 long long in_cap, long long out_cap, int* status, long long split_stride) {
   std::memset(P, 0, sizeof(*P));
   bool aligned = (row_bytes % 16) == 0;
   for (int r = 0; r < W; ++r) {
@@ -806,6 +809,7 @@ bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in
     aligned = aligned && ((uintptr_t)P->in[r] & 15) == 0 && ((uintptr_t)P->out[r] & 15) == 0;
   }
   P->splits = reinterpret_cast<const long long*>(in_splits_dev);
+  P->split_stride = split_stride;
   P->out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
   P->status = status;
   P->rb = row_bytes;
@@ -915,9 +919,14 @@ int a2av_last_launch(const a2av_handle* h, int* path, int* grid, int* block) {
   return A2AV_OK;
 }
 
-int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_splits_dev,
-             void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
-             void* stream) {
+}  // extern "C"
+
+namespace {
+
+// a2av_run and a2av_combine: the split matrix's rows are split_stride apart.
+int run_exchange(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_splits_dev,
+                 void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
+                 void* stream, long long split_stride) {
   if (h == nullptr || in_ptrs == nullptr || out_ptrs == nullptr || in_splits_dev == nullptr ||
       out_splits_offsets_dev == nullptr || row_bytes < 1)
     return A2AV_ERR_INVALID_ARG;
@@ -930,7 +939,7 @@ int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_split
   Params P;
   const bool aligned = fill_params(&P, h->W, in_ptrs, in_splits_dev, out_ptrs,
                                    out_splits_offsets_dev, row_bytes, h->in_cap, h->out_cap,
-                                   h->d_status);
+                                   h->d_status, split_stride);
   const int path = resolve_path(h->path, aligned);
   int grid = 0, block = 0;
   const int rc = launch(P, path, h->ctas_per_sm, h->sms, static_cast<cudaStream_t>(stream),
@@ -940,6 +949,29 @@ int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_split
   h->last_grid = grid;
   h->last_block = block;
   return A2AV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int a2av_run(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_splits_dev,
+             void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
+             void* stream) {
+  if (h == nullptr) return A2AV_ERR_INVALID_ARG;
+  return run_exchange(h, in_ptrs, in_splits_dev, out_ptrs, out_splits_offsets_dev, row_bytes,
+                      stream, h->W);
+}
+
+int a2av_combine(a2av_handle* h, const void* const* in_ptrs,
+                 const int64_t* dispatch_splits_offsets_dev, void* const* out_ptrs,
+                 int64_t* out_splits_offsets_dev, int64_t row_bytes, void* stream) {
+  if (h == nullptr) return A2AV_ERR_INVALID_ARG;
+  // Rank p sends back to rank r the S[r][p] rows it received from it:
+  // the reverse splits S'[p][r] = S[r][p] are row 0 of the dispatch's
+  // out_splits_offsets block of peer p, i.e. rows 2W apart.
+  return run_exchange(h, in_ptrs, dispatch_splits_offsets_dev, out_ptrs,
+                      out_splits_offsets_dev, row_bytes, stream, 2LL * h->W);
 }
 
 int a2av_status(a2av_handle* h, void* stream, int* device_status) {
@@ -1019,7 +1051,7 @@ extern "C" int a2av_run_noalloc(int world_size, int64_t in_capacity_rows,
   Params P;
   const bool aligned = fill_params(&P, world_size, in_ptrs, in_splits_dev, out_ptrs,
                                    out_splits_offsets_dev, row_bytes, in_capacity_rows,
-                                   out_capacity_rows, status);
+                                   out_capacity_rows, status, world_size);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The kernels only ever set the status word, so it must start at zero.
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
