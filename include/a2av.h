@@ -54,7 +54,8 @@ typedef enum {
   A2AV_ERR_UNSUPPORTED = -2, /* a valid request this build does not serve (W > 32) */
   A2AV_ERR_CUDA = -3,        /* a CUDA runtime call failed (no device, launch failure...) */
   A2AV_ERR_BAD_SPLITS = -4,  /* device-detected: the split matrix is invalid */
-  A2AV_ERR_TIMEOUT = -5      /* device-detected: a bounded wait inside a kernel gave up */
+  A2AV_ERR_TIMEOUT = -5,     /* device-detected: a bounded wait inside a kernel gave up */
+  A2AV_ERR_BAD_INDEX = -6    /* device-detected: a dispatch key or source row is out of range */
 } a2av_status_t;
 
 /* Copy engine selection (a2av_set_path). */
@@ -152,9 +153,73 @@ int a2av_combine(a2av_handle *h, const void *const *in_ptrs,
                  const int64_t *dispatch_splits_offsets_dev, void *const *out_ptrs,
                  int64_t *out_splits_offsets_dev, int64_t row_bytes, void *stream);
 
+/* Largest number of keys (W * keys_per_peer) a fused dispatch sorts by. */
+#define A2AV_MAX_DISPATCH_KEYS 1024
+
+/*
+ * a2av_dispatch_workspace_bytes -- device workspace a2av_dispatch needs for
+ * `world_size` ranks, `keys_per_peer` keys per peer and at most
+ * `max_items_per_rank` items on any rank; -1 for arguments a2av_dispatch
+ * would reject.  The workspace is caller-owned scratch, 256-byte aligned.
+ */
+int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
+                                      int64_t max_items_per_rank);
+
+/*
+ * a2av_dispatch -- fused dispatch preparation: the exchange of a2av_run on
+ * rows that are not yet grouped by destination.  The pages take the split
+ * matrix as given; this entry point also builds it, the step before the
+ * exchange in an MoE dispatch ("MoE related region", PR 154580) or an
+ * embedding-key exchange (torchrec PR 2570, "EmbeddingKey alltoall").
+ *
+ * Rank r has rows_per_rank[r] source rows at rows_ptrs[r] (row_bytes each)
+ * and items_per_rank[r] = m_r items.  Item i names a source row
+ * src_row_ptrs[r][i] (int32, in [0, rows_per_rank[r])) and a key
+ * key_ptrs[r][i] (int32, in [0, W * keys_per_peer)); its destination peer is
+ * key / keys_per_peer.  Rank r's items, ordered stably by key (ties by item
+ * index), are its virtual input: S[r][p] = the number of items with
+ * destination p, and the exchange then proceeds exactly as a2av_run on that
+ * virtual input, which is never materialised (rows are gathered straight
+ * from rows_ptrs into the outputs).  An MoE top-k dispatch is items
+ * (token t, choice k) with src_row = t and key = expert id (keys_per_peer =
+ * experts per rank); the peer receives rows ordered by (source rank, local
+ * expert, token).
+ *
+ *  rows_ptrs, rows_per_rank, items_per_rank, src_row_ptrs, key_ptrs:
+ *                     HOST arrays of W entries (pointers to device memory for
+ *                     the *_ptrs).  Read only.
+ *  out_ptrs, out_splits_offsets_dev: as in a2av_run.
+ *  sorted_pos_ptrs    HOST array of W device int64 [m_r] arrays: written with
+ *                     each item's position in its rank's key order (the
+ *                     permutation an MoE combine needs to put rows back).
+ *  in_splits_dev      DEVICE int64 [W][W] or NULL: written with S.
+ *  workspace          DEVICE scratch of at least
+ *                     a2av_dispatch_workspace_bytes(W, keys_per_peer,
+ *                     max_r m_r) bytes, 256-byte aligned, not shared with a
+ *                     dispatch in flight.
+ *
+ * Four kernel launches on `stream`: per-range key histograms, per-rank
+ * scans, stable ranking within ranges (warp match), the row gather-copy.
+ * Errors: host -- A2AV_ERR_INVALID_ARG (NULL arrays, keys_per_peer < 1,
+ * negative counts, a small or misaligned workspace), A2AV_ERR_UNSUPPORTED
+ * (W * keys_per_peer > A2AV_MAX_DISPATCH_KEYS, counts above 2^31 - 1);
+ * device -- A2AV_ERR_BAD_INDEX for a key or source row out of range and
+ * A2AV_ERR_BAD_SPLITS for a capacity or NULL-buffer violation (the handle's
+ * output capacity applies; inputs are checked by source-row index).  On a
+ * device-detected error nothing is written: no output row, no
+ * out_splits_offsets, sorted_pos or in_splits entry.
+ */
+int a2av_dispatch(a2av_handle *h, int keys_per_peer, const void *const *rows_ptrs,
+                  const int64_t *rows_per_rank, const int32_t *const *src_row_ptrs,
+                  const int32_t *const *key_ptrs, const int64_t *items_per_rank,
+                  void *const *out_ptrs, int64_t *out_splits_offsets_dev,
+                  int64_t *const *sorted_pos_ptrs, int64_t *in_splits_dev, int64_t row_bytes,
+                  void *workspace, int64_t workspace_bytes, void *stream);
+
 /*
  * a2av_status -- read and clear the handle's device status word: the first
- * device-detected error (A2AV_ERR_BAD_SPLITS or A2AV_ERR_TIMEOUT) of the runs
+ * device-detected error (A2AV_ERR_BAD_SPLITS, A2AV_ERR_TIMEOUT or
+ * A2AV_ERR_BAD_INDEX) of the runs
  * since the last call, or A2AV_OK.  Enqueues a 4-byte device-to-host copy and
  * a reset on `stream` and synchronizes that stream: the only host round trip
  * of the library.  `device_status` is a host pointer.

@@ -28,6 +28,7 @@ LIBRARY = os.path.join(HERE, "liba2av_oracle.so")
 OK = 0
 INVALID_ARG = -1
 BAD_SPLITS = -4
+BAD_INDEX = -6
 
 _lock = threading.Lock()
 _lib = None
@@ -55,8 +56,10 @@ def _bind(lib):
                                            ctypes.POINTER(ctypes.c_int), _i64p]
     lib.a2av_oracle_combine.argtypes = [ctypes.c_int, vpp, _i64p, vpp, _i64p, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int64]
+    lib.a2av_oracle_dispatch.argtypes = [ctypes.c_int, ctypes.c_int, vpp, _i64p, vpp, vpp, _i64p,
+                                         vpp, _i64p, vpp, _i64p, ctypes.c_int64, ctypes.c_int64]
     for f in (lib.a2av_oracle, lib.a2av_oracle_dest, lib.a2av_oracle_check,
-              lib.a2av_oracle_row_source, lib.a2av_oracle_combine):
+              lib.a2av_oracle_row_source, lib.a2av_oracle_combine, lib.a2av_oracle_dispatch):
         f.restype = ctypes.c_int
     return lib
 
@@ -148,6 +151,37 @@ class Oracle:
                                             _ptrs(outputs), out_splits_offsets.ctypes.data_as(_i64p),
                                             int(row_bytes), int(in_capacity_rows),
                                             int(out_capacity_rows))
+
+    def dispatch(self, K, rows, src_rows, keys, outputs, out_splits_offsets, sorted_pos,
+                 row_bytes, in_splits=None, out_capacity_rows=0) -> int:
+        """Fused dispatch preparation (see a2av_oracle.c); numpy arrays in and out."""
+        W = len(rows)
+        src = [np.ascontiguousarray(x, dtype=np.int32) for x in src_rows]
+        key = [np.ascontiguousarray(x, dtype=np.int32) for x in keys]
+        n_rows = (ctypes.c_int64 * W)(*[r.size // int(row_bytes) for r in rows])
+        n_items = (ctypes.c_int64 * W)(*[k.size for k in key])
+        assert all(p.dtype == np.int64 and p.size == k.size for p, k in zip(sorted_pos, key))
+        isp = None if in_splits is None else in_splits.ctypes.data_as(_i64p)
+        return self.lib.a2av_oracle_dispatch(
+            W, int(K), _ptrs(rows), n_rows, _ptrs(src), _ptrs(key), n_items, _ptrs(outputs),
+            out_splits_offsets.ctypes.data_as(_i64p), _ptrs(sorted_pos), isp, int(row_bytes),
+            int(out_capacity_rows))
+
+    def dispatch_exchange(self, K, rows, src_rows, keys, row_bytes):
+        """Return (outputs, out_splits_offsets, sorted_pos, S) of a fused dispatch."""
+        W = len(rows)
+        S = np.zeros((W, W), np.int64)
+        for r in range(W):  # output sizes only
+            for k in np.asarray(keys[r]).reshape(-1):
+                S[r, int(k) // K] += 1
+        outs = [np.empty(int(S[:, p].sum()) * row_bytes, np.uint8) for p in range(W)]
+        so = np.empty((W, 2, W), np.int64)
+        pos = [np.empty(np.asarray(k).size, np.int64) for k in keys]
+        isp = np.empty((W, W), np.int64)
+        rc = self.dispatch(K, rows, src_rows, keys, outs, so, pos, row_bytes, isp)
+        if rc != OK:
+            raise ValueError(f"oracle rejected the dispatch (status {rc})")
+        return outs, so, pos, isp
 
     # ---- convenience: allocate outputs of exactly the received size -------
     def exchange(self, inputs, splits, row_bytes):

@@ -37,6 +37,7 @@
 #define ORACLE_OK 0
 #define ORACLE_INVALID_ARG (-1)
 #define ORACLE_BAD_SPLITS (-4)
+#define ORACLE_BAD_INDEX (-6)
 
 /* Largest byte count the exchange accepts: 2^62. */
 static const int64_t kMaxBytes = (int64_t)1 << 62;
@@ -164,5 +165,69 @@ int a2av_oracle_combine(int W, const uint8_t *const *in, const int64_t *dispatch
   const int rc = a2av_oracle(W, in, St, out, out_splits_offsets, row_bytes, in_capacity_rows,
                              out_capacity_rows);
   free(St);
+  return rc;
+}
+
+/* Fused dispatch preparation: rank r's m_r items, item i naming source row
+ * src_row[r][i] of rows[r] and key key[r][i] in [0, W*K), destination peer
+ * key / K.  Each rank's items taken in increasing key order, ties in item
+ * order, form its input for the exchange above (its chunks in peer order);
+ * S[r][p] is the number of its items with destination p.  Writes the
+ * exchange's outputs and out_splits_offsets, sorted_pos[r][i] = item i's
+ * place in that order and, when in_splits is not NULL, S.  A key or source
+ * row out of range gives ORACLE_BAD_INDEX and writes nothing. */
+int a2av_oracle_dispatch(int W, int K, const uint8_t *const *rows, const int64_t *n_rows,
+                         const int32_t *const *src_row, const int32_t *const *key,
+                         const int64_t *n_items, uint8_t *const *out, int64_t *out_splits_offsets,
+                         int64_t *const *sorted_pos, int64_t *in_splits, int64_t row_bytes,
+                         int64_t out_capacity_rows) {
+  if (W < 1 || K < 1 || row_bytes < 1) return ORACLE_INVALID_ARG;
+  const int64_t nkeys = (int64_t)W * K;
+  for (int r = 0; r < W; ++r)
+    for (int64_t i = 0; i < n_items[r]; ++i)
+      if (key[r][i] < 0 || key[r][i] >= nkeys || src_row[r][i] < 0 || src_row[r][i] >= n_rows[r])
+        return ORACLE_BAD_INDEX;
+  int64_t *S = (int64_t *)calloc((size_t)W * (size_t)W, sizeof(int64_t));
+  uint8_t **sorted = (uint8_t **)calloc((size_t)W, sizeof(uint8_t *));
+  int64_t **place = (int64_t **)calloc((size_t)W, sizeof(int64_t *));
+  int rc = (S == NULL || sorted == NULL || place == NULL) ? ORACLE_INVALID_ARG : ORACLE_OK;
+  for (int r = 0; r < W && rc == ORACLE_OK; ++r)
+    for (int64_t i = 0; i < n_items[r]; ++i) S[(int64_t)r * W + key[r][i] / K] += 1;
+  if (rc == ORACLE_OK)
+    rc = a2av_oracle_check(W, S, row_bytes, 0, out_capacity_rows, (const void *const *)rows,
+                           (void *const *)out);
+  /* each rank's items in key order (counting order: every key value in turn,
+   * its items in item order), rows gathered into a buffer of that order */
+  for (int r = 0; r < W && rc == ORACLE_OK; ++r) {
+    const int64_t m = n_items[r];
+    sorted[r] = (uint8_t *)malloc((size_t)(m > 0 ? m : 1) * (size_t)row_bytes);
+    place[r] = (int64_t *)malloc((size_t)(m > 0 ? m : 1) * sizeof(int64_t));
+    if (sorted[r] == NULL || place[r] == NULL) {
+      rc = ORACLE_INVALID_ARG;
+      break;
+    }
+    int64_t next = 0;
+    for (int64_t k = 0; k < nkeys; ++k)
+      for (int64_t i = 0; i < m; ++i)
+        if (key[r][i] == k) {
+          memcpy(sorted[r] + next * row_bytes, rows[r] + (int64_t)src_row[r][i] * row_bytes,
+                 (size_t)row_bytes);
+          place[r][i] = next++;
+        }
+  }
+  if (rc == ORACLE_OK)
+    rc = a2av_oracle(W, (const uint8_t *const *)sorted, S, out, out_splits_offsets, row_bytes, 0,
+                     out_capacity_rows);
+  if (rc == ORACLE_OK) {
+    for (int r = 0; r < W; ++r)
+      for (int64_t i = 0; i < n_items[r]; ++i) sorted_pos[r][i] = place[r][i];
+    if (in_splits != NULL)
+      for (int64_t e = 0; e < (int64_t)W * W; ++e) in_splits[e] = S[e];
+  }
+  for (int r = 0; sorted != NULL && r < W; ++r) free(sorted[r]);
+  for (int r = 0; place != NULL && r < W; ++r) free(place[r]);
+  free(sorted);
+  free(place);
+  free(S);
   return rc;
 }

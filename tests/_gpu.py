@@ -113,3 +113,46 @@ def combine_checked(inputs, dispatch_so, rb, path=a2av.PATH_AUTO, in_mis=None, o
     for p in range(W):
         assert np.array_equal(ins[p].view.cpu().numpy(), inputs[p]), f"combine input {p} modified"
     return [outs[r].view.cpu().numpy()[: back[r] * rb] for r in range(W)]
+
+
+def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=None):
+    """Fused dispatch on the GPU against the oracle's: outputs, offsets,
+    positions and the split matrix; canaries and slack untouched."""
+    W = len(rows)
+    rows_mis = rows_mis or [0] * W
+    out_mis = out_mis or [0] * W
+    ref, ref_so, ref_pos, ref_S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+    g_rows = [Guarded(rows[r].size, rows_mis[r], host=rows[r]) for r in range(W)]
+    g_out = [Guarded(ref[p].size + SLACK_ROWS * rb, out_mis[p], fill=SENTINEL) for p in range(W)]
+    d_src = [torch.from_numpy(np.ascontiguousarray(s, dtype=np.int32)).cuda() for s in src]
+    d_key = [torch.from_numpy(np.ascontiguousarray(k, dtype=np.int32)).cuda() for k in key]
+    d_pos = [torch.full((np.asarray(k).size,), -1, dtype=torch.int64, device="cuda") for k in key]
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    isp = torch.full((W, W), -7, dtype=torch.int64, device="cuda")
+    own = engine is None
+    eng = engine or a2av.A2av(W)
+    try:
+        eng.dispatch([g.view for g in g_rows], d_src, d_key, K, [g.view for g in g_out], so, d_pos,
+                     rb, in_splits=isp)
+        st = eng.status()
+    finally:
+        if own:
+            eng.close()
+    torch.cuda.synchronize()
+    assert st == a2av.OK, f"device status {st}"
+    assert np.array_equal(isp.cpu().numpy(), ref_S), "dispatch split matrix differs"
+    assert np.array_equal(so.cpu().numpy(), ref_so), "dispatch out_splits_offsets differ"
+    for r in range(W):
+        assert np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r]), f"rank {r}: positions differ"
+    for p in range(W):
+        got = g_out[p].view.cpu().numpy()
+        n = ref[p].size
+        if not np.array_equal(got[:n], ref[p]):
+            bad = np.nonzero(got[:n] != ref[p])[0]
+            raise AssertionError(f"dispatch peer {p}: {bad.size} bytes differ, first at row "
+                                 f"{bad[0] // rb} (W={W} K={K} rb={rb})")
+        assert np.all(got[n:] == SENTINEL), f"dispatch peer {p}: written past its rows"
+        assert g_out[p].guards_intact(), f"dispatch peer {p}: canary overwritten"
+    for r in range(W):
+        assert np.array_equal(g_rows[r].view.cpu().numpy(), rows[r]), f"rows {r} modified"
+    return ref, ref_so, ref_pos, ref_S

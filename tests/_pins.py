@@ -314,8 +314,91 @@ def pin_combine_round_trip(o):
             _eq(back[r], x.transpose(1, 0, 2, 3)[r].reshape(-1), "uniform combine = transpose")
 
 
+def _dispatch_reference(K, rows, src, key, rb):
+    """Fused dispatch written out: sort each rank's items with Python's stable
+    sort on (key, item), gather their rows, then the scatter formulation."""
+    W = len(rows)
+    sorted_rows, pos, S = [], [], np.zeros((W, W), np.int64)
+    for r in range(W):
+        order = sorted(range(len(key[r])), key=lambda i: (int(key[r][i]), i))
+        inv = np.empty(len(order), np.int64)
+        for k, i in enumerate(order):
+            inv[i] = k
+            S[r, int(key[r][i]) // K] += 1
+        buf = [rows[r][int(src[r][i]) * rb:(int(src[r][i]) + 1) * rb] for i in order]
+        sorted_rows.append(np.concatenate(buf) if buf else np.zeros(0, np.uint8))
+        pos.append(inv)
+    outs, so = scatter_reference(sorted_rows, S, rb)
+    return outs, so, pos, S
+
+
+def pin_dispatch_small(o):
+    rng = np.random.default_rng(17)
+    for trial in range(300):
+        W = int(rng.integers(1, 4))
+        K = int(rng.integers(1, 4))
+        rb = int(rng.choice([1, 3, 8]))
+        n = [int(rng.integers(0, 5)) for _ in range(W)]
+        m = [int(rng.integers(0, 7)) for _ in range(W)]
+        rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+        src = [rng.integers(0, max(n[r], 1), m[r]).astype(np.int32) if n[r] else
+               np.zeros(0, np.int32) for r in range(W)]
+        m = [s.size for s in src]
+        key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+        ref_outs, ref_so, ref_pos, ref_S = _dispatch_reference(K, rows, src, key, rb)
+        outs = [np.full(b.size, SENTINEL, np.uint8) for b in ref_outs]
+        so = np.full((W, 2, W), -7, np.int64)
+        pos = [np.full(mm, -1, np.int64) for mm in m]
+        isp = np.full((W, W), -1, np.int64)
+        assert o.dispatch(K, rows, src, key, outs, so, pos, rb, isp) == 0
+        for p in range(W):
+            _eq(outs[p], ref_outs[p], f"dispatch peer {p} (W={W} K={K})")
+        _eq(so, ref_so, "dispatch out_splits_offsets")
+        _eq(isp, ref_S, "dispatch in_splits")
+        for r in range(W):
+            _eq(pos[r], ref_pos[r], "dispatch sorted positions")
+
+
+def pin_dispatch_matches_generators(o):
+    import workloads as wl
+    for w in (wl.cfg3(2, tokens=96, hidden=4), wl.cfg5(3, batch=64)):
+        K, rows, src, key = wl.dispatch_items(w)
+        outs, so, pos, S = o.dispatch_exchange(K, rows, src, key, w.row_bytes)
+        _eq(S, w.splits, f"{w.name}: dispatch splits must equal the generator's")
+        ref, ref_so = o.exchange(w.inputs, w.splits, w.row_bytes)
+        for p in range(w.W):
+            _eq(outs[p], ref[p], f"{w.name}: dispatch must equal the exchange of the "
+                                 "generator's pre-grouped rows")
+        _eq(so, ref_so, f"{w.name}: offsets")
+        for r in range(w.W):
+            order = np.argsort(key[r], kind="stable")  # numpy's stable sort as the pin
+            inv = np.empty(order.size, np.int64)
+            inv[order] = np.arange(order.size)
+            _eq(pos[r], inv, f"{w.name}: positions = inverse stable argsort")
+
+
+def pin_dispatch_errors(o):
+    rows = [np.arange(12, dtype=np.uint8), np.arange(8, dtype=np.uint8)]
+    good_src = [np.array([0, 2, 1], np.int32), np.array([1, 0], np.int32)]
+    good_key = [np.array([0, 3, 1], np.int32), np.array([2, 2], np.int32)]
+    for what, src, key, cap, code in (
+            ("key too large", good_src, [good_key[0], np.array([2, 4], np.int32)], 0, -6),
+            ("negative key", good_src, [np.array([0, -1, 1], np.int32), good_key[1]], 0, -6),
+            ("source row too large", [good_src[0], np.array([1, 2], np.int32)], good_key, 0, -6),
+            ("output capacity", good_src, good_key, 2, -4)):
+        outs = [np.full(16, SENTINEL, np.uint8), np.full(16, SENTINEL, np.uint8)]
+        so = np.full((2, 2, 2), -7, np.int64)
+        pos = [np.full(3, -1, np.int64), np.full(2, -1, np.int64)]
+        isp = np.full((2, 2), -1, np.int64)
+        rc = o.dispatch(2, rows, src, key, outs, so, pos, 4, isp, out_capacity_rows=cap)
+        assert rc == code, f"{what}: status {rc}, expected {code}"
+        assert all(np.all(b == SENTINEL) for b in outs) and np.all(so == -7), what
+        assert all(np.all(p == -1) for p in pos) and np.all(isp == -1), what
+
+
 PINS = [pin_identity_w1, pin_errors, pin_diagonal_and_permutation, pin_uniform_transpose,
-        pin_round_trip, pin_combine_round_trip, pin_dest_and_row_source, pin_invariants_random,
+        pin_round_trip, pin_combine_round_trip, pin_dispatch_errors, pin_dispatch_small,
+        pin_dispatch_matches_generators, pin_dest_and_row_source, pin_invariants_random,
         pin_bruteforce_tiny]
 
 

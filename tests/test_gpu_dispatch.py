@@ -1,0 +1,145 @@
+"""GPU parity of the fused dispatch (a2av_dispatch) against the CPU oracle:
+grouping unsorted items by key on the device, gathering their rows into the
+exchange's outputs, positions and split matrix -- byte for byte."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from tests._gpu import dispatch_checked
+
+pytestmark = pytest.mark.gpu
+
+a2av = pytest.importorskip("variable_size_all_gb300")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    a2av.build()
+    a2av.load()
+
+
+@pytest.mark.parametrize("tokens", [1024, 8192])
+def test_moe_top2_dispatch(tokens):
+    w = wl.cfg3(0, tokens=tokens)
+    K, rows, src, key = wl.dispatch_items(w)
+    ref, *_ = dispatch_checked(K, rows, src, key, w.row_bytes)
+    for p in range(w.W):  # and it equals the exchange of the pre-grouped rows
+        assert ref[p].size == int(w.splits[:, p].sum()) * w.row_bytes
+
+
+def test_embedding_key_dispatch():
+    w = wl.cfg5(0)
+    K, rows, src, key = wl.dispatch_items(w)
+    dispatch_checked(K, rows, src, key, w.row_bytes)
+
+
+@pytest.mark.parametrize("rb", [1, 3, 8, 13, 64, 100, 256, 1040])
+def test_random_dispatch(rb):
+    rng = np.random.default_rng(rb)
+    for W, K in ((1, 1), (2, 5), (3, 32), (8, 8), (32, 32), (5, 200)):
+        n = [int(rng.integers(0, 300)) for _ in range(W)]
+        m = [int(rng.integers(0, 3000)) if n[r] else 0 for r in range(W)]
+        rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+        src = [rng.integers(0, max(n[r], 1), m[r]).astype(np.int32) for r in range(W)]
+        if rng.random() < 0.5:  # skewed keys: most items on a few keys
+            key = [np.minimum(rng.geometric(0.2, m[r]) - 1, W * K - 1).astype(np.int32)
+                   for r in range(W)]
+        else:
+            key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+        mis = [int(rng.integers(0, 16)) for _ in range(W)]
+        dispatch_checked(K, rows, src, key, rb, rows_mis=mis, out_mis=mis[::-1])
+
+
+def test_dispatch_without_items():
+    rows = [np.arange(64, dtype=np.uint8)] * 3
+    empty = [np.zeros(0, np.int32)] * 3
+    dispatch_checked(2, rows, empty, empty, 16)
+
+
+def test_dispatch_then_combine_restores_key_order():
+    w = wl.cfg3(7, tokens=512, hidden=256)
+    K, rows, src, key = wl.dispatch_items(w)
+    W, rb = w.W, w.row_bytes
+    eng = a2av.A2av(W)
+    d_rows = [torch.from_numpy(r).cuda() for r in rows]
+    d_src = [torch.from_numpy(s).cuda() for s in src]
+    d_key = [torch.from_numpy(k).cuda() for k in key]
+    d_pos = [torch.empty(k.size, dtype=torch.int64, device="cuda") for k in key]
+    out = [torch.empty(int(w.splits[:, p].sum()) * rb, dtype=torch.uint8, device="cuda")
+           for p in range(W)]
+    so = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    back = [torch.empty(k.size * rb, dtype=torch.uint8, device="cuda") for k in key]
+    cso = torch.empty_like(so)
+    eng.dispatch(d_rows, d_src, d_key, K, out, so, d_pos, rb)
+    eng.combine(out, so, back, cso, rb)
+    assert eng.status() == a2av.OK
+    eng.close()
+    for r in range(W):
+        # item i's row comes back at its sorted position
+        got = back[r].view(-1, rb)[d_pos[r]].cpu().numpy()
+        want = rows[r].reshape(-1, rb)[src[r]]
+        assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("case", ["key", "negative_key", "src", "capacity", "null_out"])
+def test_dispatch_errors_write_nothing(case):
+    W, K, rb = 2, 2, 4
+    rows = [torch.arange(12, dtype=torch.uint8, device="cuda"),
+            torch.arange(8, dtype=torch.uint8, device="cuda")]
+    src = [torch.tensor([0, 2, 1], dtype=torch.int32, device="cuda"),
+           torch.tensor([1, 0], dtype=torch.int32, device="cuda")]
+    key = [torch.tensor([0, 3, 1], dtype=torch.int32, device="cuda"),
+           torch.tensor([2, 2], dtype=torch.int32, device="cuda")]
+    cap = 0
+    outs = [torch.full((16,), 0xEE, dtype=torch.uint8, device="cuda") for _ in range(W)]
+    if case == "key":
+        key[1][1] = 4
+    elif case == "negative_key":
+        key[0][1] = -1
+    elif case == "src":
+        src[1][0] = 2
+    elif case == "capacity":
+        cap = 2
+    elif case == "null_out":
+        outs[1] = torch.empty(0, dtype=torch.uint8, device="cuda")
+    pos = [torch.full((3,), -1, dtype=torch.int64, device="cuda"),
+           torch.full((2,), -1, dtype=torch.int64, device="cuda")]
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    isp = torch.full((W, W), -7, dtype=torch.int64, device="cuda")
+    eng = a2av.A2av(W, 0, cap)
+    eng.dispatch(rows, src, key, K, outs, so, pos, rb, in_splits=isp)
+    st = eng.status()
+    eng.close()
+    want = a2av.ERR_BAD_INDEX if case in ("key", "negative_key", "src") else a2av.ERR_BAD_SPLITS
+    assert st == want
+    torch.cuda.synchronize()
+    assert all(bool((o == 0xEE).all()) for o in outs if o.numel())
+    assert bool((so == -7).all()) and bool((isp == -7).all())
+    assert all(bool((p == -1).all()) for p in pos)
+
+
+def test_dispatch_host_rejections():
+    rc, h = a2av.a2av_create(4)
+    assert rc == a2av.OK
+    z = [0] * 4
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    so = torch.empty((4, 2, 4), dtype=torch.int64, device="cuda")
+    args = dict(rows_ptrs=z, rows_per_rank=z, src_row_ptrs=z, key_ptrs=z, items_per_rank=z,
+                out_ptrs=z, out_splits_offsets_dev=so.data_ptr(), sorted_pos_ptrs=z,
+                in_splits_dev=0, row_bytes=8, workspace=ws.data_ptr(), workspace_bytes=ws.numel())
+    assert a2av.a2av_dispatch(h, 2, **args) == a2av.OK  # nothing to do is fine
+    assert a2av.a2av_dispatch(h, 0, **args) == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_dispatch(h, 257, **args) == a2av.ERR_UNSUPPORTED  # 4 x 257 keys
+    assert a2av.a2av_dispatch(h, 2, **{**args, "workspace_bytes": 64}) == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_dispatch(h, 2, **{**args, "workspace": ws.data_ptr() + 8}) \
+        == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_dispatch(h, 2, **{**args, "items_per_rank": [-1, 0, 0, 0]}) \
+        == a2av.ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert a2av.a2av_status(h)[1] == a2av.OK
+    a2av.a2av_destroy(h)
+    assert a2av.a2av_dispatch_workspace_bytes(4, 257, 10) == -1
+    assert a2av.a2av_dispatch_workspace_bytes(4, 8, 1000) > 0

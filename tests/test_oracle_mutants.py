@@ -41,6 +41,14 @@ MUTANTS = {
                                   "St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + W + r];"),
     "combine_not_transposed": ("St[(int64_t)p * W + r] = dispatch_so[(int64_t)p * 2 * W + r];",
                                "St[(int64_t)r * W + p] = dispatch_so[(int64_t)p * 2 * W + r];"),
+    "dispatch_unstable": ("      for (int64_t i = 0; i < m; ++i)\n        if (key[r][i] == k) {",
+                          "      for (int64_t i = m - 1; i >= 0; --i)\n        if (key[r][i] == k) {"),
+    "dispatch_dest_mod": ("S[(int64_t)r * W + key[r][i] / K] += 1;",
+                          "S[(int64_t)r * W + key[r][i] % W] += 1;"),
+    "dispatch_ignores_src": ("rows[r] + (int64_t)src_row[r][i] * row_bytes",
+                             "rows[r] + (int64_t)(i % n_rows[r]) * row_bytes"),
+    "dispatch_pos_off_by_one": ("place[r][i] = next++;", "place[r][i] = ++next - 0;"),
+    "dispatch_key_bound": ("key[r][i] >= nkeys ||", "key[r][i] > nkeys ||"),
     "row_source_wrong_chunk": ("*i = in_offset(W, in_splits, q, p) + (k - start);",
                                "*i = in_offset(W, in_splits, p, q) + (k - start);"),
 }

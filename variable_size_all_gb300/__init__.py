@@ -18,11 +18,14 @@ __all__ = [
     "A2av", "A2avError", "load", "build",
     "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
+    "a2av_dispatch", "a2av_dispatch_workspace_bytes", "ERR_BAD_INDEX", "MAX_DISPATCH_KEYS",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
 ]
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_BAD_SPLITS, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+ERR_BAD_INDEX = -6
+MAX_DISPATCH_KEYS = 1024
 PATH_AUTO, PATH_VECTOR, PATH_BULK, PATH_STAGED = 0, 1, 2, 3
 MAX_RANKS = 32
 
@@ -57,6 +60,11 @@ def load():
     lib.a2av_last_launch.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci),
                                      ctypes.POINTER(ci)]
     lib.a2av_run_noalloc.argtypes = [ci, i64, i64, pp, vp, pp, vp, i64, vp, ctypes.POINTER(ci)]
+    i64p = ctypes.POINTER(i64)
+    lib.a2av_dispatch_workspace_bytes.argtypes = [ci, ci, i64]
+    lib.a2av_dispatch_workspace_bytes.restype = i64
+    lib.a2av_dispatch.argtypes = [vp, ci, pp, i64p, pp, pp, i64p, pp, vp, pp, vp, i64, vp, i64, vp]
+    lib.a2av_dispatch.restype = ci
     lib.a2av_error_string.argtypes = [ci]
     lib.a2av_error_string.restype = ctypes.c_char_p
     lib.a2av_version.argtypes = []
@@ -153,6 +161,30 @@ def a2av_run_noalloc(world_size: int, in_capacity_rows: int, out_capacity_rows: 
     return rc, (v.value if wait else None)
 
 
+def a2av_dispatch_workspace_bytes(world_size: int, keys_per_peer: int,
+                                  max_items_per_rank: int) -> int:
+    return load().a2av_dispatch_workspace_bytes(int(world_size), int(keys_per_peer),
+                                                int(max_items_per_rank))
+
+
+def _i64_array(values):
+    return (ctypes.c_int64 * max(len(values), 1))(*[int(v) for v in values])
+
+
+def a2av_dispatch(handle, keys_per_peer: int, rows_ptrs, rows_per_rank, src_row_ptrs, key_ptrs,
+                  items_per_rank, out_ptrs, out_splits_offsets_dev: int, sorted_pos_ptrs,
+                  in_splits_dev: int, row_bytes: int, workspace: int, workspace_bytes: int,
+                  stream: int = 0) -> int:
+    """Raw fused dispatch: integer device addresses, host lists of counts."""
+    return load().a2av_dispatch(
+        handle, int(keys_per_peer), _ptr_array(rows_ptrs), _i64_array(rows_per_rank),
+        _ptr_array(src_row_ptrs), _ptr_array(key_ptrs), _i64_array(items_per_rank),
+        _ptr_array(out_ptrs), ctypes.c_void_p(int(out_splits_offsets_dev) or None),
+        _ptr_array(sorted_pos_ptrs), ctypes.c_void_p(int(in_splits_dev) or None),
+        int(row_bytes), ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
+        ctypes.c_void_p(int(stream) or None))
+
+
 # --------------------------------------------------------- torch-facing --
 class A2av:
     """One handle over ``world_size`` ranks; tensors in, tensors out.
@@ -232,6 +264,58 @@ class A2av:
                           dispatch_splits_offsets.data_ptr(), self._buffers(outputs, "outputs"),
                           out_splits_offsets.data_ptr(), row_bytes, self._stream(stream))
         self._check(rc, "a2av_combine")
+
+    def dispatch(self, rows, src_rows, keys, keys_per_peer: int, outputs, out_splits_offsets,
+                 sorted_pos, row_bytes: int, in_splits=None, workspace=None, stream=None):
+        """Fused dispatch: group each rank's items by key on the device and
+        exchange their rows (see include/a2av.h, a2av_dispatch).
+
+        ``rows[r]``: rank r's source rows (uint8 CUDA tensor, a multiple of
+        ``row_bytes``); ``src_rows[r]`` / ``keys[r]``: int32 CUDA tensors, one
+        entry per item; ``sorted_pos[r]``: int64 CUDA tensor receiving each
+        item's position in key order; ``in_splits``: optional int64 [W, W]
+        receiving the split matrix.  ``workspace`` defaults to a buffer the
+        object keeps (torch allocation, sized by the largest item count)."""
+        import torch
+        W = self.world_size
+        for name, ts, dt in (("src_rows", src_rows, torch.int32), ("keys", keys, torch.int32),
+                             ("sorted_pos", sorted_pos, torch.int64)):
+            if len(ts) != W:
+                raise ValueError(f"{name}: expected {W} tensors")
+            for t in ts:
+                if t is not None and t.numel() and (t.dtype != dt or not t.is_cuda
+                                                    or not t.is_contiguous()):
+                    raise ValueError(f"{name} must be contiguous CUDA {dt} tensors")
+        if not (isinstance(out_splits_offsets, torch.Tensor) and out_splits_offsets.is_cuda
+                and out_splits_offsets.dtype == torch.int64
+                and tuple(out_splits_offsets.shape) == (W, 2, W)
+                and out_splits_offsets.is_contiguous()):
+            raise ValueError(f"out_splits_offsets must be a contiguous CUDA int64 [{W}, 2, {W}]")
+        if in_splits is not None and (in_splits.dtype != torch.int64 or not in_splits.is_cuda
+                                      or tuple(in_splits.shape) != (W, W)):
+            raise ValueError(f"in_splits must be a CUDA int64 [{W}, {W}] tensor")
+        items = [0 if t is None else t.numel() for t in keys]
+        if any((0 if s is None else s.numel()) != m for s, m in zip(src_rows, items)):
+            raise ValueError("src_rows and keys must have one entry per item")
+        if any((0 if t is None else t.numel()) != m for t, m in zip(sorted_pos, items)):
+            raise ValueError("sorted_pos must have one entry per item")
+        need = a2av_dispatch_workspace_bytes(W, keys_per_peer, max(items))
+        if need < 0:
+            raise A2avError(ERR_UNSUPPORTED, "a2av_dispatch_workspace_bytes")
+        if workspace is None:
+            ws = getattr(self, "_workspace", None)
+            if ws is None or ws.numel() < need:
+                ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+                self._workspace = ws
+            workspace = ws
+        n_rows = [0 if t is None else t.numel() // int(row_bytes) for t in rows]
+        ptr = lambda ts: [0 if t is None or t.numel() == 0 else t.data_ptr() for t in ts]
+        rc = a2av_dispatch(self.handle, keys_per_peer, self._buffers(rows, "rows"), n_rows,
+                           ptr(src_rows), ptr(keys), items, self._buffers(outputs, "outputs"),
+                           out_splits_offsets.data_ptr(), ptr(sorted_pos),
+                           0 if in_splits is None else in_splits.data_ptr(), row_bytes,
+                           workspace.data_ptr(), workspace.numel(), self._stream(stream))
+        self._check(rc, "a2av_dispatch")
 
     def status(self, stream=None) -> int:
         rc, v = a2av_status(self.handle, self._stream(stream))

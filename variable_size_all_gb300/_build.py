@@ -7,7 +7,8 @@ import subprocess
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SOURCES = [os.path.join(PKG, "csrc", "a2av.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "a2av.cu"), os.path.join(PKG, "csrc", "dispatch.cu")]
+HEADERS = [os.path.join(PKG, "csrc", "a2av_device.cuh"), os.path.join(PKG, "csrc", "a2av_handle.h")]
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(PKG, "liba2av.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -28,7 +29,7 @@ def command(output: str = LIBRARY, extra=()) -> list:
 def stale(output: str = LIBRARY) -> bool:
     if not os.path.exists(output):
         return True
-    deps = SOURCES + [os.path.join(INCLUDE, "a2av.h"), __file__]
+    deps = SOURCES + HEADERS + [os.path.join(INCLUDE, "a2av.h"), __file__]
     return os.path.getmtime(output) < max(os.path.getmtime(d) for d in deps)
 
 
@@ -39,7 +40,8 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
         if verbose:
             print(" ".join(cmd))
         tmp = LIBRARY + ".tmp"
-        subprocess.run(cmd[:-len(SOURCES) - 2] + ["-o", tmp, *SOURCES], check=True)
+        subprocess.run(cmd[:-len(SOURCES) - 2] + ["-o", tmp, *SOURCES, "--threads", "0"],
+                       check=True)
         os.replace(tmp, LIBRARY)
     return LIBRARY
 

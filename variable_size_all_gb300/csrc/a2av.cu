@@ -39,7 +39,8 @@
 //      No cluster multicast anywhere.  Every mbarrier wait is bounded (~1 s),
 //      after which the kernel records A2AV_ERR_TIMEOUT and leaves.
 //   CTA 0 writes out_splits_offsets.
-#include "a2av.h"
+#include "a2av_device.cuh"
+#include "a2av_handle.h"
 
 #include <cuda_runtime.h>
 
@@ -49,15 +50,6 @@
 #include <mutex>
 #include <new>
 
-namespace {
-
-constexpr int kMaxW = A2AV_MAX_RANKS;
-constexpr long long kMaxBytes = 1LL << 62;  // byte offsets stay below 2^62
-constexpr unsigned kFull = 0xffffffffu;
-constexpr long long kTileGranule = 4096;         // tile sizes are multiples of this
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
-
-}  // namespace
 
 // Engine shapes.  Each can be overridden at compile time (-DA2AV_...) for
 // tuning sweeps; the defaults are the measured choices.
@@ -100,21 +92,9 @@ constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
 #ifndef A2AV_STAGED_CTAS_PER_SM
 #define A2AV_STAGED_CTAS_PER_SM 1
 #endif
-#ifndef A2AV_TILES_PER_CTA
-#define A2AV_TILES_PER_CTA 1
-#endif
-// L2 eviction hints of the bulk engine: bit 0 marks loaded lines
-// evict-first, bit 1 stored lines (each byte is used exactly once; marking
-// the stored lines measured best).
-#ifndef A2AV_L2_HINT
-#define A2AV_L2_HINT 2
-#endif
 
 namespace {
 
-// Tiles each CTA gets at least, when the payload allows (smaller tiles for
-// small payloads keep more of them in flight per CTA).
-constexpr long long kTilesPerCta = A2AV_TILES_PER_CTA;
 
 // Vector engine: 512 threads (64 registers each, two CTAs per SM), 4
 // independent 16-byte loads in flight per thread on the aligned path (32 KiB
@@ -144,387 +124,6 @@ constexpr int kStagedCtasPerSm = A2AV_STAGED_CTAS_PER_SM;
 constexpr int kStagedPad = 32 * kMaxW + 128;
 constexpr int kStagedAlloc = kStagedStageBytes + kStagedPad;
 static_assert(kStagedPad % 128 == 0 && kStagedStageBytes % 128 == 0, "128-byte aligned stages");
-
-struct Params {
-  const unsigned char* in[kMaxW];
-  unsigned char* out[kMaxW];
-  const long long* splits;  // S[r][p] at splits[r * split_stride + p]
-  long long split_stride;   // W for a2av_run; 2W when the splits are a previous
-                            // exchange's out_splits_offsets (a2av_combine)
-  long long* out_so;        // [W][2][W]
-  int* status;
-  long long rb;             // row bytes
-  long long in_cap;         // rows, 0 = unchecked
-  long long out_cap;        // rows, 0 = unchecked
-  int W;
-};
-
-// Per-CTA plan in shared memory.  Once build_plan returns, offsets are BYTES.
-struct Plan {
-  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = rb * sum_{q<r} S[q][p]; [p][W] = bytes p receives
-  long long in_off[kMaxW][kMaxW];       // [r][p] = rb * sum_{q<p} S[r][q]
-  long long tile_first[kMaxW + 1];      // first tile of peer p; [W] = number of tiles
-  long long tile;                       // tile size in bytes
-};
-
-__device__ __forceinline__ long long warp_inclusive_scan(long long x, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    long long y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  return x;
-}
-
-__device__ __forceinline__ void record_error(int* status, int code) {
-  atomicCAS(status, 0, code);
-}
-
-// Step 1 of the header comment.  Returns false (in every thread of the CTA)
-// when the splits are invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
-__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
-  const int W = P.W;
-  const long long rb = P.rb;
-  const long long limit = kMaxBytes / ((long long)W * rb);
-
-  int bad = 0;
-  for (int e = tid; e < W * W; e += nt) {
-    const long long s = P.splits[(long long)(e / W) * P.split_stride + e % W];
-    if (s < 0 || s > limit) bad = 1;
-    pl.in_off[e / W][e % W] = s;  // raw S[r][p] until the row scans below
-  }
-  if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
-    return false;
-  }
-
-  // Column scans: lane r holds S[r][p]; out_off[p][r] is its exclusive prefix.
-  for (int p = warp; p < W; p += nwarps) {
-    const long long x = lane < W ? pl.in_off[lane][p] : 0;
-    const long long inc = warp_inclusive_scan(x, lane);
-    if (lane < W) pl.out_off[p][lane] = inc - x;
-    if (lane == 31) {
-      pl.out_off[p][W] = inc;
-      if ((P.out_cap > 0 && inc > P.out_cap) || (P.out[p] == nullptr && inc > 0)) bad = 1;
-    }
-  }
-  __syncthreads();
-  // Row scans, in place: lane p holds S[r][p]; in_off[r][p] is its exclusive prefix.
-  for (int r = warp; r < W; r += nwarps) {
-    const long long x = lane < W ? pl.in_off[r][lane] : 0;
-    const long long inc = warp_inclusive_scan(x, lane);
-    if (lane < W) pl.in_off[r][lane] = inc - x;
-    if (lane == 31) {
-      if ((P.in_cap > 0 && inc > P.in_cap) || (P.in[r] == nullptr && inc > 0)) bad = 1;
-    }
-  }
-  if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
-    return false;
-  }
-
-  // Tiles: peer p's received stream (out_off[p][W] * rb bytes) is cut into
-  // ceil(bytes / tile) tiles; tile_first is their exclusive prefix.
-  if (warp == 0) {
-    const long long bytes = lane < W ? pl.out_off[lane][W] * rb : 0;
-    const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
-    const long long per_cta =
-        (total + kTilesPerCta * gridDim.x - 1) / (kTilesPerCta * gridDim.x);
-    long long tile = (per_cta + kTileGranule - 1) / kTileGranule * kTileGranule;
-    tile = tile < kTileGranule ? kTileGranule : (tile > max_tile ? max_tile : tile);
-    const long long n = (bytes + tile - 1) / tile;
-    const long long inc = warp_inclusive_scan(n, lane);
-    if (lane < W) pl.tile_first[lane] = inc - n;
-    if (lane == 31) {
-      pl.tile_first[W] = inc;
-      pl.tile = tile;
-    }
-  }
-  __syncthreads();
-
-  if (blockIdx.x == 0) {
-    for (int e = tid; e < W * W; e += nt) {
-      const int p = e / W, r = e % W;
-      long long* so = P.out_so + (long long)p * 2 * W;
-      so[r] = pl.out_off[p][r + 1] - pl.out_off[p][r];
-      so[W + r] = pl.out_off[p][r];
-    }
-  }
-  __syncthreads();
-  // From here on the tables hold bytes.
-  for (int e = tid; e < W * (W + 1); e += nt) pl.out_off[e / (W + 1)][e % (W + 1)] *= rb;
-  for (int e = tid; e < W * W; e += nt) pl.in_off[e / W][e % W] *= rb;
-  __syncthreads();
-  return true;
-}
-
-// Tile t -> peer p and the byte range [lo, hi) of out[p] it covers (all
-// threads of the caller compute the same).
-__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long* lo,
-                                         long long* hi) {
-  int p = 0;
-  while (p + 1 < W && pl.tile_first[p + 1] <= t) ++p;
-  *lo = (t - pl.tile_first[p]) * pl.tile;
-  const long long end = *lo + pl.tile;
-  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
-  return p;
-}
-
-// The same for a whole warp at once: the largest p with tile_first[p] <= t
-// (peers without tiles share their successor's tile_first, so the largest
-// such p is the one that owns tile t).
-__device__ __forceinline__ int tile_peer_warp(const Plan& pl, int W, long long t, int lane,
-                                              long long* lo, long long* hi) {
-  const unsigned m = __ballot_sync(kFull, lane < W && pl.tile_first[lane] <= t);
-  const int p = 31 - __clz(m);
-  *lo = (t - pl.tile_first[p]) * pl.tile;
-  const long long end = *lo + pl.tile;
-  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
-  return p;
-}
-
-// Lane r's part of the tile [lo, hi) of peer p: the destination offset a, the
-// byte count n (0 when source r contributes nothing) and the source address.
-__device__ __forceinline__ long long lane_segment(const Params& P, const Plan& pl, int W, int p,
-                                                  int r, long long lo, long long hi, long long* a,
-                                                  const unsigned char** src) {
-  *a = 0;
-  *src = nullptr;
-  if (r >= W) return 0;
-  const long long c_lo = pl.out_off[p][r], c_hi = pl.out_off[p][r + 1];
-  const long long x = lo > c_lo ? lo : c_lo, y = hi < c_hi ? hi : c_hi;
-  if (x >= y) return 0;
-  *a = x;
-  *src = P.in[r] + pl.in_off[r][p] + (x - c_lo);
-  return y - x;
-}
-
-// ------------------------------------------------------- memory helpers --
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ void st_stream(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(a));
-  return v;
-}
-
-__device__ __forceinline__ unsigned char lds8(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
-  return (unsigned char)v;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Bytes [s, s + 16) of the 32-byte little-endian concatenation a:b, where
-// s = 4*Q + r8/8.
-template <int Q>
-__device__ __forceinline__ uint4 extract16(const uint4& a, const uint4& b, unsigned r8) {
-  const unsigned w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  uint4 o;
-  o.x = __funnelshift_r(w[Q + 0], w[Q + 1], r8);
-  o.y = __funnelshift_r(w[Q + 1], w[Q + 2], r8);
-  o.z = __funnelshift_r(w[Q + 2], w[Q + 3], r8);
-  o.w = __funnelshift_r(w[Q + 3], w[Q + 4], r8);
-  return o;
-}
-
-// ------------------------------------------------------------ mbarriers --
-__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-// Bounded wait for phase `parity` of the mbarrier; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
-  const long long start = clock64();
-  for (;;) {
-    unsigned done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-    if (clock64() - start > kWaitCycles) return false;
-  }
-}
-
-// Every lane of the warp waits (so each one observes the phase, and the data
-// it guards); the warp agrees on the outcome, so a timeout is warp-uniform.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, unsigned parity) {
-  const bool ok = mbar_wait(bar, parity);
-  return __all_sync(kFull, ok) != 0;
-}
-
-__device__ __forceinline__ void mbar_fence_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t policy;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
-  return policy;
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst_smem, const void* src, unsigned bytes,
-                                          uint32_t bar) {
-  if (A2AV_L2_HINT & 1) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(dst_smem),
-        "l"(src), "r"(bytes), "r"(bar), "l"(evict_first_policy())
-        : "memory");
-  } else {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst_smem),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-  }
-}
-
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src_smem, unsigned bytes) {
-  if (A2AV_L2_HINT & 2) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
-                     "l"(dst),
-                 "r"(src_smem), "r"(bytes), "l"(evict_first_policy())
-                 : "memory");
-  } else {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                 "r"(src_smem), "r"(bytes)
-                 : "memory");
-  }
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- vector --
-// nv 16-byte vectors, source and destination both 16-byte aligned.
-template <int NT, int U>
-__device__ __forceinline__ void copy_aligned(uint4* dst, const uint4* src, long long nv, int tid) {
-  for (long long base = 0; base < nv; base += (long long)NT * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long i = base + (long long)u * NT + tid;
-      if (i < nv) v[u] = ld_stream(src + i);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long i = base + (long long)u * NT + tid;
-      if (i < nv) st_stream(dst + i, v[u]);
-    }
-  }
-}
-
-// nv destination-aligned vectors whose source starts 4*Q + r8/8 bytes
-// (1..15) past the aligned granule `src`: vector i is built from source
-// granules i and i + 1.  A warp owns 32*U consecutive vectors per pass, lane
-// l of step u holding vector 32*u + l, so granule i + 1 is the next lane's
-// granule i, or for lane 31 lane 0's granule of step u + 1: one rotated
-// shuffle per step delivers both.  Only lane 31 of the last step and the
-// last vector of the span load their second granule themselves.
-template <int NT, int U, int Q>
-__device__ __forceinline__ void copy_shifted(uint4* dst, const uint4* src, long long nv,
-                                             unsigned r8, int tid) {
-  const int lane = tid & 31, warp = tid >> 5;
-  for (long long base = 0; base < nv; base += (long long)NT * U) {
-    const long long wbase = base + (long long)warp * 32 * U + lane;
-    uint4 a[U];
-    uint4 extra = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long i = wbase + 32 * u;
-      a[u] = make_uint4(0, 0, 0, 0);
-      if (i < nv) {
-        a[u] = ld_stream(src + i);
-        if (i == nv - 1 || (lane == 31 && u == U - 1)) extra = ld_stream(src + i + 1);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long i = wbase + 32 * u;
-      const uint4 give = (u + 1 < U && lane == 0) ? a[u + 1 < U ? u + 1 : u] : a[u];
-      uint4 n;
-      n.x = __shfl_sync(kFull, give.x, lane + 1);
-      n.y = __shfl_sync(kFull, give.y, lane + 1);
-      n.z = __shfl_sync(kFull, give.z, lane + 1);
-      n.w = __shfl_sync(kFull, give.w, lane + 1);
-      if (i < nv) {
-        const bool own = i == nv - 1 || (lane == 31 && u == U - 1);
-        st_stream(dst + i, extract16<Q>(a[u], own ? extra : n, r8));
-      }
-    }
-  }
-}
-
-// n bytes from s to d, any alignment, by all NT threads of the CTA.
-template <int NT, int U, int US>
-__device__ __forceinline__ void copy_span(unsigned char* d, const unsigned char* s, long long n,
-                                          int tid) {
-  long long head = (16 - (long long)((uintptr_t)d & 15)) & 15;
-  if (head > n) head = n;
-  if (tid < head) d[tid] = __ldg(s + tid);
-  d += head;
-  s += head;
-  n -= head;
-  const long long nv = n >> 4;
-  const int tail = (int)(n & 15);
-  if (tid < tail) d[nv * 16 + tid] = __ldg(s + nv * 16 + tid);
-  if (nv == 0) return;
-  uint4* dv = reinterpret_cast<uint4*>(d);
-  const unsigned shift = (unsigned)((uintptr_t)s & 15);
-  if (shift == 0) {
-    copy_aligned<NT, U>(dv, reinterpret_cast<const uint4*>(s), nv, tid);
-    return;
-  }
-  const uint4* sa = reinterpret_cast<const uint4*>(s - shift);
-  const unsigned r8 = (shift & 3) * 8;
-  switch (shift >> 2) {
-    case 0: copy_shifted<NT, US, 0>(dv, sa, nv, r8, tid); break;
-    case 1: copy_shifted<NT, US, 1>(dv, sa, nv, r8, tid); break;
-    case 2: copy_shifted<NT, US, 2>(dv, sa, nv, r8, tid); break;
-    default: copy_shifted<NT, US, 3>(dv, sa, nv, r8, tid); break;
-  }
-}
 
 template <int NT, int U, int US>
 __global__ void __launch_bounds__(NT, kVecCtasPerSm)
@@ -760,16 +359,6 @@ __global__ void __launch_bounds__(32 * (NC + 1))
 }  // namespace
 
 // ================================================================ host ABI ==
-struct a2av_handle {
-  int W;
-  long long in_cap, out_cap;
-  int device;
-  int sms;
-  int* d_status;
-  int path;         // a2av_path_t
-  int ctas_per_sm;  // 0 = engine default
-  int last_path, last_grid, last_block;
-};
 
 namespace {
 

@@ -1,0 +1,13 @@
+// a2av_handle.h -- the opaque handle behind include/a2av.h (host side only).
+#pragma once
+
+struct a2av_handle {
+  int W;
+  long long in_cap, out_cap;  // rows, 0 = unchecked
+  int device;
+  int sms;
+  int* d_status;              // device status word (first device-detected error)
+  int path;                   // a2av_path_t
+  int ctas_per_sm;            // 0 = engine default
+  int last_path, last_grid, last_block;
+};

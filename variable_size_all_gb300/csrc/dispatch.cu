@@ -1,0 +1,338 @@
+// dispatch.cu -- fused dispatch preparation for the variable-size all-to-all:
+// the exchange of rows that are not yet grouped by destination (declared in
+// include/a2av.h, a2av_dispatch).
+//
+// Each rank's items carry a key (destination = key / K) and a source row.
+// The exchange runs on the rank's items ordered stably by key -- the input
+// a2av_run would expect -- without ever materialising that order:
+//   1. count  (grid ranges x W, 256 threads): per range of 256 items, the key
+//      histogram in shared memory; keys and source rows are validated here.
+//   2. scan   (grid W, 1024 threads): per rank, the exclusive prefix of every
+//      key's count over the ranges (in place), the key start offsets and the
+//      split matrix row S[r][*].
+//   3. rank   (grid ranges x W, one warp): items of a range in order, 32 at a
+//      time; __match_any_sync groups equal keys, a lane's rank among them
+//      plus the running count of its key gives its stable position.
+//   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
+//      prologue), then gather every item's row straight into its place in
+//      the output of its destination; a warp per row for rows of 64 bytes or
+//      more, a thread per row below.
+// A workspace flag, cleared first, stops every later kernel once a kernel has
+// found invalid input, so nothing is written on an error.
+#include "a2av_device.cuh"
+#include "a2av_handle.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+namespace {
+
+constexpr int kRange = 256;                       // items per histogram range
+constexpr int kMaxBins = A2AV_MAX_DISPATCH_KEYS;  // W * K at most
+constexpr int kScanThreads = 1024;
+constexpr int kCopyThreads = 256;
+constexpr int kCopyCtasPerSm = 4;
+constexpr long long kWarpRowBytes = 64;  // rows this long get a warp each
+
+struct DispatchParams {
+  const int* key[kMaxW];
+  const int* src[kMaxW];
+  long long* sorted_pos[kMaxW];
+  long long items[kMaxW];           // m_r
+  long long rows[kMaxW];            // source rows per rank
+  long long item_first[kMaxW + 1];  // exclusive prefix of m_r
+  int* flag;                        // workspace: set once input is found invalid
+  long long* S;                     // workspace: [W][W]
+  long long* key_start;             // workspace: [W][NB]
+  int* hist;                        // workspace: [W][ranges_max][NB]
+  int* status;
+  long long* in_splits_out;         // optional [W][W]
+  long long ranges_max;
+  long long out_cap;
+  unsigned out_null;                // bit p: out[p] is NULL
+  unsigned in_null;                 // bit r: rows of rank r are NULL
+  int W, K;
+};
+
+__device__ __forceinline__ bool flagged(const DispatchParams& D) {
+  return *reinterpret_cast<volatile int*>(D.flag) != 0;
+}
+
+__device__ __forceinline__ void fail(const DispatchParams& D, int code) {
+  atomicExch(D.flag, 1);
+  record_error(D.status, code);
+}
+
+__global__ void __launch_bounds__(kRange) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
+  const int r = blockIdx.y;
+  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
+  if (i0 >= m) return;
+  __shared__ int hist[kMaxBins];
+  const int NB = D.W * D.K;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0;
+  __syncthreads();
+  const long long i = i0 + threadIdx.x;
+  if (i < m) {
+    const int key = D.key[r][i], src = D.src[r][i];
+    if (key < 0 || key >= NB || src < 0 || src >= D.rows[r])
+      fail(D, A2AV_ERR_BAD_INDEX);
+    else
+      atomicAdd(&hist[key], 1);
+  }
+  __syncthreads();
+  int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
+  for (int b = threadIdx.x; b < NB; b += blockDim.x) H[b] = hist[b];
+}
+
+// Per rank: H[j][b] becomes the number of items with key b in ranges < j;
+// key_start[b] = items with a smaller key; S[r][p] = items with key / K = p.
+// Thread (g, b) sums key b over its group g of consecutive ranges, the groups
+// are scanned per key, then each thread rewrites its ranges.
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __grid_constant__ DispatchParams D) {
+  if (flagged(D)) return;
+  const int r = blockIdx.x, NB = D.W * D.K, t = threadIdx.x, lane = t & 31;
+  const long long R = (D.items[r] + kRange - 1) / kRange;
+  int* H = D.hist + (long long)r * D.ranges_max * NB;
+  __shared__ long long part[kScanThreads];
+  __shared__ long long total[kMaxBins];
+  const int G = kScanThreads / NB;
+  const int b = t % NB, g = t / NB;
+  const long long per = (R + G - 1) / G;
+  const long long j0 = g * per, j1 = j0 + per < R ? j0 + per : R;
+  if (g < G) {
+    long long sum = 0;
+    for (long long j = j0; j < j1; ++j) sum += H[j * NB + b];
+    part[g * NB + b] = sum;
+  }
+  __syncthreads();
+  if (t < NB) {
+    long long run = 0;
+    for (int q = 0; q < G; ++q) {
+      const long long x = part[q * NB + t];
+      part[q * NB + t] = run;
+      run += x;
+    }
+    total[t] = run;
+  }
+  __syncthreads();
+  if (g < G) {
+    long long run = part[g * NB + b];
+    for (long long j = j0; j < j1; ++j) {
+      const int x = H[j * NB + b];
+      H[j * NB + b] = (int)run;
+      run += x;
+    }
+  }
+  if (t < 32) {
+    // key starts: lane l scans keys [32 l, 32 l + 32), lanes chained by a warp scan
+    const int k0 = lane * 32, k1 = k0 + 32 < NB ? k0 + 32 : NB;
+    long long local = 0;
+    for (int k = k0; k < k1; ++k) local += total[k];
+    long long run = warp_inclusive_scan(local, lane) - local;
+    for (int k = k0; k < k1; ++k) {
+      D.key_start[(long long)r * NB + k] = run;
+      run += total[k];
+    }
+  }
+  if (t < D.W) {
+    long long s = 0;
+    for (int k = 0; k < D.K; ++k) s += total[t * D.K + k];
+    D.S[(long long)r * D.W + t] = s;
+  }
+}
+
+__global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
+  if (flagged(D)) return;
+  const int r = blockIdx.y, lane = threadIdx.x, W = D.W, NB = W * D.K;
+  // Capacity and NULL-buffer checks on the complete split matrix: every CTA
+  // reaches the same verdict before any position is written.
+  bool bad = false;
+  for (int p = lane; p < W; p += 32) {
+    long long col = 0;
+    for (int q = 0; q < W; ++q) col += D.S[(long long)q * W + p];
+    if ((D.out_cap > 0 && col > D.out_cap) || (((D.out_null >> p) & 1u) && col > 0)) bad = true;
+  }
+  for (int q = lane; q < W; q += 32)
+    if (((D.in_null >> q) & 1u) && D.items[q] > 0) bad = true;
+  if (__any_sync(kFull, bad)) {
+    if (lane == 0) fail(D, A2AV_ERR_BAD_SPLITS);
+    return;
+  }
+  if (blockIdx.x == 0 && r == 0 && D.in_splits_out != nullptr)
+    for (int e = lane; e < W * W; e += 32) D.in_splits_out[e] = D.S[e];
+
+  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
+  if (i0 >= m) return;
+  __shared__ long long next[kMaxBins];  // next position of each key in this range
+  const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
+  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + H[k];
+  __syncwarp();
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    const bool valid = i < m;
+    const int key = valid ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
+    const unsigned same = __match_any_sync(kFull, key);
+    long long pos = 0;
+    if (valid) pos = next[key] + __popc(same & ((1u << lane) - 1u));
+    __syncwarp();
+    if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
+    __syncwarp();
+    if (valid) D.sorted_pos[r][i] = pos;
+  }
+}
+
+// A row of n bytes, any alignment, copied by one thread.
+__device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned char* s,
+                                                long long n) {
+  const uintptr_t a = (uintptr_t)d | (uintptr_t)s | (uintptr_t)n;
+  if ((a & 7) == 0) {
+    for (long long k = 0; k < n; k += 8)
+      *reinterpret_cast<unsigned long long*>(d + k) =
+          __ldg(reinterpret_cast<const unsigned long long*>(s + k));
+  } else if ((a & 3) == 0) {
+    for (long long k = 0; k < n; k += 4)
+      *reinterpret_cast<unsigned*>(d + k) = __ldg(reinterpret_cast<const unsigned*>(s + k));
+  } else {
+    for (long long k = 0; k < n; ++k) d[k] = __ldg(s + k);
+  }
+}
+
+__global__ void __launch_bounds__(kCopyThreads)
+    dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  if (flagged(D)) return;
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, kTileGranule)) return;
+  const int W = D.W, K = D.K;
+  const long long rb = P.rb, total = D.item_first[W];
+  const bool warp_rows = rb >= kWarpRowBytes;
+  const long long team = warp_rows ? (long long)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5)
+                                   : (long long)blockIdx.x * kCopyThreads + threadIdx.x;
+  const long long teams = warp_rows ? (long long)gridDim.x * (kCopyThreads / 32)
+                                    : (long long)gridDim.x * kCopyThreads;
+  for (long long g = team; g < total; g += teams) {
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    const long long i = g - D.item_first[r];
+    const int p = D.key[r][i] / K;
+    const long long pos = D.sorted_pos[r][i];
+    unsigned char* dst = P.out[p] + pl.out_off[p][r] + (pos * rb - pl.in_off[r][p]);
+    const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
+    if (warp_rows)
+      copy_span<32, 4, 2>(dst, src, rb, threadIdx.x & 31);
+    else
+      copy_row_thread(dst, src, rb);
+  }
+}
+
+struct Layout {
+  long long flag, S, key_start, hist, total;
+};
+
+Layout layout(int W, int K, long long ranges_max) {
+  auto up = [](long long x) { return (x + 255) / 256 * 256; };
+  const long long NB = (long long)W * K;
+  Layout L;
+  L.flag = 0;
+  L.S = 256;
+  L.key_start = L.S + up(8LL * W * W);
+  L.hist = L.key_start + up(8LL * W * NB);
+  L.total = L.hist + up(4LL * W * (ranges_max < 1 ? 1 : ranges_max) * NB);
+  return L;
+}
+
+}  // namespace
+
+extern "C" int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
+                                                 int64_t max_items_per_rank) {
+  if (world_size < 1 || world_size > kMaxW || keys_per_peer < 1 || max_items_per_rank < 0 ||
+      (long long)world_size * keys_per_peer > kMaxBins || max_items_per_rank > 0x7fffffffLL)
+    return -1;
+  return layout(world_size, keys_per_peer, (max_items_per_rank + kRange - 1) / kRange).total;
+}
+
+extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* const* rows_ptrs,
+                             const int64_t* rows_per_rank, const int32_t* const* src_row_ptrs,
+                             const int32_t* const* key_ptrs, const int64_t* items_per_rank,
+                             void* const* out_ptrs, int64_t* out_splits_offsets_dev,
+                             int64_t* const* sorted_pos_ptrs, int64_t* in_splits_dev,
+                             int64_t row_bytes, void* workspace, int64_t workspace_bytes,
+                             void* stream) {
+  if (h == nullptr || rows_ptrs == nullptr || rows_per_rank == nullptr || src_row_ptrs == nullptr ||
+      key_ptrs == nullptr || items_per_rank == nullptr || out_ptrs == nullptr ||
+      out_splits_offsets_dev == nullptr || sorted_pos_ptrs == nullptr || workspace == nullptr ||
+      row_bytes < 1 || keys_per_peer < 1)
+    return A2AV_ERR_INVALID_ARG;
+  const int W = h->W, K = keys_per_peer;
+  if ((long long)W * K > kMaxBins) return A2AV_ERR_UNSUPPORTED;
+  if (((uintptr_t)workspace & 255) != 0 || ((uintptr_t)out_splits_offsets_dev & 7) != 0 ||
+      ((uintptr_t)in_splits_dev & 7) != 0)
+    return A2AV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (dev != h->device) return A2AV_ERR_INVALID_ARG;
+
+  DispatchParams D;
+  std::memset(&D, 0, sizeof(D));
+  long long ranges_max = 0;
+  D.item_first[0] = 0;
+  for (int r = 0; r < W; ++r) {
+    const long long m = items_per_rank[r], n = rows_per_rank[r];
+    if (m < 0 || n < 0) return A2AV_ERR_INVALID_ARG;
+    if (m > 0x7fffffffLL || n > 0x7fffffffLL) return A2AV_ERR_UNSUPPORTED;
+    if (m > 0 && (key_ptrs[r] == nullptr || src_row_ptrs[r] == nullptr ||
+                  sorted_pos_ptrs[r] == nullptr))
+      return A2AV_ERR_INVALID_ARG;
+    D.key[r] = key_ptrs[r];
+    D.src[r] = src_row_ptrs[r];
+    D.sorted_pos[r] = reinterpret_cast<long long*>(sorted_pos_ptrs[r]);
+    D.items[r] = m;
+    D.rows[r] = n;
+    D.item_first[r + 1] = D.item_first[r] + m;
+    const long long R = (m + kRange - 1) / kRange;
+    ranges_max = R > ranges_max ? R : ranges_max;
+    if (out_ptrs[r] == nullptr) D.out_null |= 1u << r;
+    if (rows_ptrs[r] == nullptr) D.in_null |= 1u << r;
+  }
+  const Layout L = layout(W, K, ranges_max);
+  if (workspace_bytes < L.total) return A2AV_ERR_INVALID_ARG;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  D.flag = reinterpret_cast<int*>(ws + L.flag);
+  D.S = reinterpret_cast<long long*>(ws + L.S);
+  D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
+  D.hist = reinterpret_cast<int*>(ws + L.hist);
+  D.status = h->d_status;
+  D.in_splits_out = reinterpret_cast<long long*>(in_splits_dev);
+  D.ranges_max = ranges_max;
+  D.out_cap = h->out_cap;
+  D.W = W;
+  D.K = K;
+
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  for (int r = 0; r < W; ++r) {
+    P.in[r] = static_cast<const unsigned char*>(rows_ptrs[r]);
+    P.out[r] = static_cast<unsigned char*>(out_ptrs[r]);
+  }
+  P.splits = D.S;
+  P.split_stride = W;
+  P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
+  P.status = h->d_status;
+  P.rb = row_bytes;
+  P.in_cap = 0;  // sources are checked by row index in the count kernel
+  P.out_cap = h->out_cap;
+  P.W = W;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(D.flag, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (ranges_max > 0) {
+    const dim3 grid((unsigned)ranges_max, (unsigned)W);
+    dispatch_count_kernel<<<grid, kRange, 0, s>>>(D);
+  }
+  dispatch_scan_kernel<<<W, kScanThreads, 0, s>>>(D);
+  dispatch_rank_kernel<<<dim3((unsigned)(ranges_max > 0 ? ranges_max : 1), (unsigned)W), 32, 0, s>>>(D);
+  dispatch_copy_kernel<<<h->sms * kCopyCtasPerSm, kCopyThreads, 0, s>>>(P, D);
+  if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  return A2AV_OK;
+}

@@ -47,6 +47,7 @@ __all__ = [
     "cfg4",
     "cfg5",
     "random_case",
+    "dispatch_items",
     "random_bits",
     "normal_bf16",
     "CFG2_ROW_BYTES",
@@ -207,10 +208,11 @@ def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 6
     logp = np.log(weights / weights.sum())
     rb = hidden * 2
     splits = np.zeros((W, W), dtype=np.int64)
-    inputs, routes = [], []
+    inputs, routes, token_rows, choices = [], [], [], []
     for r in range(W):
         scores = logp[None, :] + rng.gumbel(size=(tokens, experts))
         chosen = np.argsort(-scores, axis=1, kind="stable")[:, :topk]  # [tokens, topk]
+        choices.append(chosen.astype(np.int64))
         tok = np.repeat(np.arange(tokens), topk)
         exp = chosen.reshape(-1)
         dest, local = exp // per_rank, exp % per_rank
@@ -221,9 +223,10 @@ def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 6
         normal_bf16(x, (seed, 3, r))
         inputs.append(np.ascontiguousarray(x[tok]).view(np.uint8).reshape(-1))
         routes.append((tok.astype(np.int64), exp.astype(np.int64)))
+        token_rows.append(x.view(np.uint8).reshape(-1))
     return Workload("cfg3", W, rb, splits, inputs,
                     {"tokens": tokens, "experts": experts, "topk": topk, "routes": routes,
-                     "expert_weight": weights})
+                     "expert_weight": weights, "token_rows": token_rows, "choices": choices})
 
 
 def cfg4(seed: int = 0, rows: int = 1 << 20, row_bytes: int = 13, alpha: float = 0.1,
@@ -252,11 +255,12 @@ def cfg5(seed: int = 0, features: int = 26, batch: int = 8192, lam: float = 3.0,
     """
     rng = np.random.default_rng(np.random.SeedSequence([seed, 5]))
     splits = np.zeros((W, W), dtype=np.int64)
-    inputs, lengths = [], []
+    inputs, lengths, kjt = [], [], []
     for r in range(W):
         L = np.minimum(rng.poisson(lam, size=(features, batch)), max_len).astype(np.int64)
         per_feature = L.sum(axis=1)
         keys = rng.integers(0, key_max, size=int(per_feature.sum()), dtype=np.int64)
+        kjt.append(keys)
         starts = np.concatenate([[0], np.cumsum(per_feature)])
         blocks = []
         for p in range(W):
@@ -266,7 +270,43 @@ def cfg5(seed: int = 0, features: int = 26, batch: int = 8192, lam: float = 3.0,
         inputs.append(np.concatenate(blocks).view(np.uint8))
         lengths.append(L)
     return Workload("cfg5", W, 8, splits, inputs,
-                    {"features": features, "batch": batch, "lengths": lengths})
+                    {"features": features, "batch": batch, "lengths": lengths, "kjt_keys": kjt})
+
+
+def dispatch_items(w: Workload):
+    """Unsorted items for the fused dispatch of an MoE or embedding-key workload.
+
+    Returns (K, rows, src_rows, keys): per rank, the source rows as bytes and,
+    per item, its source row and its key (destination = key // K).
+      cfg3: items (token t, choice k) in token-major order, source row t, key =
+            the chosen expert (K = experts per rank).
+      cfg5: items = the keys in feature-major (feature, bag, position) order,
+            each its own source row; key = (f mod W) * ceil(F / W) + f // W,
+            so that keys order items by (owner, feature).
+    Ordering each rank's items stably by key gives exactly ``w.inputs``.
+    """
+    W = w.W
+    if w.name == "cfg3":
+        K = w.meta["experts"] // W
+        rows = w.meta["token_rows"]
+        src, key = [], []
+        for ch in w.meta["choices"]:
+            tokens, topk = ch.shape
+            src.append(np.repeat(np.arange(tokens, dtype=np.int32), topk))
+            key.append(ch.reshape(-1).astype(np.int32))
+        return K, rows, src, key
+    if w.name == "cfg5":
+        F = w.meta["features"]
+        K = -(-F // W)
+        rows, src, key = [], [], []
+        for r in range(W):
+            per_feature = w.meta["lengths"][r].sum(axis=1)
+            f = np.repeat(np.arange(F), per_feature)
+            rows.append(w.meta["kjt_keys"][r].view(np.uint8))
+            src.append(np.arange(f.size, dtype=np.int32))
+            key.append(((f % W) * K + f // W).astype(np.int32))
+        return K, rows, src, key
+    raise ValueError(f"{w.name} has no dispatch items")
 
 
 def random_case(seed: int, W: int, row_bytes: int, max_rows: int = 64, mode: str = "uniform") -> Workload:
