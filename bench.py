@@ -184,8 +184,13 @@ def hbm_peak():
 
 
 def kernel_source_sha() -> str:
-    src = os.path.join(ROOT, "variable_size_all_gb300", "csrc", "a2av.cu")
-    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    """Hash of every CUDA source the kernels are built from."""
+    csrc = os.path.join(ROOT, "variable_size_all_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel: str, algo_bytes: int):
@@ -528,6 +533,226 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------ fused dispatch ----
+def _timed(torch, stream, fn, reps, cold, flush):
+    """Median and mean CUDA-event time of fn over reps launches (seconds)."""
+    ts = []
+    for _ in range(reps):
+        if cold:
+            flush.sum()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    return statistics.median(ts), statistics.mean(ts)
+
+
+def run_fused_dispatch(args):
+    """a2av_dispatch on unsorted MoE or embedding-key items, against the
+    unfused path (torch stable sort + row gather, then a2av_run)."""
+    import torch
+    import variable_size_all_gb300 as a2av
+    import workloads as wl
+    import oracle
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    a2av.build()
+    if args.workload not in ("cfg3", "cfg5"):
+        raise SystemExit("--op fused_dispatch needs --workload cfg3 or cfg5")
+    w = {"cfg3": wl.cfg3, "cfg5": wl.cfg5}[args.workload](args.seed)
+    K, rows, src, key = wl.dispatch_items(w)
+    Wn, rb, S = w.W, w.row_bytes, w.splits
+    m = [k.size for k in key]
+    T = moved_bytes(S, rb)
+    d_rows = [torch.from_numpy(r).to(dev) for r in rows]
+    d_src = [torch.from_numpy(x).to(dev) for x in src]
+    d_key = [torch.from_numpy(x).to(dev) for x in key]
+    d_pos = [torch.empty(x, dtype=torch.int64, device=dev) for x in m]
+    recv = [int(S[:, p].sum()) * rb for p in range(Wn)]
+    d_out = [torch.empty(n, dtype=torch.uint8, device=dev) for n in recv]
+    d_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, device=dev)
+    eng = a2av.A2av(Wn)
+    stream = torch.cuda.current_stream()
+    cold = sum(r.size for r in rows) < 2 * L2_BYTES
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+
+    def fused():
+        eng.dispatch(d_rows, d_src, d_key, K, d_out, d_so, d_pos, rb, stream=stream)
+
+    u_out = [torch.empty_like(t) for t in d_out]
+    u_so = torch.empty_like(d_so)
+
+    def unfused():
+        gathered, counts = [], []
+        for r in range(Wn):
+            order = torch.sort(d_key[r], stable=True).indices
+            gathered.append(d_rows[r].view(-1, rb).index_select(0, d_src[r][order]).view(-1))
+            counts.append(torch.bincount(d_key[r] // K, minlength=Wn))
+        splits = torch.stack(counts).to(torch.int64)
+        eng.run(gathered, splits, u_out, u_so, rb, stream=stream)
+
+    for _ in range(args.warmup):
+        fused()
+        unfused()
+    torch.cuda.synchronize()
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during warm-up")
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        f_med, f_mean = _timed(torch, stream, fused, args.steps, cold, flush)
+        torch.cuda.synchronize()
+        barrier()
+    u_med, u_mean = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during the timed region")
+    max_s = reduce_max(f_mean, dev)
+    value = whole_job_value(T / 1e9, world, max_s)
+    # ideal traffic: every distinct source row read once (a token routed to
+    # two experts is read once), every moved row written once, each item's
+    # key and source row read once and its position written once
+    items = sum(m)
+    distinct = sum(int(np.unique(x).size) for x in src) * rb
+    algo = distinct + T + items * (4 + 4 + 8) + 24 * Wn * Wn
+    peak, peak_kind = hbm_peak()
+    roofline = {"bound": "hbm", "kernel": "a2av_dispatch (4 launches: count, scan, rank, copy)",
+                "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
+                "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
+                "traffic": measured_traffic("dispatch_copy_kernel:" + args.workload, algo),
+                "algorithmic_bytes_per_launch": algo}
+    cpu = parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        ref, ref_so, ref_pos, _ = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+        spent = time.perf_counter() - t0
+        ok = all(np.array_equal(d_out[p].cpu().numpy(), ref[p]) for p in range(Wn))
+        ok = ok and np.array_equal(d_so.cpu().numpy(), ref_so)
+        ok = ok and all(np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r]) for r in range(Wn))
+        ok = ok and all(torch.equal(u_out[p], d_out[p]) for p in range(Wn))
+        parity = {"bit_exact": bool(ok), "check": "outputs, offsets and positions equal the "
+                                                  "oracle's; the unfused path agrees"}
+        cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "the whole fused dispatch of the same workload", "seconds": round(spent, 3)}
+        if not ok:
+            raise SystemExit("fused dispatch differs from the oracle")
+    eng.close()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws; no dataset)",
+        "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed) +
+                   " -- items unsorted (token-major / feature-major), grouped on the device",
+                   "name": args.workload, "op": "fused_dispatch", "ranks": Wn, "row_bytes": rb,
+                   "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
+                   "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
+                          "inputs larger than L2"),
+                   "timing": "CUDA events around the 4-launch dispatch, mean over steps"},
+        "unfused_torch_sort_gather_a2av": {"ms_mean": round(u_mean * 1e3, 4),
+                                           "ms_median": round(u_med * 1e3, 4),
+                                           "value": round(T / u_mean / 1e9, 2), "unit": UNIT},
+        "fused_ms_median": round(f_med * 1e3, 4),
+        "speedup_vs_unfused": round(u_mean / f_mean, 3),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(), "parity": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------- overlap ----
+def run_overlap(args):
+    """The exchange on a side stream while a bf16 GEMM runs on the main one:
+    each alone, then both at once (the separate-stream idea of torchrec PR
+    2570, measured here as HBM interference inside one GPU)."""
+    import torch
+    import variable_size_all_gb300 as a2av
+    import workloads as wl
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    a2av.build()
+    w = wl.cfg3(args.seed) if args.workload == "cfg3" else None
+    if w is None:
+        raise SystemExit("--op overlap runs the MoE exchange: --workload cfg3")
+    Wn, rb, S = w.W, w.row_bytes, w.splits
+    T = moved_bytes(S, rb)
+    d_in = [torch.from_numpy(b).to(dev) for b in w.inputs]
+    d_out = [torch.empty(int(S[:, p].sum()) * rb, dtype=torch.uint8, device=dev) for p in range(Wn)]
+    d_S = torch.from_numpy(S).to(dev)
+    d_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, device=dev)
+    n = args.gemm_n
+    A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    B = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    C = torch.empty(n, n, device=dev, dtype=torch.bfloat16)
+    eng = a2av.A2av(Wn)
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    reps = args.steps
+
+    def gemms():
+        for _ in range(reps):
+            torch.matmul(A, B, out=C)
+
+    def exchanges():
+        for _ in range(reps):
+            eng.run(d_in, d_S, d_out, d_so, rb, stream=side)
+
+    def span(fn_main, fn_side):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(main)
+        side.wait_event(a)
+        if fn_main:
+            fn_main()
+        b.record(main)
+        with torch.cuda.stream(side):
+            c.record(side)
+            if fn_side:
+                fn_side()
+            d.record(side)
+        main.wait_stream(side)
+        torch.cuda.synchronize()
+        wall = max(a.elapsed_time(b), a.elapsed_time(d)) / 1e3
+        return a.elapsed_time(b) / 1e3, c.elapsed_time(d) / 1e3, wall
+
+    for _ in range(2):
+        span(gemms, exchanges)
+    g_alone = span(gemms, None)[0]
+    x_alone = span(None, exchanges)[1]
+    with ClockSampler(local) as clocks:
+        g_both, x_both, wall = span(gemms, exchanges)
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error")
+    eng.close()
+    flops = 2.0 * n * n * n * reps
+    line = {
+        "metric": METRIC, "value": round(T * reps / x_both / 1e9, 2), "unit": UNIT,
+        "n_gpus": world, "steps": reps, "warmup": 2, "ms_per_step": round(x_both / reps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic", "config": {"workload": describe("cfg3", 0, args.seed) +
+                                        f" on a side stream, with {reps} bf16 GEMMs "
+                                        f"{n}x{n}x{n} on the main stream", "op": "overlap"},
+        "exchange_alone_GBps": round(T * reps / x_alone / 1e9, 2),
+        "exchange_overlapped_GBps": round(T * reps / x_both / 1e9, 2),
+        "gemm_alone_TFLOPs": round(flops / g_alone / 1e12, 1),
+        "gemm_overlapped_TFLOPs": round(flops / g_both / 1e12, 1),
+        "serial_ms": round((g_alone + x_alone) * 1e3, 3), "overlapped_wall_ms": round(wall * 1e3, 3),
+        "overlap_saving": round(1 - wall / (g_alone + x_alone), 4),
+        "gpu_launches": reps, "clocks": clocks.summary(), "roofline": None, "cpu_baseline": None,
+        "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------ reference ----
 def run_reference(args):
     """The CPU oracle as the reference arm: each step runs it on one peer's
@@ -576,8 +801,12 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="cfg2")
-    ap.add_argument("--op", choices=["dispatch", "combine"], default="dispatch",
-                    help="dispatch = a2av_run; combine = a2av_combine on its outputs")
+    ap.add_argument("--op", choices=["dispatch", "combine", "fused_dispatch", "overlap"],
+                    default="dispatch",
+                    help="dispatch = a2av_run; combine = a2av_combine on its outputs; "
+                         "fused_dispatch = a2av_dispatch on unsorted items (cfg3, cfg5); "
+                         "overlap = cfg3 exchange on a side stream beside bf16 GEMMs")
+    ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--per-rank-bytes", type=int, default=1 << 32, help="cfg2 payload per rank")
     ap.add_argument("--path", choices=["auto", "vector", "bulk", "staged"], default="auto")
@@ -592,6 +821,10 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "fused_dispatch":
+        run_fused_dispatch(args)
+    elif args.op == "overlap":
+        run_overlap(args)
     else:
         run_ours(args)
 
