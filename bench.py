@@ -453,12 +453,50 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         e_s = reduce_max(a.elapsed_time(b) / 1e3, dev)
-        e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, e_s), 2), "unit": UNIT,
-               "h2d_bytes_per_step": sum(t.numel() for t in e_src) + e_sp.numel() * 8,
-               "d2h_bytes_per_step": sum(t.numel() for t in h_out) + 2 * Wn * Wn * 8,
-               "steps": Ke}
+        copy_e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, e_s), 2), "unit": UNIT,
+                    "h2d_bytes_per_step": sum(t.numel() for t in e_src) + e_sp.numel() * 8,
+                    "d2h_bytes_per_step": sum(t.numel() for t in h_out) + 2 * Wn * Wn * 8,
+                    "steps": Ke, "mode": "copy: H2D of the inputs and splits, the exchange, "
+                                         "D2H of the outputs and offsets (one stream)"}
         if eng.status() != a2av.OK:
             raise SystemExit("device reported an error during the e2e run")
+        # Zero-copy: the same call with the pinned host buffers themselves; the
+        # kernel reads the inputs and writes the outputs over the host link.
+        zc = a2av.A2av(Wn, path=a2av.PATH_VECTOR, ctas_per_sm=args.ctas_per_sm)
+        for t in h_out:
+            t.fill_(0xEE)
+
+        def zc_step():
+            e_spd.copy_(e_sp, non_blocking=True)
+            (zc.combine if args.op == "combine" else zc.run)(e_src, e_spd, h_out, e_so, rb,
+                                                              stream=stream)
+            h_so.copy_(e_so, non_blocking=True)
+
+        zc_step()
+        torch.cuda.synchronize()
+        zc_ok = all(torch.equal(h_out[k], e_outs[k].cpu()) for k in range(Wn))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(Ke):
+            zc_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        z_s = reduce_max(a.elapsed_time(b) / 1e3, dev)
+        if zc.status() != a2av.OK or not zc_ok:
+            raise SystemExit("zero-copy exchange failed or differs from the device run")
+        zc.close()
+        zero_e2e = {"value": round(whole_job_value(T * Ke / 1e9, world, z_s), 2), "unit": UNIT,
+                    "h2d_bytes_per_step": copy_e2e["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": sum(t.numel() for t in h_out) + 2 * Wn * Wn * 8,
+                    "steps": Ke, "mode": "zero-copy: the exchange reads the pinned host inputs "
+                                         "and writes the pinned host outputs itself (vector "
+                                         "engine over NVLink-C2C); splits H2D",
+                    "bit_exact_vs_device_run": zc_ok}
+        e2e = zero_e2e if zero_e2e["value"] >= copy_e2e["value"] else copy_e2e
+        e2e["other"] = copy_e2e if e2e is zero_e2e else zero_e2e
 
     # ---- CPU oracle: baseline timing and a parity check of this run -------
     cpu = None

@@ -104,7 +104,13 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
  *  stream             cudaStream_t as void*.
  *
  * Memory rules: no output may overlap an input, the split matrix or another
- * output; inputs may share memory.  Bytes of an input past its last chunk are
+ * output; inputs may share memory.  Input and output buffers may also be
+ * pinned host memory that the device can address (zero-copy over the host
+ * link) when the vector engine runs (A2AV_PATH_VECTOR): it reaches every
+ * buffer with plain loads and stores.  The bulk and staged engines use
+ * cp.async.bulk copies, which this library applies to device memory only,
+ * and AUTO does not inspect pointers: request A2AV_PATH_VECTOR for
+ * host-resident buffers (the Python binding does so by itself).  Bytes of an input past its last chunk are
  * never used and bytes of an output past its last received row are never
  * written.  (Whole 16-byte-aligned granules that hold a needed input byte may
  * be loaded and their other bytes discarded; such loads never leave the

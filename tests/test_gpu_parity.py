@@ -214,3 +214,31 @@ def test_dispatch_then_combine_on_device():
     for r in range(W):
         assert torch.equal(back[r], ins[r])
     assert torch.equal(cso[:, 0, :], S)
+
+
+def test_pinned_host_buffers_zero_copy():
+    # inputs and outputs in pinned host memory: the kernel reads and writes
+    # them over the host link (the binding picks the vector engine)
+    import oracle
+    for w in (wl.cfg4(11, rows=1 << 14), wl.cfg1(2)):
+        W, rb = w.W, w.row_bytes
+        ref, ref_so = oracle.default().exchange(w.inputs, w.splits, rb)
+        S = torch.from_numpy(w.splits).cuda()
+        so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+        host_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
+        dev_in = [t.cuda() for t in host_in]
+        for ins in (host_in, dev_in):
+            outs = [torch.full((r.size,), 0xEE, dtype=torch.uint8).pin_memory() for r in ref]
+            with a2av.A2av(W) as eng:
+                eng.run(ins, S, outs, so, rb)
+                assert eng.status() == a2av.OK
+                assert eng.last_launch()["path"] == VEC
+                # the configured engine comes back for device-only calls
+                d_outs = [torch.empty(r.size, dtype=torch.uint8, device="cuda") for r in ref]
+                eng.run(dev_in, S, d_outs, so, rb)
+                assert eng.last_launch()["path"] == (BULK if rb % 16 == 0 else STAGED)
+            torch.cuda.synchronize()
+            for p in range(W):
+                assert np.array_equal(outs[p].numpy(), ref[p])
+                assert np.array_equal(d_outs[p].cpu().numpy(), ref[p])
+            assert np.array_equal(so.cpu().numpy(), ref_so)

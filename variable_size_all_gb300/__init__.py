@@ -202,7 +202,7 @@ class A2av:
         rc, h = a2av_create(world_size, in_capacity_rows, out_capacity_rows)
         if rc != OK:
             raise A2avError(rc, "a2av_create")
-        self.handle, self.world_size = h, int(world_size)
+        self.handle, self.world_size, self._path = h, int(world_size), int(path)
         if path != PATH_AUTO:
             self._check(a2av_set_path(h, path), "a2av_set_path")
         if ctas_per_sm:
@@ -221,49 +221,68 @@ class A2av:
         return int(getattr(stream, "cuda_stream", stream))
 
     def _buffers(self, tensors, what):
-        import torch
-        if len(tensors) != self.world_size:
-            raise ValueError(f"{what}: expected {self.world_size} buffers, got {len(tensors)}")
-        ptrs = []
-        for t in tensors:
+        """Pointer array for W buffers; True when one lives in pinned host memory."""
+        W = self.world_size
+        if len(tensors) != W:
+            raise ValueError(f"{what}: expected {W} buffers, got {len(tensors)}")
+        arr = (ctypes.c_void_p * W)()
+        host = False
+        for k, t in enumerate(tensors):
             if t is None or t.numel() == 0:
-                ptrs.append(0)
                 continue
-            if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
-                raise ValueError(f"{what}: buffers must be contiguous CUDA tensors")
-            ptrs.append(t.data_ptr())
-        return ptrs
+            if not t.is_contiguous():
+                raise ValueError(f"{what}: buffers must be contiguous")
+            if t.is_cuda:
+                arr[k] = t.data_ptr()
+            elif t.is_pinned():
+                arr[k] = t.data_ptr()
+                host = True
+            else:
+                raise ValueError(f"{what}: buffers must be CUDA tensors or pinned host tensors")
+        return arr, host
+
+    @staticmethod
+    def _matrix(t, shape, name):
+        import torch
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.int64 or not t.is_cuda
+                or tuple(t.shape) != shape or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of shape {shape}")
+        return ctypes.c_void_p(t.data_ptr())
+
+    def _launch(self, fn, what, inputs, splits, outputs, out_splits_offsets, row_bytes, stream,
+                split_shape):
+        W = self.world_size
+        sp = self._matrix(splits, split_shape, "splits")
+        so = self._matrix(out_splits_offsets, (W, 2, W), "out_splits_offsets")
+        ins, host_in = self._buffers(inputs, "inputs")
+        outs, host_out = self._buffers(outputs, "outputs")
+        st = ctypes.c_void_p(self._stream(stream) or None)
+        lib = load()
+        if host_in or host_out:
+            # Buffers in pinned host memory are reached with plain loads and
+            # stores (zero-copy over the host link): the vector engine.
+            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
+            try:
+                rc = fn(self.handle, ins, sp, outs, so, int(row_bytes), st)
+            finally:
+                lib.a2av_set_path(self.handle, self._path)
+        else:
+            rc = fn(self.handle, ins, sp, outs, so, int(row_bytes), st)
+        self._check(rc, what)
 
     def run(self, inputs, in_splits, outputs, out_splits_offsets, row_bytes: int, stream=None):
-        import torch
         W = self.world_size
-        for t, shape, name in ((in_splits, (W, W), "in_splits"),
-                               (out_splits_offsets, (W, 2, W), "out_splits_offsets")):
-            if (not isinstance(t, torch.Tensor) or t.dtype != torch.int64 or not t.is_cuda
-                    or tuple(t.shape) != shape or not t.is_contiguous()):
-                raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of shape {shape}")
-        rc = a2av_run(self.handle, self._buffers(inputs, "inputs"), in_splits.data_ptr(),
-                      self._buffers(outputs, "outputs"), out_splits_offsets.data_ptr(),
-                      row_bytes, self._stream(stream))
-        self._check(rc, "a2av_run")
+        self._launch(load().a2av_run, "a2av_run", inputs, in_splits, outputs, out_splits_offsets,
+                     row_bytes, stream, (W, W))
 
     def combine(self, inputs, dispatch_splits_offsets, outputs, out_splits_offsets,
                 row_bytes: int, stream=None):
         """The reverse exchange: send every received chunk back to its source
         rank; ``dispatch_splits_offsets`` is the [W, 2, W] tensor a previous
         ``run`` wrote."""
-        import torch
         W = self.world_size
-        for t, name in ((dispatch_splits_offsets, "dispatch_splits_offsets"),
-                        (out_splits_offsets, "out_splits_offsets")):
-            if (not isinstance(t, torch.Tensor) or t.dtype != torch.int64 or not t.is_cuda
-                    or tuple(t.shape) != (W, 2, W) or not t.is_contiguous()):
-                raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of shape "
-                                 f"{(W, 2, W)}")
-        rc = a2av_combine(self.handle, self._buffers(inputs, "inputs"),
-                          dispatch_splits_offsets.data_ptr(), self._buffers(outputs, "outputs"),
-                          out_splits_offsets.data_ptr(), row_bytes, self._stream(stream))
-        self._check(rc, "a2av_combine")
+        self._launch(load().a2av_combine, "a2av_combine", inputs, dispatch_splits_offsets,
+                     outputs, out_splits_offsets, row_bytes, stream, (W, 2, W))
 
     def dispatch(self, rows, src_rows, keys, keys_per_peer: int, outputs, out_splits_offsets,
                  sorted_pos, row_bytes: int, in_splits=None, workspace=None, stream=None):
@@ -310,8 +329,12 @@ class A2av:
             workspace = ws
         n_rows = [0 if t is None else t.numel() // int(row_bytes) for t in rows]
         ptr = lambda ts: [0 if t is None or t.numel() == 0 else t.data_ptr() for t in ts]
-        rc = a2av_dispatch(self.handle, keys_per_peer, self._buffers(rows, "rows"), n_rows,
-                           ptr(src_rows), ptr(keys), items, self._buffers(outputs, "outputs"),
+        rows_arr, host_rows = self._buffers(rows, "rows")
+        outs_arr, host_outs = self._buffers(outputs, "outputs")
+        if host_rows or host_outs:
+            raise ValueError("a2av_dispatch takes device buffers only")
+        rc = a2av_dispatch(self.handle, keys_per_peer, list(rows_arr), n_rows,
+                           ptr(src_rows), ptr(keys), items, list(outs_arr),
                            out_splits_offsets.data_ptr(), ptr(sorted_pos),
                            0 if in_splits is None else in_splits.data_ptr(), row_bytes,
                            workspace.data_ptr(), workspace.numel(), self._stream(stream))

@@ -132,15 +132,16 @@ __global__ void __launch_bounds__(NT, kVecCtasPerSm)
   if (!build_plan(P, pl, max_tile)) return;
   const int W = P.W, tid = threadIdx.x;
   const long long ntiles = pl.tile_first[W];
+  const long long rb = P.rb;
   for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
     long long lo, hi;
-    const int p = tile_peer(pl, W, t, &lo, &hi);
+    const int p = tile_peer(pl, W, t, rb, &lo, &hi);
     unsigned char* out = P.out[p];
     for (int r = 0; r < W; ++r) {
-      const long long c_lo = pl.out_off[p][r], c_hi = pl.out_off[p][r + 1];
+      const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
       const long long a = lo > c_lo ? lo : c_lo, b = hi < c_hi ? hi : c_hi;
       if (a >= b) continue;
-      const unsigned char* src = P.in[r] + pl.in_off[r][p] + (a - c_lo);
+      const unsigned char* src = P.in[r] + pl.in_off[r][p] * rb + (a - c_lo);
       copy_span<NT, U, US>(out + a, src, b - a, tid);
     }
   }
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(kBulkThreads)
       __syncwarp();
       long long lo, hi, a;
       const unsigned char* src;
-      const int p = tile_peer_warp(pl, W, b0 + k * G, lane, &lo, &hi);
+      const int p = tile_peer_warp(pl, W, b0 + k * G, P.rb, lane, &lo, &hi);
       const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
       const uint32_t bar = bar0 + 8 * s, stage = stage0 + (uint32_t)s * stage_bytes;
       if (lane == 0) {
@@ -304,7 +305,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       long long lo, hi, a;
       const unsigned char* src;
-      const int p = tile_peer_warp(pl, W, b0 + k * G, lane, &lo, &hi);
+      const int p = tile_peer_warp(pl, W, b0 + k * G, P.rb, lane, &lo, &hi);
       const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
       const uintptr_t g_lo = (uintptr_t)src & ~(uintptr_t)15;
       const unsigned gb =
@@ -402,6 +403,7 @@ bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in
   P->out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
   P->status = status;
   P->rb = row_bytes;
+  P->limit = split_limit(W, row_bytes);
   P->in_cap = in_cap;
   P->out_cap = out_cap;
   P->W = W;

@@ -46,17 +46,25 @@ struct Params {
   long long* out_so;        // [W][2][W]
   int* status;
   long long rb;             // row bytes
+  long long limit;          // largest valid split: 2^62 / (W * rb), computed on the host
   long long in_cap;         // rows, 0 = unchecked
   long long out_cap;        // rows, 0 = unchecked
   int W;
 };
 
-// Per-CTA plan in shared memory.  Once build_plan returns, offsets are BYTES.
+// Host side of Params::limit: every byte offset then stays below 2^62.
+inline long long split_limit(int W, long long rb) { return kMaxBytes / ((long long)W * rb); }
+
+// Per-CTA plan in shared memory.  Offsets are in ROWS; callers multiply by the
+// row size where they need bytes.  Tiles are a power of two bytes long.
+// Rows are padded to kMaxW + 1 entries so that lanes reading a column (lane
+// r at [r][k]) hit 32 different shared-memory banks.
 struct Plan {
-  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = rb * sum_{q<r} S[q][p]; [p][W] = bytes p receives
-  long long in_off[kMaxW][kMaxW];       // [r][p] = rb * sum_{q<p} S[r][q]
+  long long s[kMaxW][kMaxW + 1];        // S[r][p] as loaded
+  long long out_off[kMaxW][kMaxW + 1];  // [p][r] = sum_{q<r} S[q][p]; [p][W] = rows p receives
+  long long in_off[kMaxW][kMaxW + 1];   // [r][p] = sum_{q<p} S[r][q]
   long long tile_first[kMaxW + 1];      // first tile of peer p; [W] = number of tiles
-  long long tile;                       // tile size in bytes
+  int tile_shift;                       // tile size = 1 << tile_shift bytes
 };
 
 __device__ __forceinline__ long long warp_inclusive_scan(long long x, int lane) {
@@ -72,44 +80,44 @@ __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
-// Step 1 of the header comment.  Returns false (in every thread of the CTA)
-// when the splits are invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
+// Step 1 of the exchange.  Three barriers: load + range check; column scans
+// (out_off) and row scans (in_off) side by side + capacity checks; tiles and
+// out_splits_offsets.  Returns false (in every thread of the CTA) when the
+// splits are invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
 __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
-  const long long rb = P.rb;
-  const long long limit = kMaxBytes / ((long long)W * rb);
 
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {
-    const long long s = P.splits[(long long)(e / W) * P.split_stride + e % W];
-    if (s < 0 || s > limit) bad = 1;
-    pl.in_off[e / W][e % W] = s;  // raw S[r][p] until the row scans below
+    const int r = e / W, p = e - r * W;
+    const long long s = P.splits[(long long)r * P.split_stride + p];
+    if (s < 0 || s > P.limit) bad = 1;
+    pl.s[r][p] = s;
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
     return false;
   }
 
-  // Column scans: lane r holds S[r][p]; out_off[p][r] is its exclusive prefix.
-  for (int p = warp; p < W; p += nwarps) {
-    const long long x = lane < W ? pl.in_off[lane][p] : 0;
+  // Task k < W: column scan of peer k (lane r holds S[r][k]); task W + k: row
+  // scan of rank k (lane p holds S[k][p]).  Exclusive prefix = inclusive - own.
+  for (int task = warp; task < 2 * W; task += nwarps) {
+    const bool column = task < W;
+    const int k = column ? task : task - W;
+    const long long x = lane < W ? (column ? pl.s[lane][k] : pl.s[k][lane]) : 0;
     const long long inc = warp_inclusive_scan(x, lane);
-    if (lane < W) pl.out_off[p][lane] = inc - x;
-    if (lane == 31) {
-      pl.out_off[p][W] = inc;
-      if ((P.out_cap > 0 && inc > P.out_cap) || (P.out[p] == nullptr && inc > 0)) bad = 1;
-    }
-  }
-  __syncthreads();
-  // Row scans, in place: lane p holds S[r][p]; in_off[r][p] is its exclusive prefix.
-  for (int r = warp; r < W; r += nwarps) {
-    const long long x = lane < W ? pl.in_off[r][lane] : 0;
-    const long long inc = warp_inclusive_scan(x, lane);
-    if (lane < W) pl.in_off[r][lane] = inc - x;
-    if (lane == 31) {
-      if ((P.in_cap > 0 && inc > P.in_cap) || (P.in[r] == nullptr && inc > 0)) bad = 1;
+    if (column) {
+      if (lane < W) pl.out_off[k][lane] = inc - x;
+      if (lane == 31) {
+        pl.out_off[k][W] = inc;
+        if ((P.out_cap > 0 && inc > P.out_cap) || (P.out[k] == nullptr && inc > 0)) bad = 1;
+      }
+    } else {
+      if (lane < W) pl.in_off[k][lane] = inc - x;
+      if (lane == 31 && ((P.in_cap > 0 && inc > P.in_cap) || (P.in[k] == nullptr && inc > 0)))
+        bad = 1;
     }
   }
   if (__syncthreads_or(bad)) {
@@ -117,79 +125,79 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
     return false;
   }
 
-  // Tiles: peer p's received stream (out_off[p][W] * rb bytes) is cut into
-  // ceil(bytes / tile) tiles; tile_first is their exclusive prefix.
+  // Tiles: the smallest power of two (>= 4 KiB, <= max_tile, itself a power
+  // of two) that gives every CTA about kTilesPerCta tiles; peer p's received
+  // stream is cut into ceil(bytes / tile) of them.
   if (warp == 0) {
-    const long long bytes = lane < W ? pl.out_off[lane][W] * rb : 0;
+    const long long bytes = lane < W ? pl.out_off[lane][W] * P.rb : 0;
     const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
-    const long long per_cta =
-        (total + kTilesPerCta * gridDim.x - 1) / (kTilesPerCta * gridDim.x);
-    long long tile = (per_cta + kTileGranule - 1) / kTileGranule * kTileGranule;
-    tile = tile < kTileGranule ? kTileGranule : (tile > max_tile ? max_tile : tile);
-    const long long n = (bytes + tile - 1) / tile;
+    const long long ctas = kTilesPerCta * (long long)gridDim.x;
+    const long long per_cta = (total + ctas - 1) / ctas;
+    int shift = per_cta > 1 ? 64 - __clzll(per_cta - 1) : 0;  // ceil(log2(per_cta))
+    const int lo_shift = 63 - __clzll(kTileGranule), hi_shift = 63 - __clzll(max_tile);
+    shift = shift < lo_shift ? lo_shift : (shift > hi_shift ? hi_shift : shift);
+    const long long n = (bytes + (1LL << shift) - 1) >> shift;
     const long long inc = warp_inclusive_scan(n, lane);
     if (lane < W) pl.tile_first[lane] = inc - n;
     if (lane == 31) {
       pl.tile_first[W] = inc;
-      pl.tile = tile;
+      pl.tile_shift = shift;
     }
   }
-  __syncthreads();
-
   if (blockIdx.x == 0) {
     for (int e = tid; e < W * W; e += nt) {
-      const int p = e / W, r = e % W;
+      const int p = e / W, r = e - p * W;
       long long* so = P.out_so + (long long)p * 2 * W;
-      so[r] = pl.out_off[p][r + 1] - pl.out_off[p][r];
+      so[r] = pl.s[r][p];
       so[W + r] = pl.out_off[p][r];
     }
   }
-  __syncthreads();
-  // From here on the tables hold bytes.
-  for (int e = tid; e < W * (W + 1); e += nt) pl.out_off[e / (W + 1)][e % (W + 1)] *= rb;
-  for (int e = tid; e < W * W; e += nt) pl.in_off[e / W][e % W] *= rb;
   __syncthreads();
   return true;
 }
 
 // Tile t -> peer p and the byte range [lo, hi) of out[p] it covers (all
 // threads of the caller compute the same).
-__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long* lo,
-                                         long long* hi) {
+__device__ __forceinline__ int tile_peer(const Plan& pl, int W, long long t, long long rb,
+                                         long long* lo, long long* hi) {
   int p = 0;
   while (p + 1 < W && pl.tile_first[p + 1] <= t) ++p;
-  *lo = (t - pl.tile_first[p]) * pl.tile;
-  const long long end = *lo + pl.tile;
-  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
+  const long long bytes = pl.out_off[p][W] * rb;
+  *lo = (t - pl.tile_first[p]) << pl.tile_shift;
+  const long long end = *lo + (1LL << pl.tile_shift);
+  *hi = end < bytes ? end : bytes;
   return p;
 }
 
 // The same for a whole warp at once: the largest p with tile_first[p] <= t
 // (peers without tiles share their successor's tile_first, so the largest
 // such p is the one that owns tile t).
-__device__ __forceinline__ int tile_peer_warp(const Plan& pl, int W, long long t, int lane,
-                                              long long* lo, long long* hi) {
+__device__ __forceinline__ int tile_peer_warp(const Plan& pl, int W, long long t, long long rb,
+                                              int lane, long long* lo, long long* hi) {
   const unsigned m = __ballot_sync(kFull, lane < W && pl.tile_first[lane] <= t);
   const int p = 31 - __clz(m);
-  *lo = (t - pl.tile_first[p]) * pl.tile;
-  const long long end = *lo + pl.tile;
-  *hi = end < pl.out_off[p][W] ? end : pl.out_off[p][W];
+  const long long bytes = pl.out_off[p][W] * rb;
+  *lo = (t - pl.tile_first[p]) << pl.tile_shift;
+  const long long end = *lo + (1LL << pl.tile_shift);
+  *hi = end < bytes ? end : bytes;
   return p;
 }
 
-// Lane r's part of the tile [lo, hi) of peer p: the destination offset a, the
-// byte count n (0 when source r contributes nothing) and the source address.
+// Source r's part of the byte range [lo, hi) of peer p's output: the
+// destination offset a, the byte count (0 when source r contributes nothing)
+// and the source address.
 __device__ __forceinline__ long long lane_segment(const Params& P, const Plan& pl, int W, int p,
                                                   int r, long long lo, long long hi, long long* a,
                                                   const unsigned char** src) {
   *a = 0;
   *src = nullptr;
   if (r >= W) return 0;
-  const long long c_lo = pl.out_off[p][r], c_hi = pl.out_off[p][r + 1];
+  const long long rb = P.rb;
+  const long long c_lo = pl.out_off[p][r] * rb, c_hi = pl.out_off[p][r + 1] * rb;
   const long long x = lo > c_lo ? lo : c_lo, y = hi < c_hi ? hi : c_hi;
   if (x >= y) return 0;
   *a = x;
-  *src = P.in[r] + pl.in_off[r][p] + (x - c_lo);
+  *src = P.in[r] + pl.in_off[r][p] * rb + (x - c_lo);
   return y - x;
 }
 

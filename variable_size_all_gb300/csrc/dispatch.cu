@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kCopyThreads)
     const long long i = g - D.item_first[r];
     const int p = D.key[r][i] / K;
     const long long pos = D.sorted_pos[r][i];
-    unsigned char* dst = P.out[p] + pl.out_off[p][r] + (pos * rb - pl.in_off[r][p]);
+    unsigned char* dst = P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb;
     const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
     if (warp_rows)
       copy_span<32, 4, 2>(dst, src, rb, threadIdx.x & 31);
@@ -320,6 +320,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   P.out_so = reinterpret_cast<long long*>(out_splits_offsets_dev);
   P.status = h->d_status;
   P.rb = row_bytes;
+  P.limit = split_limit(W, row_bytes);
   P.in_cap = 0;  // sources are checked by row index in the count kernel
   P.out_cap = h->out_cap;
   P.W = W;
