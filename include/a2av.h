@@ -80,6 +80,13 @@ typedef struct a2av_handle a2av_handle;
  *  out                 receives the handle (host pointer, must not be NULL).
  *
  * Allocates a small device status word (cudaMalloc) on the current device.
+ * Reads three environment variables once: A2AV_PATH (an a2av_path_t number,
+ * the initial engine), A2AV_CTAS_PER_SM (the initial grid override) and
+ * A2AV_DEBUG_STARVE -- a test hook: when nonzero, the first CTA of every
+ * bulk or staged launch arms its first stage for 16 more bytes than its
+ * copies deliver, so that stage never completes, the bounded wait gives up
+ * after about a second and the run records A2AV_ERR_TIMEOUT.  No copy is
+ * left in flight and the context stays usable.  Never set it outside tests.
  * Errors: A2AV_ERR_INVALID_ARG (W < 1, negative capacity, out == NULL),
  * A2AV_ERR_UNSUPPORTED, A2AV_ERR_CUDA (no usable device).
  */

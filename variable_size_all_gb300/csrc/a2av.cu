@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(kBulkThreads)
       if (lane == 0) {
         stage_dst[s] = P.out[p] + lo;
         stage_len[s] = (unsigned)(hi - lo);
-        mbar_expect_tx(bar, (unsigned)(hi - lo));
+        const unsigned starve = (P.starve && blockIdx.x == 0 && k == 0) ? 16u : 0u;
+        mbar_expect_tx(bar, (unsigned)(hi - lo) + starve);
       }
       __syncwarp();
       if (n > 0) bulk_load(stage + (uint32_t)(a - lo), src, (unsigned)n, bar);
@@ -331,7 +332,8 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       __syncwarp();
       const uint32_t bar = full0 + 8 * s;
-      if (lane == 0) mbar_expect_tx(bar, total);
+      const unsigned starve = (P.starve && blockIdx.x == 0 && k == 0) ? 16u : 0u;
+      if (lane == 0) mbar_expect_tx(bar, total + starve);
       __syncwarp();
       if (n > 0) bulk_load(stage0 + (uint32_t)s * alloc + off, (const void*)g_lo, gb, bar);
     }
@@ -390,7 +392,8 @@ int configure_kernels() {
 // 16-byte aligned (the bulk engine's precondition).
 bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in_splits_dev,
                  void* const* out_ptrs, int64_t* out_splits_offsets_dev, int64_t row_bytes,
-                 long long in_cap, long long out_cap, int* status, long long split_stride) {
+                 long long in_cap, long long out_cap, int* status, long long split_stride,
+                 int starve = 0) {
   std::memset(P, 0, sizeof(*P));
   bool aligned = (row_bytes % 16) == 0;
   for (int r = 0; r < W; ++r) {
@@ -407,6 +410,7 @@ bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in
   P->in_cap = in_cap;
   P->out_cap = out_cap;
   P->W = W;
+  P->starve = starve;
   return aligned;
 }
 
@@ -485,6 +489,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   if (h->path < A2AV_PATH_AUTO || h->path > A2AV_PATH_STAGED) h->path = A2AV_PATH_AUTO;
   h->ctas_per_sm = env_int("A2AV_CTAS_PER_SM", 0);
   if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
+  h->starve = env_int("A2AV_DEBUG_STARVE", 0) != 0;
   h->last_path = h->last_grid = h->last_block = 0;
   *out = h;
   return A2AV_OK;
@@ -530,7 +535,7 @@ int run_exchange(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_s
   Params P;
   const bool aligned = fill_params(&P, h->W, in_ptrs, in_splits_dev, out_ptrs,
                                    out_splits_offsets_dev, row_bytes, h->in_cap, h->out_cap,
-                                   h->d_status, split_stride);
+                                   h->d_status, split_stride, h->starve);
   const int path = resolve_path(h->path, aligned);
   int grid = 0, block = 0;
   const int rc = launch(P, path, h->ctas_per_sm, h->sms, static_cast<cudaStream_t>(stream),

@@ -7,9 +7,10 @@
 // a2av_run would expect -- without ever materialising that order:
 //   1. count  (grid ranges x W, 256 threads): per range of 256 items, the key
 //      histogram in shared memory; keys and source rows are validated here.
-//   2. scan   (grid W, 1024 threads): per rank, the exclusive prefix of every
-//      key's count over the ranges (in place), the key start offsets and the
-//      split matrix row S[r][*].
+//   2. scan   (grid keys x W, 256 threads): per (key, rank), the exclusive
+//      prefix of the key's count over the ranges (in place); the last CTA of
+//      each rank to finish turns the key totals into key start offsets and
+//      the split matrix row S[r][*].
 //   3. rank   (grid ranges x W, one warp): items of a range in order, 32 at a
 //      time; __match_any_sync groups equal keys, a lane's rank among them
 //      plus the running count of its key gives its stable position.
@@ -31,7 +32,8 @@ namespace {
 
 constexpr int kRange = 256;                       // items per histogram range
 constexpr int kMaxBins = A2AV_MAX_DISPATCH_KEYS;  // W * K at most
-constexpr int kScanThreads = 1024;
+constexpr int kScanThreads = 256;
+static_assert(kMaxBins <= 4 * kScanThreads, "the finishing scan CTA holds 4 keys per thread");
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 4;
 constexpr long long kWarpRowBytes = 64;  // rows this long get a warp each
@@ -44,8 +46,10 @@ struct DispatchParams {
   long long rows[kMaxW];            // source rows per rank
   long long item_first[kMaxW + 1];  // exclusive prefix of m_r
   int* flag;                        // workspace: set once input is found invalid
+  int* done;                        // workspace: [W] scan CTAs finished per rank
   long long* S;                     // workspace: [W][W]
   long long* key_start;             // workspace: [W][NB]
+  long long* key_total;             // workspace: [W][NB]
   int* hist;                        // workspace: [W][ranges_max][NB]
   int* status;
   long long* in_splits_out;         // optional [W][W]
@@ -86,59 +90,73 @@ __global__ void __launch_bounds__(kRange) dispatch_count_kernel(const __grid_con
   for (int b = threadIdx.x; b < NB; b += blockDim.x) H[b] = hist[b];
 }
 
-// Per rank: H[j][b] becomes the number of items with key b in ranges < j;
-// key_start[b] = items with a smaller key; S[r][p] = items with key / K = p.
-// Thread (g, b) sums key b over its group g of consecutive ranges, the groups
-// are scanned per key, then each thread rewrites its ranges.
+// Block-wide exclusive scan of one value per thread (kScanThreads threads);
+// returns the exclusive prefix, *total gets the sum.  `warp_sums` holds
+// kScanThreads / 32 entries.
+__device__ __forceinline__ long long block_exclusive_scan(long long x, long long* warp_sums,
+                                                          long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long inc = warp_inclusive_scan(x, lane);
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  long long base = 0, all = 0;
+  for (int w = 0; w < kScanThreads / 32; ++w) {
+    if (w < warp) base += warp_sums[w];
+    all += warp_sums[w];
+  }
+  *total = all;
+  __syncthreads();
+  return base + inc - x;
+}
+
+// CTA (b, r): key b of rank r.  H[j][b] becomes the number of items with key
+// b in ranges < j (thread t scans a run of consecutive ranges), and
+// key_total[r][b] the key's count.  The last CTA of rank r to finish (an
+// atomic count, after a fence) turns the totals into key_start[r][*] (items
+// with a smaller key) and S[r][p] (items with key / K = p).
 __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __grid_constant__ DispatchParams D) {
   if (flagged(D)) return;
-  const int r = blockIdx.x, NB = D.W * D.K, t = threadIdx.x, lane = t & 31;
+  const int b = blockIdx.x, r = blockIdx.y, NB = D.W * D.K, t = threadIdx.x;
+  __shared__ long long warp_sums[kScanThreads / 32];
+  __shared__ int last;
   const long long R = (D.items[r] + kRange - 1) / kRange;
-  int* H = D.hist + (long long)r * D.ranges_max * NB;
-  __shared__ long long part[kScanThreads];
-  __shared__ long long total[kMaxBins];
-  const int G = kScanThreads / NB;
-  const int b = t % NB, g = t / NB;
-  const long long per = (R + G - 1) / G;
-  const long long j0 = g * per, j1 = j0 + per < R ? j0 + per : R;
-  if (g < G) {
-    long long sum = 0;
-    for (long long j = j0; j < j1; ++j) sum += H[j * NB + b];
-    part[g * NB + b] = sum;
+  int* H = D.hist + (long long)r * D.ranges_max * NB + b;  // range j at H[j * NB]
+  const long long per = (R + kScanThreads - 1) / kScanThreads;
+  const long long j0 = t * per, j1 = j0 + per < R ? j0 + per : R;
+  long long local = 0;
+  for (long long j = j0; j < j1; ++j) local += H[j * NB];
+  long long total;
+  long long run = block_exclusive_scan(local, warp_sums, &total);
+  for (long long j = j0; j < j1; ++j) {
+    const int x = H[j * NB];
+    H[j * NB] = (int)run;
+    run += x;
   }
+  if (t == 0) D.key_total[(long long)r * NB + b] = total;
+  __threadfence();
   __syncthreads();
-  if (t < NB) {
-    long long run = 0;
-    for (int q = 0; q < G; ++q) {
-      const long long x = part[q * NB + t];
-      part[q * NB + t] = run;
-      run += x;
-    }
-    total[t] = run;
-  }
+  if (t == 0) last = atomicAdd(&D.done[r], 1) == NB - 1;
   __syncthreads();
-  if (g < G) {
-    long long run = part[g * NB + b];
-    for (long long j = j0; j < j1; ++j) {
-      const int x = H[j * NB + b];
-      H[j * NB + b] = (int)run;
-      run += x;
-    }
+  if (!last) return;
+  __threadfence();
+  // key starts: thread t owns keys [4t, 4t + 4) (NB <= 4 * kScanThreads)
+  long long v[4], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int k = 4 * t + q;
+    v[q] = k < NB ? __ldcg(D.key_total + (long long)r * NB + k) : 0;
+    sum += v[q];
   }
-  if (t < 32) {
-    // key starts: lane l scans keys [32 l, 32 l + 32), lanes chained by a warp scan
-    const int k0 = lane * 32, k1 = k0 + 32 < NB ? k0 + 32 : NB;
-    long long local = 0;
-    for (int k = k0; k < k1; ++k) local += total[k];
-    long long run = warp_inclusive_scan(local, lane) - local;
-    for (int k = k0; k < k1; ++k) {
-      D.key_start[(long long)r * NB + k] = run;
-      run += total[k];
-    }
+  long long start = block_exclusive_scan(sum, warp_sums, &total);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int k = 4 * t + q;
+    if (k < NB) D.key_start[(long long)r * NB + k] = start;
+    start += v[q];
   }
   if (t < D.W) {
     long long s = 0;
-    for (int k = 0; k < D.K; ++k) s += total[t * D.K + k];
+    for (int k = 0; k < D.K; ++k) s += __ldcg(D.key_total + (long long)r * NB + t * D.K + k);
     D.S[(long long)r * D.W + t] = s;
   }
 }
@@ -226,8 +244,10 @@ __global__ void __launch_bounds__(kCopyThreads)
   }
 }
 
+// Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
+// cleared before every dispatch; then S, key starts, key totals, histograms.
 struct Layout {
-  long long flag, S, key_start, hist, total;
+  long long flag, done, S, key_start, key_total, hist, total;
 };
 
 Layout layout(int W, int K, long long ranges_max) {
@@ -235,9 +255,11 @@ Layout layout(int W, int K, long long ranges_max) {
   const long long NB = (long long)W * K;
   Layout L;
   L.flag = 0;
+  L.done = 4;
   L.S = 256;
   L.key_start = L.S + up(8LL * W * W);
-  L.hist = L.key_start + up(8LL * W * NB);
+  L.key_total = L.key_start + up(8LL * W * NB);
+  L.hist = L.key_total + up(8LL * W * NB);
   L.total = L.hist + up(4LL * W * (ranges_max < 1 ? 1 : ranges_max) * NB);
   return L;
 }
@@ -299,8 +321,10 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   if (workspace_bytes < L.total) return A2AV_ERR_INVALID_ARG;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   D.flag = reinterpret_cast<int*>(ws + L.flag);
+  D.done = reinterpret_cast<int*>(ws + L.done);
   D.S = reinterpret_cast<long long*>(ws + L.S);
   D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
+  D.key_total = reinterpret_cast<long long*>(ws + L.key_total);
   D.hist = reinterpret_cast<int*>(ws + L.hist);
   D.status = h->d_status;
   D.in_splits_out = reinterpret_cast<long long*>(in_splits_dev);
@@ -326,12 +350,13 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   P.W = W;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(D.flag, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
+  static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
+  if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
   if (ranges_max > 0) {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
     dispatch_count_kernel<<<grid, kRange, 0, s>>>(D);
   }
-  dispatch_scan_kernel<<<W, kScanThreads, 0, s>>>(D);
+  dispatch_scan_kernel<<<dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s>>>(D);
   dispatch_rank_kernel<<<dim3((unsigned)(ranges_max > 0 ? ranges_max : 1), (unsigned)W), 32, 0, s>>>(D);
   dispatch_copy_kernel<<<h->sms * kCopyCtasPerSm, kCopyThreads, 0, s>>>(P, D);
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
