@@ -12,7 +12,7 @@
 #include <cstdint>
 
 #ifndef A2AV_TILES_PER_CTA
-#define A2AV_TILES_PER_CTA 1
+#define A2AV_TILES_PER_CTA 2
 #endif
 // L2 eviction hints of the bulk engine: bit 0 marks loaded lines
 // evict-first, bit 1 stored lines (each byte is used exactly once; marking

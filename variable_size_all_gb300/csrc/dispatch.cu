@@ -33,10 +33,12 @@ namespace {
 constexpr int kRange = 256;                       // items per histogram range
 constexpr int kMaxBins = A2AV_MAX_DISPATCH_KEYS;  // W * K at most
 constexpr int kScanThreads = 256;
+constexpr int kScanBatch = 16;  // counts a scan thread loads at once
 static_assert(kMaxBins <= 4 * kScanThreads, "the finishing scan CTA holds 4 keys per thread");
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 4;
 constexpr long long kWarpRowBytes = 64;  // rows this long get a warp each
+constexpr int kItemsPerThread = 4;      // items a thread copies at once (short rows)
 
 struct DispatchParams {
   const int* key[kMaxW];
@@ -123,14 +125,38 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
   int* H = D.hist + (long long)r * D.ranges_max * NB + b;  // range j at H[j * NB]
   const long long per = (R + kScanThreads - 1) / kScanThreads;
   const long long j0 = t * per, j1 = j0 + per < R ? j0 + per : R;
+  // A thread's first kScanBatch counts are loaded together and kept in
+  // registers for the rewrite (runs longer than that are walked in batches).
+  int first[kScanBatch];
   long long local = 0;
-  for (long long j = j0; j < j1; ++j) local += H[j * NB];
+#pragma unroll
+  for (int q = 0; q < kScanBatch; ++q) {
+    first[q] = j0 + q < j1 ? H[(j0 + q) * NB] : 0;
+    local += first[q];
+  }
+  for (long long base = j0 + kScanBatch; base < j1; base += kScanBatch) {
+    int v[kScanBatch];
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) v[q] = base + q < j1 ? H[(base + q) * NB] : 0;
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) local += v[q];
+  }
   long long total;
   long long run = block_exclusive_scan(local, warp_sums, &total);
-  for (long long j = j0; j < j1; ++j) {
-    const int x = H[j * NB];
-    H[j * NB] = (int)run;
-    run += x;
+#pragma unroll
+  for (int q = 0; q < kScanBatch; ++q) {
+    if (j0 + q < j1) H[(j0 + q) * NB] = (int)run;
+    run += first[q];
+  }
+  for (long long base = j0 + kScanBatch; base < j1; base += kScanBatch) {
+    int v[kScanBatch];
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) v[q] = base + q < j1 ? H[(base + q) * NB] : 0;
+#pragma unroll
+    for (int q = 0; q < kScanBatch; ++q) {
+      if (base + q < j1) H[(base + q) * NB] = (int)run;
+      run += v[q];
+    }
   }
   if (t == 0) D.key_total[(long long)r * NB + b] = total;
   __threadfence();
@@ -187,10 +213,18 @@ __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant
   const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
   for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + H[k];
   __syncwarp();
+  // All keys of the range are loaded at once (8 per lane), then ranked in order.
+  int keys[kRange / 32];
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    keys[c] = i < m ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
+  }
+#pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = i0 + c * 32 + lane;
     const bool valid = i < m;
-    const int key = valid ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
+    const int key = keys[c];
     const unsigned same = __match_any_sync(kFull, key);
     long long pos = 0;
     if (valid) pos = next[key] + __popc(same & ((1u << lane) - 1u));
@@ -229,18 +263,46 @@ __global__ void __launch_bounds__(kCopyThreads)
                                    : (long long)blockIdx.x * kCopyThreads + threadIdx.x;
   const long long teams = warp_rows ? (long long)gridDim.x * (kCopyThreads / 32)
                                     : (long long)gridDim.x * kCopyThreads;
-  for (long long g = team; g < total; g += teams) {
-    int r = 0;
-    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
-    const long long i = g - D.item_first[r];
-    const int p = D.key[r][i] / K;
-    const long long pos = D.sorted_pos[r][i];
-    unsigned char* dst = P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb;
-    const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
-    if (warp_rows)
+  if (warp_rows) {
+    for (long long g = team; g < total; g += teams) {
+      int r = 0;
+      while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+      const long long i = g - D.item_first[r];
+      const int p = D.key[r][i] / K;
+      const long long pos = D.sorted_pos[r][i];
+      unsigned char* dst = P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb;
+      const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
       copy_span<32, 4, 2>(dst, src, rb, threadIdx.x & 31);
-    else
-      copy_row_thread(dst, src, rb);
+    }
+    return;
+  }
+  // Short rows: a thread takes kItemsPerThread items, their key, source row
+  // and position loads issued together, then copies the rows.
+  for (long long g0 = team; g0 < total; g0 += teams * kItemsPerThread) {
+    int rank[kItemsPerThread], key[kItemsPerThread], src_row[kItemsPerThread];
+    long long pos[kItemsPerThread];
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const long long g = g0 + q * teams;
+      rank[q] = -1;
+      if (g < total) {
+        int r = 0;
+        while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+        const long long i = g - D.item_first[r];
+        rank[q] = r;
+        key[q] = D.key[r][i];
+        src_row[q] = D.src[r][i];
+        pos[q] = D.sorted_pos[r][i];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const int r = rank[q];
+      if (r < 0) continue;
+      const int p = key[q] / K;
+      copy_row_thread(P.out[p] + (pl.out_off[p][r] + pos[q] - pl.in_off[r][p]) * rb,
+                      P.in[r] + (long long)src_row[q] * rb, rb);
+    }
   }
 }
 
