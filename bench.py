@@ -194,8 +194,9 @@ def kernel_source_sha() -> str:
 
 
 def measured_traffic(kernel: str, algo_bytes: int):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this
-    launch's algorithmic bytes; None when absent or taken on other source."""
+    """DRAM bytes per launch from the committed ncu summary of this kernel on
+    this workload ("kernel:workload"), scaled to this launch's algorithmic
+    bytes; None when absent or taken on other source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         d = json.load(open(path))
@@ -254,11 +255,29 @@ def describe(name: str, per_rank_bytes: int, seed: int) -> str:
     }[name] + f", seed {seed}"
 
 
+def host_memory_available() -> int:
+    """MemAvailable from /proc/meminfo, bytes (0 if unreadable)."""
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
 def load_workload(args, torch):
     """The workload's inputs in pinned host memory (also the e2e sources)."""
     import workloads as wl
     if args.workload == "cfg2":
         P = args.per_rank_bytes
+        # Several ranks on one node each pin their inputs and outputs: keep
+        # the payload within half of the host memory available to them.
+        _, _, world = dist_env()
+        avail = host_memory_available()
+        while avail and world * 4 * W * P > avail // 2 and P > (1 << 26):
+            P //= 2
+        args.per_rank_bytes = P
         nbytes = (P // ROW_BYTES) * ROW_BYTES
         h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
         w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
@@ -362,7 +381,8 @@ def run_ours(args):
     achieved = algo / avg_launch_s / 1e9
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": measured_traffic(kname, algo),
+                "frac": round(achieved / peak, 4),
+                "traffic": measured_traffic(f"{kname}:{args.workload}", algo),
                 "algorithmic_bytes_per_launch": algo}
 
     # ---- device-to-device memcpy ceiling for the same bytes ---------------
