@@ -373,6 +373,37 @@ def run_ours(args):
     avg_launch_s = statistics.mean(launch_ms) / 1e3
     med_launch_s = statistics.median(launch_ms) / 1e3
 
+    # ---- launch cost: eager calls vs one captured CUDA graph replayed -----
+    # (back to back, no flush: what a caller issuing many small exchanges pays)
+    graph_us = eager_us = None
+    if cold and world == 1:
+        g_stream = torch.cuda.Stream()
+        g_stream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=g_stream):
+            if args.op == "combine":
+                eng.combine(c_in, c_dso, c_out, c_so, rb, stream=g_stream)
+            else:
+                eng.run(d_in, d_S, d_out, d_so, rb, stream=g_stream)
+        torch.cuda.synchronize()
+        reps = 200
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_us = a.elapsed_time(b) * 1e3 / reps
+        a.record(stream)
+        for _ in range(reps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_us = a.elapsed_time(b) * 1e3 / reps
+        if eng.status() != a2av.OK:
+            raise SystemExit("device reported an error during graph replay")
+        del graph
+
     # ---- roofline of the (only) kernel -----------------------------------
     algo = algorithmic_bytes(S, rb)
     peak, peak_kind = hbm_peak()
@@ -577,6 +608,10 @@ def run_ours(args):
         "hbm_fraction": round(2 * T / (max_s / K) / 1e9 / peak, 4),
         "busbw_GBps": round(busbw_gbps(per_rank, max_s / K), 1),
         "launch_us_median": round(med_launch_s * 1e6, 2),
+        "back_to_back_us": None if graph_us is None else {
+            "eager_python_calls": round(eager_us, 2), "cuda_graph_replay": round(graph_us, 2),
+            "note": "per exchange, 200 in a row, warm L2; the graph replays one captured "
+                    "call (device-resident splits keep it valid when they change)"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

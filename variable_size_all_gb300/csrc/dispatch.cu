@@ -16,8 +16,9 @@
 //      plus the running count of its key gives its stable position.
 //   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
 //      prologue), then gather every item's row straight into its place in
-//      the output of its destination; a warp per row for rows of 64 bytes or
-//      more, a thread per row below.
+//      the output of its destination: with cp.async.bulk through shared
+//      memory for 16-byte aligned rows of 1..32 KiB, else a warp per row for
+//      rows of 64 bytes or more and a thread per row below.
 // A workspace flag, cleared first, stops every later kernel once a kernel has
 // found invalid input, so nothing is written on an error.
 #include "a2av_device.cuh"
@@ -308,6 +309,94 @@ __global__ void __launch_bounds__(kCopyThreads)
 
 // Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
 // cleared before every dispatch; then S, key starts, key totals, histograms.
+// Rows of 1..32 KiB, every row and buffer 16-byte aligned: one warp per CTA
+// streams each item's row global -> shared -> global with cp.async.bulk
+// through a ring of NS stages (loads LEAD rows ahead of the stores).  The
+// warp reads the metadata of 32 items at a time, lane i item i; lane 0
+// issues the copies and tracks its own bulk stores.
+template <int NS, int LEAD>
+__global__ void __launch_bounds__(128)
+    dispatch_copy_bulk_kernel(const __grid_constant__ Params P,
+                              const __grid_constant__ DispatchParams D, int stage_bytes) {
+  static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 rows ahead of stores");
+  if (flagged(D)) return;
+  __shared__ Plan pl;
+  __shared__ alignas(8) unsigned long long bars[NS];
+  __shared__ unsigned char* stage_dst[NS];
+  extern __shared__ __align__(128) unsigned char stages[];
+  if (!build_plan(P, pl, kTileGranule)) return;
+  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x >> 5) != 0) return;
+  const int W = D.W, K = D.K;
+  const long long rb = P.rb, total = D.item_first[W], G = gridDim.x, b0 = blockIdx.x;
+  const long long nk = total > b0 ? (total - b0 + G - 1) / G : 0;
+  if (nk == 0) return;
+  const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  long long msrc = 0, mdst = 0;  // this lane's item of the current batch of 32
+  long long issued = 0, stored = 0;
+  bool ok = true;
+  for (long long k = 0; k < nk + LEAD; ++k) {
+    if (k < nk) {
+      if ((k & 31) == 0) {
+        const long long kk = k + lane;
+        if (kk < nk) {
+          const long long g = b0 + kk * G;
+          int r = 0;
+          while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+          const long long i = g - D.item_first[r];
+          const int p = D.key[r][i] / K;
+          msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+          mdst = (long long)(P.out[p] +
+                             (pl.out_off[p][r] + D.sorted_pos[r][i] - pl.in_off[r][p]) * rb);
+        }
+      }
+      const int t = (int)(k & 31);
+      const long long src = __shfl_sync(kFull, msrc, t), dst = __shfl_sync(kFull, mdst, t);
+      if (lane == 0) {
+        const int s = (int)(k % NS);
+        if (k >= NS) bulk_wait_read<NS - LEAD - 1>();
+        stage_dst[s] = reinterpret_cast<unsigned char*>(dst);
+        mbar_expect_tx(bar0 + 8 * s, (unsigned)rb);
+        bulk_load(stage0 + (uint32_t)s * stage_bytes, reinterpret_cast<const void*>(src),
+                  (unsigned)rb, bar0 + 8 * s);
+      }
+      issued = k + 1;
+    }
+    const long long j = k - LEAD;
+    if (j >= 0 && j < nk) {
+      const int s = (int)(j % NS);
+      if (lane == 0) {
+        ok = mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1));
+        if (ok) bulk_store(stage_dst[s], stage0 + (uint32_t)s * stage_bytes, (unsigned)rb);
+      }
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      stored = j + 1;
+    }
+  }
+  if (lane == 0) {
+    if (!ok) {
+      record_error(P.status, A2AV_ERR_TIMEOUT);
+      for (long long j = stored; j < issued; ++j)
+        mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
+    }
+    bulk_wait_all();
+  }
+}
+
+// The two ring shapes: rows up to 16 KiB (8 stages) and up to 32 KiB (4).
+constexpr int kGatherSmallStage = 16 * 1024, kGatherLargeStage = 32 * 1024;
+using GatherKernel = void (*)(Params, DispatchParams, int);
+const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<8, 6>;
+const GatherKernel kGatherLarge = dispatch_copy_bulk_kernel<4, 2>;
+constexpr int kGatherSmem = 128 * 1024;  // 8 x 16 KiB = 4 x 32 KiB
+constexpr long long kGatherMinRow = 1024;
+
 struct Layout {
   long long flag, done, S, key_start, key_total, hist, total;
 };
@@ -420,7 +509,20 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   }
   dispatch_scan_kernel<<<dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s>>>(D);
   dispatch_rank_kernel<<<dim3((unsigned)(ranges_max > 0 ? ranges_max : 1), (unsigned)W), 32, 0, s>>>(D);
-  dispatch_copy_kernel<<<h->sms * kCopyCtasPerSm, kCopyThreads, 0, s>>>(P, D);
+  bool aligned = row_bytes % 16 == 0 && row_bytes >= kGatherMinRow &&
+                 row_bytes <= kGatherLargeStage;
+  for (int r = 0; r < W; ++r)
+    aligned = aligned && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
+  if (aligned) {
+    const bool small = row_bytes <= kGatherSmallStage;
+    const GatherKernel k = small ? kGatherSmall : kGatherLarge;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
+        cudaSuccess)
+      return A2AV_ERR_CUDA;
+    k<<<h->sms, 128, kGatherSmem, s>>>(P, D, small ? kGatherSmallStage : kGatherLargeStage);
+  } else {
+    dispatch_copy_kernel<<<h->sms * kCopyCtasPerSm, kCopyThreads, 0, s>>>(P, D);
+  }
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
   return A2AV_OK;
 }
