@@ -240,9 +240,18 @@ L2_BYTES = 129 * 10**6
 WORKLOADS = ("cfg2", "cfg1", "cfg3", "cfg4", "cfg5")
 
 
-def describe(name: str, per_rank_bytes: int, seed: int) -> str:
+def describe(name: str, per_rank_bytes: int, seed: int, tokens: int = 8192,
+             batch: int = 8192) -> str:
     if name == "cfg2":
         return workload_name(per_rank_bytes)
+    if name == "cfg3" and tokens != 8192:
+        return (f"a2av W=8 MoE dispatch: {tokens} tokens/rank, hidden 7168 bf16 (14336 B rows), "
+                f"top-2 of 64 experts (8 per rank), Zipf(1.2) popularity shuffled per seed, "
+                f"seed {seed}")
+    if name == "cfg5" and batch != 8192:
+        return (f"a2av W=2 embedding keys: 26 features x {batch} bags per rank, "
+                f"min(Poisson(3), 20) int64 keys per bag, U[0, 1e7), feature mod 2 ownership, "
+                f"seed {seed}")
     return {
         "cfg1": "a2av W=4, 4096 rows/rank of 128 bf16 (256 B), N(0,1) bf16, "
                 "in_splits ~ Multinomial(4096, 1/4)",
@@ -282,8 +291,9 @@ def load_workload(args, torch):
         h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
         w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
     else:
-        w = {"cfg1": wl.cfg1, "cfg3": wl.cfg3, "cfg4": wl.cfg4, "cfg5": wl.cfg5}[args.workload](
-            args.seed)
+        gen = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens),
+               "cfg4": wl.cfg4, "cfg5": lambda s: wl.cfg5(s, batch=args.batch)}
+        w = gen[args.workload](args.seed)
         h_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
     return w, h_in
 
@@ -616,7 +626,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed), "name": args.workload,
+        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch), "name": args.workload,
                    "op": args.op, "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
                    "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
@@ -676,7 +686,8 @@ def run_fused_dispatch(args):
     a2av.build()
     if args.workload not in ("cfg3", "cfg5"):
         raise SystemExit("--op fused_dispatch needs --workload cfg3 or cfg5")
-    w = {"cfg3": wl.cfg3, "cfg5": wl.cfg5}[args.workload](args.seed)
+    w = (wl.cfg3(args.seed, tokens=args.tokens) if args.workload == "cfg3"
+         else wl.cfg5(args.seed, batch=args.batch))
     K, rows, src, key = wl.dispatch_items(w)
     Wn, rb, S = w.W, w.row_bytes, w.splits
     m = [k.size for k in key]
@@ -758,7 +769,7 @@ def run_fused_dispatch(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed) +
+        "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed, args.tokens, args.batch) +
                    " -- items unsorted (token-major / feature-major), grouped on the device",
                    "name": args.workload, "op": "fused_dispatch", "ranks": Wn, "row_bytes": rb,
                    "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
@@ -894,7 +905,7 @@ def run_reference(args):
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(total_s * 1e3 / K, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed), "name": args.workload,
+        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch), "name": args.workload,
                    "ranks": Wn, "row_bytes": rb,
                    "per_rank_bytes": int(statistics.mean(b.size for b in inputs)),
                    "parallelism": "one host core"},
@@ -919,6 +930,8 @@ def main(argv=None):
                          "fused_dispatch = a2av_dispatch on unsorted items (cfg3, cfg5); "
                          "overlap = cfg3 exchange on a side stream beside bf16 GEMMs")
     ap.add_argument("--gemm-n", type=int, default=8192)
+    ap.add_argument("--tokens", type=int, default=8192, help="cfg3 tokens per rank")
+    ap.add_argument("--batch", type=int, default=8192, help="cfg5 bags per feature and rank")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--per-rank-bytes", type=int, default=1 << 32, help="cfg2 payload per rank")
     ap.add_argument("--path", choices=["auto", "vector", "bulk", "staged"], default="auto")

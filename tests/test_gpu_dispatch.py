@@ -143,3 +143,19 @@ def test_dispatch_host_rejections():
     a2av.a2av_destroy(h)
     assert a2av.a2av_dispatch_workspace_bytes(4, 257, 10) == -1
     assert a2av.a2av_dispatch_workspace_bytes(4, 8, 1000) > 0
+
+
+@pytest.mark.parametrize("rb", [8, 16, 1040])
+def test_small_dispatch_path(rb):
+    # every rank at most 2048 items and at most 256 keys: the fused
+    # count/scan/rank kernel; W=32 with 8 keys per peer is its widest case
+    rng = np.random.default_rng(100 + rb)
+    for W, K in ((32, 8), (8, 32), (4, 1), (1, 256)):
+        n = [int(rng.integers(1, 200)) for _ in range(W)]
+        m = [int(rng.integers(0, 2049)) for _ in range(W)]
+        m[0] = 2048
+        rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+        src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
+        key = [np.minimum(rng.geometric(0.05, m[r]) - 1, W * K - 1).astype(np.int32)
+               for r in range(W)]
+        dispatch_checked(K, rows, src, key, rb)

@@ -54,12 +54,11 @@ struct DispatchParams {
   long long* key_start;             // workspace: [W][NB]
   long long* key_total;             // workspace: [W][NB]
   int* hist;                        // workspace: [W][ranges_max][NB]
+  int* pos;                         // workspace: [W][pos_stride] item positions in key order
   int* status;
   long long* in_splits_out;         // optional [W][W]
   long long ranges_max;
-  long long out_cap;
-  unsigned out_null;                // bit p: out[p] is NULL
-  unsigned in_null;                 // bit r: rows of rank r are NULL
+  long long pos_stride;
   int W, K;
 };
 
@@ -190,24 +189,7 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
 
 __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
   if (flagged(D)) return;
-  const int r = blockIdx.y, lane = threadIdx.x, W = D.W, NB = W * D.K;
-  // Capacity and NULL-buffer checks on the complete split matrix: every CTA
-  // reaches the same verdict before any position is written.
-  bool bad = false;
-  for (int p = lane; p < W; p += 32) {
-    long long col = 0;
-    for (int q = 0; q < W; ++q) col += D.S[(long long)q * W + p];
-    if ((D.out_cap > 0 && col > D.out_cap) || (((D.out_null >> p) & 1u) && col > 0)) bad = true;
-  }
-  for (int q = lane; q < W; q += 32)
-    if (((D.in_null >> q) & 1u) && D.items[q] > 0) bad = true;
-  if (__any_sync(kFull, bad)) {
-    if (lane == 0) fail(D, A2AV_ERR_BAD_SPLITS);
-    return;
-  }
-  if (blockIdx.x == 0 && r == 0 && D.in_splits_out != nullptr)
-    for (int e = lane; e < W * W; e += 32) D.in_splits_out[e] = D.S[e];
-
+  const int r = blockIdx.y, lane = threadIdx.x, NB = D.W * D.K;
   const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
   if (i0 >= m) return;
   __shared__ long long next[kMaxBins];  // next position of each key in this range
@@ -232,8 +214,92 @@ __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant
     __syncwarp();
     if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
     __syncwarp();
-    if (valid) D.sorted_pos[r][i] = pos;
+    if (valid) D.pos[(long long)r * D.pos_stride + i] = (int)pos;
   }
+}
+
+// Small dispatches (every rank at most kSmallItems items, at most
+// kSmallKeys keys): count, scan and rank in one kernel, one CTA per rank.
+// Warp w owns items [256 w, 256 w + 256) with their keys in registers: it
+// counts them per key (warp match, its own row of `cnt`), the rows are
+// turned into per-key prefixes over the warps, a block scan of the key
+// totals gives the key starts, and each warp ranks its items in order.
+constexpr int kSmallWarps = 8;
+constexpr int kSmallItems = kSmallWarps * kRange;  // 2048
+constexpr int kSmallKeys = kScanThreads;           // one key per thread in the key scan
+
+__global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __grid_constant__ DispatchParams D) {
+  const int r = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NB = D.W * D.K;
+  const long long m = D.items[r];
+  __shared__ int cnt[kSmallWarps][kSmallKeys];
+  __shared__ long long key_start[kSmallKeys];
+  __shared__ long long warp_sums[kScanThreads / 32];
+  for (int e = tid; e < kSmallWarps * NB; e += kScanThreads) cnt[e / NB][e % NB] = 0;
+  __syncthreads();
+  int keys[kRange / 32];
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = (long long)warp * kRange + c * 32 + lane;
+    int key = -1 - lane;  // absent items match nobody
+    if (i < m) {
+      key = D.key[r][i];
+      const int src = D.src[r][i];
+      if (key < 0 || key >= NB || src < 0 || src >= D.rows[r]) {
+        bad = 1;
+        key = -1 - lane;
+      }
+    }
+    keys[c] = key;
+    const unsigned same = __match_any_sync(kFull, key);
+    if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
+    __syncwarp();
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) fail(D, A2AV_ERR_BAD_INDEX);
+    return;
+  }
+  long long total_k = 0;
+  if (tid < NB) {
+    int run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int x = cnt[w][tid];
+      cnt[w][tid] = run;
+      run += x;
+    }
+    total_k = run;
+  }
+  long long all;
+  const long long start = block_exclusive_scan(total_k, warp_sums, &all);
+  if (tid < NB) {
+    key_start[tid] = start;
+    D.key_total[(long long)r * NB + tid] = total_k;
+  }
+  __syncthreads();
+  if (tid < D.W) {
+    long long sum = 0;
+    for (int k = 0; k < D.K; ++k) sum += __ldcg(D.key_total + (long long)r * NB + tid * D.K + k);
+    D.S[(long long)r * D.W + tid] = sum;
+  }
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = (long long)warp * kRange + c * 32 + lane;
+    const int key = keys[c];
+    const unsigned same = __match_any_sync(kFull, key);
+    int pos = 0;
+    if (key >= 0) pos = (int)key_start[key] + cnt[warp][key] + __popc(same & ((1u << lane) - 1u));
+    __syncwarp();
+    if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
+    __syncwarp();
+    if (i < m) D.pos[(long long)r * D.pos_stride + i] = pos;
+  }
+}
+
+// Once build_plan has accepted the split matrix: CTA 0 writes it out.
+__device__ __forceinline__ void publish_splits(const DispatchParams& D) {
+  if (blockIdx.x == 0 && D.in_splits_out != nullptr)
+    for (int e = threadIdx.x; e < D.W * D.W; e += blockDim.x) D.in_splits_out[e] = D.S[e];
 }
 
 // A row of n bytes, any alignment, copied by one thread.
@@ -257,6 +323,7 @@ __global__ void __launch_bounds__(kCopyThreads)
   if (flagged(D)) return;
   __shared__ Plan pl;
   if (!build_plan(P, pl, kTileGranule)) return;
+  publish_splits(D);
   const int W = D.W, K = D.K;
   const long long rb = P.rb, total = D.item_first[W];
   const bool warp_rows = rb >= kWarpRowBytes;
@@ -270,7 +337,8 @@ __global__ void __launch_bounds__(kCopyThreads)
       while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
       const long long i = g - D.item_first[r];
       const int p = D.key[r][i] / K;
-      const long long pos = D.sorted_pos[r][i];
+      const long long pos = D.pos[(long long)r * D.pos_stride + i];
+      if ((threadIdx.x & 31) == 0) D.sorted_pos[r][i] = pos;
       unsigned char* dst = P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb;
       const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
       copy_span<32, 4, 2>(dst, src, rb, threadIdx.x & 31);
@@ -293,7 +361,8 @@ __global__ void __launch_bounds__(kCopyThreads)
         rank[q] = r;
         key[q] = D.key[r][i];
         src_row[q] = D.src[r][i];
-        pos[q] = D.sorted_pos[r][i];
+        pos[q] = D.pos[(long long)r * D.pos_stride + i];
+        D.sorted_pos[r][i] = pos[q];
       }
     }
 #pragma unroll
@@ -325,6 +394,7 @@ __global__ void __launch_bounds__(128)
   __shared__ unsigned char* stage_dst[NS];
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
+  publish_splits(D);
   const int lane = threadIdx.x & 31;
   if ((threadIdx.x >> 5) != 0) return;
   const int W = D.W, K = D.K;
@@ -350,9 +420,10 @@ __global__ void __launch_bounds__(128)
           while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
           const long long i = g - D.item_first[r];
           const int p = D.key[r][i] / K;
+          const long long pos = D.pos[(long long)r * D.pos_stride + i];
+          D.sorted_pos[r][i] = pos;
           msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
-          mdst = (long long)(P.out[p] +
-                             (pl.out_off[p][r] + D.sorted_pos[r][i] - pl.in_off[r][p]) * rb);
+          mdst = (long long)(P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb);
         }
       }
       const int t = (int)(k & 31);
@@ -398,20 +469,22 @@ constexpr int kGatherSmem = 128 * 1024;  // 8 x 16 KiB = 4 x 32 KiB
 constexpr long long kGatherMinRow = 1024;
 
 struct Layout {
-  long long flag, done, S, key_start, key_total, hist, total;
+  long long flag, done, S, key_start, key_total, pos, hist, total;
 };
 
-Layout layout(int W, int K, long long ranges_max) {
+Layout layout(int W, int K, long long max_items) {
   auto up = [](long long x) { return (x + 255) / 256 * 256; };
   const long long NB = (long long)W * K;
+  const long long ranges = (max_items + kRange - 1) / kRange;
   Layout L;
   L.flag = 0;
   L.done = 4;
   L.S = 256;
   L.key_start = L.S + up(8LL * W * W);
   L.key_total = L.key_start + up(8LL * W * NB);
-  L.hist = L.key_total + up(8LL * W * NB);
-  L.total = L.hist + up(4LL * W * (ranges_max < 1 ? 1 : ranges_max) * NB);
+  L.pos = L.key_total + up(8LL * W * NB);
+  L.hist = L.pos + up(4LL * W * (max_items < 1 ? 1 : max_items));
+  L.total = L.hist + up(4LL * W * (ranges < 1 ? 1 : ranges) * NB);
   return L;
 }
 
@@ -422,7 +495,7 @@ extern "C" int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_pe
   if (world_size < 1 || world_size > kMaxW || keys_per_peer < 1 || max_items_per_rank < 0 ||
       (long long)world_size * keys_per_peer > kMaxBins || max_items_per_rank > 0x7fffffffLL)
     return -1;
-  return layout(world_size, keys_per_peer, (max_items_per_rank + kRange - 1) / kRange).total;
+  return layout(world_size, keys_per_peer, max_items_per_rank).total;
 }
 
 extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* const* rows_ptrs,
@@ -448,7 +521,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
 
   DispatchParams D;
   std::memset(&D, 0, sizeof(D));
-  long long ranges_max = 0;
+  long long ranges_max = 0, max_items = 0;
   D.item_first[0] = 0;
   for (int r = 0; r < W; ++r) {
     const long long m = items_per_rank[r], n = rows_per_rank[r];
@@ -465,10 +538,9 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     D.item_first[r + 1] = D.item_first[r] + m;
     const long long R = (m + kRange - 1) / kRange;
     ranges_max = R > ranges_max ? R : ranges_max;
-    if (out_ptrs[r] == nullptr) D.out_null |= 1u << r;
-    if (rows_ptrs[r] == nullptr) D.in_null |= 1u << r;
+    max_items = m > max_items ? m : max_items;
   }
-  const Layout L = layout(W, K, ranges_max);
+  const Layout L = layout(W, K, max_items);
   if (workspace_bytes < L.total) return A2AV_ERR_INVALID_ARG;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   D.flag = reinterpret_cast<int*>(ws + L.flag);
@@ -476,11 +548,12 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   D.S = reinterpret_cast<long long*>(ws + L.S);
   D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
   D.key_total = reinterpret_cast<long long*>(ws + L.key_total);
+  D.pos = reinterpret_cast<int*>(ws + L.pos);
+  D.pos_stride = max_items < 1 ? 1 : max_items;
   D.hist = reinterpret_cast<int*>(ws + L.hist);
   D.status = h->d_status;
   D.in_splits_out = reinterpret_cast<long long*>(in_splits_dev);
   D.ranges_max = ranges_max;
-  D.out_cap = h->out_cap;
   D.W = W;
   D.K = K;
 
@@ -503,12 +576,14 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
-  if (ranges_max > 0) {
+  if (max_items <= kSmallItems && W * K <= kSmallKeys) {
+    dispatch_small_kernel<<<W, kScanThreads, 0, s>>>(D);
+  } else {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
     dispatch_count_kernel<<<grid, kRange, 0, s>>>(D);
+    dispatch_scan_kernel<<<dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s>>>(D);
+    dispatch_rank_kernel<<<grid, 32, 0, s>>>(D);
   }
-  dispatch_scan_kernel<<<dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s>>>(D);
-  dispatch_rank_kernel<<<dim3((unsigned)(ranges_max > 0 ? ranges_max : 1), (unsigned)W), 32, 0, s>>>(D);
   bool aligned = row_bytes % 16 == 0 && row_bytes >= kGatherMinRow &&
                  row_bytes <= kGatherLargeStage;
   for (int r = 0; r < W; ++r)
