@@ -13,14 +13,19 @@
 //      the split matrix row S[r][*].
 //   3. rank   (grid ranges x W, one warp): items of a range in order, 32 at a
 //      time; __match_any_sync groups equal keys, a lane's rank among them
-//      plus the running count of its key gives its stable position.
+//      plus the running count of its key gives its stable position (kept in
+//      the workspace).
+//   When every rank has at most 2048 items and there are at most 256 keys,
+//   one kernel (one CTA per rank, a warp per 256 items) does 1-3 instead.
 //   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
-//      prologue), then gather every item's row straight into its place in
-//      the output of its destination: with cp.async.bulk through shared
-//      memory for 16-byte aligned rows of 1..32 KiB, else a warp per row for
-//      rows of 64 bytes or more and a thread per row below.
-// A workspace flag, cleared first, stops every later kernel once a kernel has
-// found invalid input, so nothing is written on an error.
+//      prologue, which also checks capacities and NULL buffers), publish the
+//      positions and the split matrix, then gather every item's row straight
+//      into its place in the output of its destination: with cp.async.bulk
+//      through shared memory for 16-byte aligned rows of 1..32 KiB, else a
+//      warp per row for rows of 64 bytes or more and a thread per row below.
+// Invalid keys or source rows set a workspace flag (cleared first) that stops
+// every later kernel; invalid splits stop the copy kernel in its prologue.
+// Either way nothing the caller owns is written.
 #include "a2av_device.cuh"
 #include "a2av_handle.h"
 
