@@ -50,7 +50,6 @@
 #include <mutex>
 #include <new>
 
-
 // Engine shapes.  Each can be overridden at compile time (-DA2AV_...) for
 // tuning sweeps; the defaults are the measured choices.
 #ifndef A2AV_VEC_THREADS
@@ -92,9 +91,18 @@
 #ifndef A2AV_STAGED_CTAS_PER_SM
 #define A2AV_STAGED_CTAS_PER_SM 1
 #endif
+// Tile order: round-robin (CTA b takes tiles b, b + G, ...) or blocked (CTA
+// b takes a contiguous run of tiles).  Measured: blocked is ~0.6 % faster for
+// the bulk engine on large exchanges, round-robin ~0.9 % faster for the
+// staged engine.
+#ifndef A2AV_BULK_BLOCKED_TILES
+#define A2AV_BULK_BLOCKED_TILES 1
+#endif
+#ifndef A2AV_STAGED_BLOCKED_TILES
+#define A2AV_STAGED_BLOCKED_TILES 0
+#endif
 
 namespace {
-
 
 // Vector engine: 512 threads (64 registers each, two CTAs per SM), 4
 // independent 16-byte loads in flight per thread on the aligned path (32 KiB
@@ -105,8 +113,9 @@ constexpr int kVecShiftUnroll = A2AV_VEC_SHIFT_UNROLL;
 constexpr long long kVecMaxTile = A2AV_VEC_MAX_TILE;
 constexpr int kVecCtasPerSm = A2AV_VEC_CTAS_PER_SM;
 
-// Bulk engine: a ring of stages (tile = stage size); loads run LEAD tiles
-// ahead of the stores that drain them.
+// Bulk engine: a ring of stages, each holding one tile (tiles are powers of
+// two, at most the stage size); loads run LEAD tiles ahead of the stores that
+// drain them.
 constexpr int kBulkThreads = 128;
 constexpr int kBulkStages = A2AV_BULK_STAGES;
 constexpr int kBulkLead = A2AV_BULK_LEAD;
@@ -124,6 +133,25 @@ constexpr int kStagedCtasPerSm = A2AV_STAGED_CTAS_PER_SM;
 constexpr int kStagedPad = 32 * kMaxW + 128;
 constexpr int kStagedAlloc = kStagedStageBytes + kStagedPad;
 static_assert(kStagedPad % 128 == 0 && kStagedStageBytes % 128 == 0, "128-byte aligned stages");
+
+// The k-th of this CTA's tiles, in blocked or round-robin order.
+struct TileSeq {
+  long long first, step, count;
+  __device__ TileSeq(long long ntiles, bool blocked) {
+    const long long G = gridDim.x, b = blockIdx.x;
+    if (blocked) {
+      const long long per = (ntiles + G - 1) / G, lo = b * per;
+      first = lo;
+      step = 1;
+      count = ntiles > lo ? (ntiles - lo < per ? ntiles - lo : per) : 0;
+    } else {
+      first = b;
+      step = G;
+      count = ntiles > b ? (ntiles - b + G - 1) / G : 0;
+    }
+  }
+  __device__ long long operator[](long long k) const { return first + k * step; }
+};
 
 template <int NT, int U, int US>
 __global__ void __launch_bounds__(NT, kVecCtasPerSm)
@@ -166,8 +194,8 @@ __global__ void __launch_bounds__(kBulkThreads)
   if ((threadIdx.x >> 5) != 0) return;
 
   const int W = P.W;
-  const long long ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
-  const long long nk = ntiles > b0 ? (ntiles - b0 + G - 1) / G : 0;
+  const TileSeq tiles(pl.tile_first[W], A2AV_BULK_BLOCKED_TILES != 0);
+  const long long nk = tiles.count;
   if (nk == 0) return;
   const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
   if (lane == 0) {
@@ -187,7 +215,7 @@ __global__ void __launch_bounds__(kBulkThreads)
       __syncwarp();
       long long lo, hi, a;
       const unsigned char* src;
-      const int p = tile_peer_warp(pl, W, b0 + k * G, P.rb, lane, &lo, &hi);
+      const int p = tile_peer_warp(pl, W, tiles[k], P.rb, lane, &lo, &hi);
       const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
       const uint32_t bar = bar0 + 8 * s, stage = stage0 + (uint32_t)s * stage_bytes;
       if (lane == 0) {
@@ -282,8 +310,8 @@ __global__ void __launch_bounds__(32 * (NC + 1))
   if (!build_plan(P, pl, stage_bytes)) return;
 
   const int W = P.W, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long ntiles = pl.tile_first[W], G = gridDim.x, b0 = blockIdx.x;
-  const long long nk = ntiles > b0 ? (ntiles - b0 + G - 1) / G : 0;
+  const TileSeq tiles(pl.tile_first[W], A2AV_STAGED_BLOCKED_TILES != 0);
+  const long long nk = tiles.count;
   if (nk == 0) return;
   const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), stage0 = smem_u32(stages);
   const uint32_t alloc = (uint32_t)stage_bytes + kStagedPad;
@@ -306,7 +334,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       long long lo, hi, a;
       const unsigned char* src;
-      const int p = tile_peer_warp(pl, W, b0 + k * G, P.rb, lane, &lo, &hi);
+      const int p = tile_peer_warp(pl, W, tiles[k], P.rb, lane, &lo, &hi);
       const long long n = lane_segment(P, pl, W, p, lane, lo, hi, &a, &src);
       const uintptr_t g_lo = (uintptr_t)src & ~(uintptr_t)15;
       const unsigned gb =
