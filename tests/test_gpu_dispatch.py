@@ -159,3 +159,17 @@ def test_small_dispatch_path(rb):
         key = [np.minimum(rng.geometric(0.05, m[r]) - 1, W * K - 1).astype(np.int32)
                for r in range(W)]
         dispatch_checked(K, rows, src, key, rb)
+
+
+@pytest.mark.parametrize("rb", [20480, 40000, 16384 + 16])
+def test_dispatch_large_rows(rb):
+    # 16..32 KiB rows use the gather's 4 x 32 KiB ring; 40000 B rows (over
+    # 32 KiB) the warp path; 16400 B the large ring's lower edge
+    rng = np.random.default_rng(rb)
+    W, K = 4, 3
+    n = [int(rng.integers(1, 40)) for _ in range(W)]
+    m = [int(rng.integers(0, 120)) for _ in range(W)]
+    rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+    src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
+    key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+    dispatch_checked(K, rows, src, key, rb)

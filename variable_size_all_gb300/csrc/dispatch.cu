@@ -67,6 +67,16 @@ struct DispatchParams {
   int W, K;
 };
 
+// Programmatic dependent launch: a kernel of the chain launched with the
+// programmatic-serialization attribute may start while its predecessor runs;
+// it waits here before reading anything the predecessor wrote (a no-op when
+// the launch had no such dependency).  A predecessor lets its successor's
+// CTAs start launching once its own CTAs have begun.
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ bool flagged(const DispatchParams& D) {
   return *reinterpret_cast<volatile int*>(D.flag) != 0;
 }
@@ -77,6 +87,7 @@ __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
 }
 
 __global__ void __launch_bounds__(kRange) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
+  chain_release();
   const int r = blockIdx.y;
   const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
   if (i0 >= m) return;
@@ -122,6 +133,8 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 // atomic count, after a fence) turns the totals into key_start[r][*] (items
 // with a smaller key) and S[r][p] (items with key / K = p).
 __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __grid_constant__ DispatchParams D) {
+  chain_wait();
+  chain_release();
   if (flagged(D)) return;
   const int b = blockIdx.x, r = blockIdx.y, NB = D.W * D.K, t = threadIdx.x;
   __shared__ long long warp_sums[kScanThreads / 32];
@@ -193,6 +206,8 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
 }
 
 __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
+  chain_wait();
+  chain_release();
   if (flagged(D)) return;
   const int r = blockIdx.y, lane = threadIdx.x, NB = D.W * D.K;
   const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
@@ -234,6 +249,7 @@ constexpr int kSmallItems = kSmallWarps * kRange;  // 2048
 constexpr int kSmallKeys = kScanThreads;           // one key per thread in the key scan
 
 __global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __grid_constant__ DispatchParams D) {
+  chain_release();
   const int r = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NB = D.W * D.K;
   const long long m = D.items[r];
@@ -325,6 +341,7 @@ __device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned
 
 __global__ void __launch_bounds__(kCopyThreads)
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  chain_wait();
   if (flagged(D)) return;
   __shared__ Plan pl;
   if (!build_plan(P, pl, kTileGranule)) return;
@@ -393,6 +410,7 @@ __global__ void __launch_bounds__(128)
     dispatch_copy_bulk_kernel(const __grid_constant__ Params P,
                               const __grid_constant__ DispatchParams D, int stage_bytes) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 rows ahead of stores");
+  chain_wait();
   if (flagged(D)) return;
   __shared__ Plan pl;
   __shared__ alignas(8) unsigned long long bars[NS];
@@ -472,6 +490,25 @@ const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<8, 6>;
 const GatherKernel kGatherLarge = dispatch_copy_bulk_kernel<4, 2>;
 constexpr int kGatherSmem = 128 * 1024;  // 8 x 16 KiB = 4 x 32 KiB
 constexpr long long kGatherMinRow = 1024;
+
+// Launch a kernel of the chain with programmatic stream serialization: it
+// may begin while the previous kernel on the stream finishes (it waits in
+// chain_wait for that kernel's results).
+template <typename... Args, typename... Vals>
+cudaError_t chained(void (*kernel)(Args...), dim3 grid, int block, size_t smem, cudaStream_t s,
+                    Vals... vals) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, vals...);
+}
 
 struct Layout {
   long long flag, done, S, key_start, key_total, pos, hist, total;
@@ -586,8 +623,10 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   } else {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
     dispatch_count_kernel<<<grid, kRange, 0, s>>>(D);
-    dispatch_scan_kernel<<<dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s>>>(D);
-    dispatch_rank_kernel<<<grid, 32, 0, s>>>(D);
+    if (chained(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s,
+                D) != cudaSuccess ||
+        chained(dispatch_rank_kernel, grid, 32, 0, s, D) != cudaSuccess)
+      return A2AV_ERR_CUDA;
   }
   bool aligned = row_bytes % 16 == 0 && row_bytes >= kGatherMinRow &&
                  row_bytes <= kGatherLargeStage;
@@ -599,9 +638,12 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
         cudaSuccess)
       return A2AV_ERR_CUDA;
-    k<<<h->sms, 128, kGatherSmem, s>>>(P, D, small ? kGatherSmallStage : kGatherLargeStage);
-  } else {
-    dispatch_copy_kernel<<<h->sms * kCopyCtasPerSm, kCopyThreads, 0, s>>>(P, D);
+    if (chained(k, dim3(h->sms), 128, kGatherSmem, s, P, D,
+                small ? kGatherSmallStage : kGatherLargeStage) != cudaSuccess)
+      return A2AV_ERR_CUDA;
+  } else if (chained(dispatch_copy_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s, P,
+                     D) != cudaSuccess) {
+    return A2AV_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
   return A2AV_OK;
