@@ -743,10 +743,14 @@ def run_fused_dispatch(args):
     distinct = sum(int(np.unique(x).size) for x in src) * rb
     algo = distinct + T + items * (4 + 4 + 8) + 24 * Wn * Wn
     peak, peak_kind = hbm_peak()
-    roofline = {"bound": "hbm", "kernel": "a2av_dispatch (4 launches: count, scan, rank, copy)",
+    # the copy kernel the library picks: cp.async.bulk gather for 16-byte
+    # aligned rows of 1..32 KiB (torch allocations are aligned), else warp/thread copies
+    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 1024 <= rb <= 32768
+                   else "dispatch_copy_kernel")
+    roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
-                "traffic": measured_traffic("dispatch_copy_kernel:" + args.workload, algo),
+                "traffic": measured_traffic(copy_kernel + ":" + args.workload, algo),
                 "algorithmic_bytes_per_launch": algo}
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
