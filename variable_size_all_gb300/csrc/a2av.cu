@@ -92,11 +92,13 @@
 #define A2AV_STAGED_CTAS_PER_SM 1
 #endif
 // Tile order: round-robin (CTA b takes tiles b, b + G, ...) or blocked (CTA
-// b takes a contiguous run of tiles).  Measured: blocked is ~0.6 % faster for
-// the bulk engine on large exchanges, round-robin ~0.9 % faster for the
-// staged engine.
+// b takes a contiguous run of tiles).  Measured (interleaved A/B on one GPU):
+// blocked is ~1 % faster for the bulk engine when every CTA has thousands of
+// tiles (4 GiB per rank), round-robin equal or up to ~1 % faster below that
+// and for the staged engine.  The bulk engine switches to blocked order from
+// A2AV_BULK_BLOCKED_TILES tiles per CTA (0 = never).
 #ifndef A2AV_BULK_BLOCKED_TILES
-#define A2AV_BULK_BLOCKED_TILES 1
+#define A2AV_BULK_BLOCKED_TILES 1024
 #endif
 #ifndef A2AV_STAGED_BLOCKED_TILES
 #define A2AV_STAGED_BLOCKED_TILES 0
@@ -194,7 +196,9 @@ __global__ void __launch_bounds__(kBulkThreads)
   if ((threadIdx.x >> 5) != 0) return;
 
   const int W = P.W;
-  const TileSeq tiles(pl.tile_first[W], A2AV_BULK_BLOCKED_TILES != 0);
+  const long long ntiles = pl.tile_first[W];
+  const TileSeq tiles(ntiles, A2AV_BULK_BLOCKED_TILES > 0 &&
+                                  ntiles >= (long long)A2AV_BULK_BLOCKED_TILES * gridDim.x);
   const long long nk = tiles.count;
   if (nk == 0) return;
   const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
