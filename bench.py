@@ -241,9 +241,13 @@ WORKLOADS = ("cfg2", "cfg1", "cfg3", "cfg4", "cfg5")
 
 
 def describe(name: str, per_rank_bytes: int, seed: int, tokens: int = 8192,
-             batch: int = 8192) -> str:
+             batch: int = 8192, dedup: bool = False) -> str:
     if name == "cfg2":
         return workload_name(per_rank_bytes)
+    if name == "cfg3" and dedup:
+        return (describe(name, per_rank_bytes, seed, tokens, batch).replace(
+            "top-2 of 64 experts", "top-2 of 64 experts, one row per distinct (token, "
+            "destination rank) pair"))
     if name == "cfg3" and tokens != 8192:
         return (f"a2av W=8 MoE dispatch: {tokens} tokens/rank, hidden 7168 bf16 (14336 B rows), "
                 f"top-2 of 64 experts (8 per rank), Zipf(1.2) popularity shuffled per seed, "
@@ -291,7 +295,8 @@ def load_workload(args, torch):
         h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
         w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
     else:
-        gen = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens),
+        gen = {"cfg1": wl.cfg1,
+               "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens, dedup=args.dedup),
                "cfg4": wl.cfg4, "cfg5": lambda s: wl.cfg5(s, batch=args.batch)}
         w = gen[args.workload](args.seed)
         h_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
@@ -626,7 +631,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch), "name": args.workload,
+        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
+                                        args.dedup), "name": args.workload,
                    "op": args.op, "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
                    "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
@@ -656,19 +662,31 @@ def run_ours(args):
 
 
 # ------------------------------------------------------ fused dispatch ----
+# A spin kernel this long (about 125 us at 2.07 GHz) runs ahead of every
+# timed call of a multi-launch op, so that the host has enqueued the whole op
+# before its first event is reached: the events then bracket device time only.
+SPIN_CYCLES = 1 << 18
+
+
 def _timed(torch, stream, fn, reps, cold, flush):
-    """Median and mean CUDA-event time of fn over reps launches (seconds)."""
-    ts = []
+    """Median and mean device time of fn over reps calls (seconds), and the
+    mean host time of one call (seconds, the Python binding and the launches,
+    measured while the GPU is still busy with the spin kernel)."""
+    ts, host = [], []
     for _ in range(reps):
-        if cold:
-            flush.sum()
+        with torch.cuda.stream(stream):
+            if cold:
+                flush.sum()
+            torch.cuda._sleep(SPIN_CYCLES)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        t0 = time.perf_counter()
         fn()
+        host.append(time.perf_counter() - t0)
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b) / 1e3)
-    return statistics.median(ts), statistics.mean(ts)
+    return statistics.median(ts), statistics.mean(ts), statistics.mean(host)
 
 
 def run_fused_dispatch(args):
@@ -686,7 +704,7 @@ def run_fused_dispatch(args):
     a2av.build()
     if args.workload not in ("cfg3", "cfg5"):
         raise SystemExit("--op fused_dispatch needs --workload cfg3 or cfg5")
-    w = (wl.cfg3(args.seed, tokens=args.tokens) if args.workload == "cfg3"
+    w = (wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup) if args.workload == "cfg3"
          else wl.cfg5(args.seed, batch=args.batch))
     K, rows, src, key = wl.dispatch_items(w)
     Wn, rb, S = w.W, w.row_bytes, w.splits
@@ -728,10 +746,10 @@ def run_fused_dispatch(args):
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
-        f_med, f_mean = _timed(torch, stream, fused, args.steps, cold, flush)
+        f_med, f_mean, f_host = _timed(torch, stream, fused, args.steps, cold, flush)
         torch.cuda.synchronize()
         barrier()
-    u_med, u_mean = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
+    u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during the timed region")
     max_s = reduce_max(f_mean, dev)
@@ -773,17 +791,22 @@ def run_fused_dispatch(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed, args.tokens, args.batch) +
+        "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed,
+                                        args.tokens, args.batch, args.dedup) +
                    " -- items unsorted (token-major / feature-major), grouped on the device",
                    "name": args.workload, "op": "fused_dispatch", "ranks": Wn, "row_bytes": rb,
                    "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
                           "inputs larger than L2"),
-                   "timing": "CUDA events around the 4-launch dispatch, mean over steps"},
+                   "timing": "CUDA events around the dispatch (one memset and four kernels), "
+                             "mean over steps; a spin kernel ahead of each call keeps the "
+                             "host's call time outside the events (fused_host_call_us)"},
         "unfused_torch_sort_gather_a2av": {"ms_mean": round(u_mean * 1e3, 4),
                                            "ms_median": round(u_med * 1e3, 4),
-                                           "value": round(T / u_mean / 1e9, 2), "unit": UNIT},
+                                           "value": round(T / u_mean / 1e9, 2), "unit": UNIT,
+                                           "host_call_us": round(u_host * 1e6, 1)},
         "fused_ms_median": round(f_med * 1e3, 4),
+        "fused_host_call_us": round(f_host * 1e6, 1),
         "speedup_vs_unfused": round(u_mean / f_mean, 3),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary(), "parity": parity,
@@ -793,6 +816,154 @@ def run_fused_dispatch(args):
 
 
 # ------------------------------------------------------------- overlap ----
+def device_exchange(torch, dev, w):
+    """Device inputs, splits, outputs and out_splits_offsets for workload w."""
+    S, rb = w.splits, w.row_bytes
+    d_in = [torch.from_numpy(b).to(dev) for b in w.inputs]
+    d_out = [torch.empty(int(S[:, p].sum()) * rb, dtype=torch.uint8, device=dev)
+             for p in range(w.W)]
+    return (d_in, torch.from_numpy(S).to(dev), d_out,
+            torch.empty((w.W, 2, w.W), dtype=torch.int64, device=dev))
+
+
+def run_kjt(args):
+    """The keyed-jagged exchange of an embedding batch (cfg5): the int32 bag
+    lengths and the int64 keys, two a2av_run calls per step -- the key
+    exchange torchrec PR 2570 moves to its own stream, with the lengths that
+    cut the keys into bags.  Timed as one stream (PDL lets the keys' launch
+    overlap the lengths' tail), without PDL, on two streams, and as one
+    captured CUDA graph."""
+    import torch
+    import variable_size_all_gb300 as a2av
+    import workloads as wl
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    a2av.build()
+    if args.workload != "cfg5":
+        raise SystemExit("--op kjt runs the keyed-jagged exchange: --workload cfg5")
+    w = wl.cfg5(args.seed, batch=args.batch)
+    lw = wl.cfg5_lengths(w)
+    parts = [lw, w]
+    Wn = w.W
+    T = sum(moved_bytes(x.splits, x.row_bytes) for x in parts)
+    bufs = [device_exchange(torch, dev, x) for x in parts]
+    eng = a2av.A2av(Wn)
+    saved = os.environ.get("A2AV_PDL")
+    os.environ["A2AV_PDL"] = "0"  # read once, when the handle is made
+    try:
+        eng_plain = a2av.A2av(Wn)
+    finally:
+        if saved is None:
+            del os.environ["A2AV_PDL"]
+        else:
+            os.environ["A2AV_PDL"] = saved
+    stream, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+
+    def one_stream(e=eng, st=stream):
+        for (d_in, d_S, d_out, d_so), x in zip(bufs, parts):
+            e.run(d_in, d_S, d_out, d_so, x.row_bytes, stream=st)
+
+    def two_streams():
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        side.wait_event(fork)
+        (l_in, l_S, l_out, l_so), (k_in, k_S, k_out, k_so) = bufs
+        eng.run(l_in, l_S, l_out, l_so, lw.row_bytes, stream=side)
+        eng.run(k_in, k_S, k_out, k_so, w.row_bytes, stream=stream)
+        join = torch.cuda.Event()
+        join.record(side)
+        stream.wait_event(join)
+
+    for _ in range(args.warmup):
+        one_stream()
+        one_stream(eng_plain)
+        two_streams()
+    torch.cuda.synchronize()
+    g_stream = torch.cuda.Stream()
+    g_stream.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=g_stream):
+        one_stream(eng, g_stream)
+    torch.cuda.synchronize()
+    variants = {"one_stream_pdl": one_stream, "one_stream_no_pdl": lambda: one_stream(eng_plain),
+                "two_streams": two_streams, "cuda_graph": graph.replay}
+    times = {}
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        for name, fn in variants.items():
+            times[name] = _timed(torch, stream, fn, args.steps, True, flush)
+        torch.cuda.synchronize()
+        barrier()
+    for e in (eng, eng_plain):
+        if e.status() != a2av.OK:
+            raise SystemExit("device reported an error during the timed region")
+    t_mean = times["one_stream_pdl"][1]
+    max_s = reduce_max(t_mean, dev)
+    value = whole_job_value(T / 1e9, world, max_s)
+    algo = sum(algorithmic_bytes(x.splits, x.row_bytes) for x in parts)
+    peak, peak_kind = hbm_peak()
+    roofline = {"bound": "hbm", "kernel": "a2av_staged_kernel (two launches: lengths, keys)",
+                "achieved": round(algo / t_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
+                "unit": "GB/s", "frac": round(algo / t_mean / 1e9 / peak, 4),
+                "traffic": None, "algorithmic_bytes_per_step": algo}
+    alone = {}  # each exchange by itself
+    for (d_in, d_S, d_out, d_so), x in zip(bufs, parts):
+        alone[x.name] = _timed(torch, stream, lambda: eng.run(d_in, d_S, d_out, d_so, x.row_bytes),
+                               args.steps, True, flush)[1]
+    cpu = parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        refs = [oracle.default().exchange(x.inputs, x.splits, x.row_bytes) for x in parts]
+        spent = time.perf_counter() - t0
+        ok = True
+        for (_, _, d_out, d_so), (ref, ref_so) in zip(bufs, refs):
+            ok = ok and np.array_equal(d_so.cpu().numpy(), ref_so)
+            ok = ok and all(np.array_equal(d_out[p].cpu().numpy(), ref[p]) for p in range(Wn))
+        # the received lengths count the received keys, per source rank
+        l_out, l_so = bufs[0][2], bufs[0][3].cpu().numpy()
+        k_so = bufs[1][3].cpu().numpy()
+        for p in range(Wn):
+            got = l_out[p].cpu().numpy().view(np.int32)
+            for r in range(Wn):
+                o0, n0 = int(l_so[p][1][r]), int(l_so[p][0][r])
+                ok = ok and int(got[o0:o0 + n0].sum()) == int(k_so[p][0][r])
+        parity = {"bit_exact": bool(ok), "check": "lengths and keys equal the oracle's; the "
+                                                  "received lengths sum to the received key counts"}
+        cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "both exchanges (lengths, keys) of the same batch",
+               "seconds": round(spent, 3)}
+        if not ok:
+            raise SystemExit("keyed-jagged exchange differs from the oracle")
+    eng.close()
+    eng_plain.close()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws; no dataset)",
+        "config": {"workload": describe("cfg5", 0, args.seed, batch=args.batch) +
+                   " -- with its bag lengths (int32, one per feature and bag), two a2av_run "
+                   "per step on one stream", "name": "cfg5", "op": "kjt", "ranks": Wn,
+                   "moved_bytes_per_step": T,
+                   "l2": "L2 flushed (512 MiB read) before every timed step",
+                   "timing": "CUDA events around the step, mean over steps; a spin kernel "
+                             "ahead of each step keeps the host's call time outside"},
+        "variants_us": {k: {"mean": round(v[1] * 1e6, 2), "median": round(v[0] * 1e6, 2),
+                            "host_call": round(v[2] * 1e6, 1)} for k, v in times.items()},
+        "alone_us": {k: round(v * 1e6, 2) for k, v in alone.items()},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(), "parity": parity,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_overlap(args):
     """The exchange on a side stream while a bf16 GEMM runs on the main one:
     each alone, then both at once (the separate-stream idea of torchrec PR
@@ -806,15 +977,18 @@ def run_overlap(args):
     dev = torch.device("cuda", local)
     dist_init("nccl")
     a2av.build()
-    w = wl.cfg3(args.seed) if args.workload == "cfg3" else None
-    if w is None:
-        raise SystemExit("--op overlap runs the MoE exchange: --workload cfg3")
-    Wn, rb, S = w.W, w.row_bytes, w.splits
-    T = moved_bytes(S, rb)
-    d_in = [torch.from_numpy(b).to(dev) for b in w.inputs]
-    d_out = [torch.empty(int(S[:, p].sum()) * rb, dtype=torch.uint8, device=dev) for p in range(Wn)]
-    d_S = torch.from_numpy(S).to(dev)
-    d_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, device=dev)
+    if args.workload == "cfg3":
+        w = wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup)
+        parts = [w]  # the MoE token exchange
+    elif args.workload == "cfg5":
+        w = wl.cfg5(args.seed, batch=args.batch)
+        parts = [wl.cfg5_lengths(w), w]  # a keyed-jagged batch: bag lengths, then keys
+    else:
+        raise SystemExit("--op overlap runs the MoE exchange (cfg3) or the keyed-jagged "
+                         "exchange of bag lengths and keys (cfg5)")
+    Wn = w.W
+    T = sum(moved_bytes(x.splits, x.row_bytes) for x in parts)
+    bufs = [device_exchange(torch, dev, x) for x in parts]
     n = args.gemm_n
     A = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
     B = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
@@ -829,7 +1003,8 @@ def run_overlap(args):
 
     def exchanges():
         for _ in range(reps):
-            eng.run(d_in, d_S, d_out, d_so, rb, stream=side)
+            for (d_in, d_S, d_out, d_so), x in zip(bufs, parts):
+                eng.run(d_in, d_S, d_out, d_so, x.row_bytes, stream=side)
 
     def span(fn_main, fn_side):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -859,22 +1034,37 @@ def run_overlap(args):
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error")
     eng.close()
+    parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        ok = True
+        for (_, _, d_out, d_so), x in zip(bufs, parts):
+            ref, ref_so = oracle.default().exchange(x.inputs, x.splits, x.row_bytes)
+            ok = ok and np.array_equal(d_so.cpu().numpy(), ref_so)
+            ok = ok and all(np.array_equal(d_out[p].cpu().numpy(), ref[p]) for p in range(Wn))
+        parity = {"bit_exact": bool(ok), "check": "outputs and offsets equal the oracle's"}
+        if not ok:
+            raise SystemExit("overlapped exchange differs from the oracle")
     flops = 2.0 * n * n * n * reps
     line = {
         "metric": METRIC, "value": round(T * reps / x_both / 1e9, 2), "unit": UNIT,
         "n_gpus": world, "steps": reps, "warmup": 2, "ms_per_step": round(x_both / reps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
-        "data": "synthetic", "config": {"workload": describe("cfg3", 0, args.seed) +
-                                        f" on a side stream, with {reps} bf16 GEMMs "
-                                        f"{n}x{n}x{n} on the main stream", "op": "overlap"},
+        "data": "synthetic",
+        "config": {"workload": describe(args.workload, 0, args.seed, args.tokens, args.batch,
+                                        args.dedup) +
+                   (" (bag lengths, int32, then keys: two a2av_run per step)"
+                    if args.workload == "cfg5" else "") +
+                   f" on a side stream, with {reps} bf16 GEMMs {n}x{n}x{n} on the main stream",
+                   "name": args.workload, "op": "overlap"},
         "exchange_alone_GBps": round(T * reps / x_alone / 1e9, 2),
         "exchange_overlapped_GBps": round(T * reps / x_both / 1e9, 2),
         "gemm_alone_TFLOPs": round(flops / g_alone / 1e12, 1),
         "gemm_overlapped_TFLOPs": round(flops / g_both / 1e12, 1),
         "serial_ms": round((g_alone + x_alone) * 1e3, 3), "overlapped_wall_ms": round(wall * 1e3, 3),
         "overlap_saving": round(1 - wall / (g_alone + x_alone), 4),
-        "gpu_launches": reps, "clocks": clocks.summary(), "roofline": None, "cpu_baseline": None,
-        "e2e": None,
+        "gpu_launches": reps * len(parts), "clocks": clocks.summary(), "roofline": None,
+        "cpu_baseline": None, "e2e": None, "parity": parity,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -892,8 +1082,8 @@ def run_reference(args):
     if args.workload == "cfg2":
         w = wl.cfg2(P, seed=args.seed)
     else:
-        w = {"cfg1": wl.cfg1, "cfg3": wl.cfg3, "cfg4": wl.cfg4, "cfg5": wl.cfg5}[args.workload](
-            args.seed)
+        w = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, dedup=args.dedup), "cfg4": wl.cfg4,
+             "cfg5": wl.cfg5}[args.workload](args.seed)
     S, inputs, rb, Wn = w.splits, w.inputs, w.row_bytes, w.W
     K, Wm = args.steps, args.warmup
     for k in range(Wm):
@@ -909,7 +1099,8 @@ def run_reference(args):
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(total_s * 1e3 / K, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch), "name": args.workload,
+        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
+                                        args.dedup), "name": args.workload,
                    "ranks": Wn, "row_bytes": rb,
                    "per_rank_bytes": int(statistics.mean(b.size for b in inputs)),
                    "parallelism": "one host core"},
@@ -928,14 +1119,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="cfg2")
-    ap.add_argument("--op", choices=["dispatch", "combine", "fused_dispatch", "overlap"],
+    ap.add_argument("--op", choices=["dispatch", "combine", "fused_dispatch", "overlap", "kjt"],
                     default="dispatch",
                     help="dispatch = a2av_run; combine = a2av_combine on its outputs; "
                          "fused_dispatch = a2av_dispatch on unsorted items (cfg3, cfg5); "
-                         "overlap = cfg3 exchange on a side stream beside bf16 GEMMs")
+                         "overlap = the exchange (cfg3; cfg5: bag lengths and keys) on a side "
+                         "stream beside bf16 GEMMs; kjt = cfg5 bag lengths + keys, two a2av_run")
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--tokens", type=int, default=8192, help="cfg3 tokens per rank")
     ap.add_argument("--batch", type=int, default=8192, help="cfg5 bags per feature and rank")
+    ap.add_argument("--dedup", action="store_true",
+                    help="cfg3: one row per distinct (token, destination rank) pair")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--per-rank-bytes", type=int, default=1 << 32, help="cfg2 payload per rank")
     ap.add_argument("--path", choices=["auto", "vector", "bulk", "staged"], default="auto")
@@ -954,6 +1148,8 @@ def main(argv=None):
         run_fused_dispatch(args)
     elif args.op == "overlap":
         run_overlap(args)
+    elif args.op == "kjt":
+        run_kjt(args)
     else:
         run_ours(args)
 

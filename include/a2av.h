@@ -80,8 +80,9 @@ typedef struct a2av_handle a2av_handle;
  *  out                 receives the handle (host pointer, must not be NULL).
  *
  * Allocates a small device status word (cudaMalloc) on the current device.
- * Reads three environment variables once: A2AV_PATH (an a2av_path_t number,
- * the initial engine), A2AV_CTAS_PER_SM (the initial grid override) and
+ * Reads four environment variables once: A2AV_PATH (an a2av_path_t number,
+ * the initial engine), A2AV_CTAS_PER_SM (the initial grid override), A2AV_PDL
+ * (0 turns programmatic dependent launch off; see a2av_run) and
  * A2AV_DEBUG_STARVE -- a test hook: when nonzero, the first CTA of every
  * bulk or staged launch arms its first stage for 16 more bytes than its
  * copies deliver, so that stage never completes, the bounded wait gives up
@@ -95,7 +96,12 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
 
 /*
  * a2av_run -- one all_to_all_vdev over the handle's W ranks, enqueued on
- * `stream` as a single kernel launch; returns without waiting for it.
+ * `stream` as a single kernel launch; returns without waiting for it.  The
+ * launch uses programmatic stream serialization (unless A2AV_PDL=0): its
+ * CTAs may be scheduled while the previous kernel on `stream` still runs,
+ * and wait on the device for that kernel to finish, its writes visible,
+ * before they read or write anything -- stream order is kept, only the
+ * launch latency is hidden.
  *
  *  in_ptrs            HOST array of W device pointers: rank r's input, its chunks
  *                     back to back in peer order from row 0.  Read only.  A NULL

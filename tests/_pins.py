@@ -361,7 +361,8 @@ def pin_dispatch_small(o):
 
 def pin_dispatch_matches_generators(o):
     import workloads as wl
-    for w in (wl.cfg3(2, tokens=96, hidden=4), wl.cfg5(3, batch=64)):
+    for w in (wl.cfg3(2, tokens=96, hidden=4), wl.cfg3(2, tokens=96, hidden=4, dedup=True),
+              wl.cfg5(3, batch=64)):
         K, rows, src, key = wl.dispatch_items(w)
         outs, so, pos, S = o.dispatch_exchange(K, rows, src, key, w.row_bytes)
         _eq(S, w.splits, f"{w.name}: dispatch splits must equal the generator's")
@@ -375,6 +376,34 @@ def pin_dispatch_matches_generators(o):
             inv = np.empty(order.size, np.int64)
             inv[order] = np.arange(order.size)
             _eq(pos[r], inv, f"{w.name}: positions = inverse stable argsort")
+
+
+def pin_kjt_lengths_cut_the_keys(o):
+    """A keyed-jagged batch exchanged as two a2avs, the bag lengths and the
+    keys: what peer p receives from rank r must be exactly rank r's bags of
+    the features p owns, the lengths cutting the keys into those bags."""
+    import workloads as wl
+    w = wl.cfg5(4, features=5, batch=7, W=2)
+    lw = wl.cfg5_lengths(w)
+    keys, kso = o.exchange(w.inputs, w.splits, w.row_bytes)
+    lens, lso = o.exchange(lw.inputs, lw.splits, lw.row_bytes)
+    F = w.meta["features"]
+    for p in range(w.W):
+        owned = [f for f in range(F) if f % w.W == p]
+        got_len = lens[p].view(np.int32)
+        got_key = keys[p].view(np.int64)
+        for r in range(w.W):
+            L = w.meta["lengths"][r]
+            starts = np.concatenate([[0], np.cumsum(L.sum(axis=1))])
+            want_keys = np.concatenate([w.meta["kjt_keys"][r][starts[f]:starts[f + 1]]
+                                        for f in owned])
+            l0 = int(lso[p][1][r])
+            rl = got_len[l0:l0 + int(lso[p][0][r])]
+            _eq(rl, L[owned].reshape(-1).astype(np.int32), f"bag lengths {r} -> {p}")
+            k0 = int(kso[p][1][r])
+            rk = got_key[k0:k0 + int(kso[p][0][r])]
+            assert int(rl.sum()) == rk.size, "the lengths must count the keys received"
+            _eq(rk, want_keys, f"keys {r} -> {p}")
 
 
 def pin_dispatch_errors(o):
@@ -398,7 +427,8 @@ def pin_dispatch_errors(o):
 
 PINS = [pin_identity_w1, pin_errors, pin_diagonal_and_permutation, pin_uniform_transpose,
         pin_round_trip, pin_combine_round_trip, pin_dispatch_errors, pin_dispatch_small,
-        pin_dispatch_matches_generators, pin_dest_and_row_source, pin_invariants_random,
+        pin_dispatch_matches_generators, pin_kjt_lengths_cut_the_keys, pin_dest_and_row_source,
+        pin_invariants_random,
         pin_bruteforce_tiny]
 
 

@@ -30,6 +30,15 @@ def test_moe_top2_dispatch(tokens):
         assert ref[p].size == int(w.splits[:, p].sum()) * w.row_bytes
 
 
+def test_moe_dedup_dispatch():
+    w = wl.cfg3(3, tokens=2048, hidden=512, dedup=True)
+    K, rows, src, key = wl.dispatch_items(w)
+    assert K == 1
+    ref, *_ = dispatch_checked(K, rows, src, key, w.row_bytes)
+    for p in range(w.W):
+        assert ref[p].size == int(w.splits[:, p].sum()) * w.row_bytes
+
+
 def test_embedding_key_dispatch():
     w = wl.cfg5(0)
     K, rows, src, key = wl.dispatch_items(w)

@@ -68,6 +68,35 @@ def test_cfg3_top2_dispatch_small():
     assert counts.max() > 8 * max(counts.min(), 1)
 
 
+def test_cfg3_dedup_one_row_per_token_and_rank():
+    full = wl.cfg3(seed=1, tokens=512, hidden=64)
+    w = wl.cfg3(seed=1, tokens=512, hidden=64, dedup=True)
+    _shape_ok(w)
+    for r in range(8):
+        assert np.array_equal(w.meta["choices"][r], full.meta["choices"][r])  # same routing
+        dests = w.meta["choices"][r] // 8
+        for p in range(8):  # tokens with at least one expert on rank p
+            assert w.splits[r, p] == int(np.any(dests == p, axis=1).sum())
+        tok, exp = w.meta["routes"][r]
+        dest = exp // 8
+        assert np.all(np.diff(dest * 512 + tok) > 0)  # (destination, token), no repeats
+        rows = w.meta["token_rows"][r].reshape(512, -1)
+        assert np.array_equal(w.inputs[r].reshape(-1, 128), rows[tok])
+    assert w.splits.sum() < full.splits.sum()  # some tokens had both experts on one rank
+
+
+def test_cfg5_lengths_go_with_the_keys():
+    w = wl.cfg5(seed=2, batch=128)
+    lw = wl.cfg5_lengths(w)
+    _shape_ok(lw)
+    assert lw.row_bytes == 4 and np.all(lw.splits == 13 * 128)
+    for r in range(2):
+        L = lw.inputs[r].view(np.int32)
+        assert L[:13 * 128].sum() == w.splits[r, 0] and L[13 * 128:].sum() == w.splits[r, 1]
+    with pytest.raises(ValueError):
+        wl.cfg5_lengths(wl.cfg1(0))
+
+
 def test_cfg4_skew():
     w = wl.cfg4(seed=3, rows=1 << 12)
     _shape_ok(w)

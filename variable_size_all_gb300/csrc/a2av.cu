@@ -453,22 +453,27 @@ int resolve_path(int requested, bool aligned) {
   return aligned ? A2AV_PATH_BULK : A2AV_PATH_STAGED;
 }
 
-int launch(const Params& P, int path, int ctas_per_sm, int sms, cudaStream_t s, int* grid,
-           int* block) {
+// One launch of the chosen engine.  With `pdl` the launch may overlap the
+// tail of the previous kernel on the stream (build_plan waits for it).
+int launch(const Params& P, int path, int ctas_per_sm, int sms, cudaStream_t s, bool pdl,
+           int* grid, int* block) {
+  cudaError_t e;
   if (path == A2AV_PATH_BULK) {
     *grid = sms * (ctas_per_sm ? ctas_per_sm : kBulkCtasPerSm);
     *block = kBulkThreads;
-    kBulk<<<*grid, *block, kBulkStages * kBulkStageBytes, s>>>(P, kBulkStageBytes);
+    e = launch_kernel(kBulk, dim3(*grid), *block, kBulkStages * kBulkStageBytes, s, pdl, P,
+                      (int)kBulkStageBytes);
   } else if (path == A2AV_PATH_STAGED) {
     *grid = sms * (ctas_per_sm ? ctas_per_sm : kStagedCtasPerSm);
     *block = kStagedThreads;
-    kStaged<<<*grid, *block, kStagedStages * kStagedAlloc, s>>>(P, kStagedStageBytes);
+    e = launch_kernel(kStaged, dim3(*grid), *block, kStagedStages * kStagedAlloc, s, pdl, P,
+                      (int)kStagedStageBytes);
   } else {
     *grid = sms * (ctas_per_sm ? ctas_per_sm : kVecCtasPerSm);
     *block = kVecThreads;
-    kVec<<<*grid, *block, 0, s>>>(P, kVecMaxTile);
+    e = launch_kernel(kVec, dim3(*grid), *block, 0, s, pdl, P, (long long)kVecMaxTile);
   }
-  return cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
+  return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? A2AV_OK : A2AV_ERR_CUDA;
 }
 
 }  // namespace
@@ -522,6 +527,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   h->ctas_per_sm = env_int("A2AV_CTAS_PER_SM", 0);
   if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
   h->starve = env_int("A2AV_DEBUG_STARVE", 0) != 0;
+  h->pdl = env_int("A2AV_PDL", 1) != 0;
   h->last_path = h->last_grid = h->last_block = 0;
   *out = h;
   return A2AV_OK;
@@ -571,7 +577,7 @@ int run_exchange(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_s
   const int path = resolve_path(h->path, aligned);
   int grid = 0, block = 0;
   const int rc = launch(P, path, h->ctas_per_sm, h->sms, static_cast<cudaStream_t>(stream),
-                        &grid, &block);
+                        h->pdl, &grid, &block);
   if (rc != A2AV_OK) return rc;
   h->last_path = path;
   h->last_grid = grid;
@@ -684,7 +690,7 @@ extern "C" int a2av_run_noalloc(int world_size, int64_t in_capacity_rows,
   // The kernels only ever set the status word, so it must start at zero.
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
   int grid = 0, block = 0;
-  rc = launch(P, resolve_path(A2AV_PATH_AUTO, aligned), 0, sms, s, &grid, &block);
+  rc = launch(P, resolve_path(A2AV_PATH_AUTO, aligned), 0, sms, s, true, &grid, &block);
   if (rc != A2AV_OK) return rc;
   if (device_status != nullptr) {
     int value = 0;

@@ -56,6 +56,25 @@ struct Params {
 // Host side of Params::limit: every byte offset then stays below 2^62.
 inline long long split_limit(int W, long long rb) { return kMaxBytes / ((long long)W * rb); }
 
+// Host: launch with programmatic stream serialization when `pdl` is set, so
+// that the kernel's CTAs may be scheduled while the previous kernel on the
+// stream is still running (its griddepcontrol.wait keeps the data order).
+template <typename... Args, typename... Vals>
+cudaError_t launch_kernel(void (*kernel)(Args...), dim3 grid, int block, size_t smem,
+                          cudaStream_t s, bool pdl, Vals... vals) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, vals...);
+}
+
 // Per-CTA plan in shared memory.  Offsets are in ROWS; callers multiply by the
 // row size where they need bytes.  Tiles are a power of two bytes long.
 // Rows are padded to kMaxW + 1 entries so that lanes reading a column (lane
@@ -89,6 +108,13 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
+
+  // Programmatic dependent launch (both no-ops for a plain launch): let the
+  // next kernel of the stream start launching, then wait until the previous
+  // one has finished and its writes are visible -- it may have produced the
+  // splits or the inputs, and it may still be reading our outputs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {

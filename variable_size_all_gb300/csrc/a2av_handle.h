@@ -11,4 +11,5 @@ struct a2av_handle {
   int ctas_per_sm;            // 0 = engine default
   int last_path, last_grid, last_block;
   int starve;                 // test hook (A2AV_DEBUG_STARVE): see a2av_create in a2av.h
+  bool pdl;                   // programmatic dependent launch (A2AV_PDL, default on)
 };

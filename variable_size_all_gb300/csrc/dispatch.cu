@@ -88,6 +88,7 @@ __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
 
 __global__ void __launch_bounds__(kRange) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
+  chain_wait();
   const int r = blockIdx.y;
   const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
   if (i0 >= m) return;
@@ -250,6 +251,7 @@ constexpr int kSmallKeys = kScanThreads;           // one key per thread in the 
 
 __global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
+  chain_wait();
   const int r = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NB = D.W * D.K;
   const long long m = D.items[r];
@@ -491,24 +493,6 @@ const GatherKernel kGatherLarge = dispatch_copy_bulk_kernel<4, 2>;
 constexpr int kGatherSmem = 128 * 1024;  // 8 x 16 KiB = 4 x 32 KiB
 constexpr long long kGatherMinRow = 1024;
 
-// Launch a kernel of the chain with programmatic stream serialization: it
-// may begin while the previous kernel on the stream finishes (it waits in
-// chain_wait for that kernel's results).
-template <typename... Args, typename... Vals>
-cudaError_t chained(void (*kernel)(Args...), dim3 grid, int block, size_t smem, cudaStream_t s,
-                    Vals... vals) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, vals...);
-}
 
 struct Layout {
   long long flag, done, S, key_start, key_total, pos, hist, total;
@@ -618,16 +602,21 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
+  // Every kernel of the chain is launched with programmatic stream
+  // serialization: it may be scheduled while its predecessor runs and waits
+  // for that predecessor's results in chain_wait.
+  cudaError_t e;
   if (max_items <= kSmallItems && W * K <= kSmallKeys) {
-    dispatch_small_kernel<<<W, kScanThreads, 0, s>>>(D);
+    e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
-    dispatch_count_kernel<<<grid, kRange, 0, s>>>(D);
-    if (chained(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads, 0, s,
-                D) != cudaSuccess ||
-        chained(dispatch_rank_kernel, grid, 32, 0, s, D) != cudaSuccess)
-      return A2AV_ERR_CUDA;
+    e = launch_kernel(dispatch_count_kernel, grid, kRange, 0, s, h->pdl, D);
+    if (e == cudaSuccess)
+      e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
+                        0, s, true, D);
+    if (e == cudaSuccess) e = launch_kernel(dispatch_rank_kernel, grid, 32, 0, s, true, D);
   }
+  if (e != cudaSuccess) return A2AV_ERR_CUDA;
   bool aligned = row_bytes % 16 == 0 && row_bytes >= kGatherMinRow &&
                  row_bytes <= kGatherLargeStage;
   for (int r = 0; r < W; ++r)
@@ -638,13 +627,13 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
         cudaSuccess)
       return A2AV_ERR_CUDA;
-    if (chained(k, dim3(h->sms), 128, kGatherSmem, s, P, D,
-                small ? kGatherSmallStage : kGatherLargeStage) != cudaSuccess)
-      return A2AV_ERR_CUDA;
-  } else if (chained(dispatch_copy_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s, P,
-                     D) != cudaSuccess) {
-    return A2AV_ERR_CUDA;
+    e = launch_kernel(k, dim3(h->sms), 128, kGatherSmem, s, true, P, D,
+                      small ? kGatherSmallStage : kGatherLargeStage);
+  } else {
+    e = launch_kernel(dispatch_copy_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s,
+                      true, P, D);
   }
+  if (e != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
   return A2AV_OK;
 }

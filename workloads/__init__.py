@@ -46,6 +46,7 @@ __all__ = [
     "cfg3",
     "cfg4",
     "cfg5",
+    "cfg5_lengths",
     "random_case",
     "dispatch_items",
     "random_bits",
@@ -191,7 +192,7 @@ def cfg2(per_rank_bytes: int, seed: int = 0, W: int = 4, row_bytes: int = CFG2_R
 
 
 def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 64,
-         topk: int = 2, zipf_s: float = 1.2, W: int = 8) -> Workload:
+         topk: int = 2, zipf_s: float = 1.2, W: int = 8, dedup: bool = False) -> Workload:
     """W=8 MoE token dispatch with top-2 routing over Zipf(1.2)-popular experts.
 
     Expert popularity rank k (1-based) has weight k^-s; the ids are shuffled
@@ -199,6 +200,10 @@ def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 6
     proportional to those weights (Gumbel top-k, i.e. successive sampling
     without replacement).  One input row per (token, expert) pair, ordered by
     (destination rank, local expert, token), destination = expert // (experts/W).
+
+    ``dedup``: one input row per distinct (token, destination rank) pair
+    instead, ordered by (destination rank, token): a token whose experts sit
+    on the same rank is sent there once.  The routing draws are the same.
     """
     per_rank = experts // W
     rng = np.random.default_rng(np.random.SeedSequence([seed, 3]))
@@ -216,6 +221,10 @@ def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 6
         tok = np.repeat(np.arange(tokens), topk)
         exp = chosen.reshape(-1)
         dest, local = exp // per_rank, exp % per_rank
+        if dedup:
+            # one (token, destination) pair per group; its first expert stands for it
+            first = np.unique(tok * W + dest, return_index=True)[1]
+            tok, exp, dest, local = tok[first], exp[first], dest[first], local[first] * 0
         order = np.lexsort((tok, local, dest))
         tok, exp, dest = tok[order], exp[order], dest[order]
         splits[r] = np.bincount(dest, minlength=W)
@@ -226,7 +235,8 @@ def cfg3(seed: int = 0, tokens: int = 8192, hidden: int = 7168, experts: int = 6
         token_rows.append(x.view(np.uint8).reshape(-1))
     return Workload("cfg3", W, rb, splits, inputs,
                     {"tokens": tokens, "experts": experts, "topk": topk, "routes": routes,
-                     "expert_weight": weights, "token_rows": token_rows, "choices": choices})
+                     "expert_weight": weights, "token_rows": token_rows, "choices": choices,
+                     "dedup": dedup})
 
 
 def cfg4(seed: int = 0, rows: int = 1 << 20, row_bytes: int = 13, alpha: float = 0.1,
@@ -273,19 +283,51 @@ def cfg5(seed: int = 0, features: int = 26, batch: int = 8192, lam: float = 3.0,
                     {"features": features, "batch": batch, "lengths": lengths, "kjt_keys": kjt})
 
 
+def cfg5_lengths(w: Workload) -> Workload:
+    """The bag-length exchange that goes with a ``cfg5`` key exchange.
+
+    A keyed-jagged batch sends, beside its keys, the length of every bag:
+    per rank, one int32 row (4 B) per (feature, bag), ordered by (owner rank,
+    feature, bag) like the keys, so S[r][p] = (features owned by p) x batch.
+    Peer p can cut the keys it received from rank r into bags only with these
+    lengths: their sum over the rows from r is the number of keys from r.
+    """
+    if w.name != "cfg5":
+        raise ValueError("bag lengths go with a cfg5 workload")
+    W, F, B = w.W, w.meta["features"], w.meta["batch"]
+    owned = [[f for f in range(F) if f % W == p] for p in range(W)]
+    splits = np.array([[len(owned[p]) * B for p in range(W)] for _ in range(W)], dtype=np.int64)
+    inputs = [np.ascontiguousarray(np.concatenate([L[fs] for fs in owned]).astype(np.int32))
+              .view(np.uint8).reshape(-1) for L in w.meta["lengths"]]
+    return Workload("cfg5_lengths", W, 4, splits, inputs, {"features": F, "batch": B})
+
+
 def dispatch_items(w: Workload):
     """Unsorted items for the fused dispatch of an MoE or embedding-key workload.
 
     Returns (K, rows, src_rows, keys): per rank, the source rows as bytes and,
     per item, its source row and its key (destination = key // K).
       cfg3: items (token t, choice k) in token-major order, source row t, key =
-            the chosen expert (K = experts per rank).
+            the chosen expert (K = experts per rank); with ``dedup``, one
+            item per distinct (token, destination) in token-major order, key
+            = the destination (K = 1).
       cfg5: items = the keys in feature-major (feature, bag, position) order,
             each its own source row; key = (f mod W) * ceil(F / W) + f // W,
             so that keys order items by (owner, feature).
     Ordering each rank's items stably by key gives exactly ``w.inputs``.
     """
     W = w.W
+    if w.name == "cfg3" and w.meta.get("dedup"):
+        # one item per distinct (token, destination rank); key = destination
+        rows, src, key = w.meta["token_rows"], [], []
+        for ch in w.meta["choices"]:
+            tokens, topk = ch.shape
+            tok = np.repeat(np.arange(tokens), topk)
+            dest = ch.reshape(-1) // (w.meta["experts"] // W)
+            first = np.unique(tok * W + dest, return_index=True)[1]  # token-major order
+            src.append(tok[first].astype(np.int32))
+            key.append(dest[first].astype(np.int32))
+        return 1, rows, src, key
     if w.name == "cfg3":
         K = w.meta["experts"] // W
         rows = w.meta["token_rows"]
