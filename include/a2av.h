@@ -237,6 +237,46 @@ int a2av_dispatch(a2av_handle *h, int keys_per_peer, const void *const *rows_ptr
                   int64_t *const *sorted_pos_ptrs, int64_t *in_splits_dev, int64_t row_bytes,
                   void *workspace, int64_t workspace_bytes, void *stream);
 
+/* Most exchanges a2av_run_multi takes in one launch. */
+#define A2AV_MAX_EXCHANGES 4
+
+/* One exchange of an a2av_run_multi call: the arguments of a2av_run. */
+typedef struct {
+  const void *const *in_ptrs;       /* HOST array of W input pointers */
+  const int64_t *in_splits_dev;     /* DEVICE int64 [W][W] */
+  void *const *out_ptrs;            /* HOST array of W output pointers */
+  int64_t *out_splits_offsets_dev;  /* DEVICE int64 [W][2][W] */
+  int64_t row_bytes;
+} a2av_exchange_t;
+
+/*
+ * a2av_run_multi -- `count` independent exchanges over the handle's W ranks
+ * in ONE kernel launch, e.g. the bag lengths and the keys of a keyed-jagged
+ * embedding batch (the key all-to-all of "Different nccl stream within
+ * EmbeddingKey alltoall", torchrec PR 2570, with the lengths that cut the
+ * keys into bags), or MoE tokens and their per-token scales.  Each entry
+ * means exactly what the same arguments mean to a2av_run, with its own
+ * splits and row size; the result is that of `count` a2av_run calls.  Small
+ * exchanges are bound by launch and prologue latency, which the exchanges
+ * of one call share.
+ *
+ *  count      1 <= count <= A2AV_MAX_EXCHANGES (above: A2AV_ERR_UNSUPPORTED).
+ *  exchanges  HOST array of `count` entries; the pointer arrays they name are
+ *             read during the call only.
+ *
+ * The grid is divided among the exchanges in proportion to their bytes
+ * (each gets at least one CTA).  Engine: vector when the handle's path is
+ * A2AV_PATH_VECTOR; bulk when every row and buffer of every exchange is
+ * 16-byte aligned (path AUTO or BULK); staged otherwise.  Memory rules as for
+ * a2av_run, across all the exchanges: no output may overlap any input,
+ * split matrix or other output of the call.  Validity is checked per
+ * exchange: one with invalid splits writes nothing of its own (no output
+ * byte, no out_splits_offsets entry) and records A2AV_ERR_BAD_SPLITS; the
+ * others are carried out.  Host errors as for a2av_run (any entry), plus
+ * A2AV_ERR_INVALID_ARG for count < 1 or exchanges == NULL.
+ */
+int a2av_run_multi(a2av_handle *h, int count, const a2av_exchange_t *exchanges, void *stream);
+
 /*
  * a2av_status -- read and clear the handle's device status word: the first
  * device-detected error (A2AV_ERR_BAD_SPLITS, A2AV_ERR_TIMEOUT or

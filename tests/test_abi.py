@@ -54,6 +54,8 @@ def test_host_checks_without_gpu(lib):
     assert a2av.a2av_destroy(None) == a2av.OK
     assert a2av.a2av_set_path(None, 0) == a2av.ERR_INVALID_ARG
     assert a2av.a2av_last_launch(None)[0] == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_run_multi(None, []) == a2av.ERR_INVALID_ARG
+    assert lib.a2av_run_multi(None, 1, None, None) == a2av.ERR_INVALID_ARG
 
 
 def test_create_without_device_is_a_cuda_error(lib):

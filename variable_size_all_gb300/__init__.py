@@ -19,6 +19,7 @@ __all__ = [
     "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "a2av_dispatch", "a2av_dispatch_workspace_bytes", "ERR_BAD_INDEX", "MAX_DISPATCH_KEYS",
+    "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
 ]
@@ -28,8 +29,18 @@ ERR_BAD_INDEX = -6
 MAX_DISPATCH_KEYS = 1024
 PATH_AUTO, PATH_VECTOR, PATH_BULK, PATH_STAGED = 0, 1, 2, 3
 MAX_RANKS = 32
+MAX_EXCHANGES = 4
 
 _lib = None
+
+
+class A2avExchange(ctypes.Structure):
+    """``a2av_exchange_t``: one exchange of an ``a2av_run_multi`` call."""
+    _fields_ = [("in_ptrs", ctypes.POINTER(ctypes.c_void_p)),
+                ("in_splits_dev", ctypes.c_void_p),
+                ("out_ptrs", ctypes.POINTER(ctypes.c_void_p)),
+                ("out_splits_offsets_dev", ctypes.c_void_p),
+                ("row_bytes", ctypes.c_int64)]
 
 
 class A2avError(RuntimeError):
@@ -65,11 +76,13 @@ def load():
     lib.a2av_dispatch_workspace_bytes.restype = i64
     lib.a2av_dispatch.argtypes = [vp, ci, pp, i64p, pp, pp, i64p, pp, vp, pp, vp, i64, vp, i64, vp]
     lib.a2av_dispatch.restype = ci
+    lib.a2av_run_multi.argtypes = [vp, ci, ctypes.POINTER(A2avExchange), vp]
     lib.a2av_error_string.argtypes = [ci]
     lib.a2av_error_string.restype = ctypes.c_char_p
     lib.a2av_version.argtypes = []
     for f in ("a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
-              "a2av_set_grid", "a2av_last_launch", "a2av_version", "a2av_run_noalloc"):
+              "a2av_set_grid", "a2av_last_launch", "a2av_version", "a2av_run_noalloc",
+              "a2av_run_multi"):
         getattr(lib, f).restype = ci
     _lib = lib
     return lib
@@ -116,6 +129,21 @@ def a2av_combine(handle, in_ptrs, dispatch_splits_offsets_dev: int, out_ptrs,
                                _ptr_array(out_ptrs),
                                ctypes.c_void_p(int(out_splits_offsets_dev) or None),
                                int(row_bytes), ctypes.c_void_p(int(stream) or None))
+
+
+def a2av_run_multi(handle, exchanges, stream: int = 0) -> int:
+    """``exchanges``: a sequence of (in_ptrs, in_splits_dev, out_ptrs,
+    out_splits_offsets_dev, row_bytes), each as for ``a2av_run``."""
+    arr = (A2avExchange * max(len(exchanges), 1))()
+    keep = []
+    for k, (ins, sp, outs, so, rb) in enumerate(exchanges):
+        ia, oa = _ptr_array(ins), _ptr_array(outs)
+        keep += [ia, oa]
+        arr[k] = A2avExchange(ctypes.cast(ia, ctypes.POINTER(ctypes.c_void_p)), int(sp) or None,
+                              ctypes.cast(oa, ctypes.POINTER(ctypes.c_void_p)), int(so) or None,
+                              int(rb))
+    return load().a2av_run_multi(handle, len(exchanges), arr if exchanges else None,
+                                 ctypes.c_void_p(int(stream) or None))
 
 
 def a2av_status(handle, stream: int = 0):
@@ -274,6 +302,38 @@ class A2av:
         W = self.world_size
         self._launch(load().a2av_run, "a2av_run", inputs, in_splits, outputs, out_splits_offsets,
                      row_bytes, stream, (W, W))
+
+    def run_multi(self, exchanges, stream=None):
+        """Several exchanges over the same ranks in one launch (see
+        include/a2av.h, a2av_run_multi).  ``exchanges``: a sequence of
+        (inputs, in_splits, outputs, out_splits_offsets, row_bytes), each as
+        for ``run``."""
+        W = self.world_size
+        if not 1 <= len(exchanges) <= MAX_EXCHANGES:
+            raise ValueError(f"run_multi takes 1..{MAX_EXCHANGES} exchanges")
+        arr = (A2avExchange * len(exchanges))()
+        keep, host = [], False
+        for k, (inputs, splits, outputs, so, rb) in enumerate(exchanges):
+            sp = self._matrix(splits, (W, W), "splits")
+            sop = self._matrix(so, (W, 2, W), "out_splits_offsets")
+            ins, h_in = self._buffers(inputs, "inputs")
+            outs, h_out = self._buffers(outputs, "outputs")
+            host = host or h_in or h_out
+            keep += [ins, outs]
+            arr[k] = A2avExchange(ctypes.cast(ins, ctypes.POINTER(ctypes.c_void_p)), sp,
+                                  ctypes.cast(outs, ctypes.POINTER(ctypes.c_void_p)), sop,
+                                  int(rb))
+        st = ctypes.c_void_p(self._stream(stream) or None)
+        lib = load()
+        if host:  # pinned host buffers: the vector engine (plain loads and stores)
+            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
+            try:
+                rc = lib.a2av_run_multi(self.handle, len(exchanges), arr, st)
+            finally:
+                lib.a2av_set_path(self.handle, self._path)
+        else:
+            rc = lib.a2av_run_multi(self.handle, len(exchanges), arr, st)
+        self._check(rc, "a2av_run_multi")
 
     def combine(self, inputs, dispatch_splits_offsets, outputs, out_splits_offsets,
                 row_bytes: int, stream=None):

@@ -139,8 +139,7 @@ static_assert(kStagedPad % 128 == 0 && kStagedStageBytes % 128 == 0, "128-byte a
 // The k-th of this CTA's tiles, in blocked or round-robin order.
 struct TileSeq {
   long long first, step, count;
-  __device__ TileSeq(long long ntiles, bool blocked) {
-    const long long G = gridDim.x, b = blockIdx.x;
+  __device__ TileSeq(long long ntiles, bool blocked, long long b, long long G) {
     if (blocked) {
       const long long per = (ntiles + G - 1) / G, lo = b * per;
       first = lo;
@@ -155,15 +154,17 @@ struct TileSeq {
   __device__ long long operator[](long long k) const { return first + k * step; }
 };
 
+// Each engine is a device function run by CTA `cta` of the `ctas` CTAs that
+// work on exchange P; its kernel runs it with the whole grid.
 template <int NT, int U, int US>
-__global__ void __launch_bounds__(NT, kVecCtasPerSm)
-    a2av_vector_kernel(const __grid_constant__ Params P, long long max_tile) {
+__device__ __forceinline__ void vector_engine(const Params& P, long long max_tile, int cta,
+                                              int ctas) {
   __shared__ Plan pl;
-  if (!build_plan(P, pl, max_tile)) return;
+  if (!build_plan(P, pl, max_tile, cta, ctas)) return;
   const int W = P.W, tid = threadIdx.x;
   const long long ntiles = pl.tile_first[W];
   const long long rb = P.rb;
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+  for (long long t = cta; t < ntiles; t += ctas) {
     long long lo, hi;
     const int p = tile_peer(pl, W, t, rb, &lo, &hi);
     unsigned char* out = P.out[p];
@@ -177,28 +178,35 @@ __global__ void __launch_bounds__(NT, kVecCtasPerSm)
   }
 }
 
+template <int NT, int U, int US>
+__global__ void __launch_bounds__(NT, kVecCtasPerSm)
+    a2av_vector_kernel(const __grid_constant__ Params P, long long max_tile) {
+  vector_engine<NT, U, US>(P, max_tile, blockIdx.x, gridDim.x);
+}
+
 // ------------------------------------------------------------------ bulk --
 // Every tile's source segments, destination and size are 16-byte aligned.
 // Warp 0 does all the work: each tile is loaded by the lanes of the sources
 // it overlaps (lane r, source r) into one stage, and stored by lane 0 in one
 // piece, which tracks its own bulk stores.
 template <int NS, int LEAD>
-__global__ void __launch_bounds__(kBulkThreads)
-    a2av_bulk_kernel(const __grid_constant__ Params P, int stage_bytes) {
+__device__ __forceinline__ void bulk_engine(const Params& P, int stage_bytes, int cta, int ctas) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 tiles ahead of stores");
   __shared__ Plan pl;
   __shared__ alignas(8) unsigned long long bars[NS];
   __shared__ unsigned char* stage_dst[NS];
   __shared__ unsigned stage_len[NS];
   extern __shared__ __align__(128) unsigned char stages[];
-  if (!build_plan(P, pl, stage_bytes)) return;
+  if (!build_plan(P, pl, stage_bytes, cta, ctas)) return;
   const int lane = threadIdx.x & 31;
   if ((threadIdx.x >> 5) != 0) return;
 
   const int W = P.W;
   const long long ntiles = pl.tile_first[W];
-  const TileSeq tiles(ntiles, A2AV_BULK_BLOCKED_TILES > 0 &&
-                                  ntiles >= (long long)A2AV_BULK_BLOCKED_TILES * gridDim.x);
+  const TileSeq tiles(ntiles,
+                      A2AV_BULK_BLOCKED_TILES > 0 &&
+                          ntiles >= (long long)A2AV_BULK_BLOCKED_TILES * ctas,
+                      cta, ctas);
   const long long nk = tiles.count;
   if (nk == 0) return;
   const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(kBulkThreads)
       if (lane == 0) {
         stage_dst[s] = P.out[p] + lo;
         stage_len[s] = (unsigned)(hi - lo);
-        const unsigned starve = (P.starve && blockIdx.x == 0 && k == 0) ? 16u : 0u;
+        const unsigned starve = (P.starve && cta == 0 && k == 0) ? 16u : 0u;
         mbar_expect_tx(bar, (unsigned)(hi - lo) + starve);
       }
       __syncwarp();
@@ -255,6 +263,12 @@ __global__ void __launch_bounds__(kBulkThreads)
     }
     bulk_wait_all();
   }
+}
+
+template <int NS, int LEAD>
+__global__ void __launch_bounds__(kBulkThreads)
+    a2av_bulk_kernel(const __grid_constant__ Params P, int stage_bytes) {
+  bulk_engine<NS, LEAD>(P, stage_bytes, blockIdx.x, gridDim.x);
 }
 
 // ---------------------------------------------------------------- staged --
@@ -304,17 +318,17 @@ __device__ __forceinline__ void copy_span_smem(unsigned char* d, uint32_t m, int
 }
 
 template <int NS, int NC>
-__global__ void __launch_bounds__(32 * (NC + 1))
-    a2av_staged_kernel(const __grid_constant__ Params P, int stage_bytes) {
+__device__ __forceinline__ void staged_engine(const Params& P, int stage_bytes, int cta,
+                                              int ctas) {
   __shared__ Plan pl;
   __shared__ StageDesc desc[NS];
   __shared__ alignas(8) unsigned long long full[NS];
   __shared__ alignas(8) unsigned long long empty[NS];
   extern __shared__ __align__(128) unsigned char stages[];
-  if (!build_plan(P, pl, stage_bytes)) return;
+  if (!build_plan(P, pl, stage_bytes, cta, ctas)) return;
 
   const int W = P.W, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const TileSeq tiles(pl.tile_first[W], A2AV_STAGED_BLOCKED_TILES != 0);
+  const TileSeq tiles(pl.tile_first[W], A2AV_STAGED_BLOCKED_TILES != 0, cta, ctas);
   const long long nk = tiles.count;
   if (nk == 0) return;
   const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), stage0 = smem_u32(stages);
@@ -364,7 +378,7 @@ __global__ void __launch_bounds__(32 * (NC + 1))
       }
       __syncwarp();
       const uint32_t bar = full0 + 8 * s;
-      const unsigned starve = (P.starve && blockIdx.x == 0 && k == 0) ? 16u : 0u;
+      const unsigned starve = (P.starve && cta == 0 && k == 0) ? 16u : 0u;
       if (lane == 0) mbar_expect_tx(bar, total + starve);
       __syncwarp();
       if (n > 0) bulk_load(stage0 + (uint32_t)s * alloc + off, (const void*)g_lo, gb, bar);
@@ -391,6 +405,94 @@ __global__ void __launch_bounds__(32 * (NC + 1))
   }
 }
 
+template <int NS, int NC>
+__global__ void __launch_bounds__(32 * (NC + 1))
+    a2av_staged_kernel(const __grid_constant__ Params P, int stage_bytes) {
+  staged_engine<NS, NC>(P, stage_bytes, blockIdx.x, gridDim.x);
+}
+
+// ------------------------------------------------------ several at once --
+// Up to A2AV_MAX_EXCHANGES independent exchanges over the same ranks in one
+// launch (a2av_run_multi).  The grid is divided among them in proportion to
+// their bytes, each getting at least one CTA; every CTA computes the same
+// division from the split matrices, then runs its exchange's engine as if
+// that exchange had the launch to itself.
+constexpr int kMaxExchanges = A2AV_MAX_EXCHANGES;
+static_assert(kBulkThreads >= 32 * kMaxExchanges && kStagedThreads >= 32 * kMaxExchanges &&
+                  kVecThreads >= 32 * kMaxExchanges,
+              "multi_slot gives each exchange a warp");
+
+struct MultiParams {
+  Params ex[kMaxExchanges];
+  int count;
+};
+
+// This CTA's exchange, its index among that exchange's CTAs and their
+// number; false for a CTA left over by the rounding.  An exchange whose
+// splits are out of range weighs nothing (its one CTA finds them invalid).
+__device__ bool multi_slot(const MultiParams& M, int* which, int* cta, int* ctas) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ double weight[kMaxExchanges];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, n = M.count;
+  if (warp < n) {  // warp x sums exchange x's bytes (every engine has >= 4 warps)
+    const Params& P = M.ex[warp];
+    const int W = P.W;
+    double rows = 0.0;
+    int bad = 0;
+    for (int e = lane; e < W * W; e += 32) {
+      const long long v = P.splits[(long long)(e / W) * P.split_stride + e % W];
+      if (v < 0 || v > P.limit)
+        bad = 1;
+      else
+        rows += (double)v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rows += __shfl_xor_sync(kFull, rows, o);
+    bad = __any_sync(kFull, bad);
+    if (lane == 0) weight[warp] = bad ? 0.0 : rows * (double)P.rb;
+  }
+  __syncthreads();
+  double total = 0.0;
+  for (int x = 0; x < n; ++x) total += weight[x];
+  const int G = gridDim.x, spare = G - n;
+  int start = 0;
+  for (int x = 0; x < n; ++x) {
+    int g = 1 + (total > 0.0 ? (int)floor((double)spare * (weight[x] / total)) : 0);
+    const int room = G - (n - 1 - x) - start;  // keep one CTA for each later exchange
+    if (g > room) g = room;
+    if ((int)blockIdx.x >= start && (int)blockIdx.x < start + g) {
+      *which = x;
+      *cta = (int)blockIdx.x - start;
+      *ctas = g;
+      return true;
+    }
+    start += g;
+  }
+  return false;
+}
+
+template <int NT, int U, int US>
+__global__ void __launch_bounds__(NT, kVecCtasPerSm)
+    a2av_vector_multi_kernel(const __grid_constant__ MultiParams M, long long max_tile) {
+  int x, cta, ctas;
+  if (multi_slot(M, &x, &cta, &ctas)) vector_engine<NT, U, US>(M.ex[x], max_tile, cta, ctas);
+}
+
+template <int NS, int LEAD>
+__global__ void __launch_bounds__(kBulkThreads)
+    a2av_bulk_multi_kernel(const __grid_constant__ MultiParams M, int stage_bytes) {
+  int x, cta, ctas;
+  if (multi_slot(M, &x, &cta, &ctas)) bulk_engine<NS, LEAD>(M.ex[x], stage_bytes, cta, ctas);
+}
+
+template <int NS, int NC>
+__global__ void __launch_bounds__(32 * (NC + 1))
+    a2av_staged_multi_kernel(const __grid_constant__ MultiParams M, int stage_bytes) {
+  int x, cta, ctas;
+  if (multi_slot(M, &x, &cta, &ctas)) staged_engine<NS, NC>(M.ex[x], stage_bytes, cta, ctas);
+}
+
 }  // namespace
 
 // ================================================================ host ABI ==
@@ -402,6 +504,12 @@ const BulkKernel kBulk = a2av_bulk_kernel<kBulkStages, kBulkLead>;
 const BulkKernel kStaged = a2av_staged_kernel<kStagedStages, kStagedConsumerWarps>;
 using VecKernel = void (*)(Params, long long);
 const VecKernel kVec = a2av_vector_kernel<kVecThreads, kVecUnroll, kVecShiftUnroll>;
+using BulkMultiKernel = void (*)(MultiParams, int);
+const BulkMultiKernel kBulkMulti = a2av_bulk_multi_kernel<kBulkStages, kBulkLead>;
+const BulkMultiKernel kStagedMulti = a2av_staged_multi_kernel<kStagedStages, kStagedConsumerWarps>;
+using VecMultiKernel = void (*)(MultiParams, long long);
+const VecMultiKernel kVecMulti =
+    a2av_vector_multi_kernel<kVecThreads, kVecUnroll, kVecShiftUnroll>;
 
 int env_int(const char* name, int fallback) {
   const char* v = std::getenv(name);
@@ -415,6 +523,12 @@ int configure_kernels() {
                            kBulkStages * kBulkStageBytes) != cudaSuccess)
     return A2AV_ERR_CUDA;
   if (cudaFuncSetAttribute(kStaged, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStagedStages * kStagedAlloc) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  if (cudaFuncSetAttribute(kBulkMulti, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kBulkStages * kBulkStageBytes) != cudaSuccess)
+    return A2AV_ERR_CUDA;
+  if (cudaFuncSetAttribute(kStagedMulti, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kStagedStages * kStagedAlloc) != cudaSuccess)
     return A2AV_ERR_CUDA;
   return A2AV_OK;
@@ -606,6 +720,55 @@ int a2av_combine(a2av_handle* h, const void* const* in_ptrs,
   // out_splits_offsets block of peer p, i.e. rows 2W apart.
   return run_exchange(h, in_ptrs, dispatch_splits_offsets_dev, out_ptrs,
                       out_splits_offsets_dev, row_bytes, stream, 2LL * h->W);
+}
+
+int a2av_run_multi(a2av_handle* h, int count, const a2av_exchange_t* exchanges, void* stream) {
+  if (h == nullptr || exchanges == nullptr || count < 1) return A2AV_ERR_INVALID_ARG;
+  if (count > kMaxExchanges) return A2AV_ERR_UNSUPPORTED;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (dev != h->device) return A2AV_ERR_INVALID_ARG;
+  MultiParams M;
+  std::memset(&M, 0, sizeof(M));
+  M.count = count;
+  bool aligned = true;
+  for (int x = 0; x < count; ++x) {
+    const a2av_exchange_t& e = exchanges[x];
+    if (e.in_ptrs == nullptr || e.out_ptrs == nullptr || e.in_splits_dev == nullptr ||
+        e.out_splits_offsets_dev == nullptr || e.row_bytes < 1)
+      return A2AV_ERR_INVALID_ARG;
+    if (((uintptr_t)e.in_splits_dev & 7) != 0 || ((uintptr_t)e.out_splits_offsets_dev & 7) != 0)
+      return A2AV_ERR_INVALID_ARG;
+    aligned = fill_params(&M.ex[x], h->W, e.in_ptrs, e.in_splits_dev, e.out_ptrs,
+                          e.out_splits_offsets_dev, e.row_bytes, h->in_cap, h->out_cap,
+                          h->d_status, h->W, h->starve) &&
+              aligned;
+  }
+  // One engine for the launch: bulk only when every exchange allows it.
+  const int path = resolve_path(h->path, aligned);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int grid, block;
+  cudaError_t err;
+  if (path == A2AV_PATH_BULK) {
+    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kBulkCtasPerSm);
+    block = kBulkThreads;
+    err = launch_kernel(kBulkMulti, dim3(grid), block, kBulkStages * kBulkStageBytes, s, h->pdl,
+                        M, (int)kBulkStageBytes);
+  } else if (path == A2AV_PATH_STAGED) {
+    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kStagedCtasPerSm);
+    block = kStagedThreads;
+    err = launch_kernel(kStagedMulti, dim3(grid), block, kStagedStages * kStagedAlloc, s, h->pdl,
+                        M, (int)kStagedStageBytes);
+  } else {
+    grid = h->sms * (h->ctas_per_sm ? h->ctas_per_sm : kVecCtasPerSm);
+    block = kVecThreads;
+    err = launch_kernel(kVecMulti, dim3(grid), block, 0, s, h->pdl, M, (long long)kVecMaxTile);
+  }
+  if (err != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  h->last_path = path;
+  h->last_grid = grid;
+  h->last_block = block;
+  return A2AV_OK;
 }
 
 int a2av_status(a2av_handle* h, void* stream, int* device_status) {

@@ -102,9 +102,11 @@ __device__ __forceinline__ void record_error(int* status, int code) {
 
 // Step 1 of the exchange.  Three barriers: load + range check; column scans
 // (out_off) and row scans (in_off) side by side + capacity checks; tiles and
-// out_splits_offsets.  Returns false (in every thread of the CTA) when the
-// splits are invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
-__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
+// out_splits_offsets.  `ctas` CTAs work on this exchange and this one is
+// number `cta` among them (the whole grid, unless several exchanges share a
+// launch).  Returns false (in every thread of the CTA) when the splits are
+// invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
+__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int cta, int ctas) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
@@ -124,7 +126,7 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
     pl.s[r][p] = s;
   }
   if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+    if (cta == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
     return false;
   }
 
@@ -148,7 +150,7 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
     }
   }
   if (__syncthreads_or(bad)) {
-    if (blockIdx.x == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+    if (cta == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
     return false;
   }
 
@@ -158,8 +160,8 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   if (warp == 0) {
     const long long bytes = lane < W ? pl.out_off[lane][W] * P.rb : 0;
     const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
-    const long long ctas = kTilesPerCta * (long long)gridDim.x;
-    const long long per_cta = (total + ctas - 1) / ctas;
+    const long long slots = kTilesPerCta * (long long)ctas;
+    const long long per_cta = (total + slots - 1) / slots;
     int shift = per_cta > 1 ? 64 - __clzll(per_cta - 1) : 0;  // ceil(log2(per_cta))
     const int lo_shift = 63 - __clzll(kTileGranule), hi_shift = 63 - __clzll(max_tile);
     shift = shift < lo_shift ? lo_shift : (shift > hi_shift ? hi_shift : shift);
@@ -171,7 +173,7 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
       pl.tile_shift = shift;
     }
   }
-  if (blockIdx.x == 0) {
+  if (cta == 0) {
     for (int e = tid; e < W * W; e += nt) {
       const int p = e / W, r = e - p * W;
       long long* so = P.out_so + (long long)p * 2 * W;
@@ -181,6 +183,11 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
   }
   __syncthreads();
   return true;
+}
+
+// The whole grid on one exchange.
+__device__ __forceinline__ bool build_plan(const Params& P, Plan& pl, long long max_tile) {
+  return build_plan(P, pl, max_tile, blockIdx.x, gridDim.x);
 }
 
 // Tile t -> peer p and the byte range [lo, hi) of out[p] it covers (all
