@@ -762,8 +762,12 @@ def run_fused_dispatch(args):
     algo = distinct + T + items * (4 + 4 + 8) + 24 * Wn * Wn
     peak, peak_kind = hbm_peak()
     # the copy kernel the library picks: cp.async.bulk gather for 16-byte
-    # aligned rows of 1..32 KiB (torch allocations are aligned), else warp/thread copies
+    # aligned rows of 1..32 KiB (torch allocations are aligned); rows under
+    # 64 bytes copied by the rank kernel itself (past the one-kernel size);
+    # else warp/thread copies
+    small_path = max(m) <= 2048 and Wn * K <= 256
     copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 1024 <= rb <= 32768
+                   else "dispatch_rank_copy_kernel" if rb < 64 and not small_path
                    else "dispatch_copy_kernel")
     roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
@@ -798,7 +802,8 @@ def run_fused_dispatch(args):
                    "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
                           "inputs larger than L2"),
-                   "timing": "CUDA events around the dispatch (one memset and four kernels), "
+                   "timing": "CUDA events around the dispatch (one memset and three or four "
+                             "kernels), "
                              "mean over steps; a spin kernel ahead of each call keeps the "
                              "host's call time outside the events (fused_host_call_us)"},
         "unfused_torch_sort_gather_a2av": {"ms_mean": round(u_mean * 1e3, 4),
@@ -808,7 +813,9 @@ def run_fused_dispatch(args):
         "fused_ms_median": round(f_med * 1e3, 4),
         "fused_host_call_us": round(f_host * 1e6, 1),
         "speedup_vs_unfused": round(u_mean / f_mean, 3),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 4 * args.steps,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": (2 if small_path else 3 if copy_kernel == "dispatch_rank_copy_kernel"
+                         else 4) * args.steps,
         "clocks": clocks.summary(), "parity": parity,
     }
     if rank == 0:

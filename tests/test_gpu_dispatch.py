@@ -130,6 +130,43 @@ def test_dispatch_errors_write_nothing(case):
     assert all(bool((p == -1).all()) for p in pos)
 
 
+@pytest.mark.parametrize("rb", [4, 64, 1024])
+@pytest.mark.parametrize("case", ["key", "src", "capacity", "null_out"])
+def test_large_dispatch_errors_write_nothing(case, rb):
+    """The same checks past the one-kernel size (3000 items per rank): short
+    rows take the rank-and-copy kernel, 64-byte rows the warp copy kernel,
+    1 KiB rows the cp.async.bulk gather."""
+    W, K, m, n = 2, 3, 3000, 500
+    rng = np.random.default_rng(rb)
+    rows = [torch.from_numpy(rng.integers(0, 256, n * rb, dtype=np.uint8)).cuda()
+            for _ in range(W)]
+    src = [torch.from_numpy(rng.integers(0, n, m).astype(np.int32)).cuda() for _ in range(W)]
+    key = [torch.from_numpy(rng.integers(0, W * K, m).astype(np.int32)).cuda() for _ in range(W)]
+    cap = 0
+    outs = [torch.full((W * m * rb,), 0xEE, dtype=torch.uint8, device="cuda") for _ in range(W)]
+    if case == "key":
+        key[1][2999] = W * K
+    elif case == "src":
+        src[0][1234] = n
+    elif case == "capacity":
+        cap = m // 2
+    elif case == "null_out":
+        outs[1] = torch.empty(0, dtype=torch.uint8, device="cuda")
+    pos = [torch.full((m,), -1, dtype=torch.int64, device="cuda") for _ in range(W)]
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    isp = torch.full((W, W), -7, dtype=torch.int64, device="cuda")
+    eng = a2av.A2av(W, 0, cap)
+    eng.dispatch(rows, src, key, K, outs, so, pos, rb, in_splits=isp)
+    st = eng.status()
+    eng.close()
+    want = a2av.ERR_BAD_INDEX if case in ("key", "src") else a2av.ERR_BAD_SPLITS
+    assert st == want
+    torch.cuda.synchronize()
+    assert all(bool((o == 0xEE).all()) for o in outs if o.numel())
+    assert bool((so == -7).all()) and bool((isp == -7).all())
+    assert all(bool((p == -1).all()) for p in pos)
+
+
 def test_dispatch_host_rejections():
     rc, h = a2av.a2av_create(4)
     assert rc == a2av.OK

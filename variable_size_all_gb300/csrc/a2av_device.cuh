@@ -121,7 +121,9 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int ct
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {
     const int r = e / W, p = e - r * W;
-    const long long s = P.splits[(long long)r * P.split_stride + p];
+    // (L2 loads: the splits may have been written during this very launch
+    // by other CTAs, as in the fused dispatch's scan kernel)
+    const long long s = __ldcg(P.splits + (long long)r * P.split_stride + p);
     if (s < 0 || s > P.limit) bad = 1;
     pl.s[r][p] = s;
   }

@@ -17,6 +17,11 @@
 //      the workspace).
 //   When every rank has at most 2048 items and there are at most 256 keys,
 //   one kernel (one CTA per rank, a warp per 256 items) does 1-3 instead.
+//   Rows shorter than 64 bytes (not that small): the last scan CTA of all
+//   ranks also builds and validates the exchange plan (the a2av prologue) and
+//   keeps each rank's row displacement per peer; the rank kernel then copies
+//   every item's row itself as soon as it knows its position (rank + copy in
+//   one kernel, step 4 below not launched).
 //   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
 //      prologue, which also checks capacities and NULL buffers), publish the
 //      positions and the split matrix, then gather every item's row straight
@@ -55,6 +60,9 @@ struct DispatchParams {
   long long item_first[kMaxW + 1];  // exclusive prefix of m_r
   int* flag;                        // workspace: set once input is found invalid
   int* done;                        // workspace: [W] scan CTAs finished per rank
+  int* done_all;                    // workspace: ranks whose scan has finished
+  long long* disp;                  // workspace: [W][W] out_off[p][r] - in_off[r][p] (rows)
+  int fuse;                         // the rank kernel copies the rows (short rows)
   long long* S;                     // workspace: [W][W]
   long long* key_start;             // workspace: [W][NB]
   long long* key_total;             // workspace: [W][NB]
@@ -133,7 +141,8 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 // key_total[r][b] the key's count.  The last CTA of rank r to finish (an
 // atomic count, after a fence) turns the totals into key_start[r][*] (items
 // with a smaller key) and S[r][p] (items with key / K = p).
-__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __grid_constant__ DispatchParams D) {
+__global__ void __launch_bounds__(kScanThreads)
+    dispatch_scan_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   chain_release();
   if (flagged(D)) return;
@@ -204,6 +213,27 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
     for (int k = 0; k < D.K; ++k) s += __ldcg(D.key_total + (long long)r * NB + t * D.K + k);
     D.S[(long long)r * D.W + t] = s;
   }
+  if (!D.fuse) return;
+  // Fused copy: the last rank to finish has the whole split matrix; it runs
+  // the exchange prologue once (validation, offsets, out_splits_offsets) and
+  // keeps the row displacements for the rank kernel.
+  __threadfence();
+  __syncthreads();
+  if (t == 0) last = atomicAdd(D.done_all, 1) == D.W - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, kTileGranule, 0, 1)) {  // records A2AV_ERR_BAD_SPLITS
+    if (t == 0) atomicExch(D.flag, 1);
+    return;
+  }
+  const int W = D.W;
+  for (int e = t; e < W * W; e += kScanThreads) {
+    const int q = e / W, p = e - q * W;
+    D.disp[e] = pl.out_off[p][q] - pl.in_off[q][p];
+    if (D.in_splits_out != nullptr) D.in_splits_out[e] = pl.s[q][p];
+  }
 }
 
 __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
@@ -236,6 +266,70 @@ __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant
     if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
     __syncwarp();
     if (valid) D.pos[(long long)r * D.pos_stride + i] = (int)pos;
+  }
+}
+
+// A row of n bytes, any alignment, copied by one thread.
+__device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned char* s,
+                                                long long n) {
+  const uintptr_t a = (uintptr_t)d | (uintptr_t)s | (uintptr_t)n;
+  if ((a & 7) == 0) {
+    for (long long k = 0; k < n; k += 8)
+      *reinterpret_cast<unsigned long long*>(d + k) =
+          __ldg(reinterpret_cast<const unsigned long long*>(s + k));
+  } else if ((a & 3) == 0) {
+    for (long long k = 0; k < n; k += 4)
+      *reinterpret_cast<unsigned*>(d + k) = __ldg(reinterpret_cast<const unsigned*>(s + k));
+  } else {
+    for (long long k = 0; k < n; ++k) d[k] = __ldg(s + k);
+  }
+}
+
+// Rank and copy (rows shorter than 64 bytes): the rank kernel's ranking,
+// then each lane copies its items' rows straight to their place in the
+// output of their destination and publishes their positions.  The plan was
+// validated by the scan kernel, whose flag stops this kernel otherwise.
+__global__ void __launch_bounds__(32)
+    dispatch_rank_copy_kernel(const __grid_constant__ Params P,
+                              const __grid_constant__ DispatchParams D) {
+  chain_wait();
+  chain_release();
+  if (flagged(D)) return;
+  const int r = blockIdx.y, lane = threadIdx.x, W = D.W, K = D.K, NB = W * K;
+  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
+  if (i0 >= m) return;
+  __shared__ long long next[kMaxBins];
+  __shared__ long long disp[kMaxW];
+  const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
+  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + H[k];
+  if (lane < W) disp[lane] = __ldcg(D.disp + (long long)r * W + lane);
+  int keys[kRange / 32], srcs[kRange / 32];
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    keys[c] = i < m ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
+    srcs[c] = i < m ? D.src[r][i] : 0;
+  }
+  __syncwarp();
+  long long pos[kRange / 32];
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const bool valid = i0 + c * 32 + lane < m;
+    const int key = keys[c];
+    const unsigned same = __match_any_sync(kFull, key);
+    pos[c] = valid ? next[key] + __popc(same & ((1u << lane) - 1u)) : 0;
+    __syncwarp();
+    if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
+    __syncwarp();
+  }
+  const long long rb = P.rb;
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    if (i >= m) continue;
+    const int p = keys[c] / K;
+    D.sorted_pos[r][i] = pos[c];
+    copy_row_thread(P.out[p] + (disp[p] + pos[c]) * rb, P.in[r] + (long long)srcs[c] * rb, rb);
   }
 }
 
@@ -323,22 +417,6 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __gr
 __device__ __forceinline__ void publish_splits(const DispatchParams& D) {
   if (blockIdx.x == 0 && D.in_splits_out != nullptr)
     for (int e = threadIdx.x; e < D.W * D.W; e += blockDim.x) D.in_splits_out[e] = D.S[e];
-}
-
-// A row of n bytes, any alignment, copied by one thread.
-__device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned char* s,
-                                                long long n) {
-  const uintptr_t a = (uintptr_t)d | (uintptr_t)s | (uintptr_t)n;
-  if ((a & 7) == 0) {
-    for (long long k = 0; k < n; k += 8)
-      *reinterpret_cast<unsigned long long*>(d + k) =
-          __ldg(reinterpret_cast<const unsigned long long*>(s + k));
-  } else if ((a & 3) == 0) {
-    for (long long k = 0; k < n; k += 4)
-      *reinterpret_cast<unsigned*>(d + k) = __ldg(reinterpret_cast<const unsigned*>(s + k));
-  } else {
-    for (long long k = 0; k < n; ++k) d[k] = __ldg(s + k);
-  }
 }
 
 __global__ void __launch_bounds__(kCopyThreads)
@@ -495,7 +573,7 @@ constexpr long long kGatherMinRow = 1024;
 
 
 struct Layout {
-  long long flag, done, S, key_start, key_total, pos, hist, total;
+  long long flag, done, done_all, S, disp, key_start, key_total, pos, hist, total;
 };
 
 Layout layout(int W, int K, long long max_items) {
@@ -505,8 +583,10 @@ Layout layout(int W, int K, long long max_items) {
   Layout L;
   L.flag = 0;
   L.done = 4;
+  L.done_all = 4 + 4LL * kMaxW;
   L.S = 256;
-  L.key_start = L.S + up(8LL * W * W);
+  L.disp = L.S + up(8LL * W * W);
+  L.key_start = L.disp + up(8LL * W * W);
   L.key_total = L.key_start + up(8LL * W * NB);
   L.pos = L.key_total + up(8LL * W * NB);
   L.hist = L.pos + up(4LL * W * (max_items < 1 ? 1 : max_items));
@@ -571,7 +651,9 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   D.flag = reinterpret_cast<int*>(ws + L.flag);
   D.done = reinterpret_cast<int*>(ws + L.done);
+  D.done_all = reinterpret_cast<int*>(ws + L.done_all);
   D.S = reinterpret_cast<long long*>(ws + L.S);
+  D.disp = reinterpret_cast<long long*>(ws + L.disp);
   D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
   D.key_total = reinterpret_cast<long long*>(ws + L.key_total);
   D.pos = reinterpret_cast<int*>(ws + L.pos);
@@ -600,20 +682,27 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   P.W = W;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
+  static_assert(4 + 4 * kMaxW + 4 <= 256, "flag and done counters fit the first 256 bytes");
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
   // Every kernel of the chain is launched with programmatic stream
   // serialization: it may be scheduled while its predecessor runs and waits
   // for that predecessor's results in chain_wait.
   cudaError_t e;
-  if (max_items <= kSmallItems && W * K <= kSmallKeys) {
+  const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
+  D.fuse = !small_path && row_bytes < kWarpRowBytes;
+  if (small_path) {
     e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
     e = launch_kernel(dispatch_count_kernel, grid, kRange, 0, s, h->pdl, D);
     if (e == cudaSuccess)
       e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
-                        0, s, true, D);
+                        0, s, true, P, D);
+    if (e == cudaSuccess && D.fuse) {
+      e = launch_kernel(dispatch_rank_copy_kernel, grid, 32, 0, s, true, P, D);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+      return A2AV_OK;
+    }
     if (e == cudaSuccess) e = launch_kernel(dispatch_rank_kernel, grid, 32, 0, s, true, D);
   }
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
