@@ -17,11 +17,11 @@
 //      the workspace).
 //   When every rank has at most 2048 items and there are at most 256 keys,
 //   one kernel (one CTA per rank, a warp per 256 items) does 1-3 instead.
-//   Rows shorter than 64 bytes (not that small): the last scan CTA of all
-//   ranks also builds and validates the exchange plan (the a2av prologue) and
-//   keeps each rank's row displacement per peer; the rank kernel then copies
-//   every item's row itself as soon as it knows its position (rank + copy in
-//   one kernel, step 4 below not launched).
+//   Rows shorter than 64 bytes (not that small): the rank kernel also does
+//   the exchange's prologue for its own rank (every CTA validates the whole
+//   split matrix, as the a2av prologue does, and derives its rank's row
+//   displacement per peer) and copies every item's row as soon as it knows
+//   its position: rank + copy in one kernel, step 4 below not launched.
 //   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
 //      prologue, which also checks capacities and NULL buffers), publish the
 //      positions and the split matrix, then gather every item's row straight
@@ -60,9 +60,6 @@ struct DispatchParams {
   long long item_first[kMaxW + 1];  // exclusive prefix of m_r
   int* flag;                        // workspace: set once input is found invalid
   int* done;                        // workspace: [W] scan CTAs finished per rank
-  int* done_all;                    // workspace: ranks whose scan has finished
-  long long* disp;                  // workspace: [W][W] out_off[p][r] - in_off[r][p] (rows)
-  int fuse;                         // the rank kernel copies the rows (short rows)
   long long* S;                     // workspace: [W][W]
   long long* key_start;             // workspace: [W][NB]
   long long* key_total;             // workspace: [W][NB]
@@ -141,8 +138,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
 // key_total[r][b] the key's count.  The last CTA of rank r to finish (an
 // atomic count, after a fence) turns the totals into key_start[r][*] (items
 // with a smaller key) and S[r][p] (items with key / K = p).
-__global__ void __launch_bounds__(kScanThreads)
-    dispatch_scan_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __grid_constant__ DispatchParams D) {
   chain_wait();
   chain_release();
   if (flagged(D)) return;
@@ -213,27 +209,6 @@ __global__ void __launch_bounds__(kScanThreads)
     for (int k = 0; k < D.K; ++k) s += __ldcg(D.key_total + (long long)r * NB + t * D.K + k);
     D.S[(long long)r * D.W + t] = s;
   }
-  if (!D.fuse) return;
-  // Fused copy: the last rank to finish has the whole split matrix; it runs
-  // the exchange prologue once (validation, offsets, out_splits_offsets) and
-  // keeps the row displacements for the rank kernel.
-  __threadfence();
-  __syncthreads();
-  if (t == 0) last = atomicAdd(D.done_all, 1) == D.W - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  __shared__ Plan pl;
-  if (!build_plan(P, pl, kTileGranule, 0, 1)) {  // records A2AV_ERR_BAD_SPLITS
-    if (t == 0) atomicExch(D.flag, 1);
-    return;
-  }
-  const int W = D.W;
-  for (int e = t; e < W * W; e += kScanThreads) {
-    const int q = e / W, p = e - q * W;
-    D.disp[e] = pl.out_off[p][q] - pl.in_off[q][p];
-    if (D.in_splits_out != nullptr) D.in_splits_out[e] = pl.s[q][p];
-  }
 }
 
 __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
@@ -288,30 +263,84 @@ __device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned
 // Rank and copy (rows shorter than 64 bytes): the rank kernel's ranking,
 // then each lane copies its items' rows straight to their place in the
 // output of their destination and publishes their positions.  The plan was
-// validated by the scan kernel, whose flag stops this kernel otherwise.
-__global__ void __launch_bounds__(32)
+// validated by the scan kernel, whose flag stops this kernel otherwise.  Two
+// warps per CTA, a range each, registers capped so that a whole GPU of them
+// is resident at once (the ranking is a serial chain per warp: more warps
+// in flight, not more work per warp).
+#ifndef A2AV_RANK_COPY_WARPS
+#define A2AV_RANK_COPY_WARPS 2
+#endif
+#ifndef A2AV_RANK_COPY_MIN_CTAS
+#define A2AV_RANK_COPY_MIN_CTAS 18
+#endif
+constexpr int kRankCopyWarps = A2AV_RANK_COPY_WARPS;
+
+__global__ void __launch_bounds__(32 * kRankCopyWarps, A2AV_RANK_COPY_MIN_CTAS)
     dispatch_rank_copy_kernel(const __grid_constant__ Params P,
                               const __grid_constant__ DispatchParams D) {
   chain_wait();
   chain_release();
   if (flagged(D)) return;
-  const int r = blockIdx.y, lane = threadIdx.x, W = D.W, K = D.K, NB = W * K;
-  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
-  if (i0 >= m) return;
-  __shared__ long long next[kMaxBins];
-  __shared__ long long disp[kMaxW];
-  const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
-  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + H[k];
-  if (lane < W) disp[lane] = __ldcg(D.disp + (long long)r * W + lane);
-  int keys[kRange / 32], srcs[kRange / 32];
+  const int r = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int W = D.W, K = D.K, NB = W * K;
+  const long long range = (long long)blockIdx.x * kRankCopyWarps + warp;
+  const long long i0 = range * kRange, m = D.items[r];
+  __shared__ int next_all[kRankCopyWarps][kMaxBins];  // next position of each key in the range
+  __shared__ long long disp[kMaxW];  // out_off[p][r] - in_off[r][p], rows
+  __shared__ int bad_splits;
+  if (warp == 0) {
+    // The a2av prologue's checks on the whole split matrix (identical in
+    // every CTA, so all reach the same verdict): lane p owns column p and
+    // row p.  S was completed by the scan kernel.
+    const int p = lane;
+    long long col = 0, above = 0, row = 0, own = 0;
+    int bad = 0;
+    if (p < W) {
+      for (int q = 0; q < W; ++q) {
+        const long long v = __ldcg(D.S + (long long)q * W + p);  // S[q][p]
+        const long long h = __ldcg(D.S + (long long)p * W + q);  // S[p][q]
+        if (v < 0 || v > P.limit || h < 0 || h > P.limit) bad = 1;
+        if (q < r) above += v;
+        if (q == r) own = v;
+        col += v;
+        row += h;
+      }
+      if ((P.out_cap > 0 && col > P.out_cap) || (P.out[p] == nullptr && col > 0)) bad = 1;
+      if ((P.in_cap > 0 && row > P.in_cap) || (P.in[p] == nullptr && row > 0)) bad = 1;
+    }
+    const long long in_off = warp_inclusive_scan(own, lane) - own;  // in_off[r][p]
+    if (p < W) disp[p] = above - in_off;
+    bad = __any_sync(kFull, bad);
+    if (lane == 0) bad_splits = bad;
+    if (blockIdx.x == 0 && r == 0) {  // one CTA records the verdict and the offsets
+      if (bad) {
+        if (lane == 0) record_error(D.status, A2AV_ERR_BAD_SPLITS);
+      } else if (p < W) {
+        long long* so = P.out_so + (long long)p * 2 * W;
+        long long run = 0;
+        for (int q = 0; q < W; ++q) {
+          const long long v = __ldcg(D.S + (long long)q * W + p);
+          so[q] = v;
+          so[W + q] = run;
+          run += v;
+          if (D.in_splits_out != nullptr) D.in_splits_out[(long long)q * W + p] = v;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (bad_splits || i0 >= m) return;
+  int* next = next_all[warp];
+  const int* H = D.hist + ((long long)r * D.ranges_max + range) * NB;
+  for (int k = lane; k < NB; k += 32) next[k] = (int)D.key_start[(long long)r * NB + k] + H[k];
+  int keys[kRange / 32];
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = i0 + c * 32 + lane;
     keys[c] = i < m ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
-    srcs[c] = i < m ? D.src[r][i] : 0;
   }
   __syncwarp();
-  long long pos[kRange / 32];
+  int pos[kRange / 32];  // positions within the rank: below 2^31 items
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const bool valid = i0 + c * 32 + lane < m;
@@ -323,13 +352,20 @@ __global__ void __launch_bounds__(32)
     __syncwarp();
   }
   const long long rb = P.rb;
+  int srcs[kRange / 32];  // loaded together, after the ranking (fewer live registers)
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    srcs[c] = i < m ? D.src[r][i] : 0;
+  }
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = i0 + c * 32 + lane;
     if (i >= m) continue;
     const int p = keys[c] / K;
     D.sorted_pos[r][i] = pos[c];
-    copy_row_thread(P.out[p] + (disp[p] + pos[c]) * rb, P.in[r] + (long long)srcs[c] * rb, rb);
+    copy_row_thread(P.out[p] + (disp[p] + (long long)pos[c]) * rb,
+                    P.in[r] + (long long)srcs[c] * rb, rb);
   }
 }
 
@@ -573,7 +609,7 @@ constexpr long long kGatherMinRow = 1024;
 
 
 struct Layout {
-  long long flag, done, done_all, S, disp, key_start, key_total, pos, hist, total;
+  long long flag, done, S, key_start, key_total, pos, hist, total;
 };
 
 Layout layout(int W, int K, long long max_items) {
@@ -583,10 +619,8 @@ Layout layout(int W, int K, long long max_items) {
   Layout L;
   L.flag = 0;
   L.done = 4;
-  L.done_all = 4 + 4LL * kMaxW;
   L.S = 256;
-  L.disp = L.S + up(8LL * W * W);
-  L.key_start = L.disp + up(8LL * W * W);
+  L.key_start = L.S + up(8LL * W * W);
   L.key_total = L.key_start + up(8LL * W * NB);
   L.pos = L.key_total + up(8LL * W * NB);
   L.hist = L.pos + up(4LL * W * (max_items < 1 ? 1 : max_items));
@@ -651,9 +685,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   D.flag = reinterpret_cast<int*>(ws + L.flag);
   D.done = reinterpret_cast<int*>(ws + L.done);
-  D.done_all = reinterpret_cast<int*>(ws + L.done_all);
   D.S = reinterpret_cast<long long*>(ws + L.S);
-  D.disp = reinterpret_cast<long long*>(ws + L.disp);
   D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
   D.key_total = reinterpret_cast<long long*>(ws + L.key_total);
   D.pos = reinterpret_cast<int*>(ws + L.pos);
@@ -682,14 +714,14 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   P.W = W;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  static_assert(4 + 4 * kMaxW + 4 <= 256, "flag and done counters fit the first 256 bytes");
+  static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
   // Every kernel of the chain is launched with programmatic stream
   // serialization: it may be scheduled while its predecessor runs and waits
   // for that predecessor's results in chain_wait.
   cudaError_t e;
   const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
-  D.fuse = !small_path && row_bytes < kWarpRowBytes;
+  const bool fuse = !small_path && row_bytes < kWarpRowBytes;  // rank kernel copies the rows
   if (small_path) {
     e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
@@ -697,9 +729,11 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     e = launch_kernel(dispatch_count_kernel, grid, kRange, 0, s, h->pdl, D);
     if (e == cudaSuccess)
       e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
-                        0, s, true, P, D);
-    if (e == cudaSuccess && D.fuse) {
-      e = launch_kernel(dispatch_rank_copy_kernel, grid, 32, 0, s, true, P, D);
+                        0, s, true, D);
+    if (e == cudaSuccess && fuse) {
+      const dim3 grid2((unsigned)((ranges_max + kRankCopyWarps - 1) / kRankCopyWarps),
+                       (unsigned)W);
+      e = launch_kernel(dispatch_rank_copy_kernel, grid2, 32 * kRankCopyWarps, 0, s, true, P, D);
       if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
       return A2AV_OK;
     }
