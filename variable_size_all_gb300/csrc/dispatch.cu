@@ -5,8 +5,8 @@
 // Each rank's items carry a key (destination = key / K) and a source row.
 // The exchange runs on the rank's items ordered stably by key -- the input
 // a2av_run would expect -- without ever materialising that order:
-//   1. count  (grid ranges x W, 256 threads): per range of 256 items, the key
-//      histogram in shared memory; keys and source rows are validated here.
+//   1. count  (a warp per range of 256 items, eight per CTA): per range, the
+//      key histogram in shared memory; keys and source rows are validated here.
 //   2. scan   (grid keys x W, 256 threads): per (key, rank), the exclusive
 //      prefix of the key's count over the ranges (in place); the last CTA of
 //      each rank to finish turns the key totals into key start offsets and
@@ -91,27 +91,44 @@ __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
   record_error(D.status, code);
 }
 
-__global__ void __launch_bounds__(kRange) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
+// A warp per range of 256 items (8 per lane, all loads issued together),
+// eight ranges per CTA, so that a batch of a few thousand ranges is resident
+// in one wave; each warp counts its keys in its own slice of shared memory
+// (dynamic: 8 x W*K ints).
+constexpr int kCountWarps = 8;
+
+__global__ void __launch_bounds__(32 * kCountWarps) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
   chain_wait();
-  const int r = blockIdx.y;
-  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
-  if (i0 >= m) return;
-  __shared__ int hist[kMaxBins];
+  const int r = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long range = (long long)blockIdx.x * kCountWarps + warp;
+  const long long i0 = range * kRange, m = D.items[r];
+  if (i0 >= m) return;  // warps act alone below: no CTA barrier
+  extern __shared__ int count_hist[];
   const int NB = D.W * D.K;
-  for (int b = threadIdx.x; b < NB; b += blockDim.x) hist[b] = 0;
-  __syncthreads();
-  const long long i = i0 + threadIdx.x;
-  if (i < m) {
-    const int key = D.key[r][i], src = D.src[r][i];
-    if (key < 0 || key >= NB || src < 0 || src >= D.rows[r])
-      fail(D, A2AV_ERR_BAD_INDEX);
-    else
-      atomicAdd(&hist[key], 1);
+  int* hist = count_hist + warp * NB;
+  for (int b = lane; b < NB; b += 32) hist[b] = 0;
+  int keys[kRange / 32], srcs[kRange / 32];
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    const long long i = i0 + c * 32 + lane;
+    keys[c] = i < m ? D.key[r][i] : 0;
+    srcs[c] = i < m ? D.src[r][i] : 0;
   }
-  __syncthreads();
-  int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
-  for (int b = threadIdx.x; b < NB; b += blockDim.x) H[b] = hist[b];
+  __syncwarp();
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
+    if (i0 + c * 32 + lane >= m) continue;
+    if (keys[c] < 0 || keys[c] >= NB || srcs[c] < 0 || srcs[c] >= D.rows[r])
+      bad = 1;
+    else
+      atomicAdd(&hist[keys[c]], 1);
+  }
+  if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  __syncwarp();
+  int* H = D.hist + ((long long)r * D.ranges_max + range) * NB;
+  for (int b = lane; b < NB; b += 32) H[b] = hist[b];
 }
 
 // Block-wide exclusive scan of one value per thread (kScanThreads threads);
@@ -726,7 +743,9 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
     const dim3 grid((unsigned)ranges_max, (unsigned)W);
-    e = launch_kernel(dispatch_count_kernel, grid, kRange, 0, s, h->pdl, D);
+    const dim3 grid_count((unsigned)((ranges_max + kCountWarps - 1) / kCountWarps), (unsigned)W);
+    e = launch_kernel(dispatch_count_kernel, grid_count, 32 * kCountWarps,
+                      (size_t)kCountWarps * W * K * sizeof(int), s, h->pdl, D);
     if (e == cudaSuccess)
       e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
                         0, s, true, D);
