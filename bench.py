@@ -183,13 +183,24 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_source_sha() -> str:
-    """Hash of every CUDA source the kernels are built from."""
-    csrc = os.path.join(ROOT, "variable_size_all_gb300", "csrc")
+# The sources each family of kernels is compiled from: the fused dispatch's
+# kernels live in dispatch.cu, every other kernel in a2av.cu; both include the
+# shared device header and the C header.
+_SHARED_SOURCES = ["variable_size_all_gb300/csrc/a2av_device.cuh",
+                   "variable_size_all_gb300/csrc/a2av_handle.h", "include/a2av.h"]
+
+
+def kernel_sources(kernel: str) -> list:
+    own = "dispatch.cu" if kernel.startswith("dispatch_") else "a2av.cu"
+    return [f"variable_size_all_gb300/csrc/{own}"] + _SHARED_SOURCES
+
+
+def kernel_source_sha(kernel: str = "a2av_bulk_kernel") -> str:
+    """Hash of the CUDA sources the named kernel is built from."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        h.update(name.encode())
-        h.update(open(os.path.join(csrc, name), "rb").read())
+    for rel in kernel_sources(kernel):
+        h.update(rel.encode())
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -203,7 +214,7 @@ def measured_traffic(kernel: str, algo_bytes: int):
     except (OSError, ValueError):
         return None
     e = d.get(kernel)
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(kernel.split(":")[0]):
         return None
     return int(round(e["dram_bytes"] / e["algorithmic_bytes"] * algo_bytes))
 
