@@ -61,3 +61,45 @@ def test_graph_replay_with_new_splits(path, rb):
     torch.cuda.synchronize()
     assert eng.status() == a2av.ERR_BAD_SPLITS
     eng.close()
+
+
+def test_graph_replay_multi_with_new_splits():
+    """Two exchanges of one a2av_run_multi launch, captured once: new split
+    values for both are written between replays."""
+    W, cap_rows = 3, 2000
+    rng = np.random.default_rng(42)
+    rbs = [4, 8]
+    inputs = [[rng.integers(0, 256, cap_rows * rb, dtype=np.uint8) for _ in range(W)]
+              for rb in rbs]
+    d_in = [[torch.from_numpy(b).cuda() for b in x] for x in inputs]
+    d_out = [[torch.full((W * cap_rows * rb,), 0xEE, dtype=torch.uint8, device="cuda")
+              for _ in range(W)] for rb in rbs]
+    S = [torch.zeros((W, W), dtype=torch.int64, device="cuda") for _ in rbs]
+    so = [torch.empty((W, 2, W), dtype=torch.int64, device="cuda") for _ in rbs]
+    eng = a2av.A2av(W, in_capacity_rows=cap_rows, out_capacity_rows=W * cap_rows)
+    ex = [(d_in[k], S[k], d_out[k], so[k], rbs[k]) for k in range(2)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        eng.run_multi(ex, stream=s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        eng.run_multi(ex, stream=s)
+    for trial in range(3):
+        splits = [np.stack([rng.multinomial(int(rng.integers(0, cap_rows + 1)),
+                                            rng.dirichlet([0.5] * W)) for _ in range(W)])
+                  for _ in rbs]
+        for k in range(2):
+            S[k].copy_(torch.from_numpy(splits[k].astype(np.int64)))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert eng.status() == a2av.OK
+        for k, rb in enumerate(rbs):
+            used = [b[: int(splits[k][r].sum()) * rb] for r, b in enumerate(inputs[k])]
+            ref, ref_so = oracle.default().exchange(used, splits[k], rb)
+            assert np.array_equal(so[k].cpu().numpy(), ref_so)
+            for p in range(W):
+                got = d_out[k][p][: ref[p].size].cpu().numpy()
+                assert np.array_equal(got, ref[p]), (trial, k, p)
+    eng.close()
