@@ -39,6 +39,33 @@ def test_moved_and_algorithmic_bytes():
     assert bench.whole_job_value(10.0, 4, 2.0) == 20.0
 
 
+def test_traffic_counters_follow_their_kernels_sources(tmp_path, monkeypatch):
+    """A counter is reported only while its kernel family's sources hash to
+    the value recorded with it: the dispatch kernels and the exchange engines
+    are built from different files."""
+    ex, dp = bench.kernel_source_sha("a2av_bulk_kernel"), bench.kernel_source_sha("dispatch_x")
+    assert ex != dp and ex == bench.kernel_source_sha("a2av_staged_multi_kernel")
+    assert "dispatch.cu" in bench.kernel_sources("dispatch_rank_copy_kernel")[0]
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps({
+        "a2av_bulk_kernel:w": {"source_sha": ex, "dram_bytes": 50, "algorithmic_bytes": 100},
+        "dispatch_copy_kernel:w": {"source_sha": ex, "dram_bytes": 50, "algorithmic_bytes": 100}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for rel in bench.kernel_sources("dispatch_x") + bench.kernel_sources("a2av_x"):
+        (tmp_path / rel).parent.mkdir(parents=True, exist_ok=True)
+        (tmp_path / rel).write_bytes(open(os.path.join(ROOT, rel), "rb").read())
+    assert bench.measured_traffic("a2av_bulk_kernel:w", 1000) == 500
+    assert bench.measured_traffic("dispatch_copy_kernel:w", 1000) is None  # recorded for other sources
+    assert bench.measured_traffic("a2av_bulk_kernel:other", 1000) is None
+
+
+def test_workload_descriptions():
+    assert "distinct (token, destination rank)" in bench.describe("cfg3", 0, 0, dedup=True)
+    assert "distinct" not in bench.describe("cfg3", 0, 0)
+    assert "4096 MiB/rank" in bench.describe("cfg2", 1 << 32, 0)
+
+
 def test_reference_arm_runs_on_cpu():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--per-rank-bytes", str(1 << 22), "--steps", "3", "--warmup", "1"],
