@@ -100,6 +100,16 @@ def test_four_mixed_exchanges(path, seed):
         _check(x, d)
 
 
+@pytest.mark.parametrize("W", [1, 32])
+def test_extreme_world_sizes(W):
+    ws = [wl.random_case(70 + W, W, rb, max_rows=40, mode=mode)
+          for rb, mode in ((24, "uniform"), (5, "sparse"), (64, "skew"))]
+    devs, st, _ = _run_multi(ws)
+    assert st == a2av.OK
+    for x, d in zip(ws, devs):
+        _check(x, d)
+
+
 def test_lopsided_sizes_each_get_a_cta():
     big = wl.cfg2(1 << 24, seed=3)  # 16 MiB per rank
     tiny = wl.random_case(9, 4, 16, mode="one")
