@@ -430,7 +430,7 @@ struct MultiParams {
 // This CTA's exchange, its index among that exchange's CTAs and their
 // number; false for a CTA left over by the rounding.  An exchange whose
 // splits are out of range weighs nothing (its one CTA finds them invalid).
-__device__ bool multi_slot(const MultiParams& M, int* which, int* cta, int* ctas) {
+__device__ __forceinline__ bool multi_slot(const MultiParams& M, int* which, int* cta, int* ctas) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ double weight[kMaxExchanges];
