@@ -86,7 +86,11 @@
 #define A2AV_STAGED_STAGE_BYTES (32 * 1024)
 #endif
 #ifndef A2AV_STAGED_CONSUMER_WARPS
-#define A2AV_STAGED_CONSUMER_WARPS 8  // measured: 8 beat 4, 6, 12 and 16 on 13-byte rows
+// Measured: 8 consumer warps beat 4 by 1-4 % on 13-byte rows at 2^20 rows per
+// rank, but cost the latency-bound cases more (the one-launch keyed-jagged
+// pair +1.2 us = +9 %, small exchanges +0.2 us), whether or not all of them
+// consume: the larger CTA itself is slower to get going.
+#define A2AV_STAGED_CONSUMER_WARPS 4
 #endif
 #ifndef A2AV_STAGED_CTAS_PER_SM
 #define A2AV_STAGED_CTAS_PER_SM 1
