@@ -673,10 +673,12 @@ def run_ours(args):
 
 
 # ------------------------------------------------------ fused dispatch ----
-# A spin kernel this long (about 125 us at 2.07 GHz) runs ahead of every
-# timed call of a multi-launch op, so that the host has enqueued the whole op
-# before its first event is reached: the events then bracket device time only.
-SPIN_CYCLES = 1 << 18
+# A spin kernel this long (about 1 ms at 2.07 GHz) runs ahead of every timed
+# call of a multi-launch op, so that the host has enqueued the whole op before
+# its first event is reached: the events then bracket device time only.  (A
+# shorter spin, 125 us, let occasional host pauses of the Python binding land
+# between the events.)
+SPIN_CYCLES = 1 << 21
 
 
 def _timed(torch, stream, fn, reps, cold, flush):
