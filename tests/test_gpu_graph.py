@@ -103,3 +103,47 @@ def test_graph_replay_multi_with_new_splits():
                 got = d_out[k][p][: ref[p].size].cpu().numpy()
                 assert np.array_equal(got, ref[p]), (trial, k, p)
     eng.close()
+
+
+@pytest.mark.parametrize("rb,tokens", [(8, 3000), (14336 // 8, 256), (64, 3000)])
+def test_graph_replay_dispatch_with_new_keys(rb, tokens):
+    """The fused dispatch (a workspace memset and its chain of kernels)
+    captured once; new keys and source rows are written into the same device
+    buffers between replays.  Covers the rank-and-copy path (8-byte rows),
+    the cp.async.bulk gather (1792-byte rows) and the warp copy (64-byte)."""
+    W, K = 4, 3
+    rng = np.random.default_rng(rb)
+    n_rows = tokens
+    rows = [rng.integers(0, 256, n_rows * rb, dtype=np.uint8) for _ in range(W)]
+    d_rows = [torch.from_numpy(r).cuda() for r in rows]
+    m = 2 * tokens
+    d_src = [torch.zeros(m, dtype=torch.int32, device="cuda") for _ in range(W)]
+    d_key = [torch.zeros(m, dtype=torch.int32, device="cuda") for _ in range(W)]
+    d_pos = [torch.empty(m, dtype=torch.int64, device="cuda") for _ in range(W)]
+    d_out = [torch.full((W * m * rb,), 0xEE, dtype=torch.uint8, device="cuda") for _ in range(W)]
+    so = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    eng = a2av.A2av(W)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        eng.dispatch(d_rows, d_src, d_key, K, d_out, so, d_pos, rb, stream=s)  # allocates the workspace
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        eng.dispatch(d_rows, d_src, d_key, K, d_out, so, d_pos, rb, stream=s)
+    for trial in range(3):
+        src = [rng.integers(0, n_rows, m).astype(np.int32) for _ in range(W)]
+        key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
+        for r in range(W):
+            d_src[r].copy_(torch.from_numpy(src[r]))
+            d_key[r].copy_(torch.from_numpy(key[r]))
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert eng.status() == a2av.OK
+        ref, ref_so, ref_pos, _ = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+        assert np.array_equal(so.cpu().numpy(), ref_so)
+        for p in range(W):
+            assert np.array_equal(d_out[p][: ref[p].size].cpu().numpy(), ref[p]), (trial, p)
+        for r in range(W):
+            assert np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r]), (trial, r)
+    eng.close()
