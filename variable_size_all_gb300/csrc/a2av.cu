@@ -16,7 +16,8 @@
 //   2. The received streams of all peers, each contiguous in its output
 //      buffer, are cut into equal tiles of at most `max_tile` bytes; the tile
 //      size shrinks with the payload so that small exchanges still occupy the
-//      whole GPU.  CTAs take tiles round-robin.  A tile maps to one peer p and
+//      whole GPU.  CTAs take tiles round-robin (the bulk engine: blocked runs
+//      once every CTA has over a thousand tiles).  A tile maps to one peer p and
 //      a contiguous byte range of out[p]; the source chunks it overlaps are
 //      found from out_off[p][*].  This is the pages' "shift CTAs onto the
 //      data-parallel dimension" (same page, section "Change") taken to its
@@ -38,7 +39,10 @@
 //        shuffle of neighbouring granules and a funnel shift.
 //      No cluster multicast anywhere.  Every mbarrier wait is bounded (~1 s),
 //      after which the kernel records A2AV_ERR_TIMEOUT and leaves.
-//   CTA 0 writes out_splits_offsets.
+//   CTA 0 writes out_splits_offsets.  Every kernel is launched with
+//   programmatic dependent launch and waits for its predecessor on the stream
+//   before it reads anything; a2av_run_multi runs up to four exchanges in one
+//   launch, each on its own share of the grid.
 #include "a2av_device.cuh"
 #include "a2av_handle.h"
 
