@@ -195,12 +195,22 @@ def kernel_sources(kernel: str) -> list:
     return [f"variable_size_all_gb300/csrc/{own}"] + _SHARED_SOURCES
 
 
+def code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed: what the
+    compiler sees, so that editing a comment keeps a kernel's counters."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(kernel: str = "a2av_bulk_kernel") -> str:
-    """Hash of the CUDA sources the named kernel is built from."""
+    """Hash of the code (comments aside) of the CUDA sources the named kernel
+    is built from."""
     h = hashlib.sha256()
     for rel in kernel_sources(kernel):
         h.update(rel.encode())
-        h.update(open(os.path.join(ROOT, rel), "rb").read())
+        h.update(code_only(open(os.path.join(ROOT, rel), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

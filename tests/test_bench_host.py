@@ -60,6 +60,13 @@ def test_traffic_counters_follow_their_kernels_sources(tmp_path, monkeypatch):
     assert bench.measured_traffic("a2av_bulk_kernel:other", 1000) is None
 
 
+def test_comments_do_not_change_a_kernels_hash():
+    a = "int f(int x) { // doubled\n  return 2 * x; /* the\n value */ }\n"
+    b = "int f(int x) {\n  return 2 * x;   }  // reworded comment\n"
+    assert bench.code_only(a) == bench.code_only(b)
+    assert bench.code_only(a) != bench.code_only(a.replace("2 * x", "3 * x"))
+
+
 def test_workload_descriptions():
     assert "distinct (token, destination rank)" in bench.describe("cfg3", 0, 0, dedup=True)
     assert "distinct" not in bench.describe("cfg3", 0, 0)
