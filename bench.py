@@ -773,6 +773,9 @@ def run_fused_dispatch(args):
         torch.cuda.synchronize()
         barrier()
     u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
+    # the same dispatch marshalled once (A2av.bind_dispatch): the host's share per call
+    bound = eng.bind_dispatch(d_rows, d_src, d_key, K, d_out, d_so, d_pos, rb, stream=stream)
+    b_med, b_mean, b_host = _timed(torch, stream, bound, args.steps, cold, flush)
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during the timed region")
     max_s = reduce_max(f_mean, dev)
@@ -835,6 +838,9 @@ def run_fused_dispatch(args):
                                            "host_call_us": round(u_host * 1e6, 1)},
         "fused_ms_median": round(f_med * 1e3, 4),
         "fused_host_call_us": round(f_host * 1e6, 1),
+        "bound_call": {"ms_mean": round(b_mean * 1e3, 4), "ms_median": round(b_med * 1e3, 4),
+                       "host_call_us": round(b_host * 1e6, 1),
+                       "note": "A2av.bind_dispatch: arguments marshalled once"},
         "speedup_vs_unfused": round(u_mean / f_mean, 3),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": None,
         "gpu_launches": (2 if small_path else 3 if copy_kernel == "dispatch_rank_copy_kernel"
@@ -924,7 +930,8 @@ def run_kjt(args):
 
     for _ in range(args.warmup):
         one_launch()
-    variants = {"one_launch": one_launch, "one_stream_pdl": one_stream,
+    bound = eng.bind_run_multi([(*b, x.row_bytes) for b, x in zip(bufs, parts)], stream=stream)
+    variants = {"one_launch": one_launch, "one_launch_bound": bound, "one_stream_pdl": one_stream,
                 "one_stream_no_pdl": lambda: one_stream(eng_plain),
                 "two_streams": two_streams, "cuda_graph": graph.replay}
     times = {}

@@ -19,7 +19,7 @@ __all__ = [
     "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "a2av_dispatch", "a2av_dispatch_workspace_bytes", "ERR_BAD_INDEX", "MAX_DISPATCH_KEYS",
-    "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES",
+    "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES", "BoundCall",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
 ]
@@ -214,6 +214,29 @@ def a2av_dispatch(handle, keys_per_peer: int, rows_ptrs, rows_per_rank, src_row_
 
 
 # --------------------------------------------------------- torch-facing --
+class BoundCall:
+    """One library call whose arguments were marshalled once (``A2av.bind_run``,
+    ``bind_run_multi``, ``bind_dispatch``).  Calling it enqueues the same
+    launch again -- on the stream given at bind time, or on ``stream`` -- with
+    the same buffers: the tensors must stay alive and keep their storage, while
+    the device data they hold (splits, keys, rows) may change between calls.
+    It skips the per-call Python checks and pointer gathering, which cost more
+    host time than a small exchange takes on the device."""
+
+    def __init__(self, engine, fn, what, args, stream_index, keep):
+        self._engine, self._fn, self._what = engine, fn, what
+        self._args, self._si, self._keep = tuple(args), stream_index, keep
+
+    def __call__(self, stream=None):
+        args = self._args
+        if stream is not None:
+            args = list(args)
+            args[self._si] = ctypes.c_void_p(A2av._stream(stream) or None)
+        rc = self._fn(*args)
+        if rc != OK:
+            raise A2avError(rc, self._what)
+
+
 class A2av:
     """One handle over ``world_size`` ranks; tensors in, tensors out.
 
@@ -277,26 +300,45 @@ class A2av:
             raise ValueError(f"{name} must be a contiguous CUDA int64 tensor of shape {shape}")
         return ctypes.c_void_p(t.data_ptr())
 
-    def _launch(self, fn, what, inputs, splits, outputs, out_splits_offsets, row_bytes, stream,
-                split_shape):
+    def _launch_args(self, inputs, splits, outputs, out_splits_offsets, row_bytes, stream,
+                     split_shape):
+        """The C call's arguments (stream last) and whether a buffer is host memory."""
         W = self.world_size
         sp = self._matrix(splits, split_shape, "splits")
         so = self._matrix(out_splits_offsets, (W, 2, W), "out_splits_offsets")
         ins, host_in = self._buffers(inputs, "inputs")
         outs, host_out = self._buffers(outputs, "outputs")
         st = ctypes.c_void_p(self._stream(stream) or None)
+        return [self.handle, ins, sp, outs, so, int(row_bytes), st], host_in or host_out
+
+    def _launch(self, fn, what, inputs, splits, outputs, out_splits_offsets, row_bytes, stream,
+                split_shape):
+        args, host = self._launch_args(inputs, splits, outputs, out_splits_offsets, row_bytes,
+                                       stream, split_shape)
         lib = load()
-        if host_in or host_out:
+        if host:
             # Buffers in pinned host memory are reached with plain loads and
             # stores (zero-copy over the host link): the vector engine.
             self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
             try:
-                rc = fn(self.handle, ins, sp, outs, so, int(row_bytes), st)
+                rc = fn(*args)
             finally:
                 lib.a2av_set_path(self.handle, self._path)
         else:
-            rc = fn(self.handle, ins, sp, outs, so, int(row_bytes), st)
+            rc = fn(*args)
         self._check(rc, what)
+
+    def bind_run(self, inputs, in_splits, outputs, out_splits_offsets, row_bytes: int,
+                 stream=None) -> BoundCall:
+        """``run`` marshalled once: returns a BoundCall that re-enqueues the
+        exchange on these device buffers (pinned host buffers: use ``run``)."""
+        W = self.world_size
+        args, host = self._launch_args(inputs, in_splits, outputs, out_splits_offsets, row_bytes,
+                                       stream, (W, W))
+        if host:
+            raise ValueError("bind_run takes device buffers only")
+        keep = (inputs, in_splits, outputs, out_splits_offsets)
+        return BoundCall(self, load().a2av_run, "a2av_run", args, len(args) - 1, keep)
 
     def run(self, inputs, in_splits, outputs, out_splits_offsets, row_bytes: int, stream=None):
         W = self.world_size
@@ -308,11 +350,24 @@ class A2av:
         include/a2av.h, a2av_run_multi).  ``exchanges``: a sequence of
         (inputs, in_splits, outputs, out_splits_offsets, row_bytes), each as
         for ``run``."""
+        args, host, _ = self._multi_args(exchanges, stream)
+        lib = load()
+        if host:  # pinned host buffers: the vector engine (plain loads and stores)
+            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
+            try:
+                rc = lib.a2av_run_multi(*args)
+            finally:
+                lib.a2av_set_path(self.handle, self._path)
+        else:
+            rc = lib.a2av_run_multi(*args)
+        self._check(rc, "a2av_run_multi")
+
+    def _multi_args(self, exchanges, stream):
         W = self.world_size
         if not 1 <= len(exchanges) <= MAX_EXCHANGES:
             raise ValueError(f"run_multi takes 1..{MAX_EXCHANGES} exchanges")
         arr = (A2avExchange * len(exchanges))()
-        keep, host = [], False
+        keep, host = [arr], False
         for k, (inputs, splits, outputs, so, rb) in enumerate(exchanges):
             sp = self._matrix(splits, (W, W), "splits")
             sop = self._matrix(so, (W, 2, W), "out_splits_offsets")
@@ -324,16 +379,15 @@ class A2av:
                                   ctypes.cast(outs, ctypes.POINTER(ctypes.c_void_p)), sop,
                                   int(rb))
         st = ctypes.c_void_p(self._stream(stream) or None)
-        lib = load()
-        if host:  # pinned host buffers: the vector engine (plain loads and stores)
-            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
-            try:
-                rc = lib.a2av_run_multi(self.handle, len(exchanges), arr, st)
-            finally:
-                lib.a2av_set_path(self.handle, self._path)
-        else:
-            rc = lib.a2av_run_multi(self.handle, len(exchanges), arr, st)
-        self._check(rc, "a2av_run_multi")
+        return [self.handle, len(exchanges), arr, st], host, keep
+
+    def bind_run_multi(self, exchanges, stream=None) -> BoundCall:
+        """``run_multi`` marshalled once (device buffers only)."""
+        args, host, keep = self._multi_args(exchanges, stream)
+        if host:
+            raise ValueError("bind_run_multi takes device buffers only")
+        return BoundCall(self, load().a2av_run_multi, "a2av_run_multi", args, 3,
+                         keep + [exchanges])
 
     def combine(self, inputs, dispatch_splits_offsets, outputs, out_splits_offsets,
                 row_bytes: int, stream=None):
@@ -345,7 +399,8 @@ class A2av:
                      outputs, out_splits_offsets, row_bytes, stream, (W, 2, W))
 
     def dispatch(self, rows, src_rows, keys, keys_per_peer: int, outputs, out_splits_offsets,
-                 sorted_pos, row_bytes: int, in_splits=None, workspace=None, stream=None):
+                 sorted_pos, row_bytes: int, in_splits=None, workspace=None, stream=None,
+                 _bind=False):
         """Fused dispatch: group each rank's items by key on the device and
         exchange their rows (see include/a2av.h, a2av_dispatch).
 
@@ -393,12 +448,26 @@ class A2av:
         outs_arr, host_outs = self._buffers(outputs, "outputs")
         if host_rows or host_outs:
             raise ValueError("a2av_dispatch takes device buffers only")
-        rc = a2av_dispatch(self.handle, keys_per_peer, list(rows_arr), n_rows,
-                           ptr(src_rows), ptr(keys), items, list(outs_arr),
-                           out_splits_offsets.data_ptr(), ptr(sorted_pos),
-                           0 if in_splits is None else in_splits.data_ptr(), row_bytes,
-                           workspace.data_ptr(), workspace.numel(), self._stream(stream))
-        self._check(rc, "a2av_dispatch")
+        args = [self.handle, int(keys_per_peer), _ptr_array(list(rows_arr)), _i64_array(n_rows),
+                _ptr_array(ptr(src_rows)), _ptr_array(ptr(keys)), _i64_array(items),
+                _ptr_array(list(outs_arr)), ctypes.c_void_p(out_splits_offsets.data_ptr()),
+                _ptr_array(ptr(sorted_pos)),
+                ctypes.c_void_p(None if in_splits is None else in_splits.data_ptr()),
+                int(row_bytes), ctypes.c_void_p(workspace.data_ptr()), int(workspace.numel()),
+                ctypes.c_void_p(self._stream(stream) or None)]
+        if _bind:
+            keep = (rows, src_rows, keys, outputs, out_splits_offsets, sorted_pos, in_splits,
+                    workspace)
+            return BoundCall(self, load().a2av_dispatch, "a2av_dispatch", args, 14, keep)
+        self._check(load().a2av_dispatch(*args), "a2av_dispatch")
+
+    def bind_dispatch(self, rows, src_rows, keys, keys_per_peer: int, outputs,
+                      out_splits_offsets, sorted_pos, row_bytes: int, in_splits=None,
+                      workspace=None, stream=None) -> BoundCall:
+        """``dispatch`` marshalled once: the item counts are fixed at bind time
+        (the keys and source rows themselves may change between calls)."""
+        return self.dispatch(rows, src_rows, keys, keys_per_peer, outputs, out_splits_offsets,
+                             sorted_pos, row_bytes, in_splits, workspace, stream, _bind=True)
 
     def status(self, stream=None) -> int:
         rc, v = a2av_status(self.handle, self._stream(stream))
