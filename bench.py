@@ -185,9 +185,8 @@ def hbm_peak():
 
 # The sources each family of kernels is compiled from: the fused dispatch's
 # kernels live in dispatch.cu, every other kernel in a2av.cu; both include the
-# shared device header and the C header.
-_SHARED_SOURCES = ["variable_size_all_gb300/csrc/a2av_device.cuh",
-                   "variable_size_all_gb300/csrc/a2av_handle.h", "include/a2av.h"]
+# shared device header and the C header (a2av_handle.h is host-only).
+_SHARED_SOURCES = ["variable_size_all_gb300/csrc/a2av_device.cuh", "include/a2av.h"]
 
 
 def kernel_sources(kernel: str) -> list:

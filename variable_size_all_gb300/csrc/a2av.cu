@@ -650,6 +650,7 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
   h->starve = env_int("A2AV_DEBUG_STARVE", 0) != 0;
   h->pdl = env_int("A2AV_PDL", 1) != 0;
+  h->gather_ready = false;
   h->last_path = h->last_grid = h->last_block = 0;
   *out = h;
   return A2AV_OK;

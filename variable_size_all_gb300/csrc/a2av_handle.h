@@ -12,4 +12,5 @@ struct a2av_handle {
   int last_path, last_grid, last_block;
   int starve;                 // test hook (A2AV_DEBUG_STARVE): see a2av_create in a2av.h
   bool pdl;                   // programmatic dependent launch (A2AV_PDL, default on)
+  bool gather_ready;          // the dispatch gather kernels' shared-memory opt-in is done
 };

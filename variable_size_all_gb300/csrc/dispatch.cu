@@ -784,9 +784,14 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   if (aligned) {
     const bool small = row_bytes <= kGatherSmallStage;
     const GatherKernel k = small ? kGatherSmall : kGatherLarge;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
-        cudaSuccess)
-      return A2AV_ERR_CUDA;
+    if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
+      if (cudaFuncSetAttribute(kGatherSmall, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGatherSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(kGatherLarge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGatherSmem) != cudaSuccess)
+        return A2AV_ERR_CUDA;
+      h->gather_ready = true;
+    }
     e = launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
                       small ? kGatherSmallStage : kGatherLargeStage);
   } else {
