@@ -152,3 +152,28 @@ def test_host_rejections():
     zero_rb = [(ptrs[0], ptrs[1], ptrs[2], d[3].data_ptr(), 0)]
     assert a2av.a2av_run_multi(eng.handle, zero_rb) == a2av.ERR_INVALID_ARG
     eng.close()
+
+
+def test_pinned_host_buffers_zero_copy():
+    """Pinned host inputs and outputs: the binding selects the vector engine,
+    which reaches host memory with plain loads and stores."""
+    ws = [wl.random_case(90, 3, 24, max_rows=100), wl.random_case(91, 3, 7, max_rows=100)]
+    bufs = []
+    for w in ws:
+        ins = [torch.from_numpy(b).pin_memory() for b in w.inputs]
+        outs = [torch.full(((int(w.splits[:, p].sum()) + SLACK) * w.row_bytes,), SENTINEL,
+                           dtype=torch.uint8).pin_memory() for p in range(w.W)]
+        so = torch.full((w.W, 2, w.W), -7, dtype=torch.int64, device="cuda")
+        bufs.append((ins, torch.from_numpy(w.splits).cuda(), outs, so))
+    eng = a2av.A2av(3)
+    eng.run_multi([(*b, w.row_bytes) for b, w in zip(bufs, ws)])
+    assert eng.status() == a2av.OK
+    assert eng.last_launch()["path"] == a2av.PATH_VECTOR
+    eng.close()
+    for w, (ins, _, outs, so) in zip(ws, bufs):
+        ref, ref_so = oracle.default().exchange(w.inputs, w.splits, w.row_bytes)
+        assert np.array_equal(so.cpu().numpy(), ref_so)
+        for p in range(w.W):
+            got = outs[p].numpy()
+            assert np.array_equal(got[: ref[p].size], ref[p])
+            assert np.all(got[ref[p].size:] == SENTINEL)
