@@ -261,17 +261,17 @@ WORKLOADS = ("cfg2", "cfg1", "cfg3", "cfg4", "cfg5")
 
 
 def describe(name: str, per_rank_bytes: int, seed: int, tokens: int = 8192,
-             batch: int = 8192, dedup: bool = False) -> str:
+             batch: int = 8192, dedup: bool = False, hidden: int = 7168) -> str:
     if name == "cfg2":
         return workload_name(per_rank_bytes)
     if name == "cfg3" and dedup:
-        return (describe(name, per_rank_bytes, seed, tokens, batch).replace(
+        return (describe(name, per_rank_bytes, seed, tokens, batch, hidden=hidden).replace(
             "top-2 of 64 experts", "top-2 of 64 experts, one row per distinct (token, "
             "destination rank) pair"))
-    if name == "cfg3" and tokens != 8192:
-        return (f"a2av W=8 MoE dispatch: {tokens} tokens/rank, hidden 7168 bf16 (14336 B rows), "
-                f"top-2 of 64 experts (8 per rank), Zipf(1.2) popularity shuffled per seed, "
-                f"seed {seed}")
+    if name == "cfg3" and (tokens != 8192 or hidden != 7168):
+        return (f"a2av W=8 MoE dispatch: {tokens} tokens/rank, hidden {hidden} bf16 "
+                f"({2 * hidden} B rows), top-2 of 64 experts (8 per rank), Zipf(1.2) popularity "
+                f"shuffled per seed, seed {seed}")
     if name == "cfg5" and batch != 8192:
         return (f"a2av W=2 embedding keys: 26 features x {batch} bags per rank, "
                 f"min(Poisson(3), 20) int64 keys per bag, U[0, 1e7), feature mod 2 ownership, "
@@ -286,6 +286,31 @@ def describe(name: str, per_rank_bytes: int, seed: int, tokens: int = 8192,
         "cfg5": "a2av W=2 embedding keys: 26 features x 8192 bags per rank, "
                 "min(Poisson(3), 20) int64 keys per bag, U[0, 1e7), feature mod 2 ownership",
     }[name] + f", seed {seed}"
+
+
+def machine() -> dict:
+    """The GPU's name, the host CPU model and the host's core count, recorded
+    with every line (the oracle baseline runs on one of those cores)."""
+    info = {"nproc": os.cpu_count()}
+    try:
+        import torch
+        if torch.cuda.is_available():
+            info["gpu"] = torch.cuda.get_device_name()
+    except Exception:  # noqa: BLE001 -- a name is context, never a reason to fail
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu part", "hardware") and ":" in line:
+                info.setdefault("cpu_model", line.split(":", 1)[1].strip())
+    except OSError:
+        pass
+    return info
+
+
+def emit(line: dict) -> None:
+    line["machine"] = machine()
+    print(json.dumps(line), flush=True)
 
 
 def host_memory_available() -> int:
@@ -316,7 +341,8 @@ def load_workload(args, torch):
         w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
     else:
         gen = {"cfg1": wl.cfg1,
-               "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens, dedup=args.dedup),
+               "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens, dedup=args.dedup,
+                                         hidden=args.hidden),
                "cfg4": wl.cfg4, "cfg5": lambda s: wl.cfg5(s, batch=args.batch)}
         w = gen[args.workload](args.seed)
         h_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
@@ -652,7 +678,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
         "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
-                                        args.dedup), "name": args.workload,
+                                        args.dedup, hidden=args.hidden), "name": args.workload,
                    "op": args.op, "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
                    "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
@@ -678,7 +704,7 @@ def run_ours(args):
         "input_generation_s": round(gen_s, 2),
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(line)
 
 
 # ------------------------------------------------------ fused dispatch ----
@@ -726,8 +752,8 @@ def run_fused_dispatch(args):
     a2av.build()
     if args.workload not in ("cfg3", "cfg5"):
         raise SystemExit("--op fused_dispatch needs --workload cfg3 or cfg5")
-    w = (wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup) if args.workload == "cfg3"
-         else wl.cfg5(args.seed, batch=args.batch))
+    w = (wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup, hidden=args.hidden)
+         if args.workload == "cfg3" else wl.cfg5(args.seed, batch=args.batch))
     K, rows, src, key = wl.dispatch_items(w)
     Wn, rb, S = w.W, w.row_bytes, w.splits
     m = [k.size for k in key]
@@ -821,7 +847,7 @@ def run_fused_dispatch(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
         "config": {"workload": describe(args.workload, args.per_rank_bytes, args.seed,
-                                        args.tokens, args.batch, args.dedup) +
+                                        args.tokens, args.batch, args.dedup, hidden=args.hidden) +
                    " -- items unsorted (token-major / feature-major), grouped on the device",
                    "name": args.workload, "op": "fused_dispatch", "ranks": Wn, "row_bytes": rb,
                    "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
@@ -847,7 +873,7 @@ def run_fused_dispatch(args):
         "clocks": clocks.summary(), "parity": parity,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(line)
 
 
 # ------------------------------------------------------------- overlap ----
@@ -1005,7 +1031,7 @@ def run_kjt(args):
         "clocks": clocks.summary(), "parity": parity,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(line)
 
 
 def run_overlap(args):
@@ -1022,7 +1048,7 @@ def run_overlap(args):
     dist_init("nccl")
     a2av.build()
     if args.workload == "cfg3":
-        w = wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup)
+        w = wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup, hidden=args.hidden)
         parts = [w]  # the MoE token exchange
     elif args.workload == "cfg5":
         w = wl.cfg5(args.seed, batch=args.batch)
@@ -1104,7 +1130,7 @@ def run_overlap(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {"workload": describe(args.workload, 0, args.seed, args.tokens, args.batch,
-                                        args.dedup) +
+                                        args.dedup, hidden=args.hidden) +
                    (" (bag lengths, int32, then keys: two a2av_run per step)"
                     if args.workload == "cfg5" else "") +
                    f" on a side stream, with {reps} bf16 GEMMs {n}x{n}x{n} on the main stream",
@@ -1125,7 +1151,7 @@ def run_overlap(args):
         "cpu_baseline": None, "e2e": None, "parity": parity,
     }
     if rank == 0:
-        print(json.dumps(line), flush=True)
+        emit(line)
 
 
 # ------------------------------------------------------------ reference ----
@@ -1140,7 +1166,8 @@ def run_reference(args):
     if args.workload == "cfg2":
         w = wl.cfg2(P, seed=args.seed)
     else:
-        w = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, dedup=args.dedup), "cfg4": wl.cfg4,
+        w = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, dedup=args.dedup, hidden=args.hidden),
+             "cfg4": wl.cfg4,
              "cfg5": wl.cfg5}[args.workload](args.seed)
     S, inputs, rb, Wn = w.splits, w.inputs, w.row_bytes, w.W
     K, Wm = args.steps, args.warmup
@@ -1158,7 +1185,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
         "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
-                                        args.dedup), "name": args.workload,
+                                        args.dedup, hidden=args.hidden), "name": args.workload,
                    "ranks": Wn, "row_bytes": rb,
                    "per_rank_bytes": int(statistics.mean(b.size for b in inputs)),
                    "parallelism": "one host core"},
@@ -1167,7 +1194,7 @@ def run_reference(args):
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
-    print(json.dumps(line), flush=True)
+    emit(line)
 
 
 def main(argv=None):
@@ -1187,6 +1214,7 @@ def main(argv=None):
     ap.add_argument("--gemm-n", type=int, default=8192)
     ap.add_argument("--tokens", type=int, default=8192, help="cfg3 tokens per rank")
     ap.add_argument("--batch", type=int, default=8192, help="cfg5 bags per feature and rank")
+    ap.add_argument("--hidden", type=int, default=7168, help="cfg3 hidden size (bf16 elements)")
     ap.add_argument("--dedup", action="store_true",
                     help="cfg3: one row per distinct (token, destination rank) pair")
     ap.add_argument("--seed", type=int, default=0)
