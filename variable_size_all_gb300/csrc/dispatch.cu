@@ -48,8 +48,14 @@ constexpr int kScanBatch = 16;  // counts a scan thread loads at once
 static_assert(kMaxBins <= 4 * kScanThreads, "the finishing scan CTA holds 4 keys per thread");
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 4;
+constexpr int kCopyCtasPerSmWarpRows = 3;  // the vector runs want up to 85 registers
 constexpr long long kWarpRowBytes = 64;  // rows this long get a warp each
 constexpr int kItemsPerThread = 4;      // items a thread copies at once (short rows)
+#ifndef A2AV_COPY_VEC_ROWS
+#define A2AV_COPY_VEC_ROWS 4
+#endif
+constexpr int kVecRows = A2AV_COPY_VEC_ROWS;  // 16-byte vectors a lane keeps in flight (warp rows)
+constexpr long long kVecMaxRow = 64 * 1024;  // flat vector runs up to this row size
 
 struct DispatchParams {
   const int* key[kMaxW];
@@ -67,6 +73,7 @@ struct DispatchParams {
   int* pos;                         // workspace: [W][pos_stride] item positions in key order
   int* status;
   long long* in_splits_out;         // optional [W][W]
+  int vec16;                        // every row and buffer 16-byte aligned
   long long ranges_max;
   long long pos_stride;
   int W, K;
@@ -472,7 +479,23 @@ __device__ __forceinline__ void publish_splits(const DispatchParams& D) {
     for (int e = threadIdx.x; e < D.W * D.W; e += blockDim.x) D.in_splits_out[e] = D.S[e];
 }
 
-__global__ void __launch_bounds__(kCopyThreads)
+// The warp's n rows one at a time with the realigning span copy (rows not
+// 16-byte aligned, or very long); kept out of line so that its registers do
+// not weigh on the vector path of the kernel that calls it.
+__device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc, int n,
+                                                 long long rb, int lane) {
+  for (int j = 0; j < n; ++j) {
+    unsigned char* dst = reinterpret_cast<unsigned char*>(__shfl_sync(kFull, mdst, j));
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(__shfl_sync(kFull, msrc, j));
+    copy_span<32, 4, 2>(dst, src, rb, lane);
+  }
+}
+
+// kWarpRows: rows of kWarpRowBytes or more, a warp per row (each kernel
+// instantiation holds one of the two loops, so neither pays the other's
+// registers).
+template <bool kWarpRows>
+__global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRows : kCopyCtasPerSm)
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   if (flagged(D)) return;
@@ -481,25 +504,55 @@ __global__ void __launch_bounds__(kCopyThreads)
   publish_splits(D);
   const int W = D.W, K = D.K;
   const long long rb = P.rb, total = D.item_first[W];
-  const bool warp_rows = rb >= kWarpRowBytes;
+  constexpr bool warp_rows = kWarpRows;
   const long long team = warp_rows ? (long long)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5)
                                    : (long long)blockIdx.x * kCopyThreads + threadIdx.x;
   const long long teams = warp_rows ? (long long)gridDim.x * (kCopyThreads / 32)
                                     : (long long)gridDim.x * kCopyThreads;
-  if (warp_rows) {
-    for (long long g = team; g < total; g += teams) {
-      int r = 0;
-      while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
-      const long long i = g - D.item_first[r];
-      const int p = D.key[r][i] / K;
-      const long long pos = D.pos[(long long)r * D.pos_stride + i];
-      if ((threadIdx.x & 31) == 0) D.sorted_pos[r][i] = pos;
-      unsigned char* dst = P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb;
-      const unsigned char* src = P.in[r] + (long long)D.src[r][i] * rb;
-      copy_span<32, 4, 2>(dst, src, rb, threadIdx.x & 31);
+  if constexpr (warp_rows) {
+    // A warp takes 32 consecutive items: lane l reads item l's key, position
+    // and source row (one round trip for all 32), then the warp copies the
+    // 32 rows.  16-byte aligned rows are copied as one flat run of vectors
+    // over all 32 rows, kVecRows x 16 bytes per lane in flight; other rows
+    // one at a time with the realigning span copy.
+    const int lane = threadIdx.x & 31;
+    for (long long g0 = team * 32; g0 < total; g0 += teams * 32) {
+      const long long g = g0 + lane;
+      long long mdst = 0, msrc = 0;
+      if (g < total) {
+        int r = 0;
+        while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+        const long long i = g - D.item_first[r];
+        const int p = D.key[r][i] / K;
+        const long long pos = D.pos[(long long)r * D.pos_stride + i];
+        D.sorted_pos[r][i] = pos;
+        mdst = (long long)(P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb);
+        msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+      }
+      const int n = total - g0 < 32 ? (int)(total - g0) : 32;
+      if (D.vec16 && rb <= kVecMaxRow) {
+        const unsigned V = (unsigned)(rb >> 4), nv = (unsigned)n * V;  // < 2^17
+        for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVecRows) {  // warp-uniform trip count
+          uint4 v[kVecRows];
+          long long d[kVecRows];
+#pragma unroll
+          for (int q = 0; q < kVecRows; ++q) {
+            const unsigned idx = b0 + q * 32 + lane;
+            const bool ok = idx < nv;
+            const unsigned j = ok ? idx / V : 0, c = ok ? idx - j * V : 0;
+            const long long s = __shfl_sync(kFull, msrc, (int)j);
+            d[q] = __shfl_sync(kFull, mdst, (int)j) + 16LL * c;
+            if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s) + c);
+          }
+#pragma unroll
+          for (int q = 0; q < kVecRows; ++q)
+            if (b0 + q * 32 + lane < nv) st_stream(reinterpret_cast<uint4*>(d[q]), v[q]);
+        }
+      } else {
+        copy_rows_unaligned(mdst, msrc, n, rb, lane);
+      }
     }
-    return;
-  }
+  } else {
   // Short rows: a thread takes kItemsPerThread items, their key, source row
   // and position loads issued together, then copies the rows.
   for (long long g0 = team; g0 < total; g0 += teams * kItemsPerThread) {
@@ -528,6 +581,7 @@ __global__ void __launch_bounds__(kCopyThreads)
       copy_row_thread(P.out[p] + (pl.out_off[p][r] + pos[q] - pl.in_off[r][p]) * rb,
                       P.in[r] + (long long)src_row[q] * rb, rb);
     }
+  }
   }
 }
 
@@ -640,7 +694,15 @@ const GatherKernel kGatherLarge =
 constexpr int kGatherSmem = A2AV_GATHER_STAGES * kGatherSmallStage;  // = stages/2 x 32 KiB
 static_assert(A2AV_GATHER_STAGES % 2 == 0 && A2AV_GATHER_LEAD < A2AV_GATHER_STAGES,
               "the large ring halves the small one");
-constexpr long long kGatherMinRow = 1024;
+// Aligned rows this long or longer take the bulk gather; shorter ones the
+// warp copy's flat vector runs.  Measured on the MoE dispatch (8192 tokens,
+// top-2, W=8): rows of 1 / 2 / 4 KiB 77 / 141 / 263 us by warp copy against
+// ~405 us by gather (too few bytes in flight at a row per stage); 8 and 14 KiB
+// rows 412 / 459 us by gather against 506 / 868 us.
+#ifndef A2AV_GATHER_MIN_ROW
+#define A2AV_GATHER_MIN_ROW 8192
+#endif
+constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 
 
 struct Layout {
@@ -731,6 +793,10 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   D.ranges_max = ranges_max;
   D.W = W;
   D.K = K;
+  bool vec16 = row_bytes % 16 == 0;
+  for (int r = 0; r < W; ++r)
+    vec16 = vec16 && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
+  D.vec16 = vec16 ? 1 : 0;
 
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -777,10 +843,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     if (e == cudaSuccess) e = launch_kernel(dispatch_rank_kernel, grid, 32, 0, s, true, D);
   }
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
-  bool aligned = row_bytes % 16 == 0 && row_bytes >= kGatherMinRow &&
-                 row_bytes <= kGatherLargeStage;
-  for (int r = 0; r < W; ++r)
-    aligned = aligned && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
+  const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
   if (aligned) {
     const bool small = row_bytes <= kGatherSmallStage;
     const GatherKernel k = small ? kGatherSmall : kGatherLarge;
@@ -795,8 +858,11 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     e = launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
                       small ? kGatherSmallStage : kGatherLargeStage);
   } else {
-    e = launch_kernel(dispatch_copy_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s,
-                      true, P, D);
+    e = row_bytes >= kWarpRowBytes
+            ? launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
+                            kCopyThreads, 0, s, true, P, D)
+            : launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
+                            kCopyThreads, 0, s, true, P, D);
   }
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
