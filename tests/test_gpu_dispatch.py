@@ -62,6 +62,22 @@ def test_random_dispatch(rb):
         dispatch_checked(K, rows, src, key, rb, rows_mis=mis, out_mis=mis[::-1])
 
 
+@pytest.mark.parametrize("rb", [64, 80, 256, 1040, 4096, 8176, 8192, 65536 + 16])
+def test_aligned_row_sizes(rb):
+    """16-byte aligned buffers and rows across the warp copy's flat vector runs
+    (64 B .. 64 KiB), the switch to the cp.async.bulk gather (8 KiB .. 32 KiB)
+    and rows too long for either (span copy); item counts leave ragged tails of
+    32-item batches."""
+    rng = np.random.default_rng(rb)
+    W, K = 4, 3
+    n = [int(rng.integers(1, 40)) for _ in range(W)]
+    m = [int(rng.integers(0, 300)) for _ in range(W)]
+    rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+    src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
+    key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+    dispatch_checked(K, rows, src, key, rb)
+
+
 def test_dispatch_without_items():
     rows = [np.arange(64, dtype=np.uint8)] * 3
     empty = [np.zeros(0, np.int32)] * 3
