@@ -813,11 +813,11 @@ def run_fused_dispatch(args):
     algo = distinct + T + items * (4 + 4 + 8) + 24 * Wn * Wn
     peak, peak_kind = hbm_peak()
     # the copy kernel the library picks: cp.async.bulk gather for 16-byte
-    # aligned rows of 8..32 KiB (torch allocations are aligned); rows under
+    # aligned rows of 2..32 KiB (torch allocations are aligned); rows under
     # 64 bytes copied by the rank kernel itself (past the one-kernel size);
     # else warp/thread copies
     small_path = max(m) <= 2048 and Wn * K <= 256
-    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 8192 <= rb <= 32768
+    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 2048 <= rb <= 32768
                    else "dispatch_rank_copy_kernel" if rb < 64 and not small_path
                    else "dispatch_copy_kernel")
     roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",

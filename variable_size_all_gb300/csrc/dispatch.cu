@@ -26,8 +26,9 @@
 //      prologue, which also checks capacities and NULL buffers), publish the
 //      positions and the split matrix, then gather every item's row straight
 //      into its place in the output of its destination: with cp.async.bulk
-//      through shared memory for 16-byte aligned rows of 1..32 KiB, else a
-//      warp per row for rows of 64 bytes or more and a thread per row below.
+//      through shared memory for 16-byte aligned rows of 2..32 KiB, else 32
+//      rows per warp (flat 16-byte vector runs when aligned) for rows of 64
+//      bytes or more and a thread per row below.
 // Invalid keys or source rows set a workspace flag (cleared first) that stops
 // every later kernel; invalid splits stop the copy kernel in its prologue.
 // Either way nothing the caller owns is written.
@@ -587,31 +588,38 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
 
 // Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
 // cleared before every dispatch; then S, key starts, key totals, histograms.
-// Rows of 1..32 KiB, every row and buffer 16-byte aligned: one warp per CTA
-// streams each item's row global -> shared -> global with cp.async.bulk
-// through a ring of NS stages (loads LEAD rows ahead of the stores).  The
-// warp reads the metadata of 32 items at a time, lane i item i; lane 0
-// issues the copies and tracks its own bulk stores.
-template <int NS, int LEAD>
+// Rows of 2..32 KiB, every row and buffer 16-byte aligned: NWK warps per CTA
+// each stream their share of the CTA's items, row by row, global -> shared ->
+// global with cp.async.bulk through a ring of NS stages of their own (loads
+// LEAD rows ahead of the stores).  A warp reads the metadata of 32 items at
+// a time, lane i item i; its lane 0 issues the copies and tracks its own
+// bulk stores.
+template <int NS, int LEAD, int NWK>
 __global__ void __launch_bounds__(128)
     dispatch_copy_bulk_kernel(const __grid_constant__ Params P,
                               const __grid_constant__ DispatchParams D, int stage_bytes) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 rows ahead of stores");
+  static_assert(NWK >= 1 && NWK <= 4, "one to four issuing warps");
   chain_wait();
   if (flagged(D)) return;
   __shared__ Plan pl;
-  __shared__ alignas(8) unsigned long long bars[NS];
-  __shared__ unsigned char* stage_dst[NS];
+  __shared__ alignas(8) unsigned long long bars[NWK * NS];
+  __shared__ unsigned char* stage_dst[NWK * NS];
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
   publish_splits(D);
-  const int lane = threadIdx.x & 31;
-  if ((threadIdx.x >> 5) != 0) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp >= NWK) return;
+  // Warp w owns every NWK-th of the CTA's items, its own NS stages and
+  // barriers: NWK independent pipelines, so NWK lanes issue copies at once.
   const int W = D.W, K = D.K;
   const long long rb = P.rb, total = D.item_first[W], G = gridDim.x, b0 = blockIdx.x;
-  const long long nk = total > b0 ? (total - b0 + G - 1) / G : 0;
+  const long long nc = total > b0 ? (total - b0 + G - 1) / G : 0;  // the CTA's items
+  const long long nk = nc > warp ? (nc - warp + NWK - 1) / NWK : 0;  // this warp's
   if (nk == 0) return;
-  const uint32_t bar0 = smem_u32(bars), stage0 = smem_u32(stages);
+  const uint32_t bar0 = smem_u32(bars) + 8u * NS * warp,
+                 stage0 = smem_u32(stages) + (uint32_t)(NS * warp) * (uint32_t)stage_bytes;
+  unsigned char** const sdst = stage_dst + NS * warp;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
@@ -625,7 +633,7 @@ __global__ void __launch_bounds__(128)
       if ((k & 31) == 0) {
         const long long kk = k + lane;
         if (kk < nk) {
-          const long long g = b0 + kk * G;
+          const long long g = b0 + (warp + kk * NWK) * G;
           int r = 0;
           while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
           const long long i = g - D.item_first[r];
@@ -641,7 +649,7 @@ __global__ void __launch_bounds__(128)
       if (lane == 0) {
         const int s = (int)(k % NS);
         if (k >= NS) bulk_wait_read<NS - LEAD - 1>();
-        stage_dst[s] = reinterpret_cast<unsigned char*>(dst);
+        sdst[s] = reinterpret_cast<unsigned char*>(dst);
         mbar_expect_tx(bar0 + 8 * s, (unsigned)rb);
         bulk_load(stage0 + (uint32_t)s * stage_bytes, reinterpret_cast<const void*>(src),
                   (unsigned)rb, bar0 + 8 * s);
@@ -653,7 +661,7 @@ __global__ void __launch_bounds__(128)
       const int s = (int)(j % NS);
       if (lane == 0) {
         ok = mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1));
-        if (ok) bulk_store(stage_dst[s], stage0 + (uint32_t)s * stage_bytes, (unsigned)rb);
+        if (ok) bulk_store(sdst[s], stage0 + (uint32_t)s * stage_bytes, (unsigned)rb);
       }
       ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
@@ -684,23 +692,35 @@ __global__ void __launch_bounds__(128)
 #ifndef A2AV_GATHER_CTAS_PER_SM
 #define A2AV_GATHER_CTAS_PER_SM 1
 #endif
+// Rows of at most 8 KiB go through 8 KiB stages, several warps issuing at
+// once, each with its own ring (one lane issuing every row was the limit:
+// ~480 ns a row whatever its size).  Measured on the MoE dispatch (8192
+// tokens, top-2, W=8, us): 2 / 4 KiB rows 113 / 154 with four warps x 6
+// stages (two warps x 12: 193 / 197; the warp copy: 141 / 263); 8 KiB rows 279
+// with two warps x 12 stages (four x 6: 300; one warp, 16 KiB stages: 411).
+constexpr int kGatherTinyStage = 8 * 1024;
 constexpr int kGatherSmallStage = 16 * 1024, kGatherLargeStage = 32 * 1024;
 using GatherKernel = void (*)(Params, DispatchParams, int);
-const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES, A2AV_GATHER_LEAD>;
+const GatherKernel kGatherTiny4 = dispatch_copy_bulk_kernel<6, 4, 4>;    // rows <= 4 KiB
+const GatherKernel kGatherTiny2 = dispatch_copy_bulk_kernel<12, 10, 2>;  // rows <= 8 KiB
+// 8..16 KiB rows: one issuing warp, 12 x 16 KiB (two warps x 6: 2-4 % slower).
+const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES, A2AV_GATHER_LEAD, 1>;
 const GatherKernel kGatherLarge =
     dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES / 2, (A2AV_GATHER_LEAD + 1) / 2 - 1 >= 1
                                                           ? (A2AV_GATHER_LEAD + 1) / 2 - 1
-                                                          : 1>;
-constexpr int kGatherSmem = A2AV_GATHER_STAGES * kGatherSmallStage;  // = stages/2 x 32 KiB
+                                                          : 1, 1>;
+constexpr int kGatherSmem = A2AV_GATHER_STAGES * kGatherSmallStage;
+static_assert(4 * 6 * kGatherTinyStage <= kGatherSmem && 2 * 12 * kGatherTinyStage <= kGatherSmem,
+              "the 8 KiB rings fit the same shared memory");
+static_assert(kGatherSmem <= 192 * 1024, "shared memory per CTA");
 static_assert(A2AV_GATHER_STAGES % 2 == 0 && A2AV_GATHER_LEAD < A2AV_GATHER_STAGES,
               "the large ring halves the small one");
 // Aligned rows this long or longer take the bulk gather; shorter ones the
 // warp copy's flat vector runs.  Measured on the MoE dispatch (8192 tokens,
-// top-2, W=8): rows of 1 / 2 / 4 KiB 77 / 141 / 263 us by warp copy against
-// ~405 us by gather (too few bytes in flight at a row per stage); 8 and 14 KiB
-// rows 412 / 459 us by gather against 506 / 868 us.
+// top-2, W=8): 1 KiB rows 78 us by warp copy against 117 by the gather; from
+// 2 KiB the gather wins (above); 14 KiB rows 459 us against 868 by warp copy.
 #ifndef A2AV_GATHER_MIN_ROW
-#define A2AV_GATHER_MIN_ROW 8192
+#define A2AV_GATHER_MIN_ROW 2048
 #endif
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 
@@ -845,10 +865,17 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
   const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
   if (aligned) {
-    const bool small = row_bytes <= kGatherSmallStage;
-    const GatherKernel k = small ? kGatherSmall : kGatherLarge;
+    const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
+    const GatherKernel k = row_bytes <= 4096 ? kGatherTiny4
+                           : tiny            ? kGatherTiny2
+                           : small           ? kGatherSmall
+                                             : kGatherLarge;
     if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
-      if (cudaFuncSetAttribute(kGatherSmall, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(kGatherTiny4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGatherSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(kGatherTiny2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGatherSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(kGatherSmall, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kGatherSmem) != cudaSuccess ||
           cudaFuncSetAttribute(kGatherLarge, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kGatherSmem) != cudaSuccess)
@@ -856,7 +883,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
       h->gather_ready = true;
     }
     e = launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
-                      small ? kGatherSmallStage : kGatherLargeStage);
+                      tiny ? kGatherTinyStage : small ? kGatherSmallStage : kGatherLargeStage);
   } else {
     e = row_bytes >= kWarpRowBytes
             ? launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
