@@ -608,8 +608,9 @@ __global__ void __launch_bounds__(128)
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
   publish_splits(D);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp >= NWK) return;
+  const int lane = threadIdx.x & 31;
+  if ((int)(threadIdx.x >> 5) >= NWK) return;
+  const int warp = NWK == 1 ? 0 : (int)(threadIdx.x >> 5);  // a constant for one warp
   // Warp w owns every NWK-th of the CTA's items, its own NS stages and
   // barriers: NWK independent pipelines, so NWK lanes issue copies at once.
   const int W = D.W, K = D.K;
