@@ -823,7 +823,9 @@ def run_fused_dispatch(args):
     roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
-                "traffic": measured_traffic(copy_kernel + ":" + args.workload, algo),
+                "traffic": measured_traffic(copy_kernel + ":" + args.workload +
+                                            (f"_h{args.hidden}" if args.workload == "cfg3"
+                                             and args.hidden != 7168 else ""), algo),
                 "algorithmic_bytes_per_launch": algo}
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
