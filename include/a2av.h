@@ -217,10 +217,13 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *                     max_r m_r) bytes, 256-byte aligned, not shared with a
  *                     dispatch in flight.
  *
- * Two or four kernel launches on `stream`: per-range key histograms,
+ * Two to four kernel launches on `stream`: per-range key histograms,
  * per-key scans, stable ranking within ranges (warp match) -- one fused
  * kernel when every rank has at most 2048 items and W * keys_per_peer <=
- * 256 -- then the row gather-copy, which alone writes the caller's buffers.
+ * 256 -- then the row gather-copy, which alone writes the caller's buffers
+ * (for rows shorter than 64 bytes past that size the ranking kernel copies
+ * the rows itself, after checking the split matrix).  One memset of the
+ * workspace's first 256 bytes precedes them.
  * Errors: host -- A2AV_ERR_INVALID_ARG (NULL arrays, keys_per_peer < 1,
  * negative counts, a small or misaligned workspace), A2AV_ERR_UNSUPPORTED
  * (W * keys_per_peer > A2AV_MAX_DISPATCH_KEYS, counts above 2^31 - 1);
