@@ -706,6 +706,14 @@ const GatherKernel kGatherTiny4 = dispatch_copy_bulk_kernel<6, 4, 4>;    // rows
 const GatherKernel kGatherTiny2 = dispatch_copy_bulk_kernel<12, 10, 2>;  // rows <= 8 KiB
 // 8..16 KiB rows: one issuing warp, 12 x 16 KiB (two warps x 6: 2-4 % slower).
 const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES, A2AV_GATHER_LEAD, 1>;
+// Few items per CTA (decode-size dispatches) of 8..16 KiB rows: four warps x
+// 3 x 16 KiB, so that a CTA's handful of rows are issued four at a time
+// (14 KiB rows, 128 / 512 tokens a rank: 26.3 / 44.0 -> 25.2 / 41.8 us; no
+// gain for 8 KiB rows, which keep the two-warp ring).
+#ifndef A2AV_GATHER_FEW_ITEMS
+#define A2AV_GATHER_FEW_ITEMS 64  // items per CTA at or below which the four-warp ring is used
+#endif
+const GatherKernel kGatherSmallFew = dispatch_copy_bulk_kernel<3, 1, 4>;
 const GatherKernel kGatherLarge =
     dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES / 2, (A2AV_GATHER_LEAD + 1) / 2 - 1 >= 1
                                                           ? (A2AV_GATHER_LEAD + 1) / 2 - 1
@@ -867,9 +875,11 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
   if (aligned) {
     const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
+    const bool few = D.item_first[W] <= (long long)A2AV_GATHER_FEW_ITEMS *
+                                             (h->sms * A2AV_GATHER_CTAS_PER_SM);
     const GatherKernel k = row_bytes <= 4096 ? kGatherTiny4
                            : tiny            ? kGatherTiny2
-                           : small           ? kGatherSmall
+                           : small           ? (few ? kGatherSmallFew : kGatherSmall)
                                              : kGatherLarge;
     if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
       if (cudaFuncSetAttribute(kGatherTiny4, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -877,6 +887,8 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
           cudaFuncSetAttribute(kGatherTiny2, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kGatherSmem) != cudaSuccess ||
           cudaFuncSetAttribute(kGatherSmall, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kGatherSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(kGatherSmallFew, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kGatherSmem) != cudaSuccess ||
           cudaFuncSetAttribute(kGatherLarge, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kGatherSmem) != cudaSuccess)
