@@ -21,7 +21,7 @@ def _cuda():
     a2av.load()
 
 
-@pytest.mark.parametrize("tokens", [1024, 8192])
+@pytest.mark.parametrize("tokens", [128, 1024, 8192])
 def test_moe_top2_dispatch(tokens):
     w = wl.cfg3(0, tokens=tokens)
     K, rows, src, key = wl.dispatch_items(w)
@@ -75,6 +75,18 @@ def test_aligned_row_sizes(rb):
     rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
     src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
     key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+    dispatch_checked(K, rows, src, key, rb)
+
+
+@pytest.mark.parametrize("rb", [2048, 9216, 20480])
+def test_few_items_past_the_one_kernel_size(rb):
+    """More keys than the one-kernel path takes (W*K > 256) but only a few
+    thousand items: the gather's rings for few items per CTA."""
+    rng = np.random.default_rng(rb + 5)
+    W, K, n, m = 2, 200, 64, 3000
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, n, m).astype(np.int32) for _ in range(W)]
+    key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
     dispatch_checked(K, rows, src, key, rb)
 
 
