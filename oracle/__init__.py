@@ -58,8 +58,11 @@ def _bind(lib):
                                         ctypes.c_int64, ctypes.c_int64]
     lib.a2av_oracle_dispatch.argtypes = [ctypes.c_int, ctypes.c_int, vpp, _i64p, vpp, vpp, _i64p,
                                          vpp, _i64p, vpp, _i64p, ctypes.c_int64, ctypes.c_int64]
+    lib.a2av_oracle_combine_items.argtypes = [ctypes.c_int, ctypes.c_int, vpp, _i64p, vpp, vpp,
+                                              _i64p, vpp, ctypes.c_int64]
     for f in (lib.a2av_oracle, lib.a2av_oracle_dest, lib.a2av_oracle_check,
-              lib.a2av_oracle_row_source, lib.a2av_oracle_combine, lib.a2av_oracle_dispatch):
+              lib.a2av_oracle_row_source, lib.a2av_oracle_combine, lib.a2av_oracle_dispatch,
+              lib.a2av_oracle_combine_items):
         f.restype = ctypes.c_int
     return lib
 
@@ -166,6 +169,26 @@ class Oracle:
             W, int(K), _ptrs(rows), n_rows, _ptrs(src), _ptrs(key), n_items, _ptrs(outputs),
             out_splits_offsets.ctypes.data_as(_i64p), _ptrs(sorted_pos), isp, int(row_bytes),
             int(out_capacity_rows))
+
+    def combine_items(self, K, expert, S, keys, sorted_pos, item_out, row_bytes) -> int:
+        """The fused combine (see a2av_oracle.c): each item's row from the
+        dispatch-layout buffers ``expert`` back into ``item_out`` in item order."""
+        W = len(expert)
+        S = _splits(S, W)
+        key = [np.ascontiguousarray(x, dtype=np.int32) for x in keys]
+        pos = [np.ascontiguousarray(x, dtype=np.int64) for x in sorted_pos]
+        n_items = (ctypes.c_int64 * W)(*[k.size for k in key])
+        return self.lib.a2av_oracle_combine_items(
+            W, int(K), _ptrs(expert), S.ctypes.data_as(_i64p), _ptrs(key), _ptrs(pos), n_items,
+            _ptrs(item_out), int(row_bytes))
+
+    def combine_items_exchange(self, K, expert, S, keys, sorted_pos, row_bytes):
+        """Return the item-order rows of a fused combine (raises if rejected)."""
+        outs = [np.empty(np.asarray(k).size * row_bytes, np.uint8) for k in keys]
+        rc = self.combine_items(K, expert, S, keys, sorted_pos, outs, row_bytes)
+        if rc != OK:
+            raise ValueError(f"oracle rejected the combine (status {rc})")
+        return outs
 
     def dispatch_exchange(self, K, rows, src_rows, keys, row_bytes):
         """Return (outputs, out_splits_offsets, sorted_pos, S) of a fused dispatch."""

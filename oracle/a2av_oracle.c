@@ -231,3 +231,42 @@ int a2av_oracle_dispatch(int W, int K, const uint8_t *const *rows, const int64_t
   free(S);
   return rc;
 }
+
+/* The fused combine, the inverse of a2av_oracle_dispatch's row movement.
+ * expert[p] holds peer p's rows in the layout the dispatch wrote out[p] (the
+ * rows it received, source rank by source rank, each rank's in key order);
+ * S is the dispatch's split matrix; each item (r, i) has its key (peer
+ * p = key / K) and its position in rank r's key order, as the dispatch
+ * returned them.  The item's row sits at row out_off[p][r] + (pos -
+ * in_off[r][p]) of expert[p] (its rank's chunk starts at out_off[p][r], and
+ * within the chunk the items keep their key order), and is copied to row i
+ * of item_out[r].  Everything is checked before anything is written:
+ * invalid S (as a2av_oracle_check, expert buffers as the outputs and item
+ * buffers as the inputs) -> ORACLE_BAD_SPLITS; a key out of [0, W*K) or a
+ * position outside its peer's group [in_off[r][p], in_off[r][p] + S[r][p])
+ * -> ORACLE_BAD_INDEX. */
+int a2av_oracle_combine_items(int W, int K, const uint8_t *const *expert, const int64_t *S,
+                              const int32_t *const *key, const int64_t *const *sorted_pos,
+                              const int64_t *n_items, uint8_t *const *item_out,
+                              int64_t row_bytes) {
+  if (W < 1 || K < 1 || row_bytes < 1) return ORACLE_INVALID_ARG;
+  int rc = a2av_oracle_check(W, S, row_bytes, 0, 0, (const void *const *)item_out,
+                             (void *const *)expert);
+  if (rc != ORACLE_OK) return rc;
+  const int64_t nkeys = (int64_t)W * K;
+  for (int r = 0; r < W; ++r)
+    for (int64_t i = 0; i < n_items[r]; ++i) {
+      if (key[r][i] < 0 || key[r][i] >= nkeys) return ORACLE_BAD_INDEX;
+      const int p = key[r][i] / K;
+      const int64_t lo = in_offset(W, S, r, p);
+      if (sorted_pos[r][i] < lo || sorted_pos[r][i] >= lo + S[(int64_t)r * W + p])
+        return ORACLE_BAD_INDEX;
+    }
+  for (int r = 0; r < W; ++r)
+    for (int64_t i = 0; i < n_items[r]; ++i) {
+      const int p = key[r][i] / K;
+      const int64_t row = out_offset(W, S, p, r) + (sorted_pos[r][i] - in_offset(W, S, r, p));
+      memcpy(item_out[r] + i * row_bytes, expert[p] + row * row_bytes, (size_t)row_bytes);
+    }
+  return ORACLE_OK;
+}

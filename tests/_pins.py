@@ -406,6 +406,70 @@ def pin_kjt_lengths_cut_the_keys(o):
             _eq(rk, want_keys, f"keys {r} -> {p}")
 
 
+def _random_items(rng, W, K, rb):
+    n = [int(rng.integers(1, 12)) for _ in range(W)]
+    rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+    m = [int(rng.integers(0, 25)) for _ in range(W)]
+    src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
+    key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+    return rows, src, key
+
+
+def pin_combine_items_round_trip(o):
+    """combine_items(dispatch(x)) puts every item's source row back in item
+    order: item (r, i) gets rows[r][src[r][i]] (numpy fancy indexing)."""
+    rng = np.random.default_rng(17)
+    cases = 0
+    for W, K, rb in ((1, 1, 3), (2, 3, 1), (3, 2, 16), (4, 5, 7), (5, 1, 24)):
+        for _ in range(20):
+            rows, src, key = _random_items(rng, W, K, rb)
+            outs, so, pos, S = o.dispatch_exchange(K, rows, src, key, rb)
+            back = o.combine_items_exchange(K, outs, S, key, pos, rb)
+            for r in range(W):
+                want = rows[r].reshape(-1, rb)[src[r]].reshape(-1)
+                _eq(back[r], want, f"combine_items(dispatch(x)) (W={W} K={K} rb={rb})")
+            cases += 1
+    assert cases == 100
+
+
+def pin_combine_items_is_combine_then_gather(o):
+    """The same result as the plain reverse exchange (rows back in key order)
+    followed by a gather by sorted position: a different formulation."""
+    import workloads as wl
+    w = wl.cfg3(4, tokens=64, hidden=8)
+    K, rows, src, key = wl.dispatch_items(w)
+    rb = w.row_bytes
+    outs, so, pos, S = o.dispatch_exchange(K, rows, src, key, rb)
+    # the experts write something of their own into the dispatch layout
+    rng = np.random.default_rng(3)
+    expert = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
+    back, _ = o.exchange_back(expert, so, rb)
+    got = o.combine_items_exchange(K, expert, S, key, pos, rb)
+    for r in range(w.W):
+        want = back[r].reshape(-1, rb)[pos[r]].reshape(-1)
+        _eq(got[r], want, "combine_items = combine + gather by sorted position")
+
+
+def pin_combine_items_errors(o):
+    W, K, rb = 2, 2, 4
+    S = np.array([[2, 1], [0, 2]], np.int64)
+    expert = [np.arange(8, dtype=np.uint8), np.arange(12, dtype=np.uint8)]
+    good_key = [np.array([0, 2, 1], np.int32), np.array([3, 2], np.int32)]
+    good_pos = [np.array([0, 2, 1], np.int64), np.array([1, 0], np.int64)]
+    assert o.combine_items_exchange(K, expert, S, good_key, good_pos, rb)[0].size == 12
+    for what, key, pos, s, code in (
+            ("key too large", [good_key[0], np.array([4, 2], np.int32)], good_pos, S, -6),
+            ("negative key", [np.array([0, -1, 1], np.int32), good_key[1]], good_pos, S, -6),
+            ("position outside its group", good_key, [np.array([0, 1, 2], np.int64), good_pos[1]],
+             S, -6),
+            ("position past the rank", good_key, [good_pos[0], np.array([2, 0], np.int64)], S, -6),
+            ("negative split", good_key, good_pos, np.array([[2, 1], [-1, 2]], np.int64), -4)):
+        outs = [np.full(12, SENTINEL, np.uint8), np.full(8, SENTINEL, np.uint8)]
+        rc = o.combine_items(K, expert, s, key, pos, outs, rb)
+        assert rc == code, f"{what}: status {rc}, expected {code}"
+        assert all(np.all(b == SENTINEL) for b in outs), what
+
+
 def pin_dispatch_errors(o):
     rows = [np.arange(12, dtype=np.uint8), np.arange(8, dtype=np.uint8)]
     good_src = [np.array([0, 2, 1], np.int32), np.array([1, 0], np.int32)]
@@ -427,7 +491,9 @@ def pin_dispatch_errors(o):
 
 PINS = [pin_identity_w1, pin_errors, pin_diagonal_and_permutation, pin_uniform_transpose,
         pin_round_trip, pin_combine_round_trip, pin_dispatch_errors, pin_dispatch_small,
-        pin_dispatch_matches_generators, pin_kjt_lengths_cut_the_keys, pin_dest_and_row_source,
+        pin_dispatch_matches_generators, pin_kjt_lengths_cut_the_keys, pin_combine_items_errors,
+        pin_combine_items_is_combine_then_gather, pin_combine_items_round_trip,
+        pin_dest_and_row_source,
         pin_invariants_random,
         pin_bruteforce_tiny]
 

@@ -49,6 +49,14 @@ MUTANTS = {
                              "rows[r] + (int64_t)(i % n_rows[r]) * row_bytes"),
     "dispatch_pos_off_by_one": ("place[r][i] = next++;", "place[r][i] = ++next - 0;"),
     "dispatch_key_bound": ("key[r][i] >= nkeys ||", "key[r][i] > nkeys ||"),
+    "combine_items_no_group_start": (
+        "out_offset(W, S, p, r) + (sorted_pos[r][i] - in_offset(W, S, r, p));",
+        "out_offset(W, S, p, r) + (sorted_pos[r][i]);"),
+    "combine_items_chunk_of_peer": (
+        "out_offset(W, S, p, r) + (sorted_pos[r][i] - in_offset(W, S, r, p));",
+        "out_offset(W, S, r, p) + (sorted_pos[r][i] - in_offset(W, S, r, p));"),
+    "combine_items_group_bound": ("sorted_pos[r][i] >= lo + S[(int64_t)r * W + p])",
+                                  "sorted_pos[r][i] > lo + S[(int64_t)r * W + p])"),
     "row_source_wrong_chunk": ("*i = in_offset(W, in_splits, q, p) + (k - start);",
                                "*i = in_offset(W, in_splits, p, q) + (k - start);"),
 }
