@@ -879,6 +879,125 @@ def run_fused_dispatch(args):
 
 
 # ------------------------------------------------------------- overlap ----
+def run_fused_combine(args):
+    """a2av_combine_items after a fused dispatch (cfg3, cfg5): every item's row
+    back from the peers into item order, against the plain reverse exchange
+    followed by a torch gather by sorted position."""
+    import torch
+    import variable_size_all_gb300 as a2av
+    import workloads as wl
+    import oracle
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init("nccl")
+    a2av.build()
+    if args.workload not in ("cfg3", "cfg5"):
+        raise SystemExit("--op fused_combine needs --workload cfg3 or cfg5")
+    w = (wl.cfg3(args.seed, tokens=args.tokens, dedup=args.dedup, hidden=args.hidden)
+         if args.workload == "cfg3" else wl.cfg5(args.seed, batch=args.batch))
+    K, rows, src, key = wl.dispatch_items(w)
+    Wn, rb, S = w.W, w.row_bytes, w.splits
+    m = [k.size for k in key]
+    T = moved_bytes(S, rb)
+    d_rows = [torch.from_numpy(r).to(dev) for r in rows]
+    d_src = [torch.from_numpy(x).to(dev) for x in src]
+    d_key = [torch.from_numpy(x).to(dev) for x in key]
+    d_pos = [torch.empty(x, dtype=torch.int64, device=dev) for x in m]
+    d_out = [torch.empty(int(S[:, p].sum()) * rb, dtype=torch.uint8, device=dev)
+             for p in range(Wn)]
+    d_so = torch.empty((Wn, 2, Wn), dtype=torch.int64, device=dev)
+    d_isp = torch.empty((Wn, Wn), dtype=torch.int64, device=dev)
+    eng = a2av.A2av(Wn)
+    stream = torch.cuda.current_stream()
+    eng.dispatch(d_rows, d_src, d_key, K, d_out, d_so, d_pos, rb, in_splits=d_isp)
+    items = [torch.empty(x * rb, dtype=torch.uint8, device=dev) for x in m]
+    back = [torch.empty(int(S[r].sum()) * rb, dtype=torch.uint8, device=dev) for r in range(Wn)]
+    cso = torch.empty_like(d_so)
+    u_items = [torch.empty_like(t) for t in items]
+    cold = sum(t.numel() for t in d_out) < 2 * L2_BYTES
+    flush = torch.ones(128 << 20, dtype=torch.int32, device=dev)
+    call = eng.bind_combine_items(d_out, d_isp, d_key, d_pos, K, items, rb, stream=stream)
+
+    def unfused():
+        eng.combine(d_out, d_so, back, cso, rb, stream=stream)
+        for r in range(Wn):
+            torch.index_select(back[r].view(-1, rb), 0, d_pos[r], out=u_items[r].view(-1, rb))
+
+    for _ in range(args.warmup):
+        call()
+        unfused()
+    torch.cuda.synchronize()
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during warm-up")
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        f_med, f_mean, f_host = _timed(torch, stream, call, args.steps, cold, flush)
+        torch.cuda.synchronize()
+        barrier()
+    u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
+    if eng.status() != a2av.OK:
+        raise SystemExit("device reported an error during the timed region")
+    max_s = reduce_max(f_mean, dev)
+    value = whole_job_value(T / 1e9, world, max_s)
+    # ideal traffic: every peer row read once, every item row written once,
+    # each item's key and position read once
+    algo = T + sum(m) * rb + sum(m) * (4 + 8) + 24 * Wn * Wn
+    peak, peak_kind = hbm_peak()
+    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 2048 <= rb <= 32768
+                   else "dispatch_copy_kernel")
+    roofline = {"bound": "hbm", "kernel": f"a2av_combine_items (checks, then {copy_kernel})",
+                "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
+                "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4), "traffic": None,
+                "algorithmic_bytes_per_launch": algo}
+    cpu = parity = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        o = oracle.default()
+        peers = [t.cpu().numpy() for t in d_out]
+        Sg = d_isp.cpu().numpy()
+        pos = [t.cpu().numpy() for t in d_pos]
+        t0 = time.perf_counter()
+        ref = o.combine_items_exchange(K, peers, Sg, key, pos, rb)
+        spent = time.perf_counter() - t0
+        ok = all(np.array_equal(items[r].cpu().numpy(), ref[r]) for r in range(Wn))
+        ok = ok and all(np.array_equal(ref[r], rows[r].reshape(-1, rb)[src[r]].reshape(-1))
+                        for r in range(Wn))
+        ok = ok and all(torch.equal(u_items[r], items[r]) for r in range(Wn))
+        parity = {"bit_exact": bool(ok), "check": "item rows equal the oracle's and the items' "
+                                                  "source rows; the unfused path agrees"}
+        cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "the whole fused combine of the same workload", "seconds": round(spent, 3)}
+        if not ok:
+            raise SystemExit("fused combine differs from the oracle")
+    eng.close()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded numpy draws; no dataset)",
+        "config": {"workload": describe(args.workload, 0, args.seed, args.tokens, args.batch,
+                                        args.dedup, hidden=args.hidden) +
+                   " -- after the fused dispatch, every item's row back in item order",
+                   "name": args.workload, "op": "fused_combine", "ranks": Wn, "row_bytes": rb,
+                   "items": sum(m), "moved_bytes_per_step": T,
+                   "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
+                          "inputs larger than L2"),
+                   "timing": "CUDA events around the bound call (a memset and three kernels), "
+                             "mean over steps; a spin kernel ahead of each call"},
+        "unfused_combine_then_gather": {"ms_mean": round(u_mean * 1e3, 4),
+                                        "ms_median": round(u_med * 1e3, 4),
+                                        "host_call_us": round(u_host * 1e6, 1)},
+        "fused_ms_median": round(f_med * 1e3, 4), "fused_host_call_us": round(f_host * 1e6, 1),
+        "speedup_vs_unfused": round(u_mean / f_mean, 3),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(), "parity": parity,
+    }
+    if rank == 0:
+        emit(line)
+
+
 def device_exchange(torch, dev, w):
     """Device inputs, splits, outputs and out_splits_offsets for workload w."""
     S, rb = w.splits, w.row_bytes
@@ -1206,7 +1325,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=WORKLOADS, default="cfg2")
-    ap.add_argument("--op", choices=["dispatch", "combine", "fused_dispatch", "overlap", "kjt"],
+    ap.add_argument("--op", choices=["dispatch", "combine", "fused_dispatch", "fused_combine",
+                                     "overlap", "kjt"],
                     default="dispatch",
                     help="dispatch = a2av_run; combine = a2av_combine on its outputs; "
                          "fused_dispatch = a2av_dispatch on unsorted items (cfg3, cfg5); "
@@ -1239,6 +1359,8 @@ def main(argv=None):
         run_overlap(args)
     elif args.op == "kjt":
         run_kjt(args)
+    elif args.op == "fused_combine":
+        run_fused_combine(args)
     else:
         run_ours(args)
 

@@ -328,6 +328,50 @@ int a2av_version(void);
 /* Bytes of device memory the library reserves for a2av_run_noalloc. */
 #define A2AV_NOALLOC_SCRATCH_BYTES 256
 
+/* Device workspace a2av_combine_items needs (flag and an offsets table). */
+#define A2AV_COMBINE_WORKSPACE_BYTES (256 + 16 * A2AV_MAX_RANKS * A2AV_MAX_RANKS)
+
+/*
+ * a2av_combine_items -- the fused combine: the return path of a2av_dispatch
+ * with every row put straight back in item order.  The pages' MoE region
+ * (PR 154580) sends tokens to their experts and back; the plain reverse
+ * exchange (a2av_combine) returns each rank its rows in key order, which
+ * the caller would then permute by sorted_pos -- a second read and write of
+ * every row that this call does not make.
+ *
+ * After a2av_dispatch with keys_per_peer K, S = its in_splits_dev, and
+ * sorted_pos and keys as it took and returned them, peer p holds, in the
+ * layout the dispatch wrote out[p], a row for each of its items (e.g. an
+ * expert's output rows).  For every rank r and item i, with p = key / K:
+ *   item_out[r][i] = peer[p] row (out_off[p][r] + sorted_pos[r][i] - in_off[r][p])
+ * (offsets of S as in a2av_run): combine_items(dispatch(x)) puts every
+ * item's source row back at its item index.
+ *
+ *  peer_ptrs          HOST array of W device pointers: peer p's rows in the
+ *                     dispatch layout (sum_r S[r][p] rows).  Read only.
+ *  in_splits_dev      DEVICE int64 [W][W]: S as a2av_dispatch wrote it.
+ *  key_ptrs, sorted_pos_ptrs, items_per_rank: as a2av_dispatch took and
+ *                     wrote them (HOST arrays of W device int32 / int64
+ *                     arrays, HOST int64 counts).  Read only.
+ *  item_out_ptrs      HOST array of W device pointers: rank r's items_per_rank[r]
+ *                     rows, written in item order.
+ *  workspace          DEVICE scratch, 256-byte aligned, at least
+ *                     A2AV_COMBINE_WORKSPACE_BYTES, not shared with a call in flight.
+ *
+ * Three launches after a 256-byte workspace memset: checks (the split
+ * matrix, each key, each position within its destination's group), then the
+ * dispatch's copy kernels with the rows moving the other way.  Device
+ * errors write nothing: A2AV_ERR_BAD_SPLITS (as a2av_run; NULL buffers with
+ * rows), A2AV_ERR_BAD_INDEX (a key outside [0, W * K) or a position outside
+ * [in_off[r][p], in_off[r][p] + S[r][p])).  Host errors as a2av_dispatch
+ * (A2AV_ERR_INVALID_ARG also for a small or misaligned workspace).
+ */
+int a2av_combine_items(a2av_handle *h, int keys_per_peer, const void *const *peer_ptrs,
+                       const int64_t *in_splits_dev, const int32_t *const *key_ptrs,
+                       const int64_t *const *sorted_pos_ptrs, const int64_t *items_per_rank,
+                       void *const *item_out_ptrs, int64_t row_bytes, void *workspace,
+                       int64_t workspace_bytes, void *stream);
+
 /*
  * a2av_run_noalloc -- the same exchange as a2av_run, for callers that cannot
  * allocate device memory.  (The pages have no counterpart; this is an

@@ -19,7 +19,8 @@ __all__ = [
     "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
     "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "a2av_dispatch", "a2av_dispatch_workspace_bytes", "ERR_BAD_INDEX", "MAX_DISPATCH_KEYS",
-    "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES", "BoundCall",
+    "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES", "BoundCall", "a2av_combine_items",
+    "COMBINE_WORKSPACE_BYTES",
     "OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA", "ERR_BAD_SPLITS", "ERR_TIMEOUT",
     "PATH_AUTO", "PATH_VECTOR", "PATH_BULK", "PATH_STAGED", "MAX_RANKS",
 ]
@@ -30,6 +31,7 @@ MAX_DISPATCH_KEYS = 1024
 PATH_AUTO, PATH_VECTOR, PATH_BULK, PATH_STAGED = 0, 1, 2, 3
 MAX_RANKS = 32
 MAX_EXCHANGES = 4
+COMBINE_WORKSPACE_BYTES = 256 + 16 * 32 * 32
 
 _lib = None
 
@@ -77,6 +79,8 @@ def load():
     lib.a2av_dispatch.argtypes = [vp, ci, pp, i64p, pp, pp, i64p, pp, vp, pp, vp, i64, vp, i64, vp]
     lib.a2av_dispatch.restype = ci
     lib.a2av_run_multi.argtypes = [vp, ci, ctypes.POINTER(A2avExchange), vp]
+    lib.a2av_combine_items.argtypes = [vp, ci, pp, vp, pp, pp, i64p, pp, i64, vp, i64, vp]
+    lib.a2av_combine_items.restype = ci
     lib.a2av_error_string.argtypes = [ci]
     lib.a2av_error_string.restype = ctypes.c_char_p
     lib.a2av_version.argtypes = []
@@ -144,6 +148,18 @@ def a2av_run_multi(handle, exchanges, stream: int = 0) -> int:
                               int(rb))
     return load().a2av_run_multi(handle, len(exchanges), arr if exchanges else None,
                                  ctypes.c_void_p(int(stream) or None))
+
+
+def a2av_combine_items(handle, keys_per_peer: int, peer_ptrs, in_splits_dev: int, key_ptrs,
+                       sorted_pos_ptrs, items_per_rank, item_out_ptrs, row_bytes: int,
+                       workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """Raw fused combine: integer device addresses, host lists of counts."""
+    return load().a2av_combine_items(
+        handle, int(keys_per_peer), _ptr_array(peer_ptrs),
+        ctypes.c_void_p(int(in_splits_dev) or None), _ptr_array(key_ptrs),
+        _ptr_array(sorted_pos_ptrs), _i64_array(items_per_rank), _ptr_array(item_out_ptrs),
+        int(row_bytes), ctypes.c_void_p(int(workspace) or None), int(workspace_bytes),
+        ctypes.c_void_p(int(stream) or None))
 
 
 def a2av_status(handle, stream: int = 0):
@@ -468,6 +484,54 @@ class A2av:
         (the keys and source rows themselves may change between calls)."""
         return self.dispatch(rows, src_rows, keys, keys_per_peer, outputs, out_splits_offsets,
                              sorted_pos, row_bytes, in_splits, workspace, stream, _bind=True)
+
+    def bind_combine_items(self, peers, in_splits, keys, sorted_pos, keys_per_peer: int,
+                           item_out, row_bytes: int, workspace=None, stream=None) -> BoundCall:
+        """``combine_items`` marshalled once (see BoundCall)."""
+        return self.combine_items(peers, in_splits, keys, sorted_pos, keys_per_peer, item_out,
+                                  row_bytes, workspace, stream, _bind=True)
+
+    def combine_items(self, peers, in_splits, keys, sorted_pos, keys_per_peer: int, item_out,
+                      row_bytes: int, workspace=None, stream=None, _bind=False):
+        """The fused combine (see include/a2av.h, a2av_combine_items): every
+        item's row from the peers' dispatch-layout buffers back to row i of
+        ``item_out[r]``.  ``in_splits``, ``keys`` and ``sorted_pos`` as a
+        dispatch took or wrote them."""
+        import torch
+        W = self.world_size
+        sp = self._matrix(in_splits, (W, W), "in_splits")
+        for name, ts, dt in (("keys", keys, torch.int32), ("sorted_pos", sorted_pos, torch.int64)):
+            if len(ts) != W:
+                raise ValueError(f"{name}: expected {W} tensors")
+            for t in ts:
+                if t is not None and t.numel() and (t.dtype != dt or not t.is_cuda
+                                                    or not t.is_contiguous()):
+                    raise ValueError(f"{name} must be contiguous CUDA {dt} tensors")
+        items = [0 if t is None else t.numel() for t in keys]
+        if any((0 if t is None else t.numel()) != m for t, m in zip(sorted_pos, items)):
+            raise ValueError("sorted_pos must have one entry per item")
+        if any((0 if t is None else t.numel()) < m * int(row_bytes)
+               for t, m in zip(item_out, items)):
+            raise ValueError("item_out[r] must hold one row per item of rank r")
+        if workspace is None:
+            ws = getattr(self, "_combine_workspace", None)
+            if ws is None:
+                ws = torch.empty(COMBINE_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+                self._combine_workspace = ws
+            workspace = ws
+        peer_arr, host_p = self._buffers(peers, "peers")
+        out_arr, host_o = self._buffers(item_out, "item_out")
+        if host_p or host_o:
+            raise ValueError("a2av_combine_items takes device buffers only")
+        ptr = lambda ts: [0 if t is None or t.numel() == 0 else t.data_ptr() for t in ts]
+        args = [self.handle, int(keys_per_peer), _ptr_array(list(peer_arr)), sp,
+                _ptr_array(ptr(keys)), _ptr_array(ptr(sorted_pos)), _i64_array(items),
+                _ptr_array(list(out_arr)), int(row_bytes), ctypes.c_void_p(workspace.data_ptr()),
+                int(workspace.numel()), ctypes.c_void_p(self._stream(stream) or None)]
+        if _bind:
+            keep = (peers, in_splits, keys, sorted_pos, item_out, workspace)
+            return BoundCall(self, load().a2av_combine_items, "a2av_combine_items", args, 11, keep)
+        self._check(load().a2av_combine_items(*args), "a2av_combine_items")
 
     def status(self, stream=None) -> int:
         rc, v = a2av_status(self.handle, self._stream(stream))

@@ -75,6 +75,7 @@ struct DispatchParams {
   int* status;
   long long* in_splits_out;         // optional [W][W]
   int vec16;                        // every row and buffer 16-byte aligned
+  int combine;                      // the fused combine: rows move the other way (below)
   long long ranges_max;
   long long pos_stride;
   int W, K;
@@ -525,10 +526,16 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
         while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
         const long long i = g - D.item_first[r];
         const int p = D.key[r][i] / K;
-        const long long pos = D.pos[(long long)r * D.pos_stride + i];
-        D.sorted_pos[r][i] = pos;
-        mdst = (long long)(P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb);
-        msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+        const long long grouped = pl.out_off[p][r] - pl.in_off[r][p];  // + pos: the row in p's buffer
+        if (D.combine) {  // from the peer's buffer back to the item's row
+          msrc = (long long)(P.out[p] + (grouped + D.sorted_pos[r][i]) * rb);
+          mdst = (long long)(P.in[r] + i * rb);
+        } else {
+          const long long pos = D.pos[(long long)r * D.pos_stride + i];
+          D.sorted_pos[r][i] = pos;
+          mdst = (long long)(P.out[p] + (grouped + pos) * rb);
+          msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+        }
       }
       const int n = total - g0 < 32 ? (int)(total - g0) : 32;
       if (D.vec16 && rb <= kVecMaxRow) {
@@ -569,9 +576,14 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
         const long long i = g - D.item_first[r];
         rank[q] = r;
         key[q] = D.key[r][i];
-        src_row[q] = D.src[r][i];
-        pos[q] = D.pos[(long long)r * D.pos_stride + i];
-        D.sorted_pos[r][i] = pos[q];
+        if (D.combine) {
+          src_row[q] = (int)i;  // the item's own row of the rank's buffer
+          pos[q] = D.sorted_pos[r][i];
+        } else {
+          src_row[q] = D.src[r][i];
+          pos[q] = D.pos[(long long)r * D.pos_stride + i];
+          D.sorted_pos[r][i] = pos[q];
+        }
       }
     }
 #pragma unroll
@@ -579,11 +591,46 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
       const int r = rank[q];
       if (r < 0) continue;
       const int p = key[q] / K;
-      copy_row_thread(P.out[p] + (pl.out_off[p][r] + pos[q] - pl.in_off[r][p]) * rb,
-                      P.in[r] + (long long)src_row[q] * rb, rb);
+      unsigned char* grouped = P.out[p] + (pl.out_off[p][r] + pos[q] - pl.in_off[r][p]) * rb;
+      unsigned char* own = const_cast<unsigned char*>(P.in[r]) + (long long)src_row[q] * rb;
+      if (D.combine)
+        copy_row_thread(own, grouped, rb);
+      else
+        copy_row_thread(grouped, own, rb);
     }
   }
   }
+}
+
+// The fused combine's checks, before any row moves: the split matrix (the
+// a2av prologue, which records A2AV_ERR_BAD_SPLITS), then every item's key
+// and position -- the position must lie in its destination's group of the
+// rank's key order, [in_off[r][p], in_off[r][p] + S[r][p]) -- else the flag
+// that stops the copy kernel, and A2AV_ERR_BAD_INDEX.
+__global__ void __launch_bounds__(kCopyThreads)
+    combine_check_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  chain_wait();
+  chain_release();
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, kTileGranule)) return;
+  const int W = D.W, K = D.K, NB = W * K;
+  const long long total = D.item_first[W];
+  int bad = 0;
+  for (long long g = (long long)blockIdx.x * kCopyThreads + threadIdx.x; g < total;
+       g += (long long)gridDim.x * kCopyThreads) {
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    const long long i = g - D.item_first[r];
+    const int key = D.key[r][i];
+    if (key < 0 || key >= NB) {
+      bad = 1;
+      continue;
+    }
+    const int p = key / K;
+    const long long pos = D.sorted_pos[r][i], lo = pl.in_off[r][p];
+    if (pos < lo || pos >= lo + pl.s[r][p]) bad = 1;
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) fail(D, A2AV_ERR_BAD_INDEX);
 }
 
 // Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
@@ -639,10 +686,16 @@ __global__ void __launch_bounds__(128)
           while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
           const long long i = g - D.item_first[r];
           const int p = D.key[r][i] / K;
-          const long long pos = D.pos[(long long)r * D.pos_stride + i];
-          D.sorted_pos[r][i] = pos;
-          msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
-          mdst = (long long)(P.out[p] + (pl.out_off[p][r] + pos - pl.in_off[r][p]) * rb);
+          const long long grouped = pl.out_off[p][r] - pl.in_off[r][p];
+          if (D.combine) {  // from the peer's buffer back to the item's row
+            msrc = (long long)(P.out[p] + (grouped + D.sorted_pos[r][i]) * rb);
+            mdst = (long long)(P.in[r] + i * rb);
+          } else {
+            const long long pos = D.pos[(long long)r * D.pos_stride + i];
+            D.sorted_pos[r][i] = pos;
+            msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+            mdst = (long long)(P.out[p] + (grouped + pos) * rb);
+          }
         }
       }
       const int t = (int)(k & 31);
@@ -764,6 +817,41 @@ extern "C" int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_pe
   return layout(world_size, keys_per_peer, max_items_per_rank).total;
 }
 
+namespace {
+
+// The row copy of a dispatch or a combine: the cp.async.bulk gather for
+// 16-byte aligned rows of 2..32 KiB (its ring chosen by row size and by the
+// items per CTA), else the warp copy (rows of 64 bytes or more) or the
+// thread copy.
+cudaError_t launch_copy(a2av_handle* h, const Params& P, const DispatchParams& D,
+                        long long row_bytes, cudaStream_t s) {
+  const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
+  if (!aligned)
+    return row_bytes >= kWarpRowBytes
+               ? launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
+                               kCopyThreads, 0, s, true, P, D)
+               : launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
+                               kCopyThreads, 0, s, true, P, D);
+  const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
+  const bool few = D.item_first[D.W] <= (long long)A2AV_GATHER_FEW_ITEMS *
+                                             (h->sms * A2AV_GATHER_CTAS_PER_SM);
+  const GatherKernel k = row_bytes <= 4096 ? kGatherTiny4
+                         : tiny            ? kGatherTiny2
+                         : small           ? (few ? kGatherSmallFew : kGatherSmall)
+                                           : kGatherLarge;
+  if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
+    for (GatherKernel g : {kGatherTiny4, kGatherTiny2, kGatherSmall, kGatherSmallFew, kGatherLarge})
+      if (cudaFuncSetAttribute(g, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
+          cudaSuccess)
+        return cudaErrorInvalidValue;
+    h->gather_ready = true;
+  }
+  return launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
+                       tiny ? kGatherTinyStage : small ? kGatherSmallStage : kGatherLargeStage);
+}
+
+}  // namespace
+
 extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* const* rows_ptrs,
                              const int64_t* rows_per_rank, const int32_t* const* src_row_ptrs,
                              const int32_t* const* key_ptrs, const int64_t* items_per_rank,
@@ -872,39 +960,83 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     if (e == cudaSuccess) e = launch_kernel(dispatch_rank_kernel, grid, 32, 0, s, true, D);
   }
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
-  const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
-  if (aligned) {
-    const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
-    const bool few = D.item_first[W] <= (long long)A2AV_GATHER_FEW_ITEMS *
-                                             (h->sms * A2AV_GATHER_CTAS_PER_SM);
-    const GatherKernel k = row_bytes <= 4096 ? kGatherTiny4
-                           : tiny            ? kGatherTiny2
-                           : small           ? (few ? kGatherSmallFew : kGatherSmall)
-                                             : kGatherLarge;
-    if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
-      if (cudaFuncSetAttribute(kGatherTiny4, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGatherSmem) != cudaSuccess ||
-          cudaFuncSetAttribute(kGatherTiny2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGatherSmem) != cudaSuccess ||
-          cudaFuncSetAttribute(kGatherSmall, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGatherSmem) != cudaSuccess ||
-          cudaFuncSetAttribute(kGatherSmallFew, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGatherSmem) != cudaSuccess ||
-          cudaFuncSetAttribute(kGatherLarge, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kGatherSmem) != cudaSuccess)
-        return A2AV_ERR_CUDA;
-      h->gather_ready = true;
-    }
-    e = launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
-                      tiny ? kGatherTinyStage : small ? kGatherSmallStage : kGatherLargeStage);
-  } else {
-    e = row_bytes >= kWarpRowBytes
-            ? launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
-                            kCopyThreads, 0, s, true, P, D)
-            : launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
-                            kCopyThreads, 0, s, true, P, D);
-  }
+  e = launch_copy(h, P, D, row_bytes, s);
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  return A2AV_OK;
+}
+
+extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
+                                  const void* const* peer_ptrs, const int64_t* in_splits_dev,
+                                  const int32_t* const* key_ptrs,
+                                  const int64_t* const* sorted_pos_ptrs,
+                                  const int64_t* items_per_rank, void* const* item_out_ptrs,
+                                  int64_t row_bytes, void* workspace, int64_t workspace_bytes,
+                                  void* stream) {
+  if (h == nullptr || peer_ptrs == nullptr || in_splits_dev == nullptr || key_ptrs == nullptr ||
+      sorted_pos_ptrs == nullptr || items_per_rank == nullptr || item_out_ptrs == nullptr ||
+      workspace == nullptr || row_bytes < 1 || keys_per_peer < 1)
+    return A2AV_ERR_INVALID_ARG;
+  const int W = h->W, K = keys_per_peer;
+  if ((long long)W * K > kMaxBins) return A2AV_ERR_UNSUPPORTED;
+  if (((uintptr_t)workspace & 255) != 0 || ((uintptr_t)in_splits_dev & 7) != 0 ||
+      workspace_bytes < A2AV_COMBINE_WORKSPACE_BYTES)
+    return A2AV_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (dev != h->device) return A2AV_ERR_INVALID_ARG;
+
+  DispatchParams D;
+  std::memset(&D, 0, sizeof(D));
+  D.item_first[0] = 0;
+  for (int r = 0; r < W; ++r) {
+    const long long m = items_per_rank[r];
+    if (m < 0) return A2AV_ERR_INVALID_ARG;
+    if (m > 0x7fffffffLL) return A2AV_ERR_UNSUPPORTED;
+    if (m > 0 && (key_ptrs[r] == nullptr || sorted_pos_ptrs[r] == nullptr ||
+                  item_out_ptrs[r] == nullptr))
+      return A2AV_ERR_INVALID_ARG;
+    D.key[r] = key_ptrs[r];
+    D.sorted_pos[r] = const_cast<long long*>(reinterpret_cast<const long long*>(sorted_pos_ptrs[r]));
+    D.items[r] = m;
+    D.item_first[r + 1] = D.item_first[r] + m;
+  }
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  D.flag = reinterpret_cast<int*>(ws);
+  D.status = h->d_status;
+  D.W = W;
+  D.K = K;
+  D.combine = 1;
+  bool vec16 = row_bytes % 16 == 0;
+  for (int r = 0; r < W; ++r)
+    vec16 = vec16 && ((uintptr_t)peer_ptrs[r] & 15) == 0 && ((uintptr_t)item_out_ptrs[r] & 15) == 0;
+  D.vec16 = vec16 ? 1 : 0;
+
+  // Rank-side buffers (the items' rows, written) in P.in, peer-side buffers
+  // (the dispatch layout, read) in P.out: the prologue's checks and offsets
+  // are those of the dispatch; its offsets table goes to the workspace.
+  Params P;
+  std::memset(&P, 0, sizeof(P));
+  for (int r = 0; r < W; ++r) {
+    P.in[r] = static_cast<const unsigned char*>(item_out_ptrs[r]);
+    P.out[r] = static_cast<unsigned char*>(const_cast<void*>(peer_ptrs[r]));
+  }
+  P.splits = reinterpret_cast<const long long*>(in_splits_dev);
+  P.split_stride = W;
+  P.out_so = reinterpret_cast<long long*>(ws + 256);
+  P.status = h->d_status;
+  P.rb = row_bytes;
+  P.limit = split_limit(W, row_bytes);
+  P.in_cap = 0;
+  P.out_cap = 0;
+  P.W = W;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
+  cudaError_t e = launch_kernel(combine_check_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads,
+                                0, s, h->pdl, P, D);
+  if (e != cudaSuccess) return A2AV_ERR_CUDA;
+  e = launch_copy(h, P, D, row_bytes, s);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
   return A2AV_OK;
 }
