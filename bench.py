@@ -950,7 +950,10 @@ def run_fused_combine(args):
                    else "dispatch_copy_kernel")
     roofline = {"bound": "hbm", "kernel": f"a2av_combine_items (checks, then {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
-                "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4), "traffic": None,
+                "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
+                "traffic": measured_traffic(copy_kernel + ":" + args.workload +
+                                            (f"_h{args.hidden}" if args.workload == "cfg3"
+                                             and args.hidden != 7168 else "") + "_combine", algo),
                 "algorithmic_bytes_per_launch": algo}
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
