@@ -49,13 +49,23 @@ constexpr int kScanBatch = 16;  // counts a scan thread loads at once
 static_assert(kMaxBins <= 4 * kScanThreads, "the finishing scan CTA holds 4 keys per thread");
 constexpr int kCopyThreads = 256;
 constexpr int kCopyCtasPerSm = 4;
-constexpr int kCopyCtasPerSmWarpRows = 3;  // the vector runs want up to 85 registers
+#ifndef A2AV_COPY_WARP_ROWS_CTAS_PER_SM
+#define A2AV_COPY_WARP_ROWS_CTAS_PER_SM 3  // the vector runs want up to 85 registers
+#endif
+constexpr int kCopyCtasPerSmWarpRows = A2AV_COPY_WARP_ROWS_CTAS_PER_SM;
 constexpr long long kWarpRowBytes = 64;  // rows this long get a warp each
 constexpr int kItemsPerThread = 4;      // items a thread copies at once (short rows)
 #ifndef A2AV_COPY_VEC_ROWS
 #define A2AV_COPY_VEC_ROWS 4
 #endif
 constexpr int kVecRows = A2AV_COPY_VEC_ROWS;  // 16-byte vectors a lane keeps in flight (warp rows)
+// The combine's aligned warp rows: twice the vectors in flight at two CTAs an
+// SM (123 registers, no spill).  Measured on MoE rows of 512 B and 1 KiB: the
+// combine 5-9 % faster than at 4 vectors and three CTAs; the dispatch, which
+// reads each token's row once for its two experts, no faster; rows that need
+// realigning 7-20 % slower at two CTAs.
+constexpr int kVecRowsWide = 8;
+constexpr int kCopyCtasPerSmWide = 2;
 constexpr long long kVecMaxRow = 64 * 1024;  // flat vector runs up to this row size
 
 struct DispatchParams {
@@ -495,9 +505,12 @@ __device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc,
 
 // kWarpRows: rows of kWarpRowBytes or more, a warp per row (each kernel
 // instantiation holds one of the two loops, so neither pays the other's
-// registers).
-template <bool kWarpRows>
-__global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRows : kCopyCtasPerSm)
+// registers); kVec: the 16-byte vectors a lane keeps in flight on aligned
+// warp rows.
+template <bool kWarpRows, int kVec = kVecRows>
+__global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasPerSm
+                                                : kVec > kVecRows ? kCopyCtasPerSmWide
+                                                                  : kCopyCtasPerSmWarpRows)
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   if (flagged(D)) return;
@@ -512,16 +525,22 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
   const long long teams = warp_rows ? (long long)gridDim.x * (kCopyThreads / 32)
                                     : (long long)gridDim.x * kCopyThreads;
   if constexpr (warp_rows) {
-    // A warp takes 32 consecutive items: lane l reads item l's key, position
-    // and source row (one round trip for all 32), then the warp copies the
-    // 32 rows.  16-byte aligned rows are copied as one flat run of vectors
-    // over all 32 rows, kVecRows x 16 bytes per lane in flight; other rows
-    // one at a time with the realigning span copy.
+    // A warp takes a batch of up to 32 consecutive items: lane l reads item
+    // l's key, position and source row (one round trip for the batch), then
+    // the warp copies the batch's rows.  16-byte aligned rows are copied as
+    // one flat run of vectors over the batch, kVec x 16 bytes per lane in
+    // flight; other rows one at a time with the realigning span copy.  The
+    // batch size gives every warp the same number of batches: with 32 items
+    // a batch, 131072 items over 3648 warps would leave a second round to one
+    // warp in eight, and the kernel would take twice the time of the rest.
     const int lane = threadIdx.x & 31;
-    for (long long g0 = team * 32; g0 < total; g0 += teams * 32) {
+    const long long rounds = (total + teams * 32 - 1) / (teams * 32);
+    const long long batch = rounds > 0 ? (total + teams * rounds - 1) / (teams * rounds) : 32;
+    for (long long g0 = team * batch; g0 < total; g0 += teams * batch) {
       const long long g = g0 + lane;
+      const int n = total - g0 < batch ? (int)(total - g0) : (int)batch;
       long long mdst = 0, msrc = 0;
-      if (g < total) {
+      if (lane < n) {
         int r = 0;
         while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
         const long long i = g - D.item_first[r];
@@ -537,14 +556,13 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
           msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
         }
       }
-      const int n = total - g0 < 32 ? (int)(total - g0) : 32;
       if (D.vec16 && rb <= kVecMaxRow) {
         const unsigned V = (unsigned)(rb >> 4), nv = (unsigned)n * V;  // < 2^17
-        for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVecRows) {  // warp-uniform trip count
-          uint4 v[kVecRows];
-          long long d[kVecRows];
+        for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVec) {  // warp-uniform trip count
+          uint4 v[kVec];
+          long long d[kVec];
 #pragma unroll
-          for (int q = 0; q < kVecRows; ++q) {
+          for (int q = 0; q < kVec; ++q) {
             const unsigned idx = b0 + q * 32 + lane;
             const bool ok = idx < nv;
             const unsigned j = ok ? idx / V : 0, c = ok ? idx - j * V : 0;
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
             if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s) + c);
           }
 #pragma unroll
-          for (int q = 0; q < kVecRows; ++q)
+          for (int q = 0; q < kVec; ++q)
             if (b0 + q * 32 + lane < nv) st_stream(reinterpret_cast<uint4*>(d[q]), v[q]);
         }
       } else {
@@ -826,12 +844,16 @@ namespace {
 cudaError_t launch_copy(a2av_handle* h, const Params& P, const DispatchParams& D,
                         long long row_bytes, cudaStream_t s) {
   const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
-  if (!aligned)
-    return row_bytes >= kWarpRowBytes
-               ? launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
-                               kCopyThreads, 0, s, true, P, D)
-               : launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
-                               kCopyThreads, 0, s, true, P, D);
+  if (!aligned) {
+    if (row_bytes < kWarpRowBytes)
+      return launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
+                           kCopyThreads, 0, s, true, P, D);
+    if (D.combine && D.vec16 && row_bytes <= kVecMaxRow)
+      return launch_kernel(dispatch_copy_kernel<true, kVecRowsWide>,
+                           dim3(h->sms * kCopyCtasPerSmWide), kCopyThreads, 0, s, true, P, D);
+    return launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
+                         kCopyThreads, 0, s, true, P, D);
+  }
   const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
   const bool few = D.item_first[D.W] <= (long long)A2AV_GATHER_FEW_ITEMS *
                                              (h->sms * A2AV_GATHER_CTAS_PER_SM);
