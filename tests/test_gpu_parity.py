@@ -60,10 +60,10 @@ def test_cfg3_seeds_small_grid(seed):
     exchange_checked(w.inputs, w.splits, w.row_bytes, ctas_per_sm=1)
 
 
-@pytest.mark.parametrize("mib", [1, 2, 4, 8, 16, 32, 64])
+@pytest.mark.parametrize("mib", [0.5, 1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("path", [AUTO, VEC, STAGED])
 def test_cfg2_sweep_points(mib, path):
-    w = wl.cfg2(mib << 20)
+    w = wl.cfg2(int(mib * (1 << 20)))
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path)
 
 

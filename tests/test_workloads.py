@@ -39,7 +39,8 @@ def test_cfg2_rows_and_prefix_consistency():
     big = wl.cfg2(1 << 22)
     for r in range(4):  # a smaller payload is a prefix of a larger one (same seed)
         assert np.array_equal(big.inputs[r][: w.inputs[r].size], w.inputs[r])
-    assert wl.CFG2_SWEEP_BYTES[0] == 1 << 20 and wl.CFG2_SWEEP_BYTES[-1] == 1 << 32
+    # the page's fourteen payloads: 0.5 MiB .. 4 GiB in powers of two
+    assert wl.CFG2_SWEEP_BYTES == [1 << k for k in range(19, 33)]
 
 
 def test_random_bits_independent_of_threads(monkeypatch):

@@ -58,8 +58,10 @@ __all__ = [
 _PIECE = 4 << 20  # bytes per independently seeded piece
 
 CFG2_ROW_BYTES = 7168 * 2
-# per-rank payloads of the sweep: 1 MiB .. 4 GiB in powers of two
-CFG2_SWEEP_BYTES = [1 << k for k in range(20, 33)]
+# per-rank payloads of the sweep: 0.5 MiB .. 4 GiB in powers of two, the
+# fourteen rows of the "Before" and "After" tables of "[a2av] Improve tuning
+# for 4 GPUs" (pytorch PR 154580)
+CFG2_SWEEP_BYTES = [1 << k for k in range(19, 33)]
 
 
 @dataclass
