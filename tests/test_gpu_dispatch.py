@@ -96,6 +96,33 @@ def test_dispatch_without_items():
     dispatch_checked(2, rows, empty, empty, 16)
 
 
+@pytest.mark.parametrize("W,K", [(2, 100), (4, 100)])
+def test_dispatch_without_items_many_keys(W, K):
+    """Past the one-kernel key count (W*K > 256) an empty batch still goes
+    through the counting kernels: 200 keys with the count kernel's own scan,
+    400 with the scan kernel; both write zero splits and offsets."""
+    rows = [np.arange(64, dtype=np.uint8)] * W
+    empty = [np.zeros(0, np.int32)] * W
+    dispatch_checked(K, rows, empty, empty, 16)
+
+
+@pytest.mark.parametrize("rb", [16, 64])
+@pytest.mark.parametrize("W,K,m", [
+    (8, 8, 32768),    # 16 groups of 2048 items over 64 keys: the count kernel scans
+    (8, 8, 32769),    # 17 groups: the scan kernel
+    (2, 13, 73728),   # 36 groups over 26 keys: the count kernel scans
+    (2, 13, 73729),   # 37 groups: the scan kernel
+])
+def test_group_scan_either_side_of_the_fused_limit(W, K, m, rb):
+    rng = np.random.default_rng(m + rb)
+    n = 500
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    counts = [m] + [int(rng.integers(2049, m + 1)) for _ in range(W - 2)] + [0]
+    src = [rng.integers(0, n, c).astype(np.int32) for c in counts]
+    key = [np.minimum(rng.geometric(0.05, c) - 1, W * K - 1).astype(np.int32) for c in counts]
+    dispatch_checked(K, rows, src, key, rb)
+
+
 def test_dispatch_then_combine_restores_key_order():
     w = wl.cfg3(7, tokens=512, hidden=256)
     K, rows, src, key = wl.dispatch_items(w)

@@ -81,12 +81,15 @@ struct DispatchParams {
   long long* key_start;             // workspace: [W][NB]
   long long* key_total;             // workspace: [W][NB]
   int* hist;                        // workspace: [W][ranges_max][NB]
+  int* grp;                         // workspace: [W][groups_max][NB]
   int* pos;                         // workspace: [W][pos_stride] item positions in key order
   int* status;
   long long* in_splits_out;         // optional [W][W]
   int vec16;                        // every row and buffer 16-byte aligned
   int combine;                      // the fused combine: rows move the other way (below)
   long long ranges_max;
+  long long groups_max;             // ranges_max / kCountWarps, rounded up
+  int fuse_scan;                    // the count kernel's last CTA per rank scans the groups
   long long pos_stride;
   int W, K;
 };
@@ -110,46 +113,6 @@ __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
   record_error(D.status, code);
 }
 
-// A warp per range of 256 items (8 per lane, all loads issued together),
-// eight ranges per CTA, so that a batch of a few thousand ranges is resident
-// in one wave; each warp counts its keys in its own slice of shared memory
-// (dynamic: 8 x W*K ints).
-constexpr int kCountWarps = 8;
-
-__global__ void __launch_bounds__(32 * kCountWarps) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
-  chain_release();
-  chain_wait();
-  const int r = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long range = (long long)blockIdx.x * kCountWarps + warp;
-  const long long i0 = range * kRange, m = D.items[r];
-  if (i0 >= m) return;  // warps act alone below: no CTA barrier
-  extern __shared__ int count_hist[];
-  const int NB = D.W * D.K;
-  int* hist = count_hist + warp * NB;
-  for (int b = lane; b < NB; b += 32) hist[b] = 0;
-  int keys[kRange / 32], srcs[kRange / 32];
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = i0 + c * 32 + lane;
-    keys[c] = i < m ? D.key[r][i] : 0;
-    srcs[c] = i < m ? D.src[r][i] : 0;
-  }
-  __syncwarp();
-  int bad = 0;
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    if (i0 + c * 32 + lane >= m) continue;
-    if (keys[c] < 0 || keys[c] >= NB || srcs[c] < 0 || srcs[c] >= D.rows[r])
-      bad = 1;
-    else
-      atomicAdd(&hist[keys[c]], 1);
-  }
-  if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
-  __syncwarp();
-  int* H = D.hist + ((long long)r * D.ranges_max + range) * NB;
-  for (int b = lane; b < NB; b += 32) H[b] = hist[b];
-}
-
 // Block-wide exclusive scan of one value per thread (kScanThreads threads);
 // returns the exclusive prefix, *total gets the sum.  `warp_sums` holds
 // kScanThreads / 32 entries.
@@ -169,8 +132,151 @@ __device__ __forceinline__ long long block_exclusive_scan(long long x, long long
   return base + inc - x;
 }
 
-// CTA (b, r): key b of rank r.  H[j][b] becomes the number of items with key
-// b in ranges < j (thread t scans a run of consecutive ranges), and
+// Rank r's key totals (tot[b], in shared memory, NB <= kScanThreads) become
+// key_total[r][*], key_start[r][*] (items with a smaller key) and S[r][p]
+// (items with key / K = p).  Every thread of the CTA calls it.
+__device__ __forceinline__ void finish_rank(const DispatchParams& D, int r, const long long* tot,
+                                            long long* warp_sums) {
+  const int t = threadIdx.x, NB = D.W * D.K;
+  const long long x = t < NB ? tot[t] : 0;
+  long long all;
+  const long long start = block_exclusive_scan(x, warp_sums, &all);
+  if (t < NB) {
+    D.key_total[(long long)r * NB + t] = x;
+    D.key_start[(long long)r * NB + t] = start;
+  }
+  if (t < D.W) {
+    long long sum = 0;
+    for (int k = 0; k < D.K; ++k) sum += tot[t * D.K + k];
+    D.S[(long long)r * D.W + t] = sum;
+  }
+}
+
+// Items are counted in ranges of kRange, ranges in groups of kCountWarps (a
+// count CTA).  After the count kernel, hist[r][j][b] holds the items with key
+// b in the earlier ranges of range j's group, and grp[r][c][b] the group's
+// count; the scan (below) turns grp[r][*][b] into exclusive prefixes over the
+// groups, so that an item's place among the equal keys of its rank is
+// key_start[b] + grp[c][b] + hist[j][b] + its rank within the range.
+//
+// A warp per range of 256 items (8 per lane, all loads issued together),
+// eight ranges per CTA, registers capped for six CTAs an SM so that 7296
+// ranges (1.8 M items) are resident in one wave; each warp counts its keys in
+// its own slice of shared memory (dynamic: 8 x W*K ints).  With D.fuse_scan
+// (at most kFuseScanPer groups per thread and key) the last count CTA of each
+// rank to finish does the scan itself and the scan kernel is not launched:
+// one launch and one kernel boundary fewer (MoE dispatch of 8192 tokens).
+constexpr int kCountWarps = 8;
+constexpr int kGroupItems = kCountWarps * kRange;  // 2048
+constexpr int kFuseScanPer = 4;                    // groups a thread scans in the fused scan
+static_assert(32 * kCountWarps == kScanThreads, "a count CTA can run the block scan");
+
+// The fused scan: one CTA (kScanThreads threads) over rank r's C groups.
+// Thread t takes key b = t % NB and the slice g = t / NB of at most
+// kFuseScanPer consecutive groups (G = kScanThreads / NB slices per key).
+__device__ __forceinline__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) {
+  const int t = threadIdx.x, NB = D.W * D.K, G = kScanThreads / NB;
+  const int b = t % NB, g = t / NB;
+  const long long per = (C + G - 1) / G;
+  const long long c0 = g < G ? g * per : C, c1 = c0 + per < C ? c0 + per : C;
+  int* A = D.grp + (long long)r * D.groups_max * NB + b;  // group c at A[c * NB]
+  __shared__ long long part[kScanThreads];
+  __shared__ long long tot[kScanThreads];
+  __shared__ long long warp_sums[kScanThreads / 32];
+  int v[kFuseScanPer];
+  long long local = 0;
+#pragma unroll
+  for (int q = 0; q < kFuseScanPer; ++q) {
+    v[q] = c0 + q < c1 ? __ldcg(A + (c0 + q) * NB) : 0;
+    local += v[q];
+  }
+  part[t] = local;
+  __syncthreads();
+  long long base = 0, total = 0;
+  if (g < G)
+    for (int h = 0; h < G; ++h) {
+      const long long x = part[h * NB + b];
+      if (h < g) base += x;
+      total += x;
+    }
+#pragma unroll
+  for (int q = 0; q < kFuseScanPer; ++q) {
+    if (c0 + q < c1) A[(c0 + q) * NB] = (int)base;
+    base += v[q];
+  }
+  if (g == 0) tot[b] = total;
+  __syncthreads();
+  finish_rank(D, r, tot, warp_sums);
+}
+
+__global__ void __launch_bounds__(32 * kCountWarps, 6) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
+  chain_release();
+  chain_wait();
+  const int r = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
+  const long long c = blockIdx.x;
+  const long long range = c * kCountWarps + warp;
+  const long long i0 = range * kRange, m = D.items[r];
+  const int NB = D.W * D.K;
+  if (c * kGroupItems >= m) {  // no items in this CTA's ranges (uniform over the CTA)
+    if (c == 0 && D.fuse_scan) {  // a rank without items: zero counts and splits
+      __shared__ long long zero[kScanThreads];
+      __shared__ long long zero_sums[kScanThreads / 32];
+      zero[t] = 0;
+      __syncthreads();
+      finish_rank(D, r, zero, zero_sums);
+    }
+    return;
+  }
+  extern __shared__ int count_hist[];
+  int* hist = count_hist + warp * NB;
+  for (int b = lane; b < NB; b += 32) hist[b] = 0;
+  if (i0 < m) {
+    int keys[kRange / 32], srcs[kRange / 32];
+#pragma unroll
+    for (int q = 0; q < kRange / 32; ++q) {
+      const long long i = i0 + q * 32 + lane;
+      keys[q] = i < m ? D.key[r][i] : 0;
+      srcs[q] = i < m ? D.src[r][i] : 0;
+    }
+    __syncwarp();
+    int bad = 0;
+#pragma unroll
+    for (int q = 0; q < kRange / 32; ++q) {
+      if (i0 + q * 32 + lane >= m) continue;
+      if (keys[q] < 0 || keys[q] >= NB || srcs[q] < 0 || srcs[q] >= D.rows[r])
+        bad = 1;
+      else
+        atomicAdd(&hist[keys[q]], 1);
+    }
+    if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  }
+  __syncthreads();
+  // in-group prefixes of the ranges that hold items, and the group's count
+  const long long R = (m + kRange - 1) / kRange;
+  for (int b = t; b < NB; b += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kCountWarps; ++w) {
+      const long long j = c * kCountWarps + w;
+      if (j < R) D.hist[((long long)r * D.ranges_max + j) * NB + b] = run;
+      run += count_hist[w * NB + b];
+    }
+    D.grp[((long long)r * D.groups_max + c) * NB + b] = run;
+  }
+  if (!D.fuse_scan) return;
+  // The rank's last CTA to finish (an atomic count, after a fence) scans.
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  const long long C = (m + kGroupItems - 1) / kGroupItems;
+  if (t == 0) last = atomicAdd(&D.done[r], 1) == (int)(C - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  scan_groups_in_cta(D, r, C);
+}
+
+// CTA (b, r): key b of rank r.  grp[c][b] becomes the number of items with
+// key b in groups < c (thread t scans a run of consecutive groups), and
 // key_total[r][b] the key's count.  The last CTA of rank r to finish (an
 // atomic count, after a fence) turns the totals into key_start[r][*] (items
 // with a smaller key) and S[r][p] (items with key / K = p).
@@ -180,11 +286,12 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
   if (flagged(D)) return;
   const int b = blockIdx.x, r = blockIdx.y, NB = D.W * D.K, t = threadIdx.x;
   __shared__ long long warp_sums[kScanThreads / 32];
+  __shared__ long long tot[kMaxBins];
   __shared__ int last;
-  const long long R = (D.items[r] + kRange - 1) / kRange;
-  int* H = D.hist + (long long)r * D.ranges_max * NB + b;  // range j at H[j * NB]
-  const long long per = (R + kScanThreads - 1) / kScanThreads;
-  const long long j0 = t * per, j1 = j0 + per < R ? j0 + per : R;
+  const long long C = (D.items[r] + kGroupItems - 1) / kGroupItems;
+  int* H = D.grp + (long long)r * D.groups_max * NB + b;  // group j at H[j * NB]
+  const long long per = (C + kScanThreads - 1) / kScanThreads;
+  const long long j0 = t * per, j1 = j0 + per < C ? j0 + per : C;
   // A thread's first kScanBatch counts are loaded together and kept in
   // registers for the rewrite (runs longer than that are walked in batches).
   int first[kScanBatch];
@@ -237,12 +344,16 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int k = 4 * t + q;
-    if (k < NB) D.key_start[(long long)r * NB + k] = start;
+    if (k < NB) {
+      D.key_start[(long long)r * NB + k] = start;
+      tot[k] = v[q];
+    }
     start += v[q];
   }
+  __syncthreads();
   if (t < D.W) {
     long long s = 0;
-    for (int k = 0; k < D.K; ++k) s += __ldcg(D.key_total + (long long)r * NB + t * D.K + k);
+    for (int k = 0; k < D.K; ++k) s += tot[t * D.K + k];
     D.S[(long long)r * D.W + t] = s;
   }
 }
@@ -256,7 +367,8 @@ __global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant
   if (i0 >= m) return;
   __shared__ long long next[kMaxBins];  // next position of each key in this range
   const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
-  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + H[k];
+  const int* A = D.grp + ((long long)r * D.groups_max + blockIdx.x / kCountWarps) * NB;
+  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + A[k] + H[k];
   __syncwarp();
   // All keys of the range are loaded at once (8 per lane), then ranked in order.
   int keys[kRange / 32];
@@ -368,7 +480,8 @@ __global__ void __launch_bounds__(32 * kRankCopyWarps, A2AV_RANK_COPY_MIN_CTAS)
   if (bad_splits || i0 >= m) return;
   int* next = next_all[warp];
   const int* H = D.hist + ((long long)r * D.ranges_max + range) * NB;
-  for (int k = lane; k < NB; k += 32) next[k] = (int)D.key_start[(long long)r * NB + k] + H[k];
+  const int* A = D.grp + ((long long)r * D.groups_max + range / kCountWarps) * NB;
+  for (int k = lane; k < NB; k += 32) next[k] = (int)D.key_start[(long long)r * NB + k] + A[k] + H[k];
   int keys[kRange / 32];
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
@@ -806,7 +919,7 @@ constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 
 
 struct Layout {
-  long long flag, done, S, key_start, key_total, pos, hist, total;
+  long long flag, done, S, key_start, key_total, pos, hist, grp, total;
 };
 
 Layout layout(int W, int K, long long max_items) {
@@ -820,8 +933,10 @@ Layout layout(int W, int K, long long max_items) {
   L.key_start = L.S + up(8LL * W * W);
   L.key_total = L.key_start + up(8LL * W * NB);
   L.pos = L.key_total + up(8LL * W * NB);
+  const long long groups = (ranges + kCountWarps - 1) / kCountWarps;
   L.hist = L.pos + up(4LL * W * (max_items < 1 ? 1 : max_items));
-  L.total = L.hist + up(4LL * W * (ranges < 1 ? 1 : ranges) * NB);
+  L.grp = L.hist + up(4LL * W * (ranges < 1 ? 1 : ranges) * NB);
+  L.total = L.grp + up(4LL * W * (groups < 1 ? 1 : groups) * NB);
   return L;
 }
 
@@ -927,11 +1042,17 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   D.pos = reinterpret_cast<int*>(ws + L.pos);
   D.pos_stride = max_items < 1 ? 1 : max_items;
   D.hist = reinterpret_cast<int*>(ws + L.hist);
+  D.grp = reinterpret_cast<int*>(ws + L.grp);
   D.status = h->d_status;
   D.in_splits_out = reinterpret_cast<long long*>(in_splits_dev);
   D.ranges_max = ranges_max;
+  D.groups_max = (ranges_max + kCountWarps - 1) / kCountWarps;
   D.W = W;
   D.K = K;
+  // One count CTA per rank scans its groups when a thread's share of one key
+  // fits kFuseScanPer registers; the scan kernel and its launch are skipped.
+  const int slices = kScanThreads / (W * K);
+  D.fuse_scan = slices > 0 && D.groups_max <= (long long)kFuseScanPer * slices;
   bool vec16 = row_bytes % 16 == 0;
   for (int r = 0; r < W; ++r)
     vec16 = vec16 && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
@@ -965,15 +1086,18 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   if (small_path) {
     e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
-    const dim3 grid((unsigned)ranges_max, (unsigned)W);
-    const dim3 grid_count((unsigned)((ranges_max + kCountWarps - 1) / kCountWarps), (unsigned)W);
+    // (at least one CTA per rank: a batch without items still gets its
+    // counts, splits and offsets written)
+    const long long ranges = ranges_max > 0 ? ranges_max : 1;
+    const dim3 grid((unsigned)ranges, (unsigned)W);
+    const dim3 grid_count((unsigned)((ranges + kCountWarps - 1) / kCountWarps), (unsigned)W);
     e = launch_kernel(dispatch_count_kernel, grid_count, 32 * kCountWarps,
                       (size_t)kCountWarps * W * K * sizeof(int), s, h->pdl, D);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !D.fuse_scan)
       e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
                         0, s, true, D);
     if (e == cudaSuccess && fuse) {
-      const dim3 grid2((unsigned)((ranges_max + kRankCopyWarps - 1) / kRankCopyWarps),
+      const dim3 grid2((unsigned)((ranges + kRankCopyWarps - 1) / kRankCopyWarps),
                        (unsigned)W);
       e = launch_kernel(dispatch_rank_copy_kernel, grid2, 32 * kRankCopyWarps, 0, s, true, P, D);
       if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
