@@ -218,7 +218,10 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *                     dispatch in flight.
  *
  * Two to four kernel launches on `stream`: per-range key histograms,
- * per-key scans, stable ranking within ranges (warp match) -- one fused
+ * per-key scans over groups of eight ranges (done by the histogram kernel's
+ * last block of each rank when a rank has at most 4 * floor(256 / (W *
+ * keys_per_peer)) groups of 2048 items), stable ranking within ranges (warp
+ * match) -- one fused
  * kernel when every rank has at most 2048 items and W * keys_per_peer <=
  * 256 -- then the row gather-copy, which alone writes the caller's buffers
  * (for rows shorter than 64 bytes past that size the ranking kernel copies
