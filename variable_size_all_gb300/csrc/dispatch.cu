@@ -76,7 +76,7 @@ struct DispatchParams {
   long long rows[kMaxW];            // source rows per rank
   long long item_first[kMaxW + 1];  // exclusive prefix of m_r
   int* flag;                        // workspace: set once input is found invalid
-  int* done;                        // workspace: [W] scan CTAs finished per rank
+  int* done;                        // workspace: [W] CTAs finished per rank (the one that scans)
   long long* S;                     // workspace: [W][W]
   long long* key_start;             // workspace: [W][NB]
   long long* key_total;             // workspace: [W][NB]
