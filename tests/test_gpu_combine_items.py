@@ -81,6 +81,34 @@ def test_inverse_of_the_gpu_dispatch(rb):
         assert np.array_equal(back[r].cpu().numpy(), want), r
 
 
+@pytest.mark.parametrize("hidden", [7168, 512])
+def test_full_size_moe_round_trip(hidden):
+    """The MoE workload at full size (W=8, 8192 tokens a rank, top-2), in the
+    launch configuration the benchmark times: combine_items(dispatch(x))
+    gives every item its token's row back (14 KiB rows: the gather; 1 KiB
+    rows: the warp copy at eight vectors per lane)."""
+    w = wl.cfg3(0, hidden=hidden)
+    K, rows, src, key = wl.dispatch_items(w)
+    W, rb = w.W, w.row_bytes
+    d_rows = [torch.from_numpy(r).cuda() for r in rows]
+    d_src = [torch.from_numpy(x).cuda() for x in src]
+    d_key = [torch.from_numpy(x).cuda() for x in key]
+    d_out = [torch.empty(int(w.splits[:, p].sum()) * rb, dtype=torch.uint8, device="cuda")
+             for p in range(W)]
+    so = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    isp = torch.empty((W, W), dtype=torch.int64, device="cuda")
+    d_pos = [torch.empty(x.size, dtype=torch.int64, device="cuda") for x in key]
+    back = [torch.full((x.size * rb,), 0xEE, dtype=torch.uint8, device="cuda") for x in key]
+    with a2av.A2av(W) as eng:
+        eng.dispatch(d_rows, d_src, d_key, K, d_out, so, d_pos, rb, in_splits=isp)
+        eng.combine_items(d_out, isp, d_key, d_pos, K, back, rb)
+        assert eng.status() == a2av.OK
+    assert np.array_equal(isp.cpu().numpy(), w.splits), "split matrix differs from the workload's"
+    for r in range(W):
+        want = torch.index_select(d_rows[r].view(-1, rb), 0, d_src[r].long())
+        assert torch.equal(back[r].view(-1, rb), want), f"rank {r}: rows not restored"
+
+
 @pytest.mark.parametrize("rb", [3, 16, 64, 2048, 14336])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_against_the_oracle(rb, aligned):
