@@ -55,7 +55,8 @@ typedef enum {
   A2AV_ERR_CUDA = -3,        /* a CUDA runtime call failed (no device, launch failure...) */
   A2AV_ERR_BAD_SPLITS = -4,  /* device-detected: the split matrix is invalid */
   A2AV_ERR_TIMEOUT = -5,     /* device-detected: a bounded wait inside a kernel gave up */
-  A2AV_ERR_BAD_INDEX = -6    /* device-detected: a dispatch key or source row is out of range */
+  A2AV_ERR_BAD_INDEX = -6    /* device-detected: a dispatch key or source row, or a combine
+                                position, is out of range */
 } a2av_status_t;
 
 /* Copy engine selection (a2av_set_path). */
@@ -118,12 +119,16 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
  *
  * Memory rules: no output may overlap an input, the split matrix or another
  * output; inputs may share memory.  Input and output buffers may also be
- * pinned host memory that the device can address (zero-copy over the host
- * link) when the vector engine runs (A2AV_PATH_VECTOR): it reaches every
- * buffer with plain loads and stores.  The bulk and staged engines use
- * cp.async.bulk copies, which this library applies to device memory only,
- * and AUTO does not inspect pointers: request A2AV_PATH_VECTOR for
- * host-resident buffers (the Python binding does so by itself).  Bytes of an input past its last chunk are
+ * host memory that the device can address (pinned or registered memory, or
+ * system memory reached over NVLink-C2C: zero-copy over the host link).  The
+ * library looks at every buffer pointer (cudaPointerGetAttributes) and runs
+ * the vector engine, whose plain loads and stores reach any of them, unless
+ * every buffer is device memory; the bulk and staged engines' cp.async.bulk
+ * copies are applied to device memory only, whatever path was requested.
+ * The answer for the handle's last two sets of buffer pointers is
+ * remembered; a2av_set_path and a2av_set_grid clear that memory (call one
+ * after freeing a buffer and allocating memory of another kind at the same
+ * address).  Bytes of an input past its last chunk are
  * never used and bytes of an output past its last received row are never
  * written.  (Whole 16-byte-aligned granules that hold a needed input byte may
  * be loaded and their other bytes discarded; such loads never leave the
@@ -135,6 +140,15 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
  * nonzero; 0 rows for a NULL buffer.  Invalid splits write NOTHING (no output
  * byte, no out_splits_offsets entry) and record A2AV_ERR_BAD_SPLITS in the
  * handle's status word, read by a2av_status.
+ *
+ * Streams: a small exchange on a side stream beside long kernels that hold
+ * every SM (GEMMs) gets SMs only between those kernels unless its stream has
+ * a higher priority.  Measured on one GB300 (a 10 MB keyed-jagged exchange,
+ * about 16 us alone, beside 8192^3 bf16 GEMMs on the default-priority main
+ * stream): 254 us per step on a default-priority side stream, 25 us on a
+ * stream created with the highest priority
+ * (cudaStreamCreateWithPriority), at no cost to the GEMMs.  Give
+ * latency-sensitive exchanges a high-priority stream.
  *
  * Host errors (nothing launched): A2AV_ERR_INVALID_ARG for a NULL handle or
  * array, a NULL split or out_splits_offsets pointer, a misaligned split
@@ -217,16 +231,21 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *                     max_r m_r) bytes, 256-byte aligned, not shared with a
  *                     dispatch in flight.
  *
- * Two to four kernel launches on `stream`: per-range key histograms,
- * per-key scans over groups of eight ranges (done by the histogram kernel's
- * last block of each rank when a rank has at most 4 * floor(256 / (W *
- * keys_per_peer)) groups of 2048 items), stable ranking within ranges (warp
- * match) -- one fused
- * kernel when every rank has at most 2048 items and W * keys_per_peer <=
- * 256 -- then the row gather-copy, which alone writes the caller's buffers
- * (for rows shorter than 64 bytes past that size the ranking kernel copies
- * the rows itself, after checking the split matrix).  One memset of the
- * workspace's first 256 bytes precedes them.
+ * Launches on `stream` (a2av_last_dispatch reports which):
+ *  - at most 4096 items over all ranks (and W * W * keys_per_peer <= 2048):
+ *    ONE kernel, no workspace use, no memset -- every block counts all the
+ *    keys itself, derives the split matrix and the plan, then places and
+ *    copies its share of the items;
+ *  - otherwise a memset of the workspace's first 256 bytes, then: per-range
+ *    key counts and each item's rank within its 256-item range (the scan of
+ *    the counts over groups of ranges done by that kernel's last block of
+ *    each rank, or, for ranks with very many groups, by a second kernel;
+ *    one kernel per rank does both when every rank has at most 2048 items
+ *    and W * keys_per_peer <= 256), then the row copy, which alone writes
+ *    the caller's buffers: a cp.async.bulk gather for 16-byte aligned rows
+ *    of 64 bytes to 32 KiB, register copies otherwise (for rows shorter than
+ *    64 bytes past the one-kernel-per-rank size, one kernel places and
+ *    copies the rows of each range after checking the split matrix).
  * Errors: host -- A2AV_ERR_INVALID_ARG (NULL arrays, keys_per_peer < 1,
  * negative counts, a small or misaligned workspace), A2AV_ERR_UNSUPPORTED
  * (W * keys_per_peer > A2AV_MAX_DISPATCH_KEYS, counts above 2^31 - 1);
@@ -272,8 +291,9 @@ typedef struct {
  *
  * The grid is divided among the exchanges in proportion to their bytes
  * (each gets at least one CTA).  Engine: vector when the handle's path is
- * A2AV_PATH_VECTOR; bulk when every row and buffer of every exchange is
- * 16-byte aligned (path AUTO or BULK); staged otherwise.  Memory rules as for
+ * A2AV_PATH_VECTOR or any buffer of the call is outside device memory; bulk
+ * when every row and buffer of every exchange is 16-byte aligned (path AUTO
+ * or BULK); staged otherwise.  Memory rules as for
  * a2av_run, across all the exchanges: no output may overlap any input,
  * split matrix or other output of the call.  Validity is checked per
  * exchange: one with invalid splits writes nothing of its own (no output
@@ -304,7 +324,9 @@ int a2av_destroy(a2av_handle *h);
 /*
  * a2av_set_path -- choose the copy engine for later runs (a2av_path_t).
  * A2AV_PATH_BULK on a run whose row_bytes or buffer addresses are not all
- * 16-byte aligned falls back to the staged engine for that run.
+ * 16-byte aligned falls back to the staged engine for that run; a run with
+ * any buffer outside device memory takes the vector engine (a2av_run).
+ * Also forgets the handle's remembered pointer classifications.
  * Errors: A2AV_ERR_INVALID_ARG.
  */
 int a2av_set_path(a2av_handle *h, int path);
@@ -321,6 +343,15 @@ int a2av_set_grid(a2av_handle *h, int ctas_per_sm);
  * threads per CTA.  Any output pointer may be NULL.
  */
 int a2av_last_launch(const a2av_handle *h, int *path, int *grid, int *block);
+
+/*
+ * a2av_last_dispatch -- describe the most recent successful a2av_dispatch or
+ * a2av_combine_items of this handle: the number of kernels it enqueued, the
+ * number of workspace memsets before them (0 or 1) and the name of the
+ * kernel that moved the rows (a static string, "" before the first call).
+ * Any output pointer may be NULL.  Errors: A2AV_ERR_INVALID_ARG (h == NULL).
+ */
+int a2av_last_dispatch(const a2av_handle *h, int *kernels, int *memsets, const char **copy_kernel);
 
 /* a2av_error_string -- a static English description of a status code. */
 const char *a2av_error_string(int code);
@@ -361,9 +392,12 @@ int a2av_version(void);
  *  workspace          DEVICE scratch, 256-byte aligned, at least
  *                     A2AV_COMBINE_WORKSPACE_BYTES, not shared with a call in flight.
  *
- * Three launches after a 256-byte workspace memset: checks (the split
- * matrix, each key, each position within its destination's group), then the
- * dispatch's copy kernels with the rows moving the other way.  Device
+ * Launches: at most 4096 items over all ranks -- ONE kernel, no workspace
+ * memset (every block checks the split matrix and every key and position,
+ * then copies its share); otherwise a 256-byte workspace memset, a check
+ * kernel (the split matrix, each key, each position within its
+ * destination's group), then the dispatch's copy kernel with the rows
+ * moving the other way (a2av_last_dispatch reports which).  Device
  * errors write nothing: A2AV_ERR_BAD_SPLITS (as a2av_run; NULL buffers with
  * rows), A2AV_ERR_BAD_INDEX (a key outside [0, W * K) or a position outside
  * [in_off[r][p], in_off[r][p] + S[r][p])).  Host errors as a2av_dispatch
@@ -399,7 +433,10 @@ int a2av_combine_items(a2av_handle *h, int keys_per_peer, const void *const *pee
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) and configures the kernels, with that device
- * current.  Make that first call before any stream capture begins.
+ * current.  Make that first call before any stream capture begins.  The
+ * set-up is kept for the life of the process: a cudaDeviceReset (or any
+ * other teardown of the device's primary context) invalidates it, so do not
+ * call this entry point on a device after resetting it.
  *
  * Arguments: world_size, in_capacity_rows and out_capacity_rows as in
  * a2av_create; in_ptrs .. stream as in a2av_run (the copy engine is chosen as

@@ -115,9 +115,13 @@ def combine_checked(inputs, dispatch_so, rb, path=a2av.PATH_AUTO, in_mis=None, o
     return [outs[r].view.cpu().numpy()[: back[r] * rb] for r in range(W)]
 
 
-def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=None):
+def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=None,
+                     expect_copy=None, expect_kernels=None):
     """Fused dispatch on the GPU against the oracle's: outputs, offsets,
-    positions and the split matrix; canaries and slack untouched."""
+    positions and the split matrix; canaries and slack untouched.  With
+    ``expect_copy`` / ``expect_kernels``, also that the library took that
+    path (a2av_last_dispatch: the kernel that moved the rows, the number of
+    kernels enqueued)."""
     W = len(rows)
     rows_mis = rows_mis or [0] * W
     out_mis = out_mis or [0] * W
@@ -135,11 +139,16 @@ def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=
         eng.dispatch([g.view for g in g_rows], d_src, d_key, K, [g.view for g in g_out], so, d_pos,
                      rb, in_splits=isp)
         st = eng.status()
+        chain = eng.last_dispatch()
     finally:
         if own:
             eng.close()
     torch.cuda.synchronize()
     assert st == a2av.OK, f"device status {st}"
+    if expect_copy is not None:
+        assert chain["copy_kernel"] == expect_copy, chain
+    if expect_kernels is not None:
+        assert chain["kernels"] == expect_kernels, chain
     assert np.array_equal(isp.cpu().numpy(), ref_S), "dispatch split matrix differs"
     assert np.array_equal(so.cpu().numpy(), ref_so), "dispatch out_splits_offsets differ"
     for r in range(W):

@@ -46,6 +46,10 @@ def test_host_checks_without_gpu(lib):
     assert a2av.a2av_version() >= 10000
     assert a2av.a2av_error_string(a2av.ERR_BAD_SPLITS).startswith("invalid split")
     assert a2av.a2av_error_string(12345) == "unknown status"
+    for code in (a2av.ERR_INVALID_ARG, a2av.ERR_UNSUPPORTED, a2av.ERR_CUDA, a2av.ERR_BAD_SPLITS,
+                 a2av.ERR_TIMEOUT, a2av.ERR_BAD_INDEX):
+        assert a2av.a2av_error_string(code) != "unknown status", code
+    assert "out of range" in a2av.a2av_error_string(a2av.ERR_BAD_INDEX)
     assert a2av.a2av_create(0)[0] == a2av.ERR_INVALID_ARG
     assert a2av.a2av_create(a2av.MAX_RANKS + 1)[0] == a2av.ERR_UNSUPPORTED
     assert a2av.a2av_create(2, -1, 0)[0] == a2av.ERR_INVALID_ARG
@@ -54,6 +58,7 @@ def test_host_checks_without_gpu(lib):
     assert a2av.a2av_destroy(None) == a2av.OK
     assert a2av.a2av_set_path(None, 0) == a2av.ERR_INVALID_ARG
     assert a2av.a2av_last_launch(None)[0] == a2av.ERR_INVALID_ARG
+    assert a2av.a2av_last_dispatch(None)[0] == a2av.ERR_INVALID_ARG
     assert a2av.a2av_run_multi(None, []) == a2av.ERR_INVALID_ARG
     assert lib.a2av_run_multi(None, 1, None, None) == a2av.ERR_INVALID_ARG
 

@@ -109,14 +109,23 @@ def test_bound_dispatch_follows_new_keys(rb):
                 assert np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r])
 
 
-def test_bind_rejects_host_buffers():
-    W = 2
-    host = [torch.zeros(64, dtype=torch.uint8).pin_memory() for _ in range(W)]
-    dev = [torch.zeros(64, dtype=torch.uint8, device="cuda") for _ in range(W)]
-    S = torch.zeros((W, W), dtype=torch.int64, device="cuda")
+def test_bound_calls_on_host_buffers_take_the_vector_engine():
+    """The library, not the binding, routes host-resident buffers: a bound
+    call on pinned host memory runs the vector engine and is exact."""
+    import oracle
+    w = wl.cfg1(5)
+    W, rb = w.W, w.row_bytes
+    ref, ref_so = oracle.default().exchange(w.inputs, w.splits, rb)
+    host_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
+    outs = [torch.full((r.size,), 0xEE, dtype=torch.uint8, device="cuda") for r in ref]
+    S = torch.from_numpy(w.splits).cuda()
     so = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
     with a2av.A2av(W) as eng:
-        with pytest.raises(ValueError):
-            eng.bind_run(host, S, dev, so, 8)
-        with pytest.raises(ValueError):
-            eng.bind_run_multi([(dev, S, host, so, 8)])
+        eng.bind_run(host_in, S, outs, so, rb)()
+        assert eng.status() == a2av.OK
+        assert eng.last_launch()["path"] == a2av.PATH_VECTOR
+    for p in range(W):
+        assert np.array_equal(outs[p].cpu().numpy(), ref[p])
+    assert np.array_equal(so.cpu().numpy(), ref_so)
+
+

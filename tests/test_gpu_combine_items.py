@@ -23,8 +23,9 @@ def _cuda():
     a2av.build()
 
 
-def _combine_checked(K, peers, S, keys, pos, rb, mis=None, expect=None):
-    """Run the fused combine on host arrays; compare with the oracle's."""
+def _combine_checked(K, peers, S, keys, pos, rb, mis=None, expect=None, expect_copy=None):
+    """Run the fused combine on host arrays; compare with the oracle's (and,
+    with ``expect_copy``, that the library moved the rows with that kernel)."""
     W = len(peers)
     mis = mis or [0] * (2 * W)
     g_peer = [Guarded(peers[p].size, mis[p], host=peers[p]) for p in range(W)]
@@ -37,6 +38,9 @@ def _combine_checked(K, peers, S, keys, pos, rb, mis=None, expect=None):
         eng.combine_items([g.view for g in g_peer], d_S, d_key, d_pos, K,
                           [g.view for g in g_out], rb)
         st = eng.status()
+        chain = eng.last_dispatch()
+    if expect_copy is not None:
+        assert chain["copy_kernel"] == expect_copy, chain
     ref = [np.full((m[r] + 2) * rb, SENTINEL, np.uint8) for r in range(W)]
     rc = oracle.default().combine_items(K, peers, S, keys, pos, ref, rb)
     assert st == rc, f"device status {st}, oracle {rc}"
@@ -178,3 +182,42 @@ def test_decode_size_and_host_checks():
         rc = a2av.a2av_combine_items(eng.handle, 1, [0, 0], S2.data_ptr(), [0, 0], [0, 0], [0, 0],
                                      [0, 0], 8, ws.data_ptr(), ws.numel())
         assert rc == a2av.ERR_INVALID_ARG  # workspace too small
+
+
+# The combine's gather by ring shape (many items: the check kernel, then the
+# cp.async.bulk gather with one bulk store per stage) and its one-kernel
+# path (at most 4096 items: row slots for aligned rows, registers otherwise).
+@pytest.mark.parametrize("rb,m", [(64, 20011), (512, 9001), (1024, 6007), (2048, 6007),
+                                  (4096, 3001), (14336, 1801), (32768, 1801)])
+def test_gather_ring_shapes(rb, m):
+    """(more than 4096 items in all: past the one-kernel path)"""
+    rng = np.random.default_rng(rb + m + 1)
+    W, K = 4, 3
+    counts = [m, m - 17, m // 3, 1]
+    key = [rng.integers(0, W * K, c).astype(np.int32) for c in counts]
+    rows = [rng.integers(0, 256, 50 * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, 50, c).astype(np.int32) for c in counts]
+    outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+    peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
+    assert _combine_checked(K, peers, S, key, pos, rb,
+                            expect_copy="dispatch_gather_kernel") == a2av.OK
+
+
+@pytest.mark.parametrize("rb", [1, 8, 16, 64, 1024, 14336, 40000])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_one_kernel_path(rb, aligned):
+    rng = np.random.default_rng(rb * 5 + aligned)
+    for W, K, total in ((8, 8, 2048), (3, 5, 40), (32, 2, 4096), (1, 1, 900)):
+        if rb * total > (64 << 20):
+            total = (64 << 20) // rb
+        share = rng.dirichlet(np.ones(W)) * total
+        m = [int(x) for x in share]
+        m[0] += total - sum(m)
+        rows = [rng.integers(0, 256, 30 * rb, dtype=np.uint8) for _ in range(W)]
+        src = [rng.integers(0, 30, m[r]).astype(np.int32) for r in range(W)]
+        key = [rng.integers(0, W * K, m[r]).astype(np.int32) for r in range(W)]
+        outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+        peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
+        mis = None if aligned else [int(rng.integers(1, 16)) for _ in range(2 * W)]
+        assert _combine_checked(K, peers, S, key, pos, rb, mis,
+                                expect_copy="combine_tiny_kernel") == a2av.OK

@@ -80,14 +80,17 @@ def test_aligned_row_sizes(rb):
 
 @pytest.mark.parametrize("rb", [2048, 9216, 20480])
 def test_few_items_past_the_one_kernel_size(rb):
-    """More keys than the one-kernel path takes (W*K > 256) but only a few
-    thousand items: the gather's rings for few items per CTA."""
+    """More keys than the one-kernel-per-rank count takes (W*K > 256) and
+    more items than the one-kernel path takes, but only a few thousand: the
+    count kernel, the scan kernel (400 keys: more than one block thread a
+    key), then the gather in batches of 8 items."""
     rng = np.random.default_rng(rb + 5)
     W, K, n, m = 2, 200, 64, 3000
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
     src = [rng.integers(0, n, m).astype(np.int32) for _ in range(W)]
     key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
-    dispatch_checked(K, rows, src, key, rb)
+    dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_gather_kernel",
+                     expect_kernels=3)
 
 
 def test_dispatch_without_items():
@@ -107,20 +110,93 @@ def test_dispatch_without_items_many_keys(W, K):
 
 
 @pytest.mark.parametrize("rb", [16, 64])
-@pytest.mark.parametrize("W,K,m", [
-    (8, 8, 32768),    # 16 groups of 2048 items over 64 keys: the count kernel scans
-    (8, 8, 32769),    # 17 groups: the scan kernel
-    (2, 13, 73728),   # 36 groups over 26 keys: the count kernel scans
-    (2, 13, 73729),   # 37 groups: the scan kernel
+@pytest.mark.parametrize("W,K,m,kernels", [
+    (2, 128, 65536, 2),   # 32 groups of 2048 items over 256 keys: the count kernel scans
+    (2, 128, 65537, 3),   # 33 groups: the scan kernel
+    (8, 32, 65536, 2),    # the same limit with eight ranks
+    (8, 32, 65537, 3),
 ])
-def test_group_scan_either_side_of_the_fused_limit(W, K, m, rb):
+def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb):
+    """The count kernel's last block per rank scans the group counts when a
+    thread's share of one key is at most 32 groups (256 keys: one thread a
+    key); one group more and the scan kernel runs."""
     rng = np.random.default_rng(m + rb)
     n = 500
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
     counts = [m] + [int(rng.integers(2049, m + 1)) for _ in range(W - 2)] + [0]
     src = [rng.integers(0, n, c).astype(np.int32) for c in counts]
     key = [np.minimum(rng.geometric(0.05, c) - 1, W * K - 1).astype(np.int32) for c in counts]
-    dispatch_checked(K, rows, src, key, rb)
+    dispatch_checked(K, rows, src, key, rb, expect_kernels=kernels,
+                     expect_copy="dispatch_place_copy_kernel" if rb < 64 else
+                     "dispatch_gather_kernel")
+
+
+@pytest.mark.parametrize("rb", [8, 64])
+@pytest.mark.parametrize("W,K,kernels", [(2, 13, 2), (2, 200, 3)])
+def test_four_ranges_a_count_warp(W, K, kernels, rb):
+    """Batches so large that even with four ranges a warp every SM gets a
+    count block (640 K items a rank, the embedding-key size): 32-range
+    groups, scanned by the count kernel's last block (26 keys) or by the
+    scan kernel (400 keys, more than one block thread a key)."""
+    rng = np.random.default_rng(K + rb)
+    m, n = 640_000, 4000
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, n, m - 1000 * r).astype(np.int32) for r in range(W)]
+    key = [rng.integers(0, W * K, m - 1000 * r).astype(np.int32) for r in range(W)]
+    dispatch_checked(K, rows, src, key, rb, expect_kernels=kernels,
+                     expect_copy="dispatch_place_copy_kernel" if rb < 64 else
+                     "dispatch_gather_kernel")
+
+
+# Aligned rows by the gather's ring shapes (row-size classes up to 256 B,
+# 512 B, 1, 2, 4, 8, 16 and 32 KiB), with item counts that give 32-, 16- and
+# 8-item batches and ragged last batches per rank.
+@pytest.mark.parametrize("rb,m", [(64, 20011), (256, 20011), (272, 9001), (512, 9001),
+                                  (1024, 6007), (2048, 6007), (4096, 3001), (8192, 1801),
+                                  (14336, 1801), (16384, 1801), (32768, 1801)])
+def test_gather_ring_shapes(rb, m):
+    """(more than 4096 items in all: past the one-kernel path)"""
+    rng = np.random.default_rng(rb + m)
+    W, K, n = 4, 3, 97
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    counts = [m, m - 17, m // 3, 1]
+    src = [rng.integers(0, n, c).astype(np.int32) for c in counts]
+    key = [rng.integers(0, W * K, c).astype(np.int32) for c in counts]
+    dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_gather_kernel")
+
+
+# The one-kernel path (at most 4096 items over all ranks): row slots through
+# cp.async.bulk for aligned rows of 64 B .. 176 KiB, register copies for the
+# rest (misaligned buffers, short rows, rows too long for the slots); one
+# item per block when there are fewer items than SMs; 4096 items exactly,
+# and 4097 (past it).
+@pytest.mark.parametrize("rb", [1, 8, 13, 16, 64, 80, 1024, 14336, 40000, 200000])
+@pytest.mark.parametrize("mis", [False, True])
+def test_one_kernel_path(rb, mis):
+    rng = np.random.default_rng(rb * 3 + mis)
+    for W, K, total in ((8, 8, 2048), (3, 5, 50), (32, 2, 4096), (1, 1, 700), (5, 40, 1500)):
+        if rb * total > (64 << 20):
+            total = (64 << 20) // rb
+        share = rng.dirichlet(np.ones(W)) * total
+        m = [int(x) for x in share]
+        m[0] += total - sum(m)
+        n = [int(rng.integers(1, 60)) for _ in range(W)]
+        rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+        src = [rng.integers(0, n[r], m[r]).astype(np.int32) for r in range(W)]
+        key = [np.minimum(rng.geometric(0.1, m[r]) - 1, W * K - 1).astype(np.int32)
+               for r in range(W)]
+        mis_r = [int(rng.integers(1, 16)) for _ in range(W)] if mis else None
+        dispatch_checked(K, rows, src, key, rb, rows_mis=mis_r,
+                         out_mis=mis_r[::-1] if mis else None,
+                         expect_copy="dispatch_tiny_kernel", expect_kernels=1)
+    # one past the one-kernel size
+    W, K = 2, 3
+    rows = [rng.integers(0, 256, 40 * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, 40, c).astype(np.int32) for c in (2049, 2048)]
+    key = [rng.integers(0, W * K, c).astype(np.int32) for c in (2049, 2048)]
+    with a2av.A2av(W) as eng:
+        dispatch_checked(K, rows, src, key, rb, engine=eng)
+        assert eng.last_dispatch()["copy_kernel"] != "dispatch_tiny_kernel"
 
 
 def test_dispatch_then_combine_restores_key_order():

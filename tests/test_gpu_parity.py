@@ -242,3 +242,82 @@ def test_pinned_host_buffers_zero_copy():
                 assert np.array_equal(outs[p].numpy(), ref[p])
                 assert np.array_equal(d_outs[p].cpu().numpy(), ref[p])
             assert np.array_equal(so.cpu().numpy(), ref_so)
+
+
+@pytest.mark.parametrize("requested", [a2av.PATH_AUTO, a2av.PATH_BULK, a2av.PATH_STAGED])
+def test_library_routes_host_buffers_to_the_vector_engine(requested):
+    """Through the raw C ABI (no binding logic): whatever engine the handle
+    asks for, a call with a pinned host buffer runs the vector engine (plain
+    loads and stores reach host memory; cp.async.bulk is kept to device
+    memory), and the next all-device call gets the requested engine back."""
+    import oracle
+    w = wl.cfg1(3)
+    W, rb = w.W, w.row_bytes
+    ref, ref_so = oracle.default().exchange(w.inputs, w.splits, rb)
+    S = torch.from_numpy(w.splits).cuda()
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    host_in = [torch.from_numpy(b).pin_memory() for b in w.inputs]
+    dev_in = [t.cuda() for t in host_in]
+    outs = [torch.full((r.size,), 0xEE, dtype=torch.uint8, device="cuda") for r in ref]
+    rc, h = a2av.a2av_create(W)
+    assert rc == a2av.OK
+    try:
+        assert a2av.a2av_set_path(h, requested) == a2av.OK
+        stream = torch.cuda.current_stream().cuda_stream
+        ptrs = lambda ts: [t.data_ptr() for t in ts]  # noqa: E731
+        mixed = [host_in[0]] + dev_in[1:]  # one host buffer is enough
+        assert a2av.a2av_run(h, ptrs(mixed), S.data_ptr(), ptrs(outs), so.data_ptr(), rb,
+                             stream) == a2av.OK
+        assert a2av.a2av_status(h, stream) == (a2av.OK, a2av.OK)
+        assert a2av.a2av_last_launch(h)[1] == a2av.PATH_VECTOR
+        for p in range(W):
+            assert np.array_equal(outs[p].cpu().numpy(), ref[p])
+        assert np.array_equal(so.cpu().numpy(), ref_so)
+        assert a2av.a2av_run(h, ptrs(dev_in), S.data_ptr(), ptrs(outs), so.data_ptr(), rb,
+                             stream) == a2av.OK
+        assert a2av.a2av_status(h, stream) == (a2av.OK, a2av.OK)
+        want = a2av.PATH_BULK if requested in (a2av.PATH_AUTO, a2av.PATH_BULK) else requested
+        assert a2av.a2av_last_launch(h)[1] == want
+        for p in range(W):
+            assert np.array_equal(outs[p].cpu().numpy(), ref[p])
+    finally:
+        a2av.a2av_destroy(h)
+
+
+def test_dispatch_on_host_rows_uses_plain_loads():
+    """The fused dispatch through the raw C ABI with the source rows in
+    pinned host memory: the library copies them with plain loads and stores
+    (no cp.async.bulk), and the result equals the oracle's."""
+    import oracle
+    w = wl.cfg3(4, tokens=96, hidden=512)
+    K, rows, src, key = wl.dispatch_items(w)
+    W, rb = w.W, w.row_bytes
+    ref, ref_so, ref_pos, ref_S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+    h_rows = [torch.from_numpy(r).pin_memory() for r in rows]
+    d_src = [torch.from_numpy(s).cuda() for s in src]
+    d_key = [torch.from_numpy(k).cuda() for k in key]
+    d_pos = [torch.full((k.size,), -1, dtype=torch.int64, device="cuda") for k in key]
+    d_out = [torch.full((r.size,), 0xEE, dtype=torch.uint8, device="cuda") for r in ref]
+    so = torch.full((W, 2, W), -7, dtype=torch.int64, device="cuda")
+    isp = torch.full((W, W), -7, dtype=torch.int64, device="cuda")
+    m = [k.size for k in key]
+    nbytes = a2av.a2av_dispatch_workspace_bytes(W, K, max(m))
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    rc, h = a2av.a2av_create(W)
+    assert rc == a2av.OK
+    try:
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = a2av.a2av_dispatch(h, K, [t.data_ptr() for t in h_rows], [r.size // rb for r in rows],
+                                [t.data_ptr() for t in d_src], [t.data_ptr() for t in d_key], m,
+                                [t.data_ptr() for t in d_out], so.data_ptr(),
+                                [t.data_ptr() for t in d_pos], isp.data_ptr(), rb, ws.data_ptr(),
+                                nbytes, stream)
+        assert rc == a2av.OK
+        assert a2av.a2av_status(h, stream) == (a2av.OK, a2av.OK)
+    finally:
+        a2av.a2av_destroy(h)
+    assert np.array_equal(so.cpu().numpy(), ref_so) and np.array_equal(isp.cpu().numpy(), ref_S)
+    for r in range(W):
+        assert np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r])
+    for p in range(W):
+        assert np.array_equal(d_out[p].cpu().numpy(), ref[p])

@@ -5,9 +5,10 @@ at start-up, hosts that own the only allocator, latency paths that cannot
 afford an allocation's device synchronisation.  For them the library offers
 a2av_run_noalloc, which takes no handle and keeps its status word in a small
 array compiled into the library.  These tests check that it produces exactly
-what the handle-based a2av_run produces -- every output byte and
-out_splits_offsets -- on two calls in a row, that each call starts from a
-cleared status word, and that it rejects a rank count beyond its limit.
+what the handle-based a2av_run produces, and what the CPU oracle produces --
+every output byte and out_splits_offsets -- on two calls in a row, that each
+call starts from a cleared status word, and that it rejects a rank count
+beyond its limit.
 
 This file is collected last on purpose, so that a failure here stops a
 ``-x`` run only after every other test has run.
@@ -16,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -48,11 +50,13 @@ def _ptrs(ts):
     return [t.data_ptr() if t.numel() else 0 for t in ts]
 
 
-def _with_handle(w, ins, S, recv):
+def _with_handle(w, ins, S, recv, engine=None):
     outs, so = _fresh_outputs(recv, w.W)
     with a2av.A2av(w.W) as eng:
         eng.run(ins, S, outs, so, w.row_bytes)
         assert eng.status() == a2av.OK
+        if engine is not None:
+            assert eng.last_launch()["path"] == engine
     return outs, so
 
 
@@ -67,17 +71,27 @@ def _without_alloc(w, ins, S, recv):
 
 
 def test_noalloc_matches_a2av_run_on_two_calls_in_a_row():
-    # an aligned exchange (bulk engine) then a 13-byte-row one (vector engine)
-    cases = [wl.cfg1(0), wl.cfg4(2, rows=1 << 15)]
-    for w in cases:
+    # an aligned exchange, then one of 13-byte rows: the engine AUTO picks,
+    # which is the bulk engine for the first and the staged engine for the
+    # second (a2av_run on a handle reports it; the call without a handle
+    # chooses the same way)
+    cases = [(wl.cfg1(0), a2av.PATH_BULK), (wl.cfg4(2, rows=1 << 15), a2av.PATH_STAGED)]
+    for w, engine in cases:
         ins, S, recv = _device_case(w)
-        ref_outs, ref_so = _with_handle(w, ins, S, recv)
+        ref_outs, ref_so = _with_handle(w, ins, S, recv, engine)
         got_outs, got_so = _without_alloc(w, ins, S, recv)
         torch.cuda.synchronize()
-        # the same bar as every other test of this library: bit-exact
+        # the same bar as every other test of this library: bit-exact, against
+        # the handle-based entry point and against the CPU oracle
         assert torch.equal(got_so, ref_so)
         for g, r in zip(got_outs, ref_outs):
             assert torch.equal(g, r)
+        want, want_so = oracle.default().exchange(w.inputs, w.splits, w.row_bytes)
+        assert np.array_equal(got_so.cpu().numpy(), want_so)
+        for p, g in enumerate(got_outs):
+            n = want[p].size
+            got = g.cpu().numpy()
+            assert np.array_equal(got[:n], want[p]) and np.all(got[n:] == 0xEE)
 
 
 def test_each_call_starts_from_a_cleared_status_word():

@@ -17,7 +17,7 @@ from ._build import LIBRARY, build
 __all__ = [
     "A2av", "A2avError", "load", "build",
     "a2av_create", "a2av_run", "a2av_combine", "a2av_status", "a2av_destroy", "a2av_set_path",
-    "a2av_set_grid", "a2av_last_launch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
+    "a2av_set_grid", "a2av_last_launch", "a2av_last_dispatch", "a2av_error_string", "a2av_version", "a2av_run_noalloc",
     "a2av_dispatch", "a2av_dispatch_workspace_bytes", "ERR_BAD_INDEX", "MAX_DISPATCH_KEYS",
     "a2av_run_multi", "A2avExchange", "MAX_EXCHANGES", "BoundCall", "a2av_combine_items",
     "COMBINE_WORKSPACE_BYTES",
@@ -73,6 +73,8 @@ def load():
     lib.a2av_last_launch.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci),
                                      ctypes.POINTER(ci)]
     lib.a2av_run_noalloc.argtypes = [ci, i64, i64, pp, vp, pp, vp, i64, vp, ctypes.POINTER(ci)]
+    lib.a2av_last_dispatch.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci),
+                                       ctypes.POINTER(ctypes.c_char_p)]
     i64p = ctypes.POINTER(i64)
     lib.a2av_dispatch_workspace_bytes.argtypes = [ci, ci, i64]
     lib.a2av_dispatch_workspace_bytes.restype = i64
@@ -186,6 +188,14 @@ def a2av_last_launch(handle):
     p, g, b = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     rc = load().a2av_last_launch(handle, ctypes.byref(p), ctypes.byref(g), ctypes.byref(b))
     return rc, p.value, g.value, b.value
+
+
+def a2av_last_dispatch(handle):
+    """Returns (status, kernels, memsets, copy_kernel) of the handle's last
+    a2av_dispatch or a2av_combine_items."""
+    k, m, name = ctypes.c_int(), ctypes.c_int(), ctypes.c_char_p()
+    rc = load().a2av_last_dispatch(handle, ctypes.byref(k), ctypes.byref(m), ctypes.byref(name))
+    return rc, k.value, m.value, (name.value or b"").decode()
 
 
 def a2av_run_noalloc(world_size: int, in_capacity_rows: int, out_capacity_rows: int, in_ptrs,
@@ -329,30 +339,19 @@ class A2av:
 
     def _launch(self, fn, what, inputs, splits, outputs, out_splits_offsets, row_bytes, stream,
                 split_shape):
-        args, host = self._launch_args(inputs, splits, outputs, out_splits_offsets, row_bytes,
-                                       stream, split_shape)
-        lib = load()
-        if host:
-            # Buffers in pinned host memory are reached with plain loads and
-            # stores (zero-copy over the host link): the vector engine.
-            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
-            try:
-                rc = fn(*args)
-            finally:
-                lib.a2av_set_path(self.handle, self._path)
-        else:
-            rc = fn(*args)
-        self._check(rc, what)
+        # (buffers in pinned host memory are routed to the vector engine by
+        # the library itself)
+        args, _ = self._launch_args(inputs, splits, outputs, out_splits_offsets, row_bytes,
+                                    stream, split_shape)
+        self._check(fn(*args), what)
 
     def bind_run(self, inputs, in_splits, outputs, out_splits_offsets, row_bytes: int,
                  stream=None) -> BoundCall:
         """``run`` marshalled once: returns a BoundCall that re-enqueues the
-        exchange on these device buffers (pinned host buffers: use ``run``)."""
+        exchange on these buffers."""
         W = self.world_size
-        args, host = self._launch_args(inputs, in_splits, outputs, out_splits_offsets, row_bytes,
-                                       stream, (W, W))
-        if host:
-            raise ValueError("bind_run takes device buffers only")
+        args, _ = self._launch_args(inputs, in_splits, outputs, out_splits_offsets, row_bytes,
+                                    stream, (W, W))
         keep = (inputs, in_splits, outputs, out_splits_offsets)
         return BoundCall(self, load().a2av_run, "a2av_run", args, len(args) - 1, keep)
 
@@ -366,17 +365,8 @@ class A2av:
         include/a2av.h, a2av_run_multi).  ``exchanges``: a sequence of
         (inputs, in_splits, outputs, out_splits_offsets, row_bytes), each as
         for ``run``."""
-        args, host, _ = self._multi_args(exchanges, stream)
-        lib = load()
-        if host:  # pinned host buffers: the vector engine (plain loads and stores)
-            self._check(lib.a2av_set_path(self.handle, PATH_VECTOR), "a2av_set_path")
-            try:
-                rc = lib.a2av_run_multi(*args)
-            finally:
-                lib.a2av_set_path(self.handle, self._path)
-        else:
-            rc = lib.a2av_run_multi(*args)
-        self._check(rc, "a2av_run_multi")
+        args, _, _ = self._multi_args(exchanges, stream)
+        self._check(load().a2av_run_multi(*args), "a2av_run_multi")
 
     def _multi_args(self, exchanges, stream):
         W = self.world_size
@@ -398,10 +388,8 @@ class A2av:
         return [self.handle, len(exchanges), arr, st], host, keep
 
     def bind_run_multi(self, exchanges, stream=None) -> BoundCall:
-        """``run_multi`` marshalled once (device buffers only)."""
-        args, host, keep = self._multi_args(exchanges, stream)
-        if host:
-            raise ValueError("bind_run_multi takes device buffers only")
+        """``run_multi`` marshalled once."""
+        args, _, keep = self._multi_args(exchanges, stream)
         return BoundCall(self, load().a2av_run_multi, "a2av_run_multi", args, 3,
                          keep + [exchanges])
 
@@ -542,6 +530,12 @@ class A2av:
         rc, p, g, b = a2av_last_launch(self.handle)
         self._check(rc, "a2av_last_launch")
         return {"path": p, "grid": g, "block": b}
+
+    def last_dispatch(self):
+        """What the last ``dispatch`` or ``combine_items`` enqueued."""
+        rc, k, m, name = a2av_last_dispatch(self.handle)
+        self._check(rc, "a2av_last_dispatch")
+        return {"kernels": k, "memsets": m, "copy_kernel": name}
 
     def close(self):
         if self.handle is not None:

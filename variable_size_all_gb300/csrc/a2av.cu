@@ -332,6 +332,8 @@ __device__ __forceinline__ void staged_engine(const Params& P, int stage_bytes, 
   __shared__ StageDesc desc[NS];
   __shared__ alignas(8) unsigned long long full[NS];
   __shared__ alignas(8) unsigned long long empty[NS];
+  __shared__ long long produced;     // tiles whose loads the producer issued
+  __shared__ long long consumed[NC];  // tiles each consumer warp finished
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, stage_bytes, cta, ctas)) return;
 
@@ -352,7 +354,8 @@ __device__ __forceinline__ void staged_engine(const Params& P, int stage_bytes, 
 
   if (warp == 0) {
     // Producer: one tile per iteration, lane r loading source r's granules.
-    for (long long k = 0; k < nk; ++k) {
+    long long k = 0;
+    for (; k < nk; ++k) {
       const int s = (int)(k % NS);
       if (k >= NS && !mbar_wait_warp(empty0 + 8 * s, (unsigned)((k / NS - 1) & 1))) {
         if (lane == 0) record_error(P.status, A2AV_ERR_TIMEOUT);
@@ -391,25 +394,40 @@ __device__ __forceinline__ void staged_engine(const Params& P, int stage_bytes, 
       __syncwarp();
       if (n > 0) bulk_load(stage0 + (uint32_t)s * alloc + off, (const void*)g_lo, gb, bar);
     }
-    return;
-  }
-
-  // Consumers: rebuild each tile from its stage with destination-aligned stores.
-  const int ct = threadIdx.x - 32;
-  for (long long k = 0; k < nk; ++k) {
-    const int s = (int)(k % NS);
-    if (!mbar_wait_warp(full0 + 8 * s, (unsigned)((k / NS) & 1))) {
-      if (lane == 0) record_error(P.status, A2AV_ERR_TIMEOUT);
-      break;
+    if (lane == 0) produced = k;
+  } else {
+    // Consumers: rebuild each tile from its stage with destination-aligned stores.
+    const int ct = threadIdx.x - 32;
+    long long k = 0;
+    for (; k < nk; ++k) {
+      const int s = (int)(k % NS);
+      if (!mbar_wait_warp(full0 + 8 * s, (unsigned)((k / NS) & 1))) {
+        if (lane == 0) record_error(P.status, A2AV_ERR_TIMEOUT);
+        break;
+      }
+      const StageDesc& d = desc[s];
+      const int count = d.count;
+      unsigned char* dst = d.dst;
+      const uint32_t stage = stage0 + (uint32_t)s * alloc;
+      for (int i = 0; i < count; ++i)
+        copy_span_smem<32 * NC>(dst + d.seg_dst[i], stage + (uint32_t)d.seg_src[i], d.seg_len[i],
+                                ct);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    const StageDesc& d = desc[s];
-    const int count = d.count;
-    unsigned char* dst = d.dst;
-    const uint32_t stage = stage0 + (uint32_t)s * alloc;
-    for (int i = 0; i < count; ++i)
-      copy_span_smem<32 * NC>(dst + d.seg_dst[i], stage + (uint32_t)d.seg_src[i], d.seg_len[i], ct);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (lane == 0) consumed[warp - 1] = k;
+  }
+  // After a timeout some issued loads may not have been waited for: before
+  // the CTA leaves (and its shared memory is reused), wait -- bounded -- for
+  // every tile the producer issued that some consumer did not finish.  The
+  // producer never runs more than NS tiles ahead, so these tiles sit in
+  // distinct stages and their phases are the ones the consumers waited on.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long lo = produced;
+    for (int c = 0; c < NC; ++c) lo = consumed[c] < lo ? consumed[c] : lo;
+    for (long long k = lo; k < produced; ++k)
+      mbar_wait(full0 + 8 * (int)(k % NS), (unsigned)((k / NS) & 1));
   }
 }
 
@@ -568,11 +586,28 @@ bool fill_params(Params* P, int W, const void* const* in_ptrs, const int64_t* in
   return aligned;
 }
 
-// Engine actually used for a request: BULK needs full alignment (else STAGED);
-// AUTO is BULK when aligned, STAGED otherwise.
-int resolve_path(int requested, bool aligned) {
-  if (requested == A2AV_PATH_VECTOR || requested == A2AV_PATH_STAGED) return requested;
+// Engine actually used for a request: buffers that are not all device memory
+// take the vector engine (plain loads and stores reach host memory; the
+// cp.async.bulk engines are kept to device memory); BULK needs full
+// alignment (else STAGED); AUTO is BULK when aligned, STAGED otherwise.
+int resolve_path(int requested, bool aligned, bool device_memory) {
+  if (!device_memory || requested == A2AV_PATH_VECTOR) return A2AV_PATH_VECTOR;
+  if (requested == A2AV_PATH_STAGED) return requested;
   return aligned ? A2AV_PATH_BULK : A2AV_PATH_STAGED;
+}
+
+bool classify(const void* const* a, int na, const void* const* b, int nb) {
+  for (int k = 0; k < na + nb; ++k) {
+    const void* p = k < na ? a[k] : b[k - na];
+    if (p == nullptr) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();  // (not sticky) -- an unknown pointer is not device memory
+      return false;
+    }
+    if (at.type != cudaMemoryTypeDevice) return false;
+  }
+  return true;
 }
 
 // One launch of the chosen engine.  With `pdl` the launch may overlap the
@@ -600,9 +635,31 @@ int launch(const Params& P, int path, int ctas_per_sm, int sms, cudaStream_t s, 
 
 }  // namespace
 
+bool a2av_device_buffers(a2av_handle* h, const void* const* a, int na, const void* const* b,
+                         int nb) {
+  const int n = na + nb;
+  if (h == nullptr || n > 2 * kMaxExchanges * kMaxW) return classify(a, na, b, nb);
+  ++h->cache_clock;
+  for (a2av_ptr_cache& c : h->cache) {
+    if (c.n != n) continue;
+    bool same = true;
+    for (int k = 0; k < n && same; ++k) same = c.ptrs[k] == (k < na ? a[k] : b[k - na]);
+    if (same) {
+      c.stamp = h->cache_clock;
+      return c.device;
+    }
+  }
+  a2av_ptr_cache& c = h->cache[0].stamp <= h->cache[1].stamp ? h->cache[0] : h->cache[1];
+  c.device = classify(a, na, b, nb);
+  for (int k = 0; k < n; ++k) c.ptrs[k] = k < na ? a[k] : b[k - na];
+  c.n = n;
+  c.stamp = h->cache_clock;
+  return c.device;
+}
+
 extern "C" {
 
-int a2av_version(void) { return 10100; }
+int a2av_version(void) { return 10200; }
 
 const char* a2av_error_string(int code) {
   switch (code) {
@@ -612,6 +669,8 @@ const char* a2av_error_string(int code) {
     case A2AV_ERR_CUDA: return "CUDA runtime error";
     case A2AV_ERR_BAD_SPLITS: return "invalid split matrix (detected on the device)";
     case A2AV_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case A2AV_ERR_BAD_INDEX:
+      return "a dispatch key, source row or combine position is out of range (detected on the device)";
     default: return "unknown status";
   }
 }
@@ -652,6 +711,11 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   h->pdl = env_int("A2AV_PDL", 1) != 0;
   h->gather_ready = false;
   h->last_path = h->last_grid = h->last_block = 0;
+  h->last_kernels = h->last_memsets = 0;
+  h->last_copy = "";
+  h->cache[0].n = h->cache[1].n = 0;
+  h->cache[0].stamp = h->cache[1].stamp = 0;
+  h->cache_clock = 0;
   *out = h;
   return A2AV_OK;
 }
@@ -659,12 +723,14 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
 int a2av_set_path(a2av_handle* h, int path) {
   if (h == nullptr || path < A2AV_PATH_AUTO || path > A2AV_PATH_STAGED) return A2AV_ERR_INVALID_ARG;
   h->path = path;
+  h->cache[0].n = h->cache[1].n = 0;  // the pointers are looked at afresh
   return A2AV_OK;
 }
 
 int a2av_set_grid(a2av_handle* h, int ctas_per_sm) {
   if (h == nullptr || ctas_per_sm < 0 || ctas_per_sm > 32) return A2AV_ERR_INVALID_ARG;
   h->ctas_per_sm = ctas_per_sm;
+  h->cache[0].n = h->cache[1].n = 0;
   return A2AV_OK;
 }
 
@@ -697,7 +763,8 @@ int run_exchange(a2av_handle* h, const void* const* in_ptrs, const int64_t* in_s
   const bool aligned = fill_params(&P, h->W, in_ptrs, in_splits_dev, out_ptrs,
                                    out_splits_offsets_dev, row_bytes, h->in_cap, h->out_cap,
                                    h->d_status, split_stride, h->starve);
-  const int path = resolve_path(h->path, aligned);
+  const bool device_memory = a2av_device_buffers(h, in_ptrs, h->W, out_ptrs, h->W);
+  const int path = resolve_path(h->path, aligned, device_memory);
   int grid = 0, block = 0;
   const int rc = launch(P, path, h->ctas_per_sm, h->sms, static_cast<cudaStream_t>(stream),
                         h->pdl, &grid, &block);
@@ -741,6 +808,8 @@ int a2av_run_multi(a2av_handle* h, int count, const a2av_exchange_t* exchanges, 
   std::memset(&M, 0, sizeof(M));
   M.count = count;
   bool aligned = true;
+  const void* bufs[2 * kMaxExchanges * kMaxW];  // every buffer of the call, classified at once
+  int nbufs = 0;
   for (int x = 0; x < count; ++x) {
     const a2av_exchange_t& e = exchanges[x];
     if (e.in_ptrs == nullptr || e.out_ptrs == nullptr || e.in_splits_dev == nullptr ||
@@ -752,9 +821,14 @@ int a2av_run_multi(a2av_handle* h, int count, const a2av_exchange_t* exchanges, 
                           e.out_splits_offsets_dev, e.row_bytes, h->in_cap, h->out_cap,
                           h->d_status, h->W, h->starve) &&
               aligned;
+    for (int r = 0; r < h->W; ++r) {
+      bufs[nbufs++] = e.in_ptrs[r];
+      bufs[nbufs++] = e.out_ptrs[r];
+    }
   }
+  const bool device_memory = a2av_device_buffers(h, bufs, nbufs, nullptr, 0);
   // One engine for the launch: bulk only when every exchange allows it.
-  const int path = resolve_path(h->path, aligned);
+  const int path = resolve_path(h->path, aligned, device_memory);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int grid, block;
   cudaError_t err;
@@ -862,7 +936,10 @@ extern "C" int a2av_run_noalloc(int world_size, int64_t in_capacity_rows,
   // The kernels only ever set the status word, so it must start at zero.
   if (cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return A2AV_ERR_CUDA;
   int grid = 0, block = 0;
-  rc = launch(P, resolve_path(A2AV_PATH_AUTO, aligned), 0, sms, s, true, &grid, &block);
+  const bool device_memory = a2av_device_buffers(nullptr, in_ptrs, world_size, out_ptrs,
+                                                 world_size);
+  rc = launch(P, resolve_path(A2AV_PATH_AUTO, aligned, device_memory), 0, sms, s, true, &grid,
+              &block);
   if (rc != A2AV_OK) return rc;
   if (device_status != nullptr) {
     int value = 0;

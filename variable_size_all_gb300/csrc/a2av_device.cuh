@@ -100,37 +100,16 @@ __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
-// Step 1 of the exchange.  Three barriers: load + range check; column scans
-// (out_off) and row scans (in_off) side by side + capacity checks; tiles and
-// out_splits_offsets.  `ctas` CTAs work on this exchange and this one is
-// number `cta` among them (the whole grid, unless several exchanges share a
-// launch).  Returns false (in every thread of the CTA) when the splits are
-// invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
-__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int cta, int ctas) {
+// Steps 2 and 3 of the plan, once pl.s holds a range-checked split matrix:
+// column scans (out_off) and row scans (in_off) side by side + capacity
+// checks; tiles and out_splits_offsets.  Two barriers.  Returns false (in
+// every thread of the CTA) when a capacity or NULL-buffer rule is broken;
+// CTA 0 then records A2AV_ERR_BAD_SPLITS.
+__device__ bool plan_from_splits(const Params& P, Plan& pl, long long max_tile, int cta, int ctas) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
-
-  // Programmatic dependent launch (both no-ops for a plain launch): let the
-  // next kernel of the stream start launching, then wait until the previous
-  // one has finished and its writes are visible -- it may have produced the
-  // splits or the inputs, and it may still be reading our outputs.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
   int bad = 0;
-  for (int e = tid; e < W * W; e += nt) {
-    const int r = e / W, p = e - r * W;
-    // (L2 loads: the splits may have been written during this very launch
-    // by other CTAs, as in the fused dispatch's scan kernel)
-    const long long s = __ldcg(P.splits + (long long)r * P.split_stride + p);
-    if (s < 0 || s > P.limit) bad = 1;
-    pl.s[r][p] = s;
-  }
-  if (__syncthreads_or(bad)) {
-    if (cta == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
-    return false;
-  }
 
   // Task k < W: column scan of peer k (lane r holds S[r][k]); task W + k: row
   // scan of rank k (lane p holds S[k][p]).  Exclusive prefix = inclusive - own.
@@ -185,6 +164,39 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int ct
   }
   __syncthreads();
   return true;
+}
+
+// Step 1 of the exchange, then the rest of the plan: load the split matrix
+// into shared memory and check its range (one barrier), then
+// plan_from_splits.  `ctas` CTAs work on this exchange and this one is
+// number `cta` among them (the whole grid, unless several exchanges share a
+// launch).  Returns false (in every thread of the CTA) when the splits are
+// invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
+__device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int cta, int ctas) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int W = P.W;
+
+  // Programmatic dependent launch (both no-ops for a plain launch): let the
+  // next kernel of the stream start launching, then wait until the previous
+  // one has finished and its writes are visible -- it may have produced the
+  // splits or the inputs, and it may still be reading our outputs.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  int bad = 0;
+  for (int e = tid; e < W * W; e += nt) {
+    const int r = e / W, p = e - r * W;
+    // (L2 loads: the splits may have been written during this very launch
+    // by other CTAs, as in the fused dispatch's scan kernel)
+    const long long s = __ldcg(P.splits + (long long)r * P.split_stride + p);
+    if (s < 0 || s > P.limit) bad = 1;
+    pl.s[r][p] = s;
+  }
+  if (__syncthreads_or(bad)) {
+    if (cta == 0 && tid == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+    return false;
+  }
+  return plan_from_splits(P, pl, max_tile, cta, ctas);
 }
 
 // The whole grid on one exchange.

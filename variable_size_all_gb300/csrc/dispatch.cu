@@ -1,34 +1,45 @@
 // dispatch.cu -- fused dispatch preparation for the variable-size all-to-all:
 // the exchange of rows that are not yet grouped by destination (declared in
-// include/a2av.h, a2av_dispatch).
+// include/a2av.h, a2av_dispatch), and its return path in item order
+// (a2av_combine_items).
 //
 // Each rank's items carry a key (destination = key / K) and a source row.
 // The exchange runs on the rank's items ordered stably by key -- the input
-// a2av_run would expect -- without ever materialising that order:
-//   1. count  (a warp per range of 256 items, eight per CTA): per range, the
-//      key histogram in shared memory; keys and source rows are validated here.
-//   2. scan   (grid keys x W, 256 threads): per (key, rank), the exclusive
-//      prefix of the key's count over the ranges (in place); the last CTA of
-//      each rank to finish turns the key totals into key start offsets and
-//      the split matrix row S[r][*].
-//   3. rank   (grid ranges x W, one warp): items of a range in order, 32 at a
-//      time; __match_any_sync groups equal keys, a lane's rank among them
-//      plus the running count of its key gives its stable position (kept in
-//      the workspace).
+// a2av_run would expect -- without ever materialising that order.  An item's
+// place in it is
+//     pos = key_start[r][k] + grp[r][c][k] + hist[r][j][k] + inrank[i]
+// for item i of rank r with key k in range j (256 items) of group c (8 or 32
+// ranges): the items of smaller keys, of key k in earlier groups, in earlier
+// ranges of the group, and earlier in the item's own range.
+//   1. count  (eight warps per CTA, one to four ranges each): a warp ranks
+//      its range's items 32 at a time (warp match on the key), which gives
+//      every item its inrank byte and the range's key histogram; keys and
+//      source rows are validated here.  The CTA's histograms give each range
+//      its in-group prefix (hist) and the group its count (grp).  The last
+//      CTA of each rank to finish (an atomic count after a fence) turns the
+//      group counts into prefixes over the groups, the key totals into key
+//      starts and the split matrix row S[r][*].
+//   2. scan   (only when a rank has too many groups for one CTA): the same
+//      per-key scan over groups as a kernel of its own.
 //   When every rank has at most 2048 items and there are at most 256 keys,
-//   one kernel (one CTA per rank, a warp per 256 items) does 1-3 instead.
-//   Rows shorter than 64 bytes (not that small): the rank kernel also does
-//   the exchange's prologue for its own rank (every CTA validates the whole
-//   split matrix, as the a2av prologue does, and derives its rank's row
-//   displacement per peer) and copies every item's row as soon as it knows
-//   its position: rank + copy in one kernel, step 4 below not launched.
-//   4. copy   (grid SMs x 4): build the exchange plan from S (the a2av
-//      prologue, which also checks capacities and NULL buffers), publish the
-//      positions and the split matrix, then gather every item's row straight
-//      into its place in the output of its destination: with cp.async.bulk
-//      through shared memory for 16-byte aligned rows of 2..32 KiB, else 32
-//      rows per warp (flat 16-byte vector runs when aligned) for rows of 64
-//      bytes or more and a thread per row below.
+//   one kernel (one CTA per rank) does 1-2 instead.
+//   3. copy   (the a2av prologue builds the plan from S, which also checks
+//      capacities and NULL buffers; then S is published and every item's row
+//      goes straight to its place in the output of its destination):
+//      - 16-byte aligned rows of 64 bytes .. 32 KiB: the cp.async.bulk
+//        gather -- each warp takes batches of consecutive items, every lane
+//        issuing the copy of its own item's row into its slot of a
+//        shared-memory stage (one mbarrier per stage), then its own bulk
+//        store; the item metadata of the next two batches is loaded while
+//        the current one is copied;
+//      - other rows of 64 bytes or more: a warp per batch of rows (registers);
+//      - rows under 64 bytes: the count kernel's successor places and copies
+//        the rows of a whole range per warp (thread per row).
+// Decode-size batches (at most 4096 items over all ranks) take one kernel
+// instead: every CTA reads all keys, counts them, derives the split matrix
+// and the plan itself (so all CTAs reach the same verdict without any
+// inter-CTA communication), then places and copies its own share of the
+// items -- no workspace, no memset, one launch.
 // Invalid keys or source rows set a workspace flag (cleared first) that stops
 // every later kernel; invalid splits stop the copy kernel in its prologue.
 // Either way nothing the caller owns is written.
@@ -59,37 +70,33 @@ constexpr int kItemsPerThread = 4;      // items a thread copies at once (short 
 #define A2AV_COPY_VEC_ROWS 4
 #endif
 constexpr int kVecRows = A2AV_COPY_VEC_ROWS;  // 16-byte vectors a lane keeps in flight (warp rows)
-// The combine's aligned warp rows: twice the vectors in flight at two CTAs an
-// SM (123 registers, no spill).  Measured on MoE rows of 512 B and 1 KiB: the
-// combine 5-9 % faster than at 4 vectors and three CTAs; the dispatch, which
-// reads each token's row once for its two experts, no faster; rows that need
-// realigning 7-20 % slower at two CTAs.
-constexpr int kVecRowsWide = 8;
-constexpr int kCopyCtasPerSmWide = 2;
 constexpr long long kVecMaxRow = 64 * 1024;  // flat vector runs up to this row size
 
 struct DispatchParams {
   const int* key[kMaxW];
   const int* src[kMaxW];
   long long* sorted_pos[kMaxW];
-  long long items[kMaxW];           // m_r
-  long long rows[kMaxW];            // source rows per rank
-  long long item_first[kMaxW + 1];  // exclusive prefix of m_r
-  int* flag;                        // workspace: set once input is found invalid
-  int* done;                        // workspace: [W] CTAs finished per rank (the one that scans)
-  long long* S;                     // workspace: [W][W]
-  long long* key_start;             // workspace: [W][NB]
-  long long* key_total;             // workspace: [W][NB]
-  int* hist;                        // workspace: [W][ranges_max][NB]
-  int* grp;                         // workspace: [W][groups_max][NB]
-  int* pos;                         // workspace: [W][pos_stride] item positions in key order
+  long long items[kMaxW];            // m_r
+  long long rows[kMaxW];             // source rows per rank
+  long long item_first[kMaxW + 1];   // exclusive prefix of m_r
+  long long batch_first[kMaxW + 1];  // exclusive prefix of ceil(m_r / bs) (gather)
+  int* flag;                         // workspace: set once input is found invalid
+  int* done;                         // workspace: [W] CTAs finished per rank (the one that scans)
+  long long* S;                      // workspace: [W][W]
+  long long* key_start;              // workspace: [W][NB]
+  long long* key_total;              // workspace: [W][NB]
+  int* hist;                         // workspace: [W][ranges_max][NB]
+  int* grp;                          // workspace: [W][groups_max][NB]
+  unsigned char* inrank;             // workspace: [W][pos_stride] rank within the item's range
   int* status;
-  long long* in_splits_out;         // optional [W][W]
-  int vec16;                        // every row and buffer 16-byte aligned
-  int combine;                      // the fused combine: rows move the other way (below)
+  long long* in_splits_out;          // optional [W][W]
+  int vec16;                         // every row and buffer 16-byte aligned
+  int combine;                       // the fused combine: rows move the other way (below)
   long long ranges_max;
-  long long groups_max;             // ranges_max / kCountWarps, rounded up
-  int fuse_scan;                    // the count kernel's last CTA per rank scans the groups
+  long long groups_max;
+  int group_log2;                    // a group is 1 << group_log2 ranges (8 or 32)
+  int fuse_scan;                     // the count kernel's last CTA per rank scans the groups
+  int bs;                            // items per gather batch (8, 16 or 32)
   long long pos_stride;
   int W, K;
 };
@@ -111,6 +118,10 @@ __device__ __forceinline__ bool flagged(const DispatchParams& D) {
 __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
   atomicExch(D.flag, 1);
   record_error(D.status, code);
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 // Block-wide exclusive scan of one value per thread (kScanThreads threads);
@@ -152,43 +163,39 @@ __device__ __forceinline__ void finish_rank(const DispatchParams& D, int r, cons
   }
 }
 
-// Items are counted in ranges of kRange, ranges in groups of kCountWarps (a
-// count CTA).  After the count kernel, hist[r][j][b] holds the items with key
-// b in the earlier ranges of range j's group, and grp[r][c][b] the group's
-// count; the scan (below) turns grp[r][*][b] into exclusive prefixes over the
-// groups, so that an item's place among the equal keys of its rank is
-// key_start[b] + grp[c][b] + hist[j][b] + its rank within the range.
-//
-// A warp per range of 256 items (8 per lane, all loads issued together),
-// eight ranges per CTA, registers capped for six CTAs an SM so that 7296
-// ranges (1.8 M items) are resident in one wave; each warp counts its keys in
-// its own slice of shared memory (dynamic: 8 x W*K ints).  With D.fuse_scan
-// (at most kFuseScanPer groups per thread and key) the last count CTA of each
-// rank to finish does the scan itself and the scan kernel is not launched:
-// one launch and one kernel boundary fewer (MoE dispatch of 8192 tokens).
+// Items are counted in ranges of kRange, ranges in groups of 8 * RW (a count
+// CTA: eight warps of RW ranges each).  After the count kernel, hist[r][j][b]
+// holds the items with key b in the earlier ranges of range j's group and
+// grp[r][c][b] the group's count; the scan (below) turns grp[r][*][b] into
+// exclusive prefixes over the groups.
 constexpr int kCountWarps = 8;
-constexpr int kGroupItems = kCountWarps * kRange;  // 2048
-constexpr int kFuseScanPer = 4;                    // groups a thread scans in the fused scan
+constexpr int kFuseScanMax = 32;  // groups a thread may scan in the fused scan
 static_assert(32 * kCountWarps == kScanThreads, "a count CTA can run the block scan");
 
 // The fused scan: one CTA (kScanThreads threads) over rank r's C groups.
-// Thread t takes key b = t % NB and the slice g = t / NB of at most
-// kFuseScanPer consecutive groups (G = kScanThreads / NB slices per key).
-__device__ __forceinline__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) {
+// Thread t takes key b = t % NB and the slice g = t / NB of consecutive
+// groups (G = kScanThreads / NB slices per key): it sums its slice, the
+// slices' sums give it its base, and it rewrites its slice with running
+// prefixes.  Counts are loaded kFuseScanBatch at a time, from L2 (the other
+// count CTAs wrote them during this launch).
+constexpr int kFuseScanBatch = 8;
+__device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) {
   const int t = threadIdx.x, NB = D.W * D.K, G = kScanThreads / NB;
   const int b = t % NB, g = t / NB;
   const long long per = (C + G - 1) / G;
-  const long long c0 = g < G ? g * per : C, c1 = c0 + per < C ? c0 + per : C;
+  const long long c0 = g < G ? g * per : C;
+  const long long c1 = g < G ? (c0 + per < C ? c0 + per : C) : C;
   int* A = D.grp + (long long)r * D.groups_max * NB + b;  // group c at A[c * NB]
   __shared__ long long part[kScanThreads];
   __shared__ long long tot[kScanThreads];
   __shared__ long long warp_sums[kScanThreads / 32];
-  int v[kFuseScanPer];
   long long local = 0;
+  for (long long c = c0; c < c1; c += kFuseScanBatch) {
+    int v[kFuseScanBatch];
 #pragma unroll
-  for (int q = 0; q < kFuseScanPer; ++q) {
-    v[q] = c0 + q < c1 ? __ldcg(A + (c0 + q) * NB) : 0;
-    local += v[q];
+    for (int q = 0; q < kFuseScanBatch; ++q) v[q] = c + q < c1 ? __ldcg(A + (c + q) * NB) : 0;
+#pragma unroll
+    for (int q = 0; q < kFuseScanBatch; ++q) local += v[q];
   }
   part[t] = local;
   __syncthreads();
@@ -199,25 +206,41 @@ __device__ __forceinline__ void scan_groups_in_cta(const DispatchParams& D, int 
       if (h < g) base += x;
       total += x;
     }
+  for (long long c = c0; c < c1; c += kFuseScanBatch) {
+    int v[kFuseScanBatch];
 #pragma unroll
-  for (int q = 0; q < kFuseScanPer; ++q) {
-    if (c0 + q < c1) A[(c0 + q) * NB] = (int)base;
-    base += v[q];
+    for (int q = 0; q < kFuseScanBatch; ++q) v[q] = c + q < c1 ? __ldcg(A + (c + q) * NB) : 0;
+#pragma unroll
+    for (int q = 0; q < kFuseScanBatch; ++q) {
+      if (c + q < c1) A[(c + q) * NB] = (int)base;
+      base += v[q];
+    }
   }
   if (g == 0) tot[b] = total;
   __syncthreads();
   finish_rank(D, r, tot, warp_sums);
 }
 
-__global__ void __launch_bounds__(32 * kCountWarps, 6) dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
+// Count: CTA (c, r) holds group c of rank r; warp w ranks ranges
+// 8RW c + RW w .. + RW - 1 (all their keys and source rows loaded at once),
+// 32 items at a time: __match_any_sync groups equal keys, a lane's rank
+// among them plus the range's running count of its key is its inrank, and
+// each key's leader advances that count.  RW = 4
+// serves batches so large that one CTA per SM still has four ranges a warp
+// (fewer groups: the last CTA can still scan them).  Four CTAs an SM (64
+// registers) keep every RW = 1 grid resident in one wave: RW = 4 takes over
+// before a grid passes W * ceil(ranges / 32) >= SMs, i.e. 4 x SMs CTAs.
+template <int RW>
+__global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 4 : 2)
+    dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
   chain_wait();
+  constexpr int kGroupRanges = kCountWarps * RW;
   const int r = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   const long long c = blockIdx.x;
-  const long long range = c * kCountWarps + warp;
-  const long long i0 = range * kRange, m = D.items[r];
+  const long long m = D.items[r];
   const int NB = D.W * D.K;
-  if (c * kGroupItems >= m) {  // no items in this CTA's ranges (uniform over the CTA)
+  if (c * kGroupRanges * kRange >= m) {  // no items in this CTA's ranges (uniform over the CTA)
     if (c == 0 && D.fuse_scan) {  // a rank without items: zero counts and splits
       __shared__ long long zero[kScanThreads];
       __shared__ long long zero_sums[kScanThreads / 32];
@@ -227,36 +250,55 @@ __global__ void __launch_bounds__(32 * kCountWarps, 6) dispatch_count_kernel(con
     }
     return;
   }
-  extern __shared__ int count_hist[];
-  int* hist = count_hist + warp * NB;
-  for (int b = lane; b < NB; b += 32) hist[b] = 0;
-  if (i0 < m) {
-    int keys[kRange / 32], srcs[kRange / 32];
+  extern __shared__ int count_hist[];  // [kGroupRanges][NB], range by range
+  for (int e = t; e < kGroupRanges * NB; e += blockDim.x) count_hist[e] = 0;
+  const long long j0 = c * kGroupRanges + (long long)warp * RW;  // this warp's first range
+  int keys[RW][kRange / 32], srcs[RW][kRange / 32];
+#pragma unroll
+  for (int u = 0; u < RW; ++u)
 #pragma unroll
     for (int q = 0; q < kRange / 32; ++q) {
-      const long long i = i0 + q * 32 + lane;
-      keys[q] = i < m ? D.key[r][i] : 0;
-      srcs[q] = i < m ? D.src[r][i] : 0;
+      const long long i = (j0 + u) * kRange + q * 32 + lane;
+      keys[u][q] = i < m ? D.key[r][i] : 0;
+      srcs[u][q] = i < m ? D.src[r][i] : 0;
     }
-    __syncwarp();
-    int bad = 0;
+  int bad = 0;
+#pragma unroll
+  for (int u = 0; u < RW; ++u)
 #pragma unroll
     for (int q = 0; q < kRange / 32; ++q) {
-      if (i0 + q * 32 + lane >= m) continue;
-      if (keys[q] < 0 || keys[q] >= NB || srcs[q] < 0 || srcs[q] >= D.rows[r])
-        bad = 1;
-      else
-        atomicAdd(&hist[keys[q]], 1);
+      const long long i = (j0 + u) * kRange + q * 32 + lane;
+      const int k = keys[u][q], s = srcs[u][q];
+      const bool ok = i < m && k >= 0 && k < NB && s >= 0 && s < D.rows[r];
+      if (i < m && !ok) bad = 1;
+      keys[u][q] = ok ? k : -1 - lane;  // absent or invalid items match nobody
     }
-    if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int u = 0; u < RW; ++u) {
+    int* hist = count_hist + (warp * RW + u) * NB;
+#pragma unroll
+    for (int q = 0; q < kRange / 32; ++q) {
+      const int k = keys[u][q];
+      const unsigned same = __match_any_sync(kFull, k);
+      const int inr = k >= 0 ? hist[k] + __popc(same & lt) : 0;
+      __syncwarp();
+      if (k >= 0 && lane == 31 - __clz(same)) hist[k] += __popc(same);
+      __syncwarp();
+      if (k >= 0)
+        D.inrank[(long long)r * D.pos_stride + (j0 + u) * kRange + q * 32 + lane] =
+            (unsigned char)inr;
+    }
   }
+  if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
   __syncthreads();
   // in-group prefixes of the ranges that hold items, and the group's count
   const long long R = (m + kRange - 1) / kRange;
   for (int b = t; b < NB; b += blockDim.x) {
     int run = 0;
-    for (int w = 0; w < kCountWarps; ++w) {
-      const long long j = c * kCountWarps + w;
+    for (int w = 0; w < kGroupRanges; ++w) {
+      const long long j = c * kGroupRanges + w;
       if (j < R) D.hist[((long long)r * D.ranges_max + j) * NB + b] = run;
       run += count_hist[w * NB + b];
     }
@@ -267,7 +309,7 @@ __global__ void __launch_bounds__(32 * kCountWarps, 6) dispatch_count_kernel(con
   __shared__ int last;
   __threadfence();
   __syncthreads();
-  const long long C = (m + kGroupItems - 1) / kGroupItems;
+  const long long C = (m + kGroupRanges * kRange - 1) / (kGroupRanges * kRange);
   if (t == 0) last = atomicAdd(&D.done[r], 1) == (int)(C - 1);
   __syncthreads();
   if (!last) return;
@@ -288,7 +330,8 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
   __shared__ long long warp_sums[kScanThreads / 32];
   __shared__ long long tot[kMaxBins];
   __shared__ int last;
-  const long long C = (D.items[r] + kGroupItems - 1) / kGroupItems;
+  const long long GI = (long long)kRange << D.group_log2;
+  const long long C = (D.items[r] + GI - 1) / GI;
   int* H = D.grp + (long long)r * D.groups_max * NB + b;  // group j at H[j * NB]
   const long long per = (C + kScanThreads - 1) / kScanThreads;
   const long long j0 = t * per, j1 = j0 + per < C ? j0 + per : C;
@@ -358,38 +401,102 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(const __gri
   }
 }
 
-__global__ void __launch_bounds__(32) dispatch_rank_kernel(const __grid_constant__ DispatchParams D) {
-  chain_wait();
+// Small dispatches (every rank at most kSmallItems items, at most
+// kSmallKeys keys): count and scan in one kernel, one CTA per rank.  Warp w
+// ranks range w of the rank (items [256 w, 256 w + 256)) like the count
+// kernel; the per-warp counts become the ranges' prefixes (one group), a
+// block scan of the key totals gives the key starts.
+constexpr int kSmallWarps = 8;
+constexpr int kSmallItems = kSmallWarps * kRange;  // 2048
+constexpr int kSmallKeys = kScanThreads;           // one key per thread in the key scan
+
+__global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
-  if (flagged(D)) return;
-  const int r = blockIdx.y, lane = threadIdx.x, NB = D.W * D.K;
-  const long long i0 = (long long)blockIdx.x * kRange, m = D.items[r];
-  if (i0 >= m) return;
-  __shared__ long long next[kMaxBins];  // next position of each key in this range
-  const int* H = D.hist + ((long long)r * D.ranges_max + blockIdx.x) * NB;
-  const int* A = D.grp + ((long long)r * D.groups_max + blockIdx.x / kCountWarps) * NB;
-  for (int k = lane; k < NB; k += 32) next[k] = D.key_start[(long long)r * NB + k] + A[k] + H[k];
-  __syncwarp();
-  // All keys of the range are loaded at once (8 per lane), then ranked in order.
-  int keys[kRange / 32];
+  chain_wait();
+  const int r = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NB = D.W * D.K;
+  const long long m = D.items[r];
+  __shared__ int cnt[kSmallWarps][kSmallKeys];
+  __shared__ long long warp_sums[kScanThreads / 32];
+  for (int e = tid; e < kSmallWarps * NB; e += kScanThreads) cnt[e / NB][e % NB] = 0;
+  int keys[kRange / 32], srcs[kRange / 32];
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = i0 + c * 32 + lane;
-    keys[c] = i < m ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
+    const long long i = (long long)warp * kRange + c * 32 + lane;
+    keys[c] = i < m ? D.key[r][i] : 0;
+    srcs[c] = i < m ? D.src[r][i] : 0;
   }
+  int bad = 0;
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = i0 + c * 32 + lane;
-    const bool valid = i < m;
+    const long long i = (long long)warp * kRange + c * 32 + lane;
+    const bool ok = i < m && keys[c] >= 0 && keys[c] < NB && srcs[c] >= 0 && srcs[c] < D.rows[r];
+    if (i < m && !ok) bad = 1;
+    keys[c] = ok ? keys[c] : -1 - lane;  // absent or invalid items match nobody
+  }
+  __syncthreads();
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int c = 0; c < kRange / 32; ++c) {
     const int key = keys[c];
     const unsigned same = __match_any_sync(kFull, key);
-    long long pos = 0;
-    if (valid) pos = next[key] + __popc(same & ((1u << lane) - 1u));
+    const int inr = key >= 0 ? cnt[warp][key] + __popc(same & lt) : 0;
     __syncwarp();
-    if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
+    if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
     __syncwarp();
-    if (valid) D.pos[(long long)r * D.pos_stride + i] = (int)pos;
+    if (key >= 0)
+      D.inrank[(long long)r * D.pos_stride + (long long)warp * kRange + c * 32 + lane] =
+          (unsigned char)inr;
   }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) fail(D, A2AV_ERR_BAD_INDEX);
+    return;
+  }
+  const long long R = (m + kRange - 1) / kRange;
+  long long total_k = 0;
+  if (tid < NB) {
+    int run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      if (w < R) D.hist[((long long)r * D.ranges_max + w) * NB + tid] = run;
+      run += cnt[w][tid];
+    }
+    total_k = run;
+    D.grp[(long long)r * D.groups_max * NB + tid] = 0;  // one group
+  }
+  long long all;
+  const long long start = block_exclusive_scan(total_k, warp_sums, &all);
+  if (tid < NB) {
+    D.key_start[(long long)r * NB + tid] = start;
+    D.key_total[(long long)r * NB + tid] = total_k;
+  }
+  __syncthreads();
+  if (tid < D.W) {
+    long long sum = 0;
+    for (int k = 0; k < D.K; ++k) sum += __ldcg(D.key_total + (long long)r * NB + tid * D.K + k);
+    D.S[(long long)r * D.W + tid] = sum;
+  }
+}
+
+// Position of item i (key k) of rank r in the rank's key order, less its
+// inrank byte: items of smaller keys, of key k in earlier groups and in
+// earlier ranges of its group.
+__device__ __forceinline__ long long key_base(const DispatchParams& D, int r, long long i, int k) {
+  const int NB = D.W * D.K;
+  const long long j = i >> 8, c = j >> D.group_log2;
+  return D.key_start[(long long)r * NB + k] + D.grp[((long long)r * D.groups_max + c) * NB + k] +
+         D.hist[((long long)r * D.ranges_max + j) * NB + k];
+}
+
+// Defensive check of a computed position: it must lie in its destination's
+// group of the rank's key order, [in_off[r][p], in_off[r][p] + S[r][p]).
+// Positions are derived from validated keys, so this never fails unless the
+// position arithmetic itself is wrong; if it did, the row is not copied (no
+// write outside the outputs) and A2AV_ERR_BAD_INDEX is recorded.
+__device__ __forceinline__ bool in_group(const Plan& pl, int r, int p, long long pos, int* status) {
+  const long long lo = pl.in_off[r][p];
+  if (pos >= lo && pos < lo + pl.s[r][p]) return true;
+  record_error(status, A2AV_ERR_BAD_INDEX);
+  return false;
 }
 
 // A row of n bytes, any alignment, copied by one thread.
@@ -408,38 +515,53 @@ __device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned
   }
 }
 
-// Rank and copy (rows shorter than 64 bytes): the rank kernel's ranking,
-// then each lane copies its items' rows straight to their place in the
-// output of their destination and publishes their positions.  The plan was
-// validated by the scan kernel, whose flag stops this kernel otherwise.  Two
-// warps per CTA, a range each, registers capped so that a whole GPU of them
-// is resident at once (the ranking is a serial chain per warp: more warps
-// in flight, not more work per warp).
-#ifndef A2AV_RANK_COPY_WARPS
-#define A2AV_RANK_COPY_WARPS 2
+// Place and copy (rows shorter than 64 bytes): warp w takes one range of 256
+// items; its keys, source rows and inrank bytes and the range's key bases
+// (key_base for every key, into shared memory) are loaded at once; then
+// each lane puts its items' rows straight at their place in the output of
+// their destination and publishes their positions.  Every CTA first repeats
+// the a2av prologue's checks on the whole split matrix (so all reach the
+// same verdict) and derives its rank's row displacement per peer.  Two warps
+// per CTA, registers capped so that a whole GPU of them is resident at once.
+#ifndef A2AV_PLACE_WARPS
+#define A2AV_PLACE_WARPS 2
 #endif
-#ifndef A2AV_RANK_COPY_MIN_CTAS
-#define A2AV_RANK_COPY_MIN_CTAS 18
+#ifndef A2AV_PLACE_MIN_CTAS
+#define A2AV_PLACE_MIN_CTAS 18
 #endif
-constexpr int kRankCopyWarps = A2AV_RANK_COPY_WARPS;
+constexpr int kPlaceWarps = A2AV_PLACE_WARPS;
 
-__global__ void __launch_bounds__(32 * kRankCopyWarps, A2AV_RANK_COPY_MIN_CTAS)
-    dispatch_rank_copy_kernel(const __grid_constant__ Params P,
-                              const __grid_constant__ DispatchParams D) {
+__global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
+    dispatch_place_copy_kernel(const __grid_constant__ Params P,
+                               const __grid_constant__ DispatchParams D) {
   chain_wait();
   chain_release();
   if (flagged(D)) return;
   const int r = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int W = D.W, K = D.K, NB = W * K;
-  const long long range = (long long)blockIdx.x * kRankCopyWarps + warp;
+  const long long range = (long long)blockIdx.x * kPlaceWarps + warp;
   const long long i0 = range * kRange, m = D.items[r];
-  __shared__ int next_all[kRankCopyWarps][kMaxBins];  // next position of each key in the range
-  __shared__ long long disp[kMaxW];  // out_off[p][r] - in_off[r][p], rows
+  const bool live = i0 < m;
+  extern __shared__ int place_base[];  // [kPlaceWarps][NB]
+  __shared__ long long disp[kMaxW];    // out_off[p][r] - in_off[r][p], rows
+  __shared__ long long glo[kMaxW], gcnt[kMaxW];  // in_off[r][p], S[r][p]: p's group
   __shared__ int bad_splits;
+  int keys[kRange / 32], srcs[kRange / 32], inr[kRange / 32];
+  int* base = place_base + warp * NB;
+  if (live) {
+#pragma unroll
+    for (int c = 0; c < kRange / 32; ++c) {
+      const long long i = i0 + c * 32 + lane;
+      keys[c] = i < m ? D.key[r][i] : 0;
+      srcs[c] = i < m ? D.src[r][i] : 0;
+      inr[c] = i < m ? D.inrank[(long long)r * D.pos_stride + i] : 0;
+    }
+    for (int k = lane; k < NB; k += 32) base[k] = (int)key_base(D, r, i0, k);
+  }
   if (warp == 0) {
     // The a2av prologue's checks on the whole split matrix (identical in
     // every CTA, so all reach the same verdict): lane p owns column p and
-    // row p.  S was completed by the scan kernel.
+    // row p.  S was completed by the count (or scan) kernel.
     const int p = lane;
     long long col = 0, above = 0, row = 0, own = 0;
     int bad = 0;
@@ -457,7 +579,11 @@ __global__ void __launch_bounds__(32 * kRankCopyWarps, A2AV_RANK_COPY_MIN_CTAS)
       if ((P.in_cap > 0 && row > P.in_cap) || (P.in[p] == nullptr && row > 0)) bad = 1;
     }
     const long long in_off = warp_inclusive_scan(own, lane) - own;  // in_off[r][p]
-    if (p < W) disp[p] = above - in_off;
+    if (p < W) {
+      disp[p] = above - in_off;
+      glo[p] = in_off;
+      gcnt[p] = own;
+    }
     bad = __any_sync(kFull, bad);
     if (lane == 0) bad_splits = bad;
     if (blockIdx.x == 0 && r == 0) {  // one CTA records the verdict and the offsets
@@ -477,124 +603,20 @@ __global__ void __launch_bounds__(32 * kRankCopyWarps, A2AV_RANK_COPY_MIN_CTAS)
     }
   }
   __syncthreads();
-  if (bad_splits || i0 >= m) return;
-  int* next = next_all[warp];
-  const int* H = D.hist + ((long long)r * D.ranges_max + range) * NB;
-  const int* A = D.grp + ((long long)r * D.groups_max + range / kCountWarps) * NB;
-  for (int k = lane; k < NB; k += 32) next[k] = (int)D.key_start[(long long)r * NB + k] + A[k] + H[k];
-  int keys[kRange / 32];
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = i0 + c * 32 + lane;
-    keys[c] = i < m ? D.key[r][i] : -1 - lane;  // invalid lanes match nobody
-  }
-  __syncwarp();
-  int pos[kRange / 32];  // positions within the rank: below 2^31 items
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const bool valid = i0 + c * 32 + lane < m;
-    const int key = keys[c];
-    const unsigned same = __match_any_sync(kFull, key);
-    pos[c] = valid ? next[key] + __popc(same & ((1u << lane) - 1u)) : 0;
-    __syncwarp();
-    if (valid && lane == 31 - __clz(same)) next[key] += __popc(same);
-    __syncwarp();
-  }
+  if (bad_splits || !live) return;
   const long long rb = P.rb;
-  int srcs[kRange / 32];  // loaded together, after the ranking (fewer live registers)
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = i0 + c * 32 + lane;
-    srcs[c] = i < m ? D.src[r][i] : 0;
-  }
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = i0 + c * 32 + lane;
     if (i >= m) continue;
     const int p = keys[c] / K;
-    D.sorted_pos[r][i] = pos[c];
-    copy_row_thread(P.out[p] + (disp[p] + (long long)pos[c]) * rb,
-                    P.in[r] + (long long)srcs[c] * rb, rb);
-  }
-}
-
-// Small dispatches (every rank at most kSmallItems items, at most
-// kSmallKeys keys): count, scan and rank in one kernel, one CTA per rank.
-// Warp w owns items [256 w, 256 w + 256) with their keys in registers: it
-// counts them per key (warp match, its own row of `cnt`), the rows are
-// turned into per-key prefixes over the warps, a block scan of the key
-// totals gives the key starts, and each warp ranks its items in order.
-constexpr int kSmallWarps = 8;
-constexpr int kSmallItems = kSmallWarps * kRange;  // 2048
-constexpr int kSmallKeys = kScanThreads;           // one key per thread in the key scan
-
-__global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __grid_constant__ DispatchParams D) {
-  chain_release();
-  chain_wait();
-  const int r = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NB = D.W * D.K;
-  const long long m = D.items[r];
-  __shared__ int cnt[kSmallWarps][kSmallKeys];
-  __shared__ long long key_start[kSmallKeys];
-  __shared__ long long warp_sums[kScanThreads / 32];
-  for (int e = tid; e < kSmallWarps * NB; e += kScanThreads) cnt[e / NB][e % NB] = 0;
-  __syncthreads();
-  int keys[kRange / 32];
-  int bad = 0;
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = (long long)warp * kRange + c * 32 + lane;
-    int key = -1 - lane;  // absent items match nobody
-    if (i < m) {
-      key = D.key[r][i];
-      const int src = D.src[r][i];
-      if (key < 0 || key >= NB || src < 0 || src >= D.rows[r]) {
-        bad = 1;
-        key = -1 - lane;
-      }
+    const long long pos = (long long)base[keys[c]] + inr[c];
+    D.sorted_pos[r][i] = pos;
+    if (pos < glo[p] || pos >= glo[p] + gcnt[p]) {  // never: see in_group
+      record_error(D.status, A2AV_ERR_BAD_INDEX);
+      continue;
     }
-    keys[c] = key;
-    const unsigned same = __match_any_sync(kFull, key);
-    if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
-    __syncwarp();
-  }
-  if (__syncthreads_or(bad)) {
-    if (tid == 0) fail(D, A2AV_ERR_BAD_INDEX);
-    return;
-  }
-  long long total_k = 0;
-  if (tid < NB) {
-    int run = 0;
-    for (int w = 0; w < kSmallWarps; ++w) {
-      const int x = cnt[w][tid];
-      cnt[w][tid] = run;
-      run += x;
-    }
-    total_k = run;
-  }
-  long long all;
-  const long long start = block_exclusive_scan(total_k, warp_sums, &all);
-  if (tid < NB) {
-    key_start[tid] = start;
-    D.key_total[(long long)r * NB + tid] = total_k;
-  }
-  __syncthreads();
-  if (tid < D.W) {
-    long long sum = 0;
-    for (int k = 0; k < D.K; ++k) sum += __ldcg(D.key_total + (long long)r * NB + tid * D.K + k);
-    D.S[(long long)r * D.W + tid] = sum;
-  }
-#pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
-    const long long i = (long long)warp * kRange + c * 32 + lane;
-    const int key = keys[c];
-    const unsigned same = __match_any_sync(kFull, key);
-    int pos = 0;
-    if (key >= 0) pos = (int)key_start[key] + cnt[warp][key] + __popc(same & ((1u << lane) - 1u));
-    __syncwarp();
-    if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
-    __syncwarp();
-    if (i < m) D.pos[(long long)r * D.pos_stride + i] = pos;
+    copy_row_thread(P.out[p] + (disp[p] + pos) * rb, P.in[r] + (long long)srcs[c] * rb, rb);
   }
 }
 
@@ -616,14 +638,12 @@ __device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc,
   }
 }
 
-// kWarpRows: rows of kWarpRowBytes or more, a warp per row (each kernel
-// instantiation holds one of the two loops, so neither pays the other's
-// registers); kVec: the 16-byte vectors a lane keeps in flight on aligned
-// warp rows.
-template <bool kWarpRows, int kVec = kVecRows>
-__global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasPerSm
-                                                : kVec > kVecRows ? kCopyCtasPerSmWide
-                                                                  : kCopyCtasPerSmWarpRows)
+// Register copies (rows the gather does not take): kWarpRows -- rows of
+// kWarpRowBytes or more, a warp per batch of rows (each kernel instantiation
+// holds one of the two loops, so neither pays the other's registers); else
+// a thread per row.
+template <bool kWarpRows>
+__global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRows : kCopyCtasPerSm)
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   if (flagged(D)) return;
@@ -639,13 +659,12 @@ __global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasP
                                     : (long long)gridDim.x * kCopyThreads;
   if constexpr (warp_rows) {
     // A warp takes a batch of up to 32 consecutive items: lane l reads item
-    // l's key, position and source row (one round trip for the batch), then
-    // the warp copies the batch's rows.  16-byte aligned rows are copied as
-    // one flat run of vectors over the batch, kVec x 16 bytes per lane in
-    // flight; other rows one at a time with the realigning span copy.  The
-    // batch size gives every warp the same number of batches: with 32 items
-    // a batch, 131072 items over 3648 warps would leave a second round to one
-    // warp in eight, and the kernel would take twice the time of the rest.
+    // l's metadata (one round trip for the batch, a second for the key
+    // bases), then the warp copies the batch's rows.  16-byte aligned rows
+    // are copied as one flat run of vectors over the batch, kVecRows x 16
+    // bytes per lane in flight; other rows one at a time with the
+    // realigning span copy.  The batch size gives every warp the same
+    // number of batches.
     const int lane = threadIdx.x & 31;
     const long long rounds = (total + teams * 32 - 1) / (teams * 32);
     const long long batch = rounds > 0 ? (total + teams * rounds - 1) / (teams * rounds) : 32;
@@ -657,25 +676,29 @@ __global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasP
         int r = 0;
         while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
         const long long i = g - D.item_first[r];
-        const int p = D.key[r][i] / K;
+        const int k = D.key[r][i];
+        const int p = k / K;
         const long long grouped = pl.out_off[p][r] - pl.in_off[r][p];  // + pos: the row in p's buffer
         if (D.combine) {  // from the peer's buffer back to the item's row
           msrc = (long long)(P.out[p] + (grouped + D.sorted_pos[r][i]) * rb);
           mdst = (long long)(P.in[r] + i * rb);
         } else {
-          const long long pos = D.pos[(long long)r * D.pos_stride + i];
+          const int s = D.src[r][i];
+          const long long pos = key_base(D, r, i, k) + D.inrank[(long long)r * D.pos_stride + i];
           D.sorted_pos[r][i] = pos;
           mdst = (long long)(P.out[p] + (grouped + pos) * rb);
-          msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
+          msrc = (long long)(P.in[r] + (long long)s * rb);
+          if (!in_group(pl, r, p, pos, D.status)) mdst = msrc = 0;
         }
       }
+      if (!D.combine && __any_sync(kFull, lane < n && mdst == 0)) continue;  // (never: in_group)
       if (D.vec16 && rb <= kVecMaxRow) {
         const unsigned V = (unsigned)(rb >> 4), nv = (unsigned)n * V;  // < 2^17
-        for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVec) {  // warp-uniform trip count
-          uint4 v[kVec];
-          long long d[kVec];
+        for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVecRows) {  // warp-uniform trip count
+          uint4 v[kVecRows];
+          long long d[kVecRows];
 #pragma unroll
-          for (int q = 0; q < kVec; ++q) {
+          for (int q = 0; q < kVecRows; ++q) {
             const unsigned idx = b0 + q * 32 + lane;
             const bool ok = idx < nv;
             const unsigned j = ok ? idx / V : 0, c = ok ? idx - j * V : 0;
@@ -684,7 +707,7 @@ __global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasP
             if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s) + c);
           }
 #pragma unroll
-          for (int q = 0; q < kVec; ++q)
+          for (int q = 0; q < kVecRows; ++q)
             if (b0 + q * 32 + lane < nv) st_stream(reinterpret_cast<uint4*>(d[q]), v[q]);
         }
       } else {
@@ -692,8 +715,8 @@ __global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasP
       }
     }
   } else {
-  // Short rows: a thread takes kItemsPerThread items, their key, source row
-  // and position loads issued together, then copies the rows.
+  // Short rows: a thread takes kItemsPerThread items, their metadata loads
+  // issued together, then copies the rows.
   for (long long g0 = team; g0 < total; g0 += teams * kItemsPerThread) {
     int rank[kItemsPerThread], key[kItemsPerThread], src_row[kItemsPerThread];
     long long pos[kItemsPerThread];
@@ -712,10 +735,18 @@ __global__ void __launch_bounds__(kCopyThreads, !kWarpRows          ? kCopyCtasP
           pos[q] = D.sorted_pos[r][i];
         } else {
           src_row[q] = D.src[r][i];
-          pos[q] = D.pos[(long long)r * D.pos_stride + i];
-          D.sorted_pos[r][i] = pos[q];
+          pos[q] = D.inrank[(long long)r * D.pos_stride + i];
         }
       }
+    }
+#pragma unroll
+    for (int q = 0; q < kItemsPerThread; ++q) {
+      const int r = rank[q];
+      if (r < 0 || D.combine) continue;
+      const long long i = g0 + q * teams - D.item_first[r];
+      pos[q] += key_base(D, r, i, key[q]);
+      D.sorted_pos[r][i] = pos[q];
+      if (!in_group(pl, r, key[q] / K, pos[q], D.status)) rank[q] = -1;
     }
 #pragma unroll
     for (int q = 0; q < kItemsPerThread; ++q) {
@@ -764,177 +795,632 @@ __global__ void __launch_bounds__(kCopyThreads)
   if (__syncthreads_or(bad) && threadIdx.x == 0) fail(D, A2AV_ERR_BAD_INDEX);
 }
 
-// Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
-// cleared before every dispatch; then S, key starts, key totals, histograms.
-// Rows of 2..32 KiB, every row and buffer 16-byte aligned: NWK warps per CTA
-// each stream their share of the CTA's items, row by row, global -> shared ->
-// global with cp.async.bulk through a ring of NS stages of their own (loads
-// LEAD rows ahead of the stores).  A warp reads the metadata of 32 items at
-// a time, lane i item i; its lane 0 issues the copies and tracks its own
-// bulk stores.
-template <int NS, int LEAD, int NWK>
-__global__ void __launch_bounds__(128)
-    dispatch_copy_bulk_kernel(const __grid_constant__ Params P,
-                              const __grid_constant__ DispatchParams D, int stage_bytes) {
-  static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 rows ahead of stores");
-  static_assert(NWK >= 1 && NWK <= 4, "one to four issuing warps");
+// ------------------------------------------------------------- gather --
+// One lane's item of a gather batch: where it is and its raw metadata.
+struct GatherItem {
+  long long i;     // index within its rank
+  long long spos;  // combine: the item's position in its rank's key order
+  int r, key, src, inr;
+  bool v;          // the lane holds an item
+};
+
+// Batch b (global over the ranks, bs items each) -> lane's item; b < 0: none.
+__device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long long b, int lane) {
+  GatherItem x;
+  x.i = 0;
+  x.spos = 0;
+  x.r = 0;
+  x.key = 0;
+  x.src = 0;
+  x.inr = 0;
+  x.v = false;
+  if (b < 0) return x;
+  int r = 0;
+  while (r + 1 < D.W && D.batch_first[r + 1] <= b) ++r;
+  const long long i = (b - D.batch_first[r]) * D.bs + lane;
+  x.r = r;
+  x.i = i;
+  if (lane < D.bs && i < D.items[r]) {
+    x.v = true;
+    x.key = D.key[r][i];
+    if (D.combine) {
+      x.spos = D.sorted_pos[r][i];
+    } else {
+      x.src = D.src[r][i];
+      x.inr = D.inrank[(long long)r * D.pos_stride + i];
+    }
+  }
+  return x;
+}
+
+// The cp.async.bulk gather for 16-byte aligned rows of 64 B .. 32 KiB.  NWK
+// warps per CTA, each an independent pipeline with a ring of NS stages of
+// IPS row slots (its own mbarriers, its own bulk groups).  A warp takes every
+// (grid x NWK)-th batch of bs consecutive items of one rank; a batch is
+// copied as bs / min(bs, IPS) stages.  In a stage every lane that holds an
+// item issues the bulk load of its row into its slot (one mbarrier per
+// stage, armed by lane 0 with the stage's byte count); LEAD stages later the
+// lanes wait for the stage and issue one bulk store each (the combine: one
+// store of the whole stage, whose rows are consecutive items of one rank),
+// and every lane commits one bulk group per stage, so that
+// cp.async.bulk.wait_group.read NS - LEAD - 1 frees the stage reused next.
+// A batch's addresses need two dependent round trips (its keys, then their
+// key bases), so they are loaded two and one batches ahead.  Waits are
+// bounded: on a timeout the warp records A2AV_ERR_TIMEOUT, waits (bounded)
+// for every load it issued and leaves.
+template <int NS, int LEAD, int NWK, int IPS>
+__global__ void __launch_bounds__(32 * NWK, 1)
+    dispatch_gather_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 stages ahead of stores");
+  static_assert(NWK >= 1 && NWK <= 4 && IPS >= 1 && IPS <= 32 && (IPS & (IPS - 1)) == 0,
+                "one to four warps, a power-of-two number of slots per stage");
   chain_wait();
   if (flagged(D)) return;
   __shared__ Plan pl;
-  __shared__ alignas(8) unsigned long long bars[NWK * NS];
-  __shared__ unsigned char* stage_dst[NWK * NS];
+  __shared__ alignas(8) unsigned long long bars[NWK][NS];
+  __shared__ unsigned long long sdst[NWK][NS][IPS];  // each slot's destination
+  __shared__ unsigned smask[NWK][NS];               // slots holding a row, per stage
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
   publish_splits(D);
   const int lane = threadIdx.x & 31;
-  if ((int)(threadIdx.x >> 5) >= NWK) return;
   const int warp = NWK == 1 ? 0 : (int)(threadIdx.x >> 5);  // a constant for one warp
-  // Warp w owns every NWK-th of the CTA's items, its own NS stages and
-  // barriers: NWK independent pipelines, so NWK lanes issue copies at once.
-  const int W = D.W, K = D.K;
-  const long long rb = P.rb, total = D.item_first[W], G = gridDim.x, b0 = blockIdx.x;
-  const long long nc = total > b0 ? (total - b0 + G - 1) / G : 0;  // the CTA's items
-  const long long nk = nc > warp ? (nc - warp + NWK - 1) / NWK : 0;  // this warp's
-  if (nk == 0) return;
-  const uint32_t bar0 = smem_u32(bars) + 8u * NS * warp,
-                 stage0 = smem_u32(stages) + (uint32_t)(NS * warp) * (uint32_t)stage_bytes;
-  unsigned char** const sdst = stage_dst + NS * warp;
+  const int W = D.W, K = D.K, bs = D.bs;
+  const int unit = bs < IPS ? bs : IPS, spb = bs / unit;  // slots used per stage, stages per batch
+  const long long rb = P.rb;
+  const long long WG = (long long)gridDim.x * NWK, wg = (long long)blockIdx.x * NWK + warp;
+  const long long nbatch = D.batch_first[W];
+  const long long nt = nbatch > wg ? (nbatch - wg + WG - 1) / WG : 0;  // this warp's batches
+  if (nt == 0) return;
+  const uint32_t stage_bytes = (uint32_t)(IPS * rb);
+  const uint32_t bar0 = smem_u32(&bars[warp][0]);
+  const uint32_t st0 = smem_u32(stages) + (uint32_t)(NS * warp) * stage_bytes;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(bar0 + 8 * s, 1);
     mbar_fence_init();
   }
   __syncwarp();
-  long long msrc = 0, mdst = 0;  // this lane's item of the current batch of 32
-  long long issued = 0, stored = 0;
+
+  long long issued = 0, drained = 0;  // stages
   bool ok = true;
-  for (long long k = 0; k < nk + LEAD; ++k) {
-    if (k < nk) {
-      if ((k & 31) == 0) {
-        const long long kk = k + lane;
-        if (kk < nk) {
-          const long long g = b0 + (warp + kk * NWK) * G;
-          int r = 0;
-          while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
-          const long long i = g - D.item_first[r];
-          const int p = D.key[r][i] / K;
-          const long long grouped = pl.out_off[p][r] - pl.in_off[r][p];
-          if (D.combine) {  // from the peer's buffer back to the item's row
-            msrc = (long long)(P.out[p] + (grouped + D.sorted_pos[r][i]) * rb);
-            mdst = (long long)(P.in[r] + i * rb);
-          } else {
-            const long long pos = D.pos[(long long)r * D.pos_stride + i];
-            D.sorted_pos[r][i] = pos;
-            msrc = (long long)(P.in[r] + (long long)D.src[r][i] * rb);
-            mdst = (long long)(P.out[p] + (grouped + pos) * rb);
-          }
+  // Wait for stage j's loads and store its rows; false on a timeout.
+  auto drain = [&](long long j) -> bool {
+    const int s = (int)(j % NS);
+    if (!mbar_wait_warp(bar0 + 8 * s, (unsigned)((j / NS) & 1))) return false;
+    const unsigned mask = smask[warp][s];
+    const uint32_t st = st0 + (uint32_t)s * stage_bytes;
+    if (D.combine) {  // the slots in use are a prefix, consecutive items of one rank
+      if (lane == 0 && mask != 0)
+        bulk_store(reinterpret_cast<void*>(sdst[warp][s][0]), st, (unsigned)(__popc(mask) * rb));
+      else
+        bulk_commit();
+    } else if ((mask >> lane) & 1u) {
+      bulk_store(reinterpret_cast<void*>(sdst[warp][s][lane]), st + (uint32_t)(lane * rb),
+                 (unsigned)rb);
+    } else {
+      bulk_commit();
+    }
+    return true;
+  };
+
+  GatherItem a0 = gather_item(D, wg, lane);
+  GatherItem a1 = gather_item(D, nt > 1 ? wg + WG : -1, lane);
+  long long b0 = a0.v && !D.combine ? key_base(D, a0.r, a0.i, a0.key) : 0;
+  for (long long t = 0; t < nt && ok; ++t) {
+    const GatherItem a2 = gather_item(D, t + 2 < nt ? wg + (t + 2) * WG : -1, lane);
+    const long long b1 = a1.v && !D.combine ? key_base(D, a1.r, a1.i, a1.key) : 0;
+    // batch t's row addresses
+    long long src = 0, dst = 0;
+    if (a0.v) {
+      const int p = a0.key / K;
+      const long long grouped = pl.out_off[p][a0.r] - pl.in_off[a0.r][p];
+      if (D.combine) {
+        src = (long long)(P.out[p] + (grouped + a0.spos) * rb);
+        dst = (long long)(P.in[a0.r] + a0.i * rb);
+      } else {
+        const long long pos = b0 + a0.inr;
+        D.sorted_pos[a0.r][a0.i] = pos;
+        src = (long long)(P.in[a0.r] + (long long)a0.src * rb);
+        dst = (long long)(P.out[p] + (grouped + pos) * rb);
+        if (!in_group(pl, a0.r, p, pos, D.status)) a0.v = false;
+      }
+    }
+    for (int u = 0; u < spb; ++u) {
+      const int s = (int)(issued % NS);
+      if (issued >= NS) bulk_wait_read<NS - LEAD - 1>();  // the store that last read stage s
+      __syncwarp();
+      const int slot = lane - u * unit;
+      const bool mine = a0.v && slot >= 0 && slot < unit;
+      const unsigned held = __ballot_sync(kFull, mine);
+      const unsigned n = __popc(held);
+      const uint32_t bar = bar0 + 8 * s;
+      if (mine) sdst[warp][s][slot] = (unsigned long long)dst;
+      if (lane == 0) {
+        smask[warp][s] = unit == 32 ? held : (held >> (u * unit)) & ((1u << unit) - 1u);
+        const unsigned starve = (P.starve && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
+        mbar_expect_tx(bar, (unsigned)(n * rb) + starve);
+      }
+      __syncwarp();
+      if (mine)
+        bulk_load(st0 + (uint32_t)s * stage_bytes + (uint32_t)(slot * rb),
+                  reinterpret_cast<const void*>(src), (unsigned)rb, bar);
+      ++issued;
+      while (issued - drained > LEAD) {
+        if (!drain(drained)) {
+          ok = false;
+          break;
         }
+        ++drained;
       }
-      const int t = (int)(k & 31);
-      const long long src = __shfl_sync(kFull, msrc, t), dst = __shfl_sync(kFull, mdst, t);
-      if (lane == 0) {
-        const int s = (int)(k % NS);
-        if (k >= NS) bulk_wait_read<NS - LEAD - 1>();
-        sdst[s] = reinterpret_cast<unsigned char*>(dst);
-        mbar_expect_tx(bar0 + 8 * s, (unsigned)rb);
-        bulk_load(stage0 + (uint32_t)s * stage_bytes, reinterpret_cast<const void*>(src),
-                  (unsigned)rb, bar0 + 8 * s);
-      }
-      issued = k + 1;
-    }
-    const long long j = k - LEAD;
-    if (j >= 0 && j < nk) {
-      const int s = (int)(j % NS);
-      if (lane == 0) {
-        ok = mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1));
-        if (ok) bulk_store(sdst[s], stage0 + (uint32_t)s * stage_bytes, (unsigned)rb);
-      }
-      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
-      stored = j + 1;
     }
+    a0 = a1;
+    a1 = a2;
+    b0 = b1;
   }
-  if (lane == 0) {
-    if (!ok) {
+  while (ok && drained < issued) {
+    if (!drain(drained)) {
+      ok = false;
+      break;
+    }
+    ++drained;
+  }
+  if (!ok) {
+    // A stage never completed: report it, give every load still in flight a
+    // bounded chance to land, then leave.
+    if (lane == 0) {
       record_error(P.status, A2AV_ERR_TIMEOUT);
-      for (long long j = stored; j < issued; ++j)
+      for (long long j = drained; j < issued; ++j)
         mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
     }
-    bulk_wait_all();
+    __syncwarp();
+  }
+  bulk_wait_all();
+}
+
+// ------------------------------------------------------------- stream --
+// 16-byte asynchronous copies (cp.async, global -> shared, no registers
+// held while in flight) for 16-byte aligned rows of 16 B .. 2 KiB: a warp
+// takes every (grid x warps)-th batch of bs consecutive items of one rank
+// (lane i item i), loads the batch's rows into one of its two shared-memory
+// buffers -- the rows cut into 16-byte pieces spread over the lanes -- and,
+// while that batch is in flight, writes the previous one from the other
+// buffer to its destinations with st.global.v4.  A warp thus keeps a whole
+// batch (up to 16 KiB) of loads in flight without spending registers on it,
+// and a CTA of up to 16 warps keeps ~96 KiB in flight per SM.  The batch
+// metadata is loaded two and one batches ahead, as in the gather.
+__device__ __forceinline__ void cp_async16(uint32_t smem, const void* g) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(g) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(512, 1)
+    dispatch_stream_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  chain_wait();
+  if (flagged(D)) return;
+  __shared__ Plan pl;
+  extern __shared__ __align__(128) unsigned char stream_bufs[];
+  if (!build_plan(P, pl, kTileGranule)) return;
+  publish_splits(D);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int W = D.W, K = D.K, bs = D.bs;
+  const long long rb = P.rb;
+  const unsigned V = (unsigned)(rb >> 4);  // 16-byte pieces per row
+  const uint32_t half = (uint32_t)(bs * rb);
+  const uint32_t buf0 = smem_u32(stream_bufs) + (uint32_t)warp * 2u * half;
+  const long long WG = (long long)gridDim.x * nw, wg = (long long)blockIdx.x * nw + warp;
+  const long long nbatch = D.batch_first[W];
+  const long long nt = nbatch > wg ? (nbatch - wg + WG - 1) / WG : 0;  // this warp's batches
+  if (nt == 0) return;
+  GatherItem a0 = gather_item(D, wg, lane);
+  GatherItem a1 = gather_item(D, nt > 1 ? wg + WG : -1, lane);
+  long long b0 = a0.v && !D.combine ? key_base(D, a0.r, a0.i, a0.key) : 0;
+  long long pdst = 0;  // the previous batch: this lane's row destination (0: none)
+  unsigned prows = 0;  // and its rows
+  for (long long t = 0; t <= nt; ++t) {
+    long long dst = 0;
+    unsigned rows = 0;
+    GatherItem a2;
+    long long b1 = 0;
+    if (t < nt) {
+      a2 = gather_item(D, t + 2 < nt ? wg + (t + 2) * WG : -1, lane);
+      b1 = a1.v && !D.combine ? key_base(D, a1.r, a1.i, a1.key) : 0;
+      long long src = 0;
+      if (a0.v) {
+        const int p = a0.key / K;
+        const long long grouped = pl.out_off[p][a0.r] - pl.in_off[a0.r][p];
+        if (D.combine) {
+          src = (long long)(P.out[p] + (grouped + a0.spos) * rb);
+          dst = (long long)(P.in[a0.r] + a0.i * rb);
+        } else {
+          const long long pos = b0 + a0.inr;
+          D.sorted_pos[a0.r][a0.i] = pos;
+          src = (long long)(P.in[a0.r] + (long long)a0.src * rb);
+          dst = (long long)(P.out[p] + (grouped + pos) * rb);
+          if (!in_group(pl, a0.r, p, pos, D.status)) src = dst = 0;
+        }
+      }
+      // the batch's rows into buffer t & 1 (rows of lanes without an item skipped)
+      const unsigned held = __ballot_sync(kFull, a0.v);
+      rows = held ? 32u - __clz(held) : 0u;
+      const uint32_t buf = buf0 + (uint32_t)(t & 1) * half;
+      const unsigned total = rows * V;
+#pragma unroll 4
+      for (unsigned base = 0; base < total; base += 32) {  // warp-uniform trip count
+        const unsigned q = base + lane;
+        const unsigned j = q < total ? q / V : 0, c = q - j * V;
+        const long long sj = __shfl_sync(kFull, src, (int)j);
+        if (q < total && sj != 0)
+          cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
+      }
+      cp_async_commit();
+    }
+    if (t > 0) {  // the previous batch, from buffer (t - 1) & 1
+      if (t < nt)
+        cp_async_wait<1>();
+      else
+        cp_async_wait<0>();
+      __syncwarp();
+      const uint32_t pbuf = buf0 + (uint32_t)((t - 1) & 1) * half;
+      const unsigned total = prows * V;
+#pragma unroll 4
+      for (unsigned base = 0; base < total; base += 32) {
+        const unsigned q = base + lane;
+        const unsigned j = q < total ? q / V : 0, c = q - j * V;
+        const long long dj = __shfl_sync(kFull, pdst, (int)j);
+        if (q < total && dj != 0)
+          st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
+      }
+      __syncwarp();  // every lane has read the buffer before the next batch refills it
+    }
+    pdst = dst;
+    prows = rows;
+    a0 = a1;
+    a1 = a2;
+    b0 = b1;
   }
 }
 
-// The two ring shapes: rows up to 16 KiB (16 KiB stages) and up to 32 KiB
-// (half as many 32 KiB stages).
-// The gather's ring: measured on the cfg3 dispatch (14 KiB rows), 12 x 16
-// KiB stages with loads 10 rows ahead beat 8 stages / 6 ahead by 3 % and two
-// CTAs per SM with smaller rings by 4-6 %: bytes in flight per SM decide.
-#ifndef A2AV_GATHER_STAGES
-#define A2AV_GATHER_STAGES 12  // 16 KiB stages of the small ring
+// The gather's ring shapes by row size: NWK x NS stages of IPS slots, at most
+// 192 KiB of shared memory (1 CTA per SM, 4 x 32 KiB .. 12 x 16 KiB of loads
+// in flight per SM).
+#ifndef A2AV_GATHER_NS
+#define A2AV_GATHER_NS 6
 #endif
 #ifndef A2AV_GATHER_LEAD
-#define A2AV_GATHER_LEAD 10
+#define A2AV_GATHER_LEAD 4
 #endif
-#ifndef A2AV_GATHER_CTAS_PER_SM
-#define A2AV_GATHER_CTAS_PER_SM 1
-#endif
-// Rows of at most 8 KiB go through 8 KiB stages, several warps issuing at
-// once, each with its own ring (one lane issuing every row was the limit:
-// ~480 ns a row whatever its size).  Measured on the MoE dispatch (8192
-// tokens, top-2, W=8, us): 2 / 4 KiB rows 113 / 154 with four warps x 6
-// stages (two warps x 12: 193 / 197; the warp copy: 141 / 263); 8 KiB rows 279
-// with two warps x 12 stages (four x 6: 300; one warp, 16 KiB stages: 411).
-constexpr int kGatherTinyStage = 8 * 1024;
-constexpr int kGatherSmallStage = 16 * 1024, kGatherLargeStage = 32 * 1024;
-using GatherKernel = void (*)(Params, DispatchParams, int);
-const GatherKernel kGatherTiny4 = dispatch_copy_bulk_kernel<6, 4, 4>;    // rows <= 4 KiB
-const GatherKernel kGatherTiny2 = dispatch_copy_bulk_kernel<12, 10, 2>;  // rows <= 8 KiB
-// 8..16 KiB rows: one issuing warp, 12 x 16 KiB (two warps x 6: 2-4 % slower).
-const GatherKernel kGatherSmall = dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES, A2AV_GATHER_LEAD, 1>;
-// Few items per CTA (decode-size dispatches) of 8..16 KiB rows: four warps x
-// 3 x 16 KiB, so that a CTA's handful of rows are issued four at a time
-// (14 KiB rows, 128 / 512 tokens a rank: 26.3 / 44.0 -> 25.2 / 41.8 us; no
-// gain for 8 KiB rows, which keep the two-warp ring).
-#ifndef A2AV_GATHER_FEW_ITEMS
-#define A2AV_GATHER_FEW_ITEMS 64  // items per CTA at or below which the four-warp ring is used
-#endif
-const GatherKernel kGatherSmallFew = dispatch_copy_bulk_kernel<3, 1, 4>;
-const GatherKernel kGatherLarge =
-    dispatch_copy_bulk_kernel<A2AV_GATHER_STAGES / 2, (A2AV_GATHER_LEAD + 1) / 2 - 1 >= 1
-                                                          ? (A2AV_GATHER_LEAD + 1) / 2 - 1
-                                                          : 1, 1>;
-constexpr int kGatherSmem = A2AV_GATHER_STAGES * kGatherSmallStage;
-static_assert(4 * 6 * kGatherTinyStage <= kGatherSmem && 2 * 12 * kGatherTinyStage <= kGatherSmem,
-              "the 8 KiB rings fit the same shared memory");
-static_assert(kGatherSmem <= 192 * 1024, "shared memory per CTA");
-static_assert(A2AV_GATHER_STAGES % 2 == 0 && A2AV_GATHER_LEAD < A2AV_GATHER_STAGES,
-              "the large ring halves the small one");
-// Aligned rows this long or longer take the bulk gather; shorter ones the
-// warp copy's flat vector runs.  Measured on the MoE dispatch (8192 tokens,
-// top-2, W=8): 1 KiB rows 78 us by warp copy against 117 by the gather; from
-// 2 KiB the gather wins (above); 14 KiB rows 459 us against 868 by warp copy.
 #ifndef A2AV_GATHER_MIN_ROW
-#define A2AV_GATHER_MIN_ROW 2048
+#define A2AV_GATHER_MIN_ROW 2048  // aligned rows this long or longer take the gather
 #endif
+constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
+constexpr long long kGatherMaxRow = 32 * 1024;
+constexpr int kGatherSmem = 192 * 1024;
+#ifndef A2AV_STREAM_MAX_ROW
+#define A2AV_STREAM_MAX_ROW 2048  // aligned rows up to this long take the stream copy
+#endif
+constexpr long long kStreamMaxRow = A2AV_STREAM_MAX_ROW;
+constexpr long long kStreamFlight = 96 * 1024;  // bytes of loads in flight per CTA
+constexpr int kStreamSmem = 192 * 1024;
+using GatherKernel = void (*)(Params, DispatchParams);
+struct GatherShape {
+  long long max_row;
+  GatherKernel kernel;
+  int nwk, ns, ips;
+};
+#ifndef A2AV_GATHER_LANES
+#define A2AV_GATHER_LANES 0  // 1: every lane issues its own row's copy (slower, measured)
+#endif
+const GatherShape kGatherShapes[] = {
+#if A2AV_GATHER_LANES
+    {256, dispatch_gather_kernel<kGatherNs, kGatherLead, 4, 32>, 4, kGatherNs, 32},
+    {512, dispatch_gather_kernel<kGatherNs, kGatherLead, 2, 32>, 2, kGatherNs, 32},
+    {1024, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 32>, 1, kGatherNs, 32},
+    {2048, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 16>, 1, kGatherNs, 16},
+    {4096, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 8>, 1, kGatherNs, 8},
+    {8192, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 4>, 1, kGatherNs, 4},
+#else
+    // one row a stage, one issuing lane per warp, several warps with rings of
+    // their own (MoE dispatch, 8192 tokens, W=8: 2 / 4 KiB rows 113 / 154 us
+    // with four warps x 6 stages; 8 KiB rows 279 us with two warps x 12)
+    {4096, dispatch_gather_kernel<6, 4, 4, 1>, 4, 6, 1},
+    {8192, dispatch_gather_kernel<12, 10, 2, 1>, 2, 12, 1},
+#endif
+    // 14 KiB MoE rows: 12 x 16 KiB stages, loads 10 ahead (measured best for
+    // a one-row ring: 8 stages / 6 ahead 3 % slower, two CTAs an SM 4-6 %)
+    {16384, dispatch_gather_kernel<12, 10, 1, 1>, 1, 12, 1},
+    {32768, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 1>, 1, kGatherNs, 1},
+};
+static_assert(4 * 6 * 4096 <= kGatherSmem && 2 * 12 * 8192 <= kGatherSmem &&
+                  12 * 16384 <= kGatherSmem && kGatherNs * 32768 <= kGatherSmem,
+              "every ring fits the gather's shared memory");
 
+// ------------------------------------------------------------ one kernel --
+// Decode-size batches: at most kTinyItems items over all ranks.  Every CTA
+// reads every key, so all reach the same verdict and the same plan without
+// any exchange between CTAs; CTA b then places and copies the items
+// [b n / G, (b + 1) n / G) of the global item order (at most kTinyOwn).
+constexpr int kTinyThreads = 256;
+constexpr int kTinyItems = 4096;
+constexpr int kTinyCounts = 2048;  // W * W * K counters in shared memory
+constexpr int kTinyOwn = 64;
+constexpr int kTinySlotBytes = 176 * 1024;  // dynamic shared memory for row slots
 
+// The CTA's c rows (addresses listed in shared memory), 16-byte aligned:
+// warp 0 copies them through `slots` shared-memory slots with cp.async.bulk,
+// min(32, slots) rows a round (a lane per row, one mbarrier); with slots == 0
+// every warp copies with registers (a warp per row from 64 bytes, a thread
+// per row below).  The bounded wait records A2AV_ERR_TIMEOUT and waits
+// (bounded) for the round's loads before leaving.
+__device__ void copy_listed_rows(const unsigned long long* src, const unsigned long long* dst,
+                                 int c, long long rb, int slots, uint32_t slot0, uint32_t bar,
+                                 int* status) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (slots == 0) {
+    // (dst 0: a row the position check dropped)
+    if (rb >= kWarpRowBytes) {
+      for (int x = warp; x < c; x += kTinyThreads / 32)
+        if (dst[x] != 0)
+          copy_span<32, 4, 2>(reinterpret_cast<unsigned char*>(dst[x]),
+                              reinterpret_cast<const unsigned char*>(src[x]), rb, lane);
+    } else {
+      for (int x = tid; x < c; x += kTinyThreads)
+        if (dst[x] != 0)
+          copy_row_thread(reinterpret_cast<unsigned char*>(dst[x]),
+                          reinterpret_cast<const unsigned char*>(src[x]), rb);
+    }
+    return;
+  }
+  if (warp != 0 || c == 0) return;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  const int per = slots < 32 ? slots : 32;
+  unsigned phase = 0;
+  for (int base = 0; base < c; base += per) {
+    const int nr = c - base < per ? c - base : per;
+    if (base > 0) bulk_wait_read<0>();  // the previous round's stores have read their slots
+    __syncwarp();
+    if (lane == 0) mbar_expect_tx(bar, (unsigned)(nr * rb));
+    __syncwarp();
+    if (lane < nr)
+      bulk_load(slot0 + (uint32_t)(lane * rb), reinterpret_cast<const void*>(src[base + lane]),
+                (unsigned)rb, bar);
+    if (!mbar_wait_warp(bar, phase)) {
+      if (lane == 0) {
+        record_error(status, A2AV_ERR_TIMEOUT);
+        mbar_wait(bar, phase);
+      }
+      __syncwarp();
+      break;
+    }
+    phase ^= 1;
+    if (lane < nr && dst[base + lane] != 0)  // (0: a row the position check dropped)
+      bulk_store(reinterpret_cast<void*>(dst[base + lane]), slot0 + (uint32_t)(lane * rb),
+                 (unsigned)rb);
+    else
+      bulk_commit();
+  }
+  bulk_wait_all();
+}
+
+// This CTA's share [a, e) of the n items (global order, rank-major).
+__device__ __forceinline__ void tiny_share(const DispatchParams& D, long long* a, long long* e) {
+  const long long n = D.item_first[D.W];
+  *a = (long long)blockIdx.x * n / gridDim.x;
+  *e = (long long)(blockIdx.x + 1) * n / gridDim.x;
+}
+
+__global__ void __launch_bounds__(kTinyThreads, 1)
+    dispatch_tiny_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D,
+                         int slots) {
+  chain_release();
+  chain_wait();
+  __shared__ Plan pl;
+  __shared__ int cnt[kTinyCounts];  // [r][key]: counts, then the rank's key starts
+  __shared__ int run[kMaxBins];     // running count of each key while placing
+  __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
+  __shared__ alignas(8) unsigned long long bar;
+  extern __shared__ __align__(128) unsigned char slot_mem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int W = D.W, K = D.K, NB = W * K;
+  long long a, e;
+  tiny_share(D, &a, &e);
+  int ra = 0;  // the rank of item a
+  while (ra + 1 < W && D.item_first[ra + 1] <= a) ++ra;
+  const long long ia = a - D.item_first[ra];
+  for (int x = tid; x < W * NB; x += kTinyThreads) cnt[x] = 0;
+  for (int x = tid; x < NB; x += kTinyThreads) run[x] = 0;
+  __syncthreads();
+  // every item: validity, its rank's key counts, and for rank ra the counts
+  // of the items before this CTA's share
+  int bad = 0;
+  for (int r = 0; r < W; ++r) {
+    const long long m = D.items[r];
+    for (long long i0 = 0; i0 < m; i0 += 4 * kTinyThreads) {
+      int k[4], s[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long i = i0 + q * kTinyThreads + tid;
+        k[q] = i < m ? D.key[r][i] : 0;
+        s[q] = i < m ? D.src[r][i] : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long i = i0 + q * kTinyThreads + tid;
+        if (i >= m) continue;
+        if (k[q] < 0 || k[q] >= NB || s[q] < 0 || s[q] >= D.rows[r]) {
+          bad = 1;
+          continue;
+        }
+        atomicAdd(&cnt[r * NB + k[q]], 1);
+        if (r == ra && i < ia) atomicAdd(&run[k[q]], 1);
+      }
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
+    return;
+  }
+  // per rank: key starts (exclusive scan in place) and S[r][*]
+  for (int r = warp; r < W; r += kTinyThreads / 32) {
+    int carry = 0;
+    for (int k0 = 0; k0 < NB; k0 += 32) {
+      const int k = k0 + lane;
+      const int x = k < NB ? cnt[r * NB + k] : 0;
+      const int inc = (int)warp_inclusive_scan(x, lane);
+      if (k < NB) cnt[r * NB + k] = carry + inc - x;
+      carry += __shfl_sync(kFull, inc, 31);
+    }
+    __syncwarp();
+    for (int p = lane; p < W; p += 32) {
+      const long long hi = p + 1 < W ? cnt[r * NB + (p + 1) * K] : D.items[r];
+      pl.s[r][p] = hi - cnt[r * NB + p * K];
+    }
+  }
+  __syncthreads();
+  int over = 0;
+  for (int x = tid; x < W * W; x += kTinyThreads)
+    if (pl.s[x / W][x % W] > P.limit) over = 1;
+  if (__syncthreads_or(over)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_SPLITS);
+    return;
+  }
+  if (!plan_from_splits(P, pl, kTileGranule, blockIdx.x, gridDim.x)) return;
+  if (blockIdx.x == 0 && D.in_splits_out != nullptr)
+    for (int x = tid; x < W * W; x += kTinyThreads) D.in_splits_out[x] = pl.s[x / W][x % W];
+  // place the CTA's items, rank by rank, 32 at a time (warp 0)
+  const long long rb = P.rb;
+  if (warp == 0) {
+    const unsigned lt = (1u << lane) - 1u;
+    int idx = 0, r = ra;
+    for (long long g = a; g < e;) {
+      while (D.item_first[r + 1] <= g) ++r;
+      const long long seg_end = e < D.item_first[r + 1] ? e : D.item_first[r + 1];
+      if (r != ra) {  // a later rank starts at its first item
+        for (int k = lane; k < NB; k += 32) run[k] = 0;
+        __syncwarp();
+      }
+      for (long long g0 = g; g0 < seg_end; g0 += 32) {
+        const long long gi = g0 + lane;
+        const bool v = gi < seg_end;
+        const long long i = gi - D.item_first[r];
+        const int key = v ? D.key[r][i] : -1 - lane;
+        const int s = v ? D.src[r][i] : 0;
+        const unsigned same = __match_any_sync(kFull, key);
+        long long pos = 0;
+        if (v) pos = (long long)cnt[r * NB + key] + run[key] + __popc(same & lt);
+        __syncwarp();
+        if (v && lane == 31 - __clz(same)) run[key] += __popc(same);
+        __syncwarp();
+        if (v) {
+          const int p = key / K;
+          D.sorted_pos[r][i] = pos;
+          const bool ok = in_group(pl, r, p, pos, D.status);
+          own_dst[idx + lane] =
+              ok ? (unsigned long long)(P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pos) * rb)
+                 : 0ull;
+          own_src[idx + lane] = (unsigned long long)(P.in[r] + (long long)s * rb);
+        }
+        idx += (int)(seg_end - g0 < 32 ? seg_end - g0 : 32);
+      }
+      g = seg_end;
+    }
+  }
+  __syncthreads();
+  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(&bar),
+                   D.status);
+}
+
+// The fused combine in one kernel (decode sizes): every CTA checks the split
+// matrix (the a2av prologue) and every item's key and position, then copies
+// its own share of the items' rows back to their item rows.
+__global__ void __launch_bounds__(kTinyThreads, 1)
+    combine_tiny_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D,
+                        int slots) {
+  __shared__ Plan pl;
+  __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
+  __shared__ alignas(8) unsigned long long bar;
+  extern __shared__ __align__(128) unsigned char slot_mem[];
+  if (!build_plan(P, pl, kTileGranule)) return;  // (waits for the previous kernel first)
+  const int tid = threadIdx.x, W = D.W, K = D.K, NB = W * K;
+  int bad = 0;
+  for (int r = 0; r < W; ++r) {
+    const long long m = D.items[r];
+    for (long long i0 = 0; i0 < m; i0 += 4 * kTinyThreads) {
+      int k[4];
+      long long pos[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long i = i0 + q * kTinyThreads + tid;
+        k[q] = i < m ? D.key[r][i] : 0;
+        pos[q] = i < m ? D.sorted_pos[r][i] : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long i = i0 + q * kTinyThreads + tid;
+        if (i >= m) continue;
+        if (k[q] < 0 || k[q] >= NB) {
+          bad = 1;
+          continue;
+        }
+        const int p = k[q] / K;
+        const long long lo = pl.in_off[r][p];
+        if (pos[q] < lo || pos[q] >= lo + pl.s[r][p]) bad = 1;
+      }
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
+    return;
+  }
+  long long a, e;
+  tiny_share(D, &a, &e);
+  const long long rb = P.rb;
+  for (long long g = a + tid; g < e; g += kTinyThreads) {
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    const long long i = g - D.item_first[r];
+    const int p = D.key[r][i] / K;
+    const long long pos = D.sorted_pos[r][i];
+    own_src[g - a] =
+        (unsigned long long)(P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pos) * rb);
+    own_dst[g - a] = (unsigned long long)(P.in[r] + i * rb);
+  }
+  __syncthreads();
+  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(&bar),
+                   D.status);
+}
+
+// Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
+// cleared before every dispatch that uses them; then S, key starts, key
+// totals, inrank bytes, range prefixes, group counts.
 struct Layout {
-  long long flag, done, S, key_start, key_total, pos, hist, grp, total;
+  long long flag, done, S, key_start, key_total, inrank, hist, grp, total;
 };
 
 Layout layout(int W, int K, long long max_items) {
   auto up = [](long long x) { return (x + 255) / 256 * 256; };
   const long long NB = (long long)W * K;
   const long long ranges = (max_items + kRange - 1) / kRange;
+  const long long groups = (ranges + kCountWarps - 1) / kCountWarps;  // groups of 8 ranges at most
   Layout L;
   L.flag = 0;
   L.done = 4;
   L.S = 256;
   L.key_start = L.S + up(8LL * W * W);
   L.key_total = L.key_start + up(8LL * W * NB);
-  L.pos = L.key_total + up(8LL * W * NB);
-  const long long groups = (ranges + kCountWarps - 1) / kCountWarps;
-  L.hist = L.pos + up(4LL * W * (max_items < 1 ? 1 : max_items));
+  L.inrank = L.key_total + up(8LL * W * NB);
+  L.hist = L.inrank + up((long long)W * (max_items < 1 ? 1 : max_items));
   L.grp = L.hist + up(4LL * W * (ranges < 1 ? 1 : ranges) * NB);
   L.total = L.grp + up(4LL * W * (groups < 1 ? 1 : groups) * NB);
   return L;
@@ -952,39 +1438,115 @@ extern "C" int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_pe
 
 namespace {
 
+// Shared-memory opt-in of the gather and one-kernel paths, once per handle
+// (a host call per launch otherwise).
+cudaError_t prepare_kernels(a2av_handle* h) {
+  if (h->gather_ready) return cudaSuccess;
+  for (const GatherShape& g : kGatherShapes)
+    if (cudaFuncSetAttribute(g.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
+        cudaSuccess)
+      return cudaErrorInvalidValue;
+  // (count histograms: 8 ranges a warp x 4 x W * K ints, up to 128 KiB)
+  if (cudaFuncSetAttribute(dispatch_count_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCountWarps * 4 * kMaxBins * (int)sizeof(int)) != cudaSuccess ||
+      cudaFuncSetAttribute(dispatch_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kStreamSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(dispatch_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTinySlotBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(combine_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTinySlotBytes) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  h->gather_ready = true;
+  return cudaSuccess;
+}
+
+// Row slots of the one-kernel paths: 0 (register copies) unless every row
+// and buffer is 16-byte aligned and a row fits the slot memory.
+int tiny_slots(const DispatchParams& D, long long rb) {
+  if (!D.vec16 || rb < kWarpRowBytes || rb > kTinySlotBytes) return 0;
+  const long long n = kTinySlotBytes / rb;
+  return (int)(n < 32 ? n : 32);
+}
+
+// One-kernel path: at most kTinyItems items, their counts fit shared memory,
+// and no CTA gets more than kTinyOwn of them.
+bool tiny_fits(const a2av_handle* h, const DispatchParams& D) {
+  const long long n = D.item_first[D.W];
+  return n <= kTinyItems && (long long)D.W * D.W * D.K <= kTinyCounts &&
+         (long long)h->sms * kTinyOwn >= n;
+}
+
+int tiny_grid(const a2av_handle* h, const DispatchParams& D) {
+  const long long n = D.item_first[D.W];
+  return (int)(n < 1 ? 1 : (n < h->sms ? n : h->sms));
+}
+
+// What the last dispatch or combine enqueued (a2av_last_dispatch).
+void record_chain(a2av_handle* h, int kernels, int memsets, const char* copy) {
+  h->last_kernels = kernels;
+  h->last_memsets = memsets;
+  h->last_copy = copy;
+}
+
 // The row copy of a dispatch or a combine: the cp.async.bulk gather for
-// 16-byte aligned rows of 2..32 KiB (its ring chosen by row size and by the
-// items per CTA), else the warp copy (rows of 64 bytes or more) or the
-// thread copy.
-cudaError_t launch_copy(a2av_handle* h, const Params& P, const DispatchParams& D,
-                        long long row_bytes, cudaStream_t s) {
-  const bool aligned = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherLargeStage;
-  if (!aligned) {
+// 16-byte aligned rows of kGatherMinRow .. 32 KiB (its ring by row size),
+// else the warp copy (rows of 64 bytes or more) or the thread copy.
+cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long long row_bytes,
+                        cudaStream_t s, const char** name) {
+  if (D.vec16 && row_bytes >= 16 && row_bytes <= kStreamMaxRow) {
+    const cudaError_t e = prepare_kernels(h);
+    if (e != cudaSuccess) return e;
+    // batches of at most 16 KiB (32, 16 or 8 items, fewer when that leaves
+    // some warps without four), warps so that ~96 KiB are in flight per SM
+    int bs = 32;
+    while (bs > 8 && bs * row_bytes > 16384) bs >>= 1;
+    const long long batch_bytes = bs * row_bytes;
+    int nw = (int)(kStreamFlight / batch_bytes);
+    nw = nw < 1 ? 1 : (nw > 16 ? 16 : nw);
+    const size_t smem = (size_t)nw * 2 * batch_bytes;  // <= 2 x kStreamFlight = kStreamSmem
+    const long long warps = (long long)h->sms * nw;  // one CTA per SM
+    for (;;) {
+      long long nb = 0;
+      for (int r = 0; r < D.W; ++r) nb += (D.items[r] + bs - 1) / bs;
+      if (bs == 8 || nb >= 4 * warps) break;
+      bs >>= 1;
+    }
+    D.bs = bs;
+    D.batch_first[0] = 0;
+    for (int r = 0; r < D.W; ++r)
+      D.batch_first[r + 1] = D.batch_first[r] + (D.items[r] + bs - 1) / bs;
+    *name = "dispatch_stream_kernel";
+    return launch_kernel(dispatch_stream_kernel, dim3(h->sms), 32 * nw, smem, s, true, P, D);
+  }
+  const bool gather = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherMaxRow;
+  if (!gather) {
+    *name = "dispatch_copy_kernel";
     if (row_bytes < kWarpRowBytes)
       return launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
                            kCopyThreads, 0, s, true, P, D);
-    if (D.combine && D.vec16 && row_bytes <= kVecMaxRow)
-      return launch_kernel(dispatch_copy_kernel<true, kVecRowsWide>,
-                           dim3(h->sms * kCopyCtasPerSmWide), kCopyThreads, 0, s, true, P, D);
     return launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
                          kCopyThreads, 0, s, true, P, D);
   }
-  const bool tiny = row_bytes <= kGatherTinyStage, small = row_bytes <= kGatherSmallStage;
-  const bool few = D.item_first[D.W] <= (long long)A2AV_GATHER_FEW_ITEMS *
-                                             (h->sms * A2AV_GATHER_CTAS_PER_SM);
-  const GatherKernel k = row_bytes <= 4096 ? kGatherTiny4
-                         : tiny            ? kGatherTiny2
-                         : small           ? (few ? kGatherSmallFew : kGatherSmall)
-                                           : kGatherLarge;
-  if (!h->gather_ready) {  // shared-memory opt-in, once per handle (a host call per launch otherwise)
-    for (GatherKernel g : {kGatherTiny4, kGatherTiny2, kGatherSmall, kGatherSmallFew, kGatherLarge})
-      if (cudaFuncSetAttribute(g, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
-          cudaSuccess)
-        return cudaErrorInvalidValue;
-    h->gather_ready = true;
+  *name = "dispatch_gather_kernel";
+  const cudaError_t e = prepare_kernels(h);
+  if (e != cudaSuccess) return e;
+  const GatherShape* g = &kGatherShapes[0];
+  while (g->max_row < row_bytes) ++g;
+  // Batches of 32 items, or of 16 / 8 when that gives every warp at least
+  // four (balance for mid-size batches).
+  const long long warps = (long long)h->sms * g->nwk;
+  int bs = 32;
+  for (;;) {
+    long long nb = 0;
+    for (int r = 0; r < D.W; ++r) nb += (D.items[r] + bs - 1) / bs;
+    if (bs == 8 || nb >= 4 * warps) break;
+    bs >>= 1;
   }
-  return launch_kernel(k, dim3(h->sms * A2AV_GATHER_CTAS_PER_SM), 128, kGatherSmem, s, true, P, D,
-                       tiny ? kGatherTinyStage : small ? kGatherSmallStage : kGatherLargeStage);
+  D.bs = bs;
+  D.batch_first[0] = 0;
+  for (int r = 0; r < D.W; ++r) D.batch_first[r + 1] = D.batch_first[r] + (D.items[r] + bs - 1) / bs;
+  const size_t smem = (size_t)g->nwk * g->ns * g->ips * row_bytes;
+  return launch_kernel(g->kernel, dim3(h->sms), 32 * g->nwk, smem, s, true, P, D);
 }
 
 }  // namespace
@@ -1039,24 +1601,21 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   D.S = reinterpret_cast<long long*>(ws + L.S);
   D.key_start = reinterpret_cast<long long*>(ws + L.key_start);
   D.key_total = reinterpret_cast<long long*>(ws + L.key_total);
-  D.pos = reinterpret_cast<int*>(ws + L.pos);
+  D.inrank = ws + L.inrank;
   D.pos_stride = max_items < 1 ? 1 : max_items;
   D.hist = reinterpret_cast<int*>(ws + L.hist);
   D.grp = reinterpret_cast<int*>(ws + L.grp);
   D.status = h->d_status;
   D.in_splits_out = reinterpret_cast<long long*>(in_splits_dev);
   D.ranges_max = ranges_max;
-  D.groups_max = (ranges_max + kCountWarps - 1) / kCountWarps;
   D.W = W;
   D.K = K;
-  // One count CTA per rank scans its groups when a thread's share of one key
-  // fits kFuseScanPer registers; the scan kernel and its launch are skipped.
-  const int slices = kScanThreads / (W * K);
-  D.fuse_scan = slices > 0 && D.groups_max <= (long long)kFuseScanPer * slices;
+  // (16-byte vectors and cp.async.bulk only on aligned device memory; rows in
+  // host memory are copied with plain loads and stores)
   bool vec16 = row_bytes % 16 == 0;
   for (int r = 0; r < W; ++r)
     vec16 = vec16 && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
-  D.vec16 = vec16 ? 1 : 0;
+  D.vec16 = vec16 && a2av_device_buffers(h, rows_ptrs, W, out_ptrs, W) ? 1 : 0;
 
   Params P;
   std::memset(&P, 0, sizeof(P));
@@ -1073,42 +1632,67 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   P.in_cap = 0;  // sources are checked by row index in the count kernel
   P.out_cap = h->out_cap;
   P.W = W;
+  P.starve = h->starve;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tiny_fits(h, D)) {  // decode sizes: one kernel, no workspace
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    const int slots = tiny_slots(D, row_bytes);
+    e = launch_kernel(dispatch_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads,
+                      (size_t)slots * row_bytes, s, h->pdl, P, D, slots);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+    record_chain(h, 1, 0, "dispatch_tiny_kernel");
+    return A2AV_OK;
+  }
+  const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
+  // Four ranges a count warp when even then every SM gets a count CTA.
+  const int rw = !small_path && (long long)W * ((ranges_max + 31) / 32) >= h->sms ? 4 : 1;
+  D.group_log2 = rw == 4 ? 5 : 3;
+  D.groups_max = (ranges_max + (1LL << D.group_log2) - 1) >> D.group_log2;
+  // One count CTA per rank scans its groups when a thread's share of one key
+  // stays short; the scan kernel and its launch are skipped.
+  const int slices = kScanThreads / (W * K);
+  D.fuse_scan = small_path || (slices > 0 && D.groups_max <= (long long)kFuseScanMax * slices);
+
   static_assert(4 + 4 * kMaxW <= 256, "flag and done counters fit the first 256 bytes");
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
   // Every kernel of the chain is launched with programmatic stream
   // serialization: it may be scheduled while its predecessor runs and waits
   // for that predecessor's results in chain_wait.
-  cudaError_t e;
-  const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
-  const bool fuse = !small_path && row_bytes < kWarpRowBytes;  // rank kernel copies the rows
   if (small_path) {
     e = launch_kernel(dispatch_small_kernel, dim3(W), kScanThreads, 0, s, h->pdl, D);
   } else {
     // (at least one CTA per rank: a batch without items still gets its
     // counts, splits and offsets written)
-    const long long ranges = ranges_max > 0 ? ranges_max : 1;
-    const dim3 grid((unsigned)ranges, (unsigned)W);
-    const dim3 grid_count((unsigned)((ranges + kCountWarps - 1) / kCountWarps), (unsigned)W);
-    e = launch_kernel(dispatch_count_kernel, grid_count, 32 * kCountWarps,
-                      (size_t)kCountWarps * W * K * sizeof(int), s, h->pdl, D);
+    const long long groups = D.groups_max > 0 ? D.groups_max : 1;
+    const size_t hist_smem = (size_t)kCountWarps * rw * W * K * sizeof(int);
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    if (rw == 4)
+      e = launch_kernel(dispatch_count_kernel<4>, dim3((unsigned)groups, (unsigned)W),
+                        32 * kCountWarps, hist_smem, s, h->pdl, D);
+    else
+      e = launch_kernel(dispatch_count_kernel<1>, dim3((unsigned)groups, (unsigned)W),
+                        32 * kCountWarps, hist_smem, s, h->pdl, D);
     if (e == cudaSuccess && !D.fuse_scan)
       e = launch_kernel(dispatch_scan_kernel, dim3((unsigned)(W * K), (unsigned)W), kScanThreads,
                         0, s, true, D);
-    if (e == cudaSuccess && fuse) {
-      const dim3 grid2((unsigned)((ranges + kRankCopyWarps - 1) / kRankCopyWarps),
-                       (unsigned)W);
-      e = launch_kernel(dispatch_rank_copy_kernel, grid2, 32 * kRankCopyWarps, 0, s, true, P, D);
+    if (e == cudaSuccess && row_bytes < kWarpRowBytes) {  // place and copy in one kernel
+      const long long ranges = ranges_max > 0 ? ranges_max : 1;
+      const dim3 grid2((unsigned)((ranges + kPlaceWarps - 1) / kPlaceWarps), (unsigned)W);
+      e = launch_kernel(dispatch_place_copy_kernel, grid2, 32 * kPlaceWarps,
+                        (size_t)kPlaceWarps * W * K * sizeof(int), s, true, P, D);
       if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+      record_chain(h, D.fuse_scan ? 2 : 3, 1, "dispatch_place_copy_kernel");
       return A2AV_OK;
     }
-    if (e == cudaSuccess) e = launch_kernel(dispatch_rank_kernel, grid, 32, 0, s, true, D);
   }
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
-  e = launch_copy(h, P, D, row_bytes, s);
+  const char* copy = nullptr;
+  e = launch_copy(h, P, D, row_bytes, s, &copy);
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  record_chain(h, small_path || D.fuse_scan ? 2 : 3, 1, copy);
   return A2AV_OK;
 }
 
@@ -1156,7 +1740,7 @@ extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
   bool vec16 = row_bytes % 16 == 0;
   for (int r = 0; r < W; ++r)
     vec16 = vec16 && ((uintptr_t)peer_ptrs[r] & 15) == 0 && ((uintptr_t)item_out_ptrs[r] & 15) == 0;
-  D.vec16 = vec16 ? 1 : 0;
+  D.vec16 = vec16 && a2av_device_buffers(h, peer_ptrs, W, item_out_ptrs, W) ? 1 : 0;
 
   // Rank-side buffers (the items' rows, written) in P.in, peer-side buffers
   // (the dispatch layout, read) in P.out: the prologue's checks and offsets
@@ -1176,13 +1760,35 @@ extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
   P.in_cap = 0;
   P.out_cap = 0;
   P.W = W;
+  P.starve = h->starve;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (tiny_fits(h, D)) {  // decode sizes: one kernel, no flag
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    const int slots = tiny_slots(D, row_bytes);
+    e = launch_kernel(combine_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads,
+                      (size_t)slots * row_bytes, s, h->pdl, P, D, slots);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+    record_chain(h, 1, 0, "combine_tiny_kernel");
+    return A2AV_OK;
+  }
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
-  cudaError_t e = launch_kernel(combine_check_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads,
-                                0, s, h->pdl, P, D);
+  e = launch_kernel(combine_check_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s,
+                    h->pdl, P, D);
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
-  e = launch_copy(h, P, D, row_bytes, s);
+  const char* copy = nullptr;
+  e = launch_copy(h, P, D, row_bytes, s, &copy);
   if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+  record_chain(h, 2, 1, copy);
+  return A2AV_OK;
+}
+
+extern "C" int a2av_last_dispatch(const a2av_handle* h, int* kernels, int* memsets,
+                                  const char** copy_kernel) {
+  if (h == nullptr) return A2AV_ERR_INVALID_ARG;
+  if (kernels) *kernels = h->last_kernels;
+  if (memsets) *memsets = h->last_memsets;
+  if (copy_kernel) *copy_kernel = h->last_copy;
   return A2AV_OK;
 }
