@@ -184,13 +184,14 @@ def hbm_peak():
 
 
 # The sources each family of kernels is compiled from: the fused dispatch's
-# kernels live in dispatch.cu, every other kernel in a2av.cu; both include the
+# and fused combine's kernels (dispatch_*, combine_*) live in dispatch.cu,
+# every other kernel in a2av.cu; both include the
 # shared device header and the C header (a2av_handle.h is host-only).
 _SHARED_SOURCES = ["variable_size_all_gb300/csrc/a2av_device.cuh", "include/a2av.h"]
 
 
 def kernel_sources(kernel: str) -> list:
-    own = "dispatch.cu" if kernel.startswith("dispatch_") else "a2av.cu"
+    own = "dispatch.cu" if kernel.startswith(("dispatch_", "combine_")) else "a2av.cu"
     return [f"variable_size_all_gb300/csrc/{own}"] + _SHARED_SOURCES
 
 
@@ -324,18 +325,27 @@ def host_memory_available() -> int:
     return 0
 
 
+def host_bytes_needed(args, world: int) -> int:
+    """Pinned host memory all local ranks hold for the cfg2 line: each rank's
+    inputs (the e2e sources) and the e2e outputs, W buffers of P bytes each."""
+    return world * 2 * W * args.per_rank_bytes
+
+
 def load_workload(args, torch):
-    """The workload's inputs in pinned host memory (also the e2e sources)."""
+    """The workload's inputs in pinned host memory (also the e2e sources).
+    The payload is never reduced to fit: a host without room for every local
+    rank's buffers is refused with the numbers."""
     import workloads as wl
     if args.workload == "cfg2":
         P = args.per_rank_bytes
-        # Several ranks on one node each pin their inputs and outputs: keep
-        # the payload within half of the host memory available to them.
         _, _, world = dist_env()
         avail = host_memory_available()
-        while avail and world * 4 * W * P > avail // 2 and P > (1 << 26):
-            P //= 2
-        args.per_rank_bytes = P
+        need = host_bytes_needed(args, world)
+        if avail and need > 0.85 * avail:
+            raise SystemExit(f"bench.py: {world} rank(s) at {P / 2**30:g} GiB per emulated rank "
+                             f"need {need / 2**30:.0f} GiB of pinned host memory (inputs and e2e "
+                             f"outputs); {avail / 2**30:.0f} GiB available. Refusing rather than "
+                             f"running a smaller configuration.")
         nbytes = (P // ROW_BYTES) * ROW_BYTES
         h_in = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=True) for _ in range(W)]
         w = wl.cfg2(P, seed=args.seed, buffers=[t.numpy() for t in h_in])
@@ -349,7 +359,11 @@ def load_workload(args, torch):
     return w, h_in
 
 
-def run_ours(args):
+def run_ours(args, light=False):
+    """One exchange workload (a2av_run, or a2av_combine with --op combine).
+    Returns the JSON line.  ``light``: the timed steps, the roofline and a
+    full bit-exact check against the oracle only (an entry of the cfg2 line's
+    ``configs`` block)."""
     import torch
     import variable_size_all_gb300 as a2av
     import workloads as wl
@@ -437,7 +451,7 @@ def run_ours(args):
     # ---- launch cost: eager calls vs one captured CUDA graph replayed -----
     # (back to back, no flush: what a caller issuing many small exchanges pays)
     graph_us = eager_us = None
-    if cold and world == 1:
+    if cold and world == 1 and not light:
         g_stream = torch.cuda.Stream()
         g_stream.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -477,27 +491,40 @@ def run_ours(args):
                 "traffic": measured_traffic(f"{kname}:{args.workload}", algo),
                 "algorithmic_bytes_per_launch": algo}
 
-    # ---- device-to-device memcpy ceiling for the same bytes ---------------
-    src = torch.cat([t for t in d_in])
-    dst = torch.empty_like(src)
-    for _ in range(3):
-        dst.copy_(src)
-    d2d = []
-    for _ in range(5):
-        if cold:
-            flush.sum()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        dst.copy_(src)
-        b.record(stream)
-        b.synchronize()
-        d2d.append(a.elapsed_time(b) / 1e3)
-    d2d_gbps = src.numel() / statistics.median(d2d) / 1e9
-    del src, dst
+    # ---- the same bytes through a device-to-device copy, interleaved -------
+    # (exchange and copy alternate, 20 of each, the L2 treated as in the timed
+    # region; the ratio of the medians is the exchange's speed against the
+    # practical copy ceiling measured side by side)
+    d2d_gbps = vs_copy = None
+    if not light:
+        src = torch.cat([t for t in d_in])
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            dst.copy_(src)
+        t_x, t_c = [], []
+        for _ in range(20):
+            for fn, acc in ((step, t_x), (lambda: dst.copy_(src), t_c)):
+                if cold:
+                    flush.sum()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                b.synchronize()
+                acc.append(a.elapsed_time(b) / 1e3)
+        d2d_gbps = src.numel() / statistics.median(t_c) / 1e9
+        vs_copy = statistics.median(t_c) / statistics.median(t_x)
+        roofline["vs_same_run_copy"] = round(vs_copy, 4)
+        roofline["same_run_copy"] = {"GBps_moved": round(d2d_gbps, 1), "reps": 20,
+                                     "what": "torch device-to-device copy of the same bytes, "
+                                             "interleaved with the exchange"}
+        del src, dst
+        if eng.status() != a2av.OK:
+            raise SystemExit("device reported an error during the interleaved comparison")
 
     # ---- payload sweep (cold L2 between launches) --------------------------
     sweep = []
-    if args.workload == "cfg2" and args.op == "dispatch" and not args.no_sweep:
+    if args.workload == "cfg2" and args.op == "dispatch" and not args.no_sweep and not light:
         for Pk in wl.CFG2_SWEEP_BYTES:
             if Pk > P:
                 break
@@ -550,7 +577,7 @@ def run_ours(args):
 
     # ---- end to end through the public API, host buffers ------------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not light:
         if args.op == "combine":
             # host copies of the combine's own inputs (the forward outputs)
             e_src = [t.cpu().pin_memory() for t in c_in]
@@ -632,7 +659,7 @@ def run_ours(args):
     # ---- CPU oracle: baseline timing and a parity check of this run -------
     cpu = None
     parity = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.op == "combine":
+    if rank == 0 and world == 1 and (light or not args.no_cpu_baseline) and args.op == "combine":
         import oracle
         inputs = [t.numpy() for t in h_in]
         mid, dso = oracle.default().exchange(inputs, S, rb)
@@ -651,7 +678,7 @@ def run_ours(args):
                                                   "offsets equal the oracle's"}
         if not ok:
             raise SystemExit("the GPU's reverse exchange does not return the inputs")
-    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+    elif rank == 0 and world == 1 and (light or not args.no_cpu_baseline):
         inputs = [t.numpy() for t in h_in]
         mismatched = []
 
@@ -660,7 +687,8 @@ def run_ours(args):
                     and np.array_equal(d_so[p].cpu().numpy(), so)):
                 mismatched.append(p)
 
-        spent, moved, peers = time_oracle(inputs, S, rb, args.cpu_budget, check=compare)
+        spent, moved, peers = time_oracle(inputs, S, rb, float("inf") if light else args.cpu_budget,
+                                          check=compare)
         cpu = {"value": round(moved / spent / 1e9, 3), "unit": UNIT, "cores": 1,
                "kind": "oracle",
                "sample": f"peers {peers} of the same exchange "
@@ -677,15 +705,11 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
-                                        args.dedup, hidden=args.hidden), "name": args.workload,
-                   "op": args.op, "ranks": Wn, "row_bytes": rb, "per_rank_bytes": int(per_rank),
-                   "moved_bytes_per_step": T,
-                   "l2": ("L2 flushed (512 MiB read) before every timed launch; step time = "
-                          "the launch's CUDA-event duration") if cold else
-                         "inputs larger than L2; step time = bracketed CUDA-event time",
-                   "engine": kname, "grid": launch["grid"], "block": launch["block"],
-                   "parallelism": f"replicas x{world} (ranks emulated inside each GPU)"},
+        "config": exchange_config(args, Wn, rb, int(per_rank), T, cold, world),
+        "launch": {"engine": kname, "grid": launch["grid"], "block": launch["block"],
+                   "timing": ("L2 flushed (512 MiB read) before every timed launch; step time = "
+                              "the launch's CUDA-event duration") if cold else
+                             "step time = CUDA events bracketing the K steps"},
         "hbm_fraction": round(2 * T / (max_s / K) / 1e9 / peak, 4),
         "busbw_GBps": round(busbw_gbps(per_rank, max_s / K), 1),
         "launch_us_median": round(med_launch_s * 1e6, 2),
@@ -698,13 +722,65 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": K,
         "clocks": clocks.summary(),
-        "d2d_memcpy_GBps": round(d2d_gbps, 1),
+        "d2d_memcpy_GBps": None if d2d_gbps is None else round(d2d_gbps, 1),
         "sweep": sweep,
         "parity": parity,
         "input_generation_s": round(gen_s, 2),
     }
-    if rank == 0:
-        emit(line)
+    return line
+
+
+def exchange_config(args, Wn, rb, per_rank, T, cold, world):
+    """The `config` of an exchange line -- the same dict on both arms."""
+    return {"workload": describe(args.workload, args.per_rank_bytes, args.seed, args.tokens,
+                                 args.batch, args.dedup, hidden=args.hidden),
+            "name": args.workload, "op": args.op, "ranks": Wn, "row_bytes": rb,
+            "per_rank_bytes": per_rank, "moved_bytes_per_step": T,
+            "l2": ("inputs smaller than the GPU's L2: flushed (a 512 MiB read) before every "
+                   "timed launch") if cold else "inputs larger than the GPU's L2 (no flush)",
+            "parallelism": f"{Wn} emulated ranks per replica, {world} replica(s)"}
+
+
+# The other workloads of the survey's hot-path table, each an entry of the
+# default (cfg2) line: timed steps, roofline and a bit-exact check against the
+# oracle outside the timed region.
+CONFIG_ENTRIES = [
+    ("cfg1", dict(workload="cfg1")),
+    ("cfg3", dict(workload="cfg3")),
+    ("cfg4", dict(workload="cfg4", seed=0)),
+    ("cfg5", dict(workload="cfg5")),
+    ("cfg3_fused_dispatch", dict(workload="cfg3", op="fused_dispatch")),
+    ("cfg3_fused_combine", dict(workload="cfg3", op="fused_combine")),
+]
+
+
+def config_block(args) -> dict:
+    import copy
+    import torch
+    out = {}
+    for name, over in CONFIG_ENTRIES:
+        a = copy.copy(args)
+        a.workload, a.op, a.seed = over["workload"], over.get("op", "dispatch"), over.get("seed", 0)
+        a.steps, a.warmup = 20, 3
+        a.tokens, a.hidden, a.batch, a.dedup = 8192, 7168, 8192, False
+        a.path, a.ctas_per_sm = "auto", 0
+        a.no_cpu_baseline = False  # (the entry's bit-exact check runs with it)
+        torch.cuda.empty_cache()
+        if a.op == "fused_dispatch":
+            line = run_fused_dispatch(a, light=True)
+        elif a.op == "fused_combine":
+            line = run_fused_combine(a, light=True)
+        else:
+            line = run_ours(a, light=True)
+        r = line["roofline"]
+        out[name] = {"workload": line["config"]["workload"], "op": a.op,
+                     "us_per_step": round(line["ms_per_step"] * 1e3, 2),
+                     "moved_GBps": line["value"], "kernel": r["kernel"], "frac": r["frac"],
+                     "traffic": r["traffic"], "algorithmic_bytes": r["algorithmic_bytes_per_launch"],
+                     "launches_per_step": line["gpu_launches"] // line["steps"],
+                     "bit_exact": None if line["parity"] is None else line["parity"]["bit_exact"],
+                     "clocks": line["clocks"]}
+    return out
 
 
 # ------------------------------------------------------ fused dispatch ----
@@ -737,9 +813,11 @@ def _timed(torch, stream, fn, reps, cold, flush):
     return statistics.median(ts), statistics.mean(ts), statistics.mean(host)
 
 
-def run_fused_dispatch(args):
+def run_fused_dispatch(args, light=False):
     """a2av_dispatch on unsorted MoE or embedding-key items, against the
-    unfused path (torch stable sort + row gather, then a2av_run)."""
+    unfused path (torch stable sort + row gather, then a2av_run).  Returns
+    the JSON line; ``light`` skips the unfused path and the bound call (an
+    entry of the cfg2 line's ``configs`` block)."""
     import torch
     import variable_size_all_gb300 as a2av
     import workloads as wl
@@ -787,7 +865,8 @@ def run_fused_dispatch(args):
 
     for _ in range(args.warmup):
         fused()
-        unfused()
+        if not light:
+            unfused()
     torch.cuda.synchronize()
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during warm-up")
@@ -797,10 +876,13 @@ def run_fused_dispatch(args):
         f_med, f_mean, f_host = _timed(torch, stream, fused, args.steps, cold, flush)
         torch.cuda.synchronize()
         barrier()
-    u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
-    # the same dispatch marshalled once (A2av.bind_dispatch): the host's share per call
-    bound = eng.bind_dispatch(d_rows, d_src, d_key, K, d_out, d_so, d_pos, rb, stream=stream)
-    b_med, b_mean, b_host = _timed(torch, stream, bound, args.steps, cold, flush)
+    u_med = u_mean = u_host = b_med = b_mean = b_host = None
+    if not light:
+        u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold,
+                                       flush)
+        # the same dispatch marshalled once (A2av.bind_dispatch): the host's share per call
+        bound = eng.bind_dispatch(d_rows, d_src, d_key, K, d_out, d_so, d_pos, rb, stream=stream)
+        b_med, b_mean, b_host = _timed(torch, stream, bound, args.steps, cold, flush)
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during the timed region")
     max_s = reduce_max(f_mean, dev)
@@ -812,14 +894,9 @@ def run_fused_dispatch(args):
     distinct = sum(int(np.unique(x).size) for x in src) * rb
     algo = distinct + T + items * (4 + 4 + 8) + 24 * Wn * Wn
     peak, peak_kind = hbm_peak()
-    # the copy kernel the library picks: cp.async.bulk gather for 16-byte
-    # aligned rows of 2..32 KiB (torch allocations are aligned); rows under
-    # 64 bytes copied by the rank kernel itself (past the one-kernel size);
-    # else warp/thread copies
-    small_path = max(m) <= 2048 and Wn * K <= 256
-    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 2048 <= rb <= 32768
-                   else "dispatch_rank_copy_kernel" if rb < 64 and not small_path
-                   else "dispatch_copy_kernel")
+    # the kernels the library enqueued for this dispatch (a2av_last_dispatch)
+    chain = eng.last_dispatch()
+    copy_kernel = chain["copy_kernel"]
     roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
@@ -835,9 +912,11 @@ def run_fused_dispatch(args):
         ok = all(np.array_equal(d_out[p].cpu().numpy(), ref[p]) for p in range(Wn))
         ok = ok and np.array_equal(d_so.cpu().numpy(), ref_so)
         ok = ok and all(np.array_equal(d_pos[r].cpu().numpy(), ref_pos[r]) for r in range(Wn))
-        ok = ok and all(torch.equal(u_out[p], d_out[p]) for p in range(Wn))
+        if not light:
+            ok = ok and all(torch.equal(u_out[p], d_out[p]) for p in range(Wn))
         parity = {"bit_exact": bool(ok), "check": "outputs, offsets and positions equal the "
-                                                  "oracle's; the unfused path agrees"}
+                                                  "oracle's" + ("" if light else
+                                                                "; the unfused path agrees")}
         cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "the whole fused dispatch of the same workload", "seconds": round(spent, 3)}
         if not ok:
@@ -855,34 +934,34 @@ def run_fused_dispatch(args):
                    "items": items, "keys_per_peer": K, "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
                           "inputs larger than L2"),
-                   "timing": "CUDA events around the dispatch (one memset and three or four "
-                             "kernels), "
+                   "timing": f"CUDA events around the dispatch ({chain['memsets']} memset and "
+                             f"{chain['kernels']} kernels, ending in {copy_kernel}), "
                              "mean over steps; a spin kernel ahead of each call keeps the "
                              "host's call time outside the events (fused_host_call_us)"},
-        "unfused_torch_sort_gather_a2av": {"ms_mean": round(u_mean * 1e3, 4),
-                                           "ms_median": round(u_med * 1e3, 4),
-                                           "value": round(T / u_mean / 1e9, 2), "unit": UNIT,
-                                           "host_call_us": round(u_host * 1e6, 1)},
+        "unfused_torch_sort_gather_a2av": None if light else {
+            "ms_mean": round(u_mean * 1e3, 4), "ms_median": round(u_med * 1e3, 4),
+            "value": round(T / u_mean / 1e9, 2), "unit": UNIT,
+            "host_call_us": round(u_host * 1e6, 1)},
         "fused_ms_median": round(f_med * 1e3, 4),
         "fused_host_call_us": round(f_host * 1e6, 1),
-        "bound_call": {"ms_mean": round(b_mean * 1e3, 4), "ms_median": round(b_med * 1e3, 4),
-                       "host_call_us": round(b_host * 1e6, 1),
-                       "note": "A2av.bind_dispatch: arguments marshalled once"},
-        "speedup_vs_unfused": round(u_mean / f_mean, 3),
+        "bound_call": None if light else {
+            "ms_mean": round(b_mean * 1e3, 4), "ms_median": round(b_med * 1e3, 4),
+            "host_call_us": round(b_host * 1e6, 1),
+            "note": "A2av.bind_dispatch: arguments marshalled once"},
+        "speedup_vs_unfused": None if light else round(u_mean / f_mean, 3),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": None,
-        "gpu_launches": (2 if small_path else 3 if copy_kernel == "dispatch_rank_copy_kernel"
-                         else 4) * args.steps,
+        "gpu_launches": chain["kernels"] * args.steps,
         "clocks": clocks.summary(), "parity": parity,
     }
-    if rank == 0:
-        emit(line)
+    return line
 
 
 # ------------------------------------------------------------- overlap ----
-def run_fused_combine(args):
+def run_fused_combine(args, light=False):
     """a2av_combine_items after a fused dispatch (cfg3, cfg5): every item's row
     back from the peers into item order, against the plain reverse exchange
-    followed by a torch gather by sorted position."""
+    followed by a torch gather by sorted position.  Returns the JSON line;
+    ``light`` skips the unfused path."""
     import torch
     import variable_size_all_gb300 as a2av
     import workloads as wl
@@ -927,7 +1006,8 @@ def run_fused_combine(args):
 
     for _ in range(args.warmup):
         call()
-        unfused()
+        if not light:
+            unfused()
     torch.cuda.synchronize()
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during warm-up")
@@ -937,7 +1017,10 @@ def run_fused_combine(args):
         f_med, f_mean, f_host = _timed(torch, stream, call, args.steps, cold, flush)
         torch.cuda.synchronize()
         barrier()
-    u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold, flush)
+    u_med = u_mean = u_host = None
+    if not light:
+        u_med, u_mean, u_host = _timed(torch, stream, unfused, max(3, args.steps // 4), cold,
+                                       flush)
     if eng.status() != a2av.OK:
         raise SystemExit("device reported an error during the timed region")
     max_s = reduce_max(f_mean, dev)
@@ -946,9 +1029,10 @@ def run_fused_combine(args):
     # each item's key and position read once
     algo = T + sum(m) * rb + sum(m) * (4 + 8) + 24 * Wn * Wn
     peak, peak_kind = hbm_peak()
-    copy_kernel = ("dispatch_copy_bulk_kernel" if rb % 16 == 0 and 2048 <= rb <= 32768
-                   else "dispatch_copy_kernel")
-    roofline = {"bound": "hbm", "kernel": f"a2av_combine_items (checks, then {copy_kernel})",
+    chain = eng.last_dispatch()  # the kernels the library enqueued for the combine
+    copy_kernel = chain["copy_kernel"]
+    roofline = {"bound": "hbm", "kernel": f"a2av_combine_items ({chain['kernels']} kernels, "
+                                          f"ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
                 "traffic": measured_traffic(copy_kernel + ":" + args.workload +
@@ -967,9 +1051,11 @@ def run_fused_combine(args):
         ok = all(np.array_equal(items[r].cpu().numpy(), ref[r]) for r in range(Wn))
         ok = ok and all(np.array_equal(ref[r], rows[r].reshape(-1, rb)[src[r]].reshape(-1))
                         for r in range(Wn))
-        ok = ok and all(torch.equal(u_items[r], items[r]) for r in range(Wn))
+        if not light:
+            ok = ok and all(torch.equal(u_items[r], items[r]) for r in range(Wn))
         parity = {"bit_exact": bool(ok), "check": "item rows equal the oracle's and the items' "
-                                                  "source rows; the unfused path agrees"}
+                                                  "source rows" + ("" if light else
+                                                                   "; the unfused path agrees")}
         cpu = {"value": round(T / spent / 1e9, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "the whole fused combine of the same workload", "seconds": round(spent, 3)}
         if not ok:
@@ -987,18 +1073,19 @@ def run_fused_combine(args):
                    "items": sum(m), "moved_bytes_per_step": T,
                    "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
                           "inputs larger than L2"),
-                   "timing": "CUDA events around the bound call (a memset and three kernels), "
-                             "mean over steps; a spin kernel ahead of each call"},
-        "unfused_combine_then_gather": {"ms_mean": round(u_mean * 1e3, 4),
-                                        "ms_median": round(u_med * 1e3, 4),
-                                        "host_call_us": round(u_host * 1e6, 1)},
+                   "timing": f"CUDA events around the bound call ({chain['memsets']} memset and "
+                             f"{chain['kernels']} kernels), mean over steps; a spin kernel ahead "
+                             "of each call"},
+        "unfused_combine_then_gather": None if light else {
+            "ms_mean": round(u_mean * 1e3, 4), "ms_median": round(u_med * 1e3, 4),
+            "host_call_us": round(u_host * 1e6, 1)},
         "fused_ms_median": round(f_med * 1e3, 4), "fused_host_call_us": round(f_host * 1e6, 1),
-        "speedup_vs_unfused": round(u_mean / f_mean, 3),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": None, "gpu_launches": 3 * args.steps,
+        "speedup_vs_unfused": None if light else round(u_mean / f_mean, 3),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": None,
+        "gpu_launches": chain["kernels"] * args.steps,
         "clocks": clocks.summary(), "parity": parity,
     }
-    if rank == 0:
-        emit(line)
+    return line
 
 
 def device_exchange(torch, dev, w):
@@ -1290,9 +1377,11 @@ def run_reference(args):
     if args.workload == "cfg2":
         w = wl.cfg2(P, seed=args.seed)
     else:
-        w = {"cfg1": wl.cfg1, "cfg3": lambda s: wl.cfg3(s, dedup=args.dedup, hidden=args.hidden),
+        w = {"cfg1": wl.cfg1,
+             "cfg3": lambda s: wl.cfg3(s, tokens=args.tokens, dedup=args.dedup,
+                                       hidden=args.hidden),
              "cfg4": wl.cfg4,
-             "cfg5": wl.cfg5}[args.workload](args.seed)
+             "cfg5": lambda s: wl.cfg5(s, batch=args.batch)}[args.workload](args.seed)
     S, inputs, rb, Wn = w.splits, w.inputs, w.row_bytes, w.W
     K, Wm = args.steps, args.warmup
     for k in range(Wm):
@@ -1308,11 +1397,11 @@ def run_reference(args):
         "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(total_s * 1e3 / K, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic (seeded numpy draws; no dataset)",
-        "config": {"workload": describe(args.workload, P, args.seed, args.tokens, args.batch,
-                                        args.dedup, hidden=args.hidden), "name": args.workload,
-                   "ranks": Wn, "row_bytes": rb,
-                   "per_rank_bytes": int(statistics.mean(b.size for b in inputs)),
-                   "parallelism": "one host core"},
+        # the same config dict as this workload's GPU line
+        "config": exchange_config(args, Wn, rb, int(statistics.mean(b.size for b in inputs)),
+                                  moved_bytes(S, rb), sum(b.size for b in inputs) < 2 * L2_BYTES,
+                                  world),
+        "implementation": "the CPU oracle (C, one host core)",
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"one peer's whole output per step (peer = step mod {Wn})"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -1321,7 +1410,30 @@ def run_reference(args):
     emit(line)
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_replicas(n: int, argv, script=None) -> int:
+    """Start n local processes of this script with the rank variables a
+    torchrun launch sets (rendezvous on 127.0.0.1); returns the worst exit
+    code.  Only rank 0 prints the JSON line."""
+    script = script or os.path.abspath(__file__)
+    port = free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, script, *argv], env=env))
+    codes = [p.wait() for p in procs]
+    return max(codes, key=abs)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -1352,20 +1464,38 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="cfg2 line: skip the other workloads' block (configs)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is None and args.gpus > 1:
+        # N replicas without an external launcher: one process per GPU here
+        raise SystemExit(spawn_replicas(args.gpus, argv))
+    if world_env is not None and int(world_env) != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}: "
+                         "launch one process per GPU (torchrun --nproc-per-node N, or "
+                         "bench.py --gpus N alone)")
     if args.impl == "reference":
         run_reference(args)
     elif args.op == "fused_dispatch":
-        run_fused_dispatch(args)
+        line = run_fused_dispatch(args)
+        if dist_env()[0] == 0:
+            emit(line)
     elif args.op == "overlap":
         run_overlap(args)
     elif args.op == "kjt":
         run_kjt(args)
     elif args.op == "fused_combine":
-        run_fused_combine(args)
+        line = run_fused_combine(args)
+        if dist_env()[0] == 0:
+            emit(line)
     else:
-        run_ours(args)
+        line = run_ours(args)
+        if args.workload == "cfg2" and args.op == "dispatch" and not args.no_configs:
+            line["configs"] = config_block(args)
+        if dist_env()[0] == 0:
+            emit(line)
 
 
 if __name__ == "__main__":

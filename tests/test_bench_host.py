@@ -45,7 +45,8 @@ def test_traffic_counters_follow_their_kernels_sources(tmp_path, monkeypatch):
     are built from different files."""
     ex, dp = bench.kernel_source_sha("a2av_bulk_kernel"), bench.kernel_source_sha("dispatch_x")
     assert ex != dp and ex == bench.kernel_source_sha("a2av_staged_multi_kernel")
-    assert "dispatch.cu" in bench.kernel_sources("dispatch_rank_copy_kernel")[0]
+    assert "dispatch.cu" in bench.kernel_sources("dispatch_place_copy_kernel")[0]
+    assert "dispatch.cu" in bench.kernel_sources("combine_tiny_kernel")[0]
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "traffic.json").write_text(json.dumps({
@@ -113,3 +114,67 @@ def test_replicas_aggregate_over_gloo():
     res = sorted(q.get(timeout=10) for _ in range(2))
     assert [m for _, m, _ in res] == [2.0, 2.0]  # max over ranks
     assert [v for _, _, v in res] == [5.0, 5.0]  # 2 ranks x 5 units / 2 s
+
+
+def test_reference_config_equals_the_gpu_lines():
+    """Both arms describe the workload with the same config dict."""
+    import argparse
+    import workloads as wl
+    P = 1 << 22
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--per-rank-bytes", str(P), "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    got = json.loads(out.stdout.strip().splitlines()[-1])["config"]
+    w = wl.cfg2(P)
+    args = argparse.Namespace(workload="cfg2", op="dispatch", per_rank_bytes=P, seed=0,
+                              tokens=8192, batch=8192, dedup=False, hidden=7168)
+    want = bench.exchange_config(args, w.W, w.row_bytes, int(np.mean([b.size for b in w.inputs])),
+                                 bench.moved_bytes(w.splits, w.row_bytes),
+                                 sum(b.size for b in w.inputs) < 2 * bench.L2_BYTES, 1)
+    assert got == want
+
+
+def test_gpus_flag_must_match_the_launcher(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2"])
+    assert "WORLD_SIZE=1" in str(e.value)
+
+
+def test_host_memory_shortfall_is_refused_not_shrunk(monkeypatch):
+    import argparse
+    import torch
+    monkeypatch.setattr(bench, "host_memory_available", lambda: 8 << 30)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    args = argparse.Namespace(workload="cfg2", per_rank_bytes=1 << 32, seed=0)
+    with pytest.raises(SystemExit) as e:
+        bench.load_workload(args, torch)
+    assert "Refusing" in str(e.value)
+    assert args.per_rank_bytes == 1 << 32  # the request is untouched
+
+
+def test_spawned_replicas_aggregate_over_gloo(tmp_path, capfd):
+    """bench.py --gpus N without a launcher starts N local processes with the
+    rank variables torchrun sets; here each runs a stand-in step over a gloo
+    group and rank 0 prints the aggregated line."""
+    script = tmp_path / "replica.py"
+    script.write_text(
+        "import json, os, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "rank, local, world = bench.dist_env()\n"
+        "bench.dist_init('gloo')\n"
+        "bench.barrier()\n"
+        "t = bench.reduce_max(1.0 + rank)\n"
+        "if rank == 0:\n"
+        "    print(json.dumps({'world': world, 'local': local, 'max_s': t,\n"
+        "                      'value': bench.whole_job_value(6.0, world, t),\n"
+        "                      'argv': sys.argv[1:]}))\n")
+    rc = bench.spawn_replicas(2, ["--gpus", "2", "--steps", "3"], script=str(script))
+    assert rc == 0
+    lines = [ln for ln in capfd.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["world"] == 2 and line["max_s"] == 2.0 and line["value"] == 6.0
+    assert line["argv"] == ["--gpus", "2", "--steps", "3"]
