@@ -145,10 +145,6 @@ def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=
             eng.close()
     torch.cuda.synchronize()
     assert st == a2av.OK, f"device status {st}"
-    if expect_copy is not None:
-        assert chain["copy_kernel"] == expect_copy, chain
-    if expect_kernels is not None:
-        assert chain["kernels"] == expect_kernels, chain
     assert np.array_equal(isp.cpu().numpy(), ref_S), "dispatch split matrix differs"
     assert np.array_equal(so.cpu().numpy(), ref_so), "dispatch out_splits_offsets differ"
     for r in range(W):
@@ -164,4 +160,16 @@ def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=
         assert g_out[p].guards_intact(), f"dispatch peer {p}: canary overwritten"
     for r in range(W):
         assert np.array_equal(g_rows[r].view.cpu().numpy(), rows[r]), f"rows {r} modified"
+    if expect_copy is not None:
+        assert chain["copy_kernel"] == expect_copy, chain
+    if expect_kernels is not None:
+        assert chain["kernels"] == expect_kernels, chain
     return ref, ref_so, ref_pos, ref_S
+
+
+def aligned_copy_kernel(rb: int) -> str:
+    """The kernel that moves 16-byte aligned rows of rb bytes past the
+    one-kernel size: the register warp copy below 1.5 KiB, the cp.async
+    stream copy up to 4 KiB, the cp.async.bulk gather up to 32 KiB."""
+    return ("dispatch_copy_kernel" if rb < 1536 else
+            "dispatch_stream_kernel" if rb <= 4096 else "dispatch_gather_kernel")

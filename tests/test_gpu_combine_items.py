@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as wl
-from tests._gpu import Guarded, SENTINEL
+from tests._gpu import Guarded, SENTINEL, aligned_copy_kernel
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +39,6 @@ def _combine_checked(K, peers, S, keys, pos, rb, mis=None, expect=None, expect_c
                           [g.view for g in g_out], rb)
         st = eng.status()
         chain = eng.last_dispatch()
-    if expect_copy is not None:
-        assert chain["copy_kernel"] == expect_copy, chain
     ref = [np.full((m[r] + 2) * rb, SENTINEL, np.uint8) for r in range(W)]
     rc = oracle.default().combine_items(K, peers, S, keys, pos, ref, rb)
     assert st == rc, f"device status {st}, oracle {rc}"
@@ -52,6 +50,8 @@ def _combine_checked(K, peers, S, keys, pos, rb, mis=None, expect=None, expect_c
     if expect is not None:
         for r in range(W):
             assert np.array_equal(g_out[r].view.cpu().numpy()[: m[r] * rb], expect[r])
+    if expect_copy is not None:
+        assert chain["copy_kernel"] == expect_copy, chain
     return st
 
 
@@ -184,12 +184,13 @@ def test_decode_size_and_host_checks():
         assert rc == a2av.ERR_INVALID_ARG  # workspace too small
 
 
-# The combine's gather by ring shape (many items: the check kernel, then the
-# cp.async.bulk gather with one bulk store per stage) and its one-kernel
-# path (at most 4096 items: row slots for aligned rows, registers otherwise).
+# The combine's copy by row size (many items: the check kernel, then the
+# cp.async stream copy up to 2 KiB rows or the cp.async.bulk gather above)
+# and its one-kernel path (at most 4096 items: row slots for aligned rows,
+# registers otherwise).
 @pytest.mark.parametrize("rb,m", [(64, 20011), (512, 9001), (1024, 6007), (2048, 6007),
                                   (4096, 3001), (14336, 1801), (32768, 1801)])
-def test_gather_ring_shapes(rb, m):
+def test_aligned_copy_shapes(rb, m):
     """(more than 4096 items in all: past the one-kernel path)"""
     rng = np.random.default_rng(rb + m + 1)
     W, K = 4, 3
@@ -200,7 +201,7 @@ def test_gather_ring_shapes(rb, m):
     outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
     peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
     assert _combine_checked(K, peers, S, key, pos, rb,
-                            expect_copy="dispatch_gather_kernel") == a2av.OK
+                            expect_copy=aligned_copy_kernel(rb)) == a2av.OK
 
 
 @pytest.mark.parametrize("rb", [1, 8, 16, 64, 1024, 14336, 40000])

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import workloads as wl
-from tests._gpu import dispatch_checked
+from tests._gpu import aligned_copy_kernel, dispatch_checked
 
 pytestmark = pytest.mark.gpu
 
@@ -89,7 +89,7 @@ def test_few_items_past_the_one_kernel_size(rb):
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
     src = [rng.integers(0, n, m).astype(np.int32) for _ in range(W)]
     key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
-    dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_gather_kernel",
+    dispatch_checked(K, rows, src, key, rb, expect_copy=aligned_copy_kernel(rb),
                      expect_kernels=3)
 
 
@@ -128,7 +128,7 @@ def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb):
     key = [np.minimum(rng.geometric(0.05, c) - 1, W * K - 1).astype(np.int32) for c in counts]
     dispatch_checked(K, rows, src, key, rb, expect_kernels=kernels,
                      expect_copy="dispatch_place_copy_kernel" if rb < 64 else
-                     "dispatch_gather_kernel")
+                     aligned_copy_kernel(rb))
 
 
 @pytest.mark.parametrize("rb", [8, 64])
@@ -145,16 +145,18 @@ def test_four_ranges_a_count_warp(W, K, kernels, rb):
     key = [rng.integers(0, W * K, m - 1000 * r).astype(np.int32) for r in range(W)]
     dispatch_checked(K, rows, src, key, rb, expect_kernels=kernels,
                      expect_copy="dispatch_place_copy_kernel" if rb < 64 else
-                     "dispatch_gather_kernel")
+                     aligned_copy_kernel(rb))
 
 
-# Aligned rows by the gather's ring shapes (row-size classes up to 256 B,
-# 512 B, 1, 2, 4, 8, 16 and 32 KiB), with item counts that give 32-, 16- and
-# 8-item batches and ragged last batches per rank.
+# Aligned rows by the copy kernels' shapes (the register warp copy below
+# 1.5 KiB, in flat runs or by 512-byte pieces; the stream copy's 16- and
+# 8-item batches for 1.5 .. 4 KiB rows; the gather's rings for 8, 16 and
+# 32 KiB rows), with ragged last batches per rank.
 @pytest.mark.parametrize("rb,m", [(64, 20011), (256, 20011), (272, 9001), (512, 9001),
-                                  (1024, 6007), (2048, 6007), (4096, 3001), (8192, 1801),
-                                  (14336, 1801), (16384, 1801), (32768, 1801)])
-def test_gather_ring_shapes(rb, m):
+                                  (1024, 6007), (1536, 6007), (2048, 6007), (3072, 3001),
+                                  (4096, 3001), (8192, 1801), (14336, 1801), (16384, 1801),
+                                  (32768, 1801)])
+def test_aligned_copy_shapes(rb, m):
     """(more than 4096 items in all: past the one-kernel path)"""
     rng = np.random.default_rng(rb + m)
     W, K, n = 4, 3, 97
@@ -162,7 +164,7 @@ def test_gather_ring_shapes(rb, m):
     counts = [m, m - 17, m // 3, 1]
     src = [rng.integers(0, n, c).astype(np.int32) for c in counts]
     key = [rng.integers(0, W * K, c).astype(np.int32) for c in counts]
-    dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_gather_kernel")
+    dispatch_checked(K, rows, src, key, rb, expect_copy=aligned_copy_kernel(rb))
 
 
 # The one-kernel path (at most 4096 items over all ranks): row slots through

@@ -12,7 +12,7 @@
 // ranges): the items of smaller keys, of key k in earlier groups, in earlier
 // ranges of the group, and earlier in the item's own range.
 //   1. count  (eight warps per CTA, one to four ranges each): a warp ranks
-//      its range's items 32 at a time (warp match on the key), which gives
+//      its range's items 32 at a time (equal keys found by ballots), which gives
 //      every item its inrank byte and the range's key histogram; keys and
 //      source rows are validated here.  The CTA's histograms give each range
 //      its in-group prefix (hist) and the group its count (grp).  The last
@@ -120,6 +120,24 @@ __device__ __forceinline__ void fail(const DispatchParams& D, int code) {
   record_error(D.status, code);
 }
 
+// The lanes of the warp holding the same key as this lane (valid lanes only;
+// an invalid lane gets 0 and matches nobody): one ballot per key bit, keys in
+// [0, 2^bits).  Same result as __match_any_sync on the valid keys, at the
+// throughput of plain ballots (the match instruction is far slower per SM,
+// measured: ranking 640 K items a rank in 8-warp blocks took 28 us with it).
+__device__ __forceinline__ unsigned same_key_lanes(int key, bool valid, int bits) {
+  unsigned m = __ballot_sync(kFull, valid);
+  for (int b = 0; b < bits; ++b) {
+    const bool one = (key >> b) & 1;
+    const unsigned v = __ballot_sync(kFull, one);
+    m &= one ? v : ~v;
+  }
+  return valid ? m : 0u;
+}
+
+// Bits that hold every key below nb (0 for one key).
+__device__ __forceinline__ int key_bits(int nb) { return nb > 1 ? 32 - __clz(nb - 1) : 0; }
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -223,7 +241,7 @@ __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) 
 
 // Count: CTA (c, r) holds group c of rank r; warp w ranks ranges
 // 8RW c + RW w .. + RW - 1 (all their keys and source rows loaded at once),
-// 32 items at a time: __match_any_sync groups equal keys, a lane's rank
+// 32 items at a time: a ballot per key bit groups equal keys, a lane's rank
 // among them plus the range's running count of its key is its inrank, and
 // each key's leader advances that count.  RW = 4
 // serves batches so large that one CTA per SM still has four ranges a warp
@@ -253,14 +271,20 @@ __global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 4 : 2)
   extern __shared__ int count_hist[];  // [kGroupRanges][NB], range by range
   for (int e = t; e < kGroupRanges * NB; e += blockDim.x) count_hist[e] = 0;
   const long long j0 = c * kGroupRanges + (long long)warp * RW;  // this warp's first range
+  // Every load unconditional (an index past the rank's last item reads its
+  // last item again, then counts for nothing), so all of them issue at once.
+  const int* const kp = D.key[r];
+  const int* const sp = D.src[r];
+  const long long rows_r = D.rows[r];
   int keys[RW][kRange / 32], srcs[RW][kRange / 32];
 #pragma unroll
   for (int u = 0; u < RW; ++u)
 #pragma unroll
     for (int q = 0; q < kRange / 32; ++q) {
       const long long i = (j0 + u) * kRange + q * 32 + lane;
-      keys[u][q] = i < m ? D.key[r][i] : 0;
-      srcs[u][q] = i < m ? D.src[r][i] : 0;
+      const long long ii = i < m ? i : m - 1;
+      keys[u][q] = __ldg(kp + ii);
+      srcs[u][q] = __ldg(sp + ii);
     }
   int bad = 0;
 #pragma unroll
@@ -269,19 +293,20 @@ __global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 4 : 2)
     for (int q = 0; q < kRange / 32; ++q) {
       const long long i = (j0 + u) * kRange + q * 32 + lane;
       const int k = keys[u][q], s = srcs[u][q];
-      const bool ok = i < m && k >= 0 && k < NB && s >= 0 && s < D.rows[r];
+      const bool ok = i < m && k >= 0 && k < NB && s >= 0 && s < rows_r;
       if (i < m && !ok) bad = 1;
       keys[u][q] = ok ? k : -1 - lane;  // absent or invalid items match nobody
     }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
+  const int bits = key_bits(NB);
 #pragma unroll
   for (int u = 0; u < RW; ++u) {
     int* hist = count_hist + (warp * RW + u) * NB;
 #pragma unroll
     for (int q = 0; q < kRange / 32; ++q) {
       const int k = keys[u][q];
-      const unsigned same = __match_any_sync(kFull, k);
+      const unsigned same = same_key_lanes(k, k >= 0, bits);
       const int inr = k >= 0 ? hist[k] + __popc(same & lt) : 0;
       __syncwarp();
       if (k >= 0 && lane == 31 - __clz(same)) hist[k] += __popc(same);
@@ -420,26 +445,31 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_small_kernel(const __gr
   __shared__ long long warp_sums[kScanThreads / 32];
   for (int e = tid; e < kSmallWarps * NB; e += kScanThreads) cnt[e / NB][e % NB] = 0;
   int keys[kRange / 32], srcs[kRange / 32];
+  const int* const kp = D.key[r];
+  const int* const sp = D.src[r];
+  const long long rows_r = D.rows[r];
 #pragma unroll
-  for (int c = 0; c < kRange / 32; ++c) {
+  for (int c = 0; c < kRange / 32; ++c) {  // (unconditional loads, as in the count kernel)
     const long long i = (long long)warp * kRange + c * 32 + lane;
-    keys[c] = i < m ? D.key[r][i] : 0;
-    srcs[c] = i < m ? D.src[r][i] : 0;
+    const long long ii = i < m ? i : (m > 0 ? m - 1 : 0);
+    keys[c] = m > 0 ? __ldg(kp + ii) : 0;
+    srcs[c] = m > 0 ? __ldg(sp + ii) : 0;
   }
   int bad = 0;
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = (long long)warp * kRange + c * 32 + lane;
-    const bool ok = i < m && keys[c] >= 0 && keys[c] < NB && srcs[c] >= 0 && srcs[c] < D.rows[r];
+    const bool ok = i < m && keys[c] >= 0 && keys[c] < NB && srcs[c] >= 0 && srcs[c] < rows_r;
     if (i < m && !ok) bad = 1;
     keys[c] = ok ? keys[c] : -1 - lane;  // absent or invalid items match nobody
   }
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
+  const int bits = key_bits(NB);
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const int key = keys[c];
-    const unsigned same = __match_any_sync(kFull, key);
+    const unsigned same = same_key_lanes(key, key >= 0, bits);
     const int inr = key >= 0 ? cnt[warp][key] + __popc(same & lt) : 0;
     __syncwarp();
     if (key >= 0 && lane == 31 - __clz(same)) cnt[warp][key] += __popc(same);
@@ -549,12 +579,16 @@ __global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
   int keys[kRange / 32], srcs[kRange / 32], inr[kRange / 32];
   int* base = place_base + warp * NB;
   if (live) {
+    const int* const kp = D.key[r];
+    const int* const sp = D.src[r];
+    const unsigned char* const ip = D.inrank + (long long)r * D.pos_stride;
 #pragma unroll
-    for (int c = 0; c < kRange / 32; ++c) {
+    for (int c = 0; c < kRange / 32; ++c) {  // (unconditional loads, as in the count kernel)
       const long long i = i0 + c * 32 + lane;
-      keys[c] = i < m ? D.key[r][i] : 0;
-      srcs[c] = i < m ? D.src[r][i] : 0;
-      inr[c] = i < m ? D.inrank[(long long)r * D.pos_stride + i] : 0;
+      const long long ii = i < m ? i : m - 1;
+      keys[c] = __ldg(kp + ii);
+      srcs[c] = __ldg(sp + ii);
+      inr[c] = ip[ii];
     }
     for (int k = lane; k < NB; k += 32) base[k] = (int)key_base(D, r, i0, k);
   }
@@ -638,12 +672,19 @@ __device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc,
   }
 }
 
-// Register copies (rows the gather does not take): kWarpRows -- rows of
-// kWarpRowBytes or more, a warp per batch of rows (each kernel instantiation
-// holds one of the two loops, so neither pays the other's registers); else
-// a thread per row.
-template <bool kWarpRows>
-__global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRows : kCopyCtasPerSm)
+// Register copies (rows the stream copy and the gather do not take):
+// kWarpRows -- rows of kWarpRowBytes or more, a warp per batch of rows; else
+// a thread per row.  kRows512: every row and buffer 16-byte aligned and rows
+// a multiple of 512 bytes (the host checks).  Each instantiation holds one
+// loop, so none pays another's registers.
+#ifndef A2AV_ROWS512_CTAS_PER_SM
+#define A2AV_ROWS512_CTAS_PER_SM 4  // 64 registers: four CTAs an SM, 2 KiB a warp in flight
+#endif
+constexpr int kRows512CtasPerSm = A2AV_ROWS512_CTAS_PER_SM;
+template <bool kWarpRows, bool kRows512 = false>
+__global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
+                                                : kWarpRows ? kCopyCtasPerSmWarpRows
+                                                            : kCopyCtasPerSm)
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   if (flagged(D)) return;
@@ -692,7 +733,31 @@ __global__ void __launch_bounds__(kCopyThreads, kWarpRows ? kCopyCtasPerSmWarpRo
         }
       }
       if (!D.combine && __any_sync(kFull, lane < n && mdst == 0)) continue;  // (never: in_group)
-      if (D.vec16 && rb <= kVecMaxRow) {
+      if constexpr (kRows512) {
+        // rows of a multiple of 512 bytes: lane l takes pieces l, l + 32, ...
+        // of every row; (row, piece) advance by a counter, no division
+        const unsigned vpl = (unsigned)(rb >> 9), np = (unsigned)n * vpl;  // a lane's pieces
+        unsigned j = 0, c = 0;
+        for (unsigned b0 = 0; b0 < np; b0 += kVecRows) {  // warp-uniform trip count
+          uint4 v[kVecRows];
+          long long d[kVecRows];
+#pragma unroll
+          for (int q = 0; q < kVecRows; ++q) {
+            const bool ok = b0 + q < np;
+            const long long s = __shfl_sync(kFull, msrc, (int)(j & 31u));
+            const long long off = 16LL * (lane + 32 * c);
+            d[q] = __shfl_sync(kFull, mdst, (int)(j & 31u)) + off;
+            if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s + off));
+            if (++c == vpl) {
+              c = 0;
+              ++j;
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < kVecRows; ++q)
+            if (b0 + q < np) st_stream(reinterpret_cast<uint4*>(d[q]), v[q]);
+        }
+      } else if (D.vec16 && rb <= kVecMaxRow) {
         const unsigned V = (unsigned)(rb >> 4), nv = (unsigned)n * V;  // < 2^17
         for (unsigned b0 = 0; b0 < nv; b0 += 32 * kVecRows) {  // warp-uniform trip count
           uint4 v[kVecRows];
@@ -1050,14 +1115,22 @@ __global__ void __launch_bounds__(512, 1)
       const unsigned held = __ballot_sync(kFull, a0.v);
       rows = held ? 32u - __clz(held) : 0u;
       const uint32_t buf = buf0 + (uint32_t)(t & 1) * half;
-      const unsigned total = rows * V;
-#pragma unroll 4
-      for (unsigned base = 0; base < total; base += 32) {  // warp-uniform trip count
-        const unsigned q = base + lane;
-        const unsigned j = q < total ? q / V : 0, c = q - j * V;
-        const long long sj = __shfl_sync(kFull, src, (int)j);
-        if (q < total && sj != 0)
-          cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
+      if (V >= 32) {  // a row at a time, its pieces over the lanes
+        for (unsigned j = 0; j < rows; ++j) {
+          const long long sj = __shfl_sync(kFull, src, (int)j);
+          if (sj != 0)
+#pragma unroll 2
+            for (unsigned c = lane; c < V; c += 32)
+              cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
+        }
+      } else {  // 32 / V rows at a time, lane -> (row, piece) fixed
+        const unsigned rpp = 32u / V, jl = lane / V, c = lane - jl * V;
+        for (unsigned j0 = 0; j0 < rows; j0 += rpp) {
+          const unsigned j = j0 + jl;
+          const long long sj = __shfl_sync(kFull, src, (int)(j & 31u));
+          if (jl < rpp && j < rows && sj != 0)
+            cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
+        }
       }
       cp_async_commit();
     }
@@ -1068,14 +1141,22 @@ __global__ void __launch_bounds__(512, 1)
         cp_async_wait<0>();
       __syncwarp();
       const uint32_t pbuf = buf0 + (uint32_t)((t - 1) & 1) * half;
-      const unsigned total = prows * V;
-#pragma unroll 4
-      for (unsigned base = 0; base < total; base += 32) {
-        const unsigned q = base + lane;
-        const unsigned j = q < total ? q / V : 0, c = q - j * V;
-        const long long dj = __shfl_sync(kFull, pdst, (int)j);
-        if (q < total && dj != 0)
-          st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
+      if (V >= 32) {
+        for (unsigned j = 0; j < prows; ++j) {
+          const long long dj = __shfl_sync(kFull, pdst, (int)j);
+          if (dj != 0)
+#pragma unroll 2
+            for (unsigned c = lane; c < V; c += 32)
+              st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
+        }
+      } else {
+        const unsigned rpp = 32u / V, jl = lane / V, c = lane - jl * V;
+        for (unsigned j0 = 0; j0 < prows; j0 += rpp) {
+          const unsigned j = j0 + jl;
+          const long long dj = __shfl_sync(kFull, pdst, (int)(j & 31u));
+          if (jl < rpp && j < prows && dj != 0)
+            st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
+        }
       }
       __syncwarp();  // every lane has read the buffer before the next batch refills it
     }
@@ -1103,9 +1184,18 @@ constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 constexpr long long kGatherMaxRow = 32 * 1024;
 constexpr int kGatherSmem = 192 * 1024;
-#ifndef A2AV_STREAM_MAX_ROW
-#define A2AV_STREAM_MAX_ROW 2048  // aligned rows up to this long take the stream copy
+// Aligned rows of kStreamMinRow .. kStreamMaxRow bytes take the stream copy.
+// Measured (MoE dispatch / fused combine, 8192 tokens, W=8, us): 2 KiB rows
+// 91.7 / 106.7 against 125.1 / 130.2 by the gather; at 512 B and 1 KiB rows
+// the register warp copy is ahead (34.2 / 30.2 and 54.0 / 52.1 against
+// 56.0 / 48.2 and 63.5 / 54.3).
+#ifndef A2AV_STREAM_MIN_ROW
+#define A2AV_STREAM_MIN_ROW 1536
 #endif
+#ifndef A2AV_STREAM_MAX_ROW
+#define A2AV_STREAM_MAX_ROW 4096
+#endif
+constexpr long long kStreamMinRow = A2AV_STREAM_MIN_ROW;
 constexpr long long kStreamMaxRow = A2AV_STREAM_MAX_ROW;
 constexpr long long kStreamFlight = 96 * 1024;  // bytes of loads in flight per CTA
 constexpr int kStreamSmem = 192 * 1024;
@@ -1151,20 +1241,22 @@ constexpr int kTinyThreads = 256;
 constexpr int kTinyItems = 4096;
 constexpr int kTinyCounts = 2048;  // W * W * K counters in shared memory
 constexpr int kTinyOwn = 64;
-constexpr int kTinySlotBytes = 176 * 1024;  // dynamic shared memory for row slots
+constexpr int kTinySlotBytes = 196 * 1024;  // dynamic shared memory for row slots
+constexpr int kTinyCountBytes = (kTinyCounts + kMaxBins) * (int)sizeof(int);
 
-// The CTA's c rows (addresses listed in shared memory), 16-byte aligned:
-// warp 0 copies them through `slots` shared-memory slots with cp.async.bulk,
-// min(32, slots) rows a round (a lane per row, one mbarrier); with slots == 0
+// The CTA's c rows (addresses listed in shared memory; 0: a row the position
+// check dropped), by warp 0 with cp.async.bulk when slots > 0 (rows and
+// buffers 16-byte aligned): when every row has a slot, each row has its own
+// mbarrier and the lane that loaded it stores it as soon as it lands;
+// otherwise rounds of min(32, slots) rows on one mbarrier.  With slots == 0
 // every warp copies with registers (a warp per row from 64 bytes, a thread
-// per row below).  The bounded wait records A2AV_ERR_TIMEOUT and waits
-// (bounded) for the round's loads before leaving.
+// per row below).  A bounded wait that gives up records A2AV_ERR_TIMEOUT and
+// waits (bounded) once more for its load before the warp leaves.
 __device__ void copy_listed_rows(const unsigned long long* src, const unsigned long long* dst,
-                                 int c, long long rb, int slots, uint32_t slot0, uint32_t bar,
+                                 int c, long long rb, int slots, uint32_t slot0, uint32_t bar0,
                                  int* status) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (slots == 0) {
-    // (dst 0: a row the position check dropped)
     if (rb >= kWarpRowBytes) {
       for (int x = warp; x < c; x += kTinyThreads / 32)
         if (dst[x] != 0)
@@ -1179,6 +1271,29 @@ __device__ void copy_listed_rows(const unsigned long long* src, const unsigned l
     return;
   }
   if (warp != 0 || c == 0) return;
+  if (c <= slots) {  // one slot and one mbarrier a row; lane l takes rows l, l + 32
+    for (int x = lane; x < c; x += 32) {
+      mbar_init(bar0 + 8 * x, 1);
+      mbar_fence_init();
+    }
+    for (int x = lane; x < c; x += 32) {
+      mbar_expect_tx(bar0 + 8 * x, (unsigned)rb);
+      bulk_load(slot0 + (uint32_t)(x * rb), reinterpret_cast<const void*>(src[x]), (unsigned)rb,
+                bar0 + 8 * x);
+    }
+    for (int x = lane; x < c; x += 32) {
+      if (!mbar_wait(bar0 + 8 * x, 0)) {
+        record_error(status, A2AV_ERR_TIMEOUT);
+        mbar_wait(bar0 + 8 * x, 0);
+        continue;
+      }
+      if (dst[x] != 0)
+        bulk_store(reinterpret_cast<void*>(dst[x]), slot0 + (uint32_t)(x * rb), (unsigned)rb);
+    }
+    bulk_wait_all();
+    return;
+  }
+  const uint32_t bar = bar0;
   if (lane == 0) {
     mbar_init(bar, 1);
     mbar_fence_init();
@@ -1204,7 +1319,7 @@ __device__ void copy_listed_rows(const unsigned long long* src, const unsigned l
       break;
     }
     phase ^= 1;
-    if (lane < nr && dst[base + lane] != 0)  // (0: a row the position check dropped)
+    if (lane < nr && dst[base + lane] != 0)
       bulk_store(reinterpret_cast<void*>(dst[base + lane]), slot0 + (uint32_t)(lane * rb),
                  (unsigned)rb);
     else
@@ -1226,11 +1341,13 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   chain_release();
   chain_wait();
   __shared__ Plan pl;
-  __shared__ int cnt[kTinyCounts];  // [r][key]: counts, then the rank's key starts
-  __shared__ int run[kMaxBins];     // running count of each key while placing
   __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
-  __shared__ alignas(8) unsigned long long bar;
+  __shared__ alignas(8) unsigned long long bars[kTinyOwn];
   extern __shared__ __align__(128) unsigned char slot_mem[];
+  // The counters live in the row slots' memory (at least kTinyCountBytes),
+  // which the rows take over only after every item is placed.
+  int* const cnt = reinterpret_cast<int*>(slot_mem);  // [r][key]: counts, then key starts
+  int* const run = cnt + kTinyCounts;                  // running count of each key
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int W = D.W, K = D.K, NB = W * K;
   long long a, e;
@@ -1316,7 +1433,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
         const long long i = gi - D.item_first[r];
         const int key = v ? D.key[r][i] : -1 - lane;
         const int s = v ? D.src[r][i] : 0;
-        const unsigned same = __match_any_sync(kFull, key);
+        const unsigned same = same_key_lanes(key, v, key_bits(NB));
         long long pos = 0;
         if (v) pos = (long long)cnt[r * NB + key] + run[key] + __popc(same & lt);
         __syncwarp();
@@ -1337,7 +1454,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     }
   }
   __syncthreads();
-  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(&bar),
+  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(bars),
                    D.status);
 }
 
@@ -1349,7 +1466,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
                         int slots) {
   __shared__ Plan pl;
   __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
-  __shared__ alignas(8) unsigned long long bar;
+  __shared__ alignas(8) unsigned long long bars[kTinyOwn];
   extern __shared__ __align__(128) unsigned char slot_mem[];
   if (!build_plan(P, pl, kTileGranule)) return;  // (waits for the previous kernel first)
   const int tid = threadIdx.x, W = D.W, K = D.K, NB = W * K;
@@ -1397,7 +1514,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     own_dst[g - a] = (unsigned long long)(P.in[r] + i * rb);
   }
   __syncthreads();
-  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(&bar),
+  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(bars),
                    D.status);
 }
 
@@ -1465,7 +1582,7 @@ cudaError_t prepare_kernels(a2av_handle* h) {
 int tiny_slots(const DispatchParams& D, long long rb) {
   if (!D.vec16 || rb < kWarpRowBytes || rb > kTinySlotBytes) return 0;
   const long long n = kTinySlotBytes / rb;
-  return (int)(n < 32 ? n : 32);
+  return (int)(n < kTinyOwn ? n : kTinyOwn);
 }
 
 // One-kernel path: at most kTinyItems items, their counts fit shared memory,
@@ -1493,11 +1610,12 @@ void record_chain(a2av_handle* h, int kernels, int memsets, const char* copy) {
 // else the warp copy (rows of 64 bytes or more) or the thread copy.
 cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long long row_bytes,
                         cudaStream_t s, const char** name) {
-  if (D.vec16 && row_bytes >= 16 && row_bytes <= kStreamMaxRow) {
+  if (D.vec16 && row_bytes >= kStreamMinRow && row_bytes <= kStreamMaxRow) {
     const cudaError_t e = prepare_kernels(h);
     if (e != cudaSuccess) return e;
-    // batches of at most 16 KiB (32, 16 or 8 items, fewer when that leaves
-    // some warps without four), warps so that ~96 KiB are in flight per SM
+    // batches of at most 16 KiB (32, 16 or 8 items; 8 items of rows over 2
+    // KiB; fewer when that leaves some warps without four), warps so that
+    // ~96 KiB are in flight per SM
     int bs = 32;
     while (bs > 8 && bs * row_bytes > 16384) bs >>= 1;
     const long long batch_bytes = bs * row_bytes;
@@ -1523,6 +1641,9 @@ cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long 
     *name = "dispatch_copy_kernel";
     if (row_bytes < kWarpRowBytes)
       return launch_kernel(dispatch_copy_kernel<false>, dim3(h->sms * kCopyCtasPerSm),
+                           kCopyThreads, 0, s, true, P, D);
+    if (D.vec16 && row_bytes <= kVecMaxRow && row_bytes % 512 == 0)
+      return launch_kernel(dispatch_copy_kernel<true, true>, dim3(h->sms * kRows512CtasPerSm),
                            kCopyThreads, 0, s, true, P, D);
     return launch_kernel(dispatch_copy_kernel<true>, dim3(h->sms * kCopyCtasPerSmWarpRows),
                          kCopyThreads, 0, s, true, P, D);
@@ -1639,15 +1760,21 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   if (tiny_fits(h, D)) {  // decode sizes: one kernel, no workspace
     if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
     const int slots = tiny_slots(D, row_bytes);
-    e = launch_kernel(dispatch_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads,
-                      (size_t)slots * row_bytes, s, h->pdl, P, D, slots);
+    const size_t smem = (size_t)slots * row_bytes > (size_t)kTinyCountBytes
+                            ? (size_t)slots * row_bytes : (size_t)kTinyCountBytes;
+    e = launch_kernel(dispatch_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads, smem, s, h->pdl,
+                      P, D, slots);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
     record_chain(h, 1, 0, "dispatch_tiny_kernel");
     return A2AV_OK;
   }
   const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
   // Four ranges a count warp when even then every SM gets a count CTA.
-  const int rw = !small_path && (long long)W * ((ranges_max + 31) / 32) >= h->sms ? 4 : 1;
+#ifndef A2AV_COUNT_RW4
+#define A2AV_COUNT_RW4 1
+#endif
+  const int rw = A2AV_COUNT_RW4 && !small_path &&
+                         (long long)W * ((ranges_max + 31) / 32) >= h->sms ? 4 : 1;
   D.group_log2 = rw == 4 ? 5 : 3;
   D.groups_max = (ranges_max + (1LL << D.group_log2) - 1) >> D.group_log2;
   // One count CTA per rank scans its groups when a thread's share of one key
