@@ -214,6 +214,19 @@ def kernel_source_sha(kernel: str = "a2av_bulk_kernel") -> str:
     return h.hexdigest()[:16]
 
 
+def workload_key(args) -> str:
+    """The workload part of a traffic.json key: the config name plus what
+    differs from its defaults (cfg3 hidden size, tokens, per-rank dedup; cfg5
+    batch)."""
+    k = args.workload
+    if k == "cfg3":
+        k += (f"_h{args.hidden}" if args.hidden != 7168 else "") + \
+             (f"_t{args.tokens}" if args.tokens != 8192 else "") + ("_dedup" if args.dedup else "")
+    elif k == "cfg5" and args.batch != 8192:
+        k += f"_b{args.batch}"
+    return k
+
+
 def measured_traffic(kernel: str, algo_bytes: int):
     """DRAM bytes per launch from the committed ncu summary of this kernel on
     this workload ("kernel:workload"), scaled to this launch's algorithmic
@@ -488,7 +501,7 @@ def run_ours(args, light=False):
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_kind, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": measured_traffic(f"{kname}:{args.workload}", algo),
+                "traffic": measured_traffic(f"{kname}:{workload_key(args)}", algo),
                 "algorithmic_bytes_per_launch": algo}
 
     # ---- the same bytes through a device-to-device copy, interleaved -------
@@ -900,9 +913,7 @@ def run_fused_dispatch(args, light=False):
     roofline = {"bound": "hbm", "kernel": f"a2av_dispatch (chain ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
-                "traffic": measured_traffic(copy_kernel + ":" + args.workload +
-                                            (f"_h{args.hidden}" if args.workload == "cfg3"
-                                             and args.hidden != 7168 else ""), algo),
+                "traffic": measured_traffic(f"{copy_kernel}:{workload_key(args)}", algo),
                 "algorithmic_bytes_per_launch": algo}
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1035,9 +1046,7 @@ def run_fused_combine(args, light=False):
                                           f"ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),
-                "traffic": measured_traffic(copy_kernel + ":" + args.workload +
-                                            (f"_h{args.hidden}" if args.workload == "cfg3"
-                                             and args.hidden != 7168 else "") + "_combine", algo),
+                "traffic": measured_traffic(f"{copy_kernel}:{workload_key(args)}_combine", algo),
                 "algorithmic_bytes_per_launch": algo}
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -167,9 +167,9 @@ def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=
     return ref, ref_so, ref_pos, ref_S
 
 
-def aligned_copy_kernel(rb: int) -> str:
+def aligned_copy_kernel(rb: int, combine: bool = False) -> str:
     """The kernel that moves 16-byte aligned rows of rb bytes past the
-    one-kernel size: the register warp copy below 1.5 KiB, the cp.async
-    stream copy up to 4 KiB, the cp.async.bulk gather up to 32 KiB."""
-    return ("dispatch_copy_kernel" if rb < 1536 else
-            "dispatch_stream_kernel" if rb <= 4096 else "dispatch_gather_kernel")
+    one-kernel size: the cp.async.bulk gather for rows of 1.5 KiB .. 32 KiB
+    (the combine: from 64 B), register copies otherwise."""
+    lo = 64 if combine else 1536
+    return "dispatch_gather_kernel" if lo <= rb <= 32768 else "dispatch_copy_kernel"

@@ -178,3 +178,13 @@ def test_spawned_replicas_aggregate_over_gloo(tmp_path, capfd):
     line = json.loads(lines[0])
     assert line["world"] == 2 and line["max_s"] == 2.0 and line["value"] == 6.0
     assert line["argv"] == ["--gpus", "2", "--steps", "3"]
+
+
+def test_traffic_keys_name_the_workload_variant():
+    import argparse
+    a = argparse.Namespace(workload="cfg3", hidden=512, tokens=8192, dedup=False, batch=8192)
+    assert bench.workload_key(a) == "cfg3_h512"
+    a.hidden, a.tokens = 7168, 128
+    assert bench.workload_key(a) == "cfg3_t128"
+    a.workload = "cfg2"
+    assert bench.workload_key(a) == "cfg2"

@@ -185,9 +185,9 @@ def test_decode_size_and_host_checks():
 
 
 # The combine's copy by row size (many items: the check kernel, then the
-# cp.async stream copy up to 2 KiB rows or the cp.async.bulk gather above)
-# and its one-kernel path (at most 4096 items: row slots for aligned rows,
-# registers otherwise).
+# cp.async.bulk gather: lanes issuing their own rows up to 2 KiB, one-row
+# rings above) and its one-kernel path (at most 4096 items: row slots for
+# aligned rows, registers otherwise).
 @pytest.mark.parametrize("rb,m", [(64, 20011), (512, 9001), (1024, 6007), (2048, 6007),
                                   (4096, 3001), (14336, 1801), (32768, 1801)])
 def test_aligned_copy_shapes(rb, m):
@@ -201,7 +201,7 @@ def test_aligned_copy_shapes(rb, m):
     outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
     peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
     assert _combine_checked(K, peers, S, key, pos, rb,
-                            expect_copy=aligned_copy_kernel(rb)) == a2av.OK
+                            expect_copy=aligned_copy_kernel(rb, combine=True)) == a2av.OK
 
 
 @pytest.mark.parametrize("rb", [1, 8, 16, 64, 1024, 14336, 40000])

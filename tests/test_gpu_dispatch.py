@@ -132,14 +132,15 @@ def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb):
 
 
 @pytest.mark.parametrize("rb", [8, 64])
-@pytest.mark.parametrize("W,K,kernels", [(2, 13, 2), (2, 200, 3)])
-def test_four_ranges_a_count_warp(W, K, kernels, rb):
-    """Batches so large that even with four ranges a warp every SM gets a
-    count block (640 K items a rank, the embedding-key size): 32-range
-    groups, scanned by the count kernel's last block (26 keys) or by the
-    scan kernel (400 keys, more than one block thread a key)."""
-    rng = np.random.default_rng(K + rb)
-    m, n = 640_000, 4000
+@pytest.mark.parametrize("W,K,m,kernels", [(2, 13, 589_824, 2), (2, 13, 640_000, 3),
+                                           (2, 200, 640_000, 3)])
+def test_embedding_size_batches(W, K, m, kernels, rb):
+    """Batches of the embedding-key size (640 K items a rank): the count
+    kernel's last block scans up to 288 groups of 2048 items over 26 keys (9
+    block threads a key, 32 groups each); past that, or with 400 keys (more
+    than one block thread a key), the scan kernel runs."""
+    rng = np.random.default_rng(K + rb + m)
+    n = 4000
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
     src = [rng.integers(0, n, m - 1000 * r).astype(np.int32) for r in range(W)]
     key = [rng.integers(0, W * K, m - 1000 * r).astype(np.int32) for r in range(W)]
@@ -149,9 +150,9 @@ def test_four_ranges_a_count_warp(W, K, kernels, rb):
 
 
 # Aligned rows by the copy kernels' shapes (the register warp copy below
-# 1.5 KiB, in flat runs or by 512-byte pieces; the stream copy's 16- and
-# 8-item batches for 1.5 .. 4 KiB rows; the gather's rings for 8, 16 and
-# 32 KiB rows), with ragged last batches per rank.
+# 1.5 KiB, in flat runs or by 512-byte pieces; the gather's lane-issued
+# 8-row stages for 1.5 .. 2 KiB rows and its one-row rings, items in
+# strided order, for 3 .. 32 KiB rows), with ragged last batches per rank.
 @pytest.mark.parametrize("rb,m", [(64, 20011), (256, 20011), (272, 9001), (512, 9001),
                                   (1024, 6007), (1536, 6007), (2048, 6007), (3072, 3001),
                                   (4096, 3001), (8192, 1801), (14336, 1801), (16384, 1801),

@@ -45,3 +45,41 @@ def test_starved_stage_times_out_and_context_survives(monkeypatch, path):
     torch.cuda.synchronize()
     # the context is intact: a normal exchange right after is exact
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path, expect_path=path)
+
+
+@pytest.mark.parametrize("rb,combine", [(2048, False), (14336, False), (512, True)])
+def test_starved_gather_stage_times_out_and_context_survives(monkeypatch, rb, combine):
+    """The same hook on the dispatch's cp.async.bulk gather (lane-issued
+    16- or 8-row stages, one-row rings) and in combine mode: the first stage
+    of the first warp never completes, the warp reports A2AV_ERR_TIMEOUT and
+    waits (bounded) for the copies it issued; a normal dispatch on a fresh
+    handle afterwards is exact."""
+    from tests._gpu import dispatch_checked
+    rng = np.random.default_rng(rb)
+    W, K, n, m = 4, 3, 64, 2000  # 8000 items: past the one-kernel path
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, n, m).astype(np.int32) for _ in range(W)]
+    key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
+    d_rows = [torch.from_numpy(r).cuda() for r in rows]
+    d_src = [torch.from_numpy(x).cuda() for x in src]
+    d_key = [torch.from_numpy(x).cuda() for x in key]
+    d_pos = [torch.empty(m, dtype=torch.int64, device="cuda") for _ in range(W)]
+    out = [torch.empty(W * m * rb, dtype=torch.uint8, device="cuda") for _ in range(W)]
+    so = torch.empty((W, 2, W), dtype=torch.int64, device="cuda")
+    isp = torch.empty((W, W), dtype=torch.int64, device="cuda")
+    items = [torch.empty(m * rb, dtype=torch.uint8, device="cuda") for _ in range(W)]
+    if combine:
+        with a2av.A2av(W) as eng:
+            eng.dispatch(d_rows, d_src, d_key, K, out, so, d_pos, rb, in_splits=isp)
+            assert eng.status() == a2av.OK
+    monkeypatch.setenv("A2AV_DEBUG_STARVE", "1")
+    with a2av.A2av(W) as eng:
+        monkeypatch.delenv("A2AV_DEBUG_STARVE")
+        if combine:
+            eng.combine_items(out, isp, d_key, d_pos, K, items, rb)
+        else:
+            eng.dispatch(d_rows, d_src, d_key, K, out, so, d_pos, rb, in_splits=isp)
+        assert eng.status() == a2av.ERR_TIMEOUT
+        assert eng.last_dispatch()["copy_kernel"] == "dispatch_gather_kernel"
+    torch.cuda.synchronize()
+    dispatch_checked(K, rows, src, key, rb)

@@ -26,12 +26,13 @@
 //   3. copy   (the a2av prologue builds the plan from S, which also checks
 //      capacities and NULL buffers; then S is published and every item's row
 //      goes straight to its place in the output of its destination):
-//      - 16-byte aligned rows of 64 bytes .. 32 KiB: the cp.async.bulk
-//        gather -- each warp takes batches of consecutive items, every lane
-//        issuing the copy of its own item's row into its slot of a
+//      - 16-byte aligned rows of 1.5 KiB .. 32 KiB (the combine: from 64 B):
+//        the cp.async.bulk gather -- up to 2 KiB, every lane of a warp
+//        issues the copy of its own item's row into its slot of a 16-row
 //        shared-memory stage (one mbarrier per stage), then its own bulk
-//        store; the item metadata of the next two batches is loaded while
-//        the current one is copied;
+//        store, with as many warps per CTA as keep ~96 KiB of loads in flight
+//        per SM; above 2 KiB one row a stage, issued by one lane per warp;
+//        the item metadata is loaded two and one batches ahead;
 //      - other rows of 64 bytes or more: a warp per batch of rows (registers);
 //      - rows under 64 bytes: the count kernel's successor places and copies
 //        the rows of a whole range per warp (thread per row).
@@ -97,6 +98,7 @@ struct DispatchParams {
   int group_log2;                    // a group is 1 << group_log2 ranges (8 or 32)
   int fuse_scan;                     // the count kernel's last CTA per rank scans the groups
   int bs;                            // items per gather batch (8, 16 or 32)
+
   long long pos_stride;
   int W, K;
 };
@@ -243,13 +245,11 @@ __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) 
 // 8RW c + RW w .. + RW - 1 (all their keys and source rows loaded at once),
 // 32 items at a time: a ballot per key bit groups equal keys, a lane's rank
 // among them plus the range's running count of its key is its inrank, and
-// each key's leader advances that count.  RW = 4
-// serves batches so large that one CTA per SM still has four ranges a warp
-// (fewer groups: the last CTA can still scan them).  Four CTAs an SM (64
-// registers) keep every RW = 1 grid resident in one wave: RW = 4 takes over
-// before a grid passes W * ceil(ranges / 32) >= SMs, i.e. 4 x SMs CTAs.
+// each key's leader advances that count.  RW = 1 (the default) at five CTAs
+// an SM (48 registers) keeps a batch of 760 groups of 2048 items (1.5 M items) resident
+// in one wave; RW = 4 (fewer, longer CTAs, for sweeps) was measured slower.
 template <int RW>
-__global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 4 : 2)
+__global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 5 : 2)
     dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
   chain_wait();
@@ -672,7 +672,7 @@ __device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc,
   }
 }
 
-// Register copies (rows the stream copy and the gather do not take):
+// Register copies (rows the gather does not take):
 // kWarpRows -- rows of kWarpRowBytes or more, a warp per batch of rows; else
 // a thread per row.  kRows512: every row and buffer 16-byte aligned and rows
 // a multiple of 512 bytes (the host checks).  Each instantiation holds one
@@ -869,6 +869,33 @@ struct GatherItem {
   bool v;          // the lane holds an item
 };
 
+// Item g of the global order (rank-major) when `ok`, else none.
+__device__ __forceinline__ GatherItem gather_item_at(const DispatchParams& D, long long g, bool ok) {
+  GatherItem x;
+  x.i = 0;
+  x.spos = 0;
+  x.r = 0;
+  x.key = 0;
+  x.src = 0;
+  x.inr = 0;
+  x.v = false;
+  if (!ok) return x;
+  int r = 0;
+  while (r + 1 < D.W && D.item_first[r + 1] <= g) ++r;
+  const long long i = g - D.item_first[r];
+  x.r = r;
+  x.i = i;
+  x.v = true;
+  x.key = D.key[r][i];
+  if (D.combine) {
+    x.spos = D.sorted_pos[r][i];
+  } else {
+    x.src = D.src[r][i];
+    x.inr = D.inrank[(long long)r * D.pos_stride + i];
+  }
+  return x;
+}
+
 // Batch b (global over the ranks, bs items each) -> lane's item; b < 0: none.
 __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long long b, int lane) {
   GatherItem x;
@@ -917,8 +944,8 @@ template <int NS, int LEAD, int NWK, int IPS>
 __global__ void __launch_bounds__(32 * NWK, 1)
     dispatch_gather_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 stages ahead of stores");
-  static_assert(NWK >= 1 && NWK <= 4 && IPS >= 1 && IPS <= 32 && (IPS & (IPS - 1)) == 0,
-                "one to four warps, a power-of-two number of slots per stage");
+  static_assert(NWK >= 1 && NWK <= 16 && IPS >= 1 && IPS <= 32 && (IPS & (IPS - 1)) == 0,
+                "one to sixteen warps, a power-of-two number of slots per stage");
   chain_wait();
   if (flagged(D)) return;
   __shared__ Plan pl;
@@ -930,13 +957,28 @@ __global__ void __launch_bounds__(32 * NWK, 1)
   publish_splits(D);
   const int lane = threadIdx.x & 31;
   const int warp = NWK == 1 ? 0 : (int)(threadIdx.x >> 5);  // a constant for one warp
-  const int W = D.W, K = D.K, bs = D.bs;
+  // One-row stages (IPS == 1) take the items in a strided order: the warp's
+  // k-th row is item wg + k WG of the global order, so that the warps of the
+  // grid work on neighbouring items at any time.  Otherwise batches of bs
+  // consecutive items of one rank.  With one row a stage, only lane 0 waits,
+  // stores and tracks bulk groups (the row's lane issues its load).
+  constexpr bool kStrided = IPS == 1;
+  const int W = D.W, K = D.K, bs = kStrided ? 32 : D.bs;
   const int unit = bs < IPS ? bs : IPS, spb = bs / unit;  // slots used per stage, stages per batch
   const long long rb = P.rb;
   const long long WG = (long long)gridDim.x * NWK, wg = (long long)blockIdx.x * NWK + warp;
-  const long long nbatch = D.batch_first[W];
-  const long long nt = nbatch > wg ? (nbatch - wg + WG - 1) / WG : 0;  // this warp's batches
+  const long long total = D.item_first[W], nbatch = D.batch_first[W];
+  const long long mine = total > wg ? (total - wg + WG - 1) / WG : 0;  // strided: this warp's items
+  const long long nt = kStrided ? (mine + 31) / 32
+                                : (nbatch > wg ? (nbatch - wg + WG - 1) / WG : 0);  // its batches
   if (nt == 0) return;
+  auto fetch = [&](long long t) -> GatherItem {  // the lane's item of the warp's batch t
+    if (kStrided) {
+      const long long k = t * 32 + lane;
+      return gather_item_at(D, wg + k * WG, t < nt && k < mine);
+    }
+    return gather_item(D, t < nt ? wg + t * WG : -1, lane);
+  };
   const uint32_t stage_bytes = (uint32_t)(IPS * rb);
   const uint32_t bar0 = smem_u32(&bars[warp][0]);
   const uint32_t st0 = smem_u32(stages) + (uint32_t)(NS * warp) * stage_bytes;
@@ -951,6 +993,18 @@ __global__ void __launch_bounds__(32 * NWK, 1)
   // Wait for stage j's loads and store its rows; false on a timeout.
   auto drain = [&](long long j) -> bool {
     const int s = (int)(j % NS);
+    if (IPS == 1) {
+      bool done = true;
+      if (lane == 0) {
+        done = mbar_wait(bar0 + 8 * s, (unsigned)((j / NS) & 1));
+        if (done && smask[warp][s] != 0)
+          bulk_store(reinterpret_cast<void*>(sdst[warp][s][0]), st0 + (uint32_t)s * stage_bytes,
+                     (unsigned)rb);
+        else if (done)
+          bulk_commit();
+      }
+      return __shfl_sync(kFull, done ? 1 : 0, 0) != 0;
+    }
     if (!mbar_wait_warp(bar0 + 8 * s, (unsigned)((j / NS) & 1))) return false;
     const unsigned mask = smask[warp][s];
     const uint32_t st = st0 + (uint32_t)s * stage_bytes;
@@ -968,11 +1022,11 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     return true;
   };
 
-  GatherItem a0 = gather_item(D, wg, lane);
-  GatherItem a1 = gather_item(D, nt > 1 ? wg + WG : -1, lane);
+  GatherItem a0 = fetch(0);
+  GatherItem a1 = fetch(1);
   long long b0 = a0.v && !D.combine ? key_base(D, a0.r, a0.i, a0.key) : 0;
   for (long long t = 0; t < nt && ok; ++t) {
-    const GatherItem a2 = gather_item(D, t + 2 < nt ? wg + (t + 2) * WG : -1, lane);
+    const GatherItem a2 = fetch(t + 2);
     const long long b1 = a1.v && !D.combine ? key_base(D, a1.r, a1.i, a1.key) : 0;
     // batch t's row addresses
     long long src = 0, dst = 0;
@@ -992,7 +1046,8 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     }
     for (int u = 0; u < spb; ++u) {
       const int s = (int)(issued % NS);
-      if (issued >= NS) bulk_wait_read<NS - LEAD - 1>();  // the store that last read stage s
+      if (issued >= NS && (IPS > 1 || lane == 0))
+        bulk_wait_read<NS - LEAD - 1>();  // the store that last read stage s
       __syncwarp();
       const int slot = lane - u * unit;
       const bool mine = a0.v && slot >= 0 && slot < unit;
@@ -1040,132 +1095,7 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     }
     __syncwarp();
   }
-  bulk_wait_all();
-}
-
-// ------------------------------------------------------------- stream --
-// 16-byte asynchronous copies (cp.async, global -> shared, no registers
-// held while in flight) for 16-byte aligned rows of 16 B .. 2 KiB: a warp
-// takes every (grid x warps)-th batch of bs consecutive items of one rank
-// (lane i item i), loads the batch's rows into one of its two shared-memory
-// buffers -- the rows cut into 16-byte pieces spread over the lanes -- and,
-// while that batch is in flight, writes the previous one from the other
-// buffer to its destinations with st.global.v4.  A warp thus keeps a whole
-// batch (up to 16 KiB) of loads in flight without spending registers on it,
-// and a CTA of up to 16 warps keeps ~96 KiB in flight per SM.  The batch
-// metadata is loaded two and one batches ahead, as in the gather.
-__device__ __forceinline__ void cp_async16(uint32_t smem, const void* g) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(g) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__global__ void __launch_bounds__(512, 1)
-    dispatch_stream_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
-  chain_wait();
-  if (flagged(D)) return;
-  __shared__ Plan pl;
-  extern __shared__ __align__(128) unsigned char stream_bufs[];
-  if (!build_plan(P, pl, kTileGranule)) return;
-  publish_splits(D);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int W = D.W, K = D.K, bs = D.bs;
-  const long long rb = P.rb;
-  const unsigned V = (unsigned)(rb >> 4);  // 16-byte pieces per row
-  const uint32_t half = (uint32_t)(bs * rb);
-  const uint32_t buf0 = smem_u32(stream_bufs) + (uint32_t)warp * 2u * half;
-  const long long WG = (long long)gridDim.x * nw, wg = (long long)blockIdx.x * nw + warp;
-  const long long nbatch = D.batch_first[W];
-  const long long nt = nbatch > wg ? (nbatch - wg + WG - 1) / WG : 0;  // this warp's batches
-  if (nt == 0) return;
-  GatherItem a0 = gather_item(D, wg, lane);
-  GatherItem a1 = gather_item(D, nt > 1 ? wg + WG : -1, lane);
-  long long b0 = a0.v && !D.combine ? key_base(D, a0.r, a0.i, a0.key) : 0;
-  long long pdst = 0;  // the previous batch: this lane's row destination (0: none)
-  unsigned prows = 0;  // and its rows
-  for (long long t = 0; t <= nt; ++t) {
-    long long dst = 0;
-    unsigned rows = 0;
-    GatherItem a2;
-    long long b1 = 0;
-    if (t < nt) {
-      a2 = gather_item(D, t + 2 < nt ? wg + (t + 2) * WG : -1, lane);
-      b1 = a1.v && !D.combine ? key_base(D, a1.r, a1.i, a1.key) : 0;
-      long long src = 0;
-      if (a0.v) {
-        const int p = a0.key / K;
-        const long long grouped = pl.out_off[p][a0.r] - pl.in_off[a0.r][p];
-        if (D.combine) {
-          src = (long long)(P.out[p] + (grouped + a0.spos) * rb);
-          dst = (long long)(P.in[a0.r] + a0.i * rb);
-        } else {
-          const long long pos = b0 + a0.inr;
-          D.sorted_pos[a0.r][a0.i] = pos;
-          src = (long long)(P.in[a0.r] + (long long)a0.src * rb);
-          dst = (long long)(P.out[p] + (grouped + pos) * rb);
-          if (!in_group(pl, a0.r, p, pos, D.status)) src = dst = 0;
-        }
-      }
-      // the batch's rows into buffer t & 1 (rows of lanes without an item skipped)
-      const unsigned held = __ballot_sync(kFull, a0.v);
-      rows = held ? 32u - __clz(held) : 0u;
-      const uint32_t buf = buf0 + (uint32_t)(t & 1) * half;
-      if (V >= 32) {  // a row at a time, its pieces over the lanes
-        for (unsigned j = 0; j < rows; ++j) {
-          const long long sj = __shfl_sync(kFull, src, (int)j);
-          if (sj != 0)
-#pragma unroll 2
-            for (unsigned c = lane; c < V; c += 32)
-              cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
-        }
-      } else {  // 32 / V rows at a time, lane -> (row, piece) fixed
-        const unsigned rpp = 32u / V, jl = lane / V, c = lane - jl * V;
-        for (unsigned j0 = 0; j0 < rows; j0 += rpp) {
-          const unsigned j = j0 + jl;
-          const long long sj = __shfl_sync(kFull, src, (int)(j & 31u));
-          if (jl < rpp && j < rows && sj != 0)
-            cp_async16(buf + j * (uint32_t)rb + 16u * c, reinterpret_cast<const void*>(sj + 16LL * c));
-        }
-      }
-      cp_async_commit();
-    }
-    if (t > 0) {  // the previous batch, from buffer (t - 1) & 1
-      if (t < nt)
-        cp_async_wait<1>();
-      else
-        cp_async_wait<0>();
-      __syncwarp();
-      const uint32_t pbuf = buf0 + (uint32_t)((t - 1) & 1) * half;
-      if (V >= 32) {
-        for (unsigned j = 0; j < prows; ++j) {
-          const long long dj = __shfl_sync(kFull, pdst, (int)j);
-          if (dj != 0)
-#pragma unroll 2
-            for (unsigned c = lane; c < V; c += 32)
-              st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
-        }
-      } else {
-        const unsigned rpp = 32u / V, jl = lane / V, c = lane - jl * V;
-        for (unsigned j0 = 0; j0 < prows; j0 += rpp) {
-          const unsigned j = j0 + jl;
-          const long long dj = __shfl_sync(kFull, pdst, (int)(j & 31u));
-          if (jl < rpp && j < prows && dj != 0)
-            st_stream(reinterpret_cast<void*>(dj + 16LL * c), lds128(pbuf + j * (uint32_t)rb + 16u * c));
-        }
-      }
-      __syncwarp();  // every lane has read the buffer before the next batch refills it
-    }
-    pdst = dst;
-    prows = rows;
-    a0 = a1;
-    a1 = a2;
-    b0 = b1;
-  }
+  if (IPS > 1 || lane == 0) bulk_wait_all();
 }
 
 // The gather's ring shapes by row size: NWK x NS stages of IPS slots, at most
@@ -1177,59 +1107,59 @@ __global__ void __launch_bounds__(512, 1)
 #ifndef A2AV_GATHER_LEAD
 #define A2AV_GATHER_LEAD 4
 #endif
+// Aligned rows this long or longer take the gather (the combine from
+// A2AV_GATHER_MIN_ROW, the dispatch from A2AV_DISPATCH_GATHER_MIN_ROW).
+// Measured on the MoE workload (8192 tokens, W=8, us, gather / register warp
+// copy): combine 24.3 / 27.6 at 128 B rows, 50.1 / 51.7 at 1 KiB; dispatch
+// 34.9 / 31.8 at 128 B, 57.2 / 52.5 at 1 KiB, 82.9 / -- at 2 KiB (the
+// dispatch's batch metadata -- key bases -- costs its few issuing warps more).
 #ifndef A2AV_GATHER_MIN_ROW
-#define A2AV_GATHER_MIN_ROW 2048  // aligned rows this long or longer take the gather
+#define A2AV_GATHER_MIN_ROW 64
+#endif
+#ifndef A2AV_DISPATCH_GATHER_MIN_ROW
+#define A2AV_DISPATCH_GATHER_MIN_ROW 1536
 #endif
 constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
+constexpr long long kDispatchGatherMinRow = A2AV_DISPATCH_GATHER_MIN_ROW;
 constexpr long long kGatherMaxRow = 32 * 1024;
 constexpr int kGatherSmem = 192 * 1024;
-// Aligned rows of kStreamMinRow .. kStreamMaxRow bytes take the stream copy.
-// Measured (MoE dispatch / fused combine, 8192 tokens, W=8, us): 2 KiB rows
-// 91.7 / 106.7 against 125.1 / 130.2 by the gather; at 512 B and 1 KiB rows
-// the register warp copy is ahead (34.2 / 30.2 and 54.0 / 52.1 against
-// 56.0 / 48.2 and 63.5 / 54.3).
-#ifndef A2AV_STREAM_MIN_ROW
-#define A2AV_STREAM_MIN_ROW 1536
-#endif
-#ifndef A2AV_STREAM_MAX_ROW
-#define A2AV_STREAM_MAX_ROW 4096
-#endif
-constexpr long long kStreamMinRow = A2AV_STREAM_MIN_ROW;
-constexpr long long kStreamMaxRow = A2AV_STREAM_MAX_ROW;
-constexpr long long kStreamFlight = 96 * 1024;  // bytes of loads in flight per CTA
-constexpr int kStreamSmem = 192 * 1024;
+
 using GatherKernel = void (*)(Params, DispatchParams);
 struct GatherShape {
   long long max_row;
   GatherKernel kernel;
   int nwk, ns, ips;
 };
-#ifndef A2AV_GATHER_LANES
-#define A2AV_GATHER_LANES 0  // 1: every lane issues its own row's copy (slower, measured)
-#endif
+// Rows of 64 B .. 2 KiB: every lane of a warp issues its own row's copy,
+// 16-row stages, loads two stages ahead, and as many warps as keep ~96 KiB
+// of loads in flight per SM (3 warps at 1 KiB rows .. 16 at 128 B).  A
+// standalone probe (256 MiB of rows to scattered destinations) measured this
+// shape at 3134 / 3060 / 2990 GB/s moved for 1 KiB / 512 B / 256 B rows,
+// against 1877 / 994 / 511 with one warp of 32-row stages and 2580 / 2155 /
+// 1283 by register copies: with enough warps issuing, the per-copy cost of
+// small cp.async.bulk operations is hidden.
 const GatherShape kGatherShapes[] = {
-#if A2AV_GATHER_LANES
-    {256, dispatch_gather_kernel<kGatherNs, kGatherLead, 4, 32>, 4, kGatherNs, 32},
-    {512, dispatch_gather_kernel<kGatherNs, kGatherLead, 2, 32>, 2, kGatherNs, 32},
-    {1024, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 32>, 1, kGatherNs, 32},
-    {2048, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 16>, 1, kGatherNs, 16},
-    {4096, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 8>, 1, kGatherNs, 8},
-    {8192, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 4>, 1, kGatherNs, 4},
-#else
+    {128, dispatch_gather_kernel<4, 2, 16, 16>, 16, 4, 16},
+    {256, dispatch_gather_kernel<4, 2, 12, 16>, 12, 4, 16},
+    {512, dispatch_gather_kernel<4, 2, 6, 16>, 6, 4, 16},
+    {1024, dispatch_gather_kernel<4, 2, 3, 16>, 3, 4, 16},
+    {2048, dispatch_gather_kernel<4, 2, 3, 8>, 3, 4, 8},
     // one row a stage, one issuing lane per warp, several warps with rings of
-    // their own (MoE dispatch, 8192 tokens, W=8: 2 / 4 KiB rows 113 / 154 us
-    // with four warps x 6 stages; 8 KiB rows 279 us with two warps x 12)
+    // their own (MoE dispatch, 8192 tokens, W=8: 4 KiB rows 149-154 us with
+    // four warps x 6 stages; 8 KiB rows 279 us with two warps x 12)
     {4096, dispatch_gather_kernel<6, 4, 4, 1>, 4, 6, 1},
     {8192, dispatch_gather_kernel<12, 10, 2, 1>, 2, 12, 1},
-#endif
     // 14 KiB MoE rows: 12 x 16 KiB stages, loads 10 ahead (measured best for
     // a one-row ring: 8 stages / 6 ahead 3 % slower, two CTAs an SM 4-6 %)
     {16384, dispatch_gather_kernel<12, 10, 1, 1>, 1, 12, 1},
     {32768, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 1>, 1, kGatherNs, 1},
 };
-static_assert(4 * 6 * 4096 <= kGatherSmem && 2 * 12 * 8192 <= kGatherSmem &&
-                  12 * 16384 <= kGatherSmem && kGatherNs * 32768 <= kGatherSmem,
+static_assert(16 * 4 * 16 * 128 <= kGatherSmem && 12 * 4 * 16 * 256 <= kGatherSmem &&
+                  6 * 4 * 16 * 512 <= kGatherSmem && 3 * 4 * 16 * 1024 <= kGatherSmem &&
+                  3 * 4 * 8 * 2048 <= kGatherSmem && 4 * 6 * 4096 <= kGatherSmem &&
+                  2 * 12 * 8192 <= kGatherSmem && 12 * 16384 <= kGatherSmem &&
+                  kGatherNs * 32768 <= kGatherSmem,
               "every ring fits the gather's shared memory");
 
 // ------------------------------------------------------------ one kernel --
@@ -1241,8 +1171,10 @@ constexpr int kTinyThreads = 256;
 constexpr int kTinyItems = 4096;
 constexpr int kTinyCounts = 2048;  // W * W * K counters in shared memory
 constexpr int kTinyOwn = 64;
-constexpr int kTinySlotBytes = 196 * 1024;  // dynamic shared memory for row slots
-constexpr int kTinyCountBytes = (kTinyCounts + kMaxBins) * (int)sizeof(int);
+// Dynamic shared memory of the one-kernel paths: row slots, then (dispatch)
+// the counters; 200 KiB with the ~27 KB of static shared memory stays within
+// the 227 KiB a CTA may have (14 slots of 14 KiB MoE rows plus counters).
+constexpr int kTinyDynBytes = 200 * 1024;
 
 // The CTA's c rows (addresses listed in shared memory; 0: a row the position
 // check dropped), by warp 0 with cp.async.bulk when slots > 0 (rows and
@@ -1344,48 +1276,79 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
   __shared__ alignas(8) unsigned long long bars[kTinyOwn];
   extern __shared__ __align__(128) unsigned char slot_mem[];
-  // The counters live in the row slots' memory (at least kTinyCountBytes),
-  // which the rows take over only after every item is placed.
-  int* const cnt = reinterpret_cast<int*>(slot_mem);  // [r][key]: counts, then key starts
-  int* const run = cnt + kTinyCounts;                  // running count of each key
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int W = D.W, K = D.K, NB = W * K;
+  const long long rb = P.rb;
+  // The counters follow the row slots in dynamic shared memory.
+  int* const cnt = reinterpret_cast<int*>(slot_mem + (((long long)slots * rb + 15) & ~15LL));
+  int* const run = cnt + W * NB;  // [r][key]: counts, then key starts; running count of each key
   long long a, e;
   tiny_share(D, &a, &e);
   int ra = 0;  // the rank of item a
   while (ra + 1 < W && D.item_first[ra + 1] <= a) ++ra;
   const long long ia = a - D.item_first[ra];
+  // When every row of this CTA's share has a slot, thread t loads the share's
+  // t-th source row at once (its index range-checked first; an invalid item
+  // loads nothing and is never stored): the loads land while the items are
+  // counted, the plan built and the rows placed.  Every exit below waits for
+  // them first.
+  const int c = (int)(e - a);
+  const bool early = slots > 0 && c <= slots;
+  if (early && tid < c) {
+    const long long g = a + tid;
+    int r = ra;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    const int src = __ldg(D.src[r] + (g - D.item_first[r]));
+    const uint32_t bar = smem_u32(&bars[tid]);
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    if (src >= 0 && src < D.rows[r]) {
+      mbar_expect_tx(bar, (unsigned)rb);
+      bulk_load(smem_u32(slot_mem) + (uint32_t)(tid * rb), P.in[r] + (long long)src * rb,
+                (unsigned)rb, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+  }
+  auto settle = [&]() {  // (bounded) every early load has landed
+    if (early && tid < c) mbar_wait(smem_u32(&bars[tid]), 0);
+  };
   for (int x = tid; x < W * NB; x += kTinyThreads) cnt[x] = 0;
   for (int x = tid; x < NB; x += kTinyThreads) run[x] = 0;
   __syncthreads();
   // every item: validity, its rank's key counts, and for rank ra the counts
-  // of the items before this CTA's share
+  // of the items before this CTA's share.  Thread t takes items t, t + 256,
+  // ... of the global order (at most kTinyItems / kTinyThreads), all their
+  // keys and source rows loaded at once.
+  constexpr int kPer = kTinyItems / kTinyThreads;
+  const long long n = D.item_first[W];
+  int kk[kPer], ss[kPer], rr[kPer];
+  long long ii[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const long long g = (long long)q * kTinyThreads + tid;
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    rr[q] = g < n ? r : -1;
+    ii[q] = g - D.item_first[r];
+    kk[q] = g < n ? __ldg(D.key[r] + ii[q]) : 0;
+    ss[q] = g < n ? __ldg(D.src[r] + ii[q]) : 0;
+  }
   int bad = 0;
-  for (int r = 0; r < W; ++r) {
-    const long long m = D.items[r];
-    for (long long i0 = 0; i0 < m; i0 += 4 * kTinyThreads) {
-      int k[4], s[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long i = i0 + q * kTinyThreads + tid;
-        k[q] = i < m ? D.key[r][i] : 0;
-        s[q] = i < m ? D.src[r][i] : 0;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long i = i0 + q * kTinyThreads + tid;
-        if (i >= m) continue;
-        if (k[q] < 0 || k[q] >= NB || s[q] < 0 || s[q] >= D.rows[r]) {
-          bad = 1;
-          continue;
-        }
-        atomicAdd(&cnt[r * NB + k[q]], 1);
-        if (r == ra && i < ia) atomicAdd(&run[k[q]], 1);
-      }
+  for (int q = 0; q < kPer; ++q) {
+    const int r = rr[q];
+    if (r < 0) continue;
+    if (kk[q] < 0 || kk[q] >= NB || ss[q] < 0 || ss[q] >= D.rows[r]) {
+      bad = 1;
+      continue;
     }
+    atomicAdd(&cnt[r * NB + kk[q]], 1);
+    if (r == ra && ii[q] < ia) atomicAdd(&run[kk[q]], 1);
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
+    settle();
     return;
   }
   // per rank: key starts (exclusive scan in place) and S[r][*]
@@ -1410,13 +1373,16 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     if (pl.s[x / W][x % W] > P.limit) over = 1;
   if (__syncthreads_or(over)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_SPLITS);
+    settle();
     return;
   }
-  if (!plan_from_splits(P, pl, kTileGranule, blockIdx.x, gridDim.x)) return;
+  if (!plan_from_splits(P, pl, kTileGranule, blockIdx.x, gridDim.x)) {
+    settle();
+    return;
+  }
   if (blockIdx.x == 0 && D.in_splits_out != nullptr)
     for (int x = tid; x < W * W; x += kTinyThreads) D.in_splits_out[x] = pl.s[x / W][x % W];
   // place the CTA's items, rank by rank, 32 at a time (warp 0)
-  const long long rb = P.rb;
   if (warp == 0) {
     const unsigned lt = (1u << lane) - 1u;
     int idx = 0, r = ra;
@@ -1454,8 +1420,21 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     }
   }
   __syncthreads();
-  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(bars),
-                   D.status);
+  if (early) {  // each loaded row stored by the thread that loaded it
+    if (tid < c) {
+      const uint32_t bar = smem_u32(&bars[tid]);
+      if (!mbar_wait(bar, 0)) {
+        record_error(D.status, A2AV_ERR_TIMEOUT);
+        mbar_wait(bar, 0);
+      } else if (own_dst[tid] != 0) {
+        bulk_store(reinterpret_cast<void*>(own_dst[tid]), smem_u32(slot_mem) + (uint32_t)(tid * rb),
+                   (unsigned)rb);
+      }
+    }
+    bulk_wait_all();
+    return;
+  }
+  copy_listed_rows(own_src, own_dst, c, rb, slots, smem_u32(slot_mem), smem_u32(bars), D.status);
 }
 
 // The fused combine in one kernel (decode sizes): every CTA checks the split
@@ -1470,31 +1449,34 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   extern __shared__ __align__(128) unsigned char slot_mem[];
   if (!build_plan(P, pl, kTileGranule)) return;  // (waits for the previous kernel first)
   const int tid = threadIdx.x, W = D.W, K = D.K, NB = W * K;
+  // every item's key and position, all loaded at once (thread t: items t,
+  // t + 256, ... of the global order)
+  constexpr int kPer = kTinyItems / kTinyThreads;
+  const long long n = D.item_first[W];
+  int kk[kPer], rr[kPer];
+  long long pp[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const long long g = (long long)q * kTinyThreads + tid;
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    rr[q] = g < n ? r : -1;
+    const long long i = g - D.item_first[r];
+    kk[q] = g < n ? __ldg(D.key[r] + i) : 0;
+    pp[q] = g < n ? __ldg(D.sorted_pos[r] + i) : 0;
+  }
   int bad = 0;
-  for (int r = 0; r < W; ++r) {
-    const long long m = D.items[r];
-    for (long long i0 = 0; i0 < m; i0 += 4 * kTinyThreads) {
-      int k[4];
-      long long pos[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long i = i0 + q * kTinyThreads + tid;
-        k[q] = i < m ? D.key[r][i] : 0;
-        pos[q] = i < m ? D.sorted_pos[r][i] : 0;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long i = i0 + q * kTinyThreads + tid;
-        if (i >= m) continue;
-        if (k[q] < 0 || k[q] >= NB) {
-          bad = 1;
-          continue;
-        }
-        const int p = k[q] / K;
-        const long long lo = pl.in_off[r][p];
-        if (pos[q] < lo || pos[q] >= lo + pl.s[r][p]) bad = 1;
-      }
+  for (int q = 0; q < kPer; ++q) {
+    const int r = rr[q];
+    if (r < 0) continue;
+    if (kk[q] < 0 || kk[q] >= NB) {
+      bad = 1;
+      continue;
     }
+    const int p = kk[q] / K;
+    const long long lo = pl.in_off[r][p];
+    if (pp[q] < lo || pp[q] >= lo + pl.s[r][p]) bad = 1;
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
@@ -1566,23 +1548,26 @@ cudaError_t prepare_kernels(a2av_handle* h) {
   // (count histograms: 8 ranges a warp x 4 x W * K ints, up to 128 KiB)
   if (cudaFuncSetAttribute(dispatch_count_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kCountWarps * 4 * kMaxBins * (int)sizeof(int)) != cudaSuccess ||
-      cudaFuncSetAttribute(dispatch_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kStreamSmem) != cudaSuccess ||
       cudaFuncSetAttribute(dispatch_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kTinySlotBytes) != cudaSuccess ||
+                           kTinyDynBytes) != cudaSuccess ||
       cudaFuncSetAttribute(combine_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kTinySlotBytes) != cudaSuccess)
+                           kTinyDynBytes) != cudaSuccess)
     return cudaErrorInvalidValue;
   h->gather_ready = true;
   return cudaSuccess;
 }
 
 // Row slots of the one-kernel paths: 0 (register copies) unless every row
-// and buffer is 16-byte aligned and a row fits the slot memory.
-int tiny_slots(const DispatchParams& D, long long rb) {
-  if (!D.vec16 || rb < kWarpRowBytes || rb > kTinySlotBytes) return 0;
-  const long long n = kTinySlotBytes / rb;
+// and buffer is 16-byte aligned and a row fits beside `reserved` bytes.
+int tiny_slots(const DispatchParams& D, long long rb, long long reserved) {
+  if (!D.vec16 || rb < kWarpRowBytes || rb > kTinyDynBytes - reserved) return 0;
+  const long long n = (kTinyDynBytes - reserved) / rb;
   return (int)(n < kTinyOwn ? n : kTinyOwn);
+}
+
+// The dispatch's counters: [W][W*K] key counts and a W*K running count.
+long long tiny_count_bytes(const DispatchParams& D) {
+  return ((long long)D.W * D.W * D.K + (long long)D.W * D.K) * (long long)sizeof(int);
 }
 
 // One-kernel path: at most kTinyItems items, their counts fit shared memory,
@@ -1610,33 +1595,8 @@ void record_chain(a2av_handle* h, int kernels, int memsets, const char* copy) {
 // else the warp copy (rows of 64 bytes or more) or the thread copy.
 cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long long row_bytes,
                         cudaStream_t s, const char** name) {
-  if (D.vec16 && row_bytes >= kStreamMinRow && row_bytes <= kStreamMaxRow) {
-    const cudaError_t e = prepare_kernels(h);
-    if (e != cudaSuccess) return e;
-    // batches of at most 16 KiB (32, 16 or 8 items; 8 items of rows over 2
-    // KiB; fewer when that leaves some warps without four), warps so that
-    // ~96 KiB are in flight per SM
-    int bs = 32;
-    while (bs > 8 && bs * row_bytes > 16384) bs >>= 1;
-    const long long batch_bytes = bs * row_bytes;
-    int nw = (int)(kStreamFlight / batch_bytes);
-    nw = nw < 1 ? 1 : (nw > 16 ? 16 : nw);
-    const size_t smem = (size_t)nw * 2 * batch_bytes;  // <= 2 x kStreamFlight = kStreamSmem
-    const long long warps = (long long)h->sms * nw;  // one CTA per SM
-    for (;;) {
-      long long nb = 0;
-      for (int r = 0; r < D.W; ++r) nb += (D.items[r] + bs - 1) / bs;
-      if (bs == 8 || nb >= 4 * warps) break;
-      bs >>= 1;
-    }
-    D.bs = bs;
-    D.batch_first[0] = 0;
-    for (int r = 0; r < D.W; ++r)
-      D.batch_first[r + 1] = D.batch_first[r] + (D.items[r] + bs - 1) / bs;
-    *name = "dispatch_stream_kernel";
-    return launch_kernel(dispatch_stream_kernel, dim3(h->sms), 32 * nw, smem, s, true, P, D);
-  }
-  const bool gather = D.vec16 && row_bytes >= kGatherMinRow && row_bytes <= kGatherMaxRow;
+  const bool gather = D.vec16 && row_bytes >= (D.combine ? kGatherMinRow : kDispatchGatherMinRow) &&
+                      row_bytes <= kGatherMaxRow;
   if (!gather) {
     *name = "dispatch_copy_kernel";
     if (row_bytes < kWarpRowBytes)
@@ -1738,6 +1698,7 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     vec16 = vec16 && ((uintptr_t)rows_ptrs[r] & 15) == 0 && ((uintptr_t)out_ptrs[r] & 15) == 0;
   D.vec16 = vec16 && a2av_device_buffers(h, rows_ptrs, W, out_ptrs, W) ? 1 : 0;
 
+
   Params P;
   std::memset(&P, 0, sizeof(P));
   for (int r = 0; r < W; ++r) {
@@ -1759,9 +1720,9 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   cudaError_t e;
   if (tiny_fits(h, D)) {  // decode sizes: one kernel, no workspace
     if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
-    const int slots = tiny_slots(D, row_bytes);
-    const size_t smem = (size_t)slots * row_bytes > (size_t)kTinyCountBytes
-                            ? (size_t)slots * row_bytes : (size_t)kTinyCountBytes;
+    const long long counters = tiny_count_bytes(D);
+    const int slots = tiny_slots(D, row_bytes, counters + 16);
+    const size_t smem = (size_t)((((long long)slots * row_bytes + 15) & ~15LL) + counters);
     e = launch_kernel(dispatch_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads, smem, s, h->pdl,
                       P, D, slots);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
@@ -1770,8 +1731,11 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
   }
   const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
   // Four ranges a count warp when even then every SM gets a count CTA.
+// Four ranges a count warp (fewer, longer count CTAs) measured slower on the
+// embedding-key dispatch (640 K items a rank: 56.5 against 35.8 us); kept
+// for sweeps.
 #ifndef A2AV_COUNT_RW4
-#define A2AV_COUNT_RW4 1
+#define A2AV_COUNT_RW4 0
 #endif
   const int rw = A2AV_COUNT_RW4 && !small_path &&
                          (long long)W * ((ranges_max + 31) / 32) >= h->sms ? 4 : 1;
@@ -1869,6 +1833,7 @@ extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
     vec16 = vec16 && ((uintptr_t)peer_ptrs[r] & 15) == 0 && ((uintptr_t)item_out_ptrs[r] & 15) == 0;
   D.vec16 = vec16 && a2av_device_buffers(h, peer_ptrs, W, item_out_ptrs, W) ? 1 : 0;
 
+
   // Rank-side buffers (the items' rows, written) in P.in, peer-side buffers
   // (the dispatch layout, read) in P.out: the prologue's checks and offsets
   // are those of the dispatch; its offsets table goes to the workspace.
@@ -1893,7 +1858,7 @@ extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
   cudaError_t e;
   if (tiny_fits(h, D)) {  // decode sizes: one kernel, no flag
     if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
-    const int slots = tiny_slots(D, row_bytes);
+    const int slots = tiny_slots(D, row_bytes, 0);
     e = launch_kernel(combine_tiny_kernel, dim3(tiny_grid(h, D)), kTinyThreads,
                       (size_t)slots * row_bytes, s, h->pdl, P, D, slots);
     if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
