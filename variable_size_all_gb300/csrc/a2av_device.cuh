@@ -100,6 +100,61 @@ __device__ __forceinline__ void record_error(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
+// Ranks for which one warp builds the whole plan (below).
+constexpr int kWarpPlanRanks = 8;
+
+// Steps 2 and 3 of the plan for W <= kWarpPlanRanks, by warp 0 alone once it
+// sees a range-checked pl.s: lane j scans column j (out_off[j][*]) and row j
+// (in_off[j][*]) in shared memory and checks peer j's and rank j's
+// capacities; then the tiles and CTA 0's out_splits_offsets.  Returns true
+// (warp-uniform) when a capacity or NULL-buffer rule is broken.  No block
+// barrier: the caller publishes the plan with one.
+__device__ __forceinline__ bool plan_one_warp(const Params& P, Plan& pl, long long max_tile, int cta,
+                                              int ctas, int lane) {
+  const int W = P.W;
+  int bad = 0;
+  long long col = 0, row = 0;
+  if (lane < W) {
+    for (int r = 0; r < W; ++r) {
+      pl.out_off[lane][r] = col;
+      col += pl.s[r][lane];
+    }
+    pl.out_off[lane][W] = col;
+    for (int p = 0; p < W; ++p) {
+      pl.in_off[lane][p] = row;
+      row += pl.s[lane][p];
+    }
+    if ((P.out_cap > 0 && col > P.out_cap) || (P.out[lane] == nullptr && col > 0)) bad = 1;
+    if ((P.in_cap > 0 && row > P.in_cap) || (P.in[lane] == nullptr && row > 0)) bad = 1;
+  }
+  if (__any_sync(kFull, bad)) return true;
+  // tiles, as in plan_from_splits
+  const long long bytes = lane < W ? col * P.rb : 0;
+  const long long total = __shfl_sync(kFull, warp_inclusive_scan(bytes, lane), 31);
+  const long long slots = kTilesPerCta * (long long)ctas;
+  const long long per_cta = (total + slots - 1) / slots;
+  int shift = per_cta > 1 ? 64 - __clzll(per_cta - 1) : 0;
+  const int lo_shift = 63 - __clzll(kTileGranule), hi_shift = 63 - __clzll(max_tile);
+  shift = shift < lo_shift ? lo_shift : (shift > hi_shift ? hi_shift : shift);
+  const long long n = (bytes + (1LL << shift) - 1) >> shift;
+  const long long inc = warp_inclusive_scan(n, lane);
+  if (lane < W) pl.tile_first[lane] = inc - n;
+  if (lane == 31) {
+    pl.tile_first[W] = inc;
+    pl.tile_shift = shift;
+  }
+  __syncwarp();
+  if (cta == 0) {
+    for (int e = lane; e < W * W; e += 32) {
+      const int p = e / W, r = e - p * W;
+      long long* so = P.out_so + (long long)p * 2 * W;
+      so[r] = pl.s[r][p];
+      so[W + r] = pl.out_off[p][r];
+    }
+  }
+  return false;
+}
+
 // Steps 2 and 3 of the plan, once pl.s holds a range-checked split matrix:
 // column scans (out_off) and row scans (in_off) side by side + capacity
 // checks; tiles and out_splits_offsets.  Two barriers.  Returns false (in
@@ -109,6 +164,18 @@ __device__ bool plan_from_splits(const Params& P, Plan& pl, long long max_tile, 
   const int tid = threadIdx.x, nt = blockDim.x;
   const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
   const int W = P.W;
+  if (W <= kWarpPlanRanks) {  // one warp, one barrier
+    __shared__ int plan_bad;
+    if (warp == 0) {
+      const bool b = plan_one_warp(P, pl, max_tile, cta, ctas, lane);
+      if (lane == 0) {
+        plan_bad = b;
+        if (b && cta == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+      }
+    }
+    __syncthreads();
+    return !plan_bad;
+  }
   int bad = 0;
 
   // Task k < W: column scan of peer k (lane r holds S[r][k]); task W + k: row
@@ -168,7 +235,9 @@ __device__ bool plan_from_splits(const Params& P, Plan& pl, long long max_tile, 
 
 // Step 1 of the exchange, then the rest of the plan: load the split matrix
 // into shared memory and check its range (one barrier), then
-// plan_from_splits.  `ctas` CTAs work on this exchange and this one is
+// plan_from_splits; for at most kWarpPlanRanks ranks warp 0 does all of it
+// and one barrier publishes the plan (measured on a cold 0.5 MiB exchange:
+// the three-barrier plan took ~1.3 us of CTA 0's time).  `ctas` CTAs work on this exchange and this one is
 // number `cta` among them (the whole grid, unless several exchanges share a
 // launch).  Returns false (in every thread of the CTA) when the splits are
 // invalid; CTA 0 then records A2AV_ERR_BAD_SPLITS.
@@ -183,6 +252,38 @@ __device__ bool build_plan(const Params& P, Plan& pl, long long max_tile, int ct
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
+  if (W <= kWarpPlanRanks) {
+    // Few ranks: warp 0 loads the split matrix (at most two entries a lane),
+    // checks it and builds the whole plan; one block barrier publishes it.
+    __shared__ int plan_bad;
+    if ((tid >> 5) == 0) {
+      const int lane = tid & 31;
+      int bad = 0;
+      long long v[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int e = lane + 32 * q;
+        v[q] = e < W * W ? __ldcg(P.splits + (long long)(e / W) * P.split_stride + e % W) : 0;
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int e = lane + 32 * q;
+        if (e < W * W) {
+          if (v[q] < 0 || v[q] > P.limit) bad = 1;
+          pl.s[e / W][e % W] = v[q];
+        }
+      }
+      bool b = __any_sync(kFull, bad) != 0;
+      __syncwarp();
+      if (!b) b = plan_one_warp(P, pl, max_tile, cta, ctas, lane);
+      if (lane == 0) {
+        plan_bad = b;
+        if (b && cta == 0) record_error(P.status, A2AV_ERR_BAD_SPLITS);
+      }
+    }
+    __syncthreads();
+    return !plan_bad;
+  }
   int bad = 0;
   for (int e = tid; e < W * W; e += nt) {
     const int r = e / W, p = e - r * W;

@@ -248,7 +248,7 @@ __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) 
 // each key's leader advances that count.  RW = 1 (the default) at five CTAs
 // an SM (48 registers) keeps a batch of 760 groups of 2048 items (1.5 M items) resident
 // in one wave; RW = 4 (fewer, longer CTAs, for sweeps) was measured slower.
-template <int RW>
+template <int RW, bool kRank = true>
 __global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 5 : 2)
     dispatch_count_kernel(const __grid_constant__ DispatchParams D) {
   chain_release();
@@ -298,23 +298,31 @@ __global__ void __launch_bounds__(32 * kCountWarps, RW == 1 ? 5 : 2)
       keys[u][q] = ok ? k : -1 - lane;  // absent or invalid items match nobody
     }
   __syncthreads();
-  const unsigned lt = (1u << lane) - 1u;
-  const int bits = key_bits(NB);
+  if constexpr (kRank) {
+    const unsigned lt = (1u << lane) - 1u;
+    const int bits = key_bits(NB);
 #pragma unroll
-  for (int u = 0; u < RW; ++u) {
-    int* hist = count_hist + (warp * RW + u) * NB;
+    for (int u = 0; u < RW; ++u) {
+      int* hist = count_hist + (warp * RW + u) * NB;
 #pragma unroll
-    for (int q = 0; q < kRange / 32; ++q) {
-      const int k = keys[u][q];
-      const unsigned same = same_key_lanes(k, k >= 0, bits);
-      const int inr = k >= 0 ? hist[k] + __popc(same & lt) : 0;
-      __syncwarp();
-      if (k >= 0 && lane == 31 - __clz(same)) hist[k] += __popc(same);
-      __syncwarp();
-      if (k >= 0)
-        D.inrank[(long long)r * D.pos_stride + (j0 + u) * kRange + q * 32 + lane] =
-            (unsigned char)inr;
+      for (int q = 0; q < kRange / 32; ++q) {
+        const int k = keys[u][q];
+        const unsigned same = same_key_lanes(k, k >= 0, bits);
+        const int inr = k >= 0 ? hist[k] + __popc(same & lt) : 0;
+        __syncwarp();
+        if (k >= 0 && lane == 31 - __clz(same)) hist[k] += __popc(same);
+        __syncwarp();
+        if (k >= 0)
+          D.inrank[(long long)r * D.pos_stride + (j0 + u) * kRange + q * 32 + lane] =
+              (unsigned char)inr;
+      }
     }
+  } else {  // counts only: the place-and-copy kernel ranks the items itself
+#pragma unroll
+    for (int u = 0; u < RW; ++u)
+#pragma unroll
+      for (int q = 0; q < kRange / 32; ++q)
+        if (keys[u][q] >= 0) atomicAdd(&count_hist[(warp * RW + u) * NB + keys[u][q]], 1);
   }
   if (__any_sync(kFull, bad) && lane == 0) fail(D, A2AV_ERR_BAD_INDEX);
   __syncthreads();
@@ -546,10 +554,11 @@ __device__ __forceinline__ void copy_row_thread(unsigned char* d, const unsigned
 }
 
 // Place and copy (rows shorter than 64 bytes): warp w takes one range of 256
-// items; its keys, source rows and inrank bytes and the range's key bases
-// (key_base for every key, into shared memory) are loaded at once; then
-// each lane puts its items' rows straight at their place in the output of
-// their destination and publishes their positions.  Every CTA first repeats
+// items; its keys and source rows and the range's key bases (key_base for
+// every key, into shared memory) are loaded at once; the warp ranks the
+// items 32 at a time (ballots on the key; the count kernel only counted
+// them on this path), then each lane puts its items' rows straight at their
+// place in the output of their destination and publishes their positions.  Every CTA first repeats
 // the a2av prologue's checks on the whole split matrix (so all reach the
 // same verdict) and derives its rank's row displacement per peer.  Two warps
 // per CTA, registers capped so that a whole GPU of them is resident at once.
@@ -576,19 +585,17 @@ __global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
   __shared__ long long disp[kMaxW];    // out_off[p][r] - in_off[r][p], rows
   __shared__ long long glo[kMaxW], gcnt[kMaxW];  // in_off[r][p], S[r][p]: p's group
   __shared__ int bad_splits;
-  int keys[kRange / 32], srcs[kRange / 32], inr[kRange / 32];
-  int* base = place_base + warp * NB;
+  int keys[kRange / 32], srcs[kRange / 32];
+  int* base = place_base + warp * NB;  // the next position of each key in this range
   if (live) {
     const int* const kp = D.key[r];
     const int* const sp = D.src[r];
-    const unsigned char* const ip = D.inrank + (long long)r * D.pos_stride;
 #pragma unroll
     for (int c = 0; c < kRange / 32; ++c) {  // (unconditional loads, as in the count kernel)
       const long long i = i0 + c * 32 + lane;
       const long long ii = i < m ? i : m - 1;
       keys[c] = __ldg(kp + ii);
       srcs[c] = __ldg(sp + ii);
-      inr[c] = ip[ii];
     }
     for (int k = lane; k < NB; k += 32) base[k] = (int)key_base(D, r, i0, k);
   }
@@ -638,13 +645,29 @@ __global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
   }
   __syncthreads();
   if (bad_splits || !live) return;
+  // the range's items ranked 32 at a time (ballots on the key), in order
+  int pos32[kRange / 32];
+  {
+    const unsigned lt = (1u << lane) - 1u;
+    const int bits = key_bits(NB);
+#pragma unroll
+    for (int c = 0; c < kRange / 32; ++c) {
+      const bool v = i0 + c * 32 + lane < m;
+      const int k = keys[c];
+      const unsigned same = same_key_lanes(k, v, bits);
+      pos32[c] = v ? base[k] + __popc(same & lt) : 0;
+      __syncwarp();
+      if (v && lane == 31 - __clz(same)) base[k] += __popc(same);
+      __syncwarp();
+    }
+  }
   const long long rb = P.rb;
 #pragma unroll
   for (int c = 0; c < kRange / 32; ++c) {
     const long long i = i0 + c * 32 + lane;
     if (i >= m) continue;
     const int p = keys[c] / K;
-    const long long pos = (long long)base[keys[c]] + inr[c];
+    const long long pos = pos32[c];
     D.sorted_pos[r][i] = pos;
     if (pos < glo[p] || pos >= glo[p] + gcnt[p]) {  // never: see in_group
       record_error(D.status, A2AV_ERR_BAD_INDEX);
@@ -1759,8 +1782,12 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     const long long groups = D.groups_max > 0 ? D.groups_max : 1;
     const size_t hist_smem = (size_t)kCountWarps * rw * W * K * sizeof(int);
     if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    const bool place = row_bytes < kWarpRowBytes;  // the place-and-copy kernel ranks
     if (rw == 4)
       e = launch_kernel(dispatch_count_kernel<4>, dim3((unsigned)groups, (unsigned)W),
+                        32 * kCountWarps, hist_smem, s, h->pdl, D);
+    else if (place)
+      e = launch_kernel(dispatch_count_kernel<1, false>, dim3((unsigned)groups, (unsigned)W),
                         32 * kCountWarps, hist_smem, s, h->pdl, D);
     else
       e = launch_kernel(dispatch_count_kernel<1>, dim3((unsigned)groups, (unsigned)W),
