@@ -561,6 +561,7 @@ def run_ours(args, light=False):
             Tk = moved_bytes(Sk, ROW_BYTES)
             point = {"per_rank_MiB": Pk / 2**20, "moved_bytes": Tk,
                      "us_median": round(t_med * 1e6, 2),
+                     "us_mean": round(statistics.mean(times) * 1e6, 2),
                      "us_min": round(min(times) * 1e6, 2),
                      "moved_GBps": round(Tk / t_med / 1e9, 1),
                      "busbw_GBps": round(busbw_gbps(nk, t_med), 1),

@@ -81,9 +81,12 @@ typedef struct a2av_handle a2av_handle;
  *  out                 receives the handle (host pointer, must not be NULL).
  *
  * Allocates a small device status word (cudaMalloc) on the current device.
- * Reads four environment variables once: A2AV_PATH (an a2av_path_t number,
+ * Reads five environment variables once: A2AV_PATH (an a2av_path_t number,
  * the initial engine), A2AV_CTAS_PER_SM (the initial grid override), A2AV_PDL
- * (0 turns programmatic dependent launch off; see a2av_run) and
+ * (0 turns programmatic dependent launch off; see a2av_run),
+ * A2AV_DISPATCH_ORDER (which batches a2av_dispatch orders in its one-launch
+ * order kernel: 0 none, 1 -- the default -- rows under 64 bytes, 2 every
+ * row size, 3 also the batches its one-CTA-per-rank count takes) and
  * A2AV_DEBUG_STARVE -- a test hook: when nonzero, the first CTA of every
  * bulk or staged launch arms its first stage for 16 more bytes than its
  * copies deliver, so that stage never completes, the bounded wait gives up

@@ -222,3 +222,61 @@ def test_one_kernel_path(rb, aligned):
         mis = None if aligned else [int(rng.integers(1, 16)) for _ in range(2 * W)]
         assert _combine_checked(K, peers, S, key, pos, rb, mis,
                                 expect_copy="combine_tiny_kernel") == a2av.OK
+
+
+# The one-launch combine of rows under 64 bytes (check, grid barrier, copy):
+# rows of 4, 8 and 16 bytes loaded all at once when aligned, other sizes and
+# misaligned buffers one row at a time; ragged ranks and an empty one, 32
+# ranks, and the embedding size.
+@pytest.mark.parametrize("aligned", [True, False])
+@pytest.mark.parametrize("rb", [1, 4, 8, 13, 16, 24, 48])
+@pytest.mark.parametrize("W,K,counts", [
+    (4, 3, [5000, 17, 1, 0]),
+    (32, 2, [300 + 11 * r for r in range(32)]),
+    (2, 13, [640_000, 638_590]),
+])
+def test_order_kernel_path(W, K, counts, rb, aligned):
+    rng = np.random.default_rng(rb * 3 + W + aligned)
+    key = [np.minimum(rng.geometric(0.08, c) - 1, W * K - 1).astype(np.int32) for c in counts]
+    rows = [rng.integers(0, 256, 40 * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, 40, c).astype(np.int32) for c in counts]
+    outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+    peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
+    mis = None if aligned else [int(rng.integers(1, 16)) for _ in range(2 * W)]
+    assert _combine_checked(K, peers, S, key, pos, rb, mis,
+                            expect_copy="combine_order_kernel") == a2av.OK
+
+
+@pytest.mark.parametrize("order", ["0", "2"])
+@pytest.mark.parametrize("rb", [8, 13, 64, 1024, 14336])
+@pytest.mark.parametrize("case", ["key", "pos_outside_group", "pos_too_large", "negative_split"])
+def test_large_errors_write_nothing(case, rb, order, monkeypatch):
+    """The combine's checks past the one-kernel size (3000 items a rank): with
+    order "2", rows under 64 bytes by the one-launch combine, aligned rows of
+    64 B .. 2 KiB by the gather that checks before it copies (a grid barrier
+    between) and longer ones by the check kernel; with order "0", all by the
+    check kernel.  Nothing is written."""
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", order)
+    rng = np.random.default_rng(rb + len(case))
+    W, K, m = 2, 3, 3000
+    key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
+    rows = [rng.integers(0, 256, 40 * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, 40, m).astype(np.int32) for _ in range(W)]
+    outs, so, pos, S = oracle.default().dispatch_exchange(K, rows, src, key, rb)
+    peers = [rng.integers(0, 256, b.size, dtype=np.uint8) for b in outs]
+    pos = [p.copy() for p in pos]
+    S = S.copy()
+    want = a2av.ERR_BAD_INDEX
+    if case == "key":
+        key[1][2999] = W * K
+    elif case == "pos_outside_group":
+        i = 1234
+        p = key[0][i] // K
+        lo = int(S[0, :p].sum())
+        pos[0][i] = lo + int(S[0, p]) if p + 1 < W else lo - 1
+    elif case == "pos_too_large":
+        pos[1][17] = m
+    elif case == "negative_split":
+        S[1, 0] = -1
+        want = a2av.ERR_BAD_SPLITS
+    assert _combine_checked(K, peers, S, key, pos, rb) == want

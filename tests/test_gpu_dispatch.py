@@ -78,19 +78,22 @@ def test_aligned_row_sizes(rb):
     dispatch_checked(K, rows, src, key, rb)
 
 
+@pytest.mark.parametrize("order", ["0", "2"])
 @pytest.mark.parametrize("rb", [2048, 9216, 20480])
-def test_few_items_past_the_one_kernel_size(rb):
+def test_few_items_past_the_one_kernel_size(rb, order, monkeypatch):
     """More keys than the one-kernel-per-rank count takes (W*K > 256) and
-    more items than the one-kernel path takes, but only a few thousand: the
-    count kernel, the scan kernel (400 keys: more than one block thread a
-    key), then the gather in batches of 8 items."""
+    more items than the one-kernel path takes, but only a few thousand:
+    without the order kernel, the count kernel, the scan kernel (400 keys:
+    more than one block thread a key), then the gather in batches of 8
+    items; with it, the order kernel, then the gather."""
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", order)
     rng = np.random.default_rng(rb + 5)
     W, K, n, m = 2, 200, 64, 3000
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
     src = [rng.integers(0, n, m).astype(np.int32) for _ in range(W)]
     key = [rng.integers(0, W * K, m).astype(np.int32) for _ in range(W)]
     dispatch_checked(K, rows, src, key, rb, expect_copy=aligned_copy_kernel(rb),
-                     expect_kernels=3)
+                     expect_kernels=3 if order == "0" else 2)
 
 
 def test_dispatch_without_items():
@@ -116,10 +119,11 @@ def test_dispatch_without_items_many_keys(W, K):
     (8, 32, 65536, 2),    # the same limit with eight ranks
     (8, 32, 65537, 3),
 ])
-def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb):
+def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb, monkeypatch):
     """The count kernel's last block per rank scans the group counts when a
     thread's share of one key is at most 32 groups (256 keys: one thread a
-    key); one group more and the scan kernel runs."""
+    key); one group more and the scan kernel runs (the order kernel off)."""
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", "0")
     rng = np.random.default_rng(m + rb)
     n = 500
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
@@ -134,11 +138,12 @@ def test_group_scan_either_side_of_the_fused_limit(W, K, m, kernels, rb):
 @pytest.mark.parametrize("rb", [8, 64])
 @pytest.mark.parametrize("W,K,m,kernels", [(2, 13, 589_824, 2), (2, 13, 640_000, 3),
                                            (2, 200, 640_000, 3)])
-def test_embedding_size_batches(W, K, m, kernels, rb):
-    """Batches of the embedding-key size (640 K items a rank): the count
-    kernel's last block scans up to 288 groups of 2048 items over 26 keys (9
-    block threads a key, 32 groups each); past that, or with 400 keys (more
-    than one block thread a key), the scan kernel runs."""
+def test_embedding_size_batches(W, K, m, kernels, rb, monkeypatch):
+    """Batches of the embedding-key size (640 K items a rank), the order
+    kernel off: the count kernel's last block scans up to 288 groups of 2048
+    items over 26 keys (9 block threads a key, 32 groups each); past that, or
+    with 400 keys (more than one block thread a key), the scan kernel runs."""
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", "0")
     rng = np.random.default_rng(K + rb + m)
     n = 4000
     rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
@@ -147,6 +152,58 @@ def test_embedding_size_batches(W, K, m, kernels, rb):
     dispatch_checked(K, rows, src, key, rb, expect_kernels=kernels,
                      expect_copy="dispatch_place_copy_kernel" if rb < 64 else
                      aligned_copy_kernel(rb))
+
+
+# The one-launch order kernel (all items in the grid's registers): rows under
+# 64 bytes copied by it (4, 8 and 16-byte rows loaded all at once when
+# aligned, other sizes and misaligned buffers one row at a time), longer rows
+# by the copy kernel that follows; ragged ranks, an empty rank, 32 ranks, the
+# largest key count, and the embedding and MoE sizes.
+ORDER_CASES = [
+    ("ragged", 4, 3, [5000, 17, 1, 0]),
+    ("moe", 8, 32, [16384] * 8),
+    ("ranks32", 32, 2, [2100 + 7 * r for r in range(32)]),
+    ("keys1024", 2, 512, [8000, 7000]),
+    ("embedding", 2, 13, [640_000, 638_590]),
+]
+
+
+@pytest.mark.parametrize("mis", [False, True])
+@pytest.mark.parametrize("rb", [1, 4, 8, 13, 16, 24, 64, 1024, 2048, 14336])
+@pytest.mark.parametrize("case", [c[0] for c in ORDER_CASES])
+def test_order_kernel_path(case, rb, mis, monkeypatch):
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", "2")  # (every row size)
+    _, W, K, counts = next(c for c in ORDER_CASES if c[0] == case)
+    total = sum(counts)
+    if total * rb > (256 << 20):
+        pytest.skip("more than 256 MiB of rows")
+    rng = np.random.default_rng(rb * 7 + W + mis)
+    n = [int(rng.integers(1, 3000)) for _ in range(W)]
+    rows = [rng.integers(0, 256, n[r] * rb, dtype=np.uint8) for r in range(W)]
+    src = [rng.integers(0, n[r], counts[r]).astype(np.int32) for r in range(W)]
+    key = [np.minimum(rng.geometric(0.08, counts[r]) - 1, W * K - 1).astype(np.int32)
+           for r in range(W)]
+    mis_r = [int(rng.integers(1, 16)) for _ in range(W)] if mis else None
+    if rb < 64:
+        copy, kernels = "dispatch_order_kernel", 1
+    else:
+        copy, kernels = aligned_copy_kernel(rb) if not mis else "dispatch_copy_kernel", 2
+    dispatch_checked(K, rows, src, key, rb, rows_mis=mis_r, out_mis=mis_r[::-1] if mis else None,
+                     expect_copy=copy, expect_kernels=kernels)
+
+
+@pytest.mark.parametrize("W,K,counts", [
+    (2, 13, [1_300_000, 1_300_000]),   # more items than the grid's registers hold
+    (2, 512, [40_000, 40_000]),        # 1024 keys over ~80 CTAs a rank: too many counts
+])
+def test_order_kernel_falls_back(W, K, counts):
+    """Batches the order kernel does not take go through the count chain."""
+    rng = np.random.default_rng(W * K)
+    rb, n = 8, 1000
+    rows = [rng.integers(0, 256, n * rb, dtype=np.uint8) for _ in range(W)]
+    src = [rng.integers(0, n, c).astype(np.int32) for c in counts]
+    key = [rng.integers(0, W * K, c).astype(np.int32) for c in counts]
+    dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_place_copy_kernel")
 
 
 # Aligned rows by the copy kernels' shapes (the register warp copy below
@@ -264,12 +321,15 @@ def test_dispatch_errors_write_nothing(case):
     assert all(bool((p == -1).all()) for p in pos)
 
 
-@pytest.mark.parametrize("rb", [4, 64, 1024])
+@pytest.mark.parametrize("order", ["0", "2"])
+@pytest.mark.parametrize("rb", [4, 64, 1024, 2048])
 @pytest.mark.parametrize("case", ["key", "src", "capacity", "null_out"])
-def test_large_dispatch_errors_write_nothing(case, rb):
-    """The same checks past the one-kernel size (3000 items per rank): short
-    rows take the rank-and-copy kernel, 64-byte rows the warp copy kernel,
-    1 KiB rows the cp.async.bulk gather."""
+def test_large_dispatch_errors_write_nothing(case, rb, order, monkeypatch):
+    """The same checks past the one-kernel size (3000 items per rank), by the
+    order kernel (order "2": it copies rows under 64 bytes itself) and by the
+    count chain (order "0": short rows by the place-and-copy kernel); longer
+    rows by the warp copy kernel or the cp.async.bulk gather."""
+    monkeypatch.setenv("A2AV_DISPATCH_ORDER", order)
     W, K, m, n = 2, 3, 3000, 500
     rng = np.random.default_rng(rb)
     rows = [torch.from_numpy(rng.integers(0, 256, n * rb, dtype=np.uint8)).cuda()

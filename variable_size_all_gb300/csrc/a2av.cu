@@ -716,6 +716,9 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   h->starve = env_int("A2AV_DEBUG_STARVE", 0) != 0;
   h->pdl = env_int("A2AV_PDL", 1) != 0;
   h->gather_ready = false;
+  h->order_grid = 0;
+  h->order_level = env_int("A2AV_DISPATCH_ORDER", A2AV_DISPATCH_ORDER);
+  if (h->order_level < 0 || h->order_level > 3) h->order_level = A2AV_DISPATCH_ORDER;
   h->last_path = h->last_grid = h->last_block = 0;
   h->last_kernels = h->last_memsets = 0;
   h->last_copy = "";

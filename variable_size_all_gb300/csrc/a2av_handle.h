@@ -13,6 +13,11 @@ struct a2av_ptr_cache {
   unsigned stamp;  // last use
 };
 
+// Default of A2AV_DISPATCH_ORDER (see a2av_create in a2av.h).
+#ifndef A2AV_DISPATCH_ORDER
+#define A2AV_DISPATCH_ORDER 1
+#endif
+
 struct a2av_handle {
   int W;
   long long in_cap, out_cap;  // rows, 0 = unchecked
@@ -25,6 +30,8 @@ struct a2av_handle {
   int starve;                 // test hook (A2AV_DEBUG_STARVE): see a2av_create in a2av.h
   bool pdl;                   // programmatic dependent launch (A2AV_PDL, default on)
   bool gather_ready;          // the dispatch gather kernels' shared-memory opt-in is done
+  int order_grid;             // CTAs of the dispatch's one-launch order kernel (all resident)
+  int order_level;            // A2AV_DISPATCH_ORDER: batches the order kernel takes
   int last_kernels;           // kernels the last dispatch / combine_items enqueued
   int last_memsets;           // and workspace memsets
   const char* last_copy;      // the kernel of that call that moved the rows (static string)

@@ -51,6 +51,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 namespace {
 
@@ -101,6 +102,12 @@ struct DispatchParams {
 
   long long pos_stride;
   int W, K;
+  // the one-launch order kernel (below)
+  int* cta_cnt;                      // workspace: [grid][NB] key counts of each CTA's chunk
+  unsigned* barrier;                 // workspace (cleared): CTAs past the grid barrier
+  long long chunk;                   // items per CTA
+  int cta_first[kMaxW + 1];          // CTAs of rank r: [cta_first[r], cta_first[r + 1])
+  int pos_ready;                     // sorted_pos already holds every item's position
 };
 
 // Programmatic dependent launch: a kernel of the chain launched with the
@@ -677,6 +684,407 @@ __global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
   }
 }
 
+// ------------------------------------------------------------ one launch --
+// The whole ordering in one cooperative launch (every CTA resident at once)
+// when every item fits the grid's registers: CTA b takes a chunk of
+// consecutive items of one rank, warp w of it a run of at most kOrderRunMax
+// consecutive items of the chunk.
+//   1. Each warp loads its run's keys and source rows (validated) and ranks
+//      them 32 at a time (ballots on the key), keeping every item's key and
+//      its rank among the run's equal keys in registers and the run's key
+//      counts in shared memory.  The CTA's key counts go to cta_cnt[b][*];
+//      its counts per destination are added to S[r][*] (cleared with the
+//      flag).
+//   2. One grid barrier (bounded: A2AV_ERR_TIMEOUT after ~1 s).
+//   3. Every CTA builds the plan from the completed S (the a2av prologue's
+//      checks), sums the counts of its rank's CTAs -- all of them (the key
+//      totals, whose exclusive scan gives the key starts) and the earlier
+//      ones (its chunk's base per key) -- and turns its runs' counts into
+//      per-run bases; an item's position is its run's base for its key plus
+//      its rank.  Positions go to sorted_pos; rows under 64 bytes are copied
+//      here (kCopy), longer ones by the copy kernel that follows.
+constexpr int kOrderWarps = 16, kOrderThreads = 32 * kOrderWarps;
+constexpr int kOrderIpt = 10;                          // items a lane holds
+constexpr long long kOrderRunMax = 32LL * kOrderIpt;   // items of a warp's run
+constexpr long long kOrderCtaItems = kOrderWarps * kOrderRunMax;
+constexpr int kOrderPrefixLoads = 16;  // most 16-byte count loads a thread makes in step 3
+#ifndef A2AV_ORDER_PREFIX_BATCH
+#define A2AV_ORDER_PREFIX_BATCH 4
+#endif
+constexpr int kOrderPrefixBatch = A2AV_ORDER_PREFIX_BATCH;  // of them in flight at once
+constexpr int kOrderBarrierOffset = 192;  // workspace byte of the grid barrier's counter
+constexpr int kOrderKeyBits = 10;          // a key and its rank in the run share an int
+static_assert(kMaxBins <= (1 << kOrderKeyBits) && kOrderRunMax < (1 << (31 - kOrderKeyBits)),
+              "key and rank fit one int");
+static_assert(kMaxBins <= 2 * kOrderThreads, "the key scan holds two keys a thread");
+
+// Exclusive scan over the CTA of one value per thread (NT threads); *total
+// gets the sum.  `warp_sums` holds NT / 32 entries.
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan_int(int x, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  int base = 0, all = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    if (w < warp) base += warp_sums[w];
+    all += warp_sums[w];
+  }
+  *total = all;
+  __syncthreads();
+  return base + inc - x;
+}
+
+#ifndef A2AV_BARRIER_SLEEP_NS
+#define A2AV_BARRIER_SLEEP_NS 32
+#endif
+// A grid barrier in two halves, so that a CTA can work between its arrival
+// and its wait.  The counter starts at zero (the workspace memset) and serves
+// one barrier.  Arrival: after a block barrier, thread 0 publishes the CTA's
+// writes (fence) and counts itself in.
+__device__ __forceinline__ void grid_arrive(unsigned* ctr) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+  }
+}
+
+// Wait (thread 0, bounded) until all `ctas` CTAs have arrived; false (in every
+// thread) when the wait ran out.  The fence after the relaxed polls orders
+// the CTA's later reads after the other CTAs' published writes.
+__device__ __forceinline__ bool grid_wait(unsigned* ctr, unsigned ctas) {
+  __shared__ int passed;
+  if (threadIdx.x == 0) {
+    const long long start = clock64();
+    int ok = 0;
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= ctas) {
+        ok = 1;
+        break;
+      }
+      if (clock64() - start > kWaitCycles) break;
+      if (A2AV_BARRIER_SLEEP_NS > 0) __nanosleep(A2AV_BARRIER_SLEEP_NS);
+    }
+    __threadfence();
+    passed = ok;
+  }
+  __syncthreads();
+  return passed != 0;
+}
+
+__device__ __forceinline__ bool grid_barrier(unsigned* ctr, unsigned ctas) {
+  grid_arrive(ctr);
+  return grid_wait(ctr, ctas);
+}
+
+// Step 3's last part for a lane's items: position (its run's base for its
+// key plus its rank), published; with T a row type (rows of exactly sizeof(T)
+// bytes at that alignment) every row is loaded first, then stored, so that a
+// lane's loads are in flight together; T = void: rows of any other size one
+// at a time (kCopy), or positions only.
+template <typename T, bool kCopy>
+__device__ __forceinline__ void order_place(const Params& P, const DispatchParams& D,
+                                            const Plan& pl, int r, long long w0, int lane, int nc,
+                                            const int* wb, const int* keys, const int* srcs) {
+  constexpr int kMask = (1 << kOrderKeyBits) - 1;
+  long long* const out_pos = D.sorted_pos[r];
+  if constexpr (std::is_void<T>::value) {
+    const long long rb = P.rb;
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c) {
+      if (c >= nc || keys[c] < 0) continue;
+      const int k = keys[c] & kMask, p = k / D.K;
+      const long long pos = wb[k] + (keys[c] >> kOrderKeyBits);
+      out_pos[w0 + c * 32 + lane] = pos;
+      if (kCopy && in_group(pl, r, p, pos, D.status))
+        copy_row_thread(P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pos) * rb,
+                        P.in[r] + (long long)srcs[c] * rb, rb);
+    }
+  } else {
+    T v[kOrderIpt];
+    const T* const in = reinterpret_cast<const T*>(P.in[r]);
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c)
+      if (c < nc && keys[c] >= 0) v[c] = __ldg(in + srcs[c]);
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c) {
+      if (c >= nc || keys[c] < 0) continue;
+      const int k = keys[c] & kMask, p = k / D.K;
+      const long long pos = wb[k] + (keys[c] >> kOrderKeyBits);
+      out_pos[w0 + c * 32 + lane] = pos;
+      if (in_group(pl, r, p, pos, D.status))
+        reinterpret_cast<T*>(P.out[p])[pl.out_off[p][r] - pl.in_off[r][p] + pos] = v[c];
+    }
+  }
+}
+
+// kRow: 0 -- positions only (rows of 64 bytes or more, copied next); 4, 8,
+// 16 -- rows of that many bytes at that alignment, copied here; -1 -- other
+// rows under 64 bytes, copied here one at a time.
+template <int kRow>
+__global__ void __launch_bounds__(kOrderThreads, 2)
+    dispatch_order_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  chain_release();
+  chain_wait();
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int W = D.W, K = D.K, NB = W * K;
+  const int b = blockIdx.x;
+  int r = 0;
+  while (r + 1 < W && D.cta_first[r + 1] <= b) ++r;
+  extern __shared__ int order_cnt[];  // [kOrderWarps][NB]: runs' key counts, then bases
+  __shared__ int cta_k[kMaxBins];     // the CTA's key counts
+  __shared__ int tot_k[kMaxBins], pre_k[kMaxBins];
+  __shared__ int dest_cnt[kMaxW];
+  __shared__ int warp_sums[kOrderWarps];
+  __shared__ Plan pl;
+  const int NBP = (NB + 3) & ~3;  // count row stride (int4 loads)
+  const long long m = D.items[r];
+  const long long lo = (long long)(b - D.cta_first[r]) * D.chunk;
+  const long long hi = lo + D.chunk < m ? lo + D.chunk : m;
+  const long long run = (D.chunk + 32 * kOrderWarps - 1) / (32 * kOrderWarps) * 32;
+  const long long w0 = lo + warp * run, w1 = w0 + run < hi ? w0 + run : hi;
+  const int nc = w1 > w0 ? (int)((w1 - w0 + 31) / 32) : 0;  // warp-uniform
+  for (int e = t; e < kOrderWarps * NB; e += kOrderThreads) order_cnt[e] = 0;
+  for (int e = t; e < NBP; e += kOrderThreads) cta_k[e] = tot_k[e] = pre_k[e] = 0;
+  if (t < W) dest_cnt[t] = 0;
+
+  // 1. load and validate; count the CTA's keys (shared atomics) and publish
+  const int* const kp = D.key[r];
+  const int* const sp = D.src[r];
+  const long long rows_r = D.rows[r];
+  // keys[c]: the item's key, then key | rank << kOrderKeyBits (-1: no item)
+  int keys[kOrderIpt], srcs[kOrderIpt];
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c) {  // (unconditional loads, clamped index)
+    keys[c] = -1;
+    srcs[c] = 0;
+    if (c < nc) {
+      const long long i = w0 + c * 32 + lane;
+      const long long ii = i < w1 ? i : w1 - 1;
+      keys[c] = __ldg(kp + ii);
+      srcs[c] = __ldg(sp + ii);
+    }
+  }
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c) {
+    const long long i = w0 + c * 32 + lane;
+    const bool in = c < nc && i < w1;
+    const bool ok = in && keys[c] >= 0 && keys[c] < NB && srcs[c] >= 0 && srcs[c] < rows_r;
+    if (in && !ok) bad = 1;
+    keys[c] = ok ? keys[c] : -1;
+  }
+  __syncthreads();  // (counters zeroed)
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c)
+    if (keys[c] >= 0) atomicAdd(&cta_k[keys[c]], 1);
+  if (__syncthreads_or(bad)) {
+    if (t == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  } else {
+    for (int k = t; k < NBP; k += kOrderThreads) {
+      const int sum = cta_k[k];  // (0 in the padding)
+      D.cta_cnt[(long long)b * NBP + k] = sum;
+      if (sum != 0) atomicAdd(&dest_cnt[k / K], sum);
+    }
+    __syncthreads();
+    if (t < W && dest_cnt[t] != 0)
+      atomicAdd(reinterpret_cast<unsigned long long*>(D.S + (long long)r * W + t),
+                (unsigned long long)dest_cnt[t]);
+  }
+  grid_arrive(D.barrier);
+
+  // 2. while the other CTAs arrive: rank each run's items 32 at a time
+  // (ballots on the key) and turn the runs' counts into their offsets in
+  // the chunk, key by key (ranking after the wait, beside the loads of
+  // step 3, measured slower: 25.6 against 23.6 us on the embedding keys)
+  {
+    int* cnt = order_cnt + warp * NB;
+    const unsigned lt = (1u << lane) - 1u;
+    const int bits = key_bits(NB);
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c) {
+      if (c < nc) {
+        const int k = keys[c];
+        const unsigned same = same_key_lanes(k, k >= 0, bits);
+        if (k >= 0) keys[c] = k | (cnt[k] + __popc(same & lt)) << kOrderKeyBits;
+        __syncwarp();
+        if (k >= 0 && lane == 31 - __clz(same)) cnt[k] += __popc(same);
+        __syncwarp();
+      }
+    }
+  }
+  __syncthreads();
+  for (int k = t; k < NB; k += kOrderThreads) {
+    int base = 0;
+#pragma unroll 4
+    for (int w = 0; w < kOrderWarps; ++w) {
+      const int c = order_cnt[w * NB + k];
+      order_cnt[w * NB + k] = base;
+      base += c;
+    }
+  }
+  if (!grid_wait(D.barrier, gridDim.x)) {  // (its block barrier also publishes order_cnt)
+    if (t == 0) fail(D, A2AV_ERR_TIMEOUT);
+    return;
+  }
+  if (flagged(D)) return;
+
+  // 3. the counts of the rank's CTAs (int4 loads: thread t takes keys
+  // 4q .. 4q + 3, q = t % Q, of every S-th CTA from t / Q), issued before
+  // the plan is built; sums over all of them (key totals) and over the
+  // earlier ones (the chunk's base per key)
+  const int c0 = D.cta_first[r], gr = D.cta_first[r + 1] - c0;
+  const int Q = NBP / 4, S = kOrderThreads / Q, q = t % Q, s0 = t / Q;
+  int tot4[4] = {0, 0, 0, 0}, pre4[4] = {0, 0, 0, 0};
+  {
+    const int4* const cnt4 = reinterpret_cast<const int4*>(D.cta_cnt);
+    int4 v[kOrderPrefixBatch];
+    auto load = [&](int j0) {
+#pragma unroll
+      for (int u = 0; u < kOrderPrefixBatch; ++u) {
+        const int j = j0 + u * S;
+        v[u] = make_int4(0, 0, 0, 0);
+        if (s0 < S && j < gr) v[u] = __ldcg(cnt4 + (long long)(c0 + j) * Q + q);
+      }
+    };
+    load(s0);
+    if (!build_plan(P, pl, kTileGranule)) return;  // (while the first loads are in flight)
+    for (int j0 = s0; j0 < gr; j0 += kOrderPrefixBatch * S) {
+      if (j0 != s0) load(j0);
+#pragma unroll
+      for (int u = 0; u < kOrderPrefixBatch; ++u) {
+        const int e[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        const bool earlier = c0 + j0 + u * S < b;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          tot4[i] += e[i];
+          if (earlier) pre4[i] += e[i];
+        }
+      }
+    }
+  }
+  if (b == 0 && D.in_splits_out != nullptr)
+    for (int e = t; e < W * W; e += kOrderThreads) D.in_splits_out[e] = pl.s[e / W][e % W];
+  if (s0 < S)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (tot4[i] != 0) atomicAdd(&tot_k[4 * q + i], tot4[i]);
+      if (pre4[i] != 0) atomicAdd(&pre_k[4 * q + i], pre4[i]);
+    }
+  __syncthreads();
+  {  // key starts (two keys a thread) plus the chunk's base
+    const int k0 = 2 * t;
+    const int x0 = k0 < NB ? tot_k[k0] : 0, x1 = k0 + 1 < NB ? tot_k[k0 + 1] : 0;
+    int all;
+    const int start = block_exclusive_scan_int<kOrderThreads>(x0 + x1, warp_sums, &all);
+    if (k0 < NB) pre_k[k0] += start;
+    if (k0 + 1 < NB) pre_k[k0 + 1] += start + x0;
+  }
+  __syncthreads();
+  for (int e = t; e < kOrderWarps * NB; e += kOrderThreads) order_cnt[e] += pre_k[e % NB];
+  __syncthreads();
+  const int* const wb = order_cnt + warp * NB;
+  if constexpr (kRow == 4)
+    order_place<unsigned, true>(P, D, pl, r, w0, lane, nc, wb, keys, srcs);
+  else if constexpr (kRow == 8)
+    order_place<unsigned long long, true>(P, D, pl, r, w0, lane, nc, wb, keys, srcs);
+  else if constexpr (kRow == 16)
+    order_place<uint4, true>(P, D, pl, r, w0, lane, nc, wb, keys, srcs);
+  else
+    order_place<void, kRow != 0>(P, D, pl, r, w0, lane, nc, wb, keys, srcs);
+}
+
+// The fused combine of rows under 64 bytes in one cooperative launch, items
+// partitioned as in the order kernel: every CTA builds the plan from the
+// split matrix (the a2av prologue's checks), loads its items' keys and
+// positions and checks them (a position must lie in its destination's group
+// of the rank's key order), then a grid barrier; if no CTA found an invalid
+// item, each moves its items' rows back -- rows of exactly kRow = 4, 8 or 16
+// bytes at that alignment all loaded first, then stored; kRow = -1 one row
+// at a time.
+template <int kRow>
+__global__ void __launch_bounds__(kOrderThreads, 2)
+    combine_order_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, kTileGranule)) return;  // (same verdict in every CTA)
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int W = D.W, K = D.K, NB = W * K;
+  const int b = blockIdx.x;
+  int r = 0;
+  while (r + 1 < W && D.cta_first[r + 1] <= b) ++r;
+  const long long m = D.items[r];
+  const long long lo = (long long)(b - D.cta_first[r]) * D.chunk;
+  const long long hi = lo + D.chunk < m ? lo + D.chunk : m;
+  const long long run = (D.chunk + 32 * kOrderWarps - 1) / (32 * kOrderWarps) * 32;
+  const long long w0 = lo + warp * run, w1 = w0 + run < hi ? w0 + run : hi;
+  const int nc = w1 > w0 ? (int)((w1 - w0 + 31) / 32) : 0;  // warp-uniform
+  const int* const kp = D.key[r];
+  const long long* const pp = D.sorted_pos[r];
+  int keys[kOrderIpt], pos[kOrderIpt];  // -1: no item; positions are below 2^31
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c) {  // (unconditional loads, clamped index)
+    keys[c] = -1;
+    pos[c] = 0;
+    if (c < nc) {
+      const long long i = w0 + c * 32 + lane;
+      const long long ii = i < w1 ? i : w1 - 1;
+      const int k = __ldg(kp + ii);
+      const long long q = __ldg(pp + ii);
+      bool ok = false;
+      if (i < w1 && k >= 0 && k < NB) {
+        const int p = k / K;
+        const long long g0 = pl.in_off[r][p];
+        ok = q >= g0 && q < g0 + pl.s[r][p];
+      }
+      keys[c] = ok ? k : (i < w1 ? -2 : -1);
+      pos[c] = ok ? (int)q : 0;
+    }
+  }
+  int bad = 0;
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c) bad |= keys[c] == -2;
+  if (__syncthreads_or(bad) && t == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  if (!grid_barrier(D.barrier, gridDim.x)) {
+    if (t == 0) fail(D, A2AV_ERR_TIMEOUT);
+    return;
+  }
+  if (flagged(D)) return;
+  const long long rb = P.rb;
+  unsigned char* const own = const_cast<unsigned char*>(P.in[r]);
+  if constexpr (kRow > 0) {
+    using T = typename std::conditional<
+        kRow == 4, unsigned, typename std::conditional<kRow == 8, unsigned long long, uint4>::type>::type;
+    T v[kOrderIpt];
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c)
+      if (keys[c] >= 0) {
+        const int p = keys[c] / K;
+        v[c] = __ldg(reinterpret_cast<const T*>(P.out[p]) + (pl.out_off[p][r] - pl.in_off[r][p] + pos[c]));
+      }
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c)
+      if (keys[c] >= 0) reinterpret_cast<T*>(own)[w0 + c * 32 + lane] = v[c];
+  } else {
+#pragma unroll
+    for (int c = 0; c < kOrderIpt; ++c)
+      if (keys[c] >= 0) {
+        const int p = keys[c] / K;
+        copy_row_thread(own + (w0 + c * 32 + lane) * rb,
+                        P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pos[c]) * rb, rb);
+      }
+  }
+}
+
 // Once build_plan has accepted the split matrix: CTA 0 writes it out.
 __device__ __forceinline__ void publish_splits(const DispatchParams& D) {
   if (blockIdx.x == 0 && D.in_splits_out != nullptr)
@@ -748,8 +1156,13 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
           mdst = (long long)(P.in[r] + i * rb);
         } else {
           const int s = D.src[r][i];
-          const long long pos = key_base(D, r, i, k) + D.inrank[(long long)r * D.pos_stride + i];
-          D.sorted_pos[r][i] = pos;
+          long long pos;
+          if (D.pos_ready) {
+            pos = D.sorted_pos[r][i];
+          } else {
+            pos = key_base(D, r, i, k) + D.inrank[(long long)r * D.pos_stride + i];
+            D.sorted_pos[r][i] = pos;
+          }
           mdst = (long long)(P.out[p] + (grouped + pos) * rb);
           msrc = (long long)(P.in[r] + (long long)s * rb);
           if (!in_group(pl, r, p, pos, D.status)) mdst = msrc = 0;
@@ -823,7 +1236,7 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
           pos[q] = D.sorted_pos[r][i];
         } else {
           src_row[q] = D.src[r][i];
-          pos[q] = D.inrank[(long long)r * D.pos_stride + i];
+          pos[q] = D.pos_ready ? D.sorted_pos[r][i] : D.inrank[(long long)r * D.pos_stride + i];
         }
       }
     }
@@ -832,8 +1245,10 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
       const int r = rank[q];
       if (r < 0 || D.combine) continue;
       const long long i = g0 + q * teams - D.item_first[r];
-      pos[q] += key_base(D, r, i, key[q]);
-      D.sorted_pos[r][i] = pos[q];
+      if (!D.pos_ready) {
+        pos[q] += key_base(D, r, i, key[q]);
+        D.sorted_pos[r][i] = pos[q];
+      }
       if (!in_group(pl, r, key[q] / K, pos[q], D.status)) rank[q] = -1;
     }
 #pragma unroll
@@ -857,30 +1272,69 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
 // and position -- the position must lie in its destination's group of the
 // rank's key order, [in_off[r][p], in_off[r][p] + S[r][p]) -- else the flag
 // that stops the copy kernel, and A2AV_ERR_BAD_INDEX.
+// Whether the items [g0 + u * stride] (u < B, below total) all have a valid
+// key and a position in their destination's group; their keys and positions
+// are loaded together.
+template <int B>
+__device__ __forceinline__ bool combine_items_ok(const DispatchParams& D, const Plan& pl,
+                                                 long long g0, long long stride, long long total) {
+  const int W = D.W, K = D.K, NB = W * K;
+  int key[B], rank[B];
+  long long pos[B];
+#pragma unroll
+  for (int u = 0; u < B; ++u) {
+    const long long g = g0 + u * stride;
+    rank[u] = -1;
+    if (g < total) {
+      int r = 0;
+      while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+      const long long i = g - D.item_first[r];
+      rank[u] = r;
+      key[u] = D.key[r][i];
+      pos[u] = D.sorted_pos[r][i];
+    }
+  }
+  bool ok = true;
+#pragma unroll
+  for (int u = 0; u < B; ++u) {
+    const int r = rank[u];
+    if (r < 0) continue;
+    if (key[u] < 0 || key[u] >= NB) {
+      ok = false;
+      continue;
+    }
+    const int p = key[u] / K;
+    const long long lo = pl.in_off[r][p];
+    if (pos[u] < lo || pos[u] >= lo + pl.s[r][p]) ok = false;
+  }
+  return ok;
+}
+
+// Every item of the combine checked by the whole grid (thread x of the grid
+// takes items x, x + G, ... in batches of B); true (in every thread of the
+// CTA) when the CTA found no invalid item -- else it has raised the flag and
+// recorded A2AV_ERR_BAD_INDEX.
+template <int B>
+__device__ __forceinline__ bool combine_check_all(const DispatchParams& D, const Plan& pl) {
+  const long long total = D.item_first[D.W];
+  const long long G = (long long)gridDim.x * blockDim.x;
+  int bad = 0;
+  for (long long g0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; g0 < total; g0 += B * G)
+    if (!combine_items_ok<B>(D, pl, g0, G, total)) bad = 1;
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) fail(D, A2AV_ERR_BAD_INDEX);
+    return false;
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(kCopyThreads)
     combine_check_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   chain_release();
   __shared__ Plan pl;
   if (!build_plan(P, pl, kTileGranule)) return;
-  const int W = D.W, K = D.K, NB = W * K;
-  const long long total = D.item_first[W];
-  int bad = 0;
-  for (long long g = (long long)blockIdx.x * kCopyThreads + threadIdx.x; g < total;
-       g += (long long)gridDim.x * kCopyThreads) {
-    int r = 0;
-    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
-    const long long i = g - D.item_first[r];
-    const int key = D.key[r][i];
-    if (key < 0 || key >= NB) {
-      bad = 1;
-      continue;
-    }
-    const int p = key / K;
-    const long long pos = D.sorted_pos[r][i], lo = pl.in_off[r][p];
-    if (pos < lo || pos >= lo + pl.s[r][p]) bad = 1;
-  }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) fail(D, A2AV_ERR_BAD_INDEX);
+  combine_check_all<4>(D, pl);
 }
 
 // ------------------------------------------------------------- gather --
@@ -910,11 +1364,10 @@ __device__ __forceinline__ GatherItem gather_item_at(const DispatchParams& D, lo
   x.i = i;
   x.v = true;
   x.key = D.key[r][i];
-  if (D.combine) {
-    x.spos = D.sorted_pos[r][i];
-  } else {
+  if (D.combine || D.pos_ready) x.spos = D.sorted_pos[r][i];
+  if (!D.combine) {
     x.src = D.src[r][i];
-    x.inr = D.inrank[(long long)r * D.pos_stride + i];
+    if (!D.pos_ready) x.inr = D.inrank[(long long)r * D.pos_stride + i];
   }
   return x;
 }
@@ -938,11 +1391,10 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
   if (lane < D.bs && i < D.items[r]) {
     x.v = true;
     x.key = D.key[r][i];
-    if (D.combine) {
-      x.spos = D.sorted_pos[r][i];
-    } else {
+    if (D.combine || D.pos_ready) x.spos = D.sorted_pos[r][i];
+    if (!D.combine) {
       x.src = D.src[r][i];
-      x.inr = D.inrank[(long long)r * D.pos_stride + i];
+      if (!D.pos_ready) x.inr = D.inrank[(long long)r * D.pos_stride + i];
     }
   }
   return x;
@@ -963,6 +1415,9 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
 // key bases), so they are loaded two and one batches ahead.  Waits are
 // bounded: on a timeout the warp records A2AV_ERR_TIMEOUT, waits (bounded)
 // for every load it issued and leaves.
+#ifndef A2AV_GATHER_ROW_LANE0
+#define A2AV_GATHER_ROW_LANE0 0
+#endif
 template <int NS, int LEAD, int NWK, int IPS>
 __global__ void __launch_bounds__(32 * NWK, 1)
     dispatch_gather_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
@@ -978,6 +1433,18 @@ __global__ void __launch_bounds__(32 * NWK, 1)
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
   publish_splits(D);
+  if (D.combine && D.barrier != nullptr) {
+    // The combine's checks in this launch (cooperative: every CTA resident):
+    // the whole grid checks every item (few threads: 16 items a thread in
+    // flight), then a grid barrier; no row moves unless every CTA found its
+    // items valid.
+    combine_check_all<16>(D, pl);
+    if (!grid_barrier(D.barrier, gridDim.x)) {
+      if (threadIdx.x == 0) fail(D, A2AV_ERR_TIMEOUT);
+      return;
+    }
+    if (flagged(D)) return;
+  }
   const int lane = threadIdx.x & 31;
   const int warp = NWK == 1 ? 0 : (int)(threadIdx.x >> 5);  // a constant for one warp
   // One-row stages (IPS == 1) take the items in a strided order: the warp's
@@ -1047,10 +1514,11 @@ __global__ void __launch_bounds__(32 * NWK, 1)
 
   GatherItem a0 = fetch(0);
   GatherItem a1 = fetch(1);
-  long long b0 = a0.v && !D.combine ? key_base(D, a0.r, a0.i, a0.key) : 0;
+  const bool bases = !D.combine && !D.pos_ready;  // positions from key bases + inrank
+  long long b0 = a0.v && bases ? key_base(D, a0.r, a0.i, a0.key) : 0;
   for (long long t = 0; t < nt && ok; ++t) {
     const GatherItem a2 = fetch(t + 2);
-    const long long b1 = a1.v && !D.combine ? key_base(D, a1.r, a1.i, a1.key) : 0;
+    const long long b1 = a1.v && bases ? key_base(D, a1.r, a1.i, a1.key) : 0;
     // batch t's row addresses
     long long src = 0, dst = 0;
     if (a0.v) {
@@ -1060,13 +1528,46 @@ __global__ void __launch_bounds__(32 * NWK, 1)
         src = (long long)(P.out[p] + (grouped + a0.spos) * rb);
         dst = (long long)(P.in[a0.r] + a0.i * rb);
       } else {
-        const long long pos = b0 + a0.inr;
-        D.sorted_pos[a0.r][a0.i] = pos;
+        const long long pos = bases ? b0 + a0.inr : a0.spos;
+        if (bases) D.sorted_pos[a0.r][a0.i] = pos;
         src = (long long)(P.in[a0.r] + (long long)a0.src * rb);
         dst = (long long)(P.out[p] + (grouped + pos) * rb);
         if (!in_group(pl, a0.r, p, pos, D.status)) a0.v = false;
       }
     }
+#if A2AV_GATHER_ROW_LANE0
+    if constexpr (IPS == 1) {
+      // one row a stage: lane 0 issues the batch's loads one by one
+      const unsigned held = __ballot_sync(kFull, a0.v);
+      for (int u = 0; u < 32 && ok; ++u) {
+        const long long su = __shfl_sync(kFull, src, u), du = __shfl_sync(kFull, dst, u);
+        if (!((held >> u) & 1u)) continue;
+        if (lane == 0) {
+          const int s = (int)(issued % NS);
+          if (issued >= NS) bulk_wait_read<NS - LEAD - 1>();
+          const uint32_t bar = bar0 + 8 * s;
+          sdst[warp][s][0] = (unsigned long long)du;
+          smask[warp][s] = 1u;
+          const unsigned starve = (P.starve && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
+          mbar_expect_tx(bar, (unsigned)rb + starve);
+          bulk_load(st0 + (uint32_t)s * stage_bytes, reinterpret_cast<const void*>(su),
+                    (unsigned)rb, bar);
+        }
+        ++issued;
+        while (issued - drained > LEAD) {
+          if (!drain(drained)) {
+            ok = false;
+            break;
+          }
+          ++drained;
+        }
+      }
+      a0 = a1;
+      a1 = a2;
+      b0 = b1;
+      continue;
+    }
+#endif
     for (int u = 0; u < spb; ++u) {
       const int s = (int)(issued % NS);
       if (issued >= NS && (IPS > 1 || lane == 0))
@@ -1146,6 +1647,7 @@ constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 constexpr long long kDispatchGatherMinRow = A2AV_DISPATCH_GATHER_MIN_ROW;
 constexpr long long kGatherMaxRow = 32 * 1024;
+constexpr long long kGatherCheckMaxRow = 2048;  // the combine's gather checks its items up to here
 constexpr int kGatherSmem = 192 * 1024;
 
 using GatherKernel = void (*)(Params, DispatchParams);
@@ -1560,6 +2062,33 @@ extern "C" int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_pe
 
 namespace {
 
+using OrderKernel = void (*)(Params, DispatchParams);
+const OrderKernel kOrderKernels[] = {
+    dispatch_order_kernel<0>,  dispatch_order_kernel<4>, dispatch_order_kernel<8>,
+    dispatch_order_kernel<16>, dispatch_order_kernel<-1>, combine_order_kernel<4>,
+    combine_order_kernel<8>,   combine_order_kernel<16>, combine_order_kernel<-1>};
+
+// The row word of rows under 64 bytes: 4, 8 or 16 when rows are exactly that
+// long and every buffer is aligned to it, else -1 (rows one at a time).
+int row_word(const Params& P, long long rb) {
+  uintptr_t a = (uintptr_t)rb;
+  for (int r = 0; r < P.W; ++r) a |= (uintptr_t)P.in[r] | (uintptr_t)P.out[r];
+  if ((rb == 4 || rb == 8 || rb == 16) && (a & (uintptr_t)(rb - 1)) == 0) return (int)rb;
+  return -1;
+}
+
+// The order kernel for a batch: positions only for rows of 64 bytes or more;
+// else the copying one for the row size and alignment.
+OrderKernel order_kernel(const Params& P, long long rb, bool combine) {
+  if (rb >= kWarpRowBytes) return dispatch_order_kernel<0>;
+  switch (row_word(P, rb)) {
+    case 4: return combine ? combine_order_kernel<4> : dispatch_order_kernel<4>;
+    case 8: return combine ? combine_order_kernel<8> : dispatch_order_kernel<8>;
+    case 16: return combine ? combine_order_kernel<16> : dispatch_order_kernel<16>;
+    default: return combine ? combine_order_kernel<-1> : dispatch_order_kernel<-1>;
+  }
+}
+
 // Shared-memory opt-in of the gather and one-kernel paths, once per handle
 // (a host call per launch otherwise).
 cudaError_t prepare_kernels(a2av_handle* h) {
@@ -1576,8 +2105,71 @@ cudaError_t prepare_kernels(a2av_handle* h) {
       cudaFuncSetAttribute(combine_tiny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTinyDynBytes) != cudaSuccess)
     return cudaErrorInvalidValue;
+  // The order kernel's grid: as many CTAs as are resident at once with the
+  // largest run-count table (a cooperative launch needs every CTA resident).
+  constexpr int kOrderSmemMax = kOrderWarps * kMaxBins * (int)sizeof(int);
+  int per_sm = 1 << 30;
+  for (OrderKernel k : kOrderKernels) {
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kOrderSmemMax) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kOrderThreads, kOrderSmemMax) !=
+            cudaSuccess)
+      return cudaErrorInvalidValue;
+    per_sm = n < per_sm ? n : per_sm;
+  }
+  h->order_grid = h->sms * per_sm;
   h->gather_ready = true;
   return cudaSuccess;
+}
+
+// Host side of the order kernels: the chunk and each rank's CTAs, or 0 when
+// the batch does not fit one launch (more items than the grid's registers
+// hold; for the dispatch -- L given -- also too many counts for step 3, or a
+// workspace too small for the CTA counts: the count / scan chain takes it
+// then).
+int order_grid(const a2av_handle* h, DispatchParams& D, const Layout* L) {
+  const int W = D.W;
+  const long long NB = (long long)W * D.K, M = D.item_first[W], G = h->order_grid;
+  if (M == 0 || G <= W) return 0;
+  long long chunk = (M + (G - W) - 1) / (G - W);
+  chunk = chunk < 32 * kOrderWarps ? 32 * kOrderWarps : chunk;  // a 32-item run per warp at least
+  if (chunk > kOrderCtaItems) return 0;
+  long long ctas = 0, most = 0;
+  for (int r = 0; r < W; ++r) {
+    const long long g = (D.items[r] + chunk - 1) / chunk;
+    D.cta_first[r] = (int)ctas;
+    ctas += g;
+    most = g > most ? g : most;
+  }
+  D.cta_first[W] = (int)ctas;
+  // (step 3: thread t loads the counts of every S-th CTA of its rank, S =
+  // threads / (NBP / 4), NBP = NB rounded up to a multiple of 4)
+  const long long NBP = (NB + 3) & ~3LL, S = kOrderThreads / (NBP / 4);
+  if (ctas > G ||
+      (L != nullptr && ((most + S - 1) / S > kOrderPrefixLoads ||
+                        4 * ctas * NBP > L->total - L->hist)))
+    return 0;
+  D.chunk = chunk;
+  return (int)ctas;
+}
+
+// A cooperative launch (every CTA resident at once: the order kernel's grid
+// barrier relies on it).
+template <typename... Args, typename... Vals>
+cudaError_t launch_cooperative(void (*kernel)(Args...), dim3 grid, int block, size_t smem,
+                               cudaStream_t s, Vals... vals) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, vals...);
 }
 
 // Row slots of the one-kernel paths: 0 (register copies) unless every row
@@ -1616,10 +2208,15 @@ void record_chain(a2av_handle* h, int kernels, int memsets, const char* copy) {
 // The row copy of a dispatch or a combine: the cp.async.bulk gather for
 // 16-byte aligned rows of kGatherMinRow .. 32 KiB (its ring by row size),
 // else the warp copy (rows of 64 bytes or more) or the thread copy.
+// Whether the cp.async.bulk gather moves rows of this size.
+bool takes_gather(const DispatchParams& D, long long row_bytes) {
+  return D.vec16 && row_bytes >= (D.combine ? kGatherMinRow : kDispatchGatherMinRow) &&
+         row_bytes <= kGatherMaxRow;
+}
+
 cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long long row_bytes,
                         cudaStream_t s, const char** name) {
-  const bool gather = D.vec16 && row_bytes >= (D.combine ? kGatherMinRow : kDispatchGatherMinRow) &&
-                      row_bytes <= kGatherMaxRow;
+  const bool gather = takes_gather(D, row_bytes);
   if (!gather) {
     *name = "dispatch_copy_kernel";
     if (row_bytes < kWarpRowBytes)
@@ -1650,6 +2247,8 @@ cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long 
   D.batch_first[0] = 0;
   for (int r = 0; r < D.W; ++r) D.batch_first[r + 1] = D.batch_first[r] + (D.items[r] + bs - 1) / bs;
   const size_t smem = (size_t)g->nwk * g->ns * g->ips * row_bytes;
+  if (D.combine && D.barrier != nullptr)  // (the combine's checks in the gather: a grid barrier)
+    return launch_cooperative(g->kernel, dim3(h->sms), 32 * g->nwk, smem, s, P, D);
   return launch_kernel(g->kernel, dim3(h->sms), 32 * g->nwk, smem, s, true, P, D);
 }
 
@@ -1753,7 +2352,35 @@ extern "C" int a2av_dispatch(a2av_handle* h, int keys_per_peer, const void* cons
     return A2AV_OK;
   }
   const bool small_path = max_items <= kSmallItems && W * K <= kSmallKeys;
-  // Four ranges a count warp when even then every SM gets a count CTA.
+  // The one-launch order kernel (the handle's A2AV_DISPATCH_ORDER level: 1
+  // for rows under 64 bytes, 2 for every row size, 3 also for batches the
+  // small kernel takes)
+  if (h->order_level >= (row_bytes < kWarpRowBytes ? 1 : 2) &&
+      (h->order_level >= 3 || !small_path)) {
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    const int ctas = order_grid(h, D, &L);
+    if (ctas > 0) {
+      static_assert(4 + 4 * kMaxW <= kOrderBarrierOffset, "done counters below the barrier");
+      D.barrier = reinterpret_cast<unsigned*>(ws + kOrderBarrierOffset);
+      D.cta_cnt = reinterpret_cast<int*>(ws + L.hist);
+      if (cudaMemsetAsync(ws, 0, (size_t)L.key_start, s) != cudaSuccess) return A2AV_ERR_CUDA;
+      const bool fused = row_bytes < kWarpRowBytes;  // rows copied by the order kernel
+      const size_t smem = (size_t)kOrderWarps * W * K * sizeof(int);
+      e = launch_cooperative(order_kernel(P, row_bytes, false), dim3((unsigned)ctas),
+                             kOrderThreads, smem, s, P, D);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+      if (fused) {
+        record_chain(h, 1, 1, "dispatch_order_kernel");
+        return A2AV_OK;
+      }
+      D.pos_ready = 1;
+      const char* copy = nullptr;
+      e = launch_copy(h, P, D, row_bytes, s, &copy);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+      record_chain(h, 2, 1, copy);
+      return A2AV_OK;
+    }
+  }
 // Four ranges a count warp (fewer, longer count CTAs) measured slower on the
 // embedding-key dispatch (640 K items a rank: 56.5 against 35.8 us); kept
 // for sweeps.
@@ -1893,6 +2520,32 @@ extern "C" int a2av_combine_items(a2av_handle* h, int keys_per_peer,
     return A2AV_OK;
   }
   if (cudaMemsetAsync(D.flag, 0, 256, s) != cudaSuccess) return A2AV_ERR_CUDA;
+  if (row_bytes < kWarpRowBytes && h->order_level >= 1) {  // check and copy in one launch
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    const int ctas = order_grid(h, D, nullptr);
+    if (ctas > 0) {
+      D.barrier = reinterpret_cast<unsigned*>(ws + kOrderBarrierOffset);
+      e = launch_cooperative(order_kernel(P, row_bytes, true), dim3((unsigned)ctas),
+                             kOrderThreads, 0, s, P, D);
+      if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+      record_chain(h, 1, 1, "combine_order_kernel");
+      return A2AV_OK;
+    }
+  }
+  // Aligned rows of 64 B .. 2 KiB: the gather checks every item itself
+  // (grid barrier) -- 1 KiB rows: the gather with its checks 45.8 us against
+  // 40.0 + 6.0 us for the check kernel and the gather, one launch less; the
+  // one-row rings above 2 KiB have too few threads to check quickly (14 KiB
+  // rows: 625.6 against 619.5 us), so they keep the check kernel.
+  if (takes_gather(D, row_bytes) && row_bytes <= kGatherCheckMaxRow && h->order_level >= 1) {
+    if ((e = prepare_kernels(h)) != cudaSuccess) return A2AV_ERR_CUDA;
+    D.barrier = reinterpret_cast<unsigned*>(ws + kOrderBarrierOffset);
+    const char* copy = nullptr;
+    e = launch_copy(h, P, D, row_bytes, s, &copy);
+    if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return A2AV_ERR_CUDA;
+    record_chain(h, 1, 1, copy);
+    return A2AV_OK;
+  }
   e = launch_kernel(combine_check_kernel, dim3(h->sms * kCopyCtasPerSm), kCopyThreads, 0, s,
                     h->pdl, P, D);
   if (e != cudaSuccess) return A2AV_ERR_CUDA;
