@@ -87,11 +87,15 @@ typedef struct a2av_handle a2av_handle;
  * A2AV_DISPATCH_ORDER (which batches a2av_dispatch orders in its one-launch
  * order kernel: 0 none, 1 -- the default -- rows under 64 bytes, 2 every
  * row size, 3 also the batches its one-CTA-per-rank count takes) and
- * A2AV_DEBUG_STARVE -- a test hook: when nonzero, the first CTA of every
- * bulk or staged launch arms its first stage for 16 more bytes than its
- * copies deliver, so that stage never completes, the bounded wait gives up
- * after about a second and the run records A2AV_ERR_TIMEOUT.  No copy is
- * left in flight and the context stays usable.  Never set it outside tests.
+ * A2AV_DEBUG_STARVE -- a test hook: 1 makes the first CTA of every bulk or
+ * staged launch (and the first warp of the fused dispatch's and combine's
+ * bulk gather) arm its first stage for 16 more bytes than its copies
+ * deliver, so that stage never completes; 2 makes the grid barrier of the
+ * one-launch dispatch and combine kernels wait for one CTA more than the
+ * grid holds.  Either way the bounded wait gives up after about a second and
+ * the run records A2AV_ERR_TIMEOUT.  No copy is left in flight, nothing is
+ * written past the failed wait, and the context stays usable.  Never set it
+ * outside tests.
  * Errors: A2AV_ERR_INVALID_ARG (W < 1, negative capacity, out == NULL),
  * A2AV_ERR_UNSUPPORTED, A2AV_ERR_CUDA (no usable device).
  */

@@ -247,7 +247,7 @@ __device__ __forceinline__ void bulk_engine(const Params& P, int stage_bytes, in
       if (lane == 0) {
         stage_dst[s] = P.out[p] + lo;
         stage_len[s] = (unsigned)(hi - lo);
-        const unsigned starve = (P.starve && cta == 0 && k == 0) ? 16u : 0u;
+        const unsigned starve = (P.starve == 1 && cta == 0 && k == 0) ? 16u : 0u;
         mbar_expect_tx(bar, (unsigned)(hi - lo) + starve);
       }
       __syncwarp();
@@ -395,7 +395,7 @@ __device__ __forceinline__ void staged_engine(const Params& P, int stage_bytes, 
       }
       __syncwarp();
       const uint32_t bar = full0 + 8 * s;
-      const unsigned starve = (P.starve && cta == 0 && k == 0) ? 16u : 0u;
+      const unsigned starve = (P.starve == 1 && cta == 0 && k == 0) ? 16u : 0u;
       if (lane == 0) mbar_expect_tx(bar, total + starve);
       __syncwarp();
       if (n > 0) bulk_load(stage0 + (uint32_t)s * alloc + off, (const void*)g_lo, gb, bar);
@@ -713,7 +713,8 @@ int a2av_create(int world_size, int64_t in_capacity_rows, int64_t out_capacity_r
   if (h->path < A2AV_PATH_AUTO || h->path > A2AV_PATH_STAGED) h->path = A2AV_PATH_AUTO;
   h->ctas_per_sm = env_int("A2AV_CTAS_PER_SM", 0);
   if (h->ctas_per_sm < 0 || h->ctas_per_sm > 32) h->ctas_per_sm = 0;
-  h->starve = env_int("A2AV_DEBUG_STARVE", 0) != 0;
+  h->starve = env_int("A2AV_DEBUG_STARVE", 0);
+  if (h->starve < 0 || h->starve > 2) h->starve = 0;
   h->pdl = env_int("A2AV_PDL", 1) != 0;
   h->gather_ready = false;
   h->order_grid = 0;

@@ -50,7 +50,8 @@ struct Params {
   long long in_cap;         // rows, 0 = unchecked
   long long out_cap;        // rows, 0 = unchecked
   int W;
-  int starve;               // test hook: CTA 0 arms its first stage for 16 bytes too many
+  int starve;               // test hook: 1 -- CTA 0 arms its first stage for 16 bytes too
+                            // many; 2 -- grid barriers wait for one CTA more than the grid
 };
 
 // Host side of Params::limit: every byte offset then stays below 2^62.

@@ -933,7 +933,7 @@ __global__ void __launch_bounds__(kOrderThreads, 2)
       base += c;
     }
   }
-  if (!grid_wait(D.barrier, gridDim.x)) {  // (its block barrier also publishes order_cnt)
+  if (!grid_wait(D.barrier, gridDim.x + (P.starve == 2))) {  // (also publishes order_cnt)
     if (t == 0) fail(D, A2AV_ERR_TIMEOUT);
     return;
   }
@@ -1054,7 +1054,7 @@ __global__ void __launch_bounds__(kOrderThreads, 2)
 #pragma unroll
   for (int c = 0; c < kOrderIpt; ++c) bad |= keys[c] == -2;
   if (__syncthreads_or(bad) && t == 0) fail(D, A2AV_ERR_BAD_INDEX);
-  if (!grid_barrier(D.barrier, gridDim.x)) {
+  if (!grid_barrier(D.barrier, gridDim.x + (P.starve == 2))) {
     if (t == 0) fail(D, A2AV_ERR_TIMEOUT);
     return;
   }
@@ -1439,7 +1439,7 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     // flight), then a grid barrier; no row moves unless every CTA found its
     // items valid.
     combine_check_all<16>(D, pl);
-    if (!grid_barrier(D.barrier, gridDim.x)) {
+    if (!grid_barrier(D.barrier, gridDim.x + (P.starve == 2))) {
       if (threadIdx.x == 0) fail(D, A2AV_ERR_TIMEOUT);
       return;
     }
@@ -1548,7 +1548,7 @@ __global__ void __launch_bounds__(32 * NWK, 1)
           const uint32_t bar = bar0 + 8 * s;
           sdst[warp][s][0] = (unsigned long long)du;
           smask[warp][s] = 1u;
-          const unsigned starve = (P.starve && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
+          const unsigned starve = (P.starve == 1 && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
           mbar_expect_tx(bar, (unsigned)rb + starve);
           bulk_load(st0 + (uint32_t)s * stage_bytes, reinterpret_cast<const void*>(su),
                     (unsigned)rb, bar);
@@ -1581,7 +1581,7 @@ __global__ void __launch_bounds__(32 * NWK, 1)
       if (mine) sdst[warp][s][slot] = (unsigned long long)dst;
       if (lane == 0) {
         smask[warp][s] = unit == 32 ? held : (held >> (u * unit)) & ((1u << unit) - 1u);
-        const unsigned starve = (P.starve && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
+        const unsigned starve = (P.starve == 1 && blockIdx.x == 0 && warp == 0 && issued == 0) ? 16u : 0u;
         mbar_expect_tx(bar, (unsigned)(n * rb) + starve);
       }
       __syncwarp();
@@ -2205,15 +2205,16 @@ void record_chain(a2av_handle* h, int kernels, int memsets, const char* copy) {
   h->last_copy = copy;
 }
 
-// The row copy of a dispatch or a combine: the cp.async.bulk gather for
-// 16-byte aligned rows of kGatherMinRow .. 32 KiB (its ring by row size),
-// else the warp copy (rows of 64 bytes or more) or the thread copy.
 // Whether the cp.async.bulk gather moves rows of this size.
 bool takes_gather(const DispatchParams& D, long long row_bytes) {
   return D.vec16 && row_bytes >= (D.combine ? kGatherMinRow : kDispatchGatherMinRow) &&
          row_bytes <= kGatherMaxRow;
 }
 
+// The row copy of a dispatch or a combine: the cp.async.bulk gather for
+// 16-byte aligned rows of kGatherMinRow (the dispatch: kDispatchGatherMinRow)
+// .. 32 KiB (its ring by row size), else the warp copy (rows of 64 bytes or
+// more) or the thread copy.
 cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long long row_bytes,
                         cudaStream_t s, const char** name) {
   const bool gather = takes_gather(D, row_bytes);
