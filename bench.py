@@ -947,7 +947,7 @@ def run_fused_dispatch(args, light=False):
                    "l2": ("L2 flushed (512 MiB read) before every timed launch" if cold else
                           "inputs larger than L2"),
                    "timing": f"CUDA events around the dispatch ({chain['memsets']} memset and "
-                             f"{chain['kernels']} kernels, ending in {copy_kernel}), "
+                             f"{chain['kernels']} kernel{'s' if chain['kernels'] != 1 else ''}, ending in {copy_kernel}), "
                              "mean over steps; a spin kernel ahead of each call keeps the "
                              "host's call time outside the events (fused_host_call_us)"},
         "unfused_torch_sort_gather_a2av": None if light else {
@@ -1043,7 +1043,8 @@ def run_fused_combine(args, light=False):
     peak, peak_kind = hbm_peak()
     chain = eng.last_dispatch()  # the kernels the library enqueued for the combine
     copy_kernel = chain["copy_kernel"]
-    roofline = {"bound": "hbm", "kernel": f"a2av_combine_items ({chain['kernels']} kernels, "
+    roofline = {"bound": "hbm", "kernel": f"a2av_combine_items ({chain['kernels']} kernel"
+                                          f"{'s' if chain['kernels'] != 1 else ''}, "
                                           f"ending in {copy_kernel})",
                 "achieved": round(algo / f_mean / 1e9, 1), "peak": peak, "peak_source": peak_kind,
                 "unit": "GB/s", "frac": round(algo / f_mean / 1e9 / peak, 4),

@@ -70,8 +70,14 @@ def test_pins_catch_mutant(tmp_path, name):
     path = tmp_path / "a2av_oracle.c"
     path.write_text(src.replace(old, new))
     lib = oracle.build(str(path), str(tmp_path / "liba2av_oracle_mutant.so"))
-    res = subprocess.run([sys.executable, "-m", "tests._pins", lib], cwd=ROOT,
-                         capture_output=True, text=True, timeout=300)
+    # Some mutants index out of bounds: the pin process may crash or, rarely,
+    # run away instead of failing an assertion (the unmutated pins take about
+    # a second).  Either way the mutant did not pass the pins.
+    try:
+        res = subprocess.run([sys.executable, "-m", "tests._pins", lib], cwd=ROOT,
+                             capture_output=True, text=True, timeout=60)
+    except subprocess.TimeoutExpired:
+        return
     assert res.returncode != 0, f"mutant {name} passed every pin:\n{res.stdout}{res.stderr}"
 
 

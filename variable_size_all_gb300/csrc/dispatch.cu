@@ -36,11 +36,19 @@
 //      - other rows of 64 bytes or more: a warp per batch of rows (registers);
 //      - rows under 64 bytes: the count kernel's successor places and copies
 //        the rows of a whole range per warp (thread per row).
+// Rows under 64 bytes, when every item fits the grid's registers, take one
+// cooperative launch instead of 1-3 (the order kernel): each CTA counts a
+// chunk of one rank's items, the CTAs exchange their counts through the
+// workspace and one bounded grid barrier, and each CTA then ranks, places
+// and copies its chunk.
 // Decode-size batches (at most 4096 items over all ranks) take one kernel
 // instead: every CTA reads all keys, counts them, derives the split matrix
 // and the plan itself (so all CTAs reach the same verdict without any
 // inter-CTA communication), then places and copies its own share of the
 // items -- no workspace, no memset, one launch.
+// The combine moves rows back with the same copy kernels after a check
+// kernel; short rows check and copy in one cooperative launch, and the
+// gather checks its items itself (grid barrier) for rows up to 2 KiB.
 // Invalid keys or source rows set a workspace flag (cleared first) that stops
 // every later kernel; invalid splits stop the copy kernel in its prologue.
 // Either way nothing the caller owns is written.
