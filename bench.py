@@ -755,9 +755,9 @@ def exchange_config(args, Wn, rb, per_rank, T, cold, world):
             "parallelism": f"{Wn} emulated ranks per replica, {world} replica(s)"}
 
 
-# The other workloads of the survey's hot-path table, each an entry of the
-# default (cfg2) line: timed steps, roofline and a bit-exact check against the
-# oracle outside the timed region.
+# The other four exchange configurations and the MoE fused dispatch and
+# combine, each an entry of the default (cfg2) line: timed steps, roofline
+# and a bit-exact check against the oracle outside the timed region.
 CONFIG_ENTRIES = [
     ("cfg1", dict(workload="cfg1")),
     ("cfg3", dict(workload="cfg3")),

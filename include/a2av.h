@@ -243,6 +243,14 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *    ONE kernel, no workspace use, no memset -- every block counts all the
  *    keys itself, derives the split matrix and the plan, then places and
  *    copies its share of the items;
+ *  - rows shorter than 64 bytes (see A2AV_DISPATCH_ORDER at a2av_create),
+ *    when every item fits the grid's registers (about 1.5 M items over all
+ *    ranks on a GB300) and the workspace holds the per-block counts: a
+ *    memset of the workspace's first 256 + 8 * W * W bytes, then ONE
+ *    cooperative kernel (every block resident at once): each block counts
+ *    a chunk of one rank's items, the blocks exchange their counts through
+ *    the workspace and one grid barrier (bounded: about a second, then
+ *    A2AV_ERR_TIMEOUT), and each block places and copies its chunk;
  *  - otherwise a memset of the workspace's first 256 bytes, then: per-range
  *    key counts and each item's rank within its 256-item range (the scan of
  *    the counts over groups of ranges done by that kernel's last block of
@@ -250,16 +258,17 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *    one kernel per rank does both when every rank has at most 2048 items
  *    and W * keys_per_peer <= 256), then the row copy, which alone writes
  *    the caller's buffers: a cp.async.bulk gather for 16-byte aligned rows
- *    of 64 bytes to 32 KiB, register copies otherwise (for rows shorter than
- *    64 bytes past the one-kernel-per-rank size, one kernel places and
- *    copies the rows of each range after checking the split matrix).
+ *    of 1.5 KiB to 32 KiB in device memory, register copies otherwise (for
+ *    rows shorter than 64 bytes, one kernel places and copies the rows of
+ *    each range after checking the split matrix).
  * Errors: host -- A2AV_ERR_INVALID_ARG (NULL arrays, keys_per_peer < 1,
  * negative counts, a small or misaligned workspace), A2AV_ERR_UNSUPPORTED
  * (W * keys_per_peer > A2AV_MAX_DISPATCH_KEYS, counts above 2^31 - 1);
- * device -- A2AV_ERR_BAD_INDEX for a key or source row out of range and
+ * device -- A2AV_ERR_BAD_INDEX for a key or source row out of range,
  * A2AV_ERR_BAD_SPLITS for a capacity or NULL-buffer violation (the handle's
- * output capacity applies; inputs are checked by source-row index).  On a
- * device-detected error nothing is written: no output row, no
+ * output capacity applies; inputs are checked by source-row index) and
+ * A2AV_ERR_TIMEOUT when a bounded wait runs out.  On a device-detected
+ * BAD_INDEX or BAD_SPLITS nothing is written: no output row, no
  * out_splits_offsets, sorted_pos or in_splits entry.
  */
 int a2av_dispatch(a2av_handle *h, int keys_per_peer, const void *const *rows_ptrs,
@@ -399,16 +408,22 @@ int a2av_version(void);
  *  workspace          DEVICE scratch, 256-byte aligned, at least
  *                     A2AV_COMBINE_WORKSPACE_BYTES, not shared with a call in flight.
  *
- * Launches: at most 4096 items over all ranks -- ONE kernel, no workspace
- * memset (every block checks the split matrix and every key and position,
- * then copies its share); otherwise a 256-byte workspace memset, a check
- * kernel (the split matrix, each key, each position within its
- * destination's group), then the dispatch's copy kernel with the rows
- * moving the other way (a2av_last_dispatch reports which).  Device
- * errors write nothing: A2AV_ERR_BAD_SPLITS (as a2av_run; NULL buffers with
- * rows), A2AV_ERR_BAD_INDEX (a key outside [0, W * K) or a position outside
- * [in_off[r][p], in_off[r][p] + S[r][p])).  Host errors as a2av_dispatch
- * (A2AV_ERR_INVALID_ARG also for a small or misaligned workspace).
+ * Launches (a2av_last_dispatch reports which): at most 4096 items over all
+ * ranks -- ONE kernel, no workspace memset (every block checks the split
+ * matrix and every key and position, then copies its share); otherwise a
+ * 256-byte workspace memset, then (A2AV_DISPATCH_ORDER at a2av_create
+ * above 0) for rows shorter than 64 bytes ONE cooperative kernel that
+ * checks every item, passes a grid barrier and copies, and for 16-byte
+ * aligned device rows of 64 bytes to 2 KiB the cp.async.bulk gather,
+ * launched cooperatively, which checks every item itself before a grid
+ * barrier; else a check kernel (the split matrix, each key, each position
+ * within its destination's group) and then the dispatch's copy kernel with
+ * the rows moving the other way.  The grid barriers are bounded (about a
+ * second, then A2AV_ERR_TIMEOUT).  Device errors A2AV_ERR_BAD_SPLITS (as
+ * a2av_run; NULL buffers with rows) and A2AV_ERR_BAD_INDEX (a key outside
+ * [0, W * K) or a position outside [in_off[r][p], in_off[r][p] + S[r][p]))
+ * write nothing.  Host errors as a2av_dispatch (A2AV_ERR_INVALID_ARG also
+ * for a small or misaligned workspace).
  */
 int a2av_combine_items(a2av_handle *h, int keys_per_peer, const void *const *peer_ptrs,
                        const int64_t *in_splits_dev, const int32_t *const *key_ptrs,

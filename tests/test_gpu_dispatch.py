@@ -30,6 +30,34 @@ def test_moe_top2_dispatch(tokens):
         assert ref[p].size == int(w.splits[:, p].sum()) * w.row_bytes
 
 
+@pytest.mark.parametrize("hidden", [256, 512, 768, 1024])
+@pytest.mark.parametrize("tokens", [2048, 8192])
+def test_moe_top2_short_rows(tokens, hidden):
+    """512 B .. 2 KiB MoE rows (the register copy of 512-byte pieces, the
+    gather's multi-row stages): a token's two items are consecutive, so the
+    token's row is loaded once and stored to both destinations."""
+    w = wl.cfg3(1, tokens=tokens, hidden=hidden)
+    K, rows, src, key = wl.dispatch_items(w)
+    dispatch_checked(K, rows, src, key, w.row_bytes, expect_copy=aligned_copy_kernel(w.row_bytes))
+
+
+@pytest.mark.parametrize("rb", [512, 1024, 1536, 2048])
+def test_runs_of_one_source_row(rb):
+    """Items that share a source row in runs of 1 to 8 (top-k routing of up
+    to eight experts, ragged at batch edges), keys in any order: every
+    destination of a run gets the row."""
+    rng = np.random.default_rng(rb)
+    W, K, n = 4, 5, 300
+    rows, src, key = [], [], []
+    for r in range(W):
+        rows.append(rng.integers(0, 256, n * rb, dtype=np.uint8))
+        runs = rng.integers(1, 9, 1500)
+        s = np.repeat(rng.integers(0, n, runs.size), runs)[: 6000 - 37 * r]
+        src.append(s.astype(np.int32))
+        key.append(rng.integers(0, W * K, s.size).astype(np.int32))
+    dispatch_checked(K, rows, src, key, rb, expect_copy=aligned_copy_kernel(rb))
+
+
 def test_moe_dedup_dispatch():
     w = wl.cfg3(3, tokens=2048, hidden=512, dedup=True)
     K, rows, src, key = wl.dispatch_items(w)

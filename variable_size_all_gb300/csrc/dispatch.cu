@@ -1179,27 +1179,44 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
       if (!D.combine && __any_sync(kFull, lane < n && mdst == 0)) continue;  // (never: in_group)
       if constexpr (kRows512) {
         // rows of a multiple of 512 bytes: lane l takes pieces l, l + 32, ...
-        // of every row; (row, piece) advance by a counter, no division
-        const unsigned vpl = (unsigned)(rb >> 9), np = (unsigned)n * vpl;  // a lane's pieces
-        unsigned j = 0, c = 0;
+        // of every row; (row, piece) advance by a counter, no division.
+        // Consecutive items with the same source row (a token routed to
+        // several experts) form a run: the row is loaded once and stored to
+        // every destination of the run.  `heads` marks the first item of
+        // each run; the loop walks the runs in order with the current run
+        // [h, hn) warp-uniform.
+        const long long prev = __shfl_up_sync(kFull, msrc, 1);
+        unsigned hm = __ballot_sync(kFull, lane < n && (lane == 0 || prev != msrc));
+        const int nu = __popc(hm);
+        auto next_head = [&](unsigned m) { return m != 0u ? __ffs(m) - 1 : n; };
+        int h = next_head(hm), hn = next_head(hm & (hm - 1u));
+        const unsigned vpl = (unsigned)(rb >> 9), np = (unsigned)nu * vpl;  // a lane's pieces
+        unsigned c = 0;
         for (unsigned b0 = 0; b0 < np; b0 += kVecRows) {  // warp-uniform trip count
           uint4 v[kVecRows];
-          long long d[kVecRows];
+          int first[kVecRows], end[kVecRows];
+          long long off[kVecRows];
 #pragma unroll
           for (int q = 0; q < kVecRows; ++q) {
             const bool ok = b0 + q < np;
-            const long long s = __shfl_sync(kFull, msrc, (int)(j & 31u));
-            const long long off = 16LL * (lane + 32 * c);
-            d[q] = __shfl_sync(kFull, mdst, (int)(j & 31u)) + off;
-            if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s + off));
-            if (++c == vpl) {
+            first[q] = h;
+            end[q] = hn;
+            const long long s = __shfl_sync(kFull, msrc, h & 31);
+            off[q] = 16LL * (lane + 32 * c);
+            if (ok) v[q] = ld_stream(reinterpret_cast<const uint4*>(s + off[q]));
+            if (++c == vpl) {  // the next run
               c = 0;
-              ++j;
+              hm &= hm - 1u;
+              h = hn;
+              hn = next_head(hm & (hm - 1u));
             }
           }
 #pragma unroll
-          for (int q = 0; q < kVecRows; ++q)
-            if (b0 + q < np) st_stream(reinterpret_cast<uint4*>(d[q]), v[q]);
+          for (int q = 0; q < kVecRows; ++q) {
+            if (b0 + q >= np) continue;  // (warp-uniform)
+            for (int e = first[q]; e < end[q]; ++e)
+              st_stream(reinterpret_cast<uint4*>(__shfl_sync(kFull, mdst, e) + off[q]), v[q]);
+          }
         }
       } else if (D.vec16 && rb <= kVecMaxRow) {
         const unsigned V = (unsigned)(rb >> 4), nv = (unsigned)n * V;  // < 2^17
