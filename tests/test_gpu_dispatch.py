@@ -234,14 +234,13 @@ def test_order_kernel_falls_back(W, K, counts):
     dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_place_copy_kernel")
 
 
-# Aligned rows by the copy kernels' shapes (the register warp copy below
-# 1.5 KiB, in flat runs or by 512-byte pieces; the gather's lane-issued
-# 8-row stages for 1.5 .. 2 KiB rows and its one-row rings, items in
-# strided order, for 3 .. 32 KiB rows), with ragged last batches per rank.
+# Aligned rows by the copy kernels' shapes (the register warp copy up to 4
+# KiB, in flat runs or by 512-byte pieces; the gather's one-row rings, items
+# in strided order, above 4 KiB), with ragged last batches per rank.
 @pytest.mark.parametrize("rb,m", [(64, 20011), (256, 20011), (272, 9001), (512, 9001),
                                   (1024, 6007), (1536, 6007), (2048, 6007), (3072, 3001),
-                                  (4096, 3001), (8192, 1801), (14336, 1801), (16384, 1801),
-                                  (32768, 1801)])
+                                  (4096, 3001), (4112, 3001), (8192, 1801), (14336, 1801),
+                                  (16384, 1801), (32768, 1801)])
 def test_aligned_copy_shapes(rb, m):
     """(more than 4096 items in all: past the one-kernel path)"""
     rng = np.random.default_rng(rb + m)

@@ -107,10 +107,11 @@ def test_graph_replay_multi_with_new_splits():
 
 @pytest.mark.parametrize("rb,tokens", [(8, 3000), (14336 // 8, 256), (64, 3000)])
 def test_graph_replay_dispatch_with_new_keys(rb, tokens):
-    """The fused dispatch (a workspace memset and its chain of kernels)
-    captured once; new keys and source rows are written into the same device
-    buffers between replays.  Covers the rank-and-copy path (8-byte rows),
-    the cp.async.bulk gather (1792-byte rows) and the warp copy (64-byte)."""
+    """The fused dispatch (a workspace memset and its kernels) captured
+    once; new keys and source rows are written into the same device buffers
+    between replays.  Covers the one-launch cooperative order kernel with its
+    grid barrier (8-byte rows) and the count chain with the register copies
+    (1792-byte and 64-byte rows)."""
     W, K = 4, 3
     rng = np.random.default_rng(rb)
     n_rows = tokens

@@ -26,7 +26,7 @@
 //   3. copy   (the a2av prologue builds the plan from S, which also checks
 //      capacities and NULL buffers; then S is published and every item's row
 //      goes straight to its place in the output of its destination):
-//      - 16-byte aligned rows of 1.5 KiB .. 32 KiB (the combine: from 64 B):
+//      - 16-byte aligned rows above 4 KiB .. 32 KiB (the combine: from 64 B):
 //        the cp.async.bulk gather -- up to 2 KiB, every lane of a warp
 //        issues the copy of its own item's row into its slot of a 16-row
 //        shared-memory stage (one mbarrier per stage), then its own bulk
@@ -1660,13 +1660,16 @@ __global__ void __launch_bounds__(32 * NWK, 1)
 // A2AV_GATHER_MIN_ROW, the dispatch from A2AV_DISPATCH_GATHER_MIN_ROW).
 // Measured on the MoE workload (8192 tokens, W=8, us, gather / register warp
 // copy): combine 24.3 / 27.6 at 128 B rows, 50.1 / 51.7 at 1 KiB; dispatch
-// 34.9 / 31.8 at 128 B, 57.2 / 52.5 at 1 KiB, 82.9 / -- at 2 KiB (the
-// dispatch's batch metadata -- key bases -- costs its few issuing warps more).
+// 34.9 / 31.8 at 128 B, 57.2 / 52.5 at 1 KiB (the dispatch's batch metadata
+// -- key bases -- costs the gather's few issuing warps more), and, with the
+// register copy loading a token's row once for all its experts, 88.1 / 84.5
+// at 2 KiB, 152.5 / 150.9 at 4 KiB, 286.0 / 285.8 at 8 KiB, 476.7 / 485.6 at
+// 14 KiB: the dispatch's gather starts above 4 KiB.
 #ifndef A2AV_GATHER_MIN_ROW
 #define A2AV_GATHER_MIN_ROW 64
 #endif
 #ifndef A2AV_DISPATCH_GATHER_MIN_ROW
-#define A2AV_DISPATCH_GATHER_MIN_ROW 1536
+#define A2AV_DISPATCH_GATHER_MIN_ROW 4097
 #endif
 constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
@@ -1722,9 +1725,11 @@ constexpr int kTinyItems = 4096;
 constexpr int kTinyCounts = 2048;  // W * W * K counters in shared memory
 constexpr int kTinyOwn = 64;
 // Dynamic shared memory of the one-kernel paths: row slots, then (dispatch)
-// the counters; 200 KiB with the ~27 KB of static shared memory stays within
-// the 227 KiB a CTA may have (14 slots of 14 KiB MoE rows plus counters).
-constexpr int kTinyDynBytes = 200 * 1024;
+// the counters; 199 KiB with the ~28 KB of static shared memory (the plan,
+// the CTA's share) stays within the 227 KiB a CTA may have (14 slots of
+// 14 KiB MoE rows plus counters).  The shared-memory opt-in of both kernels
+// fails, and so every decode-size call with it, if the sum goes above.
+constexpr int kTinyDynBytes = 199 * 1024;
 
 // The CTA's c rows (addresses listed in shared memory; 0: a row the position
 // check dropped), by warp 0 with cp.async.bulk when slots > 0 (rows and
@@ -1824,6 +1829,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   chain_wait();
   __shared__ Plan pl;
   __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
+  __shared__ int own_key[kTinyOwn], own_row[kTinyOwn];  // the share's keys and source rows
   __shared__ alignas(8) unsigned long long bars[kTinyOwn];
   extern __shared__ __align__(128) unsigned char slot_mem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1895,6 +1901,11 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     }
     atomicAdd(&cnt[r * NB + kk[q]], 1);
     if (r == ra && ii[q] < ia) atomicAdd(&run[kk[q]], 1);
+    const long long g = (long long)q * kTinyThreads + tid;
+    if (g >= a && g < e) {  // this CTA's share: kept for the placement below
+      own_key[g - a] = kk[q];
+      own_row[g - a] = ss[q];
+    }
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
@@ -1947,8 +1958,8 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
         const long long gi = g0 + lane;
         const bool v = gi < seg_end;
         const long long i = gi - D.item_first[r];
-        const int key = v ? D.key[r][i] : -1 - lane;
-        const int s = v ? D.src[r][i] : 0;
+        const int key = v ? own_key[gi - a] : -1 - lane;
+        const int s = v ? own_row[gi - a] : 0;
         const unsigned same = same_key_lanes(key, v, key_bits(NB));
         long long pos = 0;
         if (v) pos = (long long)cnt[r * NB + key] + run[key] + __popc(same & lt);
@@ -1996,11 +2007,16 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   __shared__ Plan pl;
   __shared__ unsigned long long own_src[kTinyOwn], own_dst[kTinyOwn];
   __shared__ alignas(8) unsigned long long bars[kTinyOwn];
+  __shared__ int own_key[kTinyOwn];
+  __shared__ long long own_pos[kTinyOwn];
   extern __shared__ __align__(128) unsigned char slot_mem[];
-  if (!build_plan(P, pl, kTileGranule)) return;  // (waits for the previous kernel first)
+  // The previous kernel of the stream (a dispatch) writes the positions:
+  // wait for it, then load every item's key and position at once (thread
+  // t: items t, t + 256, ... of the global order) and build the plan while
+  // they are in flight.
+  chain_release();
+  chain_wait();
   const int tid = threadIdx.x, W = D.W, K = D.K, NB = W * K;
-  // every item's key and position, all loaded at once (thread t: items t,
-  // t + 256, ... of the global order)
   constexpr int kPer = kTinyItems / kTinyThreads;
   const long long n = D.item_first[W];
   int kk[kPer], rr[kPer];
@@ -2015,6 +2031,9 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     kk[q] = g < n ? __ldg(D.key[r] + i) : 0;
     pp[q] = g < n ? __ldg(D.sorted_pos[r] + i) : 0;
   }
+  if (!build_plan(P, pl, kTileGranule)) return;
+  long long a, e;
+  tiny_share(D, &a, &e);
   int bad = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
@@ -2027,22 +2046,24 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     const int p = kk[q] / K;
     const long long lo = pl.in_off[r][p];
     if (pp[q] < lo || pp[q] >= lo + pl.s[r][p]) bad = 1;
+    const long long g = (long long)q * kTinyThreads + tid;
+    if (g >= a && g < e) {  // this CTA's share: kept for its copy
+      own_key[g - a] = kk[q];
+      own_pos[g - a] = pp[q];
+    }
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
     return;
   }
-  long long a, e;
-  tiny_share(D, &a, &e);
   const long long rb = P.rb;
   for (long long g = a + tid; g < e; g += kTinyThreads) {
     int r = 0;
     while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
     const long long i = g - D.item_first[r];
-    const int p = D.key[r][i] / K;
-    const long long pos = D.sorted_pos[r][i];
-    own_src[g - a] =
-        (unsigned long long)(P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pos) * rb);
+    const int p = own_key[g - a] / K;
+    own_src[g - a] = (unsigned long long)(P.out[p] +
+                                          (pl.out_off[p][r] - pl.in_off[r][p] + own_pos[g - a]) * rb);
     own_dst[g - a] = (unsigned long long)(P.in[r] + i * rb);
   }
   __syncthreads();
