@@ -49,11 +49,12 @@ def test_starved_stage_times_out_and_context_survives(monkeypatch, path):
     exchange_checked(w.inputs, w.splits, w.row_bytes, path=path, expect_path=path)
 
 
-@pytest.mark.parametrize("rb,combine", [(8192, False), (14336, False), (512, True), (2048, True)])
+@pytest.mark.parametrize("rb,combine", [(8192, False), (14336, False), (512, True), (2048, True),
+                                        (14336, True)])
 def test_starved_gather_stage_times_out_and_context_survives(monkeypatch, rb, combine):
     """The same hook on the dispatch's cp.async.bulk gather (one-row rings)
-    and on the combine's (lane-issued 16- or 8-row stages, after its own
-    checks and grid barrier): the first stage of the first warp never
+    and on the combine's (lane-issued 16- or 8-row stages after its own
+    checks and grid barrier; one-row rings): the first stage of the first warp never
     completes, the warp reports A2AV_ERR_TIMEOUT and waits (bounded) for the
     copies it issued; a normal dispatch on a fresh handle afterwards is
     exact."""
