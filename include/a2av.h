@@ -258,7 +258,7 @@ int64_t a2av_dispatch_workspace_bytes(int world_size, int keys_per_peer,
  *    one kernel per rank does both when every rank has at most 2048 items
  *    and W * keys_per_peer <= 256), then the row copy, which alone writes
  *    the caller's buffers: a cp.async.bulk gather for 16-byte aligned rows
- *    above 4 KiB to 32 KiB in device memory, register copies otherwise (for
+ *    above 2 KiB to 32 KiB in device memory, register copies otherwise (for
  *    rows shorter than 64 bytes, one kernel places and copies the rows of
  *    each range after checking the split matrix).
  * Errors: host -- A2AV_ERR_INVALID_ARG (NULL arrays, keys_per_peer < 1,

@@ -169,7 +169,7 @@ def dispatch_checked(K, rows, src, key, rb, rows_mis=None, out_mis=None, engine=
 
 def aligned_copy_kernel(rb: int, combine: bool = False) -> str:
     """The kernel that moves 16-byte aligned rows of rb bytes past the
-    one-kernel size: the cp.async.bulk gather for rows above 4 KiB .. 32 KiB
+    one-kernel size: the cp.async.bulk gather for rows above 2 KiB .. 32 KiB
     (the combine: from 64 B), register copies otherwise."""
-    lo = 64 if combine else 4097
+    lo = 64 if combine else 2049
     return "dispatch_gather_kernel" if lo <= rb <= 32768 else "dispatch_copy_kernel"

@@ -234,9 +234,9 @@ def test_order_kernel_falls_back(W, K, counts):
     dispatch_checked(K, rows, src, key, rb, expect_copy="dispatch_place_copy_kernel")
 
 
-# Aligned rows by the copy kernels' shapes (the register warp copy up to 4
+# Aligned rows by the copy kernels' shapes (the register warp copy up to 2
 # KiB, in flat runs or by 512-byte pieces; the gather's one-row rings, items
-# in strided order, above 4 KiB), with ragged last batches per rank.
+# in strided order, above 2 KiB), with ragged last batches per rank.
 @pytest.mark.parametrize("rb,m", [(64, 20011), (256, 20011), (272, 9001), (512, 9001),
                                   (1024, 6007), (1536, 6007), (2048, 6007), (3072, 3001),
                                   (4096, 3001), (4112, 3001), (8192, 1801), (14336, 1801),

@@ -26,7 +26,7 @@
 //   3. copy   (the a2av prologue builds the plan from S, which also checks
 //      capacities and NULL buffers; then S is published and every item's row
 //      goes straight to its place in the output of its destination):
-//      - 16-byte aligned rows above 4 KiB .. 32 KiB (the combine: from 64 B):
+//      - 16-byte aligned rows above 2 KiB .. 32 KiB (the combine: from 64 B):
 //        the cp.async.bulk gather -- up to 2 KiB, every lane of a warp
 //        issues the copy of its own item's row into its slot of a 16-row
 //        shared-memory stage (one mbarrier per stage), then its own bulk
@@ -1746,13 +1746,14 @@ __global__ void __launch_bounds__(32 * NWK, 1)
 // 34.9 / 31.8 at 128 B, 57.2 / 52.5 at 1 KiB (the dispatch's batch metadata
 // -- key bases -- costs the gather's few issuing warps more), and, with the
 // register copy loading a token's row once for all its experts, 88.1 / 84.5
-// at 2 KiB, 152.5 / 150.9 at 4 KiB, 286.0 / 285.8 at 8 KiB, 476.7 / 485.6 at
-// 14 KiB: the dispatch's gather starts above 4 KiB.
+// at 2 KiB, 152.5 / 150.9 at 4 KiB (but 150.7 / 155.5 in bench lines taken on
+// other boxes), 286.0 / 285.8 at 8 KiB, 476.7 / 485.6 at 14 KiB: the
+// dispatch's gather starts above 2 KiB.
 #ifndef A2AV_GATHER_MIN_ROW
 #define A2AV_GATHER_MIN_ROW 64
 #endif
 #ifndef A2AV_DISPATCH_GATHER_MIN_ROW
-#define A2AV_DISPATCH_GATHER_MIN_ROW 4097
+#define A2AV_DISPATCH_GATHER_MIN_ROW 2049
 #endif
 constexpr int kGatherNs = A2AV_GATHER_NS, kGatherLead = A2AV_GATHER_LEAD;
 constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
