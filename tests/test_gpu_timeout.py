@@ -32,6 +32,11 @@ def _cuda():
 
 @pytest.mark.parametrize("path", [a2av.PATH_BULK, a2av.PATH_STAGED])
 def test_starved_stage_times_out_and_context_survives(monkeypatch, path):
+    """Both staging engines: the starved stage's wait gives up; before the
+    CTA leaves, the bulk engine waits (bounded) on every stage it issued, and
+    the staged engine's producer drains the stages it filled that no
+    consumer took, so no cp.async.bulk write into shared memory is pending
+    when the CTA exits."""
     w = wl.cfg2(8 << 20)
     ins = [torch.from_numpy(b).cuda() for b in w.inputs]
     S = torch.from_numpy(w.splits).cuda()
