@@ -697,20 +697,23 @@ __global__ void __launch_bounds__(32 * kPlaceWarps, A2AV_PLACE_MIN_CTAS)
 // when every item fits the grid's registers: CTA b takes a chunk of
 // consecutive items of one rank, warp w of it a run of at most kOrderRunMax
 // consecutive items of the chunk.
-//   1. Each warp loads its run's keys and source rows (validated) and ranks
-//      them 32 at a time (ballots on the key), keeping every item's key and
-//      its rank among the run's equal keys in registers and the run's key
-//      counts in shared memory.  The CTA's key counts go to cta_cnt[b][*];
-//      its counts per destination are added to S[r][*] (cleared with the
-//      flag).
-//   2. One grid barrier (bounded: A2AV_ERR_TIMEOUT after ~1 s).
-//   3. Every CTA builds the plan from the completed S (the a2av prologue's
-//      checks), sums the counts of its rank's CTAs -- all of them (the key
-//      totals, whose exclusive scan gives the key starts) and the earlier
-//      ones (its chunk's base per key) -- and turns its runs' counts into
-//      per-run bases; an item's position is its run's base for its key plus
-//      its rank.  Positions go to sorted_pos; rows under 64 bytes are copied
-//      here (kCopy), longer ones by the copy kernel that follows.
+//   1. Each warp loads its run's keys and source rows (validated, kept in
+//      registers); the CTA counts its keys with shared atomics, publishes
+//      them to cta_cnt[b][*] and adds its counts per destination to S[r][*]
+//      (cleared with the flag), then arrives at a grid barrier (bounded:
+//      A2AV_ERR_TIMEOUT after ~1 s).
+//   2. While the other CTAs arrive, each warp ranks its run's items 32 at a
+//      time (ballots on the key), keeping every item's rank among the run's
+//      equal keys beside its key, and the runs' counts become their offsets
+//      in the chunk; then the CTA waits at the barrier.
+//   3. Every CTA loads the counts of its rank's CTAs, builds the plan from
+//      the completed S (the a2av prologue's checks) while they are in
+//      flight, sums them -- over all of the rank's CTAs (the key totals,
+//      whose exclusive scan gives the key starts) and over the earlier ones
+//      (its chunk's base per key) -- and adds those bases to the runs'
+//      offsets; an item's position is its run's offset for its key plus its
+//      rank.  Positions go to sorted_pos; rows under 64 bytes are copied
+//      here (kRow != 0), longer ones by the copy kernel that follows.
 constexpr int kOrderWarps = 16, kOrderThreads = 32 * kOrderWarps;
 constexpr int kOrderIpt = 10;                          // items a lane holds
 constexpr long long kOrderRunMax = 32LL * kOrderIpt;   // items of a warp's run
