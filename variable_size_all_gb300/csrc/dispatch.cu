@@ -768,27 +768,31 @@ __device__ __forceinline__ void grid_arrive(unsigned* ctr) {
   }
 }
 
-// Wait (thread 0, bounded) until all `ctas` CTAs have arrived; false (in every
-// thread) when the wait ran out.  The fence after the relaxed polls orders
-// the CTA's later reads after the other CTAs' published writes.
+// One thread polls (bounded) until all `ctas` CTAs have arrived; false when
+// the wait ran out.  The fence after the relaxed polls orders the thread's
+// later reads after the other CTAs' published writes.
+__device__ __forceinline__ bool grid_poll(unsigned* ctr, unsigned ctas) {
+  const long long start = clock64();
+  bool ok = false;
+  for (;;) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= ctas) {
+      ok = true;
+      break;
+    }
+    if (clock64() - start > kWaitCycles) break;
+    if (A2AV_BARRIER_SLEEP_NS > 0) __nanosleep(A2AV_BARRIER_SLEEP_NS);
+  }
+  __threadfence();
+  return ok;
+}
+
+// The whole CTA waits (thread 0 polls); false (in every thread) when the wait
+// ran out.
 __device__ __forceinline__ bool grid_wait(unsigned* ctr, unsigned ctas) {
   __shared__ int passed;
-  if (threadIdx.x == 0) {
-    const long long start = clock64();
-    int ok = 0;
-    for (;;) {
-      unsigned v;
-      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-      if (v >= ctas) {
-        ok = 1;
-        break;
-      }
-      if (clock64() - start > kWaitCycles) break;
-      if (A2AV_BARRIER_SLEEP_NS > 0) __nanosleep(A2AV_BARRIER_SLEEP_NS);
-    }
-    __threadfence();
-    passed = ok;
-  }
+  if (threadIdx.x == 0) passed = grid_poll(ctr, ctas) ? 1 : 0;
   __syncthreads();
   return passed != 0;
 }
@@ -1452,6 +1456,9 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
 #ifndef A2AV_GATHER_SIMPLE_DISPATCH
 #define A2AV_GATHER_SIMPLE_DISPATCH 0
 #endif
+#ifndef A2AV_GATHER_EARLY
+#define A2AV_GATHER_EARLY 1
+#endif
 template <int NS, int LEAD, int NWK, int IPS>
 __global__ void __launch_bounds__(32 * NWK, 1)
     dispatch_gather_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
@@ -1467,17 +1474,26 @@ __global__ void __launch_bounds__(32 * NWK, 1)
   extern __shared__ __align__(128) unsigned char stages[];
   if (!build_plan(P, pl, kTileGranule)) return;
   publish_splits(D);
+  // The combine's checks in this launch (cooperative: every CTA resident):
+  // the whole grid checks every item (few threads: 16 items a thread in
+  // flight), then a grid barrier; no row is stored unless every CTA found its
+  // items valid.  With several rows a stage each warp waits at the barrier
+  // only before its first store (`gate`): its first LEAD stages load, from
+  // items it checked itself, while the last CTAs finish their checks.
+  const unsigned ctas = gridDim.x + (P.starve == 2);
+  bool gate = false;
   if (D.combine && D.barrier != nullptr) {
-    // The combine's checks in this launch (cooperative: every CTA resident):
-    // the whole grid checks every item (few threads: 16 items a thread in
-    // flight), then a grid barrier; no row moves unless every CTA found its
-    // items valid.
     combine_check_all<16>(D, pl);
-    if (!grid_barrier(D.barrier, gridDim.x + (P.starve == 2))) {
-      if (threadIdx.x == 0) fail(D, A2AV_ERR_TIMEOUT);
-      return;
+    grid_arrive(D.barrier);
+    if (IPS == 1 || !A2AV_GATHER_EARLY) {
+      if (!grid_wait(D.barrier, ctas)) {
+        if (threadIdx.x == 0) fail(D, A2AV_ERR_TIMEOUT);
+        return;
+      }
+      if (flagged(D)) return;
+    } else {
+      gate = true;
     }
-    if (flagged(D)) return;
   }
   const int lane = threadIdx.x & 31;
   const int warp = NWK == 1 ? 0 : (int)(threadIdx.x >> 5);  // a constant for one warp
@@ -1590,9 +1606,21 @@ __global__ void __launch_bounds__(32 * NWK, 1)
 #endif
 
   long long issued = 0, drained = 0;  // stages
-  bool ok = true;
-  // Wait for stage j's loads and store its rows; false on a timeout.
+  bool ok = true, stop = false;  // stop: the gate found an invalid item somewhere
+  // Wait for stage j's loads and store its rows; false on a timeout, or when
+  // the gate (before the first store) finds the grid's verdict negative.
   auto drain = [&](long long j) -> bool {
+    if (gate) {
+      gate = false;
+      int g = 0;  // 0: every CTA passed its checks, 1: one failed, 2: the wait ran out
+      if (lane == 0) g = !grid_poll(D.barrier, ctas) ? 2 : flagged(D) ? 1 : 0;
+      g = __shfl_sync(kFull, g, 0);
+      if (g == 2 && lane == 0) fail(D, A2AV_ERR_TIMEOUT);
+      if (g != 0) {
+        stop = true;
+        return false;
+      }
+    }
     const int s = (int)(j % NS);
     if (IPS == 1) {
       bool done = true;
@@ -1632,10 +1660,15 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     const long long b1 = a1.v && bases ? key_base(D, a1.r, a1.i, a1.key) : 0;
     // batch t's row addresses
     long long src = 0, dst = 0;
+    // loads ahead of the grid's verdict (the combine's gate): only from items
+    // whose key and position are valid
+    if (gate && (a0.key < 0 || a0.key >= W * K)) a0.v = false;
     if (a0.v) {
       const int p = a0.key / K;
       const long long grouped = pl.out_off[p][a0.r] - pl.in_off[a0.r][p];
       if (D.combine) {
+        const long long lo = pl.in_off[a0.r][p];
+        if (gate && (a0.spos < lo || a0.spos >= lo + pl.s[a0.r][p])) a0.v = false;
         src = (long long)(P.out[p] + (grouped + a0.spos) * rb);
         dst = (long long)(P.in[a0.r] + a0.i * rb);
       } else {
@@ -1721,10 +1754,10 @@ __global__ void __launch_bounds__(32 * NWK, 1)
     ++drained;
   }
   if (!ok) {
-    // A stage never completed: report it, give every load still in flight a
-    // bounded chance to land, then leave.
+    // A stage never completed (reported here), or the gate said stop: give
+    // every load still in flight a bounded chance to land, then leave.
     if (lane == 0) {
-      record_error(P.status, A2AV_ERR_TIMEOUT);
+      if (!stop) record_error(P.status, A2AV_ERR_TIMEOUT);
       for (long long j = drained; j < issued; ++j)
         mbar_wait(bar0 + 8 * (int)(j % NS), (unsigned)((j / NS) & 1));
     }
