@@ -416,7 +416,8 @@ int a2av_version(void);
  * checks every item, passes a grid barrier and copies, and for 16-byte
  * aligned device rows of 64 bytes to 2 KiB the cp.async.bulk gather,
  * launched cooperatively, which checks every item itself before a grid
- * barrier; else a check kernel (the split matrix, each key, each position
+ * barrier and stores no row before every block has arrived there; else a
+ * check kernel (the split matrix, each key, each position
  * within its destination's group) and then the dispatch's copy kernel with
  * the rows moving the other way.  The grid barriers are bounded (about a
  * second, then A2AV_ERR_TIMEOUT).  Device errors A2AV_ERR_BAD_SPLITS (as
