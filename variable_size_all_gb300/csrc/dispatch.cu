@@ -1963,6 +1963,23 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   int ra = 0;  // the rank of item a
   while (ra + 1 < W && D.item_first[ra + 1] <= a) ++ra;
   const long long ia = a - D.item_first[ra];
+  // Thread t takes items t, t + 256, ... of the global order (at most
+  // kTinyItems / kTinyThreads), all their keys and source rows loaded at
+  // once, first: the counts wait for them.
+  constexpr int kPer = kTinyItems / kTinyThreads;
+  const long long n = D.item_first[W];
+  int kk[kPer], ss[kPer], rr[kPer];
+  long long ii[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const long long g = (long long)q * kTinyThreads + tid;
+    int r = 0;
+    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+    rr[q] = g < n ? r : -1;
+    ii[q] = g - D.item_first[r];
+    kk[q] = g < n ? __ldg(D.key[r] + ii[q]) : 0;
+    ss[q] = g < n ? __ldg(D.src[r] + ii[q]) : 0;
+  }
   // When every row of this CTA's share has a slot, thread t loads the share's
   // t-th source row at once (its index range-checked first; an invalid item
   // loads nothing and is never stored): the loads land while the items are
@@ -1993,23 +2010,7 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   for (int x = tid; x < NB; x += kTinyThreads) run[x] = 0;
   __syncthreads();
   // every item: validity, its rank's key counts, and for rank ra the counts
-  // of the items before this CTA's share.  Thread t takes items t, t + 256,
-  // ... of the global order (at most kTinyItems / kTinyThreads), all their
-  // keys and source rows loaded at once.
-  constexpr int kPer = kTinyItems / kTinyThreads;
-  const long long n = D.item_first[W];
-  int kk[kPer], ss[kPer], rr[kPer];
-  long long ii[kPer];
-#pragma unroll
-  for (int q = 0; q < kPer; ++q) {
-    const long long g = (long long)q * kTinyThreads + tid;
-    int r = 0;
-    while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
-    rr[q] = g < n ? r : -1;
-    ii[q] = g - D.item_first[r];
-    kk[q] = g < n ? __ldg(D.key[r] + ii[q]) : 0;
-    ss[q] = g < n ? __ldg(D.src[r] + ii[q]) : 0;
-  }
+  // of the items before this CTA's share.
   int bad = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
@@ -2154,29 +2155,53 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
   if (!build_plan(P, pl, kTileGranule)) return;
   long long a, e;
   tiny_share(D, &a, &e);
+  const long long rb = P.rb;
+  // When every row of the share has a slot, the thread holding a share item
+  // that it found valid loads its row at once (slot and mbarrier of the
+  // item), while the other items are checked; the rows are stored only once
+  // every item of the batch has passed.
+  const int c = (int)(e - a);
+  const bool early = slots > 0 && c <= slots;
+  const uint32_t slot0 = smem_u32(slot_mem);
+  unsigned armed = 0;  // bit q: this thread armed the mbarrier of its q-th item
   int bad = 0;
 #pragma unroll
   for (int q = 0; q < kPer; ++q) {
     const int r = rr[q];
     if (r < 0) continue;
-    if (kk[q] < 0 || kk[q] >= NB) {
-      bad = 1;
-      continue;
+    bool ok = kk[q] >= 0 && kk[q] < NB;
+    const int p = ok ? kk[q] / K : 0;
+    if (ok) {
+      const long long lo = pl.in_off[r][p];
+      ok = pp[q] >= lo && pp[q] < lo + pl.s[r][p];
     }
-    const int p = kk[q] / K;
-    const long long lo = pl.in_off[r][p];
-    if (pp[q] < lo || pp[q] >= lo + pl.s[r][p]) bad = 1;
+    if (!ok) bad = 1;
     const long long g = (long long)q * kTinyThreads + tid;
     if (g >= a && g < e) {  // this CTA's share: kept for its copy
       own_key[g - a] = kk[q];
       own_pos[g - a] = pp[q];
+      if (early) {
+        const uint32_t bar = smem_u32(&bars[g - a]);
+        mbar_init(bar, 1);
+        mbar_fence_init();
+        if (ok) {
+          mbar_expect_tx(bar, (unsigned)rb);
+          bulk_load(slot0 + (uint32_t)((g - a) * rb),
+                    P.out[p] + (pl.out_off[p][r] - pl.in_off[r][p] + pp[q]) * rb, (unsigned)rb, bar);
+        } else {
+          mbar_arrive(bar);
+        }
+        armed |= 1u << q;
+      }
     }
   }
   if (__syncthreads_or(bad)) {
     if (blockIdx.x == 0 && tid == 0) record_error(D.status, A2AV_ERR_BAD_INDEX);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)  // (bounded) the loads this thread issued land first
+      if ((armed >> q) & 1u) mbar_wait(smem_u32(&bars[(long long)q * kTinyThreads + tid - a]), 0);
     return;
   }
-  const long long rb = P.rb;
   for (long long g = a + tid; g < e; g += kTinyThreads) {
     int r = 0;
     while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
@@ -2187,8 +2212,20 @@ __global__ void __launch_bounds__(kTinyThreads, 1)
     own_dst[g - a] = (unsigned long long)(P.in[r] + i * rb);
   }
   __syncthreads();
-  copy_listed_rows(own_src, own_dst, (int)(e - a), rb, slots, smem_u32(slot_mem), smem_u32(bars),
-                   D.status);
+  if (early) {  // row x stored by thread x once it has landed
+    if (tid < c) {
+      const uint32_t bar = smem_u32(&bars[tid]);
+      if (!mbar_wait(bar, 0)) {
+        record_error(D.status, A2AV_ERR_TIMEOUT);
+        mbar_wait(bar, 0);
+      } else {
+        bulk_store(reinterpret_cast<void*>(own_dst[tid]), slot0 + (uint32_t)(tid * rb), (unsigned)rb);
+      }
+    }
+    bulk_wait_all();
+    return;
+  }
+  copy_listed_rows(own_src, own_dst, c, rb, slots, slot0, smem_u32(bars), D.status);
 }
 
 // Workspace: [0, 256) the flag (int) and the per-rank done counters (W ints),
