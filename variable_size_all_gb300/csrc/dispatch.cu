@@ -1020,9 +1020,9 @@ __global__ void __launch_bounds__(kOrderThreads, 2)
 }
 
 // The fused combine of rows under 64 bytes in one cooperative launch, items
-// partitioned as in the order kernel: every CTA builds the plan from the
-// split matrix (the a2av prologue's checks), loads its items' keys and
-// positions and checks them (a position must lie in its destination's group
+// partitioned as in the order kernel: every CTA loads its items' keys and
+// positions, builds the plan from the split matrix while they are in flight
+// (the a2av prologue's checks), and checks them (a position must lie in its destination's group
 // of the rank's key order), then a grid barrier; if no CTA found an invalid
 // item, each moves its items' rows back -- rows of exactly kRow = 4, 8 or 16
 // bytes at that alignment all loaded first, then stored; kRow = -1 one row
@@ -1031,7 +1031,10 @@ template <int kRow>
 __global__ void __launch_bounds__(kOrderThreads, 2)
     combine_order_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   __shared__ Plan pl;
-  if (!build_plan(P, pl, kTileGranule)) return;  // (same verdict in every CTA)
+  // the positions come from the previous kernel: wait for it, then load the
+  // items' keys and positions and build the plan while they are in flight
+  chain_release();
+  chain_wait();
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int W = D.W, K = D.K, NB = W * K;
   const int b = blockIdx.x;
@@ -1045,16 +1048,29 @@ __global__ void __launch_bounds__(kOrderThreads, 2)
   const int nc = w1 > w0 ? (int)((w1 - w0 + 31) / 32) : 0;  // warp-uniform
   const int* const kp = D.key[r];
   const long long* const pp = D.sorted_pos[r];
-  int keys[kOrderIpt], pos[kOrderIpt];  // -1: no item; positions are below 2^31
+  int kraw[kOrderIpt];
+  long long praw[kOrderIpt];
 #pragma unroll
   for (int c = 0; c < kOrderIpt; ++c) {  // (unconditional loads, clamped index)
+    kraw[c] = 0;
+    praw[c] = 0;
+    if (c < nc) {
+      const long long i = w0 + c * 32 + lane;
+      const long long ii = i < w1 ? i : w1 - 1;
+      kraw[c] = __ldg(kp + ii);
+      praw[c] = __ldg(pp + ii);
+    }
+  }
+  if (!build_plan(P, pl, kTileGranule)) return;  // (same verdict in every CTA)
+  int keys[kOrderIpt], pos[kOrderIpt];  // -1: no item; positions are below 2^31
+#pragma unroll
+  for (int c = 0; c < kOrderIpt; ++c) {
     keys[c] = -1;
     pos[c] = 0;
     if (c < nc) {
       const long long i = w0 + c * 32 + lane;
-      const long long ii = i < w1 ? i : w1 - 1;
-      const int k = __ldg(kp + ii);
-      const long long q = __ldg(pp + ii);
+      const int k = kraw[c];
+      const long long q = praw[c];
       bool ok = false;
       if (i < w1 && k >= 0 && k < NB) {
         const int p = k / K;
