@@ -212,7 +212,9 @@ static_assert(32 * kCountWarps == kScanThreads, "a count CTA can run the block s
 // groups (G = kScanThreads / NB slices per key): it sums its slice, the
 // slices' sums give it its base, and it rewrites its slice with running
 // prefixes.  Counts are loaded kFuseScanBatch at a time, from L2 (the other
-// count CTAs wrote them during this launch).
+// count CTAs wrote them during this launch); the first batch is kept in
+// registers for the second pass, so a slice of at most kFuseScanBatch groups
+// is loaded once.
 constexpr int kFuseScanBatch = 8;
 __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) {
   const int t = threadIdx.x, NB = D.W * D.K, G = kScanThreads / NB;
@@ -225,12 +227,16 @@ __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) 
   __shared__ long long tot[kScanThreads];
   __shared__ long long warp_sums[kScanThreads / 32];
   long long local = 0;
+  int v0[kFuseScanBatch];  // the first batch, kept for the second pass
   for (long long c = c0; c < c1; c += kFuseScanBatch) {
     int v[kFuseScanBatch];
 #pragma unroll
     for (int q = 0; q < kFuseScanBatch; ++q) v[q] = c + q < c1 ? __ldcg(A + (c + q) * NB) : 0;
 #pragma unroll
-    for (int q = 0; q < kFuseScanBatch; ++q) local += v[q];
+    for (int q = 0; q < kFuseScanBatch; ++q) {
+      local += v[q];
+      if (c == c0) v0[q] = v[q];
+    }
   }
   part[t] = local;
   __syncthreads();
@@ -244,7 +250,8 @@ __device__ void scan_groups_in_cta(const DispatchParams& D, int r, long long C) 
   for (long long c = c0; c < c1; c += kFuseScanBatch) {
     int v[kFuseScanBatch];
 #pragma unroll
-    for (int q = 0; q < kFuseScanBatch; ++q) v[q] = c + q < c1 ? __ldcg(A + (c + q) * NB) : 0;
+    for (int q = 0; q < kFuseScanBatch; ++q)
+      v[q] = c == c0 ? v0[q] : (c + q < c1 ? __ldcg(A + (c + q) * NB) : 0);
 #pragma unroll
     for (int q = 0; q < kFuseScanBatch; ++q) {
       if (c + q < c1) A[(c + q) * NB] = (int)base;
