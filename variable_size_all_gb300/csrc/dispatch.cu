@@ -1150,6 +1150,9 @@ __device__ __noinline__ void copy_rows_unaligned(long long mdst, long long msrc,
 #define A2AV_ROWS512_CTAS_PER_SM 4  // 64 registers: four CTAs an SM, 2 KiB a warp in flight
 #endif
 constexpr int kRows512CtasPerSm = A2AV_ROWS512_CTAS_PER_SM;
+#ifndef A2AV_COPY_PRELOAD
+#define A2AV_COPY_PRELOAD 1
+#endif
 template <bool kWarpRows, bool kRows512 = false>
 __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
                                                 : kWarpRows ? kCopyCtasPerSmWarpRows
@@ -1157,9 +1160,6 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
     dispatch_copy_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   chain_wait();
   if (flagged(D)) return;
-  __shared__ Plan pl;
-  if (!build_plan(P, pl, kTileGranule)) return;
-  publish_splits(D);
   const int W = D.W, K = D.K;
   const long long rb = P.rb, total = D.item_first[W];
   constexpr bool warp_rows = kWarpRows;
@@ -1167,6 +1167,26 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
                                    : (long long)blockIdx.x * kCopyThreads + threadIdx.x;
   const long long teams = warp_rows ? (long long)gridDim.x * (kCopyThreads / 32)
                                     : (long long)gridDim.x * kCopyThreads;
+  const long long rounds = (total + teams * 32 - 1) / (teams * 32);
+  const long long batch = rounds > 0 ? (total + teams * rounds - 1) / (teams * rounds) : 32;
+  // (512-byte pieces, the dispatch) the first batch's keys, source rows and
+  // in-range ranks are loaded before the plan is built
+  const bool pre = kRows512 && !D.combine && !D.pos_ready && A2AV_COPY_PRELOAD;
+  int pre_k = 0, pre_s = 0, pre_in = 0;
+  if (pre) {
+    const long long g = team * batch + (threadIdx.x & 31);
+    if (team * batch < total && g < total && (threadIdx.x & 31) < batch) {
+      int r = 0;
+      while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
+      const long long i = g - D.item_first[r];
+      pre_k = D.key[r][i];
+      pre_s = D.src[r][i];
+      pre_in = D.inrank[(long long)r * D.pos_stride + i];
+    }
+  }
+  __shared__ Plan pl;
+  if (!build_plan(P, pl, kTileGranule)) return;
+  publish_splits(D);
   if constexpr (warp_rows) {
     // A warp takes a batch of up to 32 consecutive items: lane l reads item
     // l's metadata (one round trip for the batch, a second for the key
@@ -1176,29 +1196,29 @@ __global__ void __launch_bounds__(kCopyThreads, kRows512    ? kRows512CtasPerSm
     // realigning span copy.  The batch size gives every warp the same
     // number of batches.
     const int lane = threadIdx.x & 31;
-    const long long rounds = (total + teams * 32 - 1) / (teams * 32);
-    const long long batch = rounds > 0 ? (total + teams * rounds - 1) / (teams * rounds) : 32;
     for (long long g0 = team * batch; g0 < total; g0 += teams * batch) {
       const long long g = g0 + lane;
       const int n = total - g0 < batch ? (int)(total - g0) : (int)batch;
+      const bool first = pre && g0 == team * batch;  // this batch's metadata loaded already
       long long mdst = 0, msrc = 0;
       if (lane < n) {
         int r = 0;
         while (r + 1 < W && D.item_first[r + 1] <= g) ++r;
         const long long i = g - D.item_first[r];
-        const int k = D.key[r][i];
+        const int k = first ? pre_k : D.key[r][i];
         const int p = k / K;
         const long long grouped = pl.out_off[p][r] - pl.in_off[r][p];  // + pos: the row in p's buffer
         if (D.combine) {  // from the peer's buffer back to the item's row
           msrc = (long long)(P.out[p] + (grouped + D.sorted_pos[r][i]) * rb);
           mdst = (long long)(P.in[r] + i * rb);
         } else {
-          const int s = D.src[r][i];
+          const int s = first ? pre_s : D.src[r][i];
           long long pos;
           if (D.pos_ready) {
             pos = D.sorted_pos[r][i];
           } else {
-            pos = key_base(D, r, i, k) + D.inrank[(long long)r * D.pos_stride + i];
+            pos = key_base(D, r, i, k) +
+                  (first ? pre_in : (int)D.inrank[(long long)r * D.pos_stride + i]);
             D.sorted_pos[r][i] = pos;
           }
           mdst = (long long)(P.out[p] + (grouped + pos) * rb);
