@@ -1509,7 +1509,9 @@ __global__ void __launch_bounds__(32 * NWK, 1)
   static_assert(NWK >= 1 && NWK <= 16 && IPS >= 1 && IPS <= 32 && (IPS & (IPS - 1)) == 0,
                 "one to sixteen warps, a power-of-two number of slots per stage");
   chain_wait();
-  if (flagged(D)) return;
+  // (the combine's checking launch follows the workspace clear directly:
+  // nothing before it can have raised the flag)
+  if (!(D.combine && D.barrier != nullptr) && flagged(D)) return;
   __shared__ Plan pl;
   __shared__ alignas(8) unsigned long long bars[NWK][NS];
   __shared__ unsigned long long sdst[NWK][NS][IPS];  // each slot's destination
