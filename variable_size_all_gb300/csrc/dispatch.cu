@@ -1873,6 +1873,24 @@ const GatherShape kGatherShapes[] = {
     {16384, dispatch_gather_kernel<12, 10, 1, 1>, 1, 12, 1},
     {32768, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 1>, 1, kGatherNs, 1},
 };
+// The combine's own rings where they differ from the dispatch's, measured
+// with the one-row loop the combine runs (MoE combine, 8192 tokens, W=8):
+// rows above 8 KiB up to 16 KiB on three warps x 4 stages, loads two ahead
+// (14 KiB rows: 584.6 against
+// 597.1 us for the dispatch's one warp x 12 stages, which stays the
+// dispatch's: three warps cost it 1 %); at 4 KiB six or eight warps, or
+// deeper rings, were 1–2 % slower than the dispatch's four warps x 6.
+#ifndef A2AV_C16K_NS
+#define A2AV_C16K_NS 4
+#define A2AV_C16K_LEAD 2
+#define A2AV_C16K_NWK 3
+#endif
+const GatherShape kCombineShapes[] = {
+    {16384, dispatch_gather_kernel<A2AV_C16K_NS, A2AV_C16K_LEAD, A2AV_C16K_NWK, 1>, A2AV_C16K_NWK,
+     A2AV_C16K_NS, 1},
+};
+static_assert(A2AV_C16K_NWK * A2AV_C16K_NS * 16384 <= kGatherSmem,
+              "the combine's rings fit the gather's shared memory");
 static_assert(16 * 4 * 16 * 128 <= kGatherSmem && 12 * 4 * 16 * 256 <= kGatherSmem &&
                   6 * 4 * 16 * 512 <= kGatherSmem && 3 * 4 * 16 * 1024 <= kGatherSmem &&
                   3 * 4 * 8 * 2048 <= kGatherSmem && 4 * 6 * 4096 <= kGatherSmem &&
@@ -2345,6 +2363,10 @@ cudaError_t prepare_kernels(a2av_handle* h) {
     if (cudaFuncSetAttribute(g.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
         cudaSuccess)
       return cudaErrorInvalidValue;
+  for (const GatherShape& g : kCombineShapes)
+    if (cudaFuncSetAttribute(g.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGatherSmem) !=
+        cudaSuccess)
+      return cudaErrorInvalidValue;
   // (count histograms: 8 ranges a warp x 4 x W * K ints, up to 128 KiB)
   if (cudaFuncSetAttribute(dispatch_count_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kCountWarps * 4 * kMaxBins * (int)sizeof(int)) != cudaSuccess ||
@@ -2482,6 +2504,9 @@ cudaError_t launch_copy(a2av_handle* h, const Params& P, DispatchParams D, long 
   if (e != cudaSuccess) return e;
   const GatherShape* g = &kGatherShapes[0];
   while (g->max_row < row_bytes) ++g;
+  if (D.combine)
+    for (const GatherShape& c : kCombineShapes)
+      if (c.max_row == g->max_row) g = &c;
   // Batches of 32 items, or of 16 / 8 when that gives every warp at least
   // four (balance for mid-size batches).
   const long long warps = (long long)h->sms * g->nwk;
