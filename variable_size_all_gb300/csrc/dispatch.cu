@@ -1497,7 +1497,7 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
 #define A2AV_GATHER_SIMPLE_COMBINE 1
 #endif
 #ifndef A2AV_GATHER_SIMPLE_DISPATCH
-#define A2AV_GATHER_SIMPLE_DISPATCH 0
+#define A2AV_GATHER_SIMPLE_DISPATCH 1
 #endif
 #ifndef A2AV_GATHER_EARLY
 #define A2AV_GATHER_EARLY 1
@@ -1580,7 +1580,9 @@ __global__ void __launch_bounds__(32 * NWK, 1)
       // the rows' addresses fetched 32 at a time (lane l: the warp's row
       // k0 + l).  (Measured against the batched issue below on the MoE
       // combine: 603.4 against 617.6 us at 14 KiB rows, 174.5 against 179.3
-      // at 4 KiB, 343.0 against 353.7 at 8 KiB.)
+      // at 4 KiB, 343.0 against 353.7 at 8 KiB; on the MoE dispatch, with
+      // the 14 KiB ring on two warps: 457.6 against 471.4 us at 14 KiB,
+      // 147.2 against 148.7 at 4 KiB, 278.9 against 279.5 at 8 KiB.)
       long long msrc = 0, mdst = 0, stored = 0, loaded = 0;
       bool fine = true;
       for (long long k = 0; k < mine + LEAD; ++k) {
@@ -1868,18 +1870,20 @@ const GatherShape kGatherShapes[] = {
     // four warps x 6 stages; 8 KiB rows 279 us with two warps x 12)
     {4096, dispatch_gather_kernel<6, 4, 4, 1>, 4, 6, 1},
     {8192, dispatch_gather_kernel<12, 10, 2, 1>, 2, 12, 1},
-    // 14 KiB MoE rows: 12 x 16 KiB stages, loads 10 ahead (measured best for
-    // a one-row ring: 8 stages / 6 ahead 3 % slower, two CTAs an SM 4-6 %)
-    {16384, dispatch_gather_kernel<12, 10, 1, 1>, 1, 12, 1},
+    // 14 KiB MoE rows: two warps x 6 x 16 KiB stages, loads 4 ahead (with
+    // the one-row loop: 462.8 us against 468.0 with three warps x 4 and
+    // 470.8 with one warp x 12, the ring that was best for the batched
+    // issue)
+    {16384, dispatch_gather_kernel<6, 4, 2, 1>, 2, 6, 1},
     {32768, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 1>, 1, kGatherNs, 1},
 };
 // The combine's own rings where they differ from the dispatch's, measured
 // with the one-row loop the combine runs (MoE combine, 8192 tokens, W=8):
 // rows above 8 KiB up to 16 KiB on three warps x 4 stages, loads two ahead
 // (14 KiB rows: 584.6 against
-// 597.1 us for the dispatch's one warp x 12 stages, which stays the
-// dispatch's: three warps cost it 1 %); at 4 KiB six or eight warps, or
-// deeper rings, were 1–2 % slower than the dispatch's four warps x 6.
+// 597.1 us for one warp x 12 stages; the dispatch's own ring there is two
+// warps x 6); at 4 KiB six or eight warps, or deeper rings, were 1–2 %
+// slower than the dispatch's four warps x 6.
 #ifndef A2AV_C16K_NS
 #define A2AV_C16K_NS 4
 #define A2AV_C16K_LEAD 2
@@ -1894,7 +1898,7 @@ static_assert(A2AV_C16K_NWK * A2AV_C16K_NS * 16384 <= kGatherSmem,
 static_assert(16 * 4 * 16 * 128 <= kGatherSmem && 12 * 4 * 16 * 256 <= kGatherSmem &&
                   6 * 4 * 16 * 512 <= kGatherSmem && 3 * 4 * 16 * 1024 <= kGatherSmem &&
                   3 * 4 * 8 * 2048 <= kGatherSmem && 4 * 6 * 4096 <= kGatherSmem &&
-                  2 * 12 * 8192 <= kGatherSmem && 12 * 16384 <= kGatherSmem &&
+                  2 * 12 * 8192 <= kGatherSmem && 2 * 6 * 16384 <= kGatherSmem &&
                   kGatherNs * 32768 <= kGatherSmem,
               "every ring fits the gather's shared memory");
 
