@@ -1866,10 +1866,13 @@ const GatherShape kGatherShapes[] = {
     {1024, dispatch_gather_kernel<4, 2, 3, 16>, 3, 4, 16},
     {2048, dispatch_gather_kernel<4, 2, 3, 8>, 3, 4, 8},
     // one row a stage, one issuing lane per warp, several warps with rings of
-    // their own (MoE dispatch, 8192 tokens, W=8: 4 KiB rows 149-154 us with
-    // four warps x 6 stages; 8 KiB rows 279 us with two warps x 12)
-    {4096, dispatch_gather_kernel<6, 4, 4, 1>, 4, 6, 1},
-    {8192, dispatch_gather_kernel<12, 10, 2, 1>, 2, 12, 1},
+    // their own (MoE dispatch / combine, 8192 tokens, W=8, the one-row loop:
+    // 4 KiB rows 142.1 / 173.3 us on eight warps x 6 stages, loads 3 ahead,
+    // against 145.5 / 174.6 on four x 6 and 145.4 / 174.2 on four x 12; 8
+    // KiB rows 268.4 / 337.3 on three x 8, loads 6 ahead, against 277.6 /
+    // 341.8 on two x 12 and 268.3 / 337.9 on four x 6)
+    {4096, dispatch_gather_kernel<6, 3, 8, 1>, 8, 6, 1},
+    {8192, dispatch_gather_kernel<8, 6, 3, 1>, 3, 8, 1},
     // 14 KiB MoE rows: two warps x 6 x 16 KiB stages, loads 4 ahead (with
     // the one-row loop: 462.8 us against 468.0 with three warps x 4 and
     // 470.8 with one warp x 12, the ring that was best for the batched
@@ -1882,8 +1885,7 @@ const GatherShape kGatherShapes[] = {
 // rows above 8 KiB up to 16 KiB on three warps x 4 stages, loads two ahead
 // (14 KiB rows: 584.6 against
 // 597.1 us for one warp x 12 stages; the dispatch's own ring there is two
-// warps x 6); at 4 KiB six or eight warps, or deeper rings, were 1–2 %
-// slower than the dispatch's four warps x 6.
+// warps x 6).
 #ifndef A2AV_C16K_NS
 #define A2AV_C16K_NS 4
 #define A2AV_C16K_LEAD 2
@@ -1897,8 +1899,8 @@ static_assert(A2AV_C16K_NWK * A2AV_C16K_NS * 16384 <= kGatherSmem,
               "the combine's rings fit the gather's shared memory");
 static_assert(16 * 4 * 16 * 128 <= kGatherSmem && 12 * 4 * 16 * 256 <= kGatherSmem &&
                   6 * 4 * 16 * 512 <= kGatherSmem && 3 * 4 * 16 * 1024 <= kGatherSmem &&
-                  3 * 4 * 8 * 2048 <= kGatherSmem && 4 * 6 * 4096 <= kGatherSmem &&
-                  2 * 12 * 8192 <= kGatherSmem && 2 * 6 * 16384 <= kGatherSmem &&
+                  3 * 4 * 8 * 2048 <= kGatherSmem && 8 * 6 * 4096 <= kGatherSmem &&
+                  3 * 8 * 8192 <= kGatherSmem && 2 * 6 * 16384 <= kGatherSmem &&
                   kGatherNs * 32768 <= kGatherSmem,
               "every ring fits the gather's shared memory");
 
