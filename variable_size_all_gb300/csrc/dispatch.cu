@@ -1502,12 +1502,15 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
 #ifndef A2AV_GATHER_EARLY
 #define A2AV_GATHER_EARLY 1
 #endif
+constexpr int kGatherSmemBound = 192 * 1024;  // the stages' dynamic shared memory (kGatherSmem)
 template <int NS, int LEAD, int NWK, int IPS>
 __global__ void __launch_bounds__(32 * NWK, 1)
     dispatch_gather_kernel(const __grid_constant__ Params P, const __grid_constant__ DispatchParams D) {
   static_assert(LEAD >= 1 && LEAD < NS, "loads run 1..NS-1 stages ahead of stores");
   static_assert(NWK >= 1 && NWK <= 16 && IPS >= 1 && IPS <= 32 && (IPS & (IPS - 1)) == 0,
                 "one to sixteen warps, a power-of-two number of slots per stage");
+  static_assert(sizeof(Plan) + NWK * NS * (8 + 8 * IPS + 4) + 256 + kGatherSmemBound <= 227 * 1024,
+                "the ring's static shared memory and the stages fit a CTA's 227 KiB");
   chain_wait();
   // (the combine's checking launch follows the workspace clear directly:
   // nothing before it can have raised the flag)
@@ -1843,7 +1846,7 @@ constexpr long long kGatherMinRow = A2AV_GATHER_MIN_ROW;
 constexpr long long kDispatchGatherMinRow = A2AV_DISPATCH_GATHER_MIN_ROW;
 constexpr long long kGatherMaxRow = 32 * 1024;
 constexpr long long kGatherCheckMaxRow = 2048;  // the combine's gather checks its items up to here
-constexpr int kGatherSmem = 192 * 1024;
+constexpr int kGatherSmem = kGatherSmemBound;
 
 using GatherKernel = void (*)(Params, DispatchParams);
 struct GatherShape {
@@ -1858,7 +1861,9 @@ struct GatherShape {
 // shape at 3134 / 3060 / 2990 GB/s moved for 1 KiB / 512 B / 256 B rows,
 // against 1877 / 994 / 511 with one warp of 32-row stages and 2580 / 2155 /
 // 1283 by register copies: with enough warps issuing, the per-copy cost of
-// small cp.async.bulk operations is hidden.
+// small cp.async.bulk operations is hidden.  (The combine takes its own
+// one-row rings for 1 and 2 KiB rows, below; the dispatch takes the
+// register copy up to 2 KiB.)
 const GatherShape kGatherShapes[] = {
     {128, dispatch_gather_kernel<4, 2, 16, 16>, 16, 4, 16},
     {256, dispatch_gather_kernel<4, 2, 12, 16>, 12, 4, 16},
@@ -1881,21 +1886,39 @@ const GatherShape kGatherShapes[] = {
     {32768, dispatch_gather_kernel<kGatherNs, kGatherLead, 1, 1>, 1, kGatherNs, 1},
 };
 // The combine's own rings where they differ from the dispatch's, measured
-// with the one-row loop the combine runs (MoE combine, 8192 tokens, W=8):
-// rows above 8 KiB up to 16 KiB on three warps x 4 stages, loads two ahead
-// (14 KiB rows: 584.6 against
-// 597.1 us for one warp x 12 stages; the dispatch's own ring there is two
-// warps x 6).
+// with the one-row loop (MoE combine, 8192 tokens, W=8): 1 and 2 KiB rows
+// on sixteen warps of one-row stages (12 and 6 stages, loads 6 and 3 ahead:
+// 48.5 against 49.7 us and 89.0 against 90.8 for the lane-per-row stages
+// above, which keep 64 B .. 512 B rows -- at 512 B one-row rings took 44.0
+// against 29.7); rows above 8 KiB up to 16 KiB on three warps x 4 stages,
+// loads two ahead (14 KiB rows: 584.6 against 597.1 us for one warp x 12;
+// the dispatch's own ring there is two warps x 6).
 #ifndef A2AV_C16K_NS
 #define A2AV_C16K_NS 4
 #define A2AV_C16K_LEAD 2
 #define A2AV_C16K_NWK 3
 #endif
+#ifndef A2AV_C1K_NS
+#define A2AV_C1K_NS 12
+#define A2AV_C1K_LEAD 6
+#define A2AV_C1K_NWK 16
+#endif
+#ifndef A2AV_C2K_NS
+#define A2AV_C2K_NS 6
+#define A2AV_C2K_LEAD 3
+#define A2AV_C2K_NWK 16
+#endif
 const GatherShape kCombineShapes[] = {
+    {1024, dispatch_gather_kernel<A2AV_C1K_NS, A2AV_C1K_LEAD, A2AV_C1K_NWK, 1>, A2AV_C1K_NWK,
+     A2AV_C1K_NS, 1},
+    {2048, dispatch_gather_kernel<A2AV_C2K_NS, A2AV_C2K_LEAD, A2AV_C2K_NWK, 1>, A2AV_C2K_NWK,
+     A2AV_C2K_NS, 1},
     {16384, dispatch_gather_kernel<A2AV_C16K_NS, A2AV_C16K_LEAD, A2AV_C16K_NWK, 1>, A2AV_C16K_NWK,
      A2AV_C16K_NS, 1},
 };
-static_assert(A2AV_C16K_NWK * A2AV_C16K_NS * 16384 <= kGatherSmem,
+static_assert(A2AV_C16K_NWK * A2AV_C16K_NS * 16384 <= kGatherSmem &&
+                  A2AV_C1K_NWK * A2AV_C1K_NS * 1024 <= kGatherSmem &&
+                  A2AV_C2K_NWK * A2AV_C2K_NS * 2048 <= kGatherSmem,
               "the combine's rings fit the gather's shared memory");
 static_assert(16 * 4 * 16 * 128 <= kGatherSmem && 12 * 4 * 16 * 256 <= kGatherSmem &&
                   6 * 4 * 16 * 512 <= kGatherSmem && 3 * 4 * 16 * 1024 <= kGatherSmem &&
