@@ -1477,7 +1477,10 @@ __device__ __forceinline__ GatherItem gather_item(const DispatchParams& D, long 
 
 // The cp.async.bulk gather for 16-byte aligned rows of 64 B .. 32 KiB.  NWK
 // warps per CTA, each an independent pipeline with a ring of NS stages of
-// IPS row slots (its own mbarriers, its own bulk groups).  A warp takes every
+// IPS row slots (its own mbarriers, its own bulk groups).  Rings of one row
+// a stage (IPS == 1) run the one-row loop below: the warp's k-th row is item
+// wg + k WG of the global order, lane 0 loads row k and stores row k - LEAD.
+// Rings of several rows a stage: a warp takes every
 // (grid x NWK)-th batch of bs consecutive items of one rank; a batch is
 // copied as bs / min(bs, IPS) stages.  In a stage every lane that holds an
 // item issues the bulk load of its row into its slot (one mbarrier per
